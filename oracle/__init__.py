@@ -1,0 +1,214 @@
+"""CPU oracle of the routed MoE layer (plain C, fp64) - TEST INFRASTRUCTURE.
+
+Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The library under
+``routed_expert_layer_router_gb300/`` never does; the two share no code.
+
+This module compiles ``oracle.c`` with gcc and exposes its functions through
+ctypes.  Every computation lives in ``oracle.c``; the helpers below only
+marshal numpy arrays and, for large layers, generate the expert records a
+forward pass needs (through the seeded generator in ``gen``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SO = os.path.join(_HERE, "liboracle.so")
+_lib = None
+openmp = False
+
+
+def build(verbose: bool = False) -> None:
+    """Compile oracle.c (with OpenMP when the compiler has it)."""
+    base = ["gcc", "-O2", "-fPIC", "-shared", "-ffp-contract=off", "-o", _SO,
+            os.path.join(_HERE, "oracle.c"), "-lm"]
+    p = subprocess.run(base[:1] + ["-fopenmp"] + base[1:], capture_output=True, text=True)
+    if p.returncode != 0:
+        p = subprocess.run(base, capture_output=True, text=True)
+        if p.returncode != 0:
+            raise RuntimeError("oracle build failed:\n" + p.stdout + p.stderr)
+    if verbose:
+        print(p.stdout + p.stderr)
+
+
+def lib():
+    global _lib, openmp
+    if _lib is None:
+        if not os.path.exists(_SO):
+            build()
+        L = ctypes.CDLL(_SO)
+        vp, i32, d = ctypes.c_void_p, ctypes.c_int, ctypes.c_double
+        L.oracle_e2m1.argtypes = [ctypes.c_uint]
+        L.oracle_e2m1.restype = d
+        L.oracle_e4m3.argtypes = [ctypes.c_uint]
+        L.oracle_e4m3.restype = d
+        L.oracle_bf16.argtypes = [ctypes.c_uint16]
+        L.oracle_bf16.restype = d
+        L.oracle_weight.argtypes = [vp, i32, i32, i32, i32, i32, vp]
+        L.oracle_weight.restype = d
+        L.oracle_dequant_matrix.argtypes = [vp, i32, i32, i32, vp, vp]
+        L.oracle_route.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp]
+        L.oracle_permute.argtypes = [vp, i32, i32, i32, vp, vp, vp, vp]
+        L.oracle_permute.restype = i32
+        L.oracle_e4m3_rne.argtypes = [ctypes.c_float]
+        L.oracle_e4m3_rne.restype = ctypes.c_uint
+        L.oracle_e2m1_rne_sat.argtypes = [ctypes.c_float]
+        L.oracle_e2m1_rne_sat.restype = ctypes.c_uint
+        L.oracle_nvfp4_quant.argtypes = [vp, i32, vp, vp, vp]
+        L.oracle_expert.argtypes = [vp, i32, i32, vp, vp, i32, vp]
+        L.oracle_shared.argtypes = [vp, vp, vp, i32, i32, vp, i32, vp]
+        L.oracle_layer_forward.argtypes = [vp, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp,
+                                           vp, vp, vp, i32, vp, vp, vp, vp]
+        L.oracle_layer_forward.restype = i32
+        L.oracle_set_defect.argtypes = [i32]
+        _lib = L
+        try:
+            openmp = "omp_get_num_threads" in open(_SO, "rb").read().decode("latin1")
+        except OSError:
+            openmp = False
+    return _lib
+
+
+def _p(a):
+    if a is None:
+        return None
+    assert isinstance(a, np.ndarray) and a.flags["C_CONTIGUOUS"], "need a C-contiguous array"
+    return a.ctypes.data
+
+
+DEFECTS = {"nibble_swap": 1, "scale_ue8m0": 2, "block_off_by_one": 3, "tie_high_id": 4,
+           "scaling_2_5": 5}
+
+
+class defect:
+    """Context manager planting one named defect in the oracle (negative controls)."""
+
+    def __init__(self, name: str):
+        self.code = DEFECTS[name]
+
+    def __enter__(self):
+        lib().oracle_set_defect(self.code)
+        return self
+
+    def __exit__(self, *exc):
+        lib().oracle_set_defect(0)
+        return False
+
+
+def e2m1(code: int) -> float:
+    return lib().oracle_e2m1(code)
+
+
+def e4m3(byte: int) -> float:
+    return lib().oracle_e4m3(byte)
+
+
+def bf16(h: int) -> float:
+    return lib().oracle_bf16(h)
+
+
+def weight(rec, H, I, m, r, c, g3) -> float:
+    return lib().oracle_weight(_p(rec), H, I, m, r, c, _p(np.ascontiguousarray(g3, np.float32)))
+
+
+def dequant_matrix(rec, H, I, m, g3) -> np.ndarray:
+    R, K = (H, I) if m == 2 else (I, H)
+    out = np.empty((R, K), np.float64)
+    lib().oracle_dequant_matrix(_p(rec), H, I, m, _p(np.ascontiguousarray(g3, np.float32)), _p(out))
+    return out
+
+
+def route(x, Wr, bias, k):
+    """Returns ids [T,k] i32, w [T,k], p_sel [T,k], logits [T,E], gap [T] (fp64)."""
+    x = np.ascontiguousarray(x, np.uint16)
+    Wr = np.ascontiguousarray(Wr, np.float32)
+    T, H = x.shape
+    E = Wr.shape[0]
+    b = None if bias is None else np.ascontiguousarray(bias, np.float32)
+    ids = np.empty((T, k), np.int32)
+    w = np.empty((T, k), np.float64)
+    p = np.empty((T, k), np.float64)
+    logits = np.empty((T, E), np.float64)
+    gap = np.empty(T, np.float64)
+    lib().oracle_route(_p(x), _p(Wr), _p(b), T, H, E, k, _p(ids), _p(w), _p(p), _p(logits), _p(gap))
+    return ids, w, p, logits, gap
+
+
+def permute(ids, E):
+    ids = np.ascontiguousarray(ids, np.int32)
+    T, k = ids.shape
+    counts = np.empty(E, np.int32)
+    offsets = np.empty(E + 1, np.int32)
+    perm = np.empty(T * k, np.int32)
+    inv = np.empty(T * k, np.int32)
+    if lib().oracle_permute(_p(ids), T, k, E, _p(counts), _p(offsets), _p(perm), _p(inv)):
+        raise ValueError("expert id out of range")
+    return counts, offsets, perm, inv
+
+
+def e4m3_rne(t: float) -> int:
+    return lib().oracle_e4m3_rne(t)
+
+
+def e2m1_rne_sat(q: float) -> int:
+    return lib().oracle_e2m1_rne_sat(q)
+
+
+def nvfp4_quant(v):
+    v = np.ascontiguousarray(v, np.float32)
+    n = v.shape[0]
+    codes = np.empty(n // 2, np.uint8)
+    scales = np.empty(n // 16, np.uint8)
+    G = np.empty(1, np.float32)
+    lib().oracle_nvfp4_quant(_p(v), n, _p(codes), _p(scales), _p(G))
+    return codes, scales, float(G[0])
+
+
+def expert(rec, H, I, g3, x, act_quant=False):
+    x = np.ascontiguousarray(x, np.float64)
+    o = np.empty(H, np.float64)
+    lib().oracle_expert(_p(rec), H, I, _p(np.ascontiguousarray(g3, np.float32)), _p(x),
+                        int(act_quant), _p(o))
+    return o
+
+
+def shared(wg, wu, wd, x, round_h_bf16=False):
+    x = np.ascontiguousarray(x, np.float64)
+    Is, H = wg.shape
+    o = np.empty(H, np.float64)
+    lib().oracle_shared(_p(wg), _p(wu), _p(wd), H, Is, _p(x), int(round_h_bf16), _p(o))
+    return o
+
+
+def layer_forward(x, H, I, E, k, Wr, bias, records, g, shared_w=None, mode=0):
+    """y [T,H] fp64 plus ids, w, p_sel.  ``records`` maps expert id -> uint8
+    record array (a dict or a sequence with None for absent experts)."""
+    x = np.ascontiguousarray(x, np.uint16)
+    T = x.shape[0]
+    keep = []
+    ptrs = (ctypes.c_void_p * E)()
+    for e in range(E):
+        r = records.get(e) if isinstance(records, dict) else records[e]
+        if r is not None:
+            r = np.ascontiguousarray(r)
+            keep.append(r)
+            ptrs[e] = r.ctypes.data
+    y = np.empty((T, H), np.float64)
+    ids = np.empty((T, k), np.int32)
+    w = np.empty((T, k), np.float64)
+    p = np.empty((T, k), np.float64)
+    Is = 0 if shared_w is None else shared_w[0].shape[0]
+    sg, su, sd = (None, None, None) if shared_w is None else shared_w
+    rc = lib().oracle_layer_forward(
+        _p(x), T, H, I, E, k, Is, _p(np.ascontiguousarray(Wr, np.float32)),
+        _p(None if bias is None else np.ascontiguousarray(bias, np.float32)), ptrs,
+        _p(np.ascontiguousarray(g, np.float32)), _p(sg), _p(su), _p(sd), mode,
+        _p(y), _p(ids), _p(w), _p(p))
+    if rc:
+        raise ValueError("oracle_layer_forward: a selected expert has no record")
+    return y, ids, w, p

@@ -1,0 +1,438 @@
+/*
+ * oracle.c - plain, slow CPU oracle of the routed MoE layer (fp64).
+ *
+ * TEST INFRASTRUCTURE ONLY.  The tests, the smoke check and the bench's CPU
+ * baseline leg may call it; the library under routed_expert_layer_router_gb300/
+ * never does, and the two share no code, header, table or constant.
+ *
+ * What it computes, step by step (sources: "Project Maya" page, sections
+ * "Three tiers and the rules between them" and "A V100 has no BF16 and no FP8";
+ * the dev.to page "A hot expert cache made a 181 GiB model faster", sections
+ * "The wall: one PCIe transfer per token" and "A gather kernel that reads
+ * wide"; the Strata-GLM blog "Day one" list):
+ *   1. formats: E2M1 codes and E4M3 block scales decoded from their
+ *      definitions; weight = e2m1(code) * e4m3(scale of its 16-block) * g.
+ *   2. router: logits = W_r x + b in fp64; experts ordered by (logit desc,
+ *      id asc) with a full sort; ids = first k; p_sel = full softmax of the
+ *      selected; w = softmax over the selected logits (renormalised top-k).
+ *   3. permute: stable counting sort of routes r = t*k + j by expert id.
+ *   4. expert: g = Wg x, u = Wu x, h = silu(g) * u, o = Wd h (no biases).
+ *   5. combine: y_t = sum_j w_tj * o(e_tj, x_t) + shared(x_t); no residual.
+ *   6. prefill mode only: x (per token) and h (per route, after rounding to
+ *      fp32) pass through NVFP4 activation quantisation first:
+ *      G = amax/(6*448) (1 if amax == 0), s_b = e4m3_rne(amax_b / (6 G)),
+ *      q = e2m1_rne_sat(v / (s_b G)), all in IEEE fp32 with correctly
+ *      rounded division; the shared expert's h is rounded to bf16.
+ *   7. cache residency is not an input: the output depends on (x, weights).
+ * Compiled with -ffp-contract=off so fp32 steps are single roundings.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORC_API __attribute__((visibility("default")))
+
+/* ------------------------------------------------------------------ formats */
+
+/* E2M1: bit 3 sign, bits 2..1 exponent (bias 1), bit 0 mantissa; exponent 0
+ * is subnormal (0 or 0.5). */
+ORC_API double oracle_e2m1(unsigned c) {
+  unsigned e = (c >> 1) & 3u, m = c & 1u;
+  double mag = (e == 0) ? 0.5 * (double)m : ldexp(1.0 + 0.5 * (double)m, (int)e - 1);
+  return (c & 8u) ? -mag : mag;
+}
+
+/* E4M3 (FN variant): bit 7 sign, bits 6..3 exponent (bias 7), bits 2..0
+ * mantissa; exponent 0 is subnormal (m/8 * 2^-6); S.1111.111 is NaN; no inf. */
+ORC_API double oracle_e4m3(unsigned b) {
+  unsigned s = (b >> 7) & 1u, e = (b >> 3) & 15u, m = b & 7u;
+  double mag;
+  if (e == 15 && m == 7) return NAN;
+  if (e == 0) mag = ldexp((double)m / 8.0, -6);
+  else mag = ldexp(1.0 + (double)m / 8.0, (int)e - 7);
+  return s ? -mag : mag;
+}
+
+/* bf16 is the top half of an IEEE binary32 */
+ORC_API double oracle_bf16(uint16_t h) {
+  uint32_t u = (uint32_t)h << 16;
+  float f;
+  memcpy(&f, &u, 4);
+  return (double)f;
+}
+
+/* Negative controls: a planted defect makes the oracle wrong on purpose, so a
+ * test can show that the parity check fails by a wide margin when such a
+ * mistake is present.  0 = none (always the default). */
+enum { ORC_DEFECT_NONE = 0, ORC_DEFECT_NIBBLE_SWAP = 1, ORC_DEFECT_SCALE_UE8M0 = 2,
+       ORC_DEFECT_BLOCK_OFF_BY_ONE = 3, ORC_DEFECT_TIE_HIGH_ID = 4, ORC_DEFECT_SCALING_2_5 = 5 };
+static int g_defect = ORC_DEFECT_NONE;
+ORC_API void oracle_set_defect(int d) { g_defect = d; }
+
+static double g_e2m1[16];
+static double g_e4m3[256];
+static int g_tables_ready = 0;
+
+static void tables_init(void) {
+  if (g_tables_ready) return;
+  for (unsigned c = 0; c < 16; ++c) g_e2m1[c] = oracle_e2m1(c);
+  for (unsigned b = 0; b < 256; ++b) g_e4m3[b] = oracle_e4m3(b);
+  g_tables_ready = 1;
+}
+
+/* ----------------------------------------------------------- record access */
+
+/* Expert record: codes of gate [I][H], up [I][H], down [H][I] (row-major,
+ * element 2j in the low nibble), then their E4M3 scales, one per 16 elements,
+ * in 512-byte atoms: atom (r/128, kb/4) at ((r/128)*(KB/4) + kb/4)*512, byte
+ * (r%32)*16 + ((r%128)/32)*4 + kb%4 inside it. */
+typedef struct {
+  const uint8_t* codes;
+  const uint8_t* scales;
+  int R, K;
+  double g;
+} orc_mat;
+
+static orc_mat orc_matrix(const uint8_t* rec, int H, int I, int m, const float* g3) {
+  orc_mat M;
+  size_t gu_codes = (size_t)I * (size_t)H / 2;
+  size_t all_codes = 3 * gu_codes;
+  size_t gu_scales = (size_t)I * (size_t)H / 16;
+  M.R = (m == 2) ? H : I;
+  M.K = (m == 2) ? I : H;
+  M.codes = rec + (size_t)m * gu_codes;
+  M.scales = rec + all_codes + (size_t)m * gu_scales;
+  M.g = (double)g3[m];
+  return M;
+}
+
+static size_t orc_scale_pos(int r, int kb, int KB) {
+  size_t atom = (size_t)(r / 128) * (size_t)(KB / 4) + (size_t)(kb / 4);
+  return atom * 512 + (size_t)(r % 32) * 16 + (size_t)((r % 128) / 32) * 4 + (size_t)(kb % 4);
+}
+
+/* W[r][c] as a double */
+static double orc_w(const orc_mat* M, int r, int c) {
+  uint8_t byte = M->codes[(size_t)r * (size_t)(M->K / 2) + (size_t)(c / 2)];
+  int hi = (c & 1);
+  if (g_defect == ORC_DEFECT_NIBBLE_SWAP) hi = !hi;
+  unsigned code = hi ? (byte >> 4) : (byte & 15u);
+  int kb = c / 16;
+  if (g_defect == ORC_DEFECT_BLOCK_OFF_BY_ONE) kb = (kb + 1) % (M->K / 16);
+  uint8_t sb = M->scales[orc_scale_pos(r, kb, M->K / 16)];
+  double s = (g_defect == ORC_DEFECT_SCALE_UE8M0) ? ldexp(1.0, (int)sb - 127) : g_e4m3[sb];
+  return g_e2m1[code] * s * M->g;
+}
+
+/* one dequantised weight, exported for the format pins */
+ORC_API double oracle_weight(const uint8_t* rec, int H, int I, int m, int r, int c,
+                             const float* g3) {
+  tables_init();
+  orc_mat M = orc_matrix(rec, H, I, m, g3);
+  return orc_w(&M, r, c);
+}
+
+/* y = W x for one matrix, fp64 */
+static void orc_matvec(const orc_mat* M, const double* x, double* y) {
+  #pragma omp parallel for schedule(static)
+  for (int r = 0; r < M->R; ++r) {
+    double acc = 0.0;
+    for (int c = 0; c < M->K; ++c) acc += orc_w(M, r, c) * x[c];
+    y[r] = acc;
+  }
+}
+
+/* whole matrix dequantised, row-major [R][K], for brute-force pins */
+ORC_API void oracle_dequant_matrix(const uint8_t* rec, int H, int I, int m, const float* g3,
+                                   double* out) {
+  tables_init();
+  orc_mat M = orc_matrix(rec, H, I, m, g3);
+  for (int r = 0; r < M.R; ++r)
+    for (int c = 0; c < M.K; ++c) out[(size_t)r * M.K + c] = orc_w(&M, r, c);
+}
+
+/* ------------------------------------------------------------------ router */
+
+typedef struct { double l; int id; } orc_pair;
+
+static int orc_pair_cmp(const void* a, const void* b) {
+  const orc_pair* p = (const orc_pair*)a;
+  const orc_pair* q = (const orc_pair*)b;
+  if (p->l > q->l) return -1;
+  if (p->l < q->l) return 1;
+  if (g_defect == ORC_DEFECT_TIE_HIGH_ID) return (p->id > q->id) ? -1 : (p->id < q->id);
+  return (p->id < q->id) ? -1 : (p->id > q->id);
+}
+
+/* Router for T tokens.  x [T][H] bf16, Wr [E][H] fp32, bias [E] (nullable).
+ * Outputs ids [T][k], w [T][k], p_sel [T][k], logits [T][E] (nullable),
+ * gap [T] (nullable) = smallest difference between consecutive logits among
+ * the k+1 largest (E > k), used to reject near-ties when drawing inputs. */
+ORC_API void oracle_route(const uint16_t* x, const float* Wr, const float* bias, int T, int H,
+                          int E, int k, int32_t* ids, double* w, double* p_sel, double* logits,
+                          double* gap) {
+  #pragma omp parallel for schedule(dynamic, 1)
+  for (int t = 0; t < T; ++t) {
+    orc_pair* ord = (orc_pair*)malloc(sizeof(orc_pair) * (size_t)E);
+    double* xd = (double*)malloc(sizeof(double) * (size_t)H);
+    for (int h = 0; h < H; ++h) xd[h] = oracle_bf16(x[(size_t)t * H + h]);
+    for (int e = 0; e < E; ++e) {
+      double acc = 0.0;
+      for (int h = 0; h < H; ++h) acc += (double)Wr[(size_t)e * H + h] * xd[h];
+      if (bias) acc += (double)bias[e];
+      ord[e].l = acc;
+      ord[e].id = e;
+      if (logits) logits[(size_t)t * E + e] = acc;
+    }
+    qsort(ord, (size_t)E, sizeof(orc_pair), orc_pair_cmp);
+    double lmax = ord[0].l;
+    double z_all = 0.0, z_sel = 0.0;
+    for (int e = 0; e < E; ++e) z_all += exp(ord[e].l - lmax);
+    for (int j = 0; j < k; ++j) z_sel += exp(ord[j].l - lmax);
+    for (int j = 0; j < k; ++j) {
+      double pj = exp(ord[j].l - lmax);
+      ids[(size_t)t * k + j] = ord[j].id;
+      if (p_sel) p_sel[(size_t)t * k + j] = pj / z_all;
+      if (w) w[(size_t)t * k + j] = pj / z_sel;
+    }
+    if (gap) {
+      double gmin = INFINITY;
+      for (int j = 0; j < k && j + 1 < E; ++j) {
+        double d = ord[j].l - ord[j + 1].l;
+        if (d < gmin) gmin = d;
+      }
+      gap[t] = gmin;
+    }
+    free(xd);
+    free(ord);
+  }
+}
+
+/* ------------------------------------------------------------------ permute */
+
+/* Stable counting sort of routes r = t*k + j by expert id: perm[p] = r for
+ * the p-th route in (expert asc, r asc) order; inv[r] = p. */
+ORC_API int oracle_permute(const int32_t* ids, int T, int k, int E, int32_t* counts,
+                           int32_t* offsets, int32_t* perm, int32_t* inv) {
+  int n = T * k;
+  for (int e = 0; e < E; ++e) counts[e] = 0;
+  for (int r = 0; r < n; ++r) {
+    if (ids[r] < 0 || ids[r] >= E) return 1;
+    counts[ids[r]]++;
+  }
+  offsets[0] = 0;
+  for (int e = 0; e < E; ++e) offsets[e + 1] = offsets[e] + counts[e];
+  int32_t* fill = (int32_t*)malloc(sizeof(int32_t) * (size_t)E);
+  for (int e = 0; e < E; ++e) fill[e] = offsets[e];
+  for (int r = 0; r < n; ++r) {
+    int p = fill[ids[r]]++;
+    perm[p] = r;
+    inv[r] = p;
+  }
+  free(fill);
+  return 0;
+}
+
+/* ------------------------------------------------- NVFP4 activation quant */
+
+/* nearest E4M3 value to t >= 0 (brute force over the finite codes), ties to
+ * the even code, values above 448 saturate to 448 (code 0x7E) */
+ORC_API unsigned oracle_e4m3_rne(float t) {
+  tables_init();
+  if (!(t > 0.0f)) return 0;
+  unsigned best = 0;
+  double bd = INFINITY;
+  for (unsigned b = 0; b <= 0x7E; ++b) {
+    double d = fabs(g_e4m3[b] - (double)t);
+    if (d < bd || (d == bd && (b & 1u) == 0)) { bd = d; best = b; }
+  }
+  return best;
+}
+
+/* nearest E2M1 magnitude to |q| (brute force), ties to the even code,
+ * saturating at 6; the sign bit follows the sign bit of q */
+ORC_API unsigned oracle_e2m1_rne_sat(float q) {
+  tables_init();
+  double a = fabs((double)q);
+  unsigned best = 0;
+  double bd = INFINITY;
+  for (unsigned c = 0; c < 8; ++c) {
+    double d = fabs(g_e2m1[c] - a);
+    if (d < bd || (d == bd && (c & 1u) == 0)) { bd = d; best = c; }
+  }
+  if (a > 6.0) best = 7;
+  return signbit(q) ? (best | 8u) : best;
+}
+
+/* NVFP4 quantisation of one row of n fp32 values (n % 16 == 0): codes [n/2]
+ * (element 2j in the low nibble), scales [n/16] (row order, one per block),
+ * G (per-row fp32 global).  Returns nothing; all steps in IEEE fp32. */
+ORC_API void oracle_nvfp4_quant(const float* v, int n, uint8_t* codes, uint8_t* scales,
+                                float* G_out) {
+  tables_init();
+  float amax = 0.0f;
+  for (int i = 0; i < n; ++i) {
+    float a = fabsf(v[i]);
+    if (a > amax) amax = a;
+  }
+  volatile float six448 = 2688.0f;
+  float G = (amax > 0.0f) ? amax / six448 : 1.0f;
+  *G_out = G;
+  for (int b = 0; b < n / 16; ++b) {
+    float ab = 0.0f;
+    for (int i = 0; i < 16; ++i) {
+      float a = fabsf(v[b * 16 + i]);
+      if (a > ab) ab = a;
+    }
+    volatile float sixG = 6.0f * G;
+    float t = ab / sixG;
+    unsigned s = oracle_e4m3_rne(t);
+    scales[b] = (uint8_t)s;
+    volatile float sdq = (float)g_e4m3[s] * G;
+    for (int i = 0; i < 16; i += 2) {
+      unsigned lo = 0, hi = 0;
+      if (s != 0) {
+        float q0 = v[b * 16 + i] / sdq;
+        float q1 = v[b * 16 + i + 1] / sdq;
+        lo = oracle_e2m1_rne_sat(q0);
+        hi = oracle_e2m1_rne_sat(q1);
+      }
+      codes[(b * 16 + i) / 2] = (uint8_t)(lo | (hi << 4));
+    }
+  }
+}
+
+/* value of a quantised row, fp64 */
+static void orc_nvfp4_dequant(const uint8_t* codes, const uint8_t* scales, float G, int n,
+                              double* out) {
+  for (int i = 0; i < n; ++i) {
+    unsigned c = (i & 1) ? (codes[i / 2] >> 4) : (codes[i / 2] & 15u);
+    out[i] = g_e2m1[c] * g_e4m3[scales[i / 16]] * (double)G;
+  }
+}
+
+/* quantise-then-dequantise of a row given in fp32 */
+static void orc_act_quant(const float* v, int n, double* out) {
+  uint8_t* codes = (uint8_t*)malloc((size_t)n / 2);
+  uint8_t* scales = (uint8_t*)malloc((size_t)n / 16);
+  float G;
+  oracle_nvfp4_quant(v, n, codes, scales, &G);
+  orc_nvfp4_dequant(codes, scales, G, n, out);
+  free(codes);
+  free(scales);
+}
+
+/* ------------------------------------------------------------------ experts */
+
+static double orc_silu(double g) { return g / (1.0 + exp(-g)); }
+
+/* One routed expert on one activation vector x [H] -> o [H].
+ * act_quant != 0: prefill numerics (h rounded to fp32 and NVFP4-quantised
+ * before the down projection; x must already be the quantised value). */
+ORC_API void oracle_expert(const uint8_t* rec, int H, int I, const float* g3, const double* x,
+                           int act_quant, double* o) {
+  tables_init();
+  orc_mat Mg = orc_matrix(rec, H, I, 0, g3);
+  orc_mat Mu = orc_matrix(rec, H, I, 1, g3);
+  orc_mat Md = orc_matrix(rec, H, I, 2, g3);
+  double* g = (double*)malloc(sizeof(double) * (size_t)I);
+  double* u = (double*)malloc(sizeof(double) * (size_t)I);
+  double* h = (double*)malloc(sizeof(double) * (size_t)I);
+  orc_matvec(&Mg, x, g);
+  orc_matvec(&Mu, x, u);
+  for (int i = 0; i < I; ++i) h[i] = orc_silu(g[i]) * u[i];
+  if (act_quant) {
+    float* hf = (float*)malloc(sizeof(float) * (size_t)I);
+    for (int i = 0; i < I; ++i) hf[i] = (float)h[i];
+    orc_act_quant(hf, I, h);
+    free(hf);
+  }
+  orc_matvec(&Md, h, o);
+  free(g);
+  free(u);
+  free(h);
+}
+
+/* Shared expert with bf16 weights gate/up [Is][H], down [H][Is].
+ * round_h_bf16 != 0: h is rounded to bf16 (RNE) before the down projection. */
+ORC_API void oracle_shared(const uint16_t* wg, const uint16_t* wu, const uint16_t* wd, int H,
+                           int Is, const double* x, int round_h_bf16, double* o) {
+  double* h = (double*)malloc(sizeof(double) * (size_t)Is);
+  #pragma omp parallel for schedule(static)
+  for (int i = 0; i < Is; ++i) {
+    double g = 0.0, u = 0.0;
+    for (int c = 0; c < H; ++c) {
+      g += oracle_bf16(wg[(size_t)i * H + c]) * x[c];
+      u += oracle_bf16(wu[(size_t)i * H + c]) * x[c];
+    }
+    double hv = orc_silu(g) * u;
+    if (round_h_bf16) {
+      float f = (float)hv;
+      uint32_t b;
+      memcpy(&b, &f, 4);
+      b = (b + 0x7FFFu + ((b >> 16) & 1u)) & 0xFFFF0000u;
+      memcpy(&f, &b, 4);
+      hv = (double)f;
+    }
+    h[i] = hv;
+  }
+  #pragma omp parallel for schedule(static)
+  for (int r = 0; r < H; ++r) {
+    double acc = 0.0;
+    for (int i = 0; i < Is; ++i) acc += oracle_bf16(wd[(size_t)r * Is + i]) * h[i];
+    o[r] = acc;
+  }
+  free(h);
+}
+
+/* -------------------------------------------------------------------- layer */
+
+/* Full layer on T tokens.  rec[e] points to expert e's record (may be NULL
+ * for experts no token selects; selecting one returns 2).  g [E][3].
+ * Shared weights may be NULL (Is == 0).  mode 0 = decode numerics, 1 =
+ * prefill numerics (activation quantisation).  Outputs y [T][H] (fp64) and,
+ * when non-NULL, ids/w/p_sel [T][k]. */
+ORC_API int oracle_layer_forward(const uint16_t* x, int T, int H, int I, int E, int k, int Is,
+                                 const float* Wr, const float* bias, const uint8_t* const* rec,
+                                 const float* g, const uint16_t* sg, const uint16_t* su,
+                                 const uint16_t* sd, int mode, double* y, int32_t* ids_out,
+                                 double* w_out, double* p_out) {
+  tables_init();
+  int32_t* ids = (int32_t*)malloc(sizeof(int32_t) * (size_t)T * k);
+  double* w = (double*)malloc(sizeof(double) * (size_t)T * k);
+  double* p = (double*)malloc(sizeof(double) * (size_t)T * k);
+  oracle_route(x, Wr, bias, T, H, E, k, ids, w, p, NULL, NULL);
+  for (int r = 0; r < T * k; ++r)
+    if (!rec[ids[r]]) { free(ids); free(w); free(p); return 2; }
+  double* xd = (double*)malloc(sizeof(double) * (size_t)H);
+  double* xq = (double*)malloc(sizeof(double) * (size_t)H);
+  float* xf = (float*)malloc(sizeof(float) * (size_t)H);
+  double* o = (double*)malloc(sizeof(double) * (size_t)H);
+  for (int t = 0; t < T; ++t) {
+    for (int c = 0; c < H; ++c) {
+      xd[c] = oracle_bf16(x[(size_t)t * H + c]);
+      xf[c] = (float)xd[c];
+    }
+    if (mode == 1) orc_act_quant(xf, H, xq);
+    else memcpy(xq, xd, sizeof(double) * (size_t)H);
+    double* yt = y + (size_t)t * H;
+    for (int c = 0; c < H; ++c) yt[c] = 0.0;
+    for (int j = 0; j < k; ++j) {
+      int e = ids[(size_t)t * k + j];
+      oracle_expert(rec[e], H, I, g + 3 * e, xq, mode == 1, o);
+      double wj = w[(size_t)t * k + j];
+      if (g_defect == ORC_DEFECT_SCALING_2_5) wj *= 2.5;
+      for (int c = 0; c < H; ++c) yt[c] += wj * o[c];
+    }
+    if (Is > 0 && sg && su && sd) {
+      oracle_shared(sg, su, sd, H, Is, xd, mode == 1, o);
+      for (int c = 0; c < H; ++c) yt[c] += o[c];
+    }
+  }
+  if (ids_out) memcpy(ids_out, ids, sizeof(int32_t) * (size_t)T * k);
+  if (w_out) memcpy(w_out, w, sizeof(double) * (size_t)T * k);
+  if (p_out) memcpy(p_out, p, sizeof(double) * (size_t)T * k);
+  free(ids); free(w); free(p); free(xd); free(xq); free(xf); free(o);
+  return 0;
+}

@@ -1,0 +1,22 @@
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def pytest_configure(config):
+    config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
+
+
+@pytest.fixture(scope="session", autouse=True)
+def _host_libs():
+    """Build the host-side C libraries (generator, oracle) once per session."""
+    import gen
+    import oracle
+    gen.build(cuda=False)
+    oracle.build()
+    yield
