@@ -1,0 +1,167 @@
+"""Builds a workload's inputs on the GPU and wires them into the library:
+router weights, global scales, shared expert, per-layer bias, expert records
+(resident ones written straight into cache slots by the device generator,
+the others into a pinned host arena), and one MoELayer per layer.
+
+Holds no arithmetic of the layer: generation is the seeded generator, the
+cache/placement decisions follow the workload recipe (all resident; the
+smallest Zipf ranks; or a given saliency order).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+import torch
+
+import gen
+from routed_expert_layer_router_gb300.layer import ExpertCache, HostArena, MoELayer
+
+
+@dataclass
+class DeviceWorkload:
+    wl: gen.Workload
+    layers: int
+    cache: ExpertCache
+    moe_layers: list
+    w_router: list
+    gscale: list            # device [E,3] per layer
+    gscale_host: list       # numpy [E,3] per layer
+    bias: list              # device or None per layer
+    bias_host: list
+    shared: list            # (g, u, d) device per layer or None
+    resident: list          # per layer: sorted list of resident experts
+    host_arena: HostArena | None = None
+    # generator layer index whose records layer l uses (l itself, or 0 when
+    # host records are aliased across layers)
+    record_layer: list = field(default_factory=list)
+    extra: dict = field(default_factory=dict)
+
+    def close(self):
+        for m in self.moe_layers:
+            m.close()
+        self.cache.close()
+        if self.host_arena is not None:
+            self.host_arena.close()
+
+
+def _hot_set(wl: gen.Workload, layer: int, bias_rank, saliency_order):
+    if wl.hot <= 0 or wl.hot >= wl.E:
+        return list(range(wl.E))
+    if wl.hot_rule == "zipf":
+        return sorted(int(e) for e in np.argsort(bias_rank)[:wl.hot])
+    if wl.hot_rule == "saliency":
+        return sorted(int(e) for e in saliency_order[layer][:wl.hot])
+    raise ValueError(wl.hot_rule)
+
+
+def build(wl: gen.Workload, layers: int | None = None, T_max: int | None = None,
+          n_stage: int | None = None, saliency_order=None, prefill_min_tokens: int | None = None,
+          alias_host_records: bool = False, resident=None, stream=None) -> DeviceWorkload:
+    """Device-resident layer(s) of workload `wl`.
+
+    layers: how many of the workload's layers to build (default: all).
+    n_stage: staging slots (default: enough for every miss of one layer).
+    saliency_order: per layer, experts by decreasing saliency (hot_rule "saliency").
+    alias_host_records: store one host copy per expert id shared by all layers
+      (the host-index table maps every layer to it) when host memory is short;
+      the records then repeat across layers for both the GPU and the oracle.
+    """
+    L = wl.layers if layers is None else layers
+    E, H, I, k = wl.E, wl.H, wl.I, wl.k
+    T_max = T_max or wl.T
+    dev = torch.device("cuda")
+    rb = gen.record_bytes(H, I)
+    s = torch.cuda.current_stream() if stream is None else stream
+    sp = s.cuda_stream
+
+    bias_host, ranks = [], []
+    for l in range(L):
+        if wl.zipf_alpha > 0:
+            b, r = gen.zipf_bias(wl.seed, l, E, wl.zipf_alpha)
+        else:
+            b, r = None, np.arange(1, E + 1, dtype=np.int32)
+        bias_host.append(b)
+        ranks.append(r)
+    rec_layer = [0 if alias_host_records else l for l in range(L)]
+    if resident is None:
+        resident = [_hot_set(wl, l, ranks[l], saliency_order) for l in range(L)]
+    else:
+        resident = [sorted(int(e) for e in r) for r in resident]
+    n_res = [len(r) for r in resident]
+    layer_slots = np.concatenate([[0], np.cumsum(n_res)]).astype(np.int32)
+    n_cache = int(layer_slots[-1])
+    miss_max = max(E - n for n in n_res)
+    if n_stage is None:
+        n_stage = min(miss_max, T_max * k) if miss_max > 0 else 0
+
+    # host arena for non-resident records
+    host_arena, host_index = None, None
+    if miss_max > 0:
+        host_index = np.full((L, E), -1, np.int64)
+        if alias_host_records:
+            ids = sorted(set(e for l in range(L) for e in range(E) if e not in set(resident[l])))
+            pos = {e: i for i, e in enumerate(ids)}
+            for l in range(L):
+                rs = set(resident[l])
+                for e in range(E):
+                    if e not in rs:
+                        host_index[l, e] = pos[e]
+            host_arena = HostArena(len(ids), rb)
+            fill_list = [(0, e, pos[e]) for e in ids]
+        else:
+            fill_list = []
+            for l in range(L):
+                rs = set(resident[l])
+                for e in range(E):
+                    if e not in rs:
+                        host_index[l, e] = len(fill_list)
+                        fill_list.append((l, e, len(fill_list)))
+            host_arena = HostArena(len(fill_list), rb)
+        # generate on the device in batches and copy down into the arena
+        batch = 16
+        buf = torch.empty((batch, rb), dtype=torch.uint8, device=dev)
+        for i0 in range(0, len(fill_list), batch):
+            chunk = fill_list[i0:i0 + batch]
+            for j, (l, e, _) in enumerate(chunk):
+                gen.dev_expert_record(wl.seed, rec_layer[l], e, H, I, buf[j].data_ptr(), sp)
+            s.synchronize()
+            for j, (l, e, idx) in enumerate(chunk):
+                torch.from_numpy(host_arena.array[idx]).copy_(buf[j].cpu())
+        del buf
+        host_arena.register()
+
+    cache = ExpertCache(L, E, H, I, n_cache, n_stage, layer_slots=layer_slots,
+                        host_arena=host_arena, host_index=host_index)
+    for l in range(L):
+        for j, e in enumerate(resident[l]):
+            slot = int(layer_slots[l]) + j
+            gen.dev_expert_record(wl.seed, rec_layer[l], e, H, I, cache.slot_ptr(slot), sp)
+            cache.set_resident(l, e, slot, s)
+
+    w_router, gscale, gscale_host, bias, shared, mls = [], [], [], [], [], []
+    pmin = prefill_min_tokens if prefill_min_tokens is not None else (
+        max(T_max, 1) if wl.prefill else 0)
+    for l in range(L):
+        wr = torch.empty((E, H), dtype=torch.float32, device=dev)
+        gen.dev_router_f32(wl.seed, l, E, H, wr.data_ptr(), sp)
+        gh = gen.global_scales(wl.seed, l, E)
+        g = torch.from_numpy(gh).to(dev)
+        b = torch.from_numpy(bias_host[l]).to(dev) if bias_host[l] is not None else None
+        sh = None
+        if wl.Is > 0:
+            sg = torch.empty((wl.Is, H), dtype=torch.bfloat16, device=dev)
+            su = torch.empty((wl.Is, H), dtype=torch.bfloat16, device=dev)
+            sd = torch.empty((H, wl.Is), dtype=torch.bfloat16, device=dev)
+            gen.dev_shared_bf16(wl.seed, l, wl.Is, H, sg.data_ptr(), su.data_ptr(), sd.data_ptr(), sp)
+            sh = (sg, su, sd)
+        w_router.append(wr)
+        gscale.append(g)
+        gscale_host.append(gh)
+        bias.append(b)
+        shared.append(sh)
+        mls.append(MoELayer(cache, l, wr, g, k, bias=b, shared=sh, T_max=T_max,
+                            prefill_min_tokens=pmin, prefill_group=wl.group))
+    s.synchronize()
+    return DeviceWorkload(wl, L, cache, mls, w_router, gscale, gscale_host, bias, bias_host,
+                          shared, resident, host_arena, record_layer=rec_layer)

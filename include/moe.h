@@ -1,0 +1,300 @@
+/*
+ * moe.h - C ABI of the routed mixture-of-experts layer library (libmoe.so)
+ * for one GB300 GPU (sm_103a).
+ *
+ * The layer (GLM-5.3-Flash style: 288 routed experts, top-8 per token, one
+ * shared expert) runs in these steps, each a hand-written CUDA kernel:
+ *   moe_route        router GEMV/GEMM + softmax + top-k + renormalisation
+ *   moe_permute      token->expert histogram, scan and stable permutation
+ *   expcache_lookup  per-layer HBM hot-expert cache: hit slot or staged miss
+ *   expcache_fill    wide-read gather of records from pinned host memory
+ *   moe_expert_ffn   NVFP4 gate/up -> SiLU*mul -> down per selected expert
+ *   moe_combine      weighted sum of the experts' outputs (+ shared) -> bf16
+ *   moe_layer_forward  all of the above in order on one stream.
+ * Sources of the operations: "Project Maya" page, sections "What is in the
+ * 96.5 GB" (an expert blob is gate+up+down; top-8 of 288; fp32 router) and
+ * "Three tiers and the rules between them" (device router, device table
+ * layer x expert -> VRAM slot, per-layer slot partitions, GPU pull of
+ * RAM-tier experts from host-mapped memory with 16-byte loads); dev.to page
+ * "A hot expert cache made a 181 GiB model faster", sections "The wall"
+ * (NVFP4 experts, 8 of 288 per token), "A gather kernel that reads wide"
+ * (wide-read gather driven by a GPU-resident expert list, no host sync, CUDA
+ * graph replay), "Offload more, cache the hot experts" (per-layer cache of
+ * the 66 most-used experts) and "Prefill in groups of 64 experts"; the
+ * Strata-GLM blog "Day one" list (exclusive tiers, byte-sized slots, chunked
+ * prefill as one batched matmul per expert).
+ *
+ * Conventions for every call:
+ *   - Pointers named d_* or documented "device" are device addresses; the
+ *     caller owns every buffer it passes and every stream.  The library owns
+ *     only its opaque handles (expcache, moe_layer) and what they allocate.
+ *   - Every call is stream-ordered and asynchronous: it enqueues work on
+ *     `stream` (a cudaStream_t, NULL = legacy default stream) and returns
+ *     without synchronising, except where documented.
+ *   - Argument errors are detected on the host and returned at once, before
+ *     anything is enqueued.  Errors only visible on the device (an expert id
+ *     out of range, a slot outside its layer's partition, a miss with no host
+ *     record, a bounded wait that ran out) are written to a sticky device
+ *     status word (int32, first error wins) when the caller passes one; no
+ *     kernel traps.  The kernel that sees such an error skips the bad item.
+ *   - Shapes: H % 256 == 0, I % 128 == 0, 1 <= k <= min(E, 32), E <= 1024.
+ *
+ * Expert record (the storage and transfer unit; fixed stride per (H, I)):
+ *   [gate codes I x H/2][up codes I x H/2][down codes H x I/2]
+ *   [gate scales I x H/16][up scales I x H/16][down scales H x I/16]
+ *   Codes: E2M1 (sign bit 3; magnitudes 0, .5, 1, 1.5, 2, 3, 4, 6), two per
+ *   byte, element 2j in the low nibble, rows contiguous (K-major).
+ *   Scales: E4M3 (FN; bias 7; max 448), one per 16 consecutive elements of a
+ *   row, stored in 512-byte atoms: for row r and 16-block kb of a matrix
+ *   with KB = K/16 blocks per row, byte
+ *     ((r/128)*(KB/4) + kb/4)*512 + (r%32)*16 + ((r%128)/32)*4 + kb%4.
+ *   weight(r, c) = e2m1(code) * e4m3(scale(r, c/16)) * g[expert][matrix],
+ *   g an fp32 per-(expert, matrix) global scale held outside the record.
+ *   Size: 3*I*H/2 + 3*I*H/16 bytes (21,233,664 for H = 6144, I = 2048).
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int moe_status;
+enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1, /* NULL where required, negative size, k > E, ...      */
+  MOE_ERR_UNSUPPORTED = 2, /* shape or alignment outside what the kernels handle  */
+  MOE_ERR_CUDA = 3,        /* a CUDA runtime call failed (launch, copy, ...)      */
+  MOE_ERR_OOM = 4,         /* device allocation failed                            */
+  MOE_ERR_TIMEOUT = 5,     /* a bounded device wait ran out (device status only)  */
+  MOE_ERR_DEVICE = 6       /* bad id / slot / record seen on the device           */
+};
+
+/* Human-readable name of a status code (static storage). */
+const char* moe_status_string(moe_status s);
+
+/* ABI version of this header (bumped on any incompatible change). */
+int moe_abi_version(void);
+
+/* Bytes of one expert record for hidden size H and expert intermediate I. */
+uint64_t moe_record_bytes(int H, int I);
+
+/* ------------------------------------------------------------------ route
+ * Router of the "Project Maya" page (device-side router, fp32 router
+ * weights): logits[t][e] = sum_h W_r[e][h] * x[t][h] + bias[e] (fp32); the
+ * k largest logits in (logit desc, id asc) order give ids[t][0..k); p_sel is
+ * the full-softmax probability of each selected expert; w is the softmax over
+ * the selected logits only (renormalised top-k, sums to 1 per token).
+ */
+typedef struct {
+  const void* x;        /* device [T][H] bf16, row-major                        */
+  const float* w_router;/* device [E][H] fp32                                   */
+  const float* bias;    /* device [E] fp32, or NULL for none                     */
+  int T, H, E, k;
+  int32_t* ids;         /* device out [T][k]                                     */
+  float* w;             /* device out [T][k] renormalised weights                */
+  float* p_sel;         /* device out [T][k] full-softmax probabilities, or NULL */
+  float* logits;        /* device [T][E] fp32: output if non-NULL; else the call
+                           needs workspace of moe_route_workspace_bytes(T, E)   */
+  void* workspace;      /* device scratch, may be NULL when logits != NULL       */
+  size_t workspace_bytes;
+  int32_t* status;      /* device sticky status word, or NULL                    */
+} moe_route_args;
+
+size_t moe_route_workspace_bytes(int T, int E);
+moe_status moe_route(const moe_route_args* a, void* stream);
+
+/* ---------------------------------------------------------------- permute
+ * Groups the T*k routes r = t*k + j by expert (the batched-matmul-per-expert
+ * grouping of the Strata-GLM blog's chunked prefill): counts[e] = routes to
+ * e; offsets = exclusive scan of counts (E+1 entries); perm[p] = r for the
+ * p-th route in (expert asc, r asc) order - a stable sort, so the result is
+ * unique; inv[r] = p.  pad_offsets (optional) is the exclusive scan of the
+ * counts rounded up to multiples of pad_align (the prefill staging layout).
+ * Out-of-range ids set MOE_ERR_DEVICE in *status and are dropped.
+ * One thread block; T*k <= 1<<20.
+ */
+moe_status moe_permute(const int32_t* ids, int T, int k, int E, int32_t* counts,
+                       int32_t* offsets, int32_t* perm, int32_t* inv, int32_t* pad_offsets,
+                       int pad_align, int32_t* status, void* stream);
+
+/* ---------------------------------------------------------- expert cache
+ * Per-layer HBM hot-expert cache ("Project Maya": a device table layer x
+ * expert -> VRAM slot, each layer owning its own run of slots; dev.to: a
+ * per-layer cache of the most-used experts, misses pulled from host RAM by
+ * a wide-read gather driven by a device-resident list).  Device memory holds
+ * n_cache_slots cache slots followed by n_stage staging slots, one record
+ * each; slot s is at expcache_slot_ptr(c, s).  Records that are not resident
+ * live in a pinned host arena owned by the caller (allocated with
+ * cudaHostAlloc(..., cudaHostAllocMapped) or registered with
+ * cudaHostRegister(..., cudaHostRegisterMapped)); the cache maps it with
+ * cudaHostGetDevicePointer and never frees it; it must stay valid and
+ * unchanged while the cache exists.
+ */
+typedef struct expcache expcache;
+
+typedef struct {
+  int L, E;                     /* layers, experts per layer                        */
+  int H, I;                     /* dims (record size = moe_record_bytes(H, I))      */
+  int n_cache_slots;            /* HBM cache slots, all layers                      */
+  const int32_t* layer_slots;   /* host [L+1]: layer l owns slots
+                                   [layer_slots[l], layer_slots[l+1]); NULL = every
+                                   layer may use every cache slot                   */
+  int n_stage;                  /* HBM staging slots for misses (>= 0)              */
+  const void* host_arena;       /* pinned host records, or NULL if none             */
+  uint64_t host_arena_records;  /* records in the host arena                        */
+  const int64_t* host_index;    /* host [L][E]: record index in the host arena of
+                                   (layer, expert), -1 = not there; NULL = none     */
+} expcache_desc;
+
+/* Allocates the slot arenas and the device slot table (all entries -1 = not
+ * resident) and maps the host arena.  Synchronous.  MOE_ERR_OOM if the
+ * arenas do not fit. */
+moe_status expcache_create(const expcache_desc* d, expcache** out);
+/* Frees what create allocated (the host arena is the caller's).  Synchronous. */
+moe_status expcache_destroy(expcache* c);
+/* Device address of slot s (cache slots first, then staging), NULL if out of range. */
+void* expcache_slot_ptr(const expcache* c, int s);
+/* Device [L][E] int32 slot table (-1 = not resident). */
+const int32_t* expcache_slot_table(const expcache* c);
+/* Marks (layer, expert) resident in cache slot `slot` (the caller has written
+ * the record there, e.g. with cudaMemcpyAsync on the same stream), or not
+ * resident when slot == -1.  Stream-ordered table write. */
+moe_status expcache_set_resident(expcache* c, int layer, int expert, int slot, void* stream);
+
+/* Wide-read gather: for list entries i in [first, first + max_count) with
+ * i < *d_n, copies the host record of (layer, d_expert_ids[i]) into cache
+ * slot d_dst_slots[i] (and marks it resident), or, when d_dst_slots is NULL,
+ * into staging slot n_cache_slots + (i mod n_stage).  The copy is done by
+ * thread blocks reading the mapped host memory with 16-byte loads.  The list
+ * and its length stay on the device (no host synchronisation), so the call
+ * can be captured in a CUDA graph. */
+moe_status expcache_fill(expcache* c, int layer, const int32_t* d_expert_ids, const int32_t* d_n,
+                         int first, int max_count, const int32_t* d_dst_slots, int32_t* status,
+                         void* stream);
+
+/* Lookup for one layer: for every expert e with counts[e] > 0 (active),
+ * src_slot[e] = its cache slot (a hit) or, for the i-th miss in ascending
+ * expert id, the staging slot n_cache_slots + (i mod n_stage); -1 when not
+ * active.  act_list lists the active experts, hits first (ascending id), then
+ * misses (ascending id); n_act[0] = active count, n_act[1] = hit count.
+ * miss_ids / n_miss list the misses (ascending id), ready for expcache_fill.
+ * A miss with n_stage == 0, or a table slot outside the layer's partition,
+ * sets MOE_ERR_DEVICE in *status. */
+moe_status expcache_lookup(const expcache* c, int layer, const int32_t* counts, int32_t* src_slot,
+                           int32_t* act_list, int32_t* n_act, int32_t* miss_ids, int32_t* n_miss,
+                           int32_t* status, void* stream);
+
+/* ------------------------------------------------------------- expert FFN
+ * For each route p (p-th route of the expert-sorted order) of the active
+ * experts of group `group` (group 0 = all hits and misses [0, n_stage);
+ * group g > 0 = misses [g*n_stage, (g+1)*n_stage)), with e its expert and t
+ * its token: g = Wg x_t, u = Wu x_t, h = silu(g) * u, o = Wd h, all weights
+ * read from the record in slot src_slot[e] (SiLU-gated FFN without biases).
+ * DECODE mode: weights dequantised in registers, fp32 FMA on the bf16
+ *   activations; writes o_route[p] = w[t][j] * o (fp32).  For routes whose
+ *   expert is not in the group nothing is written.
+ * PREFILL mode: activations quantised to NVFP4 (per token, and h per route:
+ *   G = amax/(6*448), block scale e4m3_rne(amax_b/(6 G)), codes
+ *   e2m1_rne(v/(s G))) and multiplied on the tcgen05 tensor cores (FP4 x FP4,
+ *   fp32 accumulation in tensor memory); adds w[t][j] * o into y_acc[t]
+ *   (fp32, caller-zeroed).
+ * Shared expert (Is > 0, group 0 only): bf16 gate/up [Is][H], down [H][Is];
+ *   writes o_shared[t] = shared(x_t) (fp32).
+ * stages (DECODE only): MOE_STAGE_GATE_UP computes h into the workspace,
+ *   MOE_STAGE_DOWN consumes it; MOE_STAGE_ALL does both.
+ */
+enum { MOE_MODE_DECODE = 0, MOE_MODE_PREFILL = 1 };
+enum { MOE_STAGE_GATE_UP = 1, MOE_STAGE_DOWN = 2, MOE_STAGE_ALL = 3 };
+
+typedef struct {
+  int mode, stages;
+  int T, H, I, E, k;
+  const void* x;             /* device [T][H] bf16                                  */
+  const expcache* cache;     /* weights come from its slots                          */
+  const float* gscale;       /* device [E][3] fp32 global scales (gate, up, down)    */
+  const int32_t* src_slot;   /* device [E]  (expcache_lookup)                        */
+  const int32_t* act_list;   /* device [E]  (expcache_lookup)                        */
+  const int32_t* n_act;      /* device [2]  (expcache_lookup)                        */
+  const int32_t* offsets;    /* device [E+1] (moe_permute)                            */
+  const int32_t* pad_offsets;/* device [E+1] (moe_permute, pad_align 128; PREFILL)    */
+  const int32_t* perm;       /* device [T*k] (moe_permute)                            */
+  const float* w;            /* device [T][k] routing weights (moe_route)            */
+  int group, n_stage;        /* expert group walked by this call                     */
+  int Is;                    /* shared expert intermediate size, 0 = none            */
+  const void* s_gate;        /* device bf16 [Is][H]                                   */
+  const void* s_up;          /* device bf16 [Is][H]                                   */
+  const void* s_down;        /* device bf16 [H][Is]                                   */
+  float* o_route;            /* DECODE: device out [T*k][H] fp32                      */
+  float* y_acc;              /* PREFILL: device in/out [T][H] fp32                    */
+  float* o_shared;           /* device out [T][H] fp32 (Is > 0)                       */
+  void* workspace;           /* device scratch of moe_ffn_workspace_bytes(...)        */
+  size_t workspace_bytes;
+  int32_t* status;           /* device sticky status word, or NULL                   */
+} moe_ffn_args;
+
+size_t moe_ffn_workspace_bytes(int mode, int T, int H, int I, int E, int k, int Is);
+moe_status moe_expert_ffn(const moe_ffn_args* a, void* stream);
+
+/* ---------------------------------------------------------------- combine
+ * y[t] = bf16_rne( y_acc[t] + sum_{j<k} o_route[inv[t*k+j]] + o_shared[t] ),
+ * each term skipped when its pointer is NULL; the k-term sum is taken in
+ * j order (deterministic).  No residual is added. */
+typedef struct {
+  int T, H, k;
+  const float* y_acc;     /* device [T][H] or NULL            */
+  const float* o_route;   /* device [T*k][H] or NULL          */
+  const int32_t* inv;     /* device [T*k] (with o_route)      */
+  const float* o_shared;  /* device [T][H] or NULL            */
+  void* y;                /* device out [T][H] bf16           */
+} moe_combine_args;
+
+moe_status moe_combine(const moe_combine_args* a, void* stream);
+
+/* ------------------------------------------------------------------ layer
+ * One MoE layer: owns a workspace for up to T_max tokens and runs route ->
+ * permute -> lookup -> (fill group g -> ffn group g, for every group) ->
+ * combine on one stream.  T >= prefill_min_tokens (> 0) takes the PREFILL
+ * path (experts walked in groups of prefill_group through the staging
+ * layout), otherwise DECODE.  The decode path never synchronises with the
+ * host and can be captured in a CUDA graph.
+ */
+typedef struct moe_layer moe_layer;
+
+typedef struct {
+  int H, I, E, k, Is;
+  const float* w_router;   /* device [E][H] fp32                          */
+  const float* bias;       /* device [E] fp32 or NULL                     */
+  const float* gscale;     /* device [E][3] fp32                          */
+  const void* s_gate;      /* device bf16 shared expert (NULL if Is == 0) */
+  const void* s_up;
+  const void* s_down;
+  expcache* cache;         /* weights of this layer: layer index `layer` */
+  int layer;
+  int T_max;
+  int prefill_min_tokens;  /* 0 = always DECODE                           */
+  int prefill_group;       /* experts per prefill group (e.g. 64)         */
+} moe_layer_desc;
+
+moe_status moe_layer_create(const moe_layer_desc* d, moe_layer** out);
+moe_status moe_layer_destroy(moe_layer* l);
+moe_status moe_layer_forward(moe_layer* l, const void* x, int T, void* y, void* stream);
+/* Device pointers (inside the layer's workspace) to the last forward's router
+ * outputs: ids [T][k] int32, w [T][k] fp32, p_sel [T][k] fp32; and the
+ * expert-sorted permutation perm [T*k] and lookup results src_slot [E],
+ * n_act [2]. */
+moe_status moe_layer_debug_ptrs(const moe_layer* l, const int32_t** ids, const float** w,
+                                const float** p_sel, const int32_t** perm,
+                                const int32_t** src_slot, const int32_t** n_act);
+/* Synchronises `stream`, returns the layer's sticky device status in
+ * *status_out and clears it. */
+moe_status moe_read_device_status(moe_layer* l, void* stream, int32_t* status_out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H */

@@ -1,0 +1,290 @@
+// api.cu - C-ABI entry points that tie the kernels together: status strings,
+// moe_expert_ffn dispatch and the moe_layer (route -> permute -> lookup ->
+// gather/FFN per expert group -> combine on one stream).
+#include <stdlib.h>
+#include <string.h>
+
+#include "common.cuh"
+
+namespace moe {
+const uint8_t* cache_arena(const expcache* c);
+int cache_n_cache(const expcache* c);
+int cache_n_stage(const expcache* c);
+int cache_E(const expcache* c);
+int cache_L(const expcache* c);
+int cache_H(const expcache* c);
+int cache_I(const expcache* c);
+size_t decode_workspace_bytes(int T, int I, int k, int Is);
+moe_status decode_ffn(const moe_ffn_args* a, cudaStream_t s);
+moe_status decode_setup();
+size_t prefill_workspace_bytes(int T, int H, int I, int E, int k, int Is);
+moe_status prefill_ffn(const moe_ffn_args* a, cudaStream_t s);
+moe_status prefill_setup();
+moe_status permute_setup();
+}  // namespace moe
+
+using namespace moe;
+
+MOE_API const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_OOM: return "MOE_ERR_OOM";
+    case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+    case MOE_ERR_DEVICE: return "MOE_ERR_DEVICE";
+    default: return "MOE_ERR_UNKNOWN";
+  }
+}
+
+MOE_API int moe_abi_version(void) { return 1; }
+
+static moe_status ensure_setup() {
+  static int done = 0;
+  if (done) return MOE_OK;
+  moe_status s = decode_setup();
+  if (s != MOE_OK) return s;
+  s = permute_setup();
+  if (s != MOE_OK) return s;
+  s = prefill_setup();
+  if (s != MOE_OK) return s;
+  done = 1;
+  return MOE_OK;
+}
+
+MOE_API size_t moe_ffn_workspace_bytes(int mode, int T, int H, int I, int E, int k, int Is) {
+  if (T < 0 || H <= 0 || I <= 0 || E <= 0 || k <= 0 || Is < 0) return 0;
+  if (mode == MOE_MODE_PREFILL) return prefill_workspace_bytes(T, H, I, E, k, Is);
+  return decode_workspace_bytes(T, I, k, Is);
+}
+
+MOE_API moe_status moe_expert_ffn(const moe_ffn_args* a, void* stream) {
+  if (!a || !a->cache || !a->gscale || !a->src_slot || !a->act_list || !a->n_act || !a->offsets ||
+      !a->perm || !a->w || !a->x)
+    return MOE_ERR_INVALID_ARG;
+  if (a->T < 0 || a->k <= 0 || a->k > a->E || a->group < 0 || a->n_stage < 0 || a->Is < 0)
+    return MOE_ERR_INVALID_ARG;
+  if (a->H != cache_H(a->cache) || a->I != cache_I(a->cache) || a->E != cache_E(a->cache))
+    return MOE_ERR_INVALID_ARG;
+  if (a->H % 256 || a->I % 128 || a->Is % 128 || a->H > 16384 || a->I > 16384 || a->Is > 16384)
+    return MOE_ERR_UNSUPPORTED;
+  if (a->Is > 0 && (!a->s_gate || !a->s_up || !a->s_down || !a->o_shared))
+    return MOE_ERR_INVALID_ARG;
+  if (a->T == 0) return MOE_OK;
+  if (!a->workspace ||
+      a->workspace_bytes < moe_ffn_workspace_bytes(a->mode, a->T, a->H, a->I, a->E, a->k, a->Is))
+    return MOE_ERR_INVALID_ARG;
+  moe_status st = ensure_setup();
+  if (st != MOE_OK) return st;
+  if (a->mode == MOE_MODE_DECODE) {
+    if (!a->o_route || a->stages < 1 || a->stages > 3) return MOE_ERR_INVALID_ARG;
+    return decode_ffn(a, (cudaStream_t)stream);
+  }
+  if (a->mode == MOE_MODE_PREFILL) {
+    if (!a->y_acc || !a->pad_offsets) return MOE_ERR_INVALID_ARG;
+    return prefill_ffn(a, (cudaStream_t)stream);
+  }
+  return MOE_ERR_INVALID_ARG;
+}
+
+// ------------------------------------------------------------------- layer
+struct moe_layer {
+  moe_layer_desc d;
+  void* ws;
+  size_t ws_bytes;
+  float* logits;
+  int32_t *ids, *counts, *offsets, *pad_offsets, *perm, *inv;
+  float *w, *p_sel;
+  int32_t *src_slot, *act_list, *n_act, *miss_ids, *n_miss, *status;
+  float *o_route, *o_shared, *y_acc;
+  void* ffn_ws;
+  size_t ffn_ws_bytes;
+  int last_T;
+};
+
+static size_t align256(size_t b) { return (b + 255) & ~(size_t)255; }
+
+MOE_API moe_status moe_layer_create(const moe_layer_desc* d, moe_layer** out) {
+  if (!d || !out || !d->cache || !d->w_router || !d->gscale) return MOE_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (d->T_max <= 0 || d->k <= 0 || d->k > d->E || d->k > 32 || d->Is < 0 || d->layer < 0 ||
+      d->layer >= cache_L(d->cache) || d->prefill_min_tokens < 0)
+    return MOE_ERR_INVALID_ARG;
+  if (d->H != cache_H(d->cache) || d->I != cache_I(d->cache) || d->E != cache_E(d->cache))
+    return MOE_ERR_INVALID_ARG;
+  if (d->Is > 0 && (!d->s_gate || !d->s_up || !d->s_down)) return MOE_ERR_INVALID_ARG;
+  if (d->H % 256 || d->I % 128 || d->Is % 128 || d->E > 1024) return MOE_ERR_UNSUPPORTED;
+  moe_status st = ensure_setup();
+  if (st != MOE_OK) return st;
+  moe_layer* l = (moe_layer*)calloc(1, sizeof(moe_layer));
+  if (!l) return MOE_ERR_OOM;
+  l->d = *d;
+  const int T = d->T_max, k = d->k, E = d->E, H = d->H;
+  const bool prefill = d->prefill_min_tokens > 0 && T >= d->prefill_min_tokens;
+  size_t ffn_dec = decode_workspace_bytes(T, d->I, k, d->Is);
+  size_t ffn_pre = prefill ? prefill_workspace_bytes(T, H, d->I, E, k, d->Is) : 0;
+  l->ffn_ws_bytes = ffn_dec > ffn_pre ? ffn_dec : ffn_pre;
+  size_t sizes[] = {
+      (size_t)T * E * 4,  /* logits */
+      (size_t)T * k * 4,  /* ids */
+      (size_t)T * k * 4,  /* w */
+      (size_t)T * k * 4,  /* p_sel */
+      (size_t)E * 4,      /* counts */
+      (size_t)(E + 1) * 4, /* offsets */
+      (size_t)(E + 1) * 4, /* pad_offsets */
+      (size_t)T * k * 4,  /* perm */
+      (size_t)T * k * 4,  /* inv */
+      (size_t)E * 4,      /* src_slot */
+      (size_t)E * 4,      /* act_list */
+      8,                  /* n_act */
+      (size_t)E * 4,      /* miss_ids */
+      4,                  /* n_miss */
+      4,                  /* status */
+      (size_t)T * k * H * 4, /* o_route */
+      (size_t)T * H * 4,  /* o_shared */
+      prefill ? (size_t)T * H * 4 : 0, /* y_acc */
+      l->ffn_ws_bytes};
+  const int n = (int)(sizeof(sizes) / sizeof(sizes[0]));
+  size_t total = 0;
+  for (int i = 0; i < n; ++i) total += align256(sizes[i]);
+  if (cudaMalloc(&l->ws, total) != cudaSuccess) {
+    cudaGetLastError();
+    free(l);
+    return MOE_ERR_OOM;
+  }
+  l->ws_bytes = total;
+  uint8_t* p = (uint8_t*)l->ws;
+  void* ptrs[19];
+  for (int i = 0; i < n; ++i) {
+    ptrs[i] = sizes[i] ? p : nullptr;
+    p += align256(sizes[i]);
+  }
+  l->logits = (float*)ptrs[0];
+  l->ids = (int32_t*)ptrs[1];
+  l->w = (float*)ptrs[2];
+  l->p_sel = (float*)ptrs[3];
+  l->counts = (int32_t*)ptrs[4];
+  l->offsets = (int32_t*)ptrs[5];
+  l->pad_offsets = (int32_t*)ptrs[6];
+  l->perm = (int32_t*)ptrs[7];
+  l->inv = (int32_t*)ptrs[8];
+  l->src_slot = (int32_t*)ptrs[9];
+  l->act_list = (int32_t*)ptrs[10];
+  l->n_act = (int32_t*)ptrs[11];
+  l->miss_ids = (int32_t*)ptrs[12];
+  l->n_miss = (int32_t*)ptrs[13];
+  l->status = (int32_t*)ptrs[14];
+  l->o_route = (float*)ptrs[15];
+  l->o_shared = (float*)ptrs[16];
+  l->y_acc = (float*)ptrs[17];
+  l->ffn_ws = ptrs[18];
+  if (cudaMemset(l->status, 0, 4) != cudaSuccess) {
+    cudaFree(l->ws);
+    free(l);
+    return MOE_ERR_CUDA;
+  }
+  *out = l;
+  return MOE_OK;
+}
+
+MOE_API moe_status moe_layer_destroy(moe_layer* l) {
+  if (!l) return MOE_ERR_INVALID_ARG;
+  cudaDeviceSynchronize();
+  cudaFree(l->ws);
+  free(l);
+  return MOE_OK;
+}
+
+MOE_API moe_status moe_layer_forward(moe_layer* l, const void* x, int T, void* y, void* stream) {
+  if (!l || !x || !y || T < 0 || T > l->d.T_max) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  const moe_layer_desc& d = l->d;
+  cudaStream_t s = (cudaStream_t)stream;
+  const bool prefill = d.prefill_min_tokens > 0 && T >= d.prefill_min_tokens;
+  moe_status st;
+
+  moe_route_args ra;
+  memset(&ra, 0, sizeof(ra));
+  ra.x = x; ra.w_router = d.w_router; ra.bias = d.bias;
+  ra.T = T; ra.H = d.H; ra.E = d.E; ra.k = d.k;
+  ra.ids = l->ids; ra.w = l->w; ra.p_sel = l->p_sel; ra.logits = l->logits;
+  ra.status = l->status;
+  if ((st = moe_route(&ra, stream)) != MOE_OK) return st;
+
+  if ((st = moe_permute(l->ids, T, d.k, d.E, l->counts, l->offsets, l->perm, l->inv,
+                        prefill ? l->pad_offsets : nullptr, 128, l->status, stream)) != MOE_OK)
+    return st;
+  if ((st = expcache_lookup(d.cache, d.layer, l->counts, l->src_slot, l->act_list, l->n_act,
+                            l->miss_ids, l->n_miss, l->status, stream)) != MOE_OK)
+    return st;
+
+  const int n_stage = cache_n_stage(d.cache);
+  const int max_miss = T * d.k < d.E ? T * d.k : d.E;
+  const int S = n_stage > 0 ? n_stage : 1;
+  const int groups = n_stage > 0 ? (max_miss + S - 1) / S : 1;
+
+  moe_ffn_args fa;
+  memset(&fa, 0, sizeof(fa));
+  fa.mode = prefill ? MOE_MODE_PREFILL : MOE_MODE_DECODE;
+  fa.stages = MOE_STAGE_ALL;
+  fa.T = T; fa.H = d.H; fa.I = d.I; fa.E = d.E; fa.k = d.k;
+  fa.x = x; fa.cache = d.cache; fa.gscale = d.gscale;
+  fa.src_slot = l->src_slot; fa.act_list = l->act_list; fa.n_act = l->n_act;
+  fa.offsets = l->offsets; fa.pad_offsets = l->pad_offsets; fa.perm = l->perm; fa.w = l->w;
+  fa.n_stage = n_stage;
+  fa.Is = d.Is; fa.s_gate = d.s_gate; fa.s_up = d.s_up; fa.s_down = d.s_down;
+  fa.o_route = l->o_route; fa.o_shared = d.Is > 0 ? l->o_shared : nullptr;
+  fa.y_acc = l->y_acc;
+  fa.workspace = l->ffn_ws; fa.workspace_bytes = l->ffn_ws_bytes;
+  fa.status = l->status;
+  if (prefill && cudaMemsetAsync(l->y_acc, 0, (size_t)T * d.H * 4, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  for (int g = 0; g < groups; ++g) {
+    if (n_stage > 0) {
+      int cnt = S < max_miss - g * S ? S : max_miss - g * S;
+      if ((st = expcache_fill(d.cache, d.layer, l->miss_ids, l->n_miss, g * S, cnt, nullptr,
+                              l->status, stream)) != MOE_OK)
+        return st;
+    }
+    fa.group = g;
+    if ((st = moe_expert_ffn(&fa, stream)) != MOE_OK) return st;
+  }
+
+  moe_combine_args ca;
+  memset(&ca, 0, sizeof(ca));
+  ca.T = T; ca.H = d.H; ca.k = d.k;
+  ca.y_acc = prefill ? l->y_acc : nullptr;
+  ca.o_route = prefill ? nullptr : l->o_route;
+  ca.inv = l->inv;
+  ca.o_shared = d.Is > 0 ? l->o_shared : nullptr;
+  ca.y = y;
+  if ((st = moe_combine(&ca, stream)) != MOE_OK) return st;
+  l->last_T = T;
+  return MOE_OK;
+}
+
+MOE_API moe_status moe_layer_debug_ptrs(const moe_layer* l, const int32_t** ids, const float** w,
+                                        const float** p_sel, const int32_t** perm,
+                                        const int32_t** src_slot, const int32_t** n_act) {
+  if (!l) return MOE_ERR_INVALID_ARG;
+  if (ids) *ids = l->ids;
+  if (w) *w = l->w;
+  if (p_sel) *p_sel = l->p_sel;
+  if (perm) *perm = l->perm;
+  if (src_slot) *src_slot = l->src_slot;
+  if (n_act) *n_act = l->n_act;
+  return MOE_OK;
+}
+
+MOE_API moe_status moe_read_device_status(moe_layer* l, void* stream, int32_t* status_out) {
+  if (!l || !status_out) return MOE_ERR_INVALID_ARG;
+  int32_t v = 0;
+  if (cudaMemcpyAsync(&v, l->status, 4, cudaMemcpyDeviceToHost, (cudaStream_t)stream) !=
+          cudaSuccess ||
+      cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  *status_out = v;
+  if (cudaMemsetAsync(l->status, 0, 4, (cudaStream_t)stream) != cudaSuccess) return MOE_ERR_CUDA;
+  return MOE_OK;
+}

@@ -1,0 +1,231 @@
+// cache.cu - the per-layer HBM hot-expert cache and K-gather.
+//
+// Slot arena: n_cache slots followed by n_stage staging slots, one fixed-stride
+// record each ("Project Maya": a device table layer x expert -> VRAM slot, each
+// layer owning its own run of slots so no slot is overwritten while another
+// layer reads it; Strata-GLM blog: exclusive tiers, byte-sized slots).
+// K-gather copies records of missing experts from the pinned, mapped host
+// arena with 16-byte loads issued by many thread blocks at once (the "Project
+// Maya" GPU pull of RAM-tier experts; the dev.to page's wide-read gather over a
+// GPU-resident list, which keeps CUDA graphs replayable).
+#include <stdlib.h>
+#include <string.h>
+
+#include "common.cuh"
+
+struct expcache {
+  int L, E, H, I;
+  int n_cache, n_stage;
+  uint64_t rec_bytes;
+  uint8_t* arena;            // device, (n_cache + n_stage) * rec_bytes
+  int32_t* table;            // device [L][E]
+  int32_t* slot_lo;          // host [L]: layer l owns cache slots [slot_lo[l], slot_hi[l])
+  int32_t* slot_hi;
+  const uint8_t* host_dev;   // device-side address of the host arena (or NULL)
+  uint64_t host_records;
+  int64_t* host_index_dev;   // device [L][E] (or NULL)
+};
+
+namespace moe {
+
+constexpr int kGatherThreads = 256;
+constexpr int kGatherUnroll = 8;                       // 16-byte loads in flight per thread
+constexpr uint64_t kGatherChunk = (uint64_t)kGatherThreads * kGatherUnroll * 16 * 4;  // 128 KiB
+
+__global__ void __launch_bounds__(kGatherThreads) k_gather(
+    const uint8_t* __restrict__ host, const int64_t* __restrict__ host_index, uint64_t host_records,
+    uint8_t* __restrict__ arena, int32_t* __restrict__ table_row, int E, uint64_t rec_bytes,
+    int n_cache, int n_stage, const int32_t* __restrict__ ids, const int32_t* __restrict__ d_n,
+    int first, const int32_t* __restrict__ dst_slots, int slot_lo, int slot_hi, int32_t* status) {
+  const int i = first + blockIdx.y;
+  if (i >= *d_n) return;
+  const int e = ids[i];
+  if (e < 0 || e >= E) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) set_status(status, MOE_ERR_DEVICE);
+    return;
+  }
+  const int64_t hr = host_index ? host_index[e] : -1;
+  int slot;
+  if (dst_slots) {
+    slot = dst_slots[i];
+    if (slot < slot_lo || slot >= slot_hi) slot = -1;
+  } else {
+    slot = n_stage > 0 ? n_cache + (i % n_stage) : -1;
+  }
+  if (hr < 0 || (uint64_t)hr >= host_records || !host || slot < 0) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) set_status(status, MOE_ERR_DEVICE);
+    return;
+  }
+  const uint8_t* src = host + (uint64_t)hr * rec_bytes;
+  uint8_t* dst = arena + (uint64_t)slot * rec_bytes;
+  const uint64_t n16 = rec_bytes / 16;
+  // grid-stride over 16-byte words of this record, kGatherUnroll loads in flight
+  const uint64_t stride = (uint64_t)gridDim.x * kGatherThreads;
+  uint64_t w = (uint64_t)blockIdx.x * kGatherThreads + threadIdx.x;
+  const uint4* s4 = reinterpret_cast<const uint4*>(src);
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+  for (; w + (kGatherUnroll - 1) * stride < n16; w += kGatherUnroll * stride) {
+    uint4 v[kGatherUnroll];
+#pragma unroll
+    for (int u = 0; u < kGatherUnroll; ++u) v[u] = ldg_stream(s4 + w + u * stride);
+#pragma unroll
+    for (int u = 0; u < kGatherUnroll; ++u) d4[w + u * stride] = v[u];
+  }
+  for (; w < n16; w += stride) d4[w] = ldg_stream(s4 + w);
+  if (dst_slots && blockIdx.x == 0 && threadIdx.x == 0) table_row[e] = slot;
+}
+
+__global__ void k_set_table(int32_t* table_entry, int slot) { *table_entry = slot; }
+
+moe_status launch_lookup(const int32_t* table_row, int E, const int32_t* counts, int slot_lo,
+                         int slot_hi, int n_cache, int n_stage, int32_t* src_slot,
+                         int32_t* act_list, int32_t* n_act, int32_t* miss_ids, int32_t* n_miss,
+                         int32_t* status, cudaStream_t s);
+
+}  // namespace moe
+
+using namespace moe;
+
+MOE_API uint64_t moe_record_bytes(int H, int I) {
+  if (H <= 0 || I <= 0) return 0;
+  return RecordLayout(H, I).bytes;
+}
+
+MOE_API moe_status expcache_create(const expcache_desc* d, expcache** out) {
+  if (!d || !out) return MOE_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (d->L <= 0 || d->E <= 0 || d->H <= 0 || d->I <= 0 || d->n_cache_slots < 0 || d->n_stage < 0)
+    return MOE_ERR_INVALID_ARG;
+  if (d->H % 256 || d->I % 128 || d->E > 1024) return MOE_ERR_UNSUPPORTED;
+  if (d->host_arena && !d->host_index) return MOE_ERR_INVALID_ARG;
+  if (d->layer_slots) {
+    if (d->layer_slots[0] < 0) return MOE_ERR_INVALID_ARG;
+    for (int l = 0; l < d->L; ++l)
+      if (d->layer_slots[l + 1] < d->layer_slots[l]) return MOE_ERR_INVALID_ARG;
+    if (d->layer_slots[d->L] > d->n_cache_slots) return MOE_ERR_INVALID_ARG;
+  }
+  expcache* c = (expcache*)calloc(1, sizeof(expcache));
+  if (!c) return MOE_ERR_OOM;
+  c->L = d->L; c->E = d->E; c->H = d->H; c->I = d->I;
+  c->n_cache = d->n_cache_slots; c->n_stage = d->n_stage;
+  c->rec_bytes = RecordLayout(d->H, d->I).bytes;
+  c->slot_lo = (int32_t*)malloc(sizeof(int32_t) * d->L);
+  c->slot_hi = (int32_t*)malloc(sizeof(int32_t) * d->L);
+  if (!c->slot_lo || !c->slot_hi) {
+    free(c->slot_lo); free(c->slot_hi); free(c);
+    return MOE_ERR_OOM;
+  }
+  for (int l = 0; l < d->L; ++l) {
+    c->slot_lo[l] = d->layer_slots ? d->layer_slots[l] : 0;
+    c->slot_hi[l] = d->layer_slots ? d->layer_slots[l + 1] : d->n_cache_slots;
+  }
+  uint64_t slots = (uint64_t)d->n_cache_slots + (uint64_t)d->n_stage;
+  moe_status st = MOE_OK;
+  if (slots && cudaMalloc((void**)&c->arena, slots * c->rec_bytes) != cudaSuccess) st = MOE_ERR_OOM;
+  if (st == MOE_OK &&
+      cudaMalloc((void**)&c->table, sizeof(int32_t) * (size_t)d->L * d->E) != cudaSuccess)
+    st = MOE_ERR_OOM;
+  if (st == MOE_OK && cudaMemset(c->table, 0xFF, sizeof(int32_t) * (size_t)d->L * d->E) != cudaSuccess)
+    st = MOE_ERR_CUDA;
+  if (st == MOE_OK && d->host_arena) {
+    void* dp = nullptr;
+    if (cudaHostGetDevicePointer(&dp, (void*)d->host_arena, 0) != cudaSuccess) st = MOE_ERR_CUDA;
+    c->host_dev = (const uint8_t*)dp;
+    c->host_records = d->host_arena_records;
+    if (st == MOE_OK &&
+        cudaMalloc((void**)&c->host_index_dev, sizeof(int64_t) * (size_t)d->L * d->E) != cudaSuccess)
+      st = MOE_ERR_OOM;
+    if (st == MOE_OK && cudaMemcpy(c->host_index_dev, d->host_index,
+                                   sizeof(int64_t) * (size_t)d->L * d->E,
+                                   cudaMemcpyHostToDevice) != cudaSuccess)
+      st = MOE_ERR_CUDA;
+  }
+  if (st != MOE_OK) {
+    cudaGetLastError();
+    expcache_destroy(c);
+    return st;
+  }
+  *out = c;
+  return MOE_OK;
+}
+
+MOE_API moe_status expcache_destroy(expcache* c) {
+  if (!c) return MOE_ERR_INVALID_ARG;
+  cudaDeviceSynchronize();
+  if (c->arena) cudaFree(c->arena);
+  if (c->table) cudaFree(c->table);
+  if (c->host_index_dev) cudaFree(c->host_index_dev);
+  free(c->slot_lo);
+  free(c->slot_hi);
+  free(c);
+  return MOE_OK;
+}
+
+MOE_API void* expcache_slot_ptr(const expcache* c, int s) {
+  if (!c || s < 0 || s >= c->n_cache + c->n_stage) return nullptr;
+  return c->arena + (uint64_t)s * c->rec_bytes;
+}
+
+MOE_API const int32_t* expcache_slot_table(const expcache* c) { return c ? c->table : nullptr; }
+
+MOE_API moe_status expcache_set_resident(expcache* c, int layer, int expert, int slot,
+                                         void* stream) {
+  if (!c || layer < 0 || layer >= c->L || expert < 0 || expert >= c->E) return MOE_ERR_INVALID_ARG;
+  if (slot != -1 && (slot < c->slot_lo[layer] || slot >= c->slot_hi[layer]))
+    return MOE_ERR_INVALID_ARG;
+  k_set_table<<<1, 1, 0, (cudaStream_t)stream>>>(c->table + (size_t)layer * c->E + expert, slot);
+  MOE_CHECK_LAUNCH();
+  return MOE_OK;
+}
+
+namespace moe {
+// grid width for one record: enough blocks to keep the link busy
+static int gather_blocks_per_record(uint64_t rec_bytes, int max_count) {
+  uint64_t chunks = (rec_bytes + kGatherChunk - 1) / kGatherChunk;
+  int want = (int)((2 * kSMs + max_count - 1) / max_count);  // ~2 blocks per SM overall
+  if (want < 1) want = 1;
+  return (int)(chunks < (uint64_t)want ? chunks : (uint64_t)want);
+}
+}  // namespace moe
+
+MOE_API moe_status expcache_fill(expcache* c, int layer, const int32_t* d_expert_ids,
+                                 const int32_t* d_n, int first, int max_count,
+                                 const int32_t* d_dst_slots, int32_t* status, void* stream) {
+  if (!c || !d_expert_ids || !d_n || layer < 0 || layer >= c->L || first < 0 || max_count < 0)
+    return MOE_ERR_INVALID_ARG;
+  if (max_count == 0) return MOE_OK;
+  if (!d_dst_slots && c->n_stage == 0) return MOE_ERR_INVALID_ARG;
+  if (max_count > 65535) return MOE_ERR_UNSUPPORTED;
+  dim3 grid(gather_blocks_per_record(c->rec_bytes, max_count), max_count);
+  k_gather<<<grid, kGatherThreads, 0, (cudaStream_t)stream>>>(
+      c->host_dev, c->host_index_dev ? c->host_index_dev + (size_t)layer * c->E : nullptr,
+      c->host_records, c->arena, c->table + (size_t)layer * c->E, c->E, c->rec_bytes, c->n_cache,
+      c->n_stage, d_expert_ids, d_n, first, d_dst_slots, c->slot_lo[layer], c->slot_hi[layer],
+      status);
+  MOE_CHECK_LAUNCH();
+  return MOE_OK;
+}
+
+MOE_API moe_status expcache_lookup(const expcache* c, int layer, const int32_t* counts,
+                                   int32_t* src_slot, int32_t* act_list, int32_t* n_act,
+                                   int32_t* miss_ids, int32_t* n_miss, int32_t* status,
+                                   void* stream) {
+  if (!c || !counts || !src_slot || !act_list || !n_act || !miss_ids || !n_miss || layer < 0 ||
+      layer >= c->L)
+    return MOE_ERR_INVALID_ARG;
+  return launch_lookup(c->table + (size_t)layer * c->E, c->E, counts, c->slot_lo[layer],
+                       c->slot_hi[layer], c->n_cache, c->n_stage, src_slot, act_list,
+                       n_act, miss_ids, n_miss, status, (cudaStream_t)stream);
+}
+
+// internal accessors for the FFN and the layer
+namespace moe {
+const uint8_t* cache_arena(const expcache* c) { return c->arena; }
+uint64_t cache_rec_bytes(const expcache* c) { return c->rec_bytes; }
+int cache_n_cache(const expcache* c) { return c->n_cache; }
+int cache_n_stage(const expcache* c) { return c->n_stage; }
+int cache_E(const expcache* c) { return c->E; }
+int cache_L(const expcache* c) { return c->L; }
+int cache_H(const expcache* c) { return c->H; }
+int cache_I(const expcache* c) { return c->I; }
+}  // namespace moe

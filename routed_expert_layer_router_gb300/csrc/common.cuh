@@ -1,0 +1,106 @@
+// common.cuh - small device helpers shared by the library's kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe.h"
+
+#define MOE_API extern "C" __attribute__((visibility("default")))
+
+namespace moe {
+
+constexpr int kSMs = 152;  // GB300: 2 dies x 76 SMs
+
+// ---- sticky device status: first error wins --------------------------------
+__device__ __forceinline__ void set_status(int32_t* st, int32_t code) {
+  if (st) atomicCAS(st, 0, code);
+}
+
+// ---- record layout (see moe.h) ---------------------------------------------
+struct RecordLayout {
+  uint64_t gate_codes, up_codes, down_codes;
+  uint64_t gate_scales, up_scales, down_scales;
+  uint64_t bytes;
+  __host__ __device__ RecordLayout(int H, int I) {
+    uint64_t gu = (uint64_t)I * H / 2;
+    gate_codes = 0;
+    up_codes = gu;
+    down_codes = 2 * gu;
+    uint64_t sgu = (uint64_t)I * H / 16;
+    gate_scales = 3 * gu;
+    up_scales = gate_scales + sgu;
+    down_scales = up_scales + sgu;
+    bytes = down_scales + sgu;
+  }
+};
+
+// byte offset of the 512-byte atom (row tile rt = r/128, k group kg = kb/4)
+__host__ __device__ __forceinline__ uint64_t atom_offset(int rt, int kg, int KB) {
+  return ((uint64_t)rt * (uint64_t)(KB / 4) + (uint64_t)kg) * 512u;
+}
+
+// ---- numeric helpers --------------------------------------------------------
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+__device__ __forceinline__ uint16_t f32_to_bf16_rne(float f) {
+  uint32_t u = __float_as_uint(f);
+  u += 0x7FFFu + ((u >> 16) & 1u);
+  return (uint16_t)(u >> 16);
+}
+
+// two E2M1 codes (one byte, element 2j in the low nibble) -> two floats
+__device__ __forceinline__ void e2m1x4_to_f16x2x2(uint32_t w16, uint32_t& lo, uint32_t& hi) {
+  // w16: bits 0..15 hold two bytes = four codes
+  asm("{\n .reg .b8 a, b, c, d;\n mov.b32 {a, b, c, d}, %2;\n"
+      " cvt.rn.f16x2.e2m1x2 %0, a;\n cvt.rn.f16x2.e2m1x2 %1, b;\n}"
+      : "=r"(lo), "=r"(hi) : "r"(w16));
+}
+
+__device__ __forceinline__ void e2m1x8_to_f16x2x4(uint32_t w, uint32_t h[4]) {
+  asm("{\n .reg .b8 a, b, c, d;\n mov.b32 {a, b, c, d}, %4;\n"
+      " cvt.rn.f16x2.e2m1x2 %0, a;\n cvt.rn.f16x2.e2m1x2 %1, b;\n"
+      " cvt.rn.f16x2.e2m1x2 %2, c;\n cvt.rn.f16x2.e2m1x2 %3, d;\n}"
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3]) : "r"(w));
+}
+
+// two E4M3 bytes (bits 0..15) -> f16x2 (exact)
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t w16) {
+  uint32_t r;
+  asm("{\n .reg .b16 a;\n cvt.u16.u32 a, %1;\n cvt.rn.f16x2.e4m3x2 %0, a;\n}" : "=r"(r) : "r"(w16));
+  return r;
+}
+
+__device__ __forceinline__ float f16_lo(uint32_t h2) {
+  float f;
+  asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %1;\n cvt.f32.f16 %0, l;\n}" : "=f"(f) : "r"(h2));
+  return f;
+}
+__device__ __forceinline__ float f16_hi(uint32_t h2) {
+  float f;
+  asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %1;\n cvt.f32.f16 %0, h;\n}" : "=f"(f) : "r"(h2));
+  return f;
+}
+
+// streaming 128-bit load that does not allocate in L1
+__device__ __forceinline__ uint4 ldg_stream(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  return v;
+}
+
+}  // namespace moe
+
+// host-side error plumbing
+#define MOE_CHECK_LAUNCH()                                          \
+  do {                                                              \
+    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;     \
+  } while (0)

@@ -1,0 +1,529 @@
+// decode.cu - K-decode-gu, K-decode-down and K-combine: the expert FFN for few
+// tokens per expert, HBM-bound.  Weights stream from their cache or staging
+// slot with 128-bit loads; the NVFP4 dequant (E2M1 code x E4M3 block scale x
+// fp32 global) happens in registers and feeds fp32 FMAs on the bf16
+// activations.  Work is cut so that one warp owns 4 gate rows + 4 up rows (or
+// 4 down rows) that share one 16-byte row of every 512-byte scale atom, and
+// every activation value a lane loads from shared memory is reused across the
+// warp's rows.  Sources: "Project Maya" page, section "A V100 has no BF16 and
+// no FP8" (decode is a matrix-vector product where the bytes, not the
+// arithmetic, set the speed); dev.to page, section "The wall" (NVFP4 experts).
+#include "common.cuh"
+
+namespace moe {
+
+const uint8_t* cache_arena(const expcache* c);
+uint64_t cache_rec_bytes(const expcache* c);
+int cache_n_cache(const expcache* c);
+int cache_n_stage(const expcache* c);
+
+constexpr int kDecWarps = 8;
+constexpr int kDecThreads = kDecWarps * 32;
+constexpr int kXPad = 36;  // floats per 32-element half-k-group in shared memory (bank spread)
+
+struct DecodeParams {
+  int T, H, I, E, k, Is;
+  const uint16_t* x;
+  const uint8_t* arena;
+  uint64_t rec_bytes;
+  int n_slots;      // cache + staging slots in the arena
+  const float* gscale;
+  const int32_t* src_slot;
+  const int32_t* act_list;
+  const int32_t* n_act;
+  const int32_t* offsets;
+  const int32_t* perm;
+  const float* w;
+  int group, n_stage;
+  int n_routed_units;  // grid units reserved for routed experts
+  const uint16_t* s_gate;
+  const uint16_t* s_up;
+  const uint16_t* s_down;
+  float* h_route;   // [T*k][I]
+  float* h_shared;  // [T][Is]
+  float* o_route;   // [T*k][H]
+  float* o_shared;  // [T][H]
+  int32_t* status;
+  int maxm;         // tokens staged per pass (1 or 2)
+};
+
+// act_list index range of this group
+__device__ __forceinline__ void group_range(const DecodeParams& p, int& a0, int& a1) {
+  const int n_act = p.n_act[0], n_hit = p.n_act[1], n_miss = n_act - n_hit;
+  const int S = p.n_stage > 0 ? p.n_stage : (n_miss > 0 ? n_miss : 1);
+  if (p.group == 0) {
+    a0 = 0;
+    a1 = n_hit + min(S, n_miss);
+  } else {
+    a0 = n_hit + p.group * S;
+    a1 = n_hit + min((p.group + 1) * S, n_miss);
+  }
+}
+
+// stage `m` vectors (bf16 rows or fp32 rows) into padded fp32 shared memory
+__device__ __forceinline__ void stage_bf16_rows(float* xs, const uint16_t* const* rows, int m,
+                                                int K) {
+  const int nhk = K / 32;
+  for (int j = 0; j < m; ++j) {
+    const uint32_t* src = reinterpret_cast<const uint32_t*>(rows[j]);
+    float* dst = xs + (size_t)j * nhk * kXPad;
+    for (int i = threadIdx.x; i < K / 2; i += blockDim.x) {
+      uint32_t v = __ldg(src + i);
+      int e = 2 * i;
+      dst[(e >> 5) * kXPad + (e & 31)] = bf16_lo(v);
+      dst[(e >> 5) * kXPad + (e & 31) + 1] = bf16_hi(v);
+    }
+  }
+}
+
+__device__ __forceinline__ void stage_f32_rows(float* xs, const float* const* rows, int m, int K) {
+  const int nhk = K / 32;
+  for (int j = 0; j < m; ++j) {
+    const float4* src = reinterpret_cast<const float4*>(rows[j]);
+    float* dst = xs + (size_t)j * nhk * kXPad;
+    for (int i = threadIdx.x; i < K / 4; i += blockDim.x) {
+      float4 v = src[i];
+      int e = 4 * i;
+      *reinterpret_cast<float4*>(dst + (e >> 5) * kXPad + (e & 31)) = v;
+    }
+  }
+}
+
+// 32 E2M1 codes (16 bytes) of one row against M staged vectors.
+// blocks: codes 0..15 use scale s0, 16..31 use s1.  acc[j] += s0*sum0 + s1*sum1.
+template <int M>
+__device__ __forceinline__ void fp4_dot32(const uint4& c, float s0, float s1, const float* xv,
+                                          float* acc) {
+  const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
+  float p0[M], p1[M];
+#pragma unroll
+  for (int j = 0; j < M; ++j) p0[j] = p1[j] = 0.f;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint32_t h[4];
+    e2m1x8_to_f16x2x4(cw[q], h);
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      float v0 = f16_lo(h[b]), v1 = f16_hi(h[b]);
+      const int e = q * 8 + b * 2;
+#pragma unroll
+      for (int j = 0; j < M; ++j) {
+        if (q < 2) {
+          p0[j] = fmaf(v0, xv[j * 32 + e], p0[j]);
+          p0[j] = fmaf(v1, xv[j * 32 + e + 1], p0[j]);
+        } else {
+          p1[j] = fmaf(v0, xv[j * 32 + e], p1[j]);
+          p1[j] = fmaf(v1, xv[j * 32 + e + 1], p1[j]);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < M; ++j) acc[j] = fmaf(s1, p1[j], fmaf(s0, p0[j], acc[j]));
+}
+
+// the two E4M3 scales (bytes 2*half, 2*half+1 of 4-byte word m1 of an atom row)
+__device__ __forceinline__ void scales_of(const uint4& a, int m1, int half, float& s0, float& s1) {
+  uint32_t wd = (m1 == 0) ? a.x : (m1 == 1) ? a.y : (m1 == 2) ? a.z : a.w;
+  uint32_t h2 = e4m3x2_to_f16x2((wd >> (16 * half)) & 0xFFFFu);
+  s0 = f16_lo(h2);
+  s1 = f16_hi(h2);
+}
+
+// gate+up for the 4 rows {rt*128 + m0 + 32*m1} of one expert, M staged tokens
+template <int M>
+__device__ void warp_gu_fp4(const uint8_t* rec, const RecordLayout& L, int H, int rt, int m0,
+                            const float* xs, float accg[4][M], float accu[4][M]) {
+  const int lane = threadIdx.x & 31;
+  const int KB = H / 16, nhk = H / 32;
+  const uint8_t* gc = rec + L.gate_codes;
+  const uint8_t* uc = rec + L.up_codes;
+#pragma unroll
+  for (int m1 = 0; m1 < 4; ++m1)
+#pragma unroll
+    for (int j = 0; j < M; ++j) accg[m1][j] = accu[m1][j] = 0.f;
+  for (int hk = lane; hk < nhk; hk += 32) {
+    const int kg = hk >> 1, half = hk & 1;
+    const uint64_t aoff = atom_offset(rt, kg, KB) + (uint64_t)m0 * 16;
+    uint4 sg = ldg_stream(rec + L.gate_scales + aoff);
+    uint4 su = ldg_stream(rec + L.up_scales + aoff);
+    uint4 cg[4], cu[4];
+#pragma unroll
+    for (int m1 = 0; m1 < 4; ++m1) {
+      const uint64_t roff = (uint64_t)(rt * 128 + m0 + 32 * m1) * (H / 2) + (uint64_t)hk * 16;
+      cg[m1] = ldg_stream(gc + roff);
+      cu[m1] = ldg_stream(uc + roff);
+    }
+    float xv[M * 32];
+#pragma unroll
+    for (int j = 0; j < M; ++j)
+#pragma unroll
+      for (int i = 0; i < 32; i += 4)
+        *reinterpret_cast<float4*>(xv + j * 32 + i) =
+            *reinterpret_cast<const float4*>(xs + ((size_t)j * nhk + hk) * kXPad + i);
+#pragma unroll
+    for (int m1 = 0; m1 < 4; ++m1) {
+      float s0, s1;
+      scales_of(sg, m1, half, s0, s1);
+      fp4_dot32<M>(cg[m1], s0, s1, xv, accg[m1]);
+      scales_of(su, m1, half, s0, s1);
+      fp4_dot32<M>(cu[m1], s0, s1, xv, accu[m1]);
+    }
+  }
+#pragma unroll
+  for (int m1 = 0; m1 < 4; ++m1)
+#pragma unroll
+    for (int j = 0; j < M; ++j) {
+      accg[m1][j] = warp_sum(accg[m1][j]);
+      accu[m1][j] = warp_sum(accu[m1][j]);
+    }
+}
+
+// 8 bf16 weights (16 bytes) against M staged vectors (8 consecutive values)
+template <int M>
+__device__ __forceinline__ void bf16_dot8(const uint4& c, const float* xv, float* acc) {
+  const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+#pragma unroll
+    for (int j = 0; j < M; ++j) {
+      acc[j] = fmaf(bf16_lo(cw[q]), xv[j * 8 + 2 * q], acc[j]);
+      acc[j] = fmaf(bf16_hi(cw[q]), xv[j * 8 + 2 * q + 1], acc[j]);
+    }
+}
+
+// bf16 matrix rows r[0..3] (row length K) against M staged vectors
+template <int M, int NR>
+__device__ void warp_rows_bf16(const uint16_t* const* rows, int K, const float* xs,
+                               float acc[NR][M]) {
+  const int lane = threadIdx.x & 31;
+  const int nhk = K / 32;
+#pragma unroll
+  for (int r = 0; r < NR; ++r)
+#pragma unroll
+    for (int j = 0; j < M; ++j) acc[r][j] = 0.f;
+  for (int i0 = lane * 8; i0 < K; i0 += 256) {
+    uint4 c[NR];
+#pragma unroll
+    for (int r = 0; r < NR; ++r) c[r] = ldg_stream(rows[r] + i0);
+    float xv[M * 8];
+#pragma unroll
+    for (int j = 0; j < M; ++j) {
+      const float* src = xs + ((size_t)j * nhk + (i0 >> 5)) * kXPad + (i0 & 31);
+      *reinterpret_cast<float4*>(xv + j * 8) = *reinterpret_cast<const float4*>(src);
+      *reinterpret_cast<float4*>(xv + j * 8 + 4) = *reinterpret_cast<const float4*>(src + 4);
+    }
+#pragma unroll
+    for (int r = 0; r < NR; ++r) bf16_dot8<M>(c[r], xv, acc[r]);
+  }
+#pragma unroll
+  for (int r = 0; r < NR; ++r)
+#pragma unroll
+    for (int j = 0; j < M; ++j) acc[r][j] = warp_sum(acc[r][j]);
+}
+
+__device__ __forceinline__ float silu_f(float g) { return g / (1.f + expf(-g)); }
+
+// ---- K-decode-gu -------------------------------------------------------------
+template <int M>
+__device__ void gu_routed_pass(const DecodeParams& p, const RecordLayout& L, const uint8_t* rec,
+                               int rt, int m0, int p0, int mm, const float* xs, float gg,
+                               float gu) {
+  float accg[4][M], accu[4][M];
+  warp_gu_fp4<M>(rec, L, p.H, rt, m0, xs, accg, accu);
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int m1 = 0; m1 < 4; ++m1)
+#pragma unroll
+    for (int j = 0; j < M; ++j)
+      if (lane == m1 * M + j && j < mm) {
+        float g = accg[m1][j] * gg, u = accu[m1][j] * gu;
+        p.h_route[(size_t)(p0 + j) * p.I + rt * 128 + m0 + 32 * m1] = silu_f(g) * u;
+      }
+}
+
+template <int M>
+__device__ void gu_shared_pass(const DecodeParams& p, int i0, int t0, int mm, const float* xs) {
+  const uint16_t* rows[8];
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    rows[r] = p.s_gate + (size_t)(i0 + r) * p.H;
+    rows[4 + r] = p.s_up + (size_t)(i0 + r) * p.H;
+  }
+  float acc[8][M];
+  warp_rows_bf16<M, 8>(rows, p.H, xs, acc);
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int j = 0; j < M; ++j)
+      if (lane == r * M + j && j < mm)
+        p.h_shared[(size_t)(t0 + j) * p.Is + i0 + r] = silu_f(acc[r][j]) * acc[4 + r][j];
+}
+
+__global__ void __launch_bounds__(kDecThreads) k_decode_gu(DecodeParams p) {
+  extern __shared__ float xs[];
+  const int wid = threadIdx.x >> 5;
+  const int u = blockIdx.x;
+  if (u < p.n_routed_units) {
+    const int tiles = p.I / 128;
+    const int a = u / (tiles * 4), rem = u % (tiles * 4);
+    const int rt = rem >> 2, m0 = (rem & 3) * kDecWarps + wid;
+    int a0, a1;
+    group_range(p, a0, a1);
+    if (a0 + a < a0 || a0 + a >= a1) return;
+    const int e = p.act_list[a0 + a];
+    const int slot = (e >= 0 && e < p.E) ? p.src_slot[e] : -1;
+    if (slot < 0 || slot >= p.n_slots) {
+      if (threadIdx.x == 0) set_status(p.status, MOE_ERR_DEVICE);
+      return;
+    }
+    const uint8_t* rec = p.arena + (uint64_t)slot * p.rec_bytes;
+    const RecordLayout L(p.H, p.I);
+    const float gg = p.gscale[e * 3 + 0], gu = p.gscale[e * 3 + 1];
+    const int pb = p.offsets[e], pe = p.offsets[e + 1];
+    for (int q0 = pb; q0 < pe; q0 += p.maxm) {
+      const int mm = min(p.maxm, pe - q0);
+      const uint16_t* rows[2];
+      for (int j = 0; j < mm; ++j) rows[j] = p.x + (size_t)(p.perm[q0 + j] / p.k) * p.H;
+      __syncthreads();
+      stage_bf16_rows(xs, rows, mm, p.H);
+      __syncthreads();
+      if (mm == 2) gu_routed_pass<2>(p, L, rec, rt, m0, q0, mm, xs, gg, gu);
+      else gu_routed_pass<1>(p, L, rec, rt, m0, q0, mm, xs, gg, gu);
+    }
+  } else {
+    if (p.group != 0 || p.Is == 0) return;
+    const int i0 = (u - p.n_routed_units) * (kDecWarps * 4) + wid * 4;
+    for (int t0 = 0; t0 < p.T; t0 += p.maxm) {
+      const int mm = min(p.maxm, p.T - t0);
+      const uint16_t* rows[2];
+      for (int j = 0; j < mm; ++j) rows[j] = p.x + (size_t)(t0 + j) * p.H;
+      __syncthreads();
+      stage_bf16_rows(xs, rows, mm, p.H);
+      __syncthreads();
+      if (i0 < p.Is) {
+        if (mm == 2) gu_shared_pass<2>(p, i0, t0, mm, xs);
+        else gu_shared_pass<1>(p, i0, t0, mm, xs);
+      }
+    }
+  }
+}
+
+// ---- K-decode-down -----------------------------------------------------------
+template <int M>
+__device__ void down_routed_pass(const DecodeParams& p, const RecordLayout& L, const uint8_t* rec,
+                                 int rt, int m0, int q0, int mm, const float* hs, float gd) {
+  const int lane = threadIdx.x & 31;
+  const int KB = p.I / 16, nhk = p.I / 32;
+  const uint8_t* dc = rec + L.down_codes;
+  float acc[4][M];
+#pragma unroll
+  for (int m1 = 0; m1 < 4; ++m1)
+#pragma unroll
+    for (int j = 0; j < M; ++j) acc[m1][j] = 0.f;
+  for (int hk = lane; hk < nhk; hk += 32) {
+    const int kg = hk >> 1, half = hk & 1;
+    uint4 sd = ldg_stream(rec + L.down_scales + atom_offset(rt, kg, KB) + (uint64_t)m0 * 16);
+    uint4 cd[4];
+#pragma unroll
+    for (int m1 = 0; m1 < 4; ++m1)
+      cd[m1] = ldg_stream(dc + (uint64_t)(rt * 128 + m0 + 32 * m1) * (p.I / 2) + (uint64_t)hk * 16);
+    float xv[M * 32];
+#pragma unroll
+    for (int j = 0; j < M; ++j)
+#pragma unroll
+      for (int i = 0; i < 32; i += 4)
+        *reinterpret_cast<float4*>(xv + j * 32 + i) =
+            *reinterpret_cast<const float4*>(hs + ((size_t)j * nhk + hk) * kXPad + i);
+#pragma unroll
+    for (int m1 = 0; m1 < 4; ++m1) {
+      float s0, s1;
+      scales_of(sd, m1, half, s0, s1);
+      fp4_dot32<M>(cd[m1], s0, s1, xv, acc[m1]);
+    }
+  }
+#pragma unroll
+  for (int m1 = 0; m1 < 4; ++m1)
+#pragma unroll
+    for (int j = 0; j < M; ++j) acc[m1][j] = warp_sum(acc[m1][j]);
+#pragma unroll
+  for (int m1 = 0; m1 < 4; ++m1)
+#pragma unroll
+    for (int j = 0; j < M; ++j)
+      if (lane == m1 * M + j && j < mm) {
+        const int r = p.perm[q0 + j];  // route t*k + j' -> its weight w[r]
+        p.o_route[(size_t)(q0 + j) * p.H + rt * 128 + m0 + 32 * m1] = p.w[r] * gd * acc[m1][j];
+      }
+}
+
+template <int M>
+__device__ void down_shared_pass(const DecodeParams& p, int r0, int t0, int mm, const float* hs) {
+  const uint16_t* rows[4];
+#pragma unroll
+  for (int r = 0; r < 4; ++r) rows[r] = p.s_down + (size_t)(r0 + r) * p.Is;
+  float acc[4][M];
+  warp_rows_bf16<M, 4>(rows, p.Is, hs, acc);
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int j = 0; j < M; ++j)
+      if (lane == r * M + j && j < mm) p.o_shared[(size_t)(t0 + j) * p.H + r0 + r] = acc[r][j];
+}
+
+__global__ void __launch_bounds__(kDecThreads) k_decode_down(DecodeParams p) {
+  extern __shared__ float hs[];
+  const int wid = threadIdx.x >> 5;
+  const int u = blockIdx.x;
+  if (u < p.n_routed_units) {
+    const int tiles = p.H / 128;
+    const int a = u / (tiles * 4), rem = u % (tiles * 4);
+    const int rt = rem >> 2, m0 = (rem & 3) * kDecWarps + wid;
+    int a0, a1;
+    group_range(p, a0, a1);
+    if (a0 + a >= a1) return;
+    const int e = p.act_list[a0 + a];
+    const int slot = (e >= 0 && e < p.E) ? p.src_slot[e] : -1;
+    if (slot < 0 || slot >= p.n_slots) return;  // reported by K-decode-gu
+    const uint8_t* rec = p.arena + (uint64_t)slot * p.rec_bytes;
+    const RecordLayout L(p.H, p.I);
+    const float gd = p.gscale[e * 3 + 2];
+    const int pb = p.offsets[e], pe = p.offsets[e + 1];
+    for (int q0 = pb; q0 < pe; q0 += p.maxm) {
+      const int mm = min(p.maxm, pe - q0);
+      const float* rows[2];
+      for (int j = 0; j < mm; ++j) rows[j] = p.h_route + (size_t)(q0 + j) * p.I;
+      __syncthreads();
+      stage_f32_rows(hs, rows, mm, p.I);
+      __syncthreads();
+      if (mm == 2) down_routed_pass<2>(p, L, rec, rt, m0, q0, mm, hs, gd);
+      else down_routed_pass<1>(p, L, rec, rt, m0, q0, mm, hs, gd);
+    }
+  } else {
+    if (p.group != 0 || p.Is == 0) return;
+    const int r0 = (u - p.n_routed_units) * (kDecWarps * 4) + wid * 4;
+    for (int t0 = 0; t0 < p.T; t0 += p.maxm) {
+      const int mm = min(p.maxm, p.T - t0);
+      const float* rows[2];
+      for (int j = 0; j < mm; ++j) rows[j] = p.h_shared + (size_t)(t0 + j) * p.Is;
+      __syncthreads();
+      stage_f32_rows(hs, rows, mm, p.Is);
+      __syncthreads();
+      if (r0 < p.H) {
+        if (mm == 2) down_shared_pass<2>(p, r0, t0, mm, hs);
+        else down_shared_pass<1>(p, r0, t0, mm, hs);
+      }
+    }
+  }
+}
+
+// ---- K-combine ---------------------------------------------------------------
+__global__ void k_combine(int T, int H, int k, const float* __restrict__ y_acc,
+                          const float* __restrict__ o_route, const int32_t* __restrict__ inv,
+                          const float* __restrict__ o_shared, uint16_t* __restrict__ y) {
+  const int n4 = H / 4;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < T * n4; i += gridDim.x * blockDim.x) {
+    const int t = i / n4, c = (i % n4) * 4;
+    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (y_acc) s = *reinterpret_cast<const float4*>(y_acc + (size_t)t * H + c);
+    if (o_route) {
+      for (int j = 0; j < k; ++j) {
+        const int pp = inv[t * k + j];
+        if (pp < 0) continue;
+        float4 v = *reinterpret_cast<const float4*>(o_route + (size_t)pp * H + c);
+        s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+      }
+    }
+    if (o_shared) {
+      float4 v = *reinterpret_cast<const float4*>(o_shared + (size_t)t * H + c);
+      s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+    }
+    uint2 out;
+    out.x = (uint32_t)f32_to_bf16_rne(s.x) | ((uint32_t)f32_to_bf16_rne(s.y) << 16);
+    out.y = (uint32_t)f32_to_bf16_rne(s.z) | ((uint32_t)f32_to_bf16_rne(s.w) << 16);
+    *reinterpret_cast<uint2*>(y + (size_t)t * H + c) = out;
+  }
+}
+
+// ---- host launchers -----------------------------------------------------------
+size_t decode_workspace_bytes(int T, int I, int k, int Is) {
+  return ((size_t)T * k * I + (size_t)T * Is) * sizeof(float) + 256;
+}
+
+moe_status decode_ffn(const moe_ffn_args* a, cudaStream_t s) {
+  DecodeParams p;
+  p.T = a->T; p.H = a->H; p.I = a->I; p.E = a->E; p.k = a->k; p.Is = a->Is;
+  p.x = (const uint16_t*)a->x;
+  p.arena = cache_arena(a->cache);
+  p.rec_bytes = cache_rec_bytes(a->cache);
+  p.n_slots = cache_n_cache(a->cache) + cache_n_stage(a->cache);
+  p.gscale = a->gscale; p.src_slot = a->src_slot; p.act_list = a->act_list; p.n_act = a->n_act;
+  p.offsets = a->offsets; p.perm = a->perm; p.w = a->w;
+  p.group = a->group;
+  p.n_stage = a->n_stage;
+  p.s_gate = (const uint16_t*)a->s_gate; p.s_up = (const uint16_t*)a->s_up;
+  p.s_down = (const uint16_t*)a->s_down;
+  float* ws = (float*)a->workspace;
+  p.h_route = ws;
+  p.h_shared = ws + (size_t)a->T * a->k * a->I;
+  p.o_route = a->o_route;
+  p.o_shared = a->o_shared;
+  p.status = a->status;
+  p.maxm = a->T >= 2 ? 2 : 1;
+  // experts this group can hold at most
+  int max_act = a->T * a->k < a->E ? a->T * a->k : a->E;
+  if (a->group > 0) max_act = a->n_stage < max_act ? a->n_stage : max_act;
+  const bool shared = a->group == 0 && a->Is > 0;
+  if (a->stages & MOE_STAGE_GATE_UP) {
+    p.n_routed_units = max_act * (a->I / 128) * 4;
+    int n_shared_units = shared ? (a->Is + kDecWarps * 4 - 1) / (kDecWarps * 4) : 0;
+    size_t smem = (size_t)p.maxm * (a->H / 32) * kXPad * sizeof(float);
+    int grid = p.n_routed_units + n_shared_units;
+    if (grid > 0) {
+      k_decode_gu<<<grid, kDecThreads, smem, s>>>(p);
+      MOE_CHECK_LAUNCH();
+    }
+  }
+  if (a->stages & MOE_STAGE_DOWN) {
+    p.n_routed_units = max_act * (a->H / 128) * 4;
+    int n_shared_units = shared ? (a->H + kDecWarps * 4 - 1) / (kDecWarps * 4) : 0;
+    int kin = a->I > a->Is ? a->I : a->Is;
+    size_t smem = (size_t)p.maxm * (kin / 32) * kXPad * sizeof(float);
+    int grid = p.n_routed_units + n_shared_units;
+    if (grid > 0) {
+      k_decode_down<<<grid, kDecThreads, smem, s>>>(p);
+      MOE_CHECK_LAUNCH();
+    }
+  }
+  return MOE_OK;
+}
+
+moe_status decode_setup() {
+  // H up to 16384 with two staged tokens: 2 * 512 * 36 * 4 bytes
+  if (cudaFuncSetAttribute(k_decode_gu, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024) !=
+      cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (cudaFuncSetAttribute(k_decode_down, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           160 * 1024) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+MOE_API moe_status moe_combine(const moe_combine_args* a, void* stream) {
+  if (!a || !a->y || a->T < 0 || a->H <= 0 || a->k <= 0) return MOE_ERR_INVALID_ARG;
+  if (a->o_route && !a->inv) return MOE_ERR_INVALID_ARG;
+  if (a->H % 4) return MOE_ERR_UNSUPPORTED;
+  if (a->T == 0) return MOE_OK;
+  long long n = (long long)a->T * (a->H / 4);
+  int grid = (int)((n + 255) / 256);
+  if (grid > kSMs * 16) grid = kSMs * 16;
+  k_combine<<<grid, 256, 0, (cudaStream_t)stream>>>(a->T, a->H, a->k, a->y_acc, a->o_route, a->inv,
+                                                    a->o_shared, (uint16_t*)a->y);
+  MOE_CHECK_LAUNCH();
+  return MOE_OK;
+}

@@ -1,0 +1,200 @@
+// permute.cu - K-perm: histogram, exclusive scan and stable permutation of the
+// routes by expert (the grouping behind the Strata-GLM blog's "one batched
+// matrix multiply per expert" and the dev.to page's grouped prefill).
+// One CTA of 1024 threads; ranks are computed from warp match masks and
+// per-warp counts, so the permutation is deterministic without atomics on
+// positions.
+#include "common.cuh"
+
+namespace moe {
+
+constexpr int kPermThreads = 1024;
+constexpr int kPermWarps = kPermThreads / 32;
+
+// block-wide exclusive scan of one int per thread (returns the total)
+__device__ int block_exclusive_scan(int v, int* s_warp, int& total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int n = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  if (lane == 31) s_warp[wid] = incl;
+  __syncthreads();
+  if (wid == 0) {
+    int w = (lane < (int)(blockDim.x >> 5)) ? s_warp[lane] : 0;
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int n = __shfl_up_sync(0xFFFFFFFFu, wi, o);
+      if (lane >= o) wi += n;
+    }
+    s_warp[lane] = wi - w;  // exclusive prefix of warp totals
+    if (lane == 31) s_warp[32] = wi;
+  }
+  __syncthreads();
+  int r = s_warp[wid] + incl - v;
+  total = s_warp[32];
+  __syncthreads();
+  return r;
+}
+
+// smem: counts[E] | base[E] | wcnt[32][E] | scan scratch[33]
+__global__ void __launch_bounds__(kPermThreads) k_permute(const int32_t* __restrict__ ids, int n,
+                                                          int E, int32_t* __restrict__ counts,
+                                                          int32_t* __restrict__ offsets,
+                                                          int32_t* __restrict__ perm,
+                                                          int32_t* __restrict__ inv,
+                                                          int32_t* __restrict__ pad_offsets,
+                                                          int pad_align, int32_t* status) {
+  extern __shared__ int sm[];
+  int* s_cnt = sm;
+  int* s_base = s_cnt + E;
+  int* s_w = s_base + E;  // [32][E]
+  int* s_scan = s_w + kPermWarps * E;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+
+  for (int e = tid; e < E; e += kPermThreads) s_cnt[e] = 0;
+  __syncthreads();
+  for (int r = tid; r < n; r += kPermThreads) {
+    int e = ids[r];
+    if (e >= 0 && e < E) atomicAdd(&s_cnt[e], 1);
+    else set_status(status, MOE_ERR_DEVICE);
+  }
+  __syncthreads();
+  // exclusive scans of counts (and of padded counts); E <= 1024 = one per thread
+  int c = (tid < E) ? s_cnt[tid] : 0;
+  int tot;
+  int off = block_exclusive_scan(c, s_scan, tot);
+  if (tid < E) {
+    counts[tid] = c;
+    offsets[tid] = off;
+    s_base[tid] = off;
+  }
+  if (tid == 0) offsets[E] = tot;
+  if (pad_offsets) {
+    int cp = (tid < E) ? ((c + pad_align - 1) / pad_align) * pad_align : 0;
+    int ptot;
+    int poff = block_exclusive_scan(cp, s_scan, ptot);
+    if (tid < E) pad_offsets[tid] = poff;
+    if (tid == 0) pad_offsets[E] = ptot;
+  }
+  __syncthreads();
+
+  // stable positions, 1024 routes per chunk
+  for (int r0 = 0; r0 < n; r0 += kPermThreads) {
+    for (int i = tid; i < kPermWarps * E; i += kPermThreads) s_w[i] = 0;
+    __syncthreads();
+    const int r = r0 + tid;
+    int e = (r < n) ? ids[r] : -1;
+    bool ok = (e >= 0 && e < E);
+    unsigned peers = __match_any_sync(0xFFFFFFFFu, ok ? e : -1);
+    int rank = __popc(peers & ((1u << lane) - 1u));
+    if (ok && rank == 0) s_w[wid * E + e] = __popc(peers);
+    __syncthreads();
+    // per expert: exclusive prefix over warps, then advance the base
+    for (int x = tid; x < E; x += kPermThreads) {
+      int run = s_base[x];
+      for (int w = 0; w < kPermWarps; ++w) {
+        int cw = s_w[w * E + x];
+        s_w[w * E + x] = run;
+        run += cw;
+      }
+      s_base[x] = run;
+    }
+    __syncthreads();
+    if (ok) {
+      int p = s_w[wid * E + e] + rank;
+      perm[p] = r;
+      inv[r] = p;
+    } else if (r < n) {
+      inv[r] = -1;
+    }
+    __syncthreads();
+  }
+}
+
+// K-lookup: one CTA of 1024 threads, one expert per thread
+__global__ void __launch_bounds__(kPermThreads) k_lookup(
+    const int32_t* __restrict__ table, int E, const int32_t* __restrict__ counts,
+    int slot_lo, int slot_hi, int n_cache, int n_stage, int32_t* __restrict__ src_slot,
+    int32_t* __restrict__ act_list, int32_t* __restrict__ n_act, int32_t* __restrict__ miss_ids,
+    int32_t* __restrict__ n_miss, int32_t* status) {
+  __shared__ int s_scan[33];
+  const int e = threadIdx.x;
+  bool active = (e < E) && counts[e] > 0;
+  int slot = active ? table[e] : -1;
+  if (active && slot >= 0 && (slot < slot_lo || slot >= slot_hi)) {
+    set_status(status, MOE_ERR_DEVICE);  // stale or foreign slot: treat as a miss
+    slot = -1;
+  }
+  bool hit = active && slot >= 0;
+  bool miss = active && slot < 0;
+  int nh, nm;
+  int ph = block_exclusive_scan(hit ? 1 : 0, s_scan, nh);
+  int pm = block_exclusive_scan(miss ? 1 : 0, s_scan, nm);
+  if (e < E) {
+    int s = -1;
+    if (hit) {
+      s = slot;
+      act_list[ph] = e;
+    } else if (miss) {
+      act_list[nh + pm] = e;
+      miss_ids[pm] = e;
+      if (n_stage > 0) s = n_cache + (pm % n_stage);
+      else set_status(status, MOE_ERR_DEVICE);
+    }
+    src_slot[e] = s;
+  }
+  if (e == 0) {
+    n_act[0] = nh + nm;
+    n_act[1] = nh;
+    *n_miss = nm;
+  }
+}
+
+}  // namespace moe
+
+namespace moe {
+// opt in to more than 48 KiB of dynamic shared memory (E > 340); idempotent
+moe_status permute_setup() {
+  static int done = 0;
+  if (done) return MOE_OK;
+  if (cudaFuncSetAttribute(k_permute, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024) !=
+      cudaSuccess)
+    return MOE_ERR_CUDA;
+  done = 1;
+  return MOE_OK;
+}
+}  // namespace moe
+
+using namespace moe;
+
+MOE_API moe_status moe_permute(const int32_t* ids, int T, int k, int E, int32_t* counts,
+                               int32_t* offsets, int32_t* perm, int32_t* inv,
+                               int32_t* pad_offsets, int pad_align, int32_t* status,
+                               void* stream) {
+  if (T < 0 || k <= 0 || E <= 0 || !counts || !offsets) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!ids || !perm || !inv)) return MOE_ERR_INVALID_ARG;
+  if (pad_offsets && pad_align <= 0) return MOE_ERR_INVALID_ARG;
+  if (E > 1024 || (long long)T * k > (1 << 20)) return MOE_ERR_UNSUPPORTED;
+  size_t smem = sizeof(int) * ((size_t)E * (2 + kPermWarps) + 33);
+  if (smem > 48 * 1024 && permute_setup() != MOE_OK) return MOE_ERR_CUDA;
+  k_permute<<<1, kPermThreads, smem, (cudaStream_t)stream>>>(ids, T * k, E, counts, offsets, perm,
+                                                            inv, pad_offsets, pad_align, status);
+  MOE_CHECK_LAUNCH();
+  return MOE_OK;
+}
+
+namespace moe {
+moe_status launch_lookup(const int32_t* table_row, int E, const int32_t* counts, int slot_lo,
+                         int slot_hi, int n_cache, int n_stage, int32_t* src_slot,
+                         int32_t* act_list, int32_t* n_act, int32_t* miss_ids, int32_t* n_miss,
+                         int32_t* status, cudaStream_t s) {
+  k_lookup<<<1, kPermThreads, 0, s>>>(table_row, E, counts, slot_lo, slot_hi, n_cache, n_stage,
+                                      src_slot, act_list, n_act, miss_ids, n_miss, status);
+  MOE_CHECK_LAUNCH();
+  return MOE_OK;
+}
+}  // namespace moe

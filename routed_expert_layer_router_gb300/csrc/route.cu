@@ -1,0 +1,229 @@
+// route.cu - K-route: router logits (fp32), softmax, top-k and renormalised
+// weights.  The router is the device-side router of the "Project Maya" page
+// ("Three tiers and the rules between them"): fp32 router weights, top-8 of
+// 288 experts per token, selection kept on the device.
+#include "common.cuh"
+
+namespace moe {
+
+// ---- logits for few tokens: one CTA per expert row -------------------------
+// Each thread accumulates its strided slice of the row (fixed order), then a
+// fixed-shape tree reduction: deterministic.
+constexpr int kGemvMaxT = 8;
+
+__global__ void __launch_bounds__(256) k_logits_gemv(const uint16_t* __restrict__ x,
+                                                     const float* __restrict__ wr,
+                                                     const float* __restrict__ bias, int T,
+                                                     int H, int E, float* __restrict__ logits) {
+  const int e = blockIdx.x;
+  const float4* wrow = reinterpret_cast<const float4*>(wr + (size_t)e * H);
+  float acc[kGemvMaxT];
+#pragma unroll
+  for (int t = 0; t < kGemvMaxT; ++t) acc[t] = 0.f;
+  for (int i = threadIdx.x; i < H / 4; i += blockDim.x) {
+    float4 w = __ldg(wrow + i);
+#pragma unroll
+    for (int t = 0; t < kGemvMaxT; ++t) {
+      if (t < T) {
+        uint2 xv = __ldg(reinterpret_cast<const uint2*>(x + (size_t)t * H) + i);
+        float a = acc[t];
+        a = fmaf(w.x, bf16_lo(xv.x), a);
+        a = fmaf(w.y, bf16_hi(xv.x), a);
+        a = fmaf(w.z, bf16_lo(xv.y), a);
+        a = fmaf(w.w, bf16_hi(xv.y), a);
+        acc[t] = a;
+      }
+    }
+  }
+  __shared__ float red[kGemvMaxT][8];
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+#pragma unroll
+  for (int t = 0; t < kGemvMaxT; ++t) {
+    if (t < T) {
+      float v = warp_sum(acc[t]);
+      if (lane == 0) red[t][wid] = v;
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x < T) {
+    const int t = threadIdx.x;
+    float s = 0.f;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) s += red[t][w];
+    if (bias) s += bias[e];
+    logits[(size_t)t * E + e] = s;
+  }
+}
+
+// ---- logits for many tokens: SIMT tiled GEMM --------------------------------
+// Tile 64 tokens x 64 experts, 256 threads, 4x4 outputs each, K chunks of 32.
+// Each chunk's partial sum is added to the running total with Kahan
+// compensation, keeping the fp32 error of the 6144-term dot products near
+// that of the chunk sums (the router probabilities are compared at 1e-5).
+constexpr int kTM = 64, kTN = 64, kTK = 32;
+
+__global__ void __launch_bounds__(256) k_logits_gemm(const uint16_t* __restrict__ x,
+                                                     const float* __restrict__ wr,
+                                                     const float* __restrict__ bias, int T,
+                                                     int H, int E, float* __restrict__ logits) {
+  __shared__ float xs[kTK][kTM + 4];
+  __shared__ float ws[kTK][kTN + 4];
+  const int t0 = blockIdx.y * kTM, e0 = blockIdx.x * kTN;
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  float acc[4][4], cmp[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = cmp[i][j] = 0.f;
+
+  for (int k0 = 0; k0 < H; k0 += kTK) {
+    // load x tile: 64 tokens x 32 k (bf16) -> transposed fp32
+    for (int idx = threadIdx.x; idx < kTM * kTK / 2; idx += 256) {
+      int tt = idx / (kTK / 2), kk = (idx % (kTK / 2)) * 2;
+      int t = t0 + tt;
+      uint32_t v = 0;
+      if (t < T) v = __ldg(reinterpret_cast<const uint32_t*>(x + (size_t)t * H + k0 + kk));
+      xs[kk][tt] = bf16_lo(v);
+      xs[kk + 1][tt] = bf16_hi(v);
+    }
+    for (int idx = threadIdx.x; idx < kTN * kTK / 4; idx += 256) {
+      int ee = idx / (kTK / 4), kk = (idx % (kTK / 4)) * 4;
+      int e = e0 + ee;
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (e < E) v = __ldg(reinterpret_cast<const float4*>(wr + (size_t)e * H + k0 + kk));
+      ws[kk][ee] = v.x;
+      ws[kk + 1][ee] = v.y;
+      ws[kk + 2][ee] = v.z;
+      ws[kk + 3][ee] = v.w;
+    }
+    __syncthreads();
+    float part[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) part[i][j] = 0.f;
+#pragma unroll 8
+    for (int kk = 0; kk < kTK; ++kk) {
+      float a[4], b[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) a[i] = xs[kk][ty * 4 + i];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) b[j] = ws[kk][tx * 4 + j];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) part[i][j] = fmaf(a[i], b[j], part[i][j]);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {  // Kahan: acc += part
+        float y = part[i][j] - cmp[i][j];
+        float s = acc[i][j] + y;
+        cmp[i][j] = (s - acc[i][j]) - y;
+        acc[i][j] = s;
+      }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    int t = t0 + ty * 4 + i;
+    if (t >= T) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      int e = e0 + tx * 4 + j;
+      if (e < E) logits[(size_t)t * E + e] = acc[i][j] + (bias ? bias[e] : 0.f);
+    }
+  }
+}
+
+// ---- softmax + top-k + renormalisation: one warp per token ------------------
+__global__ void __launch_bounds__(256) k_topk(const float* __restrict__ logits, int T, int E,
+                                              int k, int32_t* __restrict__ ids,
+                                              float* __restrict__ w, float* __restrict__ p_sel) {
+  extern __shared__ float sl[];  // [8 warps][E]
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int t = blockIdx.x * 8 + wid;
+  if (t >= T) return;
+  float* l = sl + (size_t)wid * E;
+  const int per = (E + 31) / 32;
+  float lmax = -INFINITY;
+  for (int j = 0; j < per; ++j) {
+    int e = lane + 32 * j;
+    float v = (e < E) ? logits[(size_t)t * E + e] : -INFINITY;
+    if (e < E) l[e] = v;
+    lmax = fmaxf(lmax, v);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) lmax = fmaxf(lmax, __shfl_xor_sync(0xFFFFFFFFu, lmax, o));
+  float z = 0.f;
+  for (int j = 0; j < per; ++j) {
+    int e = lane + 32 * j;
+    if (e < E) z += expf(l[e] - lmax);
+  }
+  z = warp_sum(z);
+  uint32_t taken = 0;  // bit j: element lane + 32 j selected
+  float sel_sum = 0.f;
+  float my_v = 0.f;
+  int my_id = -1;
+  for (int s = 0; s < k; ++s) {
+    float bv = -INFINITY;
+    int bid = 0x7FFFFFFF;
+    for (int j = 0; j < per; ++j) {
+      int e = lane + 32 * j;
+      if (e < E && !((taken >> j) & 1u)) {
+        float v = l[e];
+        if (v > bv || (v == bv && e < bid)) { bv = v; bid = e; }
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
+      int oid = __shfl_xor_sync(0xFFFFFFFFu, bid, o);
+      if (ov > bv || (ov == bv && oid < bid)) { bv = ov; bid = oid; }
+    }
+    if ((bid & 31) == lane) taken |= 1u << (bid >> 5);
+    float pe = expf(bv - lmax);
+    sel_sum += pe;  // same value and order in every lane
+    if (lane == s) { my_v = pe; my_id = bid; }
+  }
+  if (lane < k) {
+    ids[(size_t)t * k + lane] = my_id;
+    w[(size_t)t * k + lane] = my_v / sel_sum;
+    if (p_sel) p_sel[(size_t)t * k + lane] = my_v / z;
+  }
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+MOE_API size_t moe_route_workspace_bytes(int T, int E) {
+  return (T > 0 && E > 0) ? (size_t)T * E * sizeof(float) : 0;
+}
+
+MOE_API moe_status moe_route(const moe_route_args* a, void* stream) {
+  if (!a || !a->x || !a->w_router || !a->ids || !a->w) return MOE_ERR_INVALID_ARG;
+  if (a->T < 0 || a->H <= 0 || a->E <= 0 || a->k <= 0 || a->k > a->E || a->k > 32)
+    return MOE_ERR_INVALID_ARG;
+  if (a->H % 256 || a->E > 1024) return MOE_ERR_UNSUPPORTED;
+  if (a->T == 0) return MOE_OK;
+  float* logits = a->logits;
+  if (!logits) {
+    if (!a->workspace || a->workspace_bytes < moe_route_workspace_bytes(a->T, a->E))
+      return MOE_ERR_INVALID_ARG;
+    logits = (float*)a->workspace;
+  }
+  cudaStream_t s = (cudaStream_t)stream;
+  const uint16_t* x = (const uint16_t*)a->x;
+  if (a->T <= kGemvMaxT) {
+    k_logits_gemv<<<a->E, 256, 0, s>>>(x, a->w_router, a->bias, a->T, a->H, a->E, logits);
+  } else {
+    dim3 grid((a->E + kTN - 1) / kTN, (a->T + kTM - 1) / kTM);
+    k_logits_gemm<<<grid, 256, 0, s>>>(x, a->w_router, a->bias, a->T, a->H, a->E, logits);
+  }
+  MOE_CHECK_LAUNCH();
+  size_t smem = (size_t)8 * a->E * sizeof(float);
+  k_topk<<<(a->T + 7) / 8, 256, smem, s>>>(logits, a->T, a->E, a->k, a->ids, a->w, a->p_sel);
+  MOE_CHECK_LAUNCH();
+  return MOE_OK;
+}
