@@ -239,6 +239,33 @@ typedef struct {
 size_t moe_ffn_workspace_bytes(int mode, int T, int H, int I, int E, int k, int Is);
 moe_status moe_expert_ffn(const moe_ffn_args* a, void* stream);
 
+/* moe_expert_ffn_noalloc - the DECODE expert FFN for callers that cannot
+ * allocate device memory.  The pages have no counterpart to this call; it
+ * exists for code that must not allocate on its own: an engine whose device
+ * memory is fully reserved up front by an outer framework or pool (so a
+ * cudaMalloc would fail or fragment it), a latency-critical serving loop
+ * where an allocation could block on the driver, or a plugin that is only
+ * handed input and output buffers.
+ *
+ * Same arguments and results as moe_expert_ffn in MOE_MODE_DECODE, except
+ * that a->workspace and a->workspace_bytes are ignored: the scratch between
+ * the gate/up and down kernels (T*k*I + T*Is floats) lives in one fixed
+ * array in the library's device memory, MOE_NOALLOC_SCRATCH_BYTES large,
+ * which every GPU that loads the library holds until the process exits.
+ * The caller still passes inputs and outputs.  Nothing is allocated.
+ *   - Returns MOE_ERR_UNSUPPORTED when mode is not MOE_MODE_DECODE or when
+ *     moe_ffn_workspace_bytes(MOE_MODE_DECODE, T, H, I, E, k, Is) exceeds
+ *     MOE_NOALLOC_SCRATCH_BYTES (use moe_expert_ffn for such sizes).
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.
+ *   - All calls share the one array and it keeps the last call's contents;
+ *     no part of it needs to start at zero.  Calls that overlap on the GPU
+ *     (different streams, no ordering between them) race on it and give
+ *     wrong results: order them on one stream or with events. */
+#define MOE_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+moe_status moe_expert_ffn_noalloc(const moe_ffn_args* a, void* stream);
+
 /* ---------------------------------------------------------------- combine
  * y[t] = bf16_rne( y_acc[t] + sum_{j<k} o_route[inv[t*k+j]] + o_shared[t] ),
  * each term skipped when its pointer is NULL; the k-term sum is taken in

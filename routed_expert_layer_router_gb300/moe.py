@@ -78,6 +78,7 @@ SIGNATURES = {
     "expcache_lookup": (i32, [vp, i32, vp, vp, vp, vp, vp, vp, vp, vp]),
     "moe_ffn_workspace_bytes": (sz, [i32, i32, i32, i32, i32, i32, i32]),
     "moe_expert_ffn": (i32, [ctypes.POINTER(moe_ffn_args), vp]),
+    "moe_expert_ffn_noalloc": (i32, [ctypes.POINTER(moe_ffn_args), vp]),
     "moe_combine": (i32, [ctypes.POINTER(moe_combine_args), vp]),
     "moe_layer_create": (i32, [ctypes.POINTER(moe_layer_desc), ctypes.POINTER(vp)]),
     "moe_layer_destroy": (i32, [vp]),
@@ -178,6 +179,17 @@ def moe_ffn_workspace_bytes(mode, T, H, I, E, k, Is) -> int:
 
 def moe_expert_ffn(args: moe_ffn_args, stream: int = 0) -> None:
     _ck("moe_expert_ffn", lib().moe_expert_ffn(ctypes.byref(args), stream))
+
+
+MOE_NOALLOC_SCRATCH_BYTES = 8 << 20
+
+
+def moe_expert_ffn_noalloc(args: moe_ffn_args, stream: int = 0) -> None:
+    """Decode expert FFN without caller workspace (for callers that cannot
+    allocate device memory): the scratch is a fixed library-owned device
+    array of MOE_NOALLOC_SCRATCH_BYTES shared by all calls; calls that overlap
+    on the GPU race on it."""
+    _ck("moe_expert_ffn_noalloc", lib().moe_expert_ffn_noalloc(ctypes.byref(args), stream))
 
 
 def moe_combine(args: moe_combine_args, stream: int = 0) -> None:
