@@ -110,7 +110,10 @@ def run_ours(args, rank, world, local_rank):
     wl = gen.WORKLOADS["decode"]
     H, I, E, k, Is = wl.H, wl.I, wl.E, wl.k, wl.Is
     T = 1
-    dw = gd.build(wl, T_max=T)
+    # --small: the same layer with only 16 distinct expert records (expert e
+    # reads slot e mod 16): same kernels and launch shapes, ~0.5 GB on the
+    # device, for profiler captures; not a bench value
+    dw = gd.build(wl, T_max=T, slot_alias=16 if args.small else 0)
     layer = dw.moe_layers[0]
     stream = torch.cuda.current_stream()
     sp = stream.cuda_stream
@@ -371,6 +374,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-seconds", type=float, default=60.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--small", action="store_true",
+                    help="16 distinct expert records (profiler captures only)")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -57,7 +57,8 @@ def _hot_set(wl: gen.Workload, layer: int, bias_rank, saliency_order):
 
 def build(wl: gen.Workload, layers: int | None = None, T_max: int | None = None,
           n_stage: int | None = None, saliency_order=None, prefill_min_tokens: int | None = None,
-          alias_host_records: bool = False, resident=None, stream=None) -> DeviceWorkload:
+          alias_host_records: bool = False, resident=None, slot_alias: int = 0,
+          stream=None) -> DeviceWorkload:
     """Device-resident layer(s) of workload `wl`.
 
     layers: how many of the workload's layers to build (default: all).
@@ -131,12 +132,19 @@ def build(wl: gen.Workload, layers: int | None = None, T_max: int | None = None,
         del buf
         host_arena.register()
 
+    if slot_alias > 0:
+        # profiling only: every layer's experts share slot_alias records (expert
+        # e reads slot e mod slot_alias); the outputs are not those of the workload
+        assert L == 1 and miss_max == 0
+        n_cache = slot_alias
+        layer_slots = np.array([0, slot_alias], np.int32)
     cache = ExpertCache(L, E, H, I, n_cache, n_stage, layer_slots=layer_slots,
                         host_arena=host_arena, host_index=host_index)
     for l in range(L):
         for j, e in enumerate(resident[l]):
-            slot = int(layer_slots[l]) + j
-            gen.dev_expert_record(wl.seed, rec_layer[l], e, H, I, cache.slot_ptr(slot), sp)
+            slot = int(layer_slots[l]) + (j % slot_alias if slot_alias > 0 else j)
+            if slot_alias == 0 or j < slot_alias:
+                gen.dev_expert_record(wl.seed, rec_layer[l], e, H, I, cache.slot_ptr(slot), sp)
             cache.set_resident(l, e, slot, s)
 
     w_router, gscale, gscale_host, bias, shared, mls = [], [], [], [], [], []

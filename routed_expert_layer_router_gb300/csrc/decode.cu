@@ -1,13 +1,18 @@
 // decode.cu - K-decode-gu, K-decode-down and K-combine: the expert FFN for few
 // tokens per expert, HBM-bound.  Weights stream from their cache or staging
-// slot with 128-bit loads; the NVFP4 dequant (E2M1 code x E4M3 block scale x
-// fp32 global) happens in registers and feeds fp32 FMAs on the bf16
-// activations.  Work is cut so that one warp owns 4 gate rows + 4 up rows (or
-// 4 down rows) that share one 16-byte row of every 512-byte scale atom, and
-// every activation value a lane loads from shared memory is reused across the
-// warp's rows.  Sources: "Project Maya" page, section "A V100 has no BF16 and
-// no FP8" (decode is a matrix-vector product where the bytes, not the
-// arithmetic, set the speed); dev.to page, section "The wall" (NVFP4 experts).
+// slot with 128-bit loads (the next step's loads are issued before the current
+// step is computed); the NVFP4 dequant happens in registers: the E2M1 codes go
+// through the hardware e2m1x2 -> f16x2 conversion and meet the activations in
+// mixed-precision FMAs (f16 x f16 products, exact, accumulated in fp32); each
+// 16-element partial sum is scaled once by its E4M3 block scale and the fp32
+// global scale at the end.  One warp owns the rows {m0 + 32*m1 : m1 < 4} of a
+// 128-row tile, which share one 16-byte row of every 512-byte scale atom, and
+// every activation it reads from shared memory is reused across those rows.
+// Sources: "Project Maya" page, section "A V100 has no BF16 and no FP8" (decode
+// is a matrix-vector product where the bytes, not the arithmetic, set the
+// speed); dev.to page, section "The wall" (NVFP4 experts).
+#include <cuda_fp16.h>
+
 #include "common.cuh"
 
 namespace moe {
@@ -19,14 +24,16 @@ int cache_n_stage(const expcache* c);
 
 constexpr int kDecWarps = 8;
 constexpr int kDecThreads = kDecWarps * 32;
-constexpr int kXPad = 36;  // floats per 32-element half-k-group in shared memory (bank spread)
+constexpr int kXPad = 36;  // fp32 staging: floats per 32 values (bank spread)
+constexpr int kHPad = 40;  // f16 staging: halves per 32 values (80-byte stride, conflict-free)
+constexpr int kSharedKSplit = 4;  // shared gate/up: warps splitting the row length
 
 struct DecodeParams {
   int T, H, I, E, k, Is;
   const uint16_t* x;
   const uint8_t* arena;
   uint64_t rec_bytes;
-  int n_slots;      // cache + staging slots in the arena
+  int n_slots;  // cache + staging slots in the arena
   const float* gscale;
   const int32_t* src_slot;
   const int32_t* act_list;
@@ -35,7 +42,7 @@ struct DecodeParams {
   const int32_t* perm;
   const float* w;
   int group, n_stage;
-  int n_routed_units;  // grid units reserved for routed experts
+  int n_shared_units;  // leading grid units: shared expert
   const uint16_t* s_gate;
   const uint16_t* s_up;
   const uint16_t* s_down;
@@ -44,7 +51,7 @@ struct DecodeParams {
   float* o_route;   // [T*k][H]
   float* o_shared;  // [T][H]
   int32_t* status;
-  int maxm;         // tokens staged per pass (1 or 2)
+  int maxm;  // tokens staged per pass (1 or 2)
 };
 
 // act_list index range of this group
@@ -60,66 +67,99 @@ __device__ __forceinline__ void group_range(const DecodeParams& p, int& a0, int&
   }
 }
 
-// stage `m` vectors (bf16 rows or fp32 rows) into padded fp32 shared memory
-__device__ __forceinline__ void stage_bf16_rows(float* xs, const uint16_t* const* rows, int m,
-                                                int K) {
+// ---- staging ---------------------------------------------------------------
+// f16 layout: row j, half-k-group hk (32 values) at (j*nhk + hk)*kHPad halves
+__device__ __forceinline__ void stage_bf16_to_f16(__half* xs, const uint16_t* const* rows, int m,
+                                                  int K) {
+  const int nhk = K / 32;
+  for (int j = 0; j < m; ++j) {
+    const uint32_t* src = reinterpret_cast<const uint32_t*>(rows[j]);
+    __half* dst = xs + (size_t)j * nhk * kHPad;
+    for (int i = threadIdx.x; i < K / 2; i += blockDim.x) {
+      uint32_t v = __ldg(src + i);
+      const int e = 2 * i;
+      *reinterpret_cast<__half2*>(dst + (e >> 5) * kHPad + (e & 31)) =
+          __floats2half2_rn(bf16_lo(v), bf16_hi(v));
+    }
+  }
+}
+
+__device__ __forceinline__ void stage_f32_to_f16(__half* xs, const float* const* rows, int m,
+                                                 int K) {
+  const int nhk = K / 32;
+  for (int j = 0; j < m; ++j) {
+    const float2* src = reinterpret_cast<const float2*>(rows[j]);
+    __half* dst = xs + (size_t)j * nhk * kHPad;
+    for (int i = threadIdx.x; i < K / 2; i += blockDim.x) {
+      float2 v = src[i];
+      const int e = 2 * i;
+      *reinterpret_cast<__half2*>(dst + (e >> 5) * kHPad + (e & 31)) = __floats2half2_rn(v.x, v.y);
+    }
+  }
+}
+
+// fp32 layout: row j, half-k-group hk at (j*nhk + hk)*kXPad floats
+__device__ __forceinline__ void stage_bf16_to_f32(float* xs, const uint16_t* const* rows, int m,
+                                                  int K) {
   const int nhk = K / 32;
   for (int j = 0; j < m; ++j) {
     const uint32_t* src = reinterpret_cast<const uint32_t*>(rows[j]);
     float* dst = xs + (size_t)j * nhk * kXPad;
     for (int i = threadIdx.x; i < K / 2; i += blockDim.x) {
       uint32_t v = __ldg(src + i);
-      int e = 2 * i;
+      const int e = 2 * i;
       dst[(e >> 5) * kXPad + (e & 31)] = bf16_lo(v);
       dst[(e >> 5) * kXPad + (e & 31) + 1] = bf16_hi(v);
     }
   }
 }
 
-__device__ __forceinline__ void stage_f32_rows(float* xs, const float* const* rows, int m, int K) {
+__device__ __forceinline__ void stage_f32_to_f32(float* xs, const float* const* rows, int m,
+                                                 int K) {
   const int nhk = K / 32;
   for (int j = 0; j < m; ++j) {
     const float4* src = reinterpret_cast<const float4*>(rows[j]);
     float* dst = xs + (size_t)j * nhk * kXPad;
     for (int i = threadIdx.x; i < K / 4; i += blockDim.x) {
       float4 v = src[i];
-      int e = 4 * i;
+      const int e = 4 * i;
       *reinterpret_cast<float4*>(dst + (e >> 5) * kXPad + (e & 31)) = v;
     }
   }
 }
 
-// 32 E2M1 codes (16 bytes) of one row against M staged vectors.
-// blocks: codes 0..15 use scale s0, 16..31 use s1.  acc[j] += s0*sum0 + s1*sum1.
+// ---- FP4 x f16 dot products -------------------------------------------------
+// a += w.lo * x.lo, b += w.hi * x.hi : f16 operands, exact products, fp32 sums
+__device__ __forceinline__ void fma_h2(float& a, float& b, uint32_t w2, uint32_t x2) {
+  asm("{\n .reg .b16 wl, wh, xl, xh;\n mov.b32 {wl, wh}, %2;\n mov.b32 {xl, xh}, %3;\n"
+      " fma.rn.f32.f16 %0, wl, xl, %0;\n fma.rn.f32.f16 %1, wh, xh, %1;\n}"
+      : "+f"(a), "+f"(b) : "r"(w2), "r"(x2));
+}
+
+// 32 E2M1 codes (16 bytes) of one row against M staged f16 vectors (16 f16x2
+// registers each).  Codes 0..15 form the block with scale s0, 16..31 with s1.
 template <int M>
-__device__ __forceinline__ void fp4_dot32(const uint4& c, float s0, float s1, const float* xv,
-                                          float* acc) {
+__device__ __forceinline__ void fp4_dot32h(const uint4& c, float s0, float s1, const uint32_t* xh,
+                                           float* acc) {
   const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
-  float p0[M], p1[M];
 #pragma unroll
-  for (int j = 0; j < M; ++j) p0[j] = p1[j] = 0.f;
+  for (int blk = 0; blk < 2; ++blk) {
+    float pa[M], pb[M];
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    uint32_t h[4];
-    e2m1x8_to_f16x2x4(cw[q], h);
+    for (int j = 0; j < M; ++j) pa[j] = pb[j] = 0.f;
 #pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      float v0 = f16_lo(h[b]), v1 = f16_hi(h[b]);
-      const int e = q * 8 + b * 2;
+    for (int q = 2 * blk; q < 2 * blk + 2; ++q) {
+      uint32_t h[4];
+      e2m1x8_to_f16x2x4(cw[q], h);
 #pragma unroll
-      for (int j = 0; j < M; ++j) {
-        if (q < 2) {
-          p0[j] = fmaf(v0, xv[j * 32 + e], p0[j]);
-          p0[j] = fmaf(v1, xv[j * 32 + e + 1], p0[j]);
-        } else {
-          p1[j] = fmaf(v0, xv[j * 32 + e], p1[j]);
-          p1[j] = fmaf(v1, xv[j * 32 + e + 1], p1[j]);
-        }
-      }
+      for (int b = 0; b < 4; ++b)
+#pragma unroll
+        for (int j = 0; j < M; ++j) fma_h2(pa[j], pb[j], h[b], xh[j * 16 + q * 4 + b]);
     }
-  }
+    const float s = blk ? s1 : s0;
 #pragma unroll
-  for (int j = 0; j < M; ++j) acc[j] = fmaf(s1, p1[j], fmaf(s0, p0[j], acc[j]));
+    for (int j = 0; j < M; ++j) acc[j] = fmaf(s, pa[j] + pb[j], acc[j]);
+  }
 }
 
 // the two E4M3 scales (bytes 2*half, 2*half+1 of 4-byte word m1 of an atom row)
@@ -130,44 +170,71 @@ __device__ __forceinline__ void scales_of(const uint4& a, int m1, int half, floa
   s1 = f16_hi(h2);
 }
 
-// gate+up for the 4 rows {rt*128 + m0 + 32*m1} of one expert, M staged tokens
+template <int M>
+__device__ __forceinline__ void load_xh(const __half* xs, int nhk, int hk, uint32_t* xh) {
+#pragma unroll
+  for (int j = 0; j < M; ++j) {
+    const uint4* src = reinterpret_cast<const uint4*>(xs + ((size_t)j * nhk + hk) * kHPad);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint4 v = src[i];
+      xh[j * 16 + 4 * i + 0] = v.x;
+      xh[j * 16 + 4 * i + 1] = v.y;
+      xh[j * 16 + 4 * i + 2] = v.z;
+      xh[j * 16 + 4 * i + 3] = v.w;
+    }
+  }
+}
+
+// gate+up of the 4 rows {rt*128 + m0 + 32*m1} of one expert, M staged tokens.
+// Returns warp-reduced sums (all lanes).
 template <int M>
 __device__ void warp_gu_fp4(const uint8_t* rec, const RecordLayout& L, int H, int rt, int m0,
-                            const float* xs, float accg[4][M], float accu[4][M]) {
+                            const __half* xs, float accg[4][M], float accu[4][M]) {
   const int lane = threadIdx.x & 31;
   const int KB = H / 16, nhk = H / 32;
-  const uint8_t* gc = rec + L.gate_codes;
-  const uint8_t* uc = rec + L.up_codes;
+  const uint8_t* gc = rec + L.gate_codes + (uint64_t)(rt * 128 + m0) * (H / 2);
+  const uint8_t* uc = rec + L.up_codes + (uint64_t)(rt * 128 + m0) * (H / 2);
+  const uint64_t rstride = (uint64_t)32 * (H / 2);
 #pragma unroll
   for (int m1 = 0; m1 < 4; ++m1)
 #pragma unroll
     for (int j = 0; j < M; ++j) accg[m1][j] = accu[m1][j] = 0.f;
-  for (int hk = lane; hk < nhk; hk += 32) {
-    const int kg = hk >> 1, half = hk & 1;
-    const uint64_t aoff = atom_offset(rt, kg, KB) + (uint64_t)m0 * 16;
-    uint4 sg = ldg_stream(rec + L.gate_scales + aoff);
-    uint4 su = ldg_stream(rec + L.up_scales + aoff);
-    uint4 cg[4], cu[4];
+  uint4 cg[4], cu[4], sg, su;
+  auto fetch = [&](int hk, uint4* g4, uint4* u4, uint4& sgv, uint4& suv) {
+    const uint64_t aoff = atom_offset(rt, hk >> 1, KB) + (uint64_t)m0 * 16;
+    sgv = ldg_stream(rec + L.gate_scales + aoff);
+    suv = ldg_stream(rec + L.up_scales + aoff);
 #pragma unroll
     for (int m1 = 0; m1 < 4; ++m1) {
-      const uint64_t roff = (uint64_t)(rt * 128 + m0 + 32 * m1) * (H / 2) + (uint64_t)hk * 16;
-      cg[m1] = ldg_stream(gc + roff);
-      cu[m1] = ldg_stream(uc + roff);
+      g4[m1] = ldg_stream(gc + m1 * rstride + (uint64_t)hk * 16);
+      u4[m1] = ldg_stream(uc + m1 * rstride + (uint64_t)hk * 16);
     }
-    float xv[M * 32];
-#pragma unroll
-    for (int j = 0; j < M; ++j)
-#pragma unroll
-      for (int i = 0; i < 32; i += 4)
-        *reinterpret_cast<float4*>(xv + j * 32 + i) =
-            *reinterpret_cast<const float4*>(xs + ((size_t)j * nhk + hk) * kXPad + i);
+  };
+  if (lane < nhk) fetch(lane, cg, cu, sg, su);
+  for (int hk = lane; hk < nhk; hk += 32) {
+    uint4 ng[4], nu[4], nsg, nsu;
+    const bool more = hk + 32 < nhk;
+    if (more) fetch(hk + 32, ng, nu, nsg, nsu);
+    uint32_t xh[M * 16];
+    load_xh<M>(xs, nhk, hk, xh);
+    const int half = hk & 1;
 #pragma unroll
     for (int m1 = 0; m1 < 4; ++m1) {
       float s0, s1;
       scales_of(sg, m1, half, s0, s1);
-      fp4_dot32<M>(cg[m1], s0, s1, xv, accg[m1]);
+      fp4_dot32h<M>(cg[m1], s0, s1, xh, accg[m1]);
       scales_of(su, m1, half, s0, s1);
-      fp4_dot32<M>(cu[m1], s0, s1, xv, accu[m1]);
+      fp4_dot32h<M>(cu[m1], s0, s1, xh, accu[m1]);
+    }
+    if (more) {
+#pragma unroll
+      for (int m1 = 0; m1 < 4; ++m1) {
+        cg[m1] = ng[m1];
+        cu[m1] = nu[m1];
+      }
+      sg = nsg;
+      su = nsu;
     }
   }
 #pragma unroll
@@ -179,7 +246,7 @@ __device__ void warp_gu_fp4(const uint8_t* rec, const RecordLayout& L, int H, in
     }
 }
 
-// 8 bf16 weights (16 bytes) against M staged vectors (8 consecutive values)
+// ---- bf16 rows (shared expert) against fp32 staged vectors -----------------
 template <int M>
 __device__ __forceinline__ void bf16_dot8(const uint4& c, const float* xv, float* acc) {
   const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
@@ -192,9 +259,9 @@ __device__ __forceinline__ void bf16_dot8(const uint4& c, const float* xv, float
     }
 }
 
-// bf16 matrix rows r[0..3] (row length K) against M staged vectors
+// NR rows over elements [k0, k1) of length-K rows: per-lane partial sums
 template <int M, int NR>
-__device__ void warp_rows_bf16(const uint16_t* const* rows, int K, const float* xs,
+__device__ void warp_rows_bf16(const uint16_t* const* rows, int K, int k0, int k1, const float* xs,
                                float acc[NR][M]) {
   const int lane = threadIdx.x & 31;
   const int nhk = K / 32;
@@ -202,7 +269,7 @@ __device__ void warp_rows_bf16(const uint16_t* const* rows, int K, const float* 
   for (int r = 0; r < NR; ++r)
 #pragma unroll
     for (int j = 0; j < M; ++j) acc[r][j] = 0.f;
-  for (int i0 = lane * 8; i0 < K; i0 += 256) {
+  for (int i0 = k0 + lane * 8; i0 < k1; i0 += 256) {
     uint4 c[NR];
 #pragma unroll
     for (int r = 0; r < NR; ++r) c[r] = ldg_stream(rows[r] + i0);
@@ -216,10 +283,6 @@ __device__ void warp_rows_bf16(const uint16_t* const* rows, int K, const float* 
 #pragma unroll
     for (int r = 0; r < NR; ++r) bf16_dot8<M>(c[r], xv, acc[r]);
   }
-#pragma unroll
-  for (int r = 0; r < NR; ++r)
-#pragma unroll
-    for (int j = 0; j < M; ++j) acc[r][j] = warp_sum(acc[r][j]);
 }
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.f + expf(-g)); }
@@ -227,7 +290,7 @@ __device__ __forceinline__ float silu_f(float g) { return g / (1.f + expf(-g)); 
 // ---- K-decode-gu -------------------------------------------------------------
 template <int M>
 __device__ void gu_routed_pass(const DecodeParams& p, const RecordLayout& L, const uint8_t* rec,
-                               int rt, int m0, int p0, int mm, const float* xs, float gg,
+                               int rt, int m0, int q0, int mm, const __half* xs, float gg,
                                float gu) {
   float accg[4][M], accu[4][M];
   warp_gu_fp4<M>(rec, L, p.H, rt, m0, xs, accg, accu);
@@ -237,123 +300,152 @@ __device__ void gu_routed_pass(const DecodeParams& p, const RecordLayout& L, con
 #pragma unroll
     for (int j = 0; j < M; ++j)
       if (lane == m1 * M + j && j < mm) {
-        float g = accg[m1][j] * gg, u = accu[m1][j] * gu;
-        p.h_route[(size_t)(p0 + j) * p.I + rt * 128 + m0 + 32 * m1] = silu_f(g) * u;
+        const float g = accg[m1][j] * gg, u = accu[m1][j] * gu;
+        p.h_route[(size_t)(q0 + j) * p.I + rt * 128 + m0 + 32 * m1] = silu_f(g) * u;
       }
 }
 
+// shared expert: CTA = 8 row pairs; warp = (row group of 4 pairs) x (quarter of H)
 template <int M>
-__device__ void gu_shared_pass(const DecodeParams& p, int i0, int t0, int mm, const float* xs) {
+__device__ void gu_shared_pass(const DecodeParams& p, int i0, int t0, int mm, const float* xs,
+                               float* red) {
+  const int wid = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rg = wid / kSharedKSplit, ks = wid % kSharedKSplit;
+  const int r0 = i0 + rg * 4;
   const uint16_t* rows[8];
 #pragma unroll
   for (int r = 0; r < 4; ++r) {
-    rows[r] = p.s_gate + (size_t)(i0 + r) * p.H;
-    rows[4 + r] = p.s_up + (size_t)(i0 + r) * p.H;
+    rows[r] = p.s_gate + (size_t)(r0 + r) * p.H;
+    rows[4 + r] = p.s_up + (size_t)(r0 + r) * p.H;
   }
+  const int kq = p.H / kSharedKSplit;
   float acc[8][M];
-  warp_rows_bf16<M, 8>(rows, p.H, xs, acc);
-  const int lane = threadIdx.x & 31;
+  warp_rows_bf16<M, 8>(rows, p.H, ks * kq, (ks + 1) * kq, xs, acc);
 #pragma unroll
-  for (int r = 0; r < 4; ++r)
+  for (int r = 0; r < 8; ++r)
 #pragma unroll
-    for (int j = 0; j < M; ++j)
-      if (lane == r * M + j && j < mm)
-        p.h_shared[(size_t)(t0 + j) * p.Is + i0 + r] = silu_f(acc[r][j]) * acc[4 + r][j];
+    for (int j = 0; j < M; ++j) {
+      float v = warp_sum(acc[r][j]);
+      if (lane == 0) red[(wid * 8 + r) * 2 + j] = v;
+    }
+  __syncthreads();
+  // 2 row groups x 4 pairs x mm tokens: thread -> (rg, r, j)
+  const int t = threadIdx.x;
+  if (t < 2 * 4 * 2) {
+    const int g2 = t / 8, r = (t / 2) % 4, j = t % 2;
+    if (j < mm) {
+      float g = 0.f, u = 0.f;
+      for (int s = 0; s < kSharedKSplit; ++s) {
+        const int w = g2 * kSharedKSplit + s;
+        g += red[(w * 8 + r) * 2 + j];
+        u += red[(w * 8 + 4 + r) * 2 + j];
+      }
+      p.h_shared[(size_t)(t0 + j) * p.Is + i0 + g2 * 4 + r] = silu_f(g) * u;
+    }
+  }
+  __syncthreads();
 }
 
+template <int MAXM>
 __global__ void __launch_bounds__(kDecThreads) k_decode_gu(DecodeParams p) {
-  extern __shared__ float xs[];
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  __shared__ float red[kDecWarps * 8 * 2];
   const int wid = threadIdx.x >> 5;
   const int u = blockIdx.x;
-  if (u < p.n_routed_units) {
-    const int tiles = p.I / 128;
-    const int a = u / (tiles * 4), rem = u % (tiles * 4);
-    const int rt = rem >> 2, m0 = (rem & 3) * kDecWarps + wid;
-    int a0, a1;
-    group_range(p, a0, a1);
-    if (a0 + a < a0 || a0 + a >= a1) return;
-    const int e = p.act_list[a0 + a];
-    const int slot = (e >= 0 && e < p.E) ? p.src_slot[e] : -1;
-    if (slot < 0 || slot >= p.n_slots) {
-      if (threadIdx.x == 0) set_status(p.status, MOE_ERR_DEVICE);
-      return;
-    }
-    const uint8_t* rec = p.arena + (uint64_t)slot * p.rec_bytes;
-    const RecordLayout L(p.H, p.I);
-    const float gg = p.gscale[e * 3 + 0], gu = p.gscale[e * 3 + 1];
-    const int pb = p.offsets[e], pe = p.offsets[e + 1];
-    for (int q0 = pb; q0 < pe; q0 += p.maxm) {
-      const int mm = min(p.maxm, pe - q0);
-      const uint16_t* rows[2];
-      for (int j = 0; j < mm; ++j) rows[j] = p.x + (size_t)(p.perm[q0 + j] / p.k) * p.H;
-      __syncthreads();
-      stage_bf16_rows(xs, rows, mm, p.H);
-      __syncthreads();
-      if (mm == 2) gu_routed_pass<2>(p, L, rec, rt, m0, q0, mm, xs, gg, gu);
-      else gu_routed_pass<1>(p, L, rec, rt, m0, q0, mm, xs, gg, gu);
-    }
-  } else {
-    if (p.group != 0 || p.Is == 0) return;
-    const int i0 = (u - p.n_routed_units) * (kDecWarps * 4) + wid * 4;
+  if (u < p.n_shared_units) {
+    float* xs = reinterpret_cast<float*>(smem_raw);
+    const int i0 = u * 8;
     for (int t0 = 0; t0 < p.T; t0 += p.maxm) {
       const int mm = min(p.maxm, p.T - t0);
       const uint16_t* rows[2];
       for (int j = 0; j < mm; ++j) rows[j] = p.x + (size_t)(t0 + j) * p.H;
       __syncthreads();
-      stage_bf16_rows(xs, rows, mm, p.H);
+      stage_bf16_to_f32(xs, rows, mm, p.H);
       __syncthreads();
-      if (i0 < p.Is) {
-        if (mm == 2) gu_shared_pass<2>(p, i0, t0, mm, xs);
-        else gu_shared_pass<1>(p, i0, t0, mm, xs);
-      }
+      if (MAXM == 2 && mm == 2) gu_shared_pass<MAXM>(p, i0, t0, mm, xs, red);
+      else gu_shared_pass<1>(p, i0, t0, mm, xs, red);
     }
+    return;
+  }
+  __half* xs = reinterpret_cast<__half*>(smem_raw);
+  const int ur = u - p.n_shared_units;
+  const int tiles = p.I / 128;
+  const int a = ur / (tiles * 4), rem = ur % (tiles * 4);
+  const int rt = rem >> 2, m0 = (rem & 3) * kDecWarps + wid;
+  int a0, a1;
+  group_range(p, a0, a1);
+  if (a0 + a >= a1) return;
+  const int e = p.act_list[a0 + a];
+  const int slot = (e >= 0 && e < p.E) ? p.src_slot[e] : -1;
+  if (slot < 0 || slot >= p.n_slots) {
+    if (threadIdx.x == 0) set_status(p.status, MOE_ERR_DEVICE);
+    return;
+  }
+  const uint8_t* rec = p.arena + (uint64_t)slot * p.rec_bytes;
+  const RecordLayout L(p.H, p.I);
+  const float gg = p.gscale[e * 3 + 0], gu = p.gscale[e * 3 + 1];
+  const int pb = p.offsets[e], pe = p.offsets[e + 1];
+  for (int q0 = pb; q0 < pe; q0 += p.maxm) {
+    const int mm = min(p.maxm, pe - q0);
+    const uint16_t* rows[2];
+    for (int j = 0; j < mm; ++j) rows[j] = p.x + (size_t)(p.perm[q0 + j] / p.k) * p.H;
+    __syncthreads();
+    stage_bf16_to_f16(xs, rows, mm, p.H);
+    __syncthreads();
+    if (MAXM == 2 && mm == 2) gu_routed_pass<MAXM>(p, L, rec, rt, m0, q0, mm, xs, gg, gu);
+    else gu_routed_pass<1>(p, L, rec, rt, m0, q0, mm, xs, gg, gu);
   }
 }
 
 // ---- K-decode-down -----------------------------------------------------------
+// routed: CTA = one 128-row tile of one expert; warp w owns m0 in {w, w+8, w+16, w+24}
 template <int M>
 __device__ void down_routed_pass(const DecodeParams& p, const RecordLayout& L, const uint8_t* rec,
-                                 int rt, int m0, int q0, int mm, const float* hs, float gd) {
-  const int lane = threadIdx.x & 31;
+                                 int rt, int q0, int mm, const __half* hs, float gd) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const int KB = p.I / 16, nhk = p.I / 32;
   const uint8_t* dc = rec + L.down_codes;
-  float acc[4][M];
+  float acc[4][4][M];
 #pragma unroll
-  for (int m1 = 0; m1 < 4; ++m1)
-#pragma unroll
-    for (int j = 0; j < M; ++j) acc[m1][j] = 0.f;
-  for (int hk = lane; hk < nhk; hk += 32) {
-    const int kg = hk >> 1, half = hk & 1;
-    uint4 sd = ldg_stream(rec + L.down_scales + atom_offset(rt, kg, KB) + (uint64_t)m0 * 16);
-    uint4 cd[4];
+  for (int g = 0; g < 4; ++g)
 #pragma unroll
     for (int m1 = 0; m1 < 4; ++m1)
-      cd[m1] = ldg_stream(dc + (uint64_t)(rt * 128 + m0 + 32 * m1) * (p.I / 2) + (uint64_t)hk * 16);
-    float xv[M * 32];
 #pragma unroll
-    for (int j = 0; j < M; ++j)
+      for (int j = 0; j < M; ++j) acc[g][m1][j] = 0.f;
+  for (int hk = lane; hk < nhk; hk += 32) {
+    const int half = hk & 1;
+    uint4 cd[4][4], sd[4];
 #pragma unroll
-      for (int i = 0; i < 32; i += 4)
-        *reinterpret_cast<float4*>(xv + j * 32 + i) =
-            *reinterpret_cast<const float4*>(hs + ((size_t)j * nhk + hk) * kXPad + i);
+    for (int g = 0; g < 4; ++g) {
+      const int m0 = wid + 8 * g;
+      sd[g] = ldg_stream(rec + L.down_scales + atom_offset(rt, hk >> 1, KB) + (uint64_t)m0 * 16);
 #pragma unroll
-    for (int m1 = 0; m1 < 4; ++m1) {
-      float s0, s1;
-      scales_of(sd, m1, half, s0, s1);
-      fp4_dot32<M>(cd[m1], s0, s1, xv, acc[m1]);
+      for (int m1 = 0; m1 < 4; ++m1)
+        cd[g][m1] = ldg_stream(dc + (uint64_t)(rt * 128 + m0 + 32 * m1) * (p.I / 2) +
+                               (uint64_t)hk * 16);
     }
+    uint32_t xh[M * 16];
+    load_xh<M>(hs, nhk, hk, xh);
+#pragma unroll
+    for (int g = 0; g < 4; ++g)
+#pragma unroll
+      for (int m1 = 0; m1 < 4; ++m1) {
+        float s0, s1;
+        scales_of(sd[g], m1, half, s0, s1);
+        fp4_dot32h<M>(cd[g][m1], s0, s1, xh, acc[g][m1]);
+      }
   }
 #pragma unroll
-  for (int m1 = 0; m1 < 4; ++m1)
+  for (int g = 0; g < 4; ++g)
 #pragma unroll
-    for (int j = 0; j < M; ++j) acc[m1][j] = warp_sum(acc[m1][j]);
+    for (int m1 = 0; m1 < 4; ++m1)
 #pragma unroll
-  for (int m1 = 0; m1 < 4; ++m1)
-#pragma unroll
-    for (int j = 0; j < M; ++j)
-      if (lane == m1 * M + j && j < mm) {
-        const int r = p.perm[q0 + j];  // route t*k + j' -> its weight w[r]
-        p.o_route[(size_t)(q0 + j) * p.H + rt * 128 + m0 + 32 * m1] = p.w[r] * gd * acc[m1][j];
+      for (int j = 0; j < M; ++j) {
+        const float v = warp_sum(acc[g][m1][j]);
+        if (lane == (g * 4 + m1) * M + j && j < mm) {
+          const int r = p.perm[q0 + j];  // route t*k + j' -> its weight w[r]
+          p.o_route[(size_t)(q0 + j) * p.H + rt * 128 + wid + 8 * g + 32 * m1] = p.w[r] * gd * v;
+        }
       }
 }
 
@@ -363,58 +455,62 @@ __device__ void down_shared_pass(const DecodeParams& p, int r0, int t0, int mm, 
 #pragma unroll
   for (int r = 0; r < 4; ++r) rows[r] = p.s_down + (size_t)(r0 + r) * p.Is;
   float acc[4][M];
-  warp_rows_bf16<M, 4>(rows, p.Is, hs, acc);
+  warp_rows_bf16<M, 4>(rows, p.Is, 0, p.Is, hs, acc);
   const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int r = 0; r < 4; ++r)
 #pragma unroll
-    for (int j = 0; j < M; ++j)
-      if (lane == r * M + j && j < mm) p.o_shared[(size_t)(t0 + j) * p.H + r0 + r] = acc[r][j];
+    for (int j = 0; j < M; ++j) {
+      const float v = warp_sum(acc[r][j]);
+      if (lane == r * M + j && j < mm) p.o_shared[(size_t)(t0 + j) * p.H + r0 + r] = v;
+    }
 }
 
+template <int MAXM>
 __global__ void __launch_bounds__(kDecThreads) k_decode_down(DecodeParams p) {
-  extern __shared__ float hs[];
+  extern __shared__ __align__(16) unsigned char smem_raw[];
   const int wid = threadIdx.x >> 5;
   const int u = blockIdx.x;
-  if (u < p.n_routed_units) {
-    const int tiles = p.H / 128;
-    const int a = u / (tiles * 4), rem = u % (tiles * 4);
-    const int rt = rem >> 2, m0 = (rem & 3) * kDecWarps + wid;
-    int a0, a1;
-    group_range(p, a0, a1);
-    if (a0 + a >= a1) return;
-    const int e = p.act_list[a0 + a];
-    const int slot = (e >= 0 && e < p.E) ? p.src_slot[e] : -1;
-    if (slot < 0 || slot >= p.n_slots) return;  // reported by K-decode-gu
-    const uint8_t* rec = p.arena + (uint64_t)slot * p.rec_bytes;
-    const RecordLayout L(p.H, p.I);
-    const float gd = p.gscale[e * 3 + 2];
-    const int pb = p.offsets[e], pe = p.offsets[e + 1];
-    for (int q0 = pb; q0 < pe; q0 += p.maxm) {
-      const int mm = min(p.maxm, pe - q0);
-      const float* rows[2];
-      for (int j = 0; j < mm; ++j) rows[j] = p.h_route + (size_t)(q0 + j) * p.I;
-      __syncthreads();
-      stage_f32_rows(hs, rows, mm, p.I);
-      __syncthreads();
-      if (mm == 2) down_routed_pass<2>(p, L, rec, rt, m0, q0, mm, hs, gd);
-      else down_routed_pass<1>(p, L, rec, rt, m0, q0, mm, hs, gd);
-    }
-  } else {
-    if (p.group != 0 || p.Is == 0) return;
-    const int r0 = (u - p.n_routed_units) * (kDecWarps * 4) + wid * 4;
+  if (u < p.n_shared_units) {
+    float* hs = reinterpret_cast<float*>(smem_raw);
+    const int r0 = u * (kDecWarps * 4) + wid * 4;
     for (int t0 = 0; t0 < p.T; t0 += p.maxm) {
       const int mm = min(p.maxm, p.T - t0);
       const float* rows[2];
       for (int j = 0; j < mm; ++j) rows[j] = p.h_shared + (size_t)(t0 + j) * p.Is;
       __syncthreads();
-      stage_f32_rows(hs, rows, mm, p.Is);
+      stage_f32_to_f32(hs, rows, mm, p.Is);
       __syncthreads();
       if (r0 < p.H) {
-        if (mm == 2) down_shared_pass<2>(p, r0, t0, mm, hs);
+        if (MAXM == 2 && mm == 2) down_shared_pass<MAXM>(p, r0, t0, mm, hs);
         else down_shared_pass<1>(p, r0, t0, mm, hs);
       }
     }
+    return;
+  }
+  __half* hs = reinterpret_cast<__half*>(smem_raw);
+  const int ur = u - p.n_shared_units;
+  const int tiles = p.H / 128;
+  const int a = ur / tiles, rt = ur % tiles;
+  int a0, a1;
+  group_range(p, a0, a1);
+  if (a0 + a >= a1) return;
+  const int e = p.act_list[a0 + a];
+  const int slot = (e >= 0 && e < p.E) ? p.src_slot[e] : -1;
+  if (slot < 0 || slot >= p.n_slots) return;  // reported by K-decode-gu
+  const uint8_t* rec = p.arena + (uint64_t)slot * p.rec_bytes;
+  const RecordLayout L(p.H, p.I);
+  const float gd = p.gscale[e * 3 + 2];
+  const int pb = p.offsets[e], pe = p.offsets[e + 1];
+  for (int q0 = pb; q0 < pe; q0 += p.maxm) {
+    const int mm = min(p.maxm, pe - q0);
+    const float* rows[2];
+    for (int j = 0; j < mm; ++j) rows[j] = p.h_route + (size_t)(q0 + j) * p.I;
+    __syncthreads();
+    stage_f32_to_f16(hs, rows, mm, p.I);
+    __syncthreads();
+    if (MAXM == 2 && mm == 2) down_routed_pass<MAXM>(p, L, rec, rt, q0, mm, hs, gd);
+    else down_routed_pass<1>(p, L, rec, rt, q0, mm, hs, gd);
   }
 }
 
@@ -451,6 +547,9 @@ size_t decode_workspace_bytes(int T, int I, int k, int Is) {
   return ((size_t)T * k * I + (size_t)T * Is) * sizeof(float) + 256;
 }
 
+static size_t smem_f16(int maxm, int K) { return (size_t)maxm * (K / 32) * kHPad * sizeof(__half); }
+static size_t smem_f32(int maxm, int K) { return (size_t)maxm * (K / 32) * kXPad * sizeof(float); }
+
 moe_status decode_ffn(const moe_ffn_args* a, cudaStream_t s) {
   DecodeParams p;
   p.T = a->T; p.H = a->H; p.I = a->I; p.E = a->E; p.k = a->k; p.Is = a->Is;
@@ -476,23 +575,26 @@ moe_status decode_ffn(const moe_ffn_args* a, cudaStream_t s) {
   if (a->group > 0) max_act = a->n_stage < max_act ? a->n_stage : max_act;
   const bool shared = a->group == 0 && a->Is > 0;
   if (a->stages & MOE_STAGE_GATE_UP) {
-    p.n_routed_units = max_act * (a->I / 128) * 4;
-    int n_shared_units = shared ? (a->Is + kDecWarps * 4 - 1) / (kDecWarps * 4) : 0;
-    size_t smem = (size_t)p.maxm * (a->H / 32) * kXPad * sizeof(float);
-    int grid = p.n_routed_units + n_shared_units;
+    p.n_shared_units = shared ? a->Is / 8 : 0;
+    const int routed = max_act * (a->I / 128) * 4;
+    size_t smem = smem_f16(p.maxm, a->H);
+    if (shared && smem_f32(p.maxm, a->H) > smem) smem = smem_f32(p.maxm, a->H);
+    const int grid = p.n_shared_units + routed;
     if (grid > 0) {
-      k_decode_gu<<<grid, kDecThreads, smem, s>>>(p);
+      if (p.maxm == 2) k_decode_gu<2><<<grid, kDecThreads, smem, s>>>(p);
+      else k_decode_gu<1><<<grid, kDecThreads, smem, s>>>(p);
       MOE_CHECK_LAUNCH();
     }
   }
   if (a->stages & MOE_STAGE_DOWN) {
-    p.n_routed_units = max_act * (a->H / 128) * 4;
-    int n_shared_units = shared ? (a->H + kDecWarps * 4 - 1) / (kDecWarps * 4) : 0;
-    int kin = a->I > a->Is ? a->I : a->Is;
-    size_t smem = (size_t)p.maxm * (kin / 32) * kXPad * sizeof(float);
-    int grid = p.n_routed_units + n_shared_units;
+    p.n_shared_units = shared ? (a->H + kDecWarps * 4 - 1) / (kDecWarps * 4) : 0;
+    const int routed = max_act * (a->H / 128);
+    size_t smem = smem_f16(p.maxm, a->I);
+    if (shared && smem_f32(p.maxm, a->Is) > smem) smem = smem_f32(p.maxm, a->Is);
+    const int grid = p.n_shared_units + routed;
     if (grid > 0) {
-      k_decode_down<<<grid, kDecThreads, smem, s>>>(p);
+      if (p.maxm == 2) k_decode_down<2><<<grid, kDecThreads, smem, s>>>(p);
+      else k_decode_down<1><<<grid, kDecThreads, smem, s>>>(p);
       MOE_CHECK_LAUNCH();
     }
   }
@@ -500,13 +602,13 @@ moe_status decode_ffn(const moe_ffn_args* a, cudaStream_t s) {
 }
 
 moe_status decode_setup() {
-  // H up to 16384 with two staged tokens: 2 * 512 * 36 * 4 bytes
-  if (cudaFuncSetAttribute(k_decode_gu, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024) !=
-      cudaSuccess)
-    return MOE_ERR_CUDA;
-  if (cudaFuncSetAttribute(k_decode_down, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           160 * 1024) != cudaSuccess)
-    return MOE_ERR_CUDA;
+  // H up to 16384 with two staged tokens in fp32: 2 * 512 * 36 * 4 bytes
+  const void* fns[4] = {(const void*)k_decode_gu<1>, (const void*)k_decode_gu<2>,
+                        (const void*)k_decode_down<1>, (const void*)k_decode_down<2>};
+  for (const void* f : fns)
+    if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024) !=
+        cudaSuccess)
+      return MOE_ERR_CUDA;
   return MOE_OK;
 }
 
