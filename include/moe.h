@@ -201,9 +201,12 @@ moe_status expcache_lookup(const expcache* c, int layer, const int32_t* counts, 
  *   G = amax/(6*448), block scale e4m3_rne(amax_b/(6 G)), codes
  *   e2m1_rne(v/(s G))) and multiplied on the tcgen05 tensor cores (FP4 x FP4,
  *   fp32 accumulation in tensor memory); adds w[t][j] * o into y_acc[t]
- *   (fp32, caller-zeroed).
+ *   (fp32, caller-zeroed).  Experts are taken prefill_group at a time; every
+ *   active expert must be resident (a hit), group must be 0, and H and I must
+ *   be multiples of 256 (else MOE_ERR_UNSUPPORTED).
  * Shared expert (Is > 0, group 0 only): bf16 gate/up [Is][H], down [H][Is];
- *   writes o_shared[t] = shared(x_t) (fp32).
+ *   DECODE writes o_shared[t] = shared(x_t) (fp32); PREFILL adds it into
+ *   y_acc[t] (bf16 tensor-core GEMMs, h rounded to bf16).
  * stages (DECODE only): MOE_STAGE_GATE_UP computes h into the workspace,
  *   MOE_STAGE_DOWN consumes it; MOE_STAGE_ALL does both.
  */
@@ -224,6 +227,7 @@ typedef struct {
   const int32_t* perm;       /* device [T*k] (moe_permute)                            */
   const float* w;            /* device [T][k] routing weights (moe_route)            */
   int group, n_stage;        /* expert group walked by this call                     */
+  int prefill_group;         /* PREFILL: experts per launch group (<= 128; 0 = 128)  */
   int Is;                    /* shared expert intermediate size, 0 = none            */
   const void* s_gate;        /* device bf16 [Is][H]                                   */
   const void* s_up;          /* device bf16 [Is][H]                                   */

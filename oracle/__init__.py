@@ -63,9 +63,10 @@ def lib():
         L.oracle_expert.argtypes = [vp, i32, i32, vp, vp, i32, vp]
         L.oracle_shared.argtypes = [vp, vp, vp, i32, i32, vp, i32, vp]
         L.oracle_layer_forward.argtypes = [vp, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp,
-                                           vp, vp, vp, i32, vp, vp, vp, vp]
+                                           vp, vp, vp, i32, vp, vp, vp, vp, vp]
         L.oracle_layer_forward.restype = i32
         L.oracle_set_defect.argtypes = [i32]
+        L.oracle_quant_flip_delta.argtypes = [vp, i32, vp]
         _lib = L
         try:
             openmp = "omp_get_num_threads" in open(_SO, "rb").read().decode("latin1")
@@ -169,6 +170,14 @@ def nvfp4_quant(v):
     return codes, scales, float(G[0])
 
 
+def quant_flip_delta(v):
+    """Per-element rounding-boundary slack of the NVFP4 quantisation of v."""
+    v = np.ascontiguousarray(v, np.float32)
+    out = np.empty(v.shape[0], np.float64)
+    lib().oracle_quant_flip_delta(_p(v), v.shape[0], _p(out))
+    return out
+
+
 def expert(rec, H, I, g3, x, act_quant=False):
     x = np.ascontiguousarray(x, np.float64)
     o = np.empty(H, np.float64)
@@ -185,9 +194,12 @@ def shared(wg, wu, wd, x, round_h_bf16=False):
     return o
 
 
-def layer_forward(x, H, I, E, k, Wr, bias, records, g, shared_w=None, mode=0):
-    """y [T,H] fp64 plus ids, w, p_sel.  ``records`` maps expert id -> uint8
-    record array (a dict or a sequence with None for absent experts)."""
+def layer_forward(x, H, I, E, k, Wr, bias, records, g, shared_w=None, mode=0,
+                  return_bound=False):
+    """y [T,H] fp64 plus ids, w, p_sel (and, with return_bound, the
+    rounding-boundary slack [T,H] of the prefill numerics, zero in mode 0).
+    ``records`` maps expert id -> uint8 record array (a dict or a sequence
+    with None for absent experts)."""
     x = np.ascontiguousarray(x, np.uint16)
     T = x.shape[0]
     keep = []
@@ -199,6 +211,7 @@ def layer_forward(x, H, I, E, k, Wr, bias, records, g, shared_w=None, mode=0):
             keep.append(r)
             ptrs[e] = r.ctypes.data
     y = np.empty((T, H), np.float64)
+    bound = np.zeros((T, H), np.float64)
     ids = np.empty((T, k), np.int32)
     w = np.empty((T, k), np.float64)
     p = np.empty((T, k), np.float64)
@@ -208,7 +221,7 @@ def layer_forward(x, H, I, E, k, Wr, bias, records, g, shared_w=None, mode=0):
         _p(x), T, H, I, E, k, Is, _p(np.ascontiguousarray(Wr, np.float32)),
         _p(None if bias is None else np.ascontiguousarray(bias, np.float32)), ptrs,
         _p(np.ascontiguousarray(g, np.float32)), _p(sg), _p(su), _p(sd), mode,
-        _p(y), _p(ids), _p(w), _p(p))
+        _p(y), _p(ids), _p(w), _p(p), _p(bound))
     if rc:
         raise ValueError("oracle_layer_forward: a selected expert has no record")
-    return y, ids, w, p
+    return (y, ids, w, p, bound) if return_bound else (y, ids, w, p)

@@ -323,15 +323,85 @@ static void orc_act_quant(const float* v, int n, double* out) {
   free(scales);
 }
 
+/* Rounding-boundary slack of an NVFP4 quantisation.  Two implementations
+ * whose fp32 inputs differ in the last bits may round an element that sits
+ * next to a rounding boundary to either neighbour; both results are correct.
+ * delta[i] receives the largest change of element i's quantised value that
+ * such a flip can cause (0 when the element is not within relative FLIP_EPS
+ * of an E2M1 boundary and its block scale is not within FLIP_EPS of an E4M3
+ * boundary).  Same fp32 steps as oracle_nvfp4_quant. */
+#define FLIP_EPS 1e-4
+static void orc_quant_flip_delta(const float* v, int n, double* delta) {
+  static const double mids[7] = {0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0};
+  static const double lo_mag[7] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0};
+  static const double hi_mag[7] = {0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+  float amax = 0.0f;
+  for (int i = 0; i < n; ++i) {
+    float a = fabsf(v[i]);
+    if (a > amax) amax = a;
+  }
+  volatile float six448 = 2688.0f;
+  float G = (amax > 0.0f) ? amax / six448 : 1.0f;
+  for (int b = 0; b < n / 16; ++b) {
+    float ab = 0.0f;
+    for (int i = 0; i < 16; ++i) {
+      float a = fabsf(v[b * 16 + i]);
+      if (a > ab) ab = a;
+    }
+    volatile float sixG = 6.0f * G;
+    float t = ab / sixG;
+    unsigned s = oracle_e4m3_rne(t);
+    /* block scale near an E4M3 rounding boundary: the block may take the
+     * neighbouring scale, every value may move by up to its own size */
+    int scale_flip = 0;
+    for (unsigned c = 1; c <= 0x7E && !scale_flip; ++c) {
+      double mid = 0.5 * (g_e4m3[c - 1] + g_e4m3[c]);
+      if (fabs((double)t - mid) <= FLIP_EPS * mid) scale_flip = 1;
+    }
+    double sg = g_e4m3[s] * (double)G;
+    for (int i = 0; i < 16; ++i) {
+      double d = 0.0;
+      if (scale_flip) d = fabs((double)v[b * 16 + i]) + 6.0 * sg / 8.0;
+      else if (s != 0) {
+        double q = fabs((double)v[b * 16 + i]) / sg;
+        for (int j = 0; j < 7; ++j)
+          if (fabs(q - mids[j]) <= FLIP_EPS * mids[j]) d = (hi_mag[j] - lo_mag[j]) * sg;
+      }
+      delta[b * 16 + i] = d;
+    }
+  }
+}
+
+ORC_API void oracle_quant_flip_delta(const float* v, int n, double* delta) {
+  tables_init();
+  orc_quant_flip_delta(v, n, delta);
+}
+
+/* bf16 rounding slack: one bf16 step when the value lies within relative
+ * FLIP_EPS of a bf16 rounding midpoint */
+static double orc_bf16_flip_delta(double hv) {
+  float f = (float)hv;
+  uint32_t b;
+  memcpy(&b, &f, 4);
+  uint32_t lo = b & 0xFFFF0000u, hi = lo + 0x10000u;
+  float flo, fhi;
+  memcpy(&flo, &lo, 4);
+  memcpy(&fhi, &hi, 4);
+  double mid = 0.5 * ((double)flo + (double)fhi);
+  return (fabs(hv - mid) <= FLIP_EPS * fabs(mid)) ? fabs((double)fhi - (double)flo) : 0.0;
+}
+
 /* ------------------------------------------------------------------ experts */
 
 static double orc_silu(double g) { return g / (1.0 + exp(-g)); }
 
 /* One routed expert on one activation vector x [H] -> o [H].
  * act_quant != 0: prefill numerics (h rounded to fp32 and NVFP4-quantised
- * before the down projection; x must already be the quantised value). */
-ORC_API void oracle_expert(const uint8_t* rec, int H, int I, const float* g3, const double* x,
-                           int act_quant, double* o) {
+ * before the down projection; x must already be the quantised value).
+ * bound (nullable, act_quant only): bound[r] += wabs * sum_i |Wd[r][i]| *
+ * delta_i, the most that rounding-boundary flips of h can move o[r] * wabs. */
+static void orc_expert_impl(const uint8_t* rec, int H, int I, const float* g3, const double* x,
+                            int act_quant, double* o, double wabs, double* bound) {
   tables_init();
   orc_mat Mg = orc_matrix(rec, H, I, 0, g3);
   orc_mat Mu = orc_matrix(rec, H, I, 1, g3);
@@ -345,6 +415,15 @@ ORC_API void oracle_expert(const uint8_t* rec, int H, int I, const float* g3, co
   if (act_quant) {
     float* hf = (float*)malloc(sizeof(float) * (size_t)I);
     for (int i = 0; i < I; ++i) hf[i] = (float)h[i];
+    if (bound) {
+      double* delta = (double*)malloc(sizeof(double) * (size_t)I);
+      orc_quant_flip_delta(hf, I, delta);
+      for (int i = 0; i < I; ++i) {
+        if (delta[i] == 0.0) continue;
+        for (int r = 0; r < H; ++r) bound[r] += wabs * fabs(orc_w(&Md, r, i)) * delta[i];
+      }
+      free(delta);
+    }
     orc_act_quant(hf, I, h);
     free(hf);
   }
@@ -354,11 +433,17 @@ ORC_API void oracle_expert(const uint8_t* rec, int H, int I, const float* g3, co
   free(h);
 }
 
+ORC_API void oracle_expert(const uint8_t* rec, int H, int I, const float* g3, const double* x,
+                           int act_quant, double* o) {
+  orc_expert_impl(rec, H, I, g3, x, act_quant, o, 0.0, NULL);
+}
+
 /* Shared expert with bf16 weights gate/up [Is][H], down [H][Is].
  * round_h_bf16 != 0: h is rounded to bf16 (RNE) before the down projection. */
-ORC_API void oracle_shared(const uint16_t* wg, const uint16_t* wu, const uint16_t* wd, int H,
-                           int Is, const double* x, int round_h_bf16, double* o) {
+static void orc_shared_impl(const uint16_t* wg, const uint16_t* wu, const uint16_t* wd, int H,
+                            int Is, const double* x, int round_h_bf16, double* o, double* bound) {
   double* h = (double*)malloc(sizeof(double) * (size_t)Is);
+  double* hd = bound ? (double*)calloc((size_t)Is, sizeof(double)) : NULL;
   #pragma omp parallel for schedule(static)
   for (int i = 0; i < Is; ++i) {
     double g = 0.0, u = 0.0;
@@ -367,6 +452,7 @@ ORC_API void oracle_shared(const uint16_t* wg, const uint16_t* wu, const uint16_
       u += oracle_bf16(wu[(size_t)i * H + c]) * x[c];
     }
     double hv = orc_silu(g) * u;
+    if (hd) hd[i] = orc_bf16_flip_delta(hv);
     if (round_h_bf16) {
       float f = (float)hv;
       uint32_t b;
@@ -379,11 +465,21 @@ ORC_API void oracle_shared(const uint16_t* wg, const uint16_t* wu, const uint16_
   }
   #pragma omp parallel for schedule(static)
   for (int r = 0; r < H; ++r) {
-    double acc = 0.0;
-    for (int i = 0; i < Is; ++i) acc += oracle_bf16(wd[(size_t)r * Is + i]) * h[i];
+    double acc = 0.0, bd = 0.0;
+    for (int i = 0; i < Is; ++i) {
+      acc += oracle_bf16(wd[(size_t)r * Is + i]) * h[i];
+      if (hd && hd[i] != 0.0) bd += fabs(oracle_bf16(wd[(size_t)r * Is + i])) * hd[i];
+    }
     o[r] = acc;
+    if (bound) bound[r] += bd;
   }
   free(h);
+  free(hd);
+}
+
+ORC_API void oracle_shared(const uint16_t* wg, const uint16_t* wu, const uint16_t* wd, int H,
+                           int Is, const double* x, int round_h_bf16, double* o) {
+  orc_shared_impl(wg, wu, wd, H, Is, x, round_h_bf16, o, NULL);
 }
 
 /* -------------------------------------------------------------------- layer */
@@ -392,12 +488,15 @@ ORC_API void oracle_shared(const uint16_t* wg, const uint16_t* wu, const uint16_
  * for experts no token selects; selecting one returns 2).  g [E][3].
  * Shared weights may be NULL (Is == 0).  mode 0 = decode numerics, 1 =
  * prefill numerics (activation quantisation).  Outputs y [T][H] (fp64) and,
- * when non-NULL, ids/w/p_sel [T][k]. */
+ * when non-NULL, ids/w/p_sel [T][k] and, in mode 1, ybound [T][H]: the most
+ * that rounding-boundary flips of the intermediate quantisations (h to NVFP4,
+ * shared h to bf16) can move each output, for comparisons with another
+ * implementation of the same rounding steps. */
 ORC_API int oracle_layer_forward(const uint16_t* x, int T, int H, int I, int E, int k, int Is,
                                  const float* Wr, const float* bias, const uint8_t* const* rec,
                                  const float* g, const uint16_t* sg, const uint16_t* su,
                                  const uint16_t* sd, int mode, double* y, int32_t* ids_out,
-                                 double* w_out, double* p_out) {
+                                 double* w_out, double* p_out, double* ybound) {
   tables_init();
   int32_t* ids = (int32_t*)malloc(sizeof(int32_t) * (size_t)T * k);
   double* w = (double*)malloc(sizeof(double) * (size_t)T * k);
@@ -417,16 +516,18 @@ ORC_API int oracle_layer_forward(const uint16_t* x, int T, int H, int I, int E, 
     if (mode == 1) orc_act_quant(xf, H, xq);
     else memcpy(xq, xd, sizeof(double) * (size_t)H);
     double* yt = y + (size_t)t * H;
+    double* bt = (ybound && mode == 1) ? ybound + (size_t)t * H : NULL;
+    if (ybound) for (int c = 0; c < H; ++c) ybound[(size_t)t * H + c] = 0.0;
     for (int c = 0; c < H; ++c) yt[c] = 0.0;
     for (int j = 0; j < k; ++j) {
       int e = ids[(size_t)t * k + j];
-      oracle_expert(rec[e], H, I, g + 3 * e, xq, mode == 1, o);
       double wj = w[(size_t)t * k + j];
+      orc_expert_impl(rec[e], H, I, g + 3 * e, xq, mode == 1, o, fabs(wj), bt);
       if (g_defect == ORC_DEFECT_SCALING_2_5) wj *= 2.5;
       for (int c = 0; c < H; ++c) yt[c] += wj * o[c];
     }
     if (Is > 0 && sg && su && sd) {
-      oracle_shared(sg, su, sd, H, Is, xd, mode == 1, o);
+      orc_shared_impl(sg, su, sd, H, Is, xd, mode == 1, o, bt);
       for (int c = 0; c < H; ++c) yt[c] += o[c];
     }
   }

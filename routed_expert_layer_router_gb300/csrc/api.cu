@@ -233,6 +233,7 @@ MOE_API moe_status moe_layer_forward(moe_layer* l, const void* x, int T, void* y
   fa.src_slot = l->src_slot; fa.act_list = l->act_list; fa.n_act = l->n_act;
   fa.offsets = l->offsets; fa.pad_offsets = l->pad_offsets; fa.perm = l->perm; fa.w = l->w;
   fa.n_stage = n_stage;
+  fa.prefill_group = d.prefill_group;
   fa.Is = d.Is; fa.s_gate = d.s_gate; fa.s_up = d.s_up; fa.s_down = d.s_down;
   fa.o_route = l->o_route; fa.o_shared = d.Is > 0 ? l->o_shared : nullptr;
   fa.y_acc = l->y_acc;
@@ -257,7 +258,7 @@ MOE_API moe_status moe_layer_forward(moe_layer* l, const void* x, int T, void* y
   ca.y_acc = prefill ? l->y_acc : nullptr;
   ca.o_route = prefill ? nullptr : l->o_route;
   ca.inv = l->inv;
-  ca.o_shared = d.Is > 0 ? l->o_shared : nullptr;
+  ca.o_shared = (d.Is > 0 && !prefill) ? l->o_shared : nullptr;  // prefill adds it into y_acc
   ca.y = y;
   if ((st = moe_combine(&ca, stream)) != MOE_OK) return st;
   l->last_T = T;

@@ -1,18 +1,728 @@
-// prefill.cu - prefill path (tcgen05 NVFP4 grouped GEMM); filled in below.
+// prefill.cu - the prefill path: many tokens per expert, so the expert FFN is
+// a grouped GEMM on the tcgen05 tensor cores.
+//
+//   K-actq   each route's token quantised to NVFP4 (E2M1 codes, E4M3 scale per
+//            16 values, fp32 global per row) into an expert-sorted staging
+//            layout whose segments are padded to 128 rows;
+//   K-gemm   per (expert, 128 weight rows, 128 routes) tile:
+//            D[rows, routes] = W[rows, K] . Xq[routes, K]^T with
+//            tcgen05.mma kind::mxf4nvf4 (block scale, 16-value E4M3 scales in
+//            tensor memory), fp32 accumulators in tensor memory; TMA tile loads
+//            of both operands (one 3-D tensor map spans the whole slot arena, so
+//            every expert record is addressed by its slot), 4-stage mbarrier
+//            pipeline, one warp loading, one warp issuing MMAs, four warps in the
+//            epilogue.  Gate and up share the activation tile and accumulate
+//            into two TMEM accumulators; the epilogue forms silu(g)*u.
+//   K-hq     h quantised to NVFP4 per route, same layout as K-actq;
+//   K-gemm   down projection; the epilogue scales by the routing weight and
+//            adds each route's 128-value row segment into y_acc[token] with
+//            TMA bulk reductions (the weighted combine).
+// The bf16 shared expert runs through the same GEMM with kind::f16.
+// Experts are walked in groups (64 by default) in act_list order.
+// Sources: Strata-GLM blog, "Day one" list (chunked prefill: each layer's
+// experts run as one batched matrix multiply per chunk); dev.to page,
+// "Prefill in groups of 64 experts"; "Project Maya" page, "440 tokens a
+// second of prefill" (a prompt chunk touches nearly every expert).
+#include <cudaTypedefs.h>
+#include <cuda_fp16.h>
+#include <string.h>
+
 #include "common.cuh"
+#include "sm100_ptx.cuh"
 
 namespace moe {
 
-size_t prefill_workspace_bytes(int T, int H, int I, int E, int k, int Is) {
-  (void)T; (void)H; (void)I; (void)E; (void)k; (void)Is;
-  return 256;
+const uint8_t* cache_arena(const expcache* c);
+uint64_t cache_rec_bytes(const expcache* c);
+int cache_n_cache(const expcache* c);
+int cache_n_stage(const expcache* c);
+
+namespace pf {
+
+constexpr int kTileM = 128, kTileN = 128, kStageKB = 128;  // K bytes per stage and operand row
+constexpr int kStages = 4;
+constexpr int kThreads = 192;  // warp 0: TMA, warp 1: MMA, warps 2..5: epilogue
+constexpr int kMaxGroup = 128; // experts per launch (prefix table in shared memory)
+constexpr uint64_t kWaitNs = 2000000000ull;  // no wait lasts longer than 2 s
+constexpr uint32_t kTmemCols = 512;
+
+enum Epi { EPI_GU_ROUTED = 0, EPI_GU_SHARED = 1, EPI_DOWN_ROUTED = 2, EPI_DOWN_SHARED = 3 };
+
+struct GemmParams {
+  int mtiles;   // 128-row weight tiles per expert
+  int kstages;  // K / (128 bytes of each operand row)
+  // routed experts of this launch: act_list[g0 .. g1) clipped to n_act[1] (hits)
+  const int32_t* act_list;
+  const int32_t* n_act;
+  int g0, g1;
+  const int32_t* src_slot;
+  const int32_t* offsets;
+  const int32_t* pad_offsets;
+  const int32_t* perm;
+  const float* gscale;
+  const float* w;
+  int k;
+  int n_slots;
+  // shared expert: T activation rows
+  int T;
+  // block scales
+  const uint8_t* arena;
+  uint64_t rec_bytes;
+  uint64_t sfa_off0, sfa_off1;  // offsets of the A matrices' scales in a record
+  int kgroups;                  // K / 64 (scale atoms per 128-row tile row)
+  const uint8_t* b_scales;      // activation scale atoms
+  const float* b_gscale;        // activation per-row global scales
+  // outputs
+  float* h32;       int h_ld;   // routed gate/up: h [rows][I]
+  uint16_t* hs;     int hs_ld;  // shared gate/up: h [T][Is] bf16
+  float* y_acc;     int H;      // down: y_acc [T][H]
+  int32_t* status;
+};
+
+// ---- tile schedule ------------------------------------------------------------
+struct Sched {
+  int n;                     // experts in this launch
+  int e[kMaxGroup];
+  int slot[kMaxGroup];
+  int ntiles[kMaxGroup];     // 128-route column tiles of the expert
+  int tile_begin[kMaxGroup + 1];
+};
+
+// tile t -> (expert index j, m tile, n tile); returns false past the end
+__device__ __forceinline__ bool tile_coords(const Sched& S, int mtiles, int t, int& j, int& mt,
+                                            int& nt) {
+  if (t >= S.tile_begin[S.n]) return false;
+  int lo = 0, hi = S.n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (S.tile_begin[mid] <= t) lo = mid; else hi = mid - 1;
+  }
+  j = lo;
+  const int local = t - S.tile_begin[j];
+  mt = local / S.ntiles[j];
+  nt = local % S.ntiles[j];
+  (void)mtiles;
+  return true;
 }
+
+template <int KIND, int EPI>
+struct Cfg {
+  static constexpr bool kDual = (EPI == EPI_GU_ROUTED || EPI == EPI_GU_SHARED);
+  static constexpr bool kRouted = (EPI == EPI_GU_ROUTED || EPI == EPI_DOWN_ROUTED);
+  static constexpr bool kNvf4 = (KIND == 0);
+  static constexpr int kTileBytes = kTileM * kStageKB;  // 16 KiB
+  static constexpr int kSfBytes = kNvf4 ? 2048 : 0;     // 4 atoms of 512 B
+  static constexpr int kStageBytes =
+      kTileBytes * (kDual ? 3 : 2) + kSfBytes * (kDual ? 3 : 2);
+  static constexpr int kEpiStage = (EPI == EPI_DOWN_ROUTED || EPI == EPI_DOWN_SHARED)
+                                       ? kTileN * kTileM * 4 : 0;  // fp32 [routes][rows]
+  static constexpr int kSmem = 1024 + kStages * kStageBytes + kEpiStage;
+  // tensor memory: accumulators, then per-stage scale-factor columns
+  static constexpr uint32_t kAccCols = kDual ? 256 : 128;
+  static constexpr uint32_t kSfColsPerStage = kNvf4 ? (kDual ? 48 : 32) : 0;
+};
+
+__device__ __forceinline__ float silu_f(float g) { return g / (1.f + expf(-g)); }
+
+template <int KIND, int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
+           const __grid_constant__ CUtensorMap tmB, GemmParams p) {
+  using C = Cfg<KIND, EPI>;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  __shared__ uint64_t full_bar[kStages], empty_bar[kStages], acc_full, acc_empty;
+  __shared__ uint32_t tmem_base;
+  __shared__ int abort_flag;
+  __shared__ Sched S;
+  __shared__ float col_scale[kTileN];
+  __shared__ int col_row[kTileN];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // ---- schedule: the experts of this launch and their tile ranges
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    int n = 0, acc = 0;
+    if (C::kRouted) {
+      const int hits = p.n_act[1];
+      // the prefill path reads every active expert from a cache slot
+      if (p.n_act[0] != hits && blockIdx.x == 0) set_status(p.status, MOE_ERR_DEVICE);
+      const int g1 = min(p.g1, hits);
+      for (int g = p.g0; g < g1 && n < kMaxGroup; ++g) {
+        const int e = p.act_list[g];
+        const int cnt = p.offsets[e + 1] - p.offsets[e];
+        const int slot = p.src_slot[e];
+        if (cnt <= 0) continue;
+        if (slot < 0 || slot >= p.n_slots) {
+          set_status(p.status, MOE_ERR_DEVICE);
+          continue;
+        }
+        S.e[n] = e;
+        S.slot[n] = slot;
+        S.ntiles[n] = (cnt + kTileN - 1) / kTileN;
+        S.tile_begin[n] = acc;
+        acc += S.ntiles[n] * p.mtiles;
+        ++n;
+      }
+    } else {
+      S.e[0] = 0;
+      S.slot[0] = 0;
+      S.ntiles[0] = (p.T + kTileN - 1) / kTileN;
+      S.tile_begin[0] = 0;
+      acc = S.ntiles[0] * p.mtiles;
+      n = 1;
+    }
+    S.n = n;
+    S.tile_begin[n] = acc;
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(&full_bar[s], 1);
+      ptx::mbar_init(&empty_bar[s], 1);
+    }
+    ptx::mbar_init(&acc_full, 1);
+    ptx::mbar_init(&acc_empty, 4);
+    ptx::fence_barrier_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(&tmem_base, kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = tmem_base;
+  const int n_tiles = S.tile_begin[S.n];
+
+  if (warp == 0) {
+    // ================= TMA producer =================
+    if (lane == 0) {
+      uint32_t g = 0;
+      for (int t = blockIdx.x; t < n_tiles && !abort_flag; t += gridDim.x) {
+        int j, mt, nt;
+        tile_coords(S, p.mtiles, t, j, mt, nt);
+        const int e = S.e[j];
+        int brow = nt * kTileN;  // activation row of the tile
+        if (C::kRouted) brow += p.pad_offsets[e];
+        for (int kb = 0; kb < p.kstages; ++kb, ++g) {
+          const int s = g % kStages;
+          const uint32_t ph = (g / kStages) & 1;
+          if (!ptx::mbar_wait(&empty_bar[s], ph ^ 1, kWaitNs)) {
+            set_status(p.status, MOE_ERR_TIMEOUT);
+            abort_flag = 1;
+            break;
+          }
+          unsigned char* st = smem + (size_t)s * C::kStageBytes;
+          ptx::mbar_arrive_expect_tx(&full_bar[s], C::kStageBytes);
+          const int kc = C::kNvf4 ? kb * kStageKB : kb * (kStageKB / 2);  // bytes or bf16s
+          if (C::kRouted) {
+            ptx::tma_load_3d(st, &tmA0, kc, mt * kTileM, S.slot[j], &full_bar[s]);
+            if (C::kDual)
+              ptx::tma_load_3d(st + C::kTileBytes, &tmA1, kc, mt * kTileM, S.slot[j],
+                               &full_bar[s]);
+          } else {
+            ptx::tma_load_2d(st, &tmA0, kc, mt * kTileM, &full_bar[s]);
+            if (C::kDual) ptx::tma_load_2d(st + C::kTileBytes, &tmA1, kc, mt * kTileM, &full_bar[s]);
+          }
+          unsigned char* bdst = st + C::kTileBytes * (C::kDual ? 2 : 1);
+          ptx::tma_load_2d(bdst, &tmB, kc, brow, &full_bar[s]);
+          if (C::kNvf4) {
+            // 4 scale atoms (512 B each) per operand: k groups kb*4 .. kb*4+3
+            unsigned char* sf = bdst + C::kTileBytes;
+            const uint8_t* rec = p.arena + (uint64_t)S.slot[j] * p.rec_bytes;
+            const uint64_t aoff = ((uint64_t)mt * p.kgroups + (uint64_t)kb * 4) * 512;
+            ptx::bulk_load(sf, rec + p.sfa_off0 + aoff, 2048, &full_bar[s]);
+            if (C::kDual) ptx::bulk_load(sf + 2048, rec + p.sfa_off1 + aoff, 2048, &full_bar[s]);
+            const uint64_t boff = ((uint64_t)(brow / kTileN) * p.kgroups + (uint64_t)kb * 4) * 512;
+            ptx::bulk_load(sf + (C::kDual ? 4096 : 2048), p.b_scales + boff, 2048, &full_bar[s]);
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ================= MMA issuer =================
+    if (lane == 0) {
+      // instruction descriptor: M = 128, N = 128, K-major A and B
+      uint32_t idesc = ((uint32_t)(kTileN >> 3) << 17) | ((uint32_t)(kTileM >> 4) << 24);
+      if (C::kNvf4) idesc |= (1u << 7) | (1u << 10);               // E2M1 x E2M1, UE4M3 scales
+      else idesc |= (1u << 4) | (1u << 7) | (1u << 10);            // fp32 D, bf16 A and B
+      uint32_t g = 0, it = 0;
+      for (int t = blockIdx.x; t < n_tiles && !abort_flag; t += gridDim.x, ++it) {
+        if (!ptx::mbar_wait(&acc_empty, (it & 1) ^ 1, kWaitNs)) {
+          set_status(p.status, MOE_ERR_TIMEOUT);
+          abort_flag = 1;
+          break;
+        }
+        ptx::tc_fence_after();
+        bool ok = true;
+        for (int kb = 0; kb < p.kstages; ++kb, ++g) {
+          const int s = g % kStages;
+          const uint32_t ph = (g / kStages) & 1;
+          if (!ptx::mbar_wait(&full_bar[s], ph, kWaitNs)) {
+            set_status(p.status, MOE_ERR_TIMEOUT);
+            abort_flag = 1;
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          unsigned char* st = smem + (size_t)s * C::kStageBytes;
+          const uint32_t a0 = ptx::smem_u32(st);
+          const uint32_t a1 = a0 + C::kTileBytes;
+          const uint32_t b = a0 + C::kTileBytes * (C::kDual ? 2 : 1);
+          const uint32_t sf = b + C::kTileBytes;
+          const uint32_t sfcol = C::kAccCols + (uint32_t)s * C::kSfColsPerStage;
+          if (C::kNvf4) {
+            // scale atoms -> tensor memory (4 columns each)
+            for (int kk = 0; kk < 4; ++kk) {
+              const int nops = C::kDual ? 3 : 2;
+              for (int o = 0; o < nops; ++o) {
+                const uint64_t d = ptx::smem_desc(sf + o * 2048 + kk * 512, 128, 128, 0);
+                ptx::tmem_cp_32x128b_x4(tmem + sfcol + o * 16 + kk * 4, d);
+              }
+            }
+          }
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t da0 = ptx::smem_desc(a0 + kk * 32, 16, 1024, 2);
+            const uint64_t db = ptx::smem_desc(b + kk * 32, 16, 1024, 2);
+            const bool accum = (kb > 0) || (kk > 0);
+            if (C::kNvf4) {
+              const uint32_t sfb = tmem + sfcol + (C::kDual ? 32 : 16) + kk * 4;
+              ptx::mma_nvf4(tmem, da0, db, idesc, tmem + sfcol + kk * 4, sfb, accum);
+              if (C::kDual) {
+                const uint64_t da1 = ptx::smem_desc(a1 + kk * 32, 16, 1024, 2);
+                ptx::mma_nvf4(tmem + 128, da1, db, idesc, tmem + sfcol + 16 + kk * 4, sfb, accum);
+              }
+            } else {
+              ptx::mma_bf16(tmem, da0, db, idesc, accum);
+              if (C::kDual) {
+                const uint64_t da1 = ptx::smem_desc(a1 + kk * 32, 16, 1024, 2);
+                ptx::mma_bf16(tmem + 128, da1, db, idesc, accum);
+              }
+            }
+          }
+          ptx::tc_commit(&empty_bar[s]);  // stage reusable once these MMAs finish
+        }
+        if (!ok) break;
+        ptx::tc_commit(&acc_full);
+      }
+    }
+  } else {
+    // ================= epilogue (warps 2..5) =================
+    const int q = warp & 3;             // tensor-memory lane quarter of this warp
+    const int row = q * 32 + lane;      // weight row within the tile
+    const int et = threadIdx.x - 64;    // 0..127
+    float* stage_out = reinterpret_cast<float*>(smem + (size_t)kStages * C::kStageBytes);
+    uint32_t it = 0;
+    for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++it) {
+      int j, mt, nt;
+      tile_coords(S, p.mtiles, t, j, mt, nt);
+      const int e = S.e[j];
+      int n_valid, col0;
+      if (C::kRouted) {
+        const int cnt = p.offsets[e + 1] - p.offsets[e];
+        n_valid = min(kTileN, cnt - nt * kTileN);
+        col0 = p.pad_offsets[e] + nt * kTileN;  // padded activation row of column 0
+      } else {
+        n_valid = min(kTileN, p.T - nt * kTileN);
+        col0 = nt * kTileN;
+      }
+      // per-column data (column = route or token)
+      if (et < kTileN) {
+        float sc = 1.f;
+        int rr = col0 + et;
+        if (et < n_valid) {
+          if (EPI == EPI_GU_ROUTED) {
+            sc = p.b_gscale[col0 + et];
+          } else if (EPI == EPI_DOWN_ROUTED) {
+            const int route = p.perm[p.offsets[e] + nt * kTileN + et];
+            sc = p.b_gscale[col0 + et] * p.w[route] * p.gscale[e * 3 + 2];
+            rr = route / p.k;  // token
+          }
+        }
+        col_scale[et] = sc;
+        col_row[et] = rr;
+      }
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      if (!ptx::mbar_wait(&acc_full, it & 1, kWaitNs)) {
+        set_status(p.status, MOE_ERR_TIMEOUT);
+        abort_flag = 1;
+        break;
+      }
+      ptx::tc_fence_after();
+      const uint32_t lane_addr = tmem + ((uint32_t)(q * 32) << 16);
+      float gg = 1.f, gu = 1.f;
+      if (EPI == EPI_GU_ROUTED) {
+        gg = p.gscale[e * 3 + 0];
+        gu = p.gscale[e * 3 + 1];
+      }
+      for (int c0 = 0; c0 < kTileN; c0 += 32) {
+        uint32_t r0[32], r1[32];
+        ptx::tmem_ld_32x32b_x32(lane_addr + c0, r0);
+        if (C::kDual) ptx::tmem_ld_32x32b_x32(lane_addr + 128 + c0, r1);
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) {
+          const int n = c0 + jj;
+          const float a = __uint_as_float(r0[jj]);
+          if (EPI == EPI_GU_ROUTED) {
+            if (n < n_valid) {
+              const float G = col_scale[n];
+              const float gv = a * gg * G, uv = __uint_as_float(r1[jj]) * gu * G;
+              p.h32[(size_t)(col0 + n) * p.h_ld + mt * kTileM + row] = silu_f(gv) * uv;
+            }
+          } else if (EPI == EPI_GU_SHARED) {
+            if (n < n_valid) {
+              const float hv = silu_f(a) * __uint_as_float(r1[jj]);
+              p.hs[(size_t)(col0 + n) * p.hs_ld + mt * kTileM + row] = f32_to_bf16_rne(hv);
+            }
+          } else {
+            stage_out[n * kTileM + row] = a * col_scale[n];
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      if (lane == 0) ptx::mbar_arrive(&acc_empty);
+      if (EPI == EPI_DOWN_ROUTED || EPI == EPI_DOWN_SHARED) {
+        ptx::fence_proxy_async_smem();
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        if (et < n_valid) {
+          ptx::bulk_reduce_add_f32(p.y_acc + (size_t)col_row[et] * p.H + mt * kTileM,
+                                   stage_out + et * kTileM, kTileM * 4);
+          ptx::bulk_commit();
+          ptx::bulk_wait_read0();
+        }
+      }
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+    }
+    if (EPI == EPI_DOWN_ROUTED || EPI == EPI_DOWN_SHARED) ptx::bulk_wait0();
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---- NVFP4 activation quantisation -------------------------------------------------
+// nearest E2M1 magnitude of |q| (ties to the even code), saturating at 6; the
+// sign bit is the sign bit of q
+__device__ __forceinline__ uint32_t e2m1_rne_sat(float q) {
+  const float a = fabsf(q);
+  uint32_t c;
+  if (a < 0.25f) c = 0;
+  else if (a == 0.25f) c = 0;
+  else if (a < 0.75f) c = 1;
+  else if (a == 0.75f) c = 2;
+  else if (a < 1.25f) c = 2;
+  else if (a == 1.25f) c = 2;
+  else if (a < 1.75f) c = 3;
+  else if (a == 1.75f) c = 4;
+  else if (a < 2.5f) c = 4;
+  else if (a == 2.5f) c = 4;
+  else if (a < 3.5f) c = 5;
+  else if (a == 3.5f) c = 6;
+  else if (a < 5.f) c = 6;
+  else if (a == 5.f) c = 6;
+  else c = 7;
+  return (__float_as_uint(q) >> 31) ? (c | 8u) : c;
+}
+
+// E4M3 (round to nearest even, saturating to 448) of t >= 0, and its value
+__device__ __forceinline__ uint32_t e4m3_rne(float t) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.f), "f"(t));
+  return r & 0xFFu;
+}
+__device__ __forceinline__ float e4m3_value(uint32_t b) {
+  return f16_lo(e4m3x2_to_f16x2(b & 0xFFu));
+}
+
+struct QuantParams {
+  int K;                    // values per row
+  int g0, g1;               // act_list range (routed)
+  const int32_t* act_list;
+  const int32_t* n_act;
+  const int32_t* offsets;
+  const int32_t* pad_offsets;
+  const int32_t* perm;
+  int k;
+  const uint16_t* x;        // source rows (bf16 tokens) or
+  const float* h32;         // source rows (fp32 h, indexed by padded row)
+  uint8_t* codes;           // [rows][K/2]
+  uint8_t* scales;          // atoms [rows/128][K/64][512]
+  float* G;                 // [rows]
+};
+
+// one warp per padded row of the experts in act_list[g0, g1) (hits only)
+template <bool FROM_H>
+__global__ void __launch_bounds__(256) k_quant_rows(QuantParams p) {
+  __shared__ int s_n, s_pad[kMaxGroup + 1], s_e[kMaxGroup];
+  if (threadIdx.x == 0) {
+    const int g1 = min(p.g1, p.n_act[1]);
+    int n = 0;
+    for (int g = p.g0; g < g1 && n < kMaxGroup; ++g) s_e[n++] = p.act_list[g];
+    s_n = n;
+  }
+  __syncthreads();
+  for (int j = threadIdx.x; j < s_n; j += blockDim.x) s_pad[j] = p.pad_offsets[s_e[j]];
+  __syncthreads();
+  const int n_exp = s_n;
+  const int lane = threadIdx.x & 31;
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  const int KB = p.K / 16, KG = p.K / 64;
+  // rows of every expert of the launch, expert by expert
+  int total = 0;
+  for (int j = 0; j < n_exp; ++j)
+    total += p.pad_offsets[s_e[j] + 1] - s_pad[j];
+  for (int wr = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; wr < total; wr += warps) {
+    int j = 0, base = 0;
+    while (true) {
+      const int len = p.pad_offsets[s_e[j] + 1] - s_pad[j];
+      if (wr < base + len) break;
+      base += len;
+      ++j;
+    }
+    const int e = s_e[j];
+    const int local = wr - base;
+    const int row = s_pad[j] + local;
+    const int cnt = p.offsets[e + 1] - p.offsets[e];
+    const bool valid = local < cnt;
+    const int rt = row >> 7, m0 = row & 31, m1 = (row & 127) >> 5;
+    if (!valid) {
+      for (int b = lane; b < KB; b += 32) {
+        *reinterpret_cast<uint2*>(p.codes + (size_t)row * (p.K / 2) + (size_t)b * 8) =
+            make_uint2(0u, 0u);
+        p.scales[((size_t)rt * KG + (b >> 2)) * 512 + m0 * 16 + m1 * 4 + (b & 3)] = 0;
+      }
+      if (lane == 0) p.G[row] = 0.f;
+      continue;
+    }
+    // source row
+    const uint16_t* xr = nullptr;
+    const float* hr = nullptr;
+    if (FROM_H) hr = p.h32 + (size_t)row * p.K;
+    else xr = p.x + (size_t)(p.perm[p.offsets[e] + local] / p.k) * p.K;
+    // row amax
+    float amax = 0.f;
+    for (int i = lane; i < p.K; i += 32) {
+      const float v = FROM_H ? hr[i] : __uint_as_float((uint32_t)xr[i] << 16);
+      amax = fmaxf(amax, fabsf(v));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    const float G = amax > 0.f ? __fdiv_rn(amax, 2688.0f) : 1.0f;
+    const float sixG = __fmul_rn(6.0f, G);
+    for (int b = lane; b < KB; b += 32) {
+      float v[16];
+      if (FROM_H) {
+#pragma unroll
+        for (int i = 0; i < 16; i += 4) {
+          const float4 t = *reinterpret_cast<const float4*>(hr + b * 16 + i);
+          v[i] = t.x; v[i + 1] = t.y; v[i + 2] = t.z; v[i + 3] = t.w;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; i += 2) {
+          const uint32_t t = *reinterpret_cast<const uint32_t*>(xr + b * 16 + i);
+          v[i] = bf16_lo(t);
+          v[i + 1] = bf16_hi(t);
+        }
+      }
+      float ab = 0.f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) ab = fmaxf(ab, fabsf(v[i]));
+      const uint32_t s = e4m3_rne(__fdiv_rn(ab, sixG));
+      const float sdq = __fmul_rn(e4m3_value(s), G);
+      uint32_t lo = 0, hi = 0;
+      if (s != 0) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint32_t c0 = e2m1_rne_sat(__fdiv_rn(v[2 * i], sdq));
+          const uint32_t c1 = e2m1_rne_sat(__fdiv_rn(v[2 * i + 1], sdq));
+          const uint32_t byte = c0 | (c1 << 4);
+          if (i < 4) lo |= byte << (8 * i);
+          else hi |= byte << (8 * (i - 4));
+        }
+      }
+      *reinterpret_cast<uint2*>(p.codes + (size_t)row * (p.K / 2) + (size_t)b * 8) =
+          make_uint2(lo, hi);
+      p.scales[((size_t)rt * KG + (b >> 2)) * 512 + m0 * 16 + m1 * 4 + (b & 3)] = (uint8_t)s;
+    }
+    if (lane == 0) p.G[row] = G;
+  }
+}
+
+// ---- host side ---------------------------------------------------------------------
+static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+static moe_status load_encoder() {
+  if (g_encode) return MOE_OK;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                       &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !fn)
+    return MOE_ERR_CUDA;
+  g_encode = (PFN_cuTensorMapEncodeTiled_v12000)fn;
+  return MOE_OK;
+}
+
+// rows of `inner` elements (uint8 codes or bf16), box = 128 bytes x 128 rows,
+// 128-byte swizzle; optional third dimension (slots)
+static moe_status make_map(CUtensorMap* m, const void* base, bool bf16, uint64_t inner,
+                           uint64_t rows, uint64_t row_stride_bytes, uint64_t slots,
+                           uint64_t slot_stride_bytes) {
+  cuuint64_t dims[3] = {inner, rows, slots};
+  cuuint64_t strides[2] = {row_stride_bytes, slot_stride_bytes};
+  cuuint32_t box[3] = {bf16 ? 64u : 128u, 128u, 1u};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  const cuuint32_t rank = slots > 0 ? 3 : 2;
+  CUresult r = g_encode(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                        rank, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// workspace layout for a prefill call on T tokens
+struct PrefillWs {
+  size_t rows;  // padded rows
+  size_t xq_codes, xq_scales, xq_G, h32, hq_codes, hq_scales, hq_G, hs, total;
+  PrefillWs(int T, int H, int I, int E, int k, int Is) {
+    rows = (((size_t)T * k + (size_t)E * (kTileN - 1)) + kTileN - 1) / kTileN * kTileN;
+    size_t o = 0;
+    auto take = [&](size_t b) { size_t r = o; o += (b + 1023) & ~(size_t)1023; return r; };
+    xq_codes = take(rows * H / 2);
+    xq_scales = take(rows * H / 16);
+    xq_G = take(rows * 4);
+    h32 = take(rows * I * 4);
+    hq_codes = take(rows * I / 2);
+    hq_scales = take(rows * I / 16);
+    hq_G = take(rows * 4);
+    hs = take((size_t)T * Is * 2);
+    total = o + 1024;
+  }
+};
+
+template <int KIND, int EPI>
+static moe_status launch_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b,
+                              const GemmParams& p, cudaStream_t s) {
+  using C = Cfg<KIND, EPI>;
+  static bool attr = false;
+  if (!attr) {
+    if (cudaFuncSetAttribute(k_gemm<KIND, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::kSmem) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    attr = true;
+  }
+  k_gemm<KIND, EPI><<<kSMs, kThreads, C::kSmem, s>>>(a0, a1, b, p);
+  MOE_CHECK_LAUNCH();
+  return MOE_OK;
+}
+
+}  // namespace pf
+
+size_t prefill_workspace_bytes(int T, int H, int I, int E, int k, int Is) {
+  return pf::PrefillWs(T, H, I, E, k, Is).total;
+}
+
+moe_status prefill_setup() { return pf::load_encoder(); }
 
 moe_status prefill_ffn(const moe_ffn_args* a, cudaStream_t s) {
-  (void)a; (void)s;
-  return MOE_ERR_UNSUPPORTED;
-}
+  using namespace pf;
+  if (a->H % 256 || a->I % 256 || a->Is % 128 || a->group != 0) return MOE_ERR_UNSUPPORTED;
+  moe_status st = load_encoder();
+  if (st != MOE_OK) return st;
+  const PrefillWs W(a->T, a->H, a->I, a->E, a->k, a->Is);
+  uint8_t* ws = (uint8_t*)(((uintptr_t)a->workspace + 1023) & ~(uintptr_t)1023);
+  const RecordLayout L(a->H, a->I);
+  const uint8_t* arena = cache_arena(a->cache);
+  const uint64_t rb = cache_rec_bytes(a->cache);
+  const int n_slots = cache_n_cache(a->cache) + cache_n_stage(a->cache);
+  const int H = a->H, I = a->I;
 
-moe_status prefill_setup() { return MOE_OK; }
+  // tensor maps: weights of every slot; staged activations; shared expert
+  CUtensorMap mg, mu, md, mxq, mhq, msg, msu, msd, mx, mhs;
+  if ((st = make_map(&mg, arena + L.gate_codes, false, H / 2, I, H / 2, n_slots, rb)) ||
+      (st = make_map(&mu, arena + L.up_codes, false, H / 2, I, H / 2, n_slots, rb)) ||
+      (st = make_map(&md, arena + L.down_codes, false, I / 2, H, I / 2, n_slots, rb)) ||
+      (st = make_map(&mxq, ws + W.xq_codes, false, H / 2, W.rows, H / 2, 0, 0)) ||
+      (st = make_map(&mhq, ws + W.hq_codes, false, I / 2, W.rows, I / 2, 0, 0)))
+    return st;
+  const bool shared = a->Is > 0;
+  if (shared) {
+    if ((st = make_map(&msg, a->s_gate, true, H, a->Is, (uint64_t)H * 2, 0, 0)) ||
+        (st = make_map(&msu, a->s_up, true, H, a->Is, (uint64_t)H * 2, 0, 0)) ||
+        (st = make_map(&msd, a->s_down, true, a->Is, H, (uint64_t)a->Is * 2, 0, 0)) ||
+        (st = make_map(&mx, a->x, true, H, a->T, (uint64_t)H * 2, 0, 0)) ||
+        (st = make_map(&mhs, ws + W.hs, true, a->Is, a->T, (uint64_t)a->Is * 2, 0, 0)))
+      return st;
+  }
+
+  // routed experts, walked in groups of `grp` through the staging layout
+  const int grp = a->prefill_group > 0 ? (a->prefill_group < kMaxGroup ? a->prefill_group
+                                                                        : kMaxGroup)
+                                       : kMaxGroup;
+  const int max_act = a->T * a->k < a->E ? a->T * a->k : a->E;
+  for (int g0 = 0; g0 < max_act; g0 += grp) {
+    QuantParams q;
+    memset(&q, 0, sizeof(q));
+    q.g0 = g0; q.g1 = g0 + grp;
+    q.act_list = a->act_list; q.n_act = a->n_act; q.offsets = a->offsets;
+    q.pad_offsets = a->pad_offsets; q.perm = a->perm; q.k = a->k;
+    q.K = H;
+    q.x = (const uint16_t*)a->x;
+    q.codes = ws + W.xq_codes; q.scales = ws + W.xq_scales; q.G = (float*)(ws + W.xq_G);
+    k_quant_rows<false><<<kSMs * 8, 256, 0, s>>>(q);
+    MOE_CHECK_LAUNCH();
+
+    GemmParams gp;
+    memset(&gp, 0, sizeof(gp));
+    gp.act_list = a->act_list; gp.n_act = a->n_act; gp.g0 = g0; gp.g1 = g0 + grp;
+    gp.src_slot = a->src_slot; gp.offsets = a->offsets; gp.pad_offsets = a->pad_offsets;
+    gp.perm = a->perm; gp.gscale = a->gscale; gp.w = a->w; gp.k = a->k; gp.n_slots = n_slots;
+    gp.arena = arena; gp.rec_bytes = rb; gp.H = H; gp.status = a->status;
+    // gate/up
+    gp.mtiles = I / kTileM;
+    gp.kstages = (H / 2) / kStageKB;
+    gp.kgroups = H / 64;
+    gp.sfa_off0 = L.gate_scales; gp.sfa_off1 = L.up_scales;
+    gp.b_scales = ws + W.xq_scales; gp.b_gscale = (const float*)(ws + W.xq_G);
+    gp.h32 = (float*)(ws + W.h32); gp.h_ld = I;
+    if ((st = launch_gemm<0, EPI_GU_ROUTED>(mg, mu, mxq, gp, s)) != MOE_OK) return st;
+    // h -> NVFP4
+    q.K = I;
+    q.h32 = (const float*)(ws + W.h32);
+    q.codes = ws + W.hq_codes; q.scales = ws + W.hq_scales; q.G = (float*)(ws + W.hq_G);
+    k_quant_rows<true><<<kSMs * 8, 256, 0, s>>>(q);
+    MOE_CHECK_LAUNCH();
+    // down, weighted, added into y_acc
+    gp.mtiles = H / kTileM;
+    gp.kstages = (I / 2) / kStageKB;
+    gp.kgroups = I / 64;
+    gp.sfa_off0 = L.down_scales; gp.sfa_off1 = 0;
+    gp.b_scales = ws + W.hq_scales; gp.b_gscale = (const float*)(ws + W.hq_G);
+    gp.y_acc = a->y_acc;
+    if ((st = launch_gemm<0, EPI_DOWN_ROUTED>(md, md, mhq, gp, s)) != MOE_OK) return st;
+  }
+
+  // shared expert (bf16): y_acc += Wd (silu(Wg x) * Wu x)
+  if (shared) {
+    GemmParams gp;
+    memset(&gp, 0, sizeof(gp));
+    gp.T = a->T; gp.H = H; gp.status = a->status;
+    gp.mtiles = a->Is / kTileM;
+    gp.kstages = (H * 2) / kStageKB;
+    gp.hs = (uint16_t*)(ws + W.hs); gp.hs_ld = a->Is;
+    if ((st = launch_gemm<1, EPI_GU_SHARED>(msg, msu, mx, gp, s)) != MOE_OK) return st;
+    gp.mtiles = H / kTileM;
+    gp.kstages = (a->Is * 2) / kStageKB;
+    gp.y_acc = a->y_acc;
+    if ((st = launch_gemm<1, EPI_DOWN_SHARED>(msd, msd, mhs, gp, s)) != MOE_OK) return st;
+  }
+  return MOE_OK;
+}
 
 }  // namespace moe

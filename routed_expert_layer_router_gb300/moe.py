@@ -44,7 +44,8 @@ class moe_ffn_args(ctypes.Structure):
     _fields_ = [("mode", i32), ("stages", i32), ("T", i32), ("H", i32), ("I", i32), ("E", i32),
                 ("k", i32), ("x", vp), ("cache", vp), ("gscale", vp), ("src_slot", vp),
                 ("act_list", vp), ("n_act", vp), ("offsets", vp), ("pad_offsets", vp),
-                ("perm", vp), ("w", vp), ("group", i32), ("n_stage", i32), ("Is", i32),
+                ("perm", vp), ("w", vp), ("group", i32), ("n_stage", i32),
+                ("prefill_group", i32), ("Is", i32),
                 ("s_gate", vp), ("s_up", vp), ("s_down", vp), ("o_route", vp), ("y_acc", vp),
                 ("o_shared", vp), ("workspace", vp), ("workspace_bytes", sz), ("status", vp)]
 

@@ -44,7 +44,8 @@ def host_inputs(dw, layer: int):
     return Wr, dw.bias_host[layer], sh
 
 
-def oracle_layer(dw, layer: int, x: np.ndarray, mode: int = 0, record_cache=None):
+def oracle_layer(dw, layer: int, x: np.ndarray, mode: int = 0, record_cache=None,
+                 return_bound: bool = False):
     """Oracle forward of layer `layer` on tokens x: generates (on the host)
     the records of the experts the oracle's router selects."""
     wl = dw.wl
@@ -59,8 +60,11 @@ def oracle_layer(dw, layer: int, x: np.ndarray, mode: int = 0, record_cache=None
         for e, r in zip(missing, recs):
             cache[(rl, e)] = r
     records = {e: cache[(rl, e)] for e in need}
-    y, ids2, w2, p2 = oracle.layer_forward(x, wl.H, wl.I, wl.E, wl.k, Wr, bias, records,
-                                           dw.gscale_host[layer], shared_w=sh, mode=mode)
+    y, ids2, w2, p2, bound = oracle.layer_forward(x, wl.H, wl.I, wl.E, wl.k, Wr, bias, records,
+                                                  dw.gscale_host[layer], shared_w=sh, mode=mode,
+                                                  return_bound=True)
+    if return_bound:
+        return y, ids2, w2, p2, bound
     return y, ids2, w2, p2
 
 
@@ -72,10 +76,15 @@ def y_to_f64(y: torch.Tensor) -> np.ndarray:
     return bf16_to_f64(y.view(torch.int16).cpu().numpy().view(np.uint16))
 
 
-def check_outputs(y_gpu: np.ndarray, y_ref: np.ndarray, tol: float = TOL):
+def check_outputs(y_gpu: np.ndarray, y_ref: np.ndarray, tol: float = TOL, bound=None):
+    """max |y_gpu - y_ref| <= tol * rms(y_ref), element by element widened by
+    `bound` (the oracle's rounding-boundary slack of the prefill numerics:
+    where the two sides' intermediate values straddle a rounding boundary of
+    the NVFP4 or bf16 re-quantisation, either neighbour is a correct result)."""
     rms = float(np.sqrt(np.mean(y_ref ** 2)))
-    err = float(np.abs(y_gpu - y_ref).max())
     assert rms > 0
+    excess = np.abs(y_gpu - y_ref) - (0.0 if bound is None else bound)
+    err = float(excess.max())
     assert err <= tol * rms, f"max|dy| = {err:.3e} > {tol} * rms {rms:.3e} (ratio {err / rms:.3e})"
     return err / rms
 

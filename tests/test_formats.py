@@ -119,3 +119,34 @@ def test_nvfp4_quant_of_exact_values_is_exact():
 def test_nvfp4_quant_zero_row():
     codes, scales, G = oracle.nvfp4_quant(np.zeros(32, np.float32))
     assert G == 1.0 and not codes.any() and not scales.any()
+
+
+def test_quant_flip_slack_covers_nearby_inputs():
+    """The rounding-boundary slack is zero away from boundaries and covers
+    every change of the quantised value that a relative perturbation of
+    5e-5 of one element can cause (the row amax element is left alone, so G
+    does not move)."""
+    rng = np.random.default_rng(9)
+    for trial in range(40):
+        v = (rng.standard_normal(256) * rng.uniform(0.1, 10)).astype(np.float32)
+        amax_i = int(np.argmax(np.abs(v)))
+        codes, scales, G = oracle.nvfp4_quant(v)
+        base = _dequant_row(codes, scales, G)
+        delta = oracle.quant_flip_delta(v)
+        for rel in (5e-5, -5e-5):
+            vp = v.copy()
+            mask = np.ones(256, bool)
+            mask[amax_i] = False
+            vp[mask] = (vp[mask].astype(np.float64) * (1 + rel)).astype(np.float32)
+            c2, s2, G2 = oracle.nvfp4_quant(vp)
+            assert G2 == G
+            moved = np.abs(_dequant_row(c2, s2, G2) - base)
+            assert np.all(moved <= delta + 1e-12)
+    # an element exactly on an E2M1 midpoint (1.25 of its block scale) is flagged
+    v = np.zeros(16, np.float32)
+    v[0] = 6.0
+    v[1] = 1.25
+    d = oracle.quant_flip_delta(v)
+    codes, scales, G = oracle.nvfp4_quant(v)
+    s = oracle.e4m3(int(scales[0])) * G
+    assert d[1] == pytest.approx(0.5 * s) and d[2] == 0.0
