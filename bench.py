@@ -1,14 +1,23 @@
 """Benchmark of the routed MoE layer on one GB300 (or N independent replicas).
 
-Default workload: the decode MoE layer - hidden 6144, expert intermediate 2048,
-288 experts top-8 (fp32 softmax router), one bf16 shared expert, NVFP4 routed
-experts all resident in HBM, 1 token per forward.  A step is one pass of the
-whole hot path (route -> permute -> cache lookup -> expert FFN gate/up ->
-down -> combine) over one fresh token; L2 is flushed between steps (a write
-of a buffer larger than L2, outside the timed events).
+Headline (the JSON line's `value`): the decode MoE layer - hidden 6144, expert
+intermediate 2048, 288 experts top-8 (fp32 softmax router), one bf16 shared
+expert, NVFP4 routed experts all resident in HBM, 1 token per forward.  A step
+is one pass of the whole hot path (route -> permute -> cache lookup -> expert
+FFN gate/up -> down -> combine) over one fresh token; L2 is flushed between
+steps (a write of a buffer larger than L2, outside the timed events).
+
+The same run also measures (the `also` object), each in its own bounded pass:
+  prefill  one layer on a 4096-token chunk, experts walked in groups of 64
+           (tcgen05 NVFP4 grouped GEMMs): tokens/s, HBM and FP4 tensor fractions;
+  stack    16 decode layers, per-layer Zipf-skewed routing, 66 hot experts per
+           layer in HBM, misses gathered from pinned host memory: tokens/s,
+           hit rate, gather GB/s against the measured host->device link;
+  flat     8 layers, 64 tokens per step, unbiased routing, 72 experts per layer
+           cached by saliency, misses gathered from pinned host memory.
 
 Prints one JSON line (rank 0).  --impl reference times the CPU oracle on the
-same workload instead (bounded sample, host cores).
+decode workload instead (bounded sample, host cores).
 """
 from __future__ import annotations
 
@@ -28,20 +37,20 @@ import numpy as np  # noqa: E402
 
 METRIC = "MoE-layer tokens/s (decode, 4096-tok prefill); % of HBM / FP4-TC / PCIe roofline"
 UNIT = "tokens/s"
+FP4_OVER_BF16 = 6.0  # nominal dense FP4 / dense bf16 tensor throughput (13.5 / 2.25)
 
 
 def _peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         with open(p) as f:
-            d = json.load(f)
-        return d, "measured"
+            return json.load(f), "measured"
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
-    """Samples nvidia-smi clocks and throttle reasons during the timed region."""
+    """Samples nvidia-smi clocks and throttle reasons during a timed region."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -58,8 +67,7 @@ class ClockSampler:
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
                  "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.thread = threading.Thread(target=self._read, daemon=True)
-            self.thread.start()
+            threading.Thread(target=self._read, daemon=True).start()
         except OSError:
             self.proc = None
 
@@ -94,19 +102,130 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-# --------------------------------------------------------------- our arm
-def run_ours(args, rank, world, local_rank):
-    import torch
+# ------------------------------------------------------------ helpers
+def _events(torch, n):
+    return [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(n)]
 
-    import gen
-    import gen.device as gd
-    from routed_expert_layer_router_gb300 import moe
 
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
-    # a non-default stream: graph capture and all timing happen on it
-    torch.cuda.set_stream(torch.cuda.Stream(device=dev))
-    moe.lib()
+def prewarm(torch, fn, seconds=1.0):
+    """Keeps the GPU busy for `seconds` so clocks and memory leave idle states."""
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < seconds:
+        fn()
+        torch.cuda.synchronize()
+
+
+def link_h2d_gbs(torch, dev, mib=1024, reps=5):
+    """Pinned host -> device copy bandwidth (cudaMemcpyAsync), best of reps."""
+    h = torch.empty(mib << 20, dtype=torch.uint8, pin_memory=True)
+    d = torch.empty(mib << 20, dtype=torch.uint8, device=dev)
+    d.copy_(h, non_blocking=True)
+    torch.cuda.synchronize()
+    best = 1e30
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        d.copy_(h, non_blocking=True)
+        b.record()
+        b.synchronize()
+        best = min(best, a.elapsed_time(b))
+    del h, d
+    return (mib << 20) / (best * 1e-3) / 1e9
+
+
+class ExplicitLayer:
+    """One layer's hot path as the individual ABI calls (route, permute,
+    lookup, gather, expert FFN, combine) on caller-owned buffers, so that the
+    bench can put CUDA events around single launches."""
+
+    def __init__(self, torch, moe, dw, layer, T):
+        wl = dw.wl
+        self.torch, self.moe, self.dw, self.layer, self.T = torch, moe, dw, layer, T
+        H, I, E, k, Is = wl.H, wl.I, wl.E, wl.k, wl.Is
+        dev = torch.device("cuda")
+        i32, f32 = torch.int32, torch.float32
+        self.b = {n: torch.zeros(sz, dtype=dt, device=dev) for n, sz, dt in (
+            ("logits", T * E, f32), ("ids", T * k, i32), ("w", T * k, f32), ("p", T * k, f32),
+            ("counts", E, i32), ("offsets", E + 1, i32), ("perm", T * k, i32),
+            ("inv", T * k, i32), ("src", E, i32), ("act", E, i32), ("n_act", 2, i32),
+            ("miss", E, i32), ("n_miss", 1, i32), ("status", 1, i32),
+            ("o_route", T * k * H, f32), ("o_shared", T * H, f32))}
+        b = self.b
+        self.ws_bytes = moe.moe_ffn_workspace_bytes(0, T, H, I, E, k, Is)
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
+        ra = moe.moe_route_args()
+        ra.w_router = dw.w_router[layer].data_ptr()
+        ra.bias = dw.bias[layer].data_ptr() if dw.bias[layer] is not None else None
+        ra.T, ra.H, ra.E, ra.k = T, H, E, k
+        ra.ids, ra.w, ra.p_sel, ra.logits = (b[n].data_ptr() for n in ("ids", "w", "p", "logits"))
+        ra.status = b["status"].data_ptr()
+        fa = moe.moe_ffn_args()
+        fa.mode, fa.T, fa.H, fa.I, fa.E, fa.k = 0, T, H, I, E, k
+        fa.cache, fa.gscale = dw.cache.handle, dw.gscale[layer].data_ptr()
+        fa.src_slot, fa.act_list, fa.n_act = (b[n].data_ptr() for n in ("src", "act", "n_act"))
+        fa.offsets, fa.perm, fa.w = (b[n].data_ptr() for n in ("offsets", "perm", "w"))
+        fa.n_stage, fa.Is = dw.cache.n_stage, Is
+        if Is:
+            fa.s_gate, fa.s_up, fa.s_down = (t.data_ptr() for t in dw.shared[layer])
+        fa.o_route = b["o_route"].data_ptr()
+        fa.o_shared = b["o_shared"].data_ptr() if Is else None
+        fa.workspace, fa.workspace_bytes = self.ws.data_ptr(), self.ws_bytes
+        fa.status = b["status"].data_ptr()
+        ca = moe.moe_combine_args()
+        ca.T, ca.H, ca.k = T, H, k
+        ca.o_route, ca.inv = b["o_route"].data_ptr(), b["inv"].data_ptr()
+        ca.o_shared = b["o_shared"].data_ptr() if Is else None
+        self.ra, self.fa, self.ca = ra, fa, ca
+        S = max(dw.cache.n_stage, 1)
+        self.max_miss = min(T * k, E)
+        self.groups = (self.max_miss + S - 1) // S if dw.cache.n_stage > 0 else 1
+
+    def step(self, x_ptr, y_ptr, sp, ev_fill=None, ev_gu=None, ev_dn=None):
+        moe, b, dw = self.moe, self.b, self.dw
+        wl = dw.wl
+        self.ra.x = x_ptr
+        moe.moe_route(self.ra, sp)
+        moe.moe_permute(b["ids"].data_ptr(), self.T, wl.k, wl.E, b["counts"].data_ptr(),
+                        b["offsets"].data_ptr(), b["perm"].data_ptr(), b["inv"].data_ptr(), 0,
+                        128, b["status"].data_ptr(), sp)
+        moe.expcache_lookup(dw.cache.handle, self.layer, b["counts"].data_ptr(),
+                            b["src"].data_ptr(), b["act"].data_ptr(), b["n_act"].data_ptr(),
+                            b["miss"].data_ptr(), b["n_miss"].data_ptr(),
+                            b["status"].data_ptr(), sp)
+        self.fa.x = x_ptr
+        S = dw.cache.n_stage
+        for g in range(self.groups):
+            if S > 0:
+                cnt = min(S, self.max_miss - g * S)
+                if ev_fill:
+                    ev_fill[g][0].record()
+                moe.expcache_fill(dw.cache.handle, self.layer, b["miss"].data_ptr(),
+                                  b["n_miss"].data_ptr(), g * S, cnt, 0, b["status"].data_ptr(),
+                                  sp)
+                if ev_fill:
+                    ev_fill[g][1].record()
+            self.fa.group = g
+            self.fa.stages = 1
+            if ev_gu:
+                ev_gu[0].record()
+            moe.moe_expert_ffn(self.fa, sp)
+            if ev_gu:
+                ev_gu[1].record()
+            self.fa.stages = 2
+            moe.moe_expert_ffn(self.fa, sp)
+            if ev_dn:
+                ev_dn[1].record()
+        self.ca.y = y_ptr
+        moe.moe_combine(self.ca, sp)
+
+    def launches(self):
+        S = self.dw.cache.n_stage
+        return 2 + 1 + 1 + self.groups * (2 + (1 if S > 0 else 0)) + 1
+
+
+# --------------------------------------------------------------- decode
+def bench_decode(args, torch, moe, gen, gd, dev, rank, world, local_rank, peaks):
     wl = gen.WORKLOADS["decode"]
     H, I, E, k, Is = wl.H, wl.I, wl.E, wl.k, wl.Is
     T = 1
@@ -122,90 +241,25 @@ def run_ours(args, rank, world, local_rank):
     gen.dev_x_bf16(wl.seed, 0, 1_000_000 + rank * n_steps, n_steps, H, xs.data_ptr(), sp)
     ys = torch.empty((n_steps, H), dtype=torch.bfloat16, device=dev)
     flush = torch.empty(args.flush_mb << 20, dtype=torch.uint8, device=dev)
+    ex = ExplicitLayer(torch, moe, dw, 0, T)
 
-    # explicit buffers for the step made of the individual ABI calls
-    i32, f32 = torch.int32, torch.float32
-    b = {
-        "logits": torch.empty((T, E), dtype=f32, device=dev),
-        "ids": torch.empty((T, k), dtype=i32, device=dev),
-        "w": torch.empty((T, k), dtype=f32, device=dev),
-        "p": torch.empty((T, k), dtype=f32, device=dev),
-        "counts": torch.empty(E, dtype=i32, device=dev),
-        "offsets": torch.empty(E + 1, dtype=i32, device=dev),
-        "perm": torch.empty(T * k, dtype=i32, device=dev),
-        "inv": torch.empty(T * k, dtype=i32, device=dev),
-        "src": torch.empty(E, dtype=i32, device=dev),
-        "act": torch.empty(E, dtype=i32, device=dev),
-        "n_act": torch.empty(2, dtype=i32, device=dev),
-        "miss": torch.empty(E, dtype=i32, device=dev),
-        "n_miss": torch.empty(1, dtype=i32, device=dev),
-        "status": torch.zeros(1, dtype=i32, device=dev),
-        "o_route": torch.empty((T * k, H), dtype=f32, device=dev),
-        "o_shared": torch.empty((T, H), dtype=f32, device=dev),
-    }
-    ws_bytes = moe.moe_ffn_workspace_bytes(0, T, H, I, E, k, Is)
-    ffn_ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
-    ra = moe.moe_route_args()
-    ra.w_router, ra.bias = dw.w_router[0].data_ptr(), None
-    ra.T, ra.H, ra.E, ra.k = T, H, E, k
-    ra.ids, ra.w, ra.p_sel, ra.logits = (b["ids"].data_ptr(), b["w"].data_ptr(),
-                                         b["p"].data_ptr(), b["logits"].data_ptr())
-    ra.status = b["status"].data_ptr()
-    fa = moe.moe_ffn_args()
-    fa.mode, fa.T, fa.H, fa.I, fa.E, fa.k = 0, T, H, I, E, k
-    fa.cache, fa.gscale = dw.cache.handle, dw.gscale[0].data_ptr()
-    fa.src_slot, fa.act_list, fa.n_act = b["src"].data_ptr(), b["act"].data_ptr(), b["n_act"].data_ptr()
-    fa.offsets, fa.perm, fa.w = b["offsets"].data_ptr(), b["perm"].data_ptr(), b["w"].data_ptr()
-    fa.group, fa.n_stage, fa.Is = 0, 0, Is
-    fa.s_gate, fa.s_up, fa.s_down = (t.data_ptr() for t in dw.shared[0])
-    fa.o_route, fa.o_shared = b["o_route"].data_ptr(), b["o_shared"].data_ptr()
-    fa.workspace, fa.workspace_bytes = ffn_ws.data_ptr(), ws_bytes
-    fa.status = b["status"].data_ptr()
-    ca = moe.moe_combine_args()
-    ca.T, ca.H, ca.k = T, H, k
-    ca.o_route, ca.inv, ca.o_shared = b["o_route"].data_ptr(), b["inv"].data_ptr(), b["o_shared"].data_ptr()
-
-    def step(i, ev=None):
-        ra.x = xs[i].data_ptr()
-        moe.moe_route(ra, sp)
-        moe.moe_permute(b["ids"].data_ptr(), T, k, E, b["counts"].data_ptr(),
-                        b["offsets"].data_ptr(), b["perm"].data_ptr(), b["inv"].data_ptr(), 0, 128,
-                        b["status"].data_ptr(), sp)
-        moe.expcache_lookup(dw.cache.handle, 0, b["counts"].data_ptr(), b["src"].data_ptr(),
-                            b["act"].data_ptr(), b["n_act"].data_ptr(), b["miss"].data_ptr(),
-                            b["n_miss"].data_ptr(), b["status"].data_ptr(), sp)
-        fa.x = xs[i].data_ptr()
-        fa.stages = 1
-        if ev:
-            ev[0].record(stream)
-        moe.moe_expert_ffn(fa, sp)
-        if ev:
-            ev[1].record(stream)
-        fa.stages = 2
-        moe.moe_expert_ffn(fa, sp)
-        if ev:
-            ev[2].record(stream)
-        ca.y = ys[i].data_ptr()
-        moe.moe_combine(ca, sp)
-
-    launches_per_step = 2 + 1 + 1 + 1 + 1 + 1  # route(2) permute lookup gu down combine
-
-    # ---- pass 1 (headline): each step replayed from a CUDA graph -------------
-    step(0)  # eager once before capture (one-time kernel attribute set-up)
+    # ---- pass 1 (headline): each step replayed from a CUDA graph
+    ex.step(xs[0].data_ptr(), ys[0].data_ptr(), sp)  # eager once before capture
     torch.cuda.synchronize()
     graphs = []
     for i in range(n_steps):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
-            step(i)
+            ex.step(xs[i].data_ptr(), ys[i].data_ptr(), sp)
         graphs.append(g)
     torch.cuda.synchronize()
-    for i in range(args.warmup):
-        flush.zero_()
-        graphs[i].replay()
-    torch.cuda.synchronize()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
+
+    def warm():
+        for i in range(args.warmup):
+            flush.zero_()
+            graphs[i].replay()
+    prewarm(torch, warm, args.prewarm_s)
+    ev = _events(torch, args.steps)
     clocks = ClockSampler(local_rank)
     clocks.start()
     time.sleep(0.3)
@@ -223,20 +277,21 @@ def run_ours(args, rank, world, local_rank):
     if world > 1:
         torch.distributed.barrier()
     clk = clocks.stop()
-    step_ms = [a.elapsed_time(bb) for a, bb in ev]
-    total_ms = sum(step_ms)
+    total_ms = sum(a.elapsed_time(b) for a, b in ev)
+    del graphs
 
-    # ---- pass 2: per-kernel events around the FFN launches (eager) -----------
-    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    # ---- pass 2: events around the two FFN launches (eager)
+    kev = [(_events(torch, 1)[0], _events(torch, 1)[0]) for _ in range(args.steps)]
     for j in range(args.steps):
         flush.zero_()
-        step(args.warmup + j, kev[j])
+        ex.step(xs[args.warmup + j].data_ptr(), ys[args.warmup + j].data_ptr(), sp,
+                ev_gu=kev[j][0], ev_dn=(kev[j][0][1], kev[j][1][1]))
     torch.cuda.synchronize()
-    gu_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in kev)
-    dn_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in kev)
-    assert int(b["status"].item()) == 0, "device status set during the bench"
+    gu_ms = statistics.mean(e[0][0].elapsed_time(e[0][1]) for e in kev)
+    dn_ms = statistics.mean(e[0][1].elapsed_time(e[1][1]) for e in kev)
+    assert int(ex.b["status"].item()) == 0, "device status set during the bench"
 
-    # ---- e2e: the public call with host buffers --------------------------------
+    # ---- e2e: the public call with host buffers
     xh = torch.empty((n_steps, H), dtype=torch.bfloat16, pin_memory=True)
     xh.copy_(xs.cpu())
     yh = torch.empty((n_steps, H), dtype=torch.bfloat16, pin_memory=True)
@@ -262,63 +317,233 @@ def run_ours(args, rank, world, local_rank):
         e2e_ms.append(a.elapsed_time(bb))
     assert layer.read_status() == 0
 
-    # ---- aggregate over ranks -------------------------------------------------
     tot = torch.tensor([total_ms], dtype=torch.float64, device=dev)
     if world > 1:
         torch.distributed.all_reduce(tot, op=torch.distributed.ReduceOp.MAX)
     total_ms = float(tot.item())
-
-    peaks, peak_kind = _peaks()
     rb = gen.record_bytes(H, I)
-    gu_bytes = k * (2 * I * H // 2 + 2 * I * H // 16) + 2 * Is * H * 2 + T * H * 2 + (T * k * I + T * Is) * 4
-    dn_bytes = k * (H * I // 2 + H * I // 16) + H * Is * 2 + (T * k * I + T * Is) * 4 + (T * k + T) * H * 4
+    gu_bytes = (k * (2 * I * H // 2 + 2 * I * H // 16) + 2 * Is * H * 2 + T * H * 2
+                + (T * k * I + T * Is) * 4)
+    dn_bytes = (k * (H * I // 2 + H * I // 16) + H * Is * 2 + (T * k * I + T * Is) * 4
+                + (T * k + T) * H * 4)
     step_bytes = k * rb + 3 * Is * H * 2 + E * H * 4 + 2 * T * H * 2
     gu_gbs = gu_bytes / (gu_ms * 1e-3) / 1e9
     dn_gbs = dn_bytes / (dn_ms * 1e-3) / 1e9
-    value = world * args.steps * T / (total_ms * 1e-3)
-    out = {
-        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup,
+    hbm = peaks["hbm_gbs"]
+    res = {
+        "value": round(world * args.steps * T / (total_ms * 1e-3), 2),
         "ms_per_step": round(total_ms / args.steps, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "nvfp4 weights (e2m1+e4m3/16), fp32 accumulate, bf16 activations",
-        "data": "synthetic (seeded; random-init NVFP4 experts, N(0,1) bf16 tokens)",
-        "config": {"workload": "decode MoE layer: H=6144, I=2048, 288 experts top-8, fp32 softmax "
-                               "router, bf16 shared expert I=2048, NVFP4 routed experts all "
-                               "resident in HBM, 1 token per forward",
-                   "global_batch": world * T, "seq_len": 1, "parallelism": f"replicas{world}",
-                   "l2": f"flushed between steps ({args.flush_mb} MiB write, outside the events)",
-                   "timing": "CUDA-graph replay per step, CUDA events around each replay"},
-        "roofline": {"bound": "hbm", "kernel": "k_decode_gu (routed NVFP4 gate/up + shared bf16 "
-                                               "gate/up, SiLU*mul)",
-                     "achieved": round(gu_gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": round(gu_gbs / peaks["hbm_gbs"], 4), "traffic": None,
-                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
-                     if peak_kind == "measured" else "fallback 6.8 TB/s",
+        "roofline": {"bound": "hbm",
+                     "kernel": "k_decode_gu (routed NVFP4 gate/up of the 8 experts + shared "
+                               "bf16 gate/up, SiLU*mul)",
+                     "achieved": round(gu_gbs, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(gu_gbs / hbm, 4), "traffic": None,
                      "bytes_per_launch": gu_bytes, "avg_launch_ms": round(gu_ms, 5)},
         "kernels": {
             "k_decode_gu": {"ms": round(gu_ms, 5), "GB/s": round(gu_gbs, 1),
-                            "frac_hbm": round(gu_gbs / peaks["hbm_gbs"], 4)},
+                            "frac_hbm": round(gu_gbs / hbm, 4)},
             "k_decode_down": {"ms": round(dn_ms, 5), "GB/s": round(dn_gbs, 1),
-                              "frac_hbm": round(dn_gbs / peaks["hbm_gbs"], 4)},
-            "step_hbm_frac": round(step_bytes / (total_ms / args.steps * 1e-3) / 1e9
-                                   / peaks["hbm_gbs"], 4),
-        },
+                              "frac_hbm": round(dn_gbs / hbm, 4)},
+            "step_bytes": step_bytes,
+            "step_frac_hbm": round(step_bytes / (total_ms / args.steps * 1e-3) / 1e9 / hbm, 4)},
         "e2e": {"value": round(e2e_steps / (sum(e2e_ms) * 1e-3), 2), "unit": UNIT,
                 "h2d_bytes_per_step": T * H * 2, "d2h_bytes_per_step": T * H * 2,
-                "call": "moe_layer_forward with pinned host input/output copies in the events"},
-        "gpu_launches": launches_per_step * args.steps,
+                "call": "moe_layer_forward; token copied in from pinned host memory and the "
+                        "output copied back inside the events"},
+        "gpu_launches": ex.launches() * args.steps,
         "clocks": clk,
         "wall_s": round(wall, 3),
     }
     dw.close()
-    return out
+    return res
+
+
+# --------------------------------------------------------------- prefill
+def bench_prefill(args, torch, moe, gen, gd, dev, peaks):
+    wl = gen.WORKLOADS["prefill"]
+    T, H, I, E, k, Is = wl.T, wl.H, wl.I, wl.E, wl.k, wl.Is
+    dw = gd.build(wl, T_max=T)
+    layer = dw.moe_layers[0]
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+    steps = args.prefill_steps
+    n = args.warmup + steps
+    xs = torch.empty((n, T, H), dtype=torch.bfloat16, device=dev)
+    for i in range(n):
+        gen.dev_x_bf16(wl.seed, 0, 3_000_000 + i * T, T, H, xs[i].data_ptr(), sp)
+    y = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(args.flush_mb << 20, dtype=torch.uint8, device=dev)
+
+    def warm():
+        for i in range(args.warmup):
+            layer.forward(xs[i], y)
+    prewarm(torch, warm, args.prewarm_s)
+    ev = _events(torch, steps)
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    time.sleep(0.2)
+    torch.cuda.synchronize()
+    for j in range(steps):
+        flush.zero_()
+        ev[j][0].record(stream)
+        layer.forward(xs[args.warmup + j], y)
+        ev[j][1].record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = sum(a.elapsed_time(b) for a, b in ev) / steps
+    assert layer.read_status() == 0
+    # e2e: tokens copied in from pinned host memory, output copied back
+    xh = xs[args.warmup:].cpu().pin_memory()
+    yh = torch.empty((T, H), dtype=torch.bfloat16, pin_memory=True)
+    xd = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    e2e = []
+    for j in range(steps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        xd.copy_(xh[j], non_blocking=True)
+        layer.forward(xd, y)
+        yh.copy_(y, non_blocking=True)
+        b.record(stream)
+        b.synchronize()
+        e2e.append(a.elapsed_time(b))
+    rb = gen.record_bytes(H, I)
+    weight_bytes = E * rb + 3 * Is * H * 2 + E * H * 4
+    flops_fp4 = 2.0 * T * k * (2 * I * H + H * I)
+    flops_bf16 = 2.0 * T * 3 * Is * H
+    gbs = (weight_bytes + 2 * T * H * 2) / (ms * 1e-3) / 1e9
+    fp4_peak = peaks["bf16_tflops"] * FP4_OVER_BF16
+    res = {
+        "workload": "prefill MoE layer: 4096 tokens, H=6144, I=2048, 288 experts top-8, bf16 "
+                    "shared expert, all experts resident, groups of 64 experts",
+        "value": round(T / (ms * 1e-3), 1), "unit": UNIT, "ms_per_step": round(ms, 4),
+        "roofline": {
+            "bound": "hbm", "unit": "GB/s",
+            "kernel": "prefill expert FFN (NVFP4 quantisation + tcgen05 mxf4nvf4 grouped GEMMs + "
+                      "bf16 shared-expert GEMMs) and router, whole step",
+            "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
+            "frac": round(gbs / peaks["hbm_gbs"], 4),
+            "bytes_per_step": weight_bytes + 2 * T * H * 2},
+        "fp4_tensor": {"achieved_tflops": round(flops_fp4 / (ms * 1e-3) / 1e12, 1),
+                       "peak_tflops": round(fp4_peak, 1),
+                       "frac": round(flops_fp4 / (ms * 1e-3) / 1e12 / fp4_peak, 4),
+                       "peak_source": "measured bf16 burst x 6 (nominal FP4/bf16 ratio)",
+                       "routed_fp4_tflop_per_step": round(flops_fp4 / 1e12, 3),
+                       "shared_bf16_tflop_per_step": round(flops_bf16 / 1e12, 3)},
+        "e2e": {"value": round(T / (statistics.mean(e2e) * 1e-3), 1), "unit": UNIT,
+                "h2d_bytes_per_step": T * H * 2, "d2h_bytes_per_step": T * H * 2},
+        "clocks": clk,
+    }
+    dw.close()
+    return res
+
+
+# --------------------------------------------------------------- stack / flat
+def _saliency_order(torch, moe, gen, wl, layers, dev, n_tokens=512):
+    """Per layer, experts by decreasing routing-weight mass over a separate
+    seeded calibration batch (computed with the library's router)."""
+    orders = []
+    for l in range(layers):
+        wr = torch.empty((wl.E, wl.H), dtype=torch.float32, device=dev)
+        gen.dev_router_f32(wl.seed, l, wl.E, wl.H, wr.data_ptr(), 0)
+        x = torch.empty((n_tokens, wl.H), dtype=torch.bfloat16, device=dev)
+        gen.dev_x_bf16(wl.seed + 1000, l, 0, n_tokens, wl.H, x.data_ptr(), 0)
+        ids = torch.empty((n_tokens, wl.k), dtype=torch.int32, device=dev)
+        w = torch.empty((n_tokens, wl.k), dtype=torch.float32, device=dev)
+        lg = torch.empty((n_tokens, wl.E), dtype=torch.float32, device=dev)
+        a = moe.moe_route_args()
+        a.x, a.w_router, a.T, a.H, a.E, a.k = x.data_ptr(), wr.data_ptr(), n_tokens, wl.H, wl.E, wl.k
+        a.ids, a.w, a.logits = ids.data_ptr(), w.data_ptr(), lg.data_ptr()
+        moe.moe_route(a, 0)
+        torch.cuda.synchronize()
+        sal = torch.zeros(wl.E, dtype=torch.float64, device=dev)
+        sal.index_add_(0, ids.view(-1).long(), w.view(-1).double())
+        s = sal.cpu().numpy()
+        orders.append(sorted(range(wl.E), key=lambda e: (-s[e], e)))
+    return orders
+
+
+def bench_multilayer(args, torch, moe, gen, gd, dev, name, link_gbs):
+    wl = gen.WORKLOADS[name]
+    L = wl.layers if args.layers <= 0 else min(args.layers, wl.layers)
+    T = wl.T
+    order = _saliency_order(torch, moe, gen, wl, L, dev) if wl.hot_rule == "saliency" else None
+    n_stage = 64 if T > 1 else None
+    # one host copy per expert id, shared by the layers (host memory bound;
+    # the bytes each miss moves over the link are the same)
+    dw = gd.build(wl, layers=L, T_max=T, saliency_order=order, n_stage=n_stage,
+                  alias_host_records=True)
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+    steps = args.stack_steps
+    n = args.warmup + steps
+    xs = torch.empty((n, L, T, wl.H), dtype=torch.bfloat16, device=dev)
+    for i in range(n):
+        for l in range(L):
+            gen.dev_x_bf16(wl.seed, l, 5_000_000 + i * T, T, wl.H, xs[i, l].data_ptr(), sp)
+    y = torch.empty((L, T, wl.H), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(args.flush_mb << 20, dtype=torch.uint8, device=dev)
+    layers = dw.moe_layers
+
+    def fwd(i):
+        for l in range(L):
+            layers[l].forward(xs[i, l], y[l])
+
+    prewarm(torch, lambda: [fwd(i) for i in range(args.warmup)], args.prewarm_s)
+    ev = _events(torch, steps)
+    torch.cuda.synchronize()
+    for j in range(steps):
+        flush.zero_()
+        ev[j][0].record(stream)
+        fwd(args.warmup + j)
+        ev[j][1].record(stream)
+    torch.cuda.synchronize()
+    ms = sum(a.elapsed_time(b) for a, b in ev) / steps
+    for l in range(L):
+        assert layers[l].read_status() == 0
+    # gather pass: explicit calls with events around each fill
+    exs = [ExplicitLayer(torch, moe, dw, l, T) for l in range(L)]
+    fill_ms, miss, act = 0.0, 0, 0
+    yy = torch.empty((T, wl.H), dtype=torch.bfloat16, device=dev)
+    for j in range(steps):
+        flush.zero_()
+        for l in range(L):
+            evf = _events(torch, exs[l].groups)
+            exs[l].step(xs[args.warmup + j, l].data_ptr(), yy.data_ptr(), sp, ev_fill=evf)
+            torch.cuda.synchronize()
+            nm = int(exs[l].b["n_miss"].item())
+            na = int(exs[l].b["n_act"][0].item())
+            miss += nm
+            act += na
+            used = (nm + dw.cache.n_stage - 1) // max(dw.cache.n_stage, 1)
+            fill_ms += sum(evf[g][0].elapsed_time(evf[g][1]) for g in range(min(used, len(evf))))
+        assert all(int(e.b["status"].item()) == 0 for e in exs)
+    rb = gen.record_bytes(wl.H, wl.I)
+    gather_gbs = miss * rb / (fill_ms * 1e-3) / 1e9 if fill_ms > 0 else 0.0
+    res = {
+        "workload": (f"{L} decode layers, {T} token(s) per step, "
+                     + ("per-layer Zipf bias (alpha 1.556), 66 hot experts per layer in HBM"
+                        if name == "stack" else
+                        "unbiased routing, 72 experts per layer cached by saliency")
+                     + ", misses gathered from pinned host memory"),
+        "value": round(T / (ms * 1e-3), 2), "unit": UNIT + " (whole stack)",
+        "ms_per_step": round(ms, 4),
+        "per_layer_tokens_s": round(T * L / (ms * 1e-3), 1),
+        "hit_rate": round(1 - miss / max(act, 1), 4),
+        "misses_per_layer_step": round(miss / (steps * L), 2),
+        "roofline": {"bound": "link", "kernel": "k_gather (expcache_fill)",
+                     "achieved": round(gather_gbs, 1), "peak": round(link_gbs, 1),
+                     "unit": "GB/s", "frac": round(gather_gbs / link_gbs, 4) if link_gbs else None,
+                     "peak_source": "measured pinned host->device cudaMemcpyAsync (1 GiB)"},
+        "host_records": "one host copy per expert id, shared by the layers",
+    }
+    dw.close()
+    return res
 
 
 # ------------------------------------------------------- CPU oracle timing
 def oracle_sample(seconds: float, wl_name: str = "decode"):
     """Times the oracle (as it stands) on decode tokens of the same workload
-    until `seconds` of CPU work are spent; returns (tokens/s, tokens, threads)."""
+    until `seconds` of CPU work are spent; returns (tokens/s, tokens, threads, s)."""
     import gen
     import oracle
     wl = gen.WORKLOADS[wl_name]
@@ -357,11 +582,65 @@ def run_reference(args, rank, world):
                                "expert, NVFP4 experts; 1 token per forward", "global_batch": 1,
                    "seq_len": 1, "parallelism": "cpu"},
         "cpu_baseline": {"value": round(tps, 4), "unit": UNIT, "cores": threads, "kind": "oracle",
-                         "sample": f"{n} decode tokens ({spent:.1f} s of oracle time; records "
+                         "sample": f"{n} decode tokens ({spent:.1f} s of oracle time; record "
                                    f"generation excluded)"},
         "e2e": {"value": round(tps, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    import gen
+    import gen.device as gd
+    from routed_expert_layer_router_gb300 import moe
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    # a non-default stream: graph capture and all timing happen on it
+    torch.cuda.set_stream(torch.cuda.Stream(device=dev))
+    moe.lib()
+    peaks, peak_kind = _peaks()
+    d = bench_decode(args, torch, moe, gen, gd, dev, rank, world, local_rank, peaks)
+    d["roofline"]["peak_source"] = (f"{peak_kind}: MEASURED_PEAKS.json hbm_gbs (copy)"
+                                    if peak_kind == "measured" else "fallback 6.8 TB/s")
+    out = {
+        "metric": METRIC, "value": d["value"], "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": d["ms_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "nvfp4 weights (e2m1 + e4m3 per 16), fp32 accumulation, bf16 activations",
+        "data": "synthetic (seeded; random-init NVFP4 experts, N(0,1) bf16 tokens)",
+        "config": {"workload": "decode MoE layer: H=6144, I=2048, 288 experts top-8, fp32 "
+                               "softmax router, bf16 shared expert I=2048, NVFP4 routed experts "
+                               "all resident in HBM, 1 token per forward",
+                   "global_batch": world, "seq_len": 1, "parallelism": f"replicas{world}",
+                   "l2": f"flushed between steps ({args.flush_mb} MiB write, outside the events)",
+                   "timing": "CUDA-graph replay per step, CUDA events around each replay"},
+        "roofline": d["roofline"], "kernels": d["kernels"], "e2e": d["e2e"],
+        "gpu_launches": d["gpu_launches"], "clocks": d["clocks"], "wall_s": d["wall_s"],
+    }
+    torch.cuda.empty_cache()
+    if rank == 0 and not args.decode_only and not args.small:
+        also = {}
+        try:
+            also["prefill"] = bench_prefill(args, torch, moe, gen, gd, dev, peaks)
+        except Exception as exc:  # reported, not hidden
+            also["prefill"] = {"error": repr(exc)}
+        torch.cuda.empty_cache()
+        try:
+            link = link_h2d_gbs(torch, dev)
+            also["link_h2d_gbs"] = round(link, 1)
+            for name in ("stack", "flat"):
+                try:
+                    also[name] = bench_multilayer(args, torch, moe, gen, gd, dev, name, link)
+                except Exception as exc:
+                    also[name] = {"error": repr(exc)}
+                torch.cuda.empty_cache()
+        except Exception as exc:
+            also["link_h2d_gbs"] = {"error": repr(exc)}
+        out["also"] = also
+    return out
 
 
 def main():
@@ -371,9 +650,14 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--flush-mb", type=int, default=512)
+    ap.add_argument("--prewarm-s", type=float, default=1.0)
+    ap.add_argument("--prefill-steps", type=int, default=10)
+    ap.add_argument("--stack-steps", type=int, default=20)
+    ap.add_argument("--layers", type=int, default=0, help="layers of stack/flat (0 = all)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-seconds", type=float, default=60.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--decode-only", action="store_true")
     ap.add_argument("--small", action="store_true",
                     help="16 distinct expert records (profiler captures only)")
     args = ap.parse_args()
