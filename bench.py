@@ -361,6 +361,12 @@ def bench_decode(args, torch, moe, gen, gd, dev, rank, world, local_rank, peaks)
 # --------------------------------------------------------------- prefill
 def bench_prefill(args, torch, moe, gen, gd, dev, peaks):
     wl = gen.WORKLOADS["prefill"]
+    if args.prefill_experts > 0:
+        # profiler captures only: fewer experts and proportionally fewer tokens,
+        # the same tokens per expert (tile shapes) and kernels
+        E2 = args.prefill_experts
+        wl = gen.Workload(**{**wl.__dict__, "name": "prefill-part", "E": E2,
+                             "T": max(128, (wl.T * E2 // wl.E) // 128 * 128)})
     T, H, I, E, k, Is = wl.T, wl.H, wl.I, wl.E, wl.k, wl.Is
     dw = gd.build(wl, T_max=T)
     layer = dw.moe_layers[0]
@@ -602,6 +608,11 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_stream(torch.cuda.Stream(device=dev))
     moe.lib()
     peaks, peak_kind = _peaks()
+    if args.only == "prefill":
+        return {"prefill": bench_prefill(args, torch, moe, gen, gd, dev, peaks)}
+    if args.only in ("stack", "flat"):
+        link = link_h2d_gbs(torch, dev)
+        return {args.only: bench_multilayer(args, torch, moe, gen, gd, dev, args.only, link)}
     d = bench_decode(args, torch, moe, gen, gd, dev, rank, world, local_rank, peaks)
     d["roofline"]["peak_source"] = (f"{peak_kind}: MEASURED_PEAKS.json hbm_gbs (copy)"
                                     if peak_kind == "measured" else "fallback 6.8 TB/s")
@@ -660,6 +671,10 @@ def main():
     ap.add_argument("--decode-only", action="store_true")
     ap.add_argument("--small", action="store_true",
                     help="16 distinct expert records (profiler captures only)")
+    ap.add_argument("--only", default="", choices=["", "prefill", "stack", "flat"],
+                    help="run one secondary workload alone (profiler captures)")
+    ap.add_argument("--prefill-experts", type=int, default=0,
+                    help="prefill with fewer experts, same tokens per expert (profiling)")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -675,6 +690,10 @@ def main():
         import torch
         torch.distributed.init_process_group("nccl")
     out = run_ours(args, rank, world, local_rank)
+    if args.only:
+        if rank == 0:
+            print(json.dumps(out), flush=True)
+        return
     if rank == 0:
         if not args.no_cpu_baseline and world == 1:
             tps, n, threads, spent = oracle_sample(args.cpu_seconds)
