@@ -88,6 +88,7 @@ uint64_t moe_record_bytes(int H, int I);
  * k largest logits in (logit desc, id asc) order give ids[t][0..k); p_sel is
  * the full-softmax probability of each selected expert; w is the softmax over
  * the selected logits only (renormalised top-k, sums to 1 per token).
+ * moe_route_workspace_bytes(T, E) = 256 + T*E*4.
  */
 typedef struct {
   const void* x;        /* device [T][H] bf16, row-major                        */
@@ -99,7 +100,14 @@ typedef struct {
   float* p_sel;         /* device out [T][k] full-softmax probabilities, or NULL */
   float* logits;        /* device [T][E] fp32: output if non-NULL; else the call
                            needs workspace of moe_route_workspace_bytes(T, E)   */
-  void* workspace;      /* device scratch, may be NULL when logits != NULL       */
+  void* workspace;      /* device scratch, may be NULL when logits != NULL: its
+                           first 256 bytes are a control area that must be zero
+                           before the first call on it (every call leaves it
+                           zero); the logits follow it when logits == NULL.
+                           With T <= 8 and a workspace the router runs as one
+                           kernel (per-expert logits, then softmax/top-k in the
+                           CTA that finishes last); calls that share a
+                           workspace must not overlap on the GPU.           */
   size_t workspace_bytes;
   int32_t* status;      /* device sticky status word, or NULL                    */
 } moe_route_args;

@@ -21,6 +21,11 @@ size_t prefill_workspace_bytes(int T, int H, int I, int E, int k, int Is);
 moe_status prefill_ffn(const moe_ffn_args* a, cudaStream_t s);
 moe_status prefill_setup();
 moe_status permute_setup();
+moe_status launch_permute(const int32_t* ids, int T, int k, int E, int32_t* counts,
+                          int32_t* offsets, int32_t* perm, int32_t* inv, int32_t* pad_offsets,
+                          int pad_align, int32_t* status, const LookupArgs& lk, cudaStream_t s);
+void cache_lookup_args(const expcache* c, int layer, int32_t* src_slot, int32_t* act_list,
+                       int32_t* n_act, int32_t* miss_ids, int32_t* n_miss, LookupArgs* out);
 }  // namespace moe
 
 using namespace moe;
@@ -98,6 +103,7 @@ struct moe_layer {
   float *w, *p_sel;
   int32_t *src_slot, *act_list, *n_act, *miss_ids, *n_miss, *status;
   float *o_route, *o_shared, *y_acc;
+  void* route_ctl;
   void* ffn_ws;
   size_t ffn_ws_bytes;
   int last_T;
@@ -144,7 +150,8 @@ MOE_API moe_status moe_layer_create(const moe_layer_desc* d, moe_layer** out) {
       (size_t)T * k * H * 4, /* o_route */
       (size_t)T * H * 4,  /* o_shared */
       prefill ? (size_t)T * H * 4 : 0, /* y_acc */
-      l->ffn_ws_bytes};
+      l->ffn_ws_bytes,
+      256 /* route_ctl */};
   const int n = (int)(sizeof(sizes) / sizeof(sizes[0]));
   size_t total = 0;
   for (int i = 0; i < n; ++i) total += align256(sizes[i]);
@@ -155,7 +162,7 @@ MOE_API moe_status moe_layer_create(const moe_layer_desc* d, moe_layer** out) {
   }
   l->ws_bytes = total;
   uint8_t* p = (uint8_t*)l->ws;
-  void* ptrs[19];
+  void* ptrs[20];
   for (int i = 0; i < n; ++i) {
     ptrs[i] = sizes[i] ? p : nullptr;
     p += align256(sizes[i]);
@@ -179,7 +186,8 @@ MOE_API moe_status moe_layer_create(const moe_layer_desc* d, moe_layer** out) {
   l->o_shared = (float*)ptrs[16];
   l->y_acc = (float*)ptrs[17];
   l->ffn_ws = ptrs[18];
-  if (cudaMemset(l->status, 0, 4) != cudaSuccess) {
+  l->route_ctl = ptrs[19];
+  if (cudaMemset(l->ws, 0, total) != cudaSuccess) {
     cudaFree(l->ws);
     free(l);
     return MOE_ERR_CUDA;
@@ -209,14 +217,16 @@ MOE_API moe_status moe_layer_forward(moe_layer* l, const void* x, int T, void* y
   ra.x = x; ra.w_router = d.w_router; ra.bias = d.bias;
   ra.T = T; ra.H = d.H; ra.E = d.E; ra.k = d.k;
   ra.ids = l->ids; ra.w = l->w; ra.p_sel = l->p_sel; ra.logits = l->logits;
+  ra.workspace = l->route_ctl; ra.workspace_bytes = 256;
   ra.status = l->status;
   if ((st = moe_route(&ra, stream)) != MOE_OK) return st;
 
-  if ((st = moe_permute(l->ids, T, d.k, d.E, l->counts, l->offsets, l->perm, l->inv,
-                        prefill ? l->pad_offsets : nullptr, 128, l->status, stream)) != MOE_OK)
-    return st;
-  if ((st = expcache_lookup(d.cache, d.layer, l->counts, l->src_slot, l->act_list, l->n_act,
-                            l->miss_ids, l->n_miss, l->status, stream)) != MOE_OK)
+  // permutation and slot lookup in one launch
+  LookupArgs lk;
+  cache_lookup_args(d.cache, d.layer, l->src_slot, l->act_list, l->n_act, l->miss_ids, l->n_miss,
+                    &lk);
+  if ((st = launch_permute(l->ids, T, d.k, d.E, l->counts, l->offsets, l->perm, l->inv,
+                           prefill ? l->pad_offsets : nullptr, 128, l->status, lk, s)) != MOE_OK)
     return st;
 
   const int n_stage = cache_n_stage(d.cache);

@@ -77,10 +77,8 @@ __global__ void __launch_bounds__(kGatherThreads) k_gather(
 
 __global__ void k_set_table(int32_t* table_entry, int slot) { *table_entry = slot; }
 
-moe_status launch_lookup(const int32_t* table_row, int E, const int32_t* counts, int slot_lo,
-                         int slot_hi, int n_cache, int n_stage, int32_t* src_slot,
-                         int32_t* act_list, int32_t* n_act, int32_t* miss_ids, int32_t* n_miss,
-                         int32_t* status, cudaStream_t s);
+moe_status launch_lookup(const LookupArgs& a, int E, const int32_t* counts, int32_t* status,
+                         cudaStream_t s);
 
 }  // namespace moe
 
@@ -206,6 +204,22 @@ MOE_API moe_status expcache_fill(expcache* c, int layer, const int32_t* d_expert
   return MOE_OK;
 }
 
+namespace moe {
+void cache_lookup_args(const expcache* c, int layer, int32_t* src_slot, int32_t* act_list,
+                       int32_t* n_act, int32_t* miss_ids, int32_t* n_miss, LookupArgs* out) {
+  out->table = c->table + (size_t)layer * c->E;
+  out->slot_lo = c->slot_lo[layer];
+  out->slot_hi = c->slot_hi[layer];
+  out->n_cache = c->n_cache;
+  out->n_stage = c->n_stage;
+  out->src_slot = src_slot;
+  out->act_list = act_list;
+  out->n_act = n_act;
+  out->miss_ids = miss_ids;
+  out->n_miss = n_miss;
+}
+}  // namespace moe
+
 MOE_API moe_status expcache_lookup(const expcache* c, int layer, const int32_t* counts,
                                    int32_t* src_slot, int32_t* act_list, int32_t* n_act,
                                    int32_t* miss_ids, int32_t* n_miss, int32_t* status,
@@ -213,9 +227,9 @@ MOE_API moe_status expcache_lookup(const expcache* c, int layer, const int32_t* 
   if (!c || !counts || !src_slot || !act_list || !n_act || !miss_ids || !n_miss || layer < 0 ||
       layer >= c->L)
     return MOE_ERR_INVALID_ARG;
-  return launch_lookup(c->table + (size_t)layer * c->E, c->E, counts, c->slot_lo[layer],
-                       c->slot_hi[layer], c->n_cache, c->n_stage, src_slot, act_list,
-                       n_act, miss_ids, n_miss, status, (cudaStream_t)stream);
+  LookupArgs la;
+  cache_lookup_args(c, layer, src_slot, act_list, n_act, miss_ids, n_miss, &la);
+  return launch_lookup(la, c->E, counts, status, (cudaStream_t)stream);
 }
 
 // internal accessors for the FFN and the layer

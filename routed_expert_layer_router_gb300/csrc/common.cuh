@@ -17,6 +17,14 @@ __device__ __forceinline__ void set_status(int32_t* st, int32_t code) {
   if (st) atomicCAS(st, 0, code);
 }
 
+// ---- expert-cache lookup of one layer (K-lookup), run on its own or as the
+// tail of K-perm ----------------------------------------------------------------
+struct LookupArgs {
+  const int32_t* table;  // the layer's row of the slot table, nullptr: no lookup
+  int slot_lo, slot_hi, n_cache, n_stage;
+  int32_t *src_slot, *act_list, *n_act, *miss_ids, *n_miss;
+};
+
 // ---- record layout (see moe.h) ---------------------------------------------
 struct RecordLayout {
   uint64_t gate_codes, up_codes, down_codes;

@@ -26,7 +26,7 @@ constexpr int kDecWarps = 8;
 constexpr int kDecThreads = kDecWarps * 32;
 constexpr int kXPad = 36;  // fp32 staging: floats per 32 values (bank spread)
 constexpr int kHPad = 40;  // f16 staging: halves per 32 values (80-byte stride, conflict-free)
-constexpr int kSharedKSplit = 4;  // shared gate/up: warps splitting the row length
+constexpr int kSharedKSplit = kDecWarps;  // shared gate/up: warps splitting the row length
 
 struct DecodeParams {
   int T, H, I, E, k, Is;
@@ -42,7 +42,8 @@ struct DecodeParams {
   const int32_t* perm;
   const float* w;
   int group, n_stage;
-  int n_shared_units;  // leading grid units: shared expert
+  int n_shared_units;  // shared-expert grid units (down: leading; gate/up: trailing)
+  int n_routed_units;  // gate/up: leading routed grid units
   const uint16_t* s_gate;
   const uint16_t* s_up;
   const uint16_t* s_down;
@@ -305,22 +306,20 @@ __device__ void gu_routed_pass(const DecodeParams& p, const RecordLayout& L, con
       }
 }
 
-// shared expert: CTA = 8 row pairs; warp = (row group of 4 pairs) x (quarter of H)
+// shared expert: CTA = 4 row pairs (gate row i and up row i); warp = 1/8 of H
 template <int M>
 __device__ void gu_shared_pass(const DecodeParams& p, int i0, int t0, int mm, const float* xs,
                                float* red) {
   const int wid = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int rg = wid / kSharedKSplit, ks = wid % kSharedKSplit;
-  const int r0 = i0 + rg * 4;
   const uint16_t* rows[8];
 #pragma unroll
   for (int r = 0; r < 4; ++r) {
-    rows[r] = p.s_gate + (size_t)(r0 + r) * p.H;
-    rows[4 + r] = p.s_up + (size_t)(r0 + r) * p.H;
+    rows[r] = p.s_gate + (size_t)(i0 + r) * p.H;
+    rows[4 + r] = p.s_up + (size_t)(i0 + r) * p.H;
   }
   const int kq = p.H / kSharedKSplit;
   float acc[8][M];
-  warp_rows_bf16<M, 8>(rows, p.H, ks * kq, (ks + 1) * kq, xs, acc);
+  warp_rows_bf16<M, 8>(rows, p.H, wid * kq, (wid + 1) * kq, xs, acc);
 #pragma unroll
   for (int r = 0; r < 8; ++r)
 #pragma unroll
@@ -329,32 +328,34 @@ __device__ void gu_shared_pass(const DecodeParams& p, int i0, int t0, int mm, co
       if (lane == 0) red[(wid * 8 + r) * 2 + j] = v;
     }
   __syncthreads();
-  // 2 row groups x 4 pairs x mm tokens: thread -> (rg, r, j)
+  // 4 pairs x mm tokens: thread -> (r, j); the 8 warps' parts in a fixed order
   const int t = threadIdx.x;
-  if (t < 2 * 4 * 2) {
-    const int g2 = t / 8, r = (t / 2) % 4, j = t % 2;
+  if (t < 4 * 2) {
+    const int r = t / 2, j = t % 2;
     if (j < mm) {
       float g = 0.f, u = 0.f;
-      for (int s = 0; s < kSharedKSplit; ++s) {
-        const int w = g2 * kSharedKSplit + s;
+      for (int w = 0; w < kSharedKSplit; ++w) {
         g += red[(w * 8 + r) * 2 + j];
         u += red[(w * 8 + 4 + r) * 2 + j];
       }
-      p.h_shared[(size_t)(t0 + j) * p.Is + i0 + g2 * 4 + r] = silu_f(g) * u;
+      p.h_shared[(size_t)(t0 + j) * p.Is + i0 + r] = silu_f(g) * u;
     }
   }
   __syncthreads();
 }
 
+// Grid: the routed units (one expert x one 128-row tile x a quarter of its
+// 32 atom rows) first, then the shared-expert units (4 row pairs each), which
+// are half as large and so fill the last wave.
 template <int MAXM>
 __global__ void __launch_bounds__(kDecThreads) k_decode_gu(DecodeParams p) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   __shared__ float red[kDecWarps * 8 * 2];
   const int wid = threadIdx.x >> 5;
   const int u = blockIdx.x;
-  if (u < p.n_shared_units) {
+  if (u >= p.n_routed_units) {
     float* xs = reinterpret_cast<float*>(smem_raw);
-    const int i0 = u * 8;
+    const int i0 = (u - p.n_routed_units) * 4;
     for (int t0 = 0; t0 < p.T; t0 += p.maxm) {
       const int mm = min(p.maxm, p.T - t0);
       const uint16_t* rows[2];
@@ -368,7 +369,7 @@ __global__ void __launch_bounds__(kDecThreads) k_decode_gu(DecodeParams p) {
     return;
   }
   __half* xs = reinterpret_cast<__half*>(smem_raw);
-  const int ur = u - p.n_shared_units;
+  const int ur = u;
   const int tiles = p.I / 128;
   const int a = ur / (tiles * 4), rem = ur % (tiles * 4);
   const int rt = rem >> 2, m0 = (rem & 3) * kDecWarps + wid;
@@ -575,8 +576,9 @@ moe_status decode_ffn(const moe_ffn_args* a, cudaStream_t s) {
   if (a->group > 0) max_act = a->n_stage < max_act ? a->n_stage : max_act;
   const bool shared = a->group == 0 && a->Is > 0;
   if (a->stages & MOE_STAGE_GATE_UP) {
-    p.n_shared_units = shared ? a->Is / 8 : 0;
+    p.n_shared_units = shared ? a->Is / 4 : 0;
     const int routed = max_act * (a->I / 128) * 4;
+    p.n_routed_units = routed;
     size_t smem = smem_f16(p.maxm, a->H);
     if (shared && smem_f32(p.maxm, a->H) > smem) smem = smem_f32(p.maxm, a->H);
     const int grid = p.n_shared_units + routed;

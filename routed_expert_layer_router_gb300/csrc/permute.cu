@@ -40,6 +40,40 @@ __device__ int block_exclusive_scan(int v, int* s_warp, int& total) {
   return r;
 }
 
+// one expert per thread (E <= 1024 = blockDim); c = routes to expert e
+__device__ void lookup_body(const LookupArgs& a, int E, int c, int* s_scan, int32_t* status) {
+  const int e = threadIdx.x;
+  bool active = (e < E) && c > 0;
+  int slot = active ? a.table[e] : -1;
+  if (active && slot >= 0 && (slot < a.slot_lo || slot >= a.slot_hi)) {
+    set_status(status, MOE_ERR_DEVICE);  // stale or foreign slot: treat as a miss
+    slot = -1;
+  }
+  bool hit = active && slot >= 0;
+  bool miss = active && slot < 0;
+  int nh, nm;
+  int ph = block_exclusive_scan(hit ? 1 : 0, s_scan, nh);
+  int pm = block_exclusive_scan(miss ? 1 : 0, s_scan, nm);
+  if (e < E) {
+    int s = -1;
+    if (hit) {
+      s = slot;
+      a.act_list[ph] = e;
+    } else if (miss) {
+      a.act_list[nh + pm] = e;
+      a.miss_ids[pm] = e;
+      if (a.n_stage > 0) s = a.n_cache + (pm % a.n_stage);
+      else set_status(status, MOE_ERR_DEVICE);
+    }
+    a.src_slot[e] = s;
+  }
+  if (e == 0) {
+    a.n_act[0] = nh + nm;
+    a.n_act[1] = nh;
+    *a.n_miss = nm;
+  }
+}
+
 // smem: counts[E] | base[E] | wcnt[32][E] | scan scratch[33]
 __global__ void __launch_bounds__(kPermThreads) k_permute(const int32_t* __restrict__ ids, int n,
                                                           int E, int32_t* __restrict__ counts,
@@ -47,7 +81,8 @@ __global__ void __launch_bounds__(kPermThreads) k_permute(const int32_t* __restr
                                                           int32_t* __restrict__ perm,
                                                           int32_t* __restrict__ inv,
                                                           int32_t* __restrict__ pad_offsets,
-                                                          int pad_align, int32_t* status) {
+                                                          int pad_align, int32_t* status,
+                                                          LookupArgs lk) {
   extern __shared__ int sm[];
   int* s_cnt = sm;
   int* s_base = s_cnt + E;
@@ -80,6 +115,7 @@ __global__ void __launch_bounds__(kPermThreads) k_permute(const int32_t* __restr
     if (tid < E) pad_offsets[tid] = poff;
     if (tid == 0) pad_offsets[E] = ptot;
   }
+  if (lk.table) lookup_body(lk, E, c, s_scan, status);
   __syncthreads();
 
   // stable positions, 1024 routes per chunk
@@ -116,42 +152,12 @@ __global__ void __launch_bounds__(kPermThreads) k_permute(const int32_t* __restr
 }
 
 // K-lookup: one CTA of 1024 threads, one expert per thread
-__global__ void __launch_bounds__(kPermThreads) k_lookup(
-    const int32_t* __restrict__ table, int E, const int32_t* __restrict__ counts,
-    int slot_lo, int slot_hi, int n_cache, int n_stage, int32_t* __restrict__ src_slot,
-    int32_t* __restrict__ act_list, int32_t* __restrict__ n_act, int32_t* __restrict__ miss_ids,
-    int32_t* __restrict__ n_miss, int32_t* status) {
+__global__ void __launch_bounds__(kPermThreads) k_lookup(LookupArgs a, int E,
+                                                         const int32_t* __restrict__ counts,
+                                                         int32_t* status) {
   __shared__ int s_scan[33];
   const int e = threadIdx.x;
-  bool active = (e < E) && counts[e] > 0;
-  int slot = active ? table[e] : -1;
-  if (active && slot >= 0 && (slot < slot_lo || slot >= slot_hi)) {
-    set_status(status, MOE_ERR_DEVICE);  // stale or foreign slot: treat as a miss
-    slot = -1;
-  }
-  bool hit = active && slot >= 0;
-  bool miss = active && slot < 0;
-  int nh, nm;
-  int ph = block_exclusive_scan(hit ? 1 : 0, s_scan, nh);
-  int pm = block_exclusive_scan(miss ? 1 : 0, s_scan, nm);
-  if (e < E) {
-    int s = -1;
-    if (hit) {
-      s = slot;
-      act_list[ph] = e;
-    } else if (miss) {
-      act_list[nh + pm] = e;
-      miss_ids[pm] = e;
-      if (n_stage > 0) s = n_cache + (pm % n_stage);
-      else set_status(status, MOE_ERR_DEVICE);
-    }
-    src_slot[e] = s;
-  }
-  if (e == 0) {
-    n_act[0] = nh + nm;
-    n_act[1] = nh;
-    *n_miss = nm;
-  }
+  lookup_body(a, E, e < E ? counts[e] : 0, s_scan, status);
 }
 
 }  // namespace moe
@@ -171,29 +177,38 @@ moe_status permute_setup() {
 
 using namespace moe;
 
-MOE_API moe_status moe_permute(const int32_t* ids, int T, int k, int E, int32_t* counts,
-                               int32_t* offsets, int32_t* perm, int32_t* inv,
-                               int32_t* pad_offsets, int pad_align, int32_t* status,
-                               void* stream) {
+namespace moe {
+// K-perm, followed in the same launch by the expert-cache lookup when lk.table
+// is set (the layer's path: one launch instead of two)
+moe_status launch_permute(const int32_t* ids, int T, int k, int E, int32_t* counts,
+                          int32_t* offsets, int32_t* perm, int32_t* inv, int32_t* pad_offsets,
+                          int pad_align, int32_t* status, const LookupArgs& lk, cudaStream_t s) {
   if (T < 0 || k <= 0 || E <= 0 || !counts || !offsets) return MOE_ERR_INVALID_ARG;
   if (T > 0 && (!ids || !perm || !inv)) return MOE_ERR_INVALID_ARG;
   if (pad_offsets && pad_align <= 0) return MOE_ERR_INVALID_ARG;
   if (E > 1024 || (long long)T * k > (1 << 20)) return MOE_ERR_UNSUPPORTED;
   size_t smem = sizeof(int) * ((size_t)E * (2 + kPermWarps) + 33);
   if (smem > 48 * 1024 && permute_setup() != MOE_OK) return MOE_ERR_CUDA;
-  k_permute<<<1, kPermThreads, smem, (cudaStream_t)stream>>>(ids, T * k, E, counts, offsets, perm,
-                                                            inv, pad_offsets, pad_align, status);
+  k_permute<<<1, kPermThreads, smem, s>>>(ids, T * k, E, counts, offsets, perm, inv, pad_offsets,
+                                          pad_align, status, lk);
   MOE_CHECK_LAUNCH();
   return MOE_OK;
 }
+}  // namespace moe
+
+MOE_API moe_status moe_permute(const int32_t* ids, int T, int k, int E, int32_t* counts,
+                               int32_t* offsets, int32_t* perm, int32_t* inv,
+                               int32_t* pad_offsets, int pad_align, int32_t* status,
+                               void* stream) {
+  LookupArgs none = {};
+  return launch_permute(ids, T, k, E, counts, offsets, perm, inv, pad_offsets, pad_align, status,
+                        none, (cudaStream_t)stream);
+}
 
 namespace moe {
-moe_status launch_lookup(const int32_t* table_row, int E, const int32_t* counts, int slot_lo,
-                         int slot_hi, int n_cache, int n_stage, int32_t* src_slot,
-                         int32_t* act_list, int32_t* n_act, int32_t* miss_ids, int32_t* n_miss,
-                         int32_t* status, cudaStream_t s) {
-  k_lookup<<<1, kPermThreads, 0, s>>>(table_row, E, counts, slot_lo, slot_hi, n_cache, n_stage,
-                                      src_slot, act_list, n_act, miss_ids, n_miss, status);
+moe_status launch_lookup(const LookupArgs& a, int E, const int32_t* counts, int32_t* status,
+                         cudaStream_t s) {
+  k_lookup<<<1, kPermThreads, 0, s>>>(a, E, counts, status);
   MOE_CHECK_LAUNCH();
   return MOE_OK;
 }

@@ -11,11 +11,10 @@ namespace moe {
 // fixed-shape tree reduction: deterministic.
 constexpr int kGemvMaxT = 8;
 
-__global__ void __launch_bounds__(256) k_logits_gemv(const uint16_t* __restrict__ x,
-                                                     const float* __restrict__ wr,
-                                                     const float* __restrict__ bias, int T,
-                                                     int H, int E, float* __restrict__ logits) {
-  const int e = blockIdx.x;
+__device__ __forceinline__ void logits_of_expert(const uint16_t* __restrict__ x,
+                                                 const float* __restrict__ wr,
+                                                 const float* __restrict__ bias, int T, int H,
+                                                 int E, int e, float* __restrict__ logits) {
   const float4* wrow = reinterpret_cast<const float4*>(wr + (size_t)e * H);
   float acc[kGemvMaxT];
 #pragma unroll
@@ -52,6 +51,13 @@ __global__ void __launch_bounds__(256) k_logits_gemv(const uint16_t* __restrict_
     if (bias) s += bias[e];
     logits[(size_t)t * E + e] = s;
   }
+}
+
+__global__ void __launch_bounds__(256) k_logits_gemv(const uint16_t* __restrict__ x,
+                                                     const float* __restrict__ wr,
+                                                     const float* __restrict__ bias, int T,
+                                                     int H, int E, float* __restrict__ logits) {
+  logits_of_expert(x, wr, bias, T, H, E, blockIdx.x, logits);
 }
 
 // ---- logits for many tokens: SIMT tiled GEMM --------------------------------
@@ -137,19 +143,17 @@ __global__ void __launch_bounds__(256) k_logits_gemm(const uint16_t* __restrict_
 }
 
 // ---- softmax + top-k + renormalisation: one warp per token ------------------
-__global__ void __launch_bounds__(256) k_topk(const float* __restrict__ logits, int T, int E,
-                                              int k, int32_t* __restrict__ ids,
-                                              float* __restrict__ w, float* __restrict__ p_sel) {
-  extern __shared__ float sl[];  // [8 warps][E]
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  const int t = blockIdx.x * 8 + wid;
-  if (t >= T) return;
-  float* l = sl + (size_t)wid * E;
+// `src` holds the token's E logits (read once, through L2), `l` is the warp's
+// shared-memory copy of them.  Ties go to the lower expert id.
+__device__ __forceinline__ void topk_token(const float* src, float* l, int t, int E, int k,
+                                           int32_t* __restrict__ ids, float* __restrict__ w,
+                                           float* __restrict__ p_sel) {
+  const int lane = threadIdx.x & 31;
   const int per = (E + 31) / 32;
   float lmax = -INFINITY;
   for (int j = 0; j < per; ++j) {
     int e = lane + 32 * j;
-    float v = (e < E) ? logits[(size_t)t * E + e] : -INFINITY;
+    float v = (e < E) ? __ldcg(src + e) : -INFINITY;
     if (e < E) l[e] = v;
     lmax = fmaxf(lmax, v);
   }
@@ -193,12 +197,54 @@ __global__ void __launch_bounds__(256) k_topk(const float* __restrict__ logits, 
   }
 }
 
+__global__ void __launch_bounds__(256) k_topk(const float* __restrict__ logits, int T, int E,
+                                              int k, int32_t* __restrict__ ids,
+                                              float* __restrict__ w, float* __restrict__ p_sel) {
+  extern __shared__ float sl[];  // [8 warps][E]
+  const int wid = threadIdx.x >> 5;
+  const int t = blockIdx.x * 8 + wid;
+  if (t >= T) return;
+  topk_token(logits + (size_t)t * E, sl + (size_t)wid * E, t, E, k, ids, w, p_sel);
+}
+
+// ---- few tokens: logits and top-k in one kernel -----------------------------
+// One CTA per expert computes that expert's logit for every token (as
+// k_logits_gemv); the CTA that finishes last (a counter in the caller's
+// workspace, zero before the launch and reset by that CTA) then runs the
+// softmax/top-k, one warp per token, on the logits the others wrote.
+__global__ void __launch_bounds__(256) k_route_small(const uint16_t* __restrict__ x,
+                                                     const float* __restrict__ wr,
+                                                     const float* __restrict__ bias, int T,
+                                                     int H, int E, int k,
+                                                     float* __restrict__ logits,
+                                                     int32_t* __restrict__ ids,
+                                                     float* __restrict__ w,
+                                                     float* __restrict__ p_sel,
+                                                     unsigned int* __restrict__ done) {
+  extern __shared__ float sl[];  // [8 warps][E]
+  __shared__ int s_last;
+  logits_of_expert(x, wr, bias, T, H, E, blockIdx.x, logits);
+  __threadfence();  // this CTA's logits are visible before it is counted
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = atomicAdd(done, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const int wid = threadIdx.x >> 5;
+  if (wid < T) topk_token(logits + (size_t)wid * E, sl + (size_t)wid * E, wid, E, k, ids, w, p_sel);
+  if (threadIdx.x == 0) *done = 0u;  // ready for the next call
+}
+
 }  // namespace moe
 
 using namespace moe;
 
+// workspace: a 256-byte control area (the few-token kernel's completion
+// counter), then the logits when the caller passes none
+constexpr size_t kRouteCtl = 256;
+
 MOE_API size_t moe_route_workspace_bytes(int T, int E) {
-  return (T > 0 && E > 0) ? (size_t)T * E * sizeof(float) : 0;
+  return (T > 0 && E > 0) ? kRouteCtl + (size_t)T * E * sizeof(float) : 0;
 }
 
 MOE_API moe_status moe_route(const moe_route_args* a, void* stream) {
@@ -211,10 +257,18 @@ MOE_API moe_status moe_route(const moe_route_args* a, void* stream) {
   if (!logits) {
     if (!a->workspace || a->workspace_bytes < moe_route_workspace_bytes(a->T, a->E))
       return MOE_ERR_INVALID_ARG;
-    logits = (float*)a->workspace;
+    logits = (float*)((char*)a->workspace + kRouteCtl);
   }
   cudaStream_t s = (cudaStream_t)stream;
   const uint16_t* x = (const uint16_t*)a->x;
+  size_t smem = (size_t)8 * a->E * sizeof(float);
+  if (a->T <= kGemvMaxT && a->workspace && a->workspace_bytes >= kRouteCtl) {
+    k_route_small<<<a->E, 256, smem, s>>>(x, a->w_router, a->bias, a->T, a->H, a->E, a->k,
+                                          logits, a->ids, a->w, a->p_sel,
+                                          (unsigned int*)a->workspace);
+    MOE_CHECK_LAUNCH();
+    return MOE_OK;
+  }
   if (a->T <= kGemvMaxT) {
     k_logits_gemv<<<a->E, 256, 0, s>>>(x, a->w_router, a->bias, a->T, a->H, a->E, logits);
   } else {
@@ -222,7 +276,6 @@ MOE_API moe_status moe_route(const moe_route_args* a, void* stream) {
     k_logits_gemm<<<grid, 256, 0, s>>>(x, a->w_router, a->bias, a->T, a->H, a->E, logits);
   }
   MOE_CHECK_LAUNCH();
-  size_t smem = (size_t)8 * a->E * sizeof(float);
   k_topk<<<(a->T + 7) / 8, 256, smem, s>>>(logits, a->T, a->E, a->k, a->ids, a->w, a->p_sel);
   MOE_CHECK_LAUNCH();
   return MOE_OK;

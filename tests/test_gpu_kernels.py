@@ -52,7 +52,9 @@ def test_device_generator_matches_host(H, I):
     assert np.array_equal(sd.cpu().numpy().view(np.uint16), hd)
 
 
-def _route_gpu(x, Wr, bias, k):
+def _route_gpu(x, Wr, bias, k, ctl=None):
+    """moe_route; with `ctl` (a zeroed device buffer) the call gets a workspace
+    control area, which lets up to 8 tokens run as one kernel."""
     from routed_expert_layer_router_gb300 import moe
     T, H = x.shape
     E = Wr.shape[0]
@@ -67,24 +69,32 @@ def _route_gpu(x, Wr, bias, k):
     a.x, a.w_router, a.bias = xd.data_ptr(), wd.data_ptr(), bd.data_ptr() if bd is not None else None
     a.T, a.H, a.E, a.k = T, H, E, k
     a.ids, a.w, a.p_sel, a.logits = ids.data_ptr(), w.data_ptr(), p.data_ptr(), lg.data_ptr()
+    if ctl is not None:
+        a.workspace, a.workspace_bytes = ctl.data_ptr(), ctl.numel()
     moe.moe_route(a, _stream())
     torch.cuda.synchronize()
     return ids.cpu().numpy(), w.cpu().numpy(), p.cpu().numpy(), lg.cpu().numpy()
 
 
-@pytest.mark.parametrize("name,T", [("tiny", 4), ("tiny", 37), ("decode", 1), ("decode", 8),
-                                    ("decode", 64), ("decode", 300)])
-def test_route_parity(name, T):
+@pytest.mark.parametrize("name,T,one_kernel", [
+    ("tiny", 4, False), ("tiny", 37, False), ("decode", 1, False), ("decode", 8, False),
+    ("decode", 64, False), ("decode", 300, False),
+    ("tiny", 4, True), ("decode", 1, True), ("decode", 8, True), ("decode", 64, True)])
+def test_route_parity(name, T, one_kernel):
     wl = gen.WORKLOADS[name]
     Wr = gen.router_f32(wl.seed, 0, wl.E, wl.H)
     bias = gen.zipf_bias(wl.seed, 0, wl.E, 1.556)[0] if T == 8 else None
     x, _ = draw_tokens(wl, 0, T, Wr, bias)
     ids_r, w_r, p_r, lg_r, _ = oracle.route(x, Wr, bias, wl.k)
-    ids, w, p, lg = _route_gpu(x, Wr, bias, wl.k)
-    assert np.array_equal(ids, ids_r)
-    assert np.all(np.abs(w - w_r) <= PROB_RTOL * w_r)
-    assert np.all(np.abs(p - p_r) <= PROB_RTOL * p_r)
-    assert np.abs(lg - lg_r).max() <= 1e-5 * np.abs(lg_r).max()
+    ctl = torch.zeros(256, dtype=torch.uint8, device="cuda") if one_kernel else None
+    for _ in range(2 if one_kernel else 1):  # the control area is reset by each call
+        ids, w, p, lg = _route_gpu(x, Wr, bias, wl.k, ctl)
+        assert np.array_equal(ids, ids_r)
+        assert np.all(np.abs(w - w_r) <= PROB_RTOL * w_r)
+        assert np.all(np.abs(p - p_r) <= PROB_RTOL * p_r)
+        assert np.abs(lg - lg_r).max() <= 1e-5 * np.abs(lg_r).max()
+    if one_kernel:
+        assert int(ctl.view(torch.int32)[0].item()) == 0
 
 
 @pytest.mark.parametrize("T,k,E", [(1, 8, 288), (4, 2, 16), (64, 8, 288), (4096, 8, 288),
