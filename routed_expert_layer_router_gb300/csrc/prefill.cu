@@ -554,6 +554,101 @@ __global__ void __launch_bounds__(256) k_quant_rows(QuantParams p) {
   }
 }
 
+// ---- activation quantisation, once per token ---------------------------------------
+// K-actq: one warp per token, the same arithmetic as k_quant_rows (G =
+// amax/2688, block scale e4m3_rne(amax_b/(6G)), codes e2m1_rne_sat(v/(s G)),
+// all fp32 with IEEE division), into a token-major buffer: codes [T][K/2],
+// scales [T][K/16] (block b at byte b), G [T].
+__global__ void __launch_bounds__(256) k_quant_tokens(const uint16_t* __restrict__ x, int T, int K,
+                                                     uint8_t* __restrict__ codes,
+                                                     uint8_t* __restrict__ scales,
+                                                     float* __restrict__ Gt) {
+  const int lane = threadIdx.x & 31;
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  const int KB = K / 16;
+  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += warps) {
+    const uint16_t* xr = x + (size_t)t * K;
+    float amax = 0.f;
+    for (int i = lane; i < K / 8; i += 32) {  // 8 values per 16-byte load
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(xr) + i);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[q])), fabsf(bf16_hi(w[q]))));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    const float G = amax > 0.f ? __fdiv_rn(amax, 2688.0f) : 1.0f;
+    const float sixG = __fmul_rn(6.0f, G);
+    for (int b = lane; b < KB; b += 32) {
+      float v[16];
+      const uint4 a0 = __ldg(reinterpret_cast<const uint4*>(xr + b * 16));
+      const uint4 a1 = __ldg(reinterpret_cast<const uint4*>(xr + b * 16 + 8));
+      const uint32_t w[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        v[2 * i] = bf16_lo(w[i]);
+        v[2 * i + 1] = bf16_hi(w[i]);
+      }
+      float ab = 0.f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) ab = fmaxf(ab, fabsf(v[i]));
+      const uint32_t sc = e4m3_rne(__fdiv_rn(ab, sixG));
+      const float sdq = __fmul_rn(e4m3_value(sc), G);
+      uint32_t lo = 0, hi = 0;
+      if (sc != 0) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint32_t c0 = e2m1_rne_sat(__fdiv_rn(v[2 * i], sdq));
+          const uint32_t c1 = e2m1_rne_sat(__fdiv_rn(v[2 * i + 1], sdq));
+          const uint32_t byte = c0 | (c1 << 4);
+          if (i < 4) lo |= byte << (8 * i);
+          else hi |= byte << (8 * (i - 4));
+        }
+      }
+      *reinterpret_cast<uint2*>(codes + (size_t)t * (K / 2) + (size_t)b * 8) = make_uint2(lo, hi);
+      scales[(size_t)t * KB + b] = (uint8_t)sc;
+    }
+    if (lane == 0) Gt[t] = G;
+  }
+}
+
+// K-expand: one CTA per expert; route position p of the expert (token
+// perm[p] / k) goes to padded row pad_offsets[e] + (p - offsets[e]): its codes
+// row, its scales into the 512-byte atoms of the tcgen05 scale layout, its G.
+// Padding rows of the segment are zeroed.
+__global__ void __launch_bounds__(256) k_expand_routes(
+    const uint8_t* __restrict__ tcodes, const uint8_t* __restrict__ tscales,
+    const float* __restrict__ tG, int K, int E, int k, const int32_t* __restrict__ offsets,
+    const int32_t* __restrict__ pad_offsets, const int32_t* __restrict__ perm,
+    uint8_t* __restrict__ codes, uint8_t* __restrict__ scales, float* __restrict__ G) {
+  const int e = blockIdx.x;
+  if (e >= E) return;
+  const int p0 = offsets[e], cnt = offsets[e + 1] - p0;
+  const int r0 = pad_offsets[e], nrow = pad_offsets[e + 1] - r0;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int KB = K / 16, KG = K / 64, nc16 = K / 32;  // 16-byte chunks of a codes row
+  for (int i = wid; i < nrow; i += nw) {
+    const int row = r0 + i;
+    const int rt = row >> 7, m0 = row & 31, m1 = (row & 127) >> 5;
+    uint4* dst = reinterpret_cast<uint4*>(codes + (size_t)row * (K / 2));
+    if (i < cnt) {
+      const int t = perm[p0 + i] / k;
+      const uint4* src = reinterpret_cast<const uint4*>(tcodes + (size_t)t * (K / 2));
+      for (int c = lane; c < nc16; c += 32) dst[c] = __ldg(src + c);
+      const uint32_t* ssrc = reinterpret_cast<const uint32_t*>(tscales + (size_t)t * KB);
+      for (int g = lane; g < KG; g += 32)  // 4 blocks = one atom word of this row
+        *reinterpret_cast<uint32_t*>(scales + ((size_t)rt * KG + g) * 512 + m0 * 16 + m1 * 4) =
+            __ldg(ssrc + g);
+      if (lane == 0) G[row] = tG[t];
+    } else {
+      for (int c = lane; c < nc16; c += 32) dst[c] = make_uint4(0u, 0u, 0u, 0u);
+      for (int g = lane; g < KG; g += 32)
+        *reinterpret_cast<uint32_t*>(scales + ((size_t)rt * KG + g) * 512 + m0 * 16 + m1 * 4) = 0u;
+      if (lane == 0) G[row] = 0.f;
+    }
+  }
+}
+
 // ---- host side ---------------------------------------------------------------------
 static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
@@ -589,7 +684,8 @@ static moe_status make_map(CUtensorMap* m, const void* base, bool bf16, uint64_t
 // workspace layout for a prefill call on T tokens
 struct PrefillWs {
   size_t rows;  // padded rows
-  size_t xq_codes, xq_scales, xq_G, h32, hq_codes, hq_scales, hq_G, hs, total;
+  size_t xq_codes, xq_scales, xq_G, h32, hq_codes, hq_scales, hq_G, hs, tq_codes, tq_scales,
+      tq_G, total;
   PrefillWs(int T, int H, int I, int E, int k, int Is) {
     rows = (((size_t)T * k + (size_t)E * (kTileN - 1)) + kTileN - 1) / kTileN * kTileN;
     size_t o = 0;
@@ -602,6 +698,9 @@ struct PrefillWs {
     hq_scales = take(rows * I / 16);
     hq_G = take(rows * 4);
     hs = take((size_t)T * Is * 2);
+    tq_codes = take((size_t)T * H / 2);  // token-major quantised activations
+    tq_scales = take((size_t)T * H / 16);
+    tq_G = take((size_t)T * 4);
     total = o + 1024;
   }
 };
@@ -666,17 +765,24 @@ moe_status prefill_ffn(const moe_ffn_args* a, cudaStream_t s) {
                                                                         : kMaxGroup)
                                        : kMaxGroup;
   const int max_act = a->T * a->k < a->E ? a->T * a->k : a->E;
+  // the tokens, quantised once each, then copied to their routes' padded rows
+  {
+    const int grid = (a->T + 7) / 8 < kSMs * 8 ? (a->T + 7) / 8 : kSMs * 8;
+    k_quant_tokens<<<grid, 256, 0, s>>>((const uint16_t*)a->x, a->T, H, ws + W.tq_codes,
+                                        ws + W.tq_scales, (float*)(ws + W.tq_G));
+    MOE_CHECK_LAUNCH();
+    k_expand_routes<<<a->E, 256, 0, s>>>(ws + W.tq_codes, ws + W.tq_scales,
+                                         (const float*)(ws + W.tq_G), H, a->E, a->k, a->offsets,
+                                         a->pad_offsets, a->perm, ws + W.xq_codes,
+                                         ws + W.xq_scales, (float*)(ws + W.xq_G));
+    MOE_CHECK_LAUNCH();
+  }
   for (int g0 = 0; g0 < max_act; g0 += grp) {
     QuantParams q;
     memset(&q, 0, sizeof(q));
     q.g0 = g0; q.g1 = g0 + grp;
     q.act_list = a->act_list; q.n_act = a->n_act; q.offsets = a->offsets;
     q.pad_offsets = a->pad_offsets; q.perm = a->perm; q.k = a->k;
-    q.K = H;
-    q.x = (const uint16_t*)a->x;
-    q.codes = ws + W.xq_codes; q.scales = ws + W.xq_scales; q.G = (float*)(ws + W.xq_G);
-    k_quant_rows<false><<<kSMs * 8, 256, 0, s>>>(q);
-    MOE_CHECK_LAUNCH();
 
     GemmParams gp;
     memset(&gp, 0, sizeof(gp));

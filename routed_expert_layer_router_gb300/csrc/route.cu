@@ -61,47 +61,70 @@ __global__ void __launch_bounds__(256) k_logits_gemv(const uint16_t* __restrict_
 }
 
 // ---- logits for many tokens: SIMT tiled GEMM --------------------------------
-// Tile 64 tokens x 64 experts, 256 threads, 4x4 outputs each, K chunks of 32.
+// Tile 64 tokens x 32 experts, 128 threads, 4x4 outputs each, K chunks of 32.
 // Each chunk's partial sum is added to the running total with Kahan
 // compensation, keeping the fp32 error of the 6144-term dot products near
 // that of the chunk sums (the router probabilities are compared at 1e-5).
-constexpr int kTM = 64, kTN = 64, kTK = 32;
+// The next chunk's global loads are issued before the current chunk is
+// computed; the x tile is stored transposed (k-major) so that every thread
+// reads its 4 tokens and 4 experts of a k as two 16-byte shared loads.
+// 288 experts = 9 tiles: 576 CTAs of 128 threads for 4096 tokens, about four
+// per SM, all resident at once.
+constexpr int kTM = 64, kTN = 32, kTK = 32, kGemmThreads = 128;
 
-__global__ void __launch_bounds__(256) k_logits_gemm(const uint16_t* __restrict__ x,
-                                                     const float* __restrict__ wr,
-                                                     const float* __restrict__ bias, int T,
-                                                     int H, int E, float* __restrict__ logits) {
-  __shared__ float xs[kTK][kTM + 4];
-  __shared__ float ws[kTK][kTN + 4];
+__global__ void __launch_bounds__(kGemmThreads) k_logits_gemm(const uint16_t* __restrict__ x,
+                                                              const float* __restrict__ wr,
+                                                              const float* __restrict__ bias,
+                                                              int T, int H, int E,
+                                                              float* __restrict__ logits) {
+  __shared__ __align__(16) float xs[kTK][kTM + 4];
+  __shared__ __align__(16) float ws[kTK][kTN + 4];
   const int t0 = blockIdx.y * kTM, e0 = blockIdx.x * kTN;
-  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const int tid = threadIdx.x;
+  const int tx = tid & 7, ty = tid >> 3;  // 8 x 16 threads, 4 x 4 outputs each
+  // load roles: x: token lm = tid % 64, k half lkh = tid / 64 (16 values);
+  //             W: expert ln = tid % 32, k quarter lkq = tid / 32 (8 values)
+  const int lm = tid & 63, lkh = tid >> 6, ln = tid & 31, lkq = tid >> 5;
+  const bool xok = t0 + lm < T, wok = e0 + ln < E;
+  const uint4* xsrc = reinterpret_cast<const uint4*>(x + (size_t)(xok ? t0 + lm : 0) * H + lkh * 16);
+  const float4* wsrc = reinterpret_cast<const float4*>(wr + (size_t)(wok ? e0 + ln : 0) * H + lkq * 8);
+  uint4 xa, xb;
+  float4 wa, wb;
+  auto fetch = [&](int k0) {
+    if (xok) {
+      xa = __ldg(xsrc + k0 / 8);
+      xb = __ldg(xsrc + k0 / 8 + 1);
+    } else {
+      xa = xb = make_uint4(0u, 0u, 0u, 0u);
+    }
+    if (wok) {
+      wa = __ldg(wsrc + k0 / 4);
+      wb = __ldg(wsrc + k0 / 4 + 1);
+    } else {
+      wa = wb = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  };
   float acc[4][4], cmp[4][4];
 #pragma unroll
   for (int i = 0; i < 4; ++i)
 #pragma unroll
     for (int j = 0; j < 4; ++j) acc[i][j] = cmp[i][j] = 0.f;
-
+  fetch(0);
   for (int k0 = 0; k0 < H; k0 += kTK) {
-    // load x tile: 64 tokens x 32 k (bf16) -> transposed fp32
-    for (int idx = threadIdx.x; idx < kTM * kTK / 2; idx += 256) {
-      int tt = idx / (kTK / 2), kk = (idx % (kTK / 2)) * 2;
-      int t = t0 + tt;
-      uint32_t v = 0;
-      if (t < T) v = __ldg(reinterpret_cast<const uint32_t*>(x + (size_t)t * H + k0 + kk));
-      xs[kk][tt] = bf16_lo(v);
-      xs[kk + 1][tt] = bf16_hi(v);
-    }
-    for (int idx = threadIdx.x; idx < kTN * kTK / 4; idx += 256) {
-      int ee = idx / (kTK / 4), kk = (idx % (kTK / 4)) * 4;
-      int e = e0 + ee;
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (e < E) v = __ldg(reinterpret_cast<const float4*>(wr + (size_t)e * H + k0 + kk));
-      ws[kk][ee] = v.x;
-      ws[kk + 1][ee] = v.y;
-      ws[kk + 2][ee] = v.z;
-      ws[kk + 3][ee] = v.w;
+    __syncthreads();  // the previous chunk's reads of xs / ws are done
+    {
+      const uint32_t v[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        xs[lkh * 16 + 2 * i][lm] = bf16_lo(v[i]);
+        xs[lkh * 16 + 2 * i + 1][lm] = bf16_hi(v[i]);
+      }
+      const float w8[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) ws[lkq * 8 + i][ln] = w8[i];
     }
     __syncthreads();
+    if (k0 + kTK < H) fetch(k0 + kTK);  // in flight during this chunk's FMAs
     float part[4][4];
 #pragma unroll
     for (int i = 0; i < 4; ++i)
@@ -109,15 +132,13 @@ __global__ void __launch_bounds__(256) k_logits_gemm(const uint16_t* __restrict_
       for (int j = 0; j < 4; ++j) part[i][j] = 0.f;
 #pragma unroll 8
     for (int kk = 0; kk < kTK; ++kk) {
-      float a[4], b[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) a[i] = xs[kk][ty * 4 + i];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) b[j] = ws[kk][tx * 4 + j];
+      const float4 a = *reinterpret_cast<const float4*>(&xs[kk][ty * 4]);
+      const float4 b = *reinterpret_cast<const float4*>(&ws[kk][tx * 4]);
+      const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
       for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) part[i][j] = fmaf(a[i], b[j], part[i][j]);
+        for (int j = 0; j < 4; ++j) part[i][j] = fmaf(av[i], bv[j], part[i][j]);
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i)
@@ -128,15 +149,14 @@ __global__ void __launch_bounds__(256) k_logits_gemm(const uint16_t* __restrict_
         cmp[i][j] = (s - acc[i][j]) - y;
         acc[i][j] = s;
       }
-    __syncthreads();
   }
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    int t = t0 + ty * 4 + i;
+    const int t = t0 + ty * 4 + i;
     if (t >= T) continue;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      int e = e0 + tx * 4 + j;
+      const int e = e0 + tx * 4 + j;
       if (e < E) logits[(size_t)t * E + e] = acc[i][j] + (bias ? bias[e] : 0.f);
     }
   }
@@ -273,7 +293,8 @@ MOE_API moe_status moe_route(const moe_route_args* a, void* stream) {
     k_logits_gemv<<<a->E, 256, 0, s>>>(x, a->w_router, a->bias, a->T, a->H, a->E, logits);
   } else {
     dim3 grid((a->E + kTN - 1) / kTN, (a->T + kTM - 1) / kTM);
-    k_logits_gemm<<<grid, 256, 0, s>>>(x, a->w_router, a->bias, a->T, a->H, a->E, logits);
+    k_logits_gemm<<<grid, kGemmThreads, 0, s>>>(x, a->w_router, a->bias, a->T, a->H, a->E,
+                                                logits);
   }
   MOE_CHECK_LAUNCH();
   k_topk<<<(a->T + 7) / 8, 256, smem, s>>>(logits, a->T, a->E, a->k, a->ids, a->w, a->p_sel);
