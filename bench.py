@@ -390,7 +390,7 @@ def bench_decode(args, torch, moe, gen, gd, dev, rank, world, local_rank, peaks)
 
 
 # --------------------------------------------------------------- prefill
-def bench_prefill(args, torch, moe, gen, gd, dev, peaks):
+def bench_prefill(args, torch, moe, gen, gd, dev, peaks, group=None):
     wl = gen.WORKLOADS["prefill"]
     if args.prefill_experts > 0:
         # profiler captures only: fewer experts and proportionally fewer tokens,
@@ -399,7 +399,10 @@ def bench_prefill(args, torch, moe, gen, gd, dev, peaks):
         wl = gen.Workload(**{**wl.__dict__, "name": "prefill-part", "E": E2,
                              "T": max(128, (wl.T * E2 // wl.E) // 128 * 128)})
     T, H, I, E, k, Is = wl.T, wl.H, wl.I, wl.E, wl.k, wl.Is
-    dw = gd.build(wl, T_max=T)
+    # experts per launch group: all at once unless asked (every expert is
+    # resident in HBM, so the walk needs no staging buffer)
+    dw_group = (0 if args.prefill_group is None else args.prefill_group) if group is None else group
+    dw = gd.build(wl, T_max=T, prefill_group=dw_group)
     layer = dw.moe_layers[0]
     stream = torch.cuda.current_stream()
     sp = stream.cuda_stream
@@ -451,7 +454,8 @@ def bench_prefill(args, torch, moe, gen, gd, dev, peaks):
     fp4_peak = peaks["bf16_tflops"] * FP4_OVER_BF16
     res = {
         "workload": "prefill MoE layer: 4096 tokens, H=6144, I=2048, 288 experts top-8, bf16 "
-                    "shared expert, all experts resident, groups of 64 experts",
+                    "shared expert, all experts resident, experts walked in act_list order in "
+                    + (f"launch groups of {dw_group}" if dw_group else "one launch per GEMM"),
         "value": round(T / (ms * 1e-3), 1), "unit": UNIT, "ms_per_step": round(ms, 4),
         "roofline": {
             "bound": "hbm", "unit": "GB/s",
@@ -665,11 +669,8 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.empty_cache()
     if rank == 0 and not args.decode_only and not args.small:
         also = {}
-        try:
-            also["prefill"] = bench_prefill(args, torch, moe, gen, gd, dev, peaks)
-        except Exception as exc:  # reported, not hidden
-            also["prefill"] = {"error": repr(exc)}
-        torch.cuda.empty_cache()
+        # the link-bound stacks first: after the prefill passes (two 6 GB
+        # layers built and freed) the gathers over the host link measured slower
         try:
             link = link_h2d_gbs(torch, dev)
             also["link_h2d_gbs"] = round(link, 1)
@@ -681,6 +682,19 @@ def run_ours(args, rank, world, local_rank):
                 torch.cuda.empty_cache()
         except Exception as exc:
             also["link_h2d_gbs"] = {"error": repr(exc)}
+        try:
+            also["prefill"] = bench_prefill(args, torch, moe, gen, gd, dev, peaks)
+        except Exception as exc:  # reported, not hidden
+            also["prefill"] = {"error": repr(exc)}
+        torch.cuda.empty_cache()
+        try:  # the same layer walked in launch groups of 64 experts
+            g64 = bench_prefill(args, torch, moe, gen, gd, dev, peaks,
+                                group=gen.WORKLOADS["prefill"].group)
+            also["prefill_groups64"] = {k: g64[k] for k in ("workload", "value", "unit",
+                                                             "ms_per_step")}
+        except Exception as exc:
+            also["prefill_groups64"] = {"error": repr(exc)}
+        torch.cuda.empty_cache()
         out["also"] = also
     return out
 
@@ -692,6 +706,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--flush-mb", type=int, default=512)
+    ap.add_argument("--prefill-group", type=int, default=None,
+                    help="experts per prefill launch group (default: the workload's 64; 0 = all)")
     ap.add_argument("--prewarm-s", type=float, default=1.0)
     ap.add_argument("--prefill-steps", type=int, default=10)
     ap.add_argument("--stack-steps", type=int, default=20)

@@ -58,7 +58,7 @@ def _hot_set(wl: gen.Workload, layer: int, bias_rank, saliency_order):
 def build(wl: gen.Workload, layers: int | None = None, T_max: int | None = None,
           n_stage: int | None = None, saliency_order=None, prefill_min_tokens: int | None = None,
           alias_host_records: bool = False, resident=None, slot_alias: int = 0,
-          stream=None) -> DeviceWorkload:
+          stream=None, prefill_group: int | None = None) -> DeviceWorkload:
     """Device-resident layer(s) of workload `wl`.
 
     layers: how many of the workload's layers to build (default: all).
@@ -169,7 +169,8 @@ def build(wl: gen.Workload, layers: int | None = None, T_max: int | None = None,
         bias.append(b)
         shared.append(sh)
         mls.append(MoELayer(cache, l, wr, g, k, bias=b, shared=sh, T_max=T_max,
-                            prefill_min_tokens=pmin, prefill_group=wl.group))
+                            prefill_min_tokens=pmin,
+                            prefill_group=wl.group if prefill_group is None else prefill_group))
     s.synchronize()
     return DeviceWorkload(wl, L, cache, mls, w_router, gscale, gscale_host, bias, bias_host,
                           shared, resident, host_arena, record_layer=rec_layer)

@@ -235,7 +235,7 @@ typedef struct {
   const int32_t* perm;       /* device [T*k] (moe_permute)                            */
   const float* w;            /* device [T][k] routing weights (moe_route)            */
   int group, n_stage;        /* expert group walked by this call                     */
-  int prefill_group;         /* PREFILL: experts per launch group (<= 128; 0 = 128)  */
+  int prefill_group;         /* PREFILL: experts per launch group (0 = all at once)  */
   int Is;                    /* shared expert intermediate size, 0 = none            */
   const void* s_gate;        /* device bf16 [Is][H]                                   */
   const void* s_up;          /* device bf16 [Is][H]                                   */

@@ -18,7 +18,8 @@
 //            adds each route's 128-value row segment into y_acc[token] with
 //            TMA bulk reductions (the weighted combine).
 // The bf16 shared expert runs through the same GEMM with kind::f16.
-// Experts are walked in groups (64 by default) in act_list order.
+// Experts are walked in act_list order in launch groups of prefill_group
+// experts (0: every expert in one launch per GEMM).
 // Sources: Strata-GLM blog, "Day one" list (chunked prefill: each layer's
 // experts run as one batched matrix multiply per chunk); dev.to page,
 // "Prefill in groups of 64 experts"; "Project Maya" page, "440 tokens a
@@ -42,7 +43,6 @@ namespace pf {
 constexpr int kTileM = 128, kTileN = 128, kStageKB = 128;  // K bytes per stage and operand row
 constexpr int kStages = 4;
 constexpr int kThreads = 192;  // warp 0: TMA, warp 1: MMA, warps 2..5: epilogue
-constexpr int kMaxGroup = 128; // experts per launch (prefix table in shared memory)
 constexpr uint64_t kWaitNs = 2000000000ull;  // no wait lasts longer than 2 s
 constexpr uint32_t kTmemCols = 512;
 
@@ -51,11 +51,14 @@ enum Epi { EPI_GU_ROUTED = 0, EPI_GU_SHARED = 1, EPI_DOWN_ROUTED = 2, EPI_DOWN_S
 struct GemmParams {
   int mtiles;   // 128-row weight tiles per expert
   int kstages;  // K / (128 bytes of each operand row)
-  // routed experts of this launch: act_list[g0 .. g1) clipped to n_act[1] (hits)
-  const int32_t* act_list;
-  const int32_t* n_act;
+  // routed experts of this launch: planned experts [g0, g1) (act_list order),
+  // their tiles tiles[plan_begin[g0]*mtiles .. plan_begin[g1]*mtiles)
+  const uint32_t* tiles;     // packed (expert index j, m tile, n tile)
+  const int32_t* plan_e;     // expert id of index j
+  const int32_t* plan_slot;  // its cache slot
+  const int32_t* plan_begin; // prefix of its 128-route column tiles
+  const int32_t* plan_n;     // [0]: planned experts
   int g0, g1;
-  const int32_t* src_slot;
   const int32_t* offsets;
   const int32_t* pad_offsets;
   const int32_t* perm;
@@ -80,29 +83,89 @@ struct GemmParams {
 };
 
 // ---- tile schedule ------------------------------------------------------------
-struct Sched {
-  int n;                     // experts in this launch
-  int e[kMaxGroup];
-  int slot[kMaxGroup];
-  int ntiles[kMaxGroup];     // 128-route column tiles of the expert
-  int tile_begin[kMaxGroup + 1];
-};
+// packed tile entry: expert index j (11 bits) | m tile (8 bits) | n tile (13 bits)
+__host__ __device__ __forceinline__ uint32_t tile_pack(int j, int mt, int nt) {
+  return ((uint32_t)j << 21) | ((uint32_t)mt << 13) | (uint32_t)nt;
+}
 
-// tile t -> (expert index j, m tile, n tile); returns false past the end
-__device__ __forceinline__ bool tile_coords(const Sched& S, int mtiles, int t, int& j, int& mt,
-                                            int& nt) {
-  if (t >= S.tile_begin[S.n]) return false;
-  int lo = 0, hi = S.n - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (S.tile_begin[mid] <= t) lo = mid; else hi = mid - 1;
+// tile t of a launch -> (m tile, n tile, expert id, slot)
+template <bool ROUTED>
+__device__ __forceinline__ void tile_info(const GemmParams& p, int t, int& mt, int& nt, int& e,
+                                          int& slot) {
+  if (ROUTED) {
+    const uint32_t v = p.tiles[t];
+    const int j = (int)(v >> 21);
+    mt = (int)((v >> 13) & 0xFFu);
+    nt = (int)(v & 0x1FFFu);
+    e = p.plan_e[j];
+    slot = p.plan_slot[j];
+  } else {
+    const int ntn = (p.T + kTileN - 1) / kTileN;
+    mt = t / ntn;
+    nt = t % ntn;
+    e = 0;
+    slot = 0;
   }
-  j = lo;
-  const int local = t - S.tile_begin[j];
-  mt = local / S.ntiles[j];
-  nt = local % S.ntiles[j];
-  (void)mtiles;
-  return true;
+}
+
+// K-plan: the routed experts in act_list order (all hits: the prefill path
+// reads every active expert from a cache slot), their 128-route column tiles,
+// and the tile tables of the gate/up (mt_gu row tiles) and down (mt_dn) GEMMs.
+// One CTA of 1024 threads, one expert per thread.
+__global__ void __launch_bounds__(1024) k_tile_plan(
+    const int32_t* __restrict__ act_list, const int32_t* __restrict__ n_act,
+    const int32_t* __restrict__ offsets, const int32_t* __restrict__ src_slot, int n_slots, int E,
+    int mt_gu, int mt_dn, uint32_t* __restrict__ tiles_gu, uint32_t* __restrict__ tiles_dn,
+    int32_t* __restrict__ plan_e, int32_t* __restrict__ plan_slot,
+    int32_t* __restrict__ plan_begin, int32_t* __restrict__ plan_n, int32_t* status) {
+  __shared__ int s_w[33];
+  const int j = threadIdx.x, lane = j & 31, wid = j >> 5;
+  const int hits = n_act[1];
+  if (j == 0 && n_act[0] != hits) set_status(status, MOE_ERR_DEVICE);
+  int e = -1, slot = -1, nt = 0;
+  if (j < hits && j < E) {
+    e = act_list[j];
+    slot = src_slot[e];
+    const int cnt = offsets[e + 1] - offsets[e];
+    if (slot < 0 || slot >= n_slots) set_status(status, MOE_ERR_DEVICE);
+    else nt = (cnt + kTileN - 1) / kTileN;
+  }
+  // block-wide exclusive scan of nt
+  int incl = nt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) s_w[wid] = incl;
+  __syncthreads();
+  if (wid == 0) {
+    const int w = lane < (int)(blockDim.x >> 5) ? s_w[lane] : 0;
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xFFFFFFFFu, wi, o);
+      if (lane >= o) wi += v;
+    }
+    s_w[lane] = wi - w;
+    if (lane == 31) s_w[32] = wi;
+  }
+  __syncthreads();
+  const int begin = s_w[wid] + incl - nt;
+  const int n = hits < E ? hits : E;
+  if (j < n) {
+    plan_e[j] = e;
+    plan_slot[j] = slot;
+    plan_begin[j] = begin;
+    for (int m = 0; m < mt_gu; ++m)
+      for (int c = 0; c < nt; ++c) tiles_gu[(size_t)begin * mt_gu + m * nt + c] = tile_pack(j, m, c);
+    for (int m = 0; m < mt_dn; ++m)
+      for (int c = 0; c < nt; ++c) tiles_dn[(size_t)begin * mt_dn + m * nt + c] = tile_pack(j, m, c);
+  }
+  if (j == 0) {
+    plan_begin[n] = s_w[32];
+    plan_n[0] = n;
+  }
 }
 
 template <int KIND, int EPI>
@@ -135,47 +198,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ uint64_t full_bar[kStages], empty_bar[kStages], acc_full, acc_empty;
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
-  __shared__ Sched S;
+  __shared__ int s_tlo, s_thi;
   __shared__ float col_scale[kTileN];
   __shared__ int col_row[kTileN];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // ---- schedule: the experts of this launch and their tile ranges
+  // ---- the tiles of this launch
   if (threadIdx.x == 0) {
     abort_flag = 0;
-    int n = 0, acc = 0;
     if (C::kRouted) {
-      const int hits = p.n_act[1];
-      // the prefill path reads every active expert from a cache slot
-      if (p.n_act[0] != hits && blockIdx.x == 0) set_status(p.status, MOE_ERR_DEVICE);
-      const int g1 = min(p.g1, hits);
-      for (int g = p.g0; g < g1 && n < kMaxGroup; ++g) {
-        const int e = p.act_list[g];
-        const int cnt = p.offsets[e + 1] - p.offsets[e];
-        const int slot = p.src_slot[e];
-        if (cnt <= 0) continue;
-        if (slot < 0 || slot >= p.n_slots) {
-          set_status(p.status, MOE_ERR_DEVICE);
-          continue;
-        }
-        S.e[n] = e;
-        S.slot[n] = slot;
-        S.ntiles[n] = (cnt + kTileN - 1) / kTileN;
-        S.tile_begin[n] = acc;
-        acc += S.ntiles[n] * p.mtiles;
-        ++n;
-      }
+      const int n = p.plan_n[0];
+      const int g0 = min(p.g0, n), g1 = min(p.g1, n);
+      s_tlo = p.plan_begin[g0] * p.mtiles;
+      s_thi = p.plan_begin[g1] * p.mtiles;
     } else {
-      S.e[0] = 0;
-      S.slot[0] = 0;
-      S.ntiles[0] = (p.T + kTileN - 1) / kTileN;
-      S.tile_begin[0] = 0;
-      acc = S.ntiles[0] * p.mtiles;
-      n = 1;
+      s_tlo = 0;
+      s_thi = ((p.T + kTileN - 1) / kTileN) * p.mtiles;
     }
-    S.n = n;
-    S.tile_begin[n] = acc;
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(&full_bar[s], 1);
       ptx::mbar_init(&empty_bar[s], 1);
@@ -192,16 +232,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = tmem_base;
-  const int n_tiles = S.tile_begin[S.n];
+  const int tlo = s_tlo, thi = s_thi;
 
   if (warp == 0) {
     // ================= TMA producer =================
     if (lane == 0) {
       uint32_t g = 0;
-      for (int t = blockIdx.x; t < n_tiles && !abort_flag; t += gridDim.x) {
-        int j, mt, nt;
-        tile_coords(S, p.mtiles, t, j, mt, nt);
-        const int e = S.e[j];
+      for (int t = tlo + blockIdx.x; t < thi && !abort_flag; t += gridDim.x) {
+        int mt, nt, e, slot;
+        tile_info<C::kRouted>(p, t, mt, nt, e, slot);
         int brow = nt * kTileN;  // activation row of the tile
         if (C::kRouted) brow += p.pad_offsets[e];
         for (int kb = 0; kb < p.kstages; ++kb, ++g) {
@@ -216,9 +255,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::mbar_arrive_expect_tx(&full_bar[s], C::kStageBytes);
           const int kc = C::kNvf4 ? kb * kStageKB : kb * (kStageKB / 2);  // bytes or bf16s
           if (C::kRouted) {
-            ptx::tma_load_3d(st, &tmA0, kc, mt * kTileM, S.slot[j], &full_bar[s]);
+            ptx::tma_load_3d(st, &tmA0, kc, mt * kTileM, slot, &full_bar[s]);
             if (C::kDual)
-              ptx::tma_load_3d(st + C::kTileBytes, &tmA1, kc, mt * kTileM, S.slot[j],
+              ptx::tma_load_3d(st + C::kTileBytes, &tmA1, kc, mt * kTileM, slot,
                                &full_bar[s]);
           } else {
             ptx::tma_load_2d(st, &tmA0, kc, mt * kTileM, &full_bar[s]);
@@ -229,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (C::kNvf4) {
             // 4 scale atoms (512 B each) per operand: k groups kb*4 .. kb*4+3
             unsigned char* sf = bdst + C::kTileBytes;
-            const uint8_t* rec = p.arena + (uint64_t)S.slot[j] * p.rec_bytes;
+            const uint8_t* rec = p.arena + (uint64_t)slot * p.rec_bytes;
             const uint64_t aoff = ((uint64_t)mt * p.kgroups + (uint64_t)kb * 4) * 512;
             ptx::bulk_load(sf, rec + p.sfa_off0 + aoff, 2048, &full_bar[s]);
             if (C::kDual) ptx::bulk_load(sf + 2048, rec + p.sfa_off1 + aoff, 2048, &full_bar[s]);
@@ -247,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (C::kNvf4) idesc |= (1u << 7) | (1u << 10);               // E2M1 x E2M1, UE4M3 scales
       else idesc |= (1u << 4) | (1u << 7) | (1u << 10);            // fp32 D, bf16 A and B
       uint32_t g = 0, it = 0;
-      for (int t = blockIdx.x; t < n_tiles && !abort_flag; t += gridDim.x, ++it) {
+      for (int t = tlo + blockIdx.x; t < thi && !abort_flag; t += gridDim.x, ++it) {
         if (!ptx::mbar_wait(&acc_empty, (it & 1) ^ 1, kWaitNs)) {
           set_status(p.status, MOE_ERR_TIMEOUT);
           abort_flag = 1;
@@ -313,10 +352,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int et = threadIdx.x - 64;    // 0..127
     float* stage_out = reinterpret_cast<float*>(smem + (size_t)kStages * C::kStageBytes);
     uint32_t it = 0;
-    for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++it) {
-      int j, mt, nt;
-      tile_coords(S, p.mtiles, t, j, mt, nt);
-      const int e = S.e[j];
+    for (int t = tlo + blockIdx.x; t < thi; t += gridDim.x, ++it) {
+      int mt, nt, e, slot;
+      tile_info<C::kRouted>(p, t, mt, nt, e, slot);
       int n_valid, col0;
       if (C::kRouted) {
         const int cnt = p.offsets[e + 1] - p.offsets[e];
@@ -439,123 +477,92 @@ __device__ __forceinline__ float e4m3_value(uint32_t b) {
   return f16_lo(e4m3x2_to_f16x2(b & 0xFFu));
 }
 
-struct QuantParams {
-  int K;                    // values per row
-  int g0, g1;               // act_list range (routed)
-  const int32_t* act_list;
-  const int32_t* n_act;
-  const int32_t* offsets;
-  const int32_t* pad_offsets;
-  const int32_t* perm;
-  int k;
-  const uint16_t* x;        // source rows (bf16 tokens) or
-  const float* h32;         // source rows (fp32 h, indexed by padded row)
-  uint8_t* codes;           // [rows][K/2]
-  uint8_t* scales;          // atoms [rows/128][K/64][512]
-  float* G;                 // [rows]
-};
-
-// one warp per padded row of the experts in act_list[g0, g1) (hits only)
-template <bool FROM_H>
-__global__ void __launch_bounds__(256) k_quant_rows(QuantParams p) {
-  __shared__ int s_n, s_pad[kMaxGroup + 1], s_e[kMaxGroup];
-  if (threadIdx.x == 0) {
-    const int g1 = min(p.g1, p.n_act[1]);
-    int n = 0;
-    for (int g = p.g0; g < g1 && n < kMaxGroup; ++g) s_e[n++] = p.act_list[g];
-    s_n = n;
-  }
-  __syncthreads();
-  for (int j = threadIdx.x; j < s_n; j += blockDim.x) s_pad[j] = p.pad_offsets[s_e[j]];
-  __syncthreads();
-  const int n_exp = s_n;
+// NVFP4 quantisation of one fp32 row of K values (the prefill reading: G =
+// amax/2688, block scale e4m3_rne(amax_b/(6G)), codes e2m1_rne_sat(v/(s G)),
+// all fp32 with IEEE division) by one warp, into padded row `row` of the
+// tcgen05 layout (codes row-major, scales in 512-byte atoms).
+__device__ __forceinline__ void quant_row_f32(const float* __restrict__ hr, int K, int row,
+                                              uint8_t* __restrict__ codes,
+                                              uint8_t* __restrict__ scales,
+                                              float* __restrict__ Gr) {
   const int lane = threadIdx.x & 31;
-  const int warps = (gridDim.x * blockDim.x) >> 5;
-  const int KB = p.K / 16, KG = p.K / 64;
-  // rows of every expert of the launch, expert by expert
-  int total = 0;
-  for (int j = 0; j < n_exp; ++j)
-    total += p.pad_offsets[s_e[j] + 1] - s_pad[j];
-  for (int wr = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; wr < total; wr += warps) {
-    int j = 0, base = 0;
-    while (true) {
-      const int len = p.pad_offsets[s_e[j] + 1] - s_pad[j];
-      if (wr < base + len) break;
-      base += len;
-      ++j;
+  const int KB = K / 16, KG = K / 64;
+  const int rt = row >> 7, m0 = row & 31, m1 = (row & 127) >> 5;
+  float amax = 0.f;
+  for (int i = lane; i < K / 4; i += 32) {
+    const float4 v = __ldcg(reinterpret_cast<const float4*>(hr) + i);
+    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+  const float G = amax > 0.f ? __fdiv_rn(amax, 2688.0f) : 1.0f;
+  const float sixG = __fmul_rn(6.0f, G);
+  for (int b = lane; b < KB; b += 32) {
+    float v[16];
+#pragma unroll
+    for (int i = 0; i < 16; i += 4) {
+      const float4 t = __ldcg(reinterpret_cast<const float4*>(hr + b * 16 + i));
+      v[i] = t.x; v[i + 1] = t.y; v[i + 2] = t.z; v[i + 3] = t.w;
     }
-    const int e = s_e[j];
-    const int local = wr - base;
-    const int row = s_pad[j] + local;
-    const int cnt = p.offsets[e + 1] - p.offsets[e];
-    const bool valid = local < cnt;
-    const int rt = row >> 7, m0 = row & 31, m1 = (row & 127) >> 5;
-    if (!valid) {
-      for (int b = lane; b < KB; b += 32) {
-        *reinterpret_cast<uint2*>(p.codes + (size_t)row * (p.K / 2) + (size_t)b * 8) =
+    float ab = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) ab = fmaxf(ab, fabsf(v[i]));
+    const uint32_t sc = e4m3_rne(__fdiv_rn(ab, sixG));
+    const float sdq = __fmul_rn(e4m3_value(sc), G);
+    uint32_t lo = 0, hi = 0;
+    if (sc != 0) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t c0 = e2m1_rne_sat(__fdiv_rn(v[2 * i], sdq));
+        const uint32_t c1 = e2m1_rne_sat(__fdiv_rn(v[2 * i + 1], sdq));
+        const uint32_t byte = c0 | (c1 << 4);
+        if (i < 4) lo |= byte << (8 * i);
+        else hi |= byte << (8 * (i - 4));
+      }
+    }
+    *reinterpret_cast<uint2*>(codes + (size_t)row * (K / 2) + (size_t)b * 8) = make_uint2(lo, hi);
+    scales[((size_t)rt * KG + (b >> 2)) * 512 + m0 * 16 + m1 * 4 + (b & 3)] = (uint8_t)sc;
+  }
+  if (lane == 0) Gr[row] = G;
+}
+
+// K-hq: h -> NVFP4 for the padded rows of planned experts [g0, g1): CTA
+// (jx, part) takes expert g0 + jx, part `part` of its rows (4 parts); a row
+// past the expert's route count is zeroed.
+__global__ void __launch_bounds__(256) k_quant_h(
+    const float* __restrict__ h32, int K, int g0, int g1, const int32_t* __restrict__ plan_e,
+    const int32_t* __restrict__ plan_n, const int32_t* __restrict__ offsets,
+    const int32_t* __restrict__ pad_offsets, uint8_t* __restrict__ codes,
+    uint8_t* __restrict__ scales, float* __restrict__ G) {
+  const int n = plan_n[0];
+  const int j = g0 + blockIdx.x;
+  if (j >= g1 || j >= n) return;
+  const int e = plan_e[j];
+  const int cnt = offsets[e + 1] - offsets[e];
+  const int r0 = pad_offsets[e], nrow = pad_offsets[e + 1] - r0;
+  const int per = (nrow + gridDim.y - 1) / gridDim.y;
+  const int lo = blockIdx.y * per, hi = min(nrow, lo + per);
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int KB = K / 16, KG = K / 64;
+  for (int i = lo + wid; i < hi; i += nw) {
+    const int row = r0 + i;
+    if (i < cnt) {
+      quant_row_f32(h32 + (size_t)row * K, K, row, codes, scales, G);
+    } else {
+      const int rt = row >> 7, m0 = row & 31, m1 = (row & 127) >> 5;
+      for (int b = lane; b < KB; b += 32)
+        *reinterpret_cast<uint2*>(codes + (size_t)row * (K / 2) + (size_t)b * 8) =
             make_uint2(0u, 0u);
-        p.scales[((size_t)rt * KG + (b >> 2)) * 512 + m0 * 16 + m1 * 4 + (b & 3)] = 0;
-      }
-      if (lane == 0) p.G[row] = 0.f;
-      continue;
+      for (int g = lane; g < KG; g += 32)
+        *reinterpret_cast<uint32_t*>(scales + ((size_t)rt * KG + g) * 512 + m0 * 16 + m1 * 4) =
+            0u;
+      if (lane == 0) G[row] = 0.f;
     }
-    // source row
-    const uint16_t* xr = nullptr;
-    const float* hr = nullptr;
-    if (FROM_H) hr = p.h32 + (size_t)row * p.K;
-    else xr = p.x + (size_t)(p.perm[p.offsets[e] + local] / p.k) * p.K;
-    // row amax
-    float amax = 0.f;
-    for (int i = lane; i < p.K; i += 32) {
-      const float v = FROM_H ? hr[i] : __uint_as_float((uint32_t)xr[i] << 16);
-      amax = fmaxf(amax, fabsf(v));
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
-    const float G = amax > 0.f ? __fdiv_rn(amax, 2688.0f) : 1.0f;
-    const float sixG = __fmul_rn(6.0f, G);
-    for (int b = lane; b < KB; b += 32) {
-      float v[16];
-      if (FROM_H) {
-#pragma unroll
-        for (int i = 0; i < 16; i += 4) {
-          const float4 t = *reinterpret_cast<const float4*>(hr + b * 16 + i);
-          v[i] = t.x; v[i + 1] = t.y; v[i + 2] = t.z; v[i + 3] = t.w;
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 16; i += 2) {
-          const uint32_t t = *reinterpret_cast<const uint32_t*>(xr + b * 16 + i);
-          v[i] = bf16_lo(t);
-          v[i + 1] = bf16_hi(t);
-        }
-      }
-      float ab = 0.f;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) ab = fmaxf(ab, fabsf(v[i]));
-      const uint32_t s = e4m3_rne(__fdiv_rn(ab, sixG));
-      const float sdq = __fmul_rn(e4m3_value(s), G);
-      uint32_t lo = 0, hi = 0;
-      if (s != 0) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint32_t c0 = e2m1_rne_sat(__fdiv_rn(v[2 * i], sdq));
-          const uint32_t c1 = e2m1_rne_sat(__fdiv_rn(v[2 * i + 1], sdq));
-          const uint32_t byte = c0 | (c1 << 4);
-          if (i < 4) lo |= byte << (8 * i);
-          else hi |= byte << (8 * (i - 4));
-        }
-      }
-      *reinterpret_cast<uint2*>(p.codes + (size_t)row * (p.K / 2) + (size_t)b * 8) =
-          make_uint2(lo, hi);
-      p.scales[((size_t)rt * KG + (b >> 2)) * 512 + m0 * 16 + m1 * 4 + (b & 3)] = (uint8_t)s;
-    }
-    if (lane == 0) p.G[row] = G;
   }
 }
 
 // ---- activation quantisation, once per token ---------------------------------------
-// K-actq: one warp per token, the same arithmetic as k_quant_rows (G =
+// K-actq: one warp per token, the same arithmetic as quant_row_f32 (G =
 // amax/2688, block scale e4m3_rne(amax_b/(6G)), codes e2m1_rne_sat(v/(s G)),
 // all fp32 with IEEE division), into a token-major buffer: codes [T][K/2],
 // scales [T][K/16] (block b at byte b), G [T].
@@ -685,7 +692,8 @@ static moe_status make_map(CUtensorMap* m, const void* base, bool bf16, uint64_t
 struct PrefillWs {
   size_t rows;  // padded rows
   size_t xq_codes, xq_scales, xq_G, h32, hq_codes, hq_scales, hq_G, hs, tq_codes, tq_scales,
-      tq_G, total;
+      tq_G, tiles_gu, tiles_dn, plan, total;
+  size_t max_ntiles;  // 128-route column tiles of all experts, at most
   PrefillWs(int T, int H, int I, int E, int k, int Is) {
     rows = (((size_t)T * k + (size_t)E * (kTileN - 1)) + kTileN - 1) / kTileN * kTileN;
     size_t o = 0;
@@ -701,6 +709,10 @@ struct PrefillWs {
     tq_codes = take((size_t)T * H / 2);  // token-major quantised activations
     tq_scales = take((size_t)T * H / 16);
     tq_G = take((size_t)T * 4);
+    max_ntiles = ((size_t)T * k + kTileN - 1) / kTileN + (size_t)E;
+    tiles_gu = take(max_ntiles * (I / kTileM) * 4);
+    tiles_dn = take(max_ntiles * (H / kTileM) * 4);
+    plan = take(((size_t)3 * (E + 1) + 1) * 4);  // plan_e | plan_slot | plan_begin | plan_n
     total = o + 1024;
   }
 };
@@ -760,12 +772,16 @@ moe_status prefill_ffn(const moe_ffn_args* a, cudaStream_t s) {
       return st;
   }
 
-  // routed experts, walked in groups of `grp` through the staging layout
-  const int grp = a->prefill_group > 0 ? (a->prefill_group < kMaxGroup ? a->prefill_group
-                                                                        : kMaxGroup)
-                                       : kMaxGroup;
+  // routed experts, walked in groups of `grp` (act_list order); 0 = all at once
+  const int grp = a->prefill_group > 0 ? a->prefill_group : a->E;
   const int max_act = a->T * a->k < a->E ? a->T * a->k : a->E;
-  // the tokens, quantised once each, then copied to their routes' padded rows
+  int32_t* plan = (int32_t*)(ws + W.plan);
+  int32_t *plan_e = plan, *plan_slot = plan + (a->E + 1), *plan_begin = plan + 2 * (a->E + 1),
+          *plan_n = plan + 3 * (a->E + 1);
+  uint32_t* tiles_gu = (uint32_t*)(ws + W.tiles_gu);
+  uint32_t* tiles_dn = (uint32_t*)(ws + W.tiles_dn);
+  // the tokens, quantised once each, then copied to their routes' padded rows;
+  // the tile tables of both GEMMs
   {
     const int grid = (a->T + 7) / 8 < kSMs * 8 ? (a->T + 7) / 8 : kSMs * 8;
     k_quant_tokens<<<grid, 256, 0, s>>>((const uint16_t*)a->x, a->T, H, ws + W.tq_codes,
@@ -776,21 +792,22 @@ moe_status prefill_ffn(const moe_ffn_args* a, cudaStream_t s) {
                                          a->pad_offsets, a->perm, ws + W.xq_codes,
                                          ws + W.xq_scales, (float*)(ws + W.xq_G));
     MOE_CHECK_LAUNCH();
+    k_tile_plan<<<1, 1024, 0, s>>>(a->act_list, a->n_act, a->offsets, a->src_slot, n_slots, a->E,
+                                  I / kTileM, H / kTileM, tiles_gu, tiles_dn, plan_e, plan_slot,
+                                  plan_begin, plan_n, a->status);
+    MOE_CHECK_LAUNCH();
   }
   for (int g0 = 0; g0 < max_act; g0 += grp) {
-    QuantParams q;
-    memset(&q, 0, sizeof(q));
-    q.g0 = g0; q.g1 = g0 + grp;
-    q.act_list = a->act_list; q.n_act = a->n_act; q.offsets = a->offsets;
-    q.pad_offsets = a->pad_offsets; q.perm = a->perm; q.k = a->k;
-
+    const int g1 = g0 + grp;
     GemmParams gp;
     memset(&gp, 0, sizeof(gp));
-    gp.act_list = a->act_list; gp.n_act = a->n_act; gp.g0 = g0; gp.g1 = g0 + grp;
-    gp.src_slot = a->src_slot; gp.offsets = a->offsets; gp.pad_offsets = a->pad_offsets;
+    gp.plan_e = plan_e; gp.plan_slot = plan_slot; gp.plan_begin = plan_begin;
+    gp.plan_n = plan_n; gp.g0 = g0; gp.g1 = g1;
+    gp.offsets = a->offsets; gp.pad_offsets = a->pad_offsets;
     gp.perm = a->perm; gp.gscale = a->gscale; gp.w = a->w; gp.k = a->k; gp.n_slots = n_slots;
     gp.arena = arena; gp.rec_bytes = rb; gp.H = H; gp.status = a->status;
     // gate/up
+    gp.tiles = tiles_gu;
     gp.mtiles = I / kTileM;
     gp.kstages = (H / 2) / kStageKB;
     gp.kgroups = H / 64;
@@ -799,12 +816,13 @@ moe_status prefill_ffn(const moe_ffn_args* a, cudaStream_t s) {
     gp.h32 = (float*)(ws + W.h32); gp.h_ld = I;
     if ((st = launch_gemm<0, EPI_GU_ROUTED>(mg, mu, mxq, gp, s)) != MOE_OK) return st;
     // h -> NVFP4
-    q.K = I;
-    q.h32 = (const float*)(ws + W.h32);
-    q.codes = ws + W.hq_codes; q.scales = ws + W.hq_scales; q.G = (float*)(ws + W.hq_G);
-    k_quant_rows<true><<<kSMs * 8, 256, 0, s>>>(q);
+    const int ng = (g1 < max_act ? g1 : max_act) - g0;
+    k_quant_h<<<dim3(ng, 4), 256, 0, s>>>((const float*)(ws + W.h32), I, g0, g1, plan_e, plan_n,
+                                         a->offsets, a->pad_offsets, ws + W.hq_codes,
+                                         ws + W.hq_scales, (float*)(ws + W.hq_G));
     MOE_CHECK_LAUNCH();
     // down, weighted, added into y_acc
+    gp.tiles = tiles_dn;
     gp.mtiles = H / kTileM;
     gp.kstages = (I / 2) / kStageKB;
     gp.kgroups = I / 64;
