@@ -42,7 +42,8 @@ namespace pf {
 
 constexpr int kTileM = 128, kTileN = 128, kStageKB = 128;  // K bytes per stage and operand row
 constexpr int kStages = 4;
-constexpr int kThreads = 192;  // warp 0: TMA, warp 1: MMA, warps 2..5: epilogue
+constexpr int kThreads = 320;  // warp 0: TMA, warp 1: MMA, warps 2..9: epilogue
+constexpr int kEpiWarps = 8;   // two per tensor-memory lane quarter, each half of the columns
 constexpr uint64_t kWaitNs = 2000000000ull;  // no wait lasts longer than 2 s
 constexpr uint32_t kTmemCols = 512;
 
@@ -185,7 +186,9 @@ struct Cfg {
   static constexpr uint32_t kSfColsPerStage = kNvf4 ? (kDual ? 48 : 32) : 0;
 };
 
-__device__ __forceinline__ float silu_f(float g) { return g / (1.f + expf(-g)); }
+// SiLU with the fast exponential and division (a few ulp: far below the
+// tolerance and the rounding-boundary slack of the quantised h)
+__device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.f + __expf(-g)); }
 
 template <int KIND, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -221,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(&empty_bar[s], 1);
     }
     ptx::mbar_init(&acc_full, 1);
-    ptx::mbar_init(&acc_empty, 4);
+    ptx::mbar_init(&acc_empty, kEpiWarps);
     ptx::fence_barrier_init();
   }
   if (warp == 1) {
@@ -346,10 +349,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    // ================= epilogue (warps 2..5) =================
+    // ================= epilogue (warps 2..9) =================
+    // A warp reads the tensor-memory lanes of its quarter (warp id mod 4) and
+    // half of the columns; it copies its accumulator columns to registers and
+    // releases the accumulator before any arithmetic or store, so that the
+    // next tile's MMAs run while this tile's outputs are formed and written.
     const int q = warp & 3;             // tensor-memory lane quarter of this warp
+    const int ch = (warp - 2) >> 2;     // column half
     const int row = q * 32 + lane;      // weight row within the tile
-    const int et = threadIdx.x - 64;    // 0..127
+    const int et = threadIdx.x - 64;    // 0..255
+    constexpr int kHalf = kTileN / 2;
     float* stage_out = reinterpret_cast<float*>(smem + (size_t)kStages * C::kStageBytes);
     uint32_t it = 0;
     for (int t = tlo + blockIdx.x; t < thi; t += gridDim.x, ++it) {
@@ -380,49 +389,72 @@ __global__ void __launch_bounds__(kThreads, 1)
         col_scale[et] = sc;
         col_row[et] = rr;
       }
-      asm volatile("bar.sync 1, 128;" ::: "memory");
+      float gg = 1.f, gu = 1.f;
+      if (EPI == EPI_GU_ROUTED) {
+        gg = p.gscale[e * 3 + 0];
+        gu = p.gscale[e * 3 + 1];
+      }
+      asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
       if (!ptx::mbar_wait(&acc_full, it & 1, kWaitNs)) {
         set_status(p.status, MOE_ERR_TIMEOUT);
         abort_flag = 1;
         break;
       }
       ptx::tc_fence_after();
-      const uint32_t lane_addr = tmem + ((uint32_t)(q * 32) << 16);
-      float gg = 1.f, gu = 1.f;
-      if (EPI == EPI_GU_ROUTED) {
-        gg = p.gscale[e * 3 + 0];
-        gu = p.gscale[e * 3 + 1];
-      }
-      for (int c0 = 0; c0 < kTileN; c0 += 32) {
-        uint32_t r0[32], r1[32];
-        ptx::tmem_ld_32x32b_x32(lane_addr + c0, r0);
-        if (C::kDual) ptx::tmem_ld_32x32b_x32(lane_addr + 128 + c0, r1);
-        ptx::tmem_ld_wait();
+      const uint32_t lane_addr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(ch * kHalf);
+      if (C::kDual) {
+        // gate/up: h = silu(g) * u formed chunk by chunk (64 values kept), then
+        // the accumulator is released and h is written
+        float hv[kHalf];
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj) {
-          const int n = c0 + jj;
-          const float a = __uint_as_float(r0[jj]);
-          if (EPI == EPI_GU_ROUTED) {
-            if (n < n_valid) {
-              const float G = col_scale[n];
-              const float gv = a * gg * G, uv = __uint_as_float(r1[jj]) * gu * G;
-              p.h32[(size_t)(col0 + n) * p.h_ld + mt * kTileM + row] = silu_f(gv) * uv;
+        for (int c = 0; c < kHalf; c += 16) {
+          uint32_t ga[16], ua[16];
+          ptx::tmem_ld_32x32b_x16(lane_addr + c, ga);
+          ptx::tmem_ld_32x32b_x16(lane_addr + 128 + c, ua);
+          ptx::tmem_ld_wait();
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) {
+            const float g = __uint_as_float(ga[jj]), u = __uint_as_float(ua[jj]);
+            if (EPI == EPI_GU_ROUTED) {
+              const float G = col_scale[ch * kHalf + c + jj];
+              hv[c + jj] = silu_f(g * gg * G) * (u * gu * G);
+            } else {
+              hv[c + jj] = silu_f(g) * u;
             }
-          } else if (EPI == EPI_GU_SHARED) {
-            if (n < n_valid) {
-              const float hv = silu_f(a) * __uint_as_float(r1[jj]);
-              p.hs[(size_t)(col0 + n) * p.hs_ld + mt * kTileM + row] = f32_to_bf16_rne(hv);
-            }
-          } else {
-            stage_out[n * kTileM + row] = a * col_scale[n];
           }
         }
+        ptx::tc_fence_before();
+        if (lane == 0) ptx::mbar_arrive(&acc_empty);  // the accumulator is free
+#pragma unroll
+        for (int jj = 0; jj < kHalf; ++jj) {
+          const int n = ch * kHalf + jj;
+          if (n < n_valid) {
+            if (EPI == EPI_GU_ROUTED)
+              p.h32[(size_t)(col0 + n) * p.h_ld + mt * kTileM + row] = hv[jj];
+            else
+              p.hs[(size_t)(col0 + n) * p.hs_ld + mt * kTileM + row] = f32_to_bf16_rne(hv[jj]);
+          }
+        }
+      } else {
+        // down: the weighted columns to shared memory, then one bulk
+        // reduce-add per column (route) into y_acc
+        uint32_t ra[32], rb[32];
+        ptx::tmem_ld_32x32b_x32(lane_addr, ra);
+        ptx::tmem_ld_32x32b_x32(lane_addr + 32, rb);
+        ptx::tmem_ld_wait();
+        ptx::tc_fence_before();
+        if (lane == 0) ptx::mbar_arrive(&acc_empty);  // the accumulator is free
+        float* so = stage_out + (size_t)ch * kHalf * kTileM + row;
+        const float* cs = col_scale + ch * kHalf;
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) so[jj * kTileM] = __uint_as_float(ra[jj]) * cs[jj];
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj)
+          so[(32 + jj) * kTileM] = __uint_as_float(rb[jj]) * cs[32 + jj];
       }
-      ptx::tc_fence_before();
-      if (lane == 0) ptx::mbar_arrive(&acc_empty);
       if (EPI == EPI_DOWN_ROUTED || EPI == EPI_DOWN_SHARED) {
         ptx::fence_proxy_async_smem();
-        asm volatile("bar.sync 1, 128;" ::: "memory");
+        asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
         if (et < n_valid) {
           ptx::bulk_reduce_add_f32(p.y_acc + (size_t)col_row[et] * p.H + mt * kTileM,
                                    stage_out + et * kTileM, kTileM * 4);
@@ -430,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::bulk_wait_read0();
         }
       }
-      asm volatile("bar.sync 1, 128;" ::: "memory");
+      asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
     }
     if (EPI == EPI_DOWN_ROUTED || EPI == EPI_DOWN_SHARED) ptx::bulk_wait0();
   }
