@@ -61,16 +61,15 @@ __global__ void __launch_bounds__(256) k_logits_gemv(const uint16_t* __restrict_
 }
 
 // ---- logits for many tokens: SIMT tiled GEMM --------------------------------
-// Tile 64 tokens x 32 experts, 128 threads, 4x4 outputs each, K chunks of 32.
-// Each chunk's partial sum is added to the running total with Kahan
-// compensation, keeping the fp32 error of the 6144-term dot products near
-// that of the chunk sums (the router probabilities are compared at 1e-5).
-// The next chunk's global loads are issued before the current chunk is
-// computed; the x tile is stored transposed (k-major) so that every thread
-// reads its 4 tokens and 4 experts of a k as two 16-byte shared loads.
-// 288 experts = 9 tiles: 576 CTAs of 128 threads for 4096 tokens, about four
-// per SM, all resident at once.
-constexpr int kTM = 64, kTN = 32, kTK = 32, kGemmThreads = 128;
+// Tile 128 tokens x 32 experts, 128 threads, 8 tokens x 4 experts each (32
+// FMAs per three 16-byte shared loads), K chunks of 32.  Each chunk's partial
+// sum is added to the running total with Kahan compensation, keeping the fp32
+// error of the 6144-term dot products near that of the chunk sums (the router
+// probabilities are compared at 1e-5).  The next chunk's global loads are
+// issued before the current chunk is computed; the x tile is stored
+// transposed (k-major).  288 experts = 9 tiles: 288 CTAs for 4096 tokens, two
+// per SM on most SMs, all resident at once.
+constexpr int kTM = 128, kTN = 32, kTK = 32, kGemmThreads = 128;
 
 __global__ void __launch_bounds__(kGemmThreads) k_logits_gemm(const uint16_t* __restrict__ x,
                                                               const float* __restrict__ wr,
@@ -81,22 +80,18 @@ __global__ void __launch_bounds__(kGemmThreads) k_logits_gemm(const uint16_t* __
   __shared__ __align__(16) float ws[kTK][kTN + 4];
   const int t0 = blockIdx.y * kTM, e0 = blockIdx.x * kTN;
   const int tid = threadIdx.x;
-  const int tx = tid & 7, ty = tid >> 3;  // 8 x 16 threads, 4 x 4 outputs each
-  // load roles: x: token lm = tid % 64, k half lkh = tid / 64 (16 values);
-  //             W: expert ln = tid % 32, k quarter lkq = tid / 32 (8 values)
-  const int lm = tid & 63, lkh = tid >> 6, ln = tid & 31, lkq = tid >> 5;
-  const bool xok = t0 + lm < T, wok = e0 + ln < E;
-  const uint4* xsrc = reinterpret_cast<const uint4*>(x + (size_t)(xok ? t0 + lm : 0) * H + lkh * 16);
+  const int tx = tid & 7, ty = tid >> 3;  // 8 x 16 threads; tokens ty*8.., experts tx*4..
+  // load roles: x: token tid, all 32 k of the chunk; W: expert ln = tid % 32,
+  // k quarter lkq = tid / 32 (8 values)
+  const int ln = tid & 31, lkq = tid >> 5;
+  const bool xok = t0 + tid < T, wok = e0 + ln < E;
+  const uint4* xsrc = reinterpret_cast<const uint4*>(x + (size_t)(xok ? t0 + tid : 0) * H);
   const float4* wsrc = reinterpret_cast<const float4*>(wr + (size_t)(wok ? e0 + ln : 0) * H + lkq * 8);
-  uint4 xa, xb;
+  uint4 xv[4];
   float4 wa, wb;
   auto fetch = [&](int k0) {
-    if (xok) {
-      xa = __ldg(xsrc + k0 / 8);
-      xb = __ldg(xsrc + k0 / 8 + 1);
-    } else {
-      xa = xb = make_uint4(0u, 0u, 0u, 0u);
-    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) xv[i] = xok ? __ldg(xsrc + k0 / 8 + i) : make_uint4(0u, 0u, 0u, 0u);
     if (wok) {
       wa = __ldg(wsrc + k0 / 4);
       wb = __ldg(wsrc + k0 / 4 + 1);
@@ -104,44 +99,49 @@ __global__ void __launch_bounds__(kGemmThreads) k_logits_gemm(const uint16_t* __
       wa = wb = make_float4(0.f, 0.f, 0.f, 0.f);
     }
   };
-  float acc[4][4], cmp[4][4];
+  float acc[8][4], cmp[8][4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
+  for (int i = 0; i < 8; ++i)
 #pragma unroll
     for (int j = 0; j < 4; ++j) acc[i][j] = cmp[i][j] = 0.f;
   fetch(0);
   for (int k0 = 0; k0 < H; k0 += kTK) {
     __syncthreads();  // the previous chunk's reads of xs / ws are done
-    {
-      const uint32_t v[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        xs[lkh * 16 + 2 * i][lm] = bf16_lo(v[i]);
-        xs[lkh * 16 + 2 * i + 1][lm] = bf16_hi(v[i]);
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t v[4] = {xv[i].x, xv[i].y, xv[i].z, xv[i].w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        xs[i * 8 + 2 * q][tid] = bf16_lo(v[q]);
+        xs[i * 8 + 2 * q + 1][tid] = bf16_hi(v[q]);
       }
+    }
+    {
       const float w8[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
 #pragma unroll
       for (int i = 0; i < 8; ++i) ws[lkq * 8 + i][ln] = w8[i];
     }
     __syncthreads();
     if (k0 + kTK < H) fetch(k0 + kTK);  // in flight during this chunk's FMAs
-    float part[4][4];
+    float part[8][4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < 8; ++i)
 #pragma unroll
       for (int j = 0; j < 4; ++j) part[i][j] = 0.f;
-#pragma unroll 8
+#pragma unroll 4
     for (int kk = 0; kk < kTK; ++kk) {
-      const float4 a = *reinterpret_cast<const float4*>(&xs[kk][ty * 4]);
+      const float4 a0 = *reinterpret_cast<const float4*>(&xs[kk][ty * 8]);
+      const float4 a1 = *reinterpret_cast<const float4*>(&xs[kk][ty * 8 + 4]);
       const float4 b = *reinterpret_cast<const float4*>(&ws[kk][tx * 4]);
-      const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+      const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+      const float bv[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
+      for (int i = 0; i < 8; ++i)
 #pragma unroll
         for (int j = 0; j < 4; ++j) part[i][j] = fmaf(av[i], bv[j], part[i][j]);
     }
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < 8; ++i)
 #pragma unroll
       for (int j = 0; j < 4; ++j) {  // Kahan: acc += part
         float y = part[i][j] - cmp[i][j];
@@ -151,8 +151,8 @@ __global__ void __launch_bounds__(kGemmThreads) k_logits_gemm(const uint16_t* __
       }
   }
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int t = t0 + ty * 4 + i;
+  for (int i = 0; i < 8; ++i) {
+    const int t = t0 + ty * 8 + i;
     if (t >= T) continue;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
