@@ -123,7 +123,8 @@ moe_status moe_route(const moe_route_args* a, void* stream);
  * unique; inv[r] = p.  pad_offsets (optional) is the exclusive scan of the
  * counts rounded up to multiples of pad_align (the prefill staging layout).
  * Out-of-range ids set MOE_ERR_DEVICE in *status and are dropped.
- * One thread block; T*k <= 1<<20.
+ * One thread block per 1024 routes (each block histograms all routes, so
+ * the blocks never wait on one another); T*k <= 1<<20.
  */
 moe_status moe_permute(const int32_t* ids, int T, int k, int E, int32_t* counts,
                        int32_t* offsets, int32_t* perm, int32_t* inv, int32_t* pad_offsets,
@@ -233,6 +234,7 @@ typedef struct {
   const int32_t* offsets;    /* device [E+1] (moe_permute)                            */
   const int32_t* pad_offsets;/* device [E+1] (moe_permute, pad_align 128; PREFILL)    */
   const int32_t* perm;       /* device [T*k] (moe_permute)                            */
+  const int32_t* inv;        /* device [T*k] (moe_permute; PREFILL)                   */
   const float* w;            /* device [T][k] routing weights (moe_route)            */
   int group, n_stage;        /* expert group walked by this call                     */
   int prefill_group;         /* PREFILL: experts per launch group (0 = all at once)  */
@@ -277,6 +279,28 @@ moe_status moe_expert_ffn(const moe_ffn_args* a, void* stream);
  *     wrong results: order them on one stream or with events. */
 #define MOE_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
 moe_status moe_expert_ffn_noalloc(const moe_ffn_args* a, void* stream);
+
+/* moe_nvfp4_quantize - the prefill path's activation quantiser on its own:
+ * NVFP4 codes of T rows of K values, written in the tensor-core operand
+ * layout that the prefill GEMMs read (dev.to page, "The wall": NVFP4 is E2M1
+ * values with an E4M3 scale per 16 and a global fp32 scale).  Per row t:
+ * G[t] = amax_t / 2688 (1 for a row of zeros); per 16-value block b the scale
+ * byte s = e4m3_rne(amax_b / (6 G)); each value v gets the E2M1 code of
+ * v / (e4m3_value(s) * G), round to nearest even, saturating at 6 (every
+ * step fp32, quotients correctly rounded; a block whose scale byte is 0 gets
+ * codes 0).
+ *   x       device [T][K], bf16 (dtype 0) or fp32 (dtype 1)
+ *   codes   device [T][K/2]: value 2j of a row in the low nibble of byte j
+ *   scales  device, ceil(T/128)*128*K/16 bytes: the scale of block b of row t
+ *           at byte ((t/128)*(K/64) + b/4)*512 + (t%32)*16 + ((t%128)/32)*4
+ *           + b%4 (512-byte atoms of 128 rows x 4 blocks); bytes of rows >= T
+ *           are left as they were
+ *   G       device [T] fp32
+ * K % 256 == 0 and K <= 8192 (bf16) or 4096 (fp32), else
+ * MOE_ERR_UNSUPPORTED; T == 0 is a no-op.  Stream-ordered.
+ */
+moe_status moe_nvfp4_quantize(const void* x, int dtype, int T, int K, uint8_t* codes,
+                              uint8_t* scales, float* G, void* stream);
 
 /* ---------------------------------------------------------------- combine
  * y[t] = bf16_rne( y_acc[t] + sum_{j<k} o_route[inv[t*k+j]] + o_shared[t] ),

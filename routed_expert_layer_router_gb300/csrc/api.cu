@@ -20,6 +20,8 @@ moe_status decode_setup();
 size_t prefill_workspace_bytes(int T, int H, int I, int E, int k, int Is);
 moe_status prefill_ffn(const moe_ffn_args* a, cudaStream_t s);
 moe_status prefill_setup();
+moe_status nvfp4_quantize(const void* x, int dtype, int T, int K, uint8_t* codes,
+                          uint8_t* scales, float* G, cudaStream_t s);
 moe_status permute_setup();
 moe_status launch_permute(const int32_t* ids, int T, int k, int E, int32_t* counts,
                           int32_t* offsets, int32_t* perm, int32_t* inv, int32_t* pad_offsets,
@@ -43,7 +45,7 @@ MOE_API const char* moe_status_string(moe_status s) {
   }
 }
 
-MOE_API int moe_abi_version(void) { return 1; }
+MOE_API int moe_abi_version(void) { return 2; }
 
 static moe_status ensure_setup() {
   static int done = 0;
@@ -241,7 +243,8 @@ MOE_API moe_status moe_layer_forward(moe_layer* l, const void* x, int T, void* y
   fa.T = T; fa.H = d.H; fa.I = d.I; fa.E = d.E; fa.k = d.k;
   fa.x = x; fa.cache = d.cache; fa.gscale = d.gscale;
   fa.src_slot = l->src_slot; fa.act_list = l->act_list; fa.n_act = l->n_act;
-  fa.offsets = l->offsets; fa.pad_offsets = l->pad_offsets; fa.perm = l->perm; fa.w = l->w;
+  fa.offsets = l->offsets; fa.pad_offsets = l->pad_offsets; fa.perm = l->perm; fa.inv = l->inv;
+  fa.w = l->w;
   fa.n_stage = n_stage;
   fa.prefill_group = d.prefill_group;
   fa.Is = d.Is; fa.s_gate = d.s_gate; fa.s_up = d.s_up; fa.s_down = d.s_down;
@@ -298,4 +301,9 @@ MOE_API moe_status moe_read_device_status(moe_layer* l, void* stream, int32_t* s
   *status_out = v;
   if (cudaMemsetAsync(l->status, 0, 4, (cudaStream_t)stream) != cudaSuccess) return MOE_ERR_CUDA;
   return MOE_OK;
+}
+
+MOE_API moe_status moe_nvfp4_quantize(const void* x, int dtype, int T, int K, uint8_t* codes,
+                                      uint8_t* scales, float* G, void* stream) {
+  return nvfp4_quantize(x, dtype, T, K, codes, scales, G, (cudaStream_t)stream);
 }

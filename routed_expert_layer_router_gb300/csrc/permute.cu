@@ -1,9 +1,9 @@
 // permute.cu - K-perm: histogram, exclusive scan and stable permutation of the
 // routes by expert (the grouping behind the Strata-GLM blog's "one batched
 // matrix multiply per expert" and the dev.to page's grouped prefill).
-// One CTA of 1024 threads; ranks are computed from warp match masks and
-// per-warp counts, so the permutation is deterministic without atomics on
-// positions.
+// One CTA of 1024 threads per 1024 routes; ranks are computed from warp match
+// masks and per-warp counts, so the permutation is deterministic without
+// atomics on positions.
 #include "common.cuh"
 
 namespace moe {
@@ -74,7 +74,11 @@ __device__ void lookup_body(const LookupArgs& a, int E, int c, int* s_scan, int3
   }
 }
 
-// smem: counts[E] | base[E] | wcnt[32][E] | scan scratch[33]
+// One CTA per 1024-route chunk.  Every CTA histograms all n routes (split into
+// those before its chunk and the rest), so each knows both the global offsets
+// and its chunk's starting rank per expert without any exchange between CTAs;
+// CTA 0 alone writes counts/offsets/pad_offsets and runs the lookup.
+// smem: counts[E] | before[E] | base[E] | wcnt[32][E] | scan scratch[33]
 __global__ void __launch_bounds__(kPermThreads) k_permute(const int32_t* __restrict__ ids, int n,
                                                           int E, int32_t* __restrict__ counts,
                                                           int32_t* __restrict__ offsets,
@@ -85,69 +89,76 @@ __global__ void __launch_bounds__(kPermThreads) k_permute(const int32_t* __restr
                                                           LookupArgs lk) {
   extern __shared__ int sm[];
   int* s_cnt = sm;
-  int* s_base = s_cnt + E;
+  int* s_pre = s_cnt + E;
+  int* s_base = s_pre + E;
   int* s_w = s_base + E;  // [32][E]
   int* s_scan = s_w + kPermWarps * E;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const bool lead = blockIdx.x == 0;
+  const int r0 = blockIdx.x * kPermThreads;
 
-  for (int e = tid; e < E; e += kPermThreads) s_cnt[e] = 0;
+  for (int e = tid; e < E; e += kPermThreads) {
+    s_cnt[e] = 0;
+    s_pre[e] = 0;
+  }
   __syncthreads();
+  // routes before this chunk count into s_pre, the rest into s_cnt
+#pragma unroll 4
   for (int r = tid; r < n; r += kPermThreads) {
-    int e = ids[r];
-    if (e >= 0 && e < E) atomicAdd(&s_cnt[e], 1);
-    else set_status(status, MOE_ERR_DEVICE);
+    const int e = __ldg(ids + r);
+    if (e >= 0 && e < E) atomicAdd(r < r0 ? &s_pre[e] : &s_cnt[e], 1);
+    else if (lead) set_status(status, MOE_ERR_DEVICE);
   }
   __syncthreads();
   // exclusive scans of counts (and of padded counts); E <= 1024 = one per thread
-  int c = (tid < E) ? s_cnt[tid] : 0;
+  const int pre = (tid < E) ? s_pre[tid] : 0;
+  const int c = (tid < E) ? s_cnt[tid] + pre : 0;
   int tot;
-  int off = block_exclusive_scan(c, s_scan, tot);
-  if (tid < E) {
-    counts[tid] = c;
-    offsets[tid] = off;
-    s_base[tid] = off;
+  const int off = block_exclusive_scan(c, s_scan, tot);
+  if (tid < E) s_base[tid] = off + pre;
+  if (lead) {
+    if (tid < E) {
+      counts[tid] = c;
+      offsets[tid] = off;
+    }
+    if (tid == 0) offsets[E] = tot;
+    if (pad_offsets) {
+      int cp = (tid < E) ? ((c + pad_align - 1) / pad_align) * pad_align : 0;
+      int ptot;
+      int poff = block_exclusive_scan(cp, s_scan, ptot);
+      if (tid < E) pad_offsets[tid] = poff;
+      if (tid == 0) pad_offsets[E] = ptot;
+    }
+    if (lk.table) lookup_body(lk, E, c, s_scan, status);
   }
-  if (tid == 0) offsets[E] = tot;
-  if (pad_offsets) {
-    int cp = (tid < E) ? ((c + pad_align - 1) / pad_align) * pad_align : 0;
-    int ptot;
-    int poff = block_exclusive_scan(cp, s_scan, ptot);
-    if (tid < E) pad_offsets[tid] = poff;
-    if (tid == 0) pad_offsets[E] = ptot;
-  }
-  if (lk.table) lookup_body(lk, E, c, s_scan, status);
+  for (int i = tid; i < kPermWarps * E; i += kPermThreads) s_w[i] = 0;
   __syncthreads();
 
-  // stable positions, 1024 routes per chunk
-  for (int r0 = 0; r0 < n; r0 += kPermThreads) {
-    for (int i = tid; i < kPermWarps * E; i += kPermThreads) s_w[i] = 0;
-    __syncthreads();
-    const int r = r0 + tid;
-    int e = (r < n) ? ids[r] : -1;
-    bool ok = (e >= 0 && e < E);
-    unsigned peers = __match_any_sync(0xFFFFFFFFu, ok ? e : -1);
-    int rank = __popc(peers & ((1u << lane) - 1u));
-    if (ok && rank == 0) s_w[wid * E + e] = __popc(peers);
-    __syncthreads();
-    // per expert: exclusive prefix over warps, then advance the base
-    for (int x = tid; x < E; x += kPermThreads) {
-      int run = s_base[x];
-      for (int w = 0; w < kPermWarps; ++w) {
-        int cw = s_w[w * E + x];
-        s_w[w * E + x] = run;
-        run += cw;
-      }
-      s_base[x] = run;
+  // stable positions of this chunk's routes: rank within the warp from the
+  // match mask, then the per-expert prefix over the warps
+  const int r = r0 + tid;
+  const int e = (r < n) ? __ldg(ids + r) : -1;
+  const bool ok = (e >= 0 && e < E);
+  const unsigned peers = __match_any_sync(0xFFFFFFFFu, ok ? e : -1);
+  const int rank = __popc(peers & ((1u << lane) - 1u));
+  if (ok && rank == 0) s_w[wid * E + e] = __popc(peers);
+  __syncthreads();
+  for (int x = tid; x < E; x += kPermThreads) {
+    int run = s_base[x];
+#pragma unroll 8
+    for (int w = 0; w < kPermWarps; ++w) {
+      const int cw = s_w[w * E + x];
+      s_w[w * E + x] = run;
+      run += cw;
     }
-    __syncthreads();
-    if (ok) {
-      int p = s_w[wid * E + e] + rank;
-      perm[p] = r;
-      inv[r] = p;
-    } else if (r < n) {
-      inv[r] = -1;
-    }
-    __syncthreads();
+  }
+  __syncthreads();
+  if (ok) {
+    const int p = s_w[wid * E + e] + rank;
+    perm[p] = r;
+    inv[r] = p;
+  } else if (r < n) {
+    inv[r] = -1;
   }
 }
 
@@ -187,9 +198,11 @@ moe_status launch_permute(const int32_t* ids, int T, int k, int E, int32_t* coun
   if (T > 0 && (!ids || !perm || !inv)) return MOE_ERR_INVALID_ARG;
   if (pad_offsets && pad_align <= 0) return MOE_ERR_INVALID_ARG;
   if (E > 1024 || (long long)T * k > (1 << 20)) return MOE_ERR_UNSUPPORTED;
-  size_t smem = sizeof(int) * ((size_t)E * (2 + kPermWarps) + 33);
+  size_t smem = sizeof(int) * ((size_t)E * (3 + kPermWarps) + 33);
   if (smem > 48 * 1024 && permute_setup() != MOE_OK) return MOE_ERR_CUDA;
-  k_permute<<<1, kPermThreads, smem, s>>>(ids, T * k, E, counts, offsets, perm, inv, pad_offsets,
+  const int n = T * k;
+  const int grid = n > 0 ? (n + kPermThreads - 1) / kPermThreads : 1;
+  k_permute<<<grid, kPermThreads, smem, s>>>(ids, T * k, E, counts, offsets, perm, inv, pad_offsets,
                                           pad_align, status, lk);
   MOE_CHECK_LAUNCH();
   return MOE_OK;

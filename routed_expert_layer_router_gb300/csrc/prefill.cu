@@ -476,27 +476,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---- NVFP4 activation quantisation -------------------------------------------------
-// nearest E2M1 magnitude of |q| (ties to the even code), saturating at 6; the
-// sign bit is the sign bit of q
-__device__ __forceinline__ uint32_t e2m1_rne_sat(float q) {
-  const float a = fabsf(q);
-  uint32_t c;
-  if (a < 0.25f) c = 0;
-  else if (a == 0.25f) c = 0;
-  else if (a < 0.75f) c = 1;
-  else if (a == 0.75f) c = 2;
-  else if (a < 1.25f) c = 2;
-  else if (a == 1.25f) c = 2;
-  else if (a < 1.75f) c = 3;
-  else if (a == 1.75f) c = 4;
-  else if (a < 2.5f) c = 4;
-  else if (a == 2.5f) c = 4;
-  else if (a < 3.5f) c = 5;
-  else if (a == 3.5f) c = 6;
-  else if (a < 5.f) c = 6;
-  else if (a == 5.f) c = 6;
-  else c = 7;
-  return (__float_as_uint(q) >> 31) ? (c | 8u) : c;
+// The prefill reading of the activation quantiser, for a row of K values: G =
+// amax/2688 (1 for a zero row), block scale s = e4m3_rne(amax_b / (6 G)),
+// dequantised scale sdq = s * G, codes e2m1_rne_sat(v / sdq); every step fp32,
+// the quotients correctly rounded.
+
+// two values to E2M1 codes, round to nearest even, saturating at +-6 (lo in
+// bits 0-3, hi in bits 4-7; the sign bit follows the value's sign)
+__device__ __forceinline__ uint32_t e2m1x2_rn(float lo, float hi) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u32.u8 %0, t;\n\t}"
+      : "=r"(r)
+      : "f"(hi), "f"(lo));
+  return r;
 }
 
 // E4M3 (round to nearest even, saturating to 448) of t >= 0, and its value
@@ -509,58 +501,121 @@ __device__ __forceinline__ float e4m3_value(uint32_t b) {
   return f16_lo(e4m3x2_to_f16x2(b & 0xFFu));
 }
 
-// NVFP4 quantisation of one fp32 row of K values (the prefill reading: G =
-// amax/2688, block scale e4m3_rne(amax_b/(6G)), codes e2m1_rne_sat(v/(s G)),
-// all fp32 with IEEE division) by one warp, into padded row `row` of the
-// tcgen05 layout (codes row-major, scales in 512-byte atoms).
+// v / s rounded to nearest even, given y = RN(1/s): the product v*y refined
+// by two residual steps (r = v - s*q is exact under an FMA, then q = RN(q +
+// r*y)).  Markstein's theorem (IBM J. Res. Dev. 34(1), 1990) makes the last
+// step correctly rounded once q is within one ulp of v/s, which the first
+// step ensures.  Valid while s, y and the quotient stay in the normal range:
+// callers keep s in [2^-56, 2^48] (|v/s| < 16 there) and divide otherwise.
+__device__ __forceinline__ float quot_rn(float v, float s, float y) {
+  float q = __fmul_rn(v, y);
+  q = __fmaf_rn(__fmaf_rn(-s, q, v), y, q);
+  return __fmaf_rn(__fmaf_rn(-s, q, v), y, q);
+}
+
+// block scale byte and dequantised scale of a block with max |v| = ab
+__device__ __forceinline__ uint32_t block_scale(float ab, float sixG, float G, float& sdq) {
+  const uint32_t sc = e4m3_rne(__fdiv_rn(ab, sixG));
+  sdq = __fmul_rn(e4m3_value(sc), G);
+  return sc;
+}
+
+// codes of n consecutive values of one block (n even), packed 2 per byte
+template <int N>
+__device__ __forceinline__ uint32_t block_codes(const float* v, uint32_t sc, float sdq) {
+  if (sc == 0) return 0u;  // the whole block quantises to +-0; written as +0
+  float q[N];
+  if (sdq >= 0x1p-56f && sdq <= 0x1p48f) {
+    const float y = __frcp_rn(sdq);
+#pragma unroll
+    for (int i = 0; i < N; ++i) q[i] = quot_rn(v[i], sdq, y);
+  } else {
+#pragma unroll
+    for (int i = 0; i < N; ++i) q[i] = __fdiv_rn(v[i], sdq);
+  }
+  uint32_t c = 0;
+#pragma unroll
+  for (int i = 0; i < N; i += 2) c |= e2m1x2_rn(q[i], q[i + 1]) << (4 * i);
+  return c;
+}
+
+__device__ __forceinline__ float absmax4(float a, float b, float c, float d) {
+  return fmaxf(fmaxf(fabsf(a), fabsf(b)), fmaxf(fabsf(c), fabsf(d)));
+}
+
+// byte offset of the scale word (4 blocks, kg = block / 4) of padded row `row`
+// in the 512-byte scale atoms of a K-wide operand
+__device__ __forceinline__ size_t scale_word(int row, int kg, int KG) {
+  return ((size_t)(row >> 7) * KG + kg) * 512 + (row & 31) * 16 + ((row & 127) >> 5) * 4;
+}
+
+// One fp32 row of K values (K % 256 == 0, K <= KMAX) by one warp into padded
+// row `row` of the tcgen05 layout.  Each load instruction covers 512
+// contiguous bytes (lane l holds float4 j*32 + l), so four lanes share a
+// 16-value block; the row is read once and held in registers.
+template <int KMAX>
 __device__ __forceinline__ void quant_row_f32(const float* __restrict__ hr, int K, int row,
                                               uint8_t* __restrict__ codes,
                                               uint8_t* __restrict__ scales,
                                               float* __restrict__ Gr) {
+  constexpr int kNJ = KMAX / 128;
   const int lane = threadIdx.x & 31;
-  const int KB = K / 16, KG = K / 64;
-  const int rt = row >> 7, m0 = row & 31, m1 = (row & 127) >> 5;
+  const int NJ = K / 128, KG = K / 64;
+  float4 v[kNJ];
   float amax = 0.f;
-  for (int i = lane; i < K / 4; i += 32) {
-    const float4 v = __ldcg(reinterpret_cast<const float4*>(hr) + i);
-    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+#pragma unroll
+  for (int j = 0; j < kNJ; ++j) {
+    v[j] = j < NJ ? __ldcg(reinterpret_cast<const float4*>(hr) + j * 32 + lane)
+                  : make_float4(0.f, 0.f, 0.f, 0.f);
+    amax = fmaxf(amax, absmax4(v[j].x, v[j].y, v[j].z, v[j].w));
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
   const float G = amax > 0.f ? __fdiv_rn(amax, 2688.0f) : 1.0f;
   const float sixG = __fmul_rn(6.0f, G);
-  for (int b = lane; b < KB; b += 32) {
-    float v[16];
+  uint16_t* crow = reinterpret_cast<uint16_t*>(codes + (size_t)row * (K / 2));
 #pragma unroll
-    for (int i = 0; i < 16; i += 4) {
-      const float4 t = __ldcg(reinterpret_cast<const float4*>(hr + b * 16 + i));
-      v[i] = t.x; v[i + 1] = t.y; v[i + 2] = t.z; v[i + 3] = t.w;
-    }
-    float ab = 0.f;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) ab = fmaxf(ab, fabsf(v[i]));
-    const uint32_t sc = e4m3_rne(__fdiv_rn(ab, sixG));
-    const float sdq = __fmul_rn(e4m3_value(sc), G);
-    uint32_t lo = 0, hi = 0;
-    if (sc != 0) {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const uint32_t c0 = e2m1_rne_sat(__fdiv_rn(v[2 * i], sdq));
-        const uint32_t c1 = e2m1_rne_sat(__fdiv_rn(v[2 * i + 1], sdq));
-        const uint32_t byte = c0 | (c1 << 4);
-        if (i < 4) lo |= byte << (8 * i);
-        else hi |= byte << (8 * (i - 4));
-      }
-    }
-    *reinterpret_cast<uint2*>(codes + (size_t)row * (K / 2) + (size_t)b * 8) = make_uint2(lo, hi);
-    scales[((size_t)rt * KG + (b >> 2)) * 512 + m0 * 16 + m1 * 4 + (b & 3)] = (uint8_t)sc;
+  for (int j = 0; j < kNJ; ++j) {
+    if (j >= NJ) break;
+    float ab = absmax4(v[j].x, v[j].y, v[j].z, v[j].w);
+    ab = fmaxf(ab, __shfl_xor_sync(0xFFFFFFFFu, ab, 1));
+    ab = fmaxf(ab, __shfl_xor_sync(0xFFFFFFFFu, ab, 2));
+    float sdq;
+    const uint32_t sc = block_scale(ab, sixG, G, sdq);
+    const float f[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+    crow[j * 32 + lane] = (uint16_t)block_codes<4>(f, sc, sdq);
+    // blocks j*8 + lane/4; lanes 0 and 16 gather the two scale words
+    const uint32_t s1 = __shfl_down_sync(0xFFFFFFFFu, sc, 4);
+    const uint32_t s2 = __shfl_down_sync(0xFFFFFFFFu, sc, 8);
+    const uint32_t s3 = __shfl_down_sync(0xFFFFFFFFu, sc, 12);
+    if ((lane & 15) == 0)
+      *reinterpret_cast<uint32_t*>(scales + scale_word(row, j * 2 + (lane >> 4), KG)) =
+          sc | (s1 << 8) | (s2 << 16) | (s3 << 24);
   }
   if (lane == 0) Gr[row] = G;
 }
 
+// zero padded rows [r0, r1) of a K-wide operand (codes, scale words, G) with
+// the threads of one CTA
+__device__ __forceinline__ void zero_rows(int r0, int r1, int K, uint8_t* __restrict__ codes,
+                                          uint8_t* __restrict__ scales, float* __restrict__ G) {
+  const int n = r1 - r0;
+  if (n <= 0) return;
+  const int n16 = K / 32, KG = K / 64;  // 16-byte chunks of a codes row; scale words
+  uint4* c = reinterpret_cast<uint4*>(codes + (size_t)r0 * (K / 2));
+  for (int i = threadIdx.x; i < n * n16; i += blockDim.x) c[i] = make_uint4(0u, 0u, 0u, 0u);
+  for (int i = threadIdx.x; i < n * KG; i += blockDim.x)
+    *reinterpret_cast<uint32_t*>(scales + scale_word(r0 + i / KG, i % KG, KG)) = 0u;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) G[r0 + i] = 0.f;
+}
+
+constexpr int kQuantHMaxK = 4096;  // I up to 4096 (the prefill path checks)
+constexpr int kQuantXMaxK = 8192;  // H up to 8192
+
 // K-hq: h -> NVFP4 for the padded rows of planned experts [g0, g1): CTA
-// (jx, part) takes expert g0 + jx, part `part` of its rows (4 parts); a row
-// past the expert's route count is zeroed.
+// (j - g0, part) takes a quarter of expert plan_e[j]'s rows, one warp per
+// row; padding rows are zeroed.
+template <int KMAX>
 __global__ void __launch_bounds__(256) k_quant_h(
     const float* __restrict__ h32, int K, int g0, int g1, const int32_t* __restrict__ plan_e,
     const int32_t* __restrict__ plan_n, const int32_t* __restrict__ offsets,
@@ -574,117 +629,125 @@ __global__ void __launch_bounds__(256) k_quant_h(
   const int r0 = pad_offsets[e], nrow = pad_offsets[e + 1] - r0;
   const int per = (nrow + gridDim.y - 1) / gridDim.y;
   const int lo = blockIdx.y * per, hi = min(nrow, lo + per);
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  const int KB = K / 16, KG = K / 64;
-  for (int i = lo + wid; i < hi; i += nw) {
-    const int row = r0 + i;
-    if (i < cnt) {
-      quant_row_f32(h32 + (size_t)row * K, K, row, codes, scales, G);
-    } else {
-      const int rt = row >> 7, m0 = row & 31, m1 = (row & 127) >> 5;
-      for (int b = lane; b < KB; b += 32)
-        *reinterpret_cast<uint2*>(codes + (size_t)row * (K / 2) + (size_t)b * 8) =
-            make_uint2(0u, 0u);
-      for (int g = lane; g < KG; g += 32)
-        *reinterpret_cast<uint32_t*>(scales + ((size_t)rt * KG + g) * 512 + m0 * 16 + m1 * 4) =
-            0u;
-      if (lane == 0) G[row] = 0.f;
-    }
-  }
+  const int wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  for (int i = lo + wid; i < min(hi, cnt); i += nw)
+    quant_row_f32<KMAX>(h32 + (size_t)(r0 + i) * K, K, r0 + i, codes, scales, G);
+  zero_rows(r0 + max(lo, cnt), r0 + hi, K, codes, scales, G);
 }
 
-// ---- activation quantisation, once per token ---------------------------------------
-// K-actq: one warp per token, the same arithmetic as quant_row_f32 (G =
-// amax/2688, block scale e4m3_rne(amax_b/(6G)), codes e2m1_rne_sat(v/(s G)),
-// all fp32 with IEEE division), into a token-major buffer: codes [T][K/2],
-// scales [T][K/16] (block b at byte b), G [T].
-__global__ void __launch_bounds__(256) k_quant_tokens(const uint16_t* __restrict__ x, int T, int K,
-                                                     uint8_t* __restrict__ codes,
-                                                     uint8_t* __restrict__ scales,
-                                                     float* __restrict__ Gt) {
-  const int lane = threadIdx.x & 31;
-  const int warps = (gridDim.x * blockDim.x) >> 5;
-  const int KB = K / 16;
-  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += warps) {
-    const uint16_t* xr = x + (size_t)t * K;
-    float amax = 0.f;
-    for (int i = lane; i < K / 8; i += 32) {  // 8 values per 16-byte load
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(xr) + i);
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int q = 0; q < 4; ++q) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[q])), fabsf(bf16_hi(w[q]))));
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
-    const float G = amax > 0.f ? __fdiv_rn(amax, 2688.0f) : 1.0f;
-    const float sixG = __fmul_rn(6.0f, G);
-    for (int b = lane; b < KB; b += 32) {
-      float v[16];
-      const uint4 a0 = __ldg(reinterpret_cast<const uint4*>(xr + b * 16));
-      const uint4 a1 = __ldg(reinterpret_cast<const uint4*>(xr + b * 16 + 8));
-      const uint32_t w[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        v[2 * i] = bf16_lo(w[i]);
-        v[2 * i + 1] = bf16_hi(w[i]);
-      }
-      float ab = 0.f;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) ab = fmaxf(ab, fabsf(v[i]));
-      const uint32_t sc = e4m3_rne(__fdiv_rn(ab, sixG));
-      const float sdq = __fmul_rn(e4m3_value(sc), G);
-      uint32_t lo = 0, hi = 0;
-      if (sc != 0) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint32_t c0 = e2m1_rne_sat(__fdiv_rn(v[2 * i], sdq));
-          const uint32_t c1 = e2m1_rne_sat(__fdiv_rn(v[2 * i + 1], sdq));
-          const uint32_t byte = c0 | (c1 << 4);
-          if (i < 4) lo |= byte << (8 * i);
-          else hi |= byte << (8 * (i - 4));
-        }
-      }
-      *reinterpret_cast<uint2*>(codes + (size_t)t * (K / 2) + (size_t)b * 8) = make_uint2(lo, hi);
-      scales[(size_t)t * KB + b] = (uint8_t)sc;
-    }
-    if (lane == 0) Gt[t] = G;
-  }
+// K-hq over plain rows: row t of x (fp32, T rows) -> row t, one warp per row
+template <int KMAX>
+__global__ void __launch_bounds__(256) k_quant_rows_f32(const float* __restrict__ x, int T, int K,
+                                                        uint8_t* __restrict__ codes,
+                                                        uint8_t* __restrict__ scales,
+                                                        float* __restrict__ G) {
+  const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (t < T) quant_row_f32<KMAX>(x + (size_t)t * K, K, t, codes, scales, G);
 }
 
-// K-expand: one CTA per expert; route position p of the expert (token
-// perm[p] / k) goes to padded row pad_offsets[e] + (p - offsets[e]): its codes
-// row, its scales into the 512-byte atoms of the tcgen05 scale layout, its G.
-// Padding rows of the segment are zeroed.
-__global__ void __launch_bounds__(256) k_expand_routes(
-    const uint8_t* __restrict__ tcodes, const uint8_t* __restrict__ tscales,
-    const float* __restrict__ tG, int K, int E, int k, const int32_t* __restrict__ offsets,
-    const int32_t* __restrict__ pad_offsets, const int32_t* __restrict__ perm,
+// K-actq: the tokens quantised once each and written straight into the
+// padded rows of their k routes (route t*k + j at position p = inv[t*k + j]
+// of expert e goes to row pad_offsets[e] + p - offsets[e]).  CTA t < T takes
+// token t: 256 threads, thread i holding 16-byte chunks i + 256 m (8 values;
+// two threads per block).  CTA T + e zeroes expert e's padding rows.  With
+// inv == NULL (k = 1) token t goes to row t and no rows are padded.
+template <int KMAX>
+__global__ void __launch_bounds__(256) k_quant_routes(
+    const uint16_t* __restrict__ x, int T, int K, int E, int k, const int32_t* __restrict__ inv,
+    const int32_t* __restrict__ offsets, const int32_t* __restrict__ pad_offsets,
     uint8_t* __restrict__ codes, uint8_t* __restrict__ scales, float* __restrict__ G) {
-  const int e = blockIdx.x;
-  if (e >= E) return;
-  const int p0 = offsets[e], cnt = offsets[e + 1] - p0;
-  const int r0 = pad_offsets[e], nrow = pad_offsets[e + 1] - r0;
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  const int KB = K / 16, KG = K / 64, nc16 = K / 32;  // 16-byte chunks of a codes row
-  for (int i = wid; i < nrow; i += nw) {
-    const int row = r0 + i;
-    const int rt = row >> 7, m0 = row & 31, m1 = (row & 127) >> 5;
-    uint4* dst = reinterpret_cast<uint4*>(codes + (size_t)row * (K / 2));
-    if (i < cnt) {
-      const int t = perm[p0 + i] / k;
-      const uint4* src = reinterpret_cast<const uint4*>(tcodes + (size_t)t * (K / 2));
-      for (int c = lane; c < nc16; c += 32) dst[c] = __ldg(src + c);
-      const uint32_t* ssrc = reinterpret_cast<const uint32_t*>(tscales + (size_t)t * KB);
-      for (int g = lane; g < KG; g += 32)  // 4 blocks = one atom word of this row
-        *reinterpret_cast<uint32_t*>(scales + ((size_t)rt * KG + g) * 512 + m0 * 16 + m1 * 4) =
-            __ldg(ssrc + g);
-      if (lane == 0) G[row] = tG[t];
+  constexpr int kNJ = KMAX / 2048;
+  __shared__ int s_row[32];
+  __shared__ float s_max[8];
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  if ((int)blockIdx.x >= T) {
+    const int e = blockIdx.x - T;
+    if (inv && e < E)
+      zero_rows(pad_offsets[e] + offsets[e + 1] - offsets[e], pad_offsets[e + 1], K, codes,
+                scales, G);
+    return;
+  }
+  const int t = blockIdx.x;
+  const int NC = K / 8, KG = K / 64;
+  const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)t * K);
+  uint4 v[kNJ];
+#pragma unroll
+  for (int m = 0; m < kNJ; ++m) {
+    const int c = tid + 256 * m;
+    v[m] = c < NC ? __ldg(xr + c) : make_uint4(0u, 0u, 0u, 0u);
+  }
+  if (tid < k) {
+    int row = -1;
+    if (!inv) {
+      row = t;
     } else {
-      for (int c = lane; c < nc16; c += 32) dst[c] = make_uint4(0u, 0u, 0u, 0u);
-      for (int g = lane; g < KG; g += 32)
-        *reinterpret_cast<uint32_t*>(scales + ((size_t)rt * KG + g) * 512 + m0 * 16 + m1 * 4) = 0u;
-      if (lane == 0) G[row] = 0.f;
+      const int p = inv[(size_t)t * k + tid];
+      if (p >= 0) {  // expert of position p: the last e with offsets[e] <= p
+        int lo = 0, hi = E;
+        while (hi - lo > 1) {
+          const int mid = (lo + hi) >> 1;
+          if (__ldg(offsets + mid) <= p) lo = mid;
+          else hi = mid;
+        }
+        row = pad_offsets[lo] + p - offsets[lo];
+      }
     }
+    s_row[tid] = row;
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int m = 0; m < kNJ; ++m) {
+    const uint32_t w[4] = {v[m].x, v[m].y, v[m].z, v[m].w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[q])), fabsf(bf16_hi(w[q]))));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+  if (lane == 0) s_max[wid] = amax;
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < 8; ++i) amax = fmaxf(amax, s_max[i]);
+  const float Gt = amax > 0.f ? __fdiv_rn(amax, 2688.0f) : 1.0f;
+  const float sixG = __fmul_rn(6.0f, Gt);
+  uint32_t cw[kNJ], sw[kNJ];
+#pragma unroll
+  for (int m = 0; m < kNJ; ++m) {
+    cw[m] = 0u;
+    sw[m] = 0u;
+    if (tid + 256 * m >= NC) break;  // uniform per warp: NC is a multiple of 32
+    const uint32_t w[4] = {v[m].x, v[m].y, v[m].z, v[m].w};
+    float f[8];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      f[2 * q] = bf16_lo(w[q]);
+      f[2 * q + 1] = bf16_hi(w[q]);
+    }
+    float ab = 0.f;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) ab = fmaxf(ab, fabsf(f[q]));
+    ab = fmaxf(ab, __shfl_xor_sync(0xFFFFFFFFu, ab, 1));  // the other half of the block
+    float sdq;
+    const uint32_t sc = block_scale(ab, sixG, Gt, sdq);
+    cw[m] = block_codes<8>(f, sc, sdq);
+    // block (tid + 256 m) / 2; lanes 8i gather the scale word of blocks 4i..4i+3
+    const uint32_t s1 = __shfl_down_sync(0xFFFFFFFFu, sc, 2);
+    const uint32_t s2 = __shfl_down_sync(0xFFFFFFFFu, sc, 4);
+    const uint32_t s3 = __shfl_down_sync(0xFFFFFFFFu, sc, 6);
+    sw[m] = sc | (s1 << 8) | (s2 << 16) | (s3 << 24);
+  }
+  for (int j = 0; j < k; ++j) {
+    const int row = s_row[j];
+    if (row < 0) continue;
+    uint32_t* crow = reinterpret_cast<uint32_t*>(codes + (size_t)row * (K / 2));
+#pragma unroll
+    for (int m = 0; m < kNJ; ++m) {
+      const int c = tid + 256 * m;
+      if (c >= NC) break;
+      crow[c] = cw[m];
+      if ((lane & 7) == 0)
+        *reinterpret_cast<uint32_t*>(scales + scale_word(row, c >> 3, KG)) = sw[m];
+    }
+    if (tid == 0) G[row] = Gt;
   }
 }
 
@@ -723,8 +786,8 @@ static moe_status make_map(CUtensorMap* m, const void* base, bool bf16, uint64_t
 // workspace layout for a prefill call on T tokens
 struct PrefillWs {
   size_t rows;  // padded rows
-  size_t xq_codes, xq_scales, xq_G, h32, hq_codes, hq_scales, hq_G, hs, tq_codes, tq_scales,
-      tq_G, tiles_gu, tiles_dn, plan, total;
+  size_t xq_codes, xq_scales, xq_G, h32, hq_codes, hq_scales, hq_G, hs, tiles_gu, tiles_dn, plan,
+      total;
   size_t max_ntiles;  // 128-route column tiles of all experts, at most
   PrefillWs(int T, int H, int I, int E, int k, int Is) {
     rows = (((size_t)T * k + (size_t)E * (kTileN - 1)) + kTileN - 1) / kTileN * kTileN;
@@ -738,9 +801,6 @@ struct PrefillWs {
     hq_scales = take(rows * I / 16);
     hq_G = take(rows * 4);
     hs = take((size_t)T * Is * 2);
-    tq_codes = take((size_t)T * H / 2);  // token-major quantised activations
-    tq_scales = take((size_t)T * H / 16);
-    tq_G = take((size_t)T * 4);
     max_ntiles = ((size_t)T * k + kTileN - 1) / kTileN + (size_t)E;
     tiles_gu = take(max_ntiles * (I / kTileM) * 4);
     tiles_dn = take(max_ntiles * (H / kTileM) * 4);
@@ -767,6 +827,25 @@ static moe_status launch_gemm(const CUtensorMap& a0, const CUtensorMap& a1, cons
 
 }  // namespace pf
 
+moe_status nvfp4_quantize(const void* x, int dtype, int T, int K, uint8_t* codes,
+                          uint8_t* scales, float* G, cudaStream_t s) {
+  using namespace pf;
+  if (T < 0 || K <= 0 || (dtype != 0 && dtype != 1)) return MOE_ERR_INVALID_ARG;
+  if (K % 256 || K > (dtype == 0 ? kQuantXMaxK : kQuantHMaxK)) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  if (!x || !codes || !scales || !G) return MOE_ERR_INVALID_ARG;
+  if (dtype == 0) {
+    auto* kx = K <= 4096 ? k_quant_routes<4096> : k_quant_routes<kQuantXMaxK>;
+    kx<<<T, 256, 0, s>>>((const uint16_t*)x, T, K, 1, 1, nullptr, nullptr, nullptr, codes, scales,
+                         G);
+  } else {
+    auto* kq = K <= 2048 ? k_quant_rows_f32<2048> : k_quant_rows_f32<kQuantHMaxK>;
+    kq<<<(T + 7) / 8, 256, 0, s>>>((const float*)x, T, K, codes, scales, G);
+  }
+  MOE_CHECK_LAUNCH();
+  return MOE_OK;
+}
+
 size_t prefill_workspace_bytes(int T, int H, int I, int E, int k, int Is) {
   return pf::PrefillWs(T, H, I, E, k, Is).total;
 }
@@ -775,7 +854,10 @@ moe_status prefill_setup() { return pf::load_encoder(); }
 
 moe_status prefill_ffn(const moe_ffn_args* a, cudaStream_t s) {
   using namespace pf;
-  if (a->H % 256 || a->I % 256 || a->Is % 128 || a->group != 0) return MOE_ERR_UNSUPPORTED;
+  if (!a->inv || !a->pad_offsets) return MOE_ERR_INVALID_ARG;
+  if (a->H % 256 || a->I % 256 || a->Is % 128 || a->group != 0 || a->I > kQuantHMaxK ||
+      a->H > kQuantXMaxK || a->k > 32)
+    return MOE_ERR_UNSUPPORTED;
   moe_status st = load_encoder();
   if (st != MOE_OK) return st;
   const PrefillWs W(a->T, a->H, a->I, a->E, a->k, a->Is);
@@ -812,17 +894,13 @@ moe_status prefill_ffn(const moe_ffn_args* a, cudaStream_t s) {
           *plan_n = plan + 3 * (a->E + 1);
   uint32_t* tiles_gu = (uint32_t*)(ws + W.tiles_gu);
   uint32_t* tiles_dn = (uint32_t*)(ws + W.tiles_dn);
-  // the tokens, quantised once each, then copied to their routes' padded rows;
-  // the tile tables of both GEMMs
+  // the tokens, quantised once each into their routes' padded rows; the tile
+  // tables of both GEMMs
   {
-    const int grid = (a->T + 7) / 8 < kSMs * 8 ? (a->T + 7) / 8 : kSMs * 8;
-    k_quant_tokens<<<grid, 256, 0, s>>>((const uint16_t*)a->x, a->T, H, ws + W.tq_codes,
-                                        ws + W.tq_scales, (float*)(ws + W.tq_G));
-    MOE_CHECK_LAUNCH();
-    k_expand_routes<<<a->E, 256, 0, s>>>(ws + W.tq_codes, ws + W.tq_scales,
-                                         (const float*)(ws + W.tq_G), H, a->E, a->k, a->offsets,
-                                         a->pad_offsets, a->perm, ws + W.xq_codes,
-                                         ws + W.xq_scales, (float*)(ws + W.xq_G));
+    auto* kx = H <= 4096 ? k_quant_routes<4096> : k_quant_routes<kQuantXMaxK>;
+    kx<<<a->T + a->E, 256, 0, s>>>((const uint16_t*)a->x, a->T, H, a->E, a->k, a->inv, a->offsets,
+                                   a->pad_offsets, ws + W.xq_codes, ws + W.xq_scales,
+                                   (float*)(ws + W.xq_G));
     MOE_CHECK_LAUNCH();
     k_tile_plan<<<1, 1024, 0, s>>>(a->act_list, a->n_act, a->offsets, a->src_slot, n_slots, a->E,
                                   I / kTileM, H / kTileM, tiles_gu, tiles_dn, plan_e, plan_slot,
@@ -849,9 +927,10 @@ moe_status prefill_ffn(const moe_ffn_args* a, cudaStream_t s) {
     if ((st = launch_gemm<0, EPI_GU_ROUTED>(mg, mu, mxq, gp, s)) != MOE_OK) return st;
     // h -> NVFP4
     const int ng = (g1 < max_act ? g1 : max_act) - g0;
-    k_quant_h<<<dim3(ng, 4), 256, 0, s>>>((const float*)(ws + W.h32), I, g0, g1, plan_e, plan_n,
-                                         a->offsets, a->pad_offsets, ws + W.hq_codes,
-                                         ws + W.hq_scales, (float*)(ws + W.hq_G));
+    auto* kq = I <= 2048 ? k_quant_h<2048> : k_quant_h<kQuantHMaxK>;
+    kq<<<dim3(ng, 4), 256, 0, s>>>((const float*)(ws + W.h32), I, g0, g1, plan_e, plan_n,
+                                  a->offsets, a->pad_offsets, ws + W.hq_codes, ws + W.hq_scales,
+                                  (float*)(ws + W.hq_G));
     MOE_CHECK_LAUNCH();
     // down, weighted, added into y_acc
     gp.tiles = tiles_dn;

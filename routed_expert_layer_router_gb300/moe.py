@@ -44,7 +44,7 @@ class moe_ffn_args(ctypes.Structure):
     _fields_ = [("mode", i32), ("stages", i32), ("T", i32), ("H", i32), ("I", i32), ("E", i32),
                 ("k", i32), ("x", vp), ("cache", vp), ("gscale", vp), ("src_slot", vp),
                 ("act_list", vp), ("n_act", vp), ("offsets", vp), ("pad_offsets", vp),
-                ("perm", vp), ("w", vp), ("group", i32), ("n_stage", i32),
+                ("perm", vp), ("inv", vp), ("w", vp), ("group", i32), ("n_stage", i32),
                 ("prefill_group", i32), ("Is", i32),
                 ("s_gate", vp), ("s_up", vp), ("s_down", vp), ("o_route", vp), ("y_acc", vp),
                 ("o_shared", vp), ("workspace", vp), ("workspace_bytes", sz), ("status", vp)]
@@ -80,6 +80,7 @@ SIGNATURES = {
     "moe_ffn_workspace_bytes": (sz, [i32, i32, i32, i32, i32, i32, i32]),
     "moe_expert_ffn": (i32, [ctypes.POINTER(moe_ffn_args), vp]),
     "moe_expert_ffn_noalloc": (i32, [ctypes.POINTER(moe_ffn_args), vp]),
+    "moe_nvfp4_quantize": (i32, [vp, i32, i32, i32, vp, vp, vp, vp]),
     "moe_combine": (i32, [ctypes.POINTER(moe_combine_args), vp]),
     "moe_layer_create": (i32, [ctypes.POINTER(moe_layer_desc), ctypes.POINTER(vp)]),
     "moe_layer_destroy": (i32, [vp]),
@@ -191,6 +192,12 @@ def moe_expert_ffn_noalloc(args: moe_ffn_args, stream: int = 0) -> None:
     array of MOE_NOALLOC_SCRATCH_BYTES shared by all calls; calls that overlap
     on the GPU race on it."""
     _ck("moe_expert_ffn_noalloc", lib().moe_expert_ffn_noalloc(ctypes.byref(args), stream))
+
+
+def moe_nvfp4_quantize(x, dtype, T, K, codes, scales, G, stream: int = 0) -> None:
+    """NVFP4 quantisation of T rows of K values (dtype 0 = bf16, 1 = fp32) into
+    codes [T][K/2], scales in 512-byte atoms and G [T] (device pointers)."""
+    _ck("moe_nvfp4_quantize", lib().moe_nvfp4_quantize(x, dtype, T, K, codes, scales, G, stream))
 
 
 def moe_combine(args: moe_combine_args, stream: int = 0) -> None:

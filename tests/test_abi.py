@@ -41,7 +41,7 @@ def test_binding_covers_the_header(libmoe):
     from routed_expert_layer_router_gb300 import moe
     assert sorted(moe.SIGNATURES) == _declared_functions()
     L = moe.lib()
-    assert L.moe_abi_version() == 1
+    assert L.moe_abi_version() == 2
     assert L.moe_record_bytes(6144, 2048) == 21233664
     assert L.moe_status_string(6) == b"MOE_ERR_DEVICE"
 
@@ -56,6 +56,10 @@ def test_argument_errors_return_before_touching_the_device(libmoe):
     assert L.moe_route(ctypes.byref(a), None) == moe.MOE_ERR_INVALID_ARG
     a.k, a.H = 8, 100  # H not a multiple of 256
     assert L.moe_route(ctypes.byref(a), None) == moe.MOE_ERR_UNSUPPORTED
+    assert L.moe_nvfp4_quantize(16, 0, 4, 100, 16, 16, 16, None) == moe.MOE_ERR_UNSUPPORTED
+    assert L.moe_nvfp4_quantize(16, 1, 4, 8192, 16, 16, 16, None) == moe.MOE_ERR_UNSUPPORTED
+    assert L.moe_nvfp4_quantize(16, 2, 4, 256, 16, 16, 16, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_nvfp4_quantize(None, 0, 4, 256, 16, 16, 16, None) == moe.MOE_ERR_INVALID_ARG
     assert L.moe_permute(None, 1, 8, 2000, 16, 16, 16, 16, None, 128, None, None) == \
         moe.MOE_ERR_INVALID_ARG
     assert L.expcache_create(None, None) == moe.MOE_ERR_INVALID_ARG
