@@ -478,6 +478,46 @@ def bench_prefill(args, torch, moe, gen, gd, dev, peaks, group=None):
     return res
 
 
+# ------------------------------------------------------------------- router
+def bench_route(args, torch, moe, gen, dev, T=4096):
+    """The router alone at the prefill shape (T tokens, fp32 weights [E][H]):
+    moe_route per call, CUDA events around each, L2 flushed between calls."""
+    wl = gen.WORKLOADS["prefill"]
+    H, E, k = wl.H, wl.E, wl.k
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+    wr = torch.empty((E, H), dtype=torch.float32, device=dev)
+    gen.dev_router_f32(wl.seed, 0, E, H, wr.data_ptr(), sp)
+    n = args.warmup + args.prefill_steps
+    xs = torch.empty((n, T, H), dtype=torch.bfloat16, device=dev)
+    for i in range(n):
+        gen.dev_x_bf16(wl.seed, 0, 5_000_000 + i * T, T, H, xs[i].data_ptr(), sp)
+    ids = torch.empty((T, k), dtype=torch.int32, device=dev)
+    w = torch.empty((T, k), dtype=torch.float32, device=dev)
+    lg = torch.empty((T, E), dtype=torch.float32, device=dev)
+    a = moe.moe_route_args()
+    a.w_router, a.T, a.H, a.E, a.k = wr.data_ptr(), T, H, E, k
+    a.ids, a.w, a.logits = ids.data_ptr(), w.data_ptr(), lg.data_ptr()
+    flush = L2Flush(torch, args.flush_mb, dev)
+    for i in range(args.warmup):
+        a.x = xs[i].data_ptr()
+        moe.moe_route(a, sp)
+    ev = _events(torch, args.prefill_steps)
+    torch.cuda.synchronize()
+    for j in range(args.prefill_steps):
+        flush()
+        a.x = xs[args.warmup + j].data_ptr()
+        ev[j][0].record(stream)
+        moe.moe_route(a, sp)
+        ev[j][1].record(stream)
+    torch.cuda.synchronize()
+    us = sum(x.elapsed_time(y) for x, y in ev) / args.prefill_steps * 1e3
+    flops = 2.0 * T * E * H
+    return {"workload": f"router: {T} tokens, H={H}, {E} experts top-{k}, fp32 weights and "
+                        "logits (SIMT FMA, Kahan per 32-value chunk), softmax/top-k",
+            "us_per_call": round(us, 2), "fp32_tflops": round(flops / (us * 1e-6) / 1e12, 2)}
+
+
 # --------------------------------------------------------------- stack / flat
 def _saliency_order(torch, moe, gen, wl, layers, dev, n_tokens=512):
     """Per layer, experts by decreasing routing-weight mass over a separate
@@ -645,6 +685,8 @@ def run_ours(args, rank, world, local_rank):
     peaks, peak_kind = _peaks()
     if args.only == "prefill":
         return {"prefill": bench_prefill(args, torch, moe, gen, gd, dev, peaks)}
+    if args.only == "route":
+        return {"route": bench_route(args, torch, moe, gen, dev)}
     if args.only in ("stack", "flat"):
         link = link_h2d_gbs(torch, dev)
         return {args.only: bench_multilayer(args, torch, moe, gen, gd, dev, args.only, link)}
@@ -718,7 +760,7 @@ def main():
     ap.add_argument("--decode-only", action="store_true")
     ap.add_argument("--small", action="store_true",
                     help="16 distinct expert records (profiler captures only)")
-    ap.add_argument("--only", default="", choices=["", "prefill", "stack", "flat"],
+    ap.add_argument("--only", default="", choices=["", "prefill", "route", "stack", "flat"],
                     help="run one secondary workload alone (profiler captures)")
     ap.add_argument("--prefill-experts", type=int, default=0,
                     help="prefill with fewer experts, same tokens per expert (profiling)")

@@ -61,103 +61,182 @@ __global__ void __launch_bounds__(256) k_logits_gemv(const uint16_t* __restrict_
 }
 
 // ---- logits for many tokens: SIMT tiled GEMM --------------------------------
-// Tile 128 tokens x 32 experts, 128 threads, 8 tokens x 4 experts each (32
-// FMAs per three 16-byte shared loads), K chunks of 32.  Each chunk's partial
-// sum is added to the running total with Kahan compensation, keeping the fp32
-// error of the 6144-term dot products near that of the chunk sums (the router
-// probabilities are compared at 1e-5).  The next chunk's global loads are
-// issued before the current chunk is computed; the x tile is stored
-// transposed (k-major).  288 experts = 9 tiles: 288 CTAs for 4096 tokens, two
-// per SM on most SMs, all resident at once.
+// Tile 128 tokens x 32 experts, 128 threads, 8 tokens x 4 experts each, K
+// chunks of 32.  The FMAs are packed pairs (fma.rn.f32x2 over two tokens and
+// one weight; each lane rounds as a scalar fmaf would).  Shared memory holds
+// x as bf16 words of two tokens at one k and W as fp32, so one 16-byte load
+// gives a thread its 8 tokens (the same address across each quarter-warp)
+// and one its 4 weights: six shared-memory wavefronts per 1024 FMAs of a
+// warp.  Each chunk's partial sum is added to the running total with Kahan
+// compensation (packed adds), keeping the fp32 error of the 6144-term dot
+// products near that of the chunk sums (the router probabilities are
+// compared at 1e-5).  Shared memory is double-buffered: the next chunk's
+// global loads are issued before the current chunk's FMAs and stored into
+// the other buffer after them, one barrier per chunk.  288 experts = 9 tiles:
+// 288 CTAs for 4096 tokens, two per SM on most SMs, all resident at once.
 constexpr int kTM = 128, kTN = 32, kTK = 32, kGemmThreads = 128;
+constexpr int kXsLd = kTM / 2 + 4, kWsLd = kTN + 4;  // 32-bit words per shared row
+
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p)
+               : "memory");
+  return r;
+}
+// shared-tile column swizzles of the router GEMM: multiples of 8 (x words)
+// and of 4 (weights) keep each thread's 16-byte group contiguous
+__device__ __forceinline__ int xs_swz(int kk) { return ((kk >> 3) & 3) << 3; }
+__device__ __forceinline__ int ws_swz(int kk) { return ((kk >> 3) & 3) << 2; }
+__device__ __forceinline__ uint64_t f2_pack(uint32_t lo, uint32_t hi) {
+  return (uint64_t)lo | ((uint64_t)hi << 32);
+}
 
 __global__ void __launch_bounds__(kGemmThreads) k_logits_gemm(const uint16_t* __restrict__ x,
                                                               const float* __restrict__ wr,
                                                               const float* __restrict__ bias,
                                                               int T, int H, int E,
                                                               float* __restrict__ logits) {
-  __shared__ __align__(16) float xs[kTK][kTM + 4];
-  __shared__ __align__(16) float ws[kTK][kTN + 4];
+  // xs[b][kk][p] = x[t0 + 2p][k0 + kk] | x[t0 + 2p + 1][k0 + kk] << 16 (bf16 bits)
+  __shared__ __align__(16) uint32_t xs[2][kTK][kXsLd];
+  __shared__ __align__(16) float ws[2][kTK][kWsLd];  // ws[b][kk][c] = w[e0 + c][k0 + kk]
   const int t0 = blockIdx.y * kTM, e0 = blockIdx.x * kTN;
   const int tid = threadIdx.x;
-  const int tx = tid & 7, ty = tid >> 3;  // 8 x 16 threads; tokens ty*8.., experts tx*4..
-  // load roles: x: token tid, all 32 k of the chunk; W: expert ln = tid % 32,
-  // k quarter lkq = tid / 32 (8 values)
-  const int ln = tid & 31, lkq = tid >> 5;
-  const bool xok = t0 + tid < T, wok = e0 + ln < E;
-  const uint4* xsrc = reinterpret_cast<const uint4*>(x + (size_t)(xok ? t0 + tid : 0) * H);
-  const float4* wsrc = reinterpret_cast<const float4*>(wr + (size_t)(wok ? e0 + ln : 0) * H + lkq * 8);
-  uint4 xv[4];
-  float4 wa, wb;
+  const int tx = tid & 7, ty = tid >> 3;  // tokens ty*8.., experts tx*4..
+  // Load roles, each warp instruction reading whole 64- or 128-byte row
+  // pieces: x: row pair q = tid/4 (+32), 16-byte piece xc = tid % 4 (k =
+  // 8 xc..); W: expert we = tid/8 (+16), piece wc = tid % 8 (k = 4 wc..).
+  // The next chunk's loads are ordered before this chunk's shared-memory
+  // reads (a memory clobber), so they are in flight during its FMAs; rows past
+  // T and experts past E read row 0 and are zeroed when staged.  Stores are
+  // swizzled (columns XORed by a function of k) so that they hit 32 banks.
+  const int xq = tid >> 2, xc = tid & 3, we = tid >> 3, wc = tid & 7;
+  const uint4* xsrc[4];
+  bool xok[4];
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {  // rows 2(xq + 32(r/2)) + r%2
+    const int t = t0 + 2 * (xq + 32 * (r >> 1)) + (r & 1);
+    xok[r] = t < T;
+    xsrc[r] = reinterpret_cast<const uint4*>(x + (size_t)(xok[r] ? t : 0) * H + xc * 8);
+  }
+  const uint4* wsrc[2];
+  bool wok[2];
+#pragma unroll
+  for (int m = 0; m < 2; ++m) {
+    const int e = e0 + we + 16 * m;
+    wok[m] = e < E;
+    wsrc[m] = reinterpret_cast<const uint4*>(wr + (size_t)(wok[m] ? e : 0) * H + wc * 4);
+  }
+  uint4 xv4[4], wv4[2];
   auto fetch = [&](int k0) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) xv[i] = xok ? __ldg(xsrc + k0 / 8 + i) : make_uint4(0u, 0u, 0u, 0u);
-    if (wok) {
-      wa = __ldg(wsrc + k0 / 4);
-      wb = __ldg(wsrc + k0 / 4 + 1);
-    } else {
-      wa = wb = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int r = 0; r < 4; ++r) xv4[r] = ldg_nc_v4(xsrc[r] + k0 / 8);
+#pragma unroll
+    for (int m = 0; m < 2; ++m) wv4[m] = ldg_nc_v4(wsrc[m] + k0 / 4);
+  };
+  auto stage = [&](int buf) {
+#pragma unroll
+    for (int g = 0; g < 2; ++g) {
+      const uint4 lo4 = xv4[2 * g], hi4 = xv4[2 * g + 1];
+      const bool ok0 = xok[2 * g], ok1 = xok[2 * g + 1];
+      const uint32_t a[4] = {ok0 ? lo4.x : 0u, ok0 ? lo4.y : 0u, ok0 ? lo4.z : 0u,
+                             ok0 ? lo4.w : 0u};
+      const uint32_t c[4] = {ok1 ? hi4.x : 0u, ok1 ? hi4.y : 0u, ok1 ? hi4.z : 0u,
+                             ok1 ? hi4.w : 0u};
+      const int q = xq + 32 * g;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {  // word j holds k = 2j (low half), 2j + 1
+        const int kk = xc * 8 + 2 * j;
+        xs[buf][kk][q ^ xs_swz(kk)] = __byte_perm(a[j], c[j], 0x5410);
+        xs[buf][kk + 1][q ^ xs_swz(kk + 1)] = __byte_perm(a[j], c[j], 0x7632);
+      }
+    }
+#pragma unroll
+    for (int m = 0; m < 2; ++m) {
+      const uint32_t w4[4] = {wv4[m].x, wv4[m].y, wv4[m].z, wv4[m].w};
+      const int e = we + 16 * m;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int kk = wc * 4 + i;
+        ws[buf][kk][e ^ ws_swz(kk)] = __uint_as_float(wok[m] ? w4[i] : 0u);
+      }
     }
   };
-  float acc[8][4], cmp[8][4];
+  // pairs: [q][j] = tokens ty*8 + 2q (low) and + 2q + 1 (high), expert tx*4 + j
+  uint64_t acc[4][4], cmp[4][4];
 #pragma unroll
-  for (int i = 0; i < 8; ++i)
+  for (int i = 0; i < 4; ++i)
 #pragma unroll
-    for (int j = 0; j < 4; ++j) acc[i][j] = cmp[i][j] = 0.f;
+    for (int j = 0; j < 4; ++j) acc[i][j] = cmp[i][j] = 0ull;
+  const int nch = H / kTK;
   fetch(0);
-  for (int k0 = 0; k0 < H; k0 += kTK) {
-    __syncthreads();  // the previous chunk's reads of xs / ws are done
+  stage(0);
+  __syncthreads();
+  for (int c = 0; c < nch; ++c) {
+    const int buf = c & 1;
+    if (c + 1 < nch) fetch((c + 1) * kTK);  // in flight during this chunk's FMAs
+    uint64_t part[4][4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint32_t v[4] = {xv[i].x, xv[i].y, xv[i].z, xv[i].w};
+    for (int i = 0; i < 4; ++i)
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        xs[i * 8 + 2 * q][tid] = bf16_lo(v[q]);
-        xs[i * 8 + 2 * q + 1][tid] = bf16_hi(v[q]);
-      }
-    }
-    {
-      const float w8[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+      for (int j = 0; j < 4; ++j) part[i][j] = 0ull;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) ws[lkq * 8 + i][ln] = w8[i];
-    }
-    __syncthreads();
-    if (k0 + kTK < H) fetch(k0 + kTK);  // in flight during this chunk's FMAs
-    float part[8][4];
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) part[i][j] = 0.f;
-#pragma unroll 4
     for (int kk = 0; kk < kTK; ++kk) {
-      const float4 a0 = *reinterpret_cast<const float4*>(&xs[kk][ty * 8]);
-      const float4 a1 = *reinterpret_cast<const float4*>(&xs[kk][ty * 8 + 4]);
-      const float4 b = *reinterpret_cast<const float4*>(&ws[kk][tx * 4]);
-      const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-      const float bv[4] = {b.x, b.y, b.z, b.w};
+      const uint4 xv = *reinterpret_cast<const uint4*>(&xs[buf][kk][(ty * 4) ^ xs_swz(kk)]);
+      const float4 wv = *reinterpret_cast<const float4*>(&ws[buf][kk][(tx * 4) ^ ws_swz(kk)]);
+      const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+      uint64_t A[4], B[4];
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
+      for (int i = 0; i < 4; ++i) A[i] = f2_pack(xw[i] << 16, xw[i] & 0xFFFF0000u);
+      B[0] = f2_pack(__float_as_uint(wv.x), __float_as_uint(wv.x));
+      B[1] = f2_pack(__float_as_uint(wv.y), __float_as_uint(wv.y));
+      B[2] = f2_pack(__float_as_uint(wv.z), __float_as_uint(wv.z));
+      B[3] = f2_pack(__float_as_uint(wv.w), __float_as_uint(wv.w));
 #pragma unroll
-        for (int j = 0; j < 4; ++j) part[i][j] = fmaf(av[i], bv[j], part[i][j]);
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) part[i][j] = f2_fma(A[i], B[j], part[i][j]);
     }
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
+    for (int i = 0; i < 4; ++i)
 #pragma unroll
       for (int j = 0; j < 4; ++j) {  // Kahan: acc += part
-        float y = part[i][j] - cmp[i][j];
-        float s = acc[i][j] + y;
-        cmp[i][j] = (s - acc[i][j]) - y;
-        acc[i][j] = s;
+        const uint64_t y = f2_sub(part[i][j], cmp[i][j]);
+        const uint64_t s2 = f2_add(acc[i][j], y);
+        cmp[i][j] = f2_sub(f2_sub(s2, acc[i][j]), y);
+        acc[i][j] = s2;
       }
+    if (c + 1 < nch) stage(buf ^ 1);  // that buffer's last reads were in chunk c - 1
+    __syncthreads();
   }
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int t = t0 + ty * 8 + i;
-    if (t >= T) continue;
+  for (int i = 0; i < 4; ++i) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int e = e0 + tx * 4 + j;
-      if (e < E) logits[(size_t)t * E + e] = acc[i][j] + (bias ? bias[e] : 0.f);
+    for (int h = 0; h < 2; ++h) {
+      const int t = t0 + ty * 8 + 2 * i + h;
+      if (t >= T) continue;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int e = e0 + tx * 4 + j;
+        const float v = __uint_as_float((uint32_t)(acc[i][j] >> (32 * h)));
+        if (e < E) logits[(size_t)t * E + e] = v + (bias ? bias[e] : 0.f);
+      }
     }
   }
 }
