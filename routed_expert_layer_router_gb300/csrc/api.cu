@@ -15,7 +15,7 @@ int cache_L(const expcache* c);
 int cache_H(const expcache* c);
 int cache_I(const expcache* c);
 size_t decode_workspace_bytes(int T, int I, int k, int Is);
-moe_status decode_ffn(const moe_ffn_args* a, cudaStream_t s);
+moe_status decode_ffn(const moe_ffn_args* a, cudaStream_t s, bool shared_early);
 moe_status decode_setup();
 size_t prefill_workspace_bytes(int T, int H, int I, int E, int k, int Is);
 moe_status prefill_ffn(const moe_ffn_args* a, cudaStream_t s);
@@ -28,6 +28,16 @@ moe_status launch_permute(const int32_t* ids, int T, int k, int E, int32_t* coun
                           int pad_align, int32_t* status, const LookupArgs& lk, cudaStream_t s);
 void cache_lookup_args(const expcache* c, int layer, int32_t* src_slot, int32_t* act_list,
                        int32_t* n_act, int32_t* miss_ids, int32_t* n_miss, LookupArgs* out);
+}  // namespace moe
+
+namespace moe {
+bool pdl_enabled() {
+  static const int on = [] {
+    const char* v = getenv("MOE_PDL");
+    return (v && v[0] == '0') ? 0 : 1;
+  }();
+  return on != 0;
+}
 }  // namespace moe
 
 using namespace moe;
@@ -66,7 +76,9 @@ MOE_API size_t moe_ffn_workspace_bytes(int mode, int T, int H, int I, int E, int
   return decode_workspace_bytes(T, I, k, Is);
 }
 
-MOE_API moe_status moe_expert_ffn(const moe_ffn_args* a, void* stream) {
+// shared_early: the caller's previous kernel on the stream neither reads nor
+// writes the workspace's shared-expert buffer (see DecodeParams)
+static moe_status expert_ffn(const moe_ffn_args* a, void* stream, bool shared_early) {
   if (!a || !a->cache || !a->gscale || !a->src_slot || !a->act_list || !a->n_act || !a->offsets ||
       !a->perm || !a->w || !a->x)
     return MOE_ERR_INVALID_ARG;
@@ -86,13 +98,17 @@ MOE_API moe_status moe_expert_ffn(const moe_ffn_args* a, void* stream) {
   if (st != MOE_OK) return st;
   if (a->mode == MOE_MODE_DECODE) {
     if (!a->o_route || a->stages < 1 || a->stages > 3) return MOE_ERR_INVALID_ARG;
-    return decode_ffn(a, (cudaStream_t)stream);
+    return decode_ffn(a, (cudaStream_t)stream, shared_early);
   }
   if (a->mode == MOE_MODE_PREFILL) {
     if (!a->y_acc || !a->pad_offsets) return MOE_ERR_INVALID_ARG;
     return prefill_ffn(a, (cudaStream_t)stream);
   }
   return MOE_ERR_INVALID_ARG;
+}
+
+MOE_API moe_status moe_expert_ffn(const moe_ffn_args* a, void* stream) {
+  return expert_ffn(a, stream, false);
 }
 
 // ------------------------------------------------------------------- layer
@@ -262,7 +278,8 @@ MOE_API moe_status moe_layer_forward(moe_layer* l, const void* x, int T, void* y
         return st;
     }
     fa.group = g;
-    if ((st = moe_expert_ffn(&fa, stream)) != MOE_OK) return st;
+    // the kernel before this call is the permutation or the gather
+    if ((st = expert_ffn(&fa, stream, true)) != MOE_OK) return st;
   }
 
   moe_combine_args ca;

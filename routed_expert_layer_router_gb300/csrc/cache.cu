@@ -37,6 +37,8 @@ __global__ void __launch_bounds__(kGatherThreads) k_gather(
     uint8_t* __restrict__ arena, int32_t* __restrict__ table_row, int E, uint64_t rec_bytes,
     int n_cache, int n_stage, const int32_t* __restrict__ ids, const int32_t* __restrict__ d_n,
     int first, const int32_t* __restrict__ dst_slots, int slot_lo, int slot_hi, int32_t* status) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int i = first + blockIdx.y;
   if (i >= *d_n) return;
   const int e = ids[i];
@@ -195,12 +197,12 @@ MOE_API moe_status expcache_fill(expcache* c, int layer, const int32_t* d_expert
   if (!d_dst_slots && c->n_stage == 0) return MOE_ERR_INVALID_ARG;
   if (max_count > 65535) return MOE_ERR_UNSUPPORTED;
   dim3 grid(gather_blocks_per_record(c->rec_bytes, max_count), max_count);
-  k_gather<<<grid, kGatherThreads, 0, (cudaStream_t)stream>>>(
-      c->host_dev, c->host_index_dev ? c->host_index_dev + (size_t)layer * c->E : nullptr,
-      c->host_records, c->arena, c->table + (size_t)layer * c->E, c->E, c->rec_bytes, c->n_cache,
-      c->n_stage, d_expert_ids, d_n, first, d_dst_slots, c->slot_lo[layer], c->slot_hi[layer],
-      status);
-  MOE_CHECK_LAUNCH();
+  if (launch_pdl(k_gather, grid, kGatherThreads, 0, (cudaStream_t)stream, c->host_dev,
+                 c->host_index_dev ? c->host_index_dev + (size_t)layer * c->E : nullptr,
+                 c->host_records, c->arena, c->table + (size_t)layer * c->E, c->E, c->rec_bytes,
+                 c->n_cache, c->n_stage, d_expert_ids, d_n, first, d_dst_slots,
+                 c->slot_lo[layer], c->slot_hi[layer], status) != cudaSuccess)
+    return MOE_ERR_CUDA;
   return MOE_OK;
 }
 

@@ -105,6 +105,44 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+// ---- programmatic dependent launch ------------------------------------------
+// A kernel launched with launch_pdl() on a stream that is not being captured
+// may start while the previous kernel on its stream is still running (inside
+// a CUDA graph the launches stay plain: measured slower there).  pdl_wait() blocks until that kernel has
+// completed and its writes are visible; pdl_launch_dependents() lets the next
+// kernel start launching.  Every kernel launched with launch_pdl() calls
+// pdl_wait() before it touches memory that an earlier kernel writes or reads,
+// and triggers only after that wait, so each launch can run ahead of at most
+// the one kernel before it.  Both are no-ops after a normal launch.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+bool pdl_enabled();  // on unless the environment sets MOE_PDL=0
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  bool plain = !pdl_enabled();
+  if (!plain && cudaStreamIsCapturing(s, &cs) != cudaSuccess) {
+    cudaGetLastError();  // not a launch error: launch without the attribute
+    plain = true;
+  }
+  cfg.numAttrs = (plain || cs != cudaStreamCaptureStatusNone) ? 0 : 1;
+  return cudaLaunchKernelEx(&cfg, kern, ((KArgs)args)...);
+}
+
 }  // namespace moe
 
 // host-side error plumbing

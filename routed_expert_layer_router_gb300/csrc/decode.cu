@@ -53,6 +53,11 @@ struct DecodeParams {
   float* o_shared;  // [T][H]
   int32_t* status;
   int maxm;  // tokens staged per pass (1 or 2)
+  // the shared-expert units of K-decode-gu may start before the previous
+  // kernel on the stream completes: set only when that kernel neither reads
+  // nor writes h_shared (the layer's own sequence, where it is the
+  // permutation or the gather)
+  int shared_early;
 };
 
 // act_list index range of this group
@@ -354,6 +359,10 @@ __global__ void __launch_bounds__(kDecThreads) k_decode_gu(DecodeParams p) {
   const int wid = threadIdx.x >> 5;
   const int u = blockIdx.x;
   if (u >= p.n_routed_units) {
+    // the shared expert reads only x and its weights: in the layer's own
+    // sequence it runs without waiting for the routing
+    if (!p.shared_early) pdl_wait();
+    pdl_launch_dependents();
     float* xs = reinterpret_cast<float*>(smem_raw);
     const int i0 = (u - p.n_routed_units) * 4;
     for (int t0 = 0; t0 < p.T; t0 += p.maxm) {
@@ -368,6 +377,8 @@ __global__ void __launch_bounds__(kDecThreads) k_decode_gu(DecodeParams p) {
     }
     return;
   }
+  pdl_wait();
+  pdl_launch_dependents();
   __half* xs = reinterpret_cast<__half*>(smem_raw);
   const int ur = u;
   const int tiles = p.I / 128;
@@ -472,6 +483,8 @@ __global__ void __launch_bounds__(kDecThreads) k_decode_down(DecodeParams p) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   const int wid = threadIdx.x >> 5;
   const int u = blockIdx.x;
+  pdl_wait();
+  pdl_launch_dependents();
   if (u < p.n_shared_units) {
     float* hs = reinterpret_cast<float*>(smem_raw);
     const int r0 = u * (kDecWarps * 4) + wid * 4;
@@ -520,6 +533,8 @@ __global__ void k_combine(int T, int H, int k, const float* __restrict__ y_acc,
                           const float* __restrict__ o_route, const int32_t* __restrict__ inv,
                           const float* __restrict__ o_shared, uint16_t* __restrict__ y) {
   const int n4 = H / 4;
+  pdl_wait();
+  pdl_launch_dependents();
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < T * n4; i += gridDim.x * blockDim.x) {
     const int t = i / n4, c = (i % n4) * 4;
     float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -551,8 +566,9 @@ size_t decode_workspace_bytes(int T, int I, int k, int Is) {
 static size_t smem_f16(int maxm, int K) { return (size_t)maxm * (K / 32) * kHPad * sizeof(__half); }
 static size_t smem_f32(int maxm, int K) { return (size_t)maxm * (K / 32) * kXPad * sizeof(float); }
 
-moe_status decode_ffn(const moe_ffn_args* a, cudaStream_t s) {
+moe_status decode_ffn(const moe_ffn_args* a, cudaStream_t s, bool shared_early) {
   DecodeParams p;
+  p.shared_early = shared_early ? 1 : 0;
   p.T = a->T; p.H = a->H; p.I = a->I; p.E = a->E; p.k = a->k; p.Is = a->Is;
   p.x = (const uint16_t*)a->x;
   p.arena = cache_arena(a->cache);
@@ -583,9 +599,9 @@ moe_status decode_ffn(const moe_ffn_args* a, cudaStream_t s) {
     if (shared && smem_f32(p.maxm, a->H) > smem) smem = smem_f32(p.maxm, a->H);
     const int grid = p.n_shared_units + routed;
     if (grid > 0) {
-      if (p.maxm == 2) k_decode_gu<2><<<grid, kDecThreads, smem, s>>>(p);
-      else k_decode_gu<1><<<grid, kDecThreads, smem, s>>>(p);
-      MOE_CHECK_LAUNCH();
+      if (launch_pdl(p.maxm == 2 ? k_decode_gu<2> : k_decode_gu<1>, grid, kDecThreads, smem, s,
+                     p) != cudaSuccess)
+        return MOE_ERR_CUDA;
     }
   }
   if (a->stages & MOE_STAGE_DOWN) {
@@ -595,9 +611,9 @@ moe_status decode_ffn(const moe_ffn_args* a, cudaStream_t s) {
     if (shared && smem_f32(p.maxm, a->Is) > smem) smem = smem_f32(p.maxm, a->Is);
     const int grid = p.n_shared_units + routed;
     if (grid > 0) {
-      if (p.maxm == 2) k_decode_down<2><<<grid, kDecThreads, smem, s>>>(p);
-      else k_decode_down<1><<<grid, kDecThreads, smem, s>>>(p);
-      MOE_CHECK_LAUNCH();
+      if (launch_pdl(p.maxm == 2 ? k_decode_down<2> : k_decode_down<1>, grid, kDecThreads, smem,
+                     s, p) != cudaSuccess)
+        return MOE_ERR_CUDA;
     }
   }
   return MOE_OK;
@@ -626,8 +642,8 @@ MOE_API moe_status moe_combine(const moe_combine_args* a, void* stream) {
   long long n = (long long)a->T * (a->H / 4);
   int grid = (int)((n + 255) / 256);
   if (grid > kSMs * 16) grid = kSMs * 16;
-  k_combine<<<grid, 256, 0, (cudaStream_t)stream>>>(a->T, a->H, a->k, a->y_acc, a->o_route, a->inv,
-                                                    a->o_shared, (uint16_t*)a->y);
-  MOE_CHECK_LAUNCH();
+  if (launch_pdl(k_combine, grid, 256, 0, (cudaStream_t)stream, a->T, a->H, a->k, a->y_acc,
+                 a->o_route, a->inv, a->o_shared, (uint16_t*)a->y) != cudaSuccess)
+    return MOE_ERR_CUDA;
   return MOE_OK;
 }

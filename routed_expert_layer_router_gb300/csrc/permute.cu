@@ -95,6 +95,8 @@ __global__ void __launch_bounds__(kPermThreads) k_permute(const int32_t* __restr
   int* s_scan = s_w + kPermWarps * E;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const bool lead = blockIdx.x == 0;
+  pdl_wait();
+  pdl_launch_dependents();
   const int r0 = blockIdx.x * kPermThreads;
 
   for (int e = tid; e < E; e += kPermThreads) {
@@ -168,6 +170,8 @@ __global__ void __launch_bounds__(kPermThreads) k_lookup(LookupArgs a, int E,
                                                          int32_t* status) {
   __shared__ int s_scan[33];
   const int e = threadIdx.x;
+  pdl_wait();
+  pdl_launch_dependents();
   lookup_body(a, E, e < E ? counts[e] : 0, s_scan, status);
 }
 
@@ -202,9 +206,9 @@ moe_status launch_permute(const int32_t* ids, int T, int k, int E, int32_t* coun
   if (smem > 48 * 1024 && permute_setup() != MOE_OK) return MOE_ERR_CUDA;
   const int n = T * k;
   const int grid = n > 0 ? (n + kPermThreads - 1) / kPermThreads : 1;
-  k_permute<<<grid, kPermThreads, smem, s>>>(ids, T * k, E, counts, offsets, perm, inv, pad_offsets,
-                                          pad_align, status, lk);
-  MOE_CHECK_LAUNCH();
+  if (launch_pdl(k_permute, grid, kPermThreads, smem, s, ids, T * k, E, counts, offsets, perm, inv,
+                 pad_offsets, pad_align, status, lk) != cudaSuccess)
+    return MOE_ERR_CUDA;
   return MOE_OK;
 }
 }  // namespace moe
@@ -221,8 +225,8 @@ MOE_API moe_status moe_permute(const int32_t* ids, int T, int k, int E, int32_t*
 namespace moe {
 moe_status launch_lookup(const LookupArgs& a, int E, const int32_t* counts, int32_t* status,
                          cudaStream_t s) {
-  k_lookup<<<1, kPermThreads, 0, s>>>(a, E, counts, status);
-  MOE_CHECK_LAUNCH();
+  if (launch_pdl(k_lookup, 1, kPermThreads, 0, s, a, E, counts, status) != cudaSuccess)
+    return MOE_ERR_CUDA;
   return MOE_OK;
 }
 }  // namespace moe

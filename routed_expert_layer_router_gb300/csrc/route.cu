@@ -57,6 +57,8 @@ __global__ void __launch_bounds__(256) k_logits_gemv(const uint16_t* __restrict_
                                                      const float* __restrict__ wr,
                                                      const float* __restrict__ bias, int T,
                                                      int H, int E, float* __restrict__ logits) {
+  pdl_wait();
+  pdl_launch_dependents();
   logits_of_expert(x, wr, bias, T, H, E, blockIdx.x, logits);
 }
 
@@ -116,6 +118,8 @@ __global__ void __launch_bounds__(kGemmThreads) k_logits_gemm(const uint16_t* __
   // xs[b][kk][p] = x[t0 + 2p][k0 + kk] | x[t0 + 2p + 1][k0 + kk] << 16 (bf16 bits)
   __shared__ __align__(16) uint32_t xs[2][kTK][kXsLd];
   __shared__ __align__(16) float ws[2][kTK][kWsLd];  // ws[b][kk][c] = w[e0 + c][k0 + kk]
+  pdl_wait();
+  pdl_launch_dependents();
   const int t0 = blockIdx.y * kTM, e0 = blockIdx.x * kTN;
   const int tid = threadIdx.x;
   const int tx = tid & 7, ty = tid >> 3;  // tokens ty*8.., experts tx*4..
@@ -300,6 +304,8 @@ __global__ void __launch_bounds__(256) k_topk(const float* __restrict__ logits, 
                                               int k, int32_t* __restrict__ ids,
                                               float* __restrict__ w, float* __restrict__ p_sel) {
   extern __shared__ float sl[];  // [8 warps][E]
+  pdl_wait();
+  pdl_launch_dependents();
   const int wid = threadIdx.x >> 5;
   const int t = blockIdx.x * 8 + wid;
   if (t >= T) return;
@@ -322,6 +328,8 @@ __global__ void __launch_bounds__(256) k_route_small(const uint16_t* __restrict_
                                                      unsigned int* __restrict__ done) {
   extern __shared__ float sl[];  // [8 warps][E]
   __shared__ int s_last;
+  pdl_wait();
+  pdl_launch_dependents();
   logits_of_expert(x, wr, bias, T, H, E, blockIdx.x, logits);
   __threadfence();  // this CTA's logits are visible before it is counted
   __syncthreads();
@@ -362,21 +370,26 @@ MOE_API moe_status moe_route(const moe_route_args* a, void* stream) {
   const uint16_t* x = (const uint16_t*)a->x;
   size_t smem = (size_t)8 * a->E * sizeof(float);
   if (a->T <= kGemvMaxT && a->workspace && a->workspace_bytes >= kRouteCtl) {
-    k_route_small<<<a->E, 256, smem, s>>>(x, a->w_router, a->bias, a->T, a->H, a->E, a->k,
-                                          logits, a->ids, a->w, a->p_sel,
-                                          (unsigned int*)a->workspace);
-    MOE_CHECK_LAUNCH();
+    if (launch_pdl(k_route_small, a->E, 256, smem, s, x, a->w_router, a->bias, a->T, a->H, a->E,
+                   a->k, logits, a->ids, a->w, a->p_sel, (unsigned int*)a->workspace) !=
+        cudaSuccess)
+      return MOE_ERR_CUDA;
     return MOE_OK;
   }
   if (a->T <= kGemvMaxT) {
-    k_logits_gemv<<<a->E, 256, 0, s>>>(x, a->w_router, a->bias, a->T, a->H, a->E, logits);
+    if (launch_pdl(k_logits_gemv, a->E, 256, 0, s, x, a->w_router, a->bias, a->T, a->H, a->E,
+                   logits) != cudaSuccess)
+      return MOE_ERR_CUDA;
   } else {
     dim3 grid((a->E + kTN - 1) / kTN, (a->T + kTM - 1) / kTM);
-    k_logits_gemm<<<grid, kGemmThreads, 0, s>>>(x, a->w_router, a->bias, a->T, a->H, a->E,
-                                                logits);
+    if (launch_pdl(k_logits_gemm, grid, kGemmThreads, 0, s, x, a->w_router, a->bias, a->T, a->H,
+                   a->E, logits) != cudaSuccess)
+      return MOE_ERR_CUDA;
   }
   MOE_CHECK_LAUNCH();
-  k_topk<<<(a->T + 7) / 8, 256, smem, s>>>(logits, a->T, a->E, a->k, a->ids, a->w, a->p_sel);
+  if (launch_pdl(k_topk, (a->T + 7) / 8, 256, smem, s, logits, a->T, a->E, a->k, a->ids, a->w,
+                 a->p_sel) != cudaSuccess)
+    return MOE_ERR_CUDA;
   MOE_CHECK_LAUNCH();
   return MOE_OK;
 }
