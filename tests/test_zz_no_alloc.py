@@ -58,13 +58,14 @@ def _layer_out(o, os_, inv, T, k, H):
         os_.double().view(T, H).cpu().numpy()
 
 
-def test_noalloc_entry_point_matches_workspace_entry_point():
+@pytest.mark.parametrize("T", [1, 2])
+def test_noalloc_entry_point_matches_workspace_entry_point(T):
     if not torch.cuda.is_available():
         pytest.skip("no GPU")
     import gen.device as gd
     from routed_expert_layer_router_gb300 import moe
     wl = gen.WORKLOADS["decode"]
-    T, H, I, E, k, Is = 2, wl.H, wl.I, wl.E, wl.k, wl.Is
+    H, I, E, k, Is = wl.H, wl.I, wl.E, wl.k, wl.Is
     dw = gd.build(wl, T_max=T)
     try:
         s = torch.cuda.current_stream().cuda_stream
