@@ -39,6 +39,12 @@ import numpy as np  # noqa: E402
 METRIC = "MoE-layer tokens/s (decode, 4096-tok prefill); % of HBM / FP4-TC / PCIe roofline"
 UNIT = "tokens/s"
 FP4_OVER_BF16 = 6.0  # nominal dense FP4 / dense bf16 tensor throughput (13.5 / 2.25)
+# DRAM bytes (read + write) of one k_decode_gu launch on the full decode layer, from
+# one ncu capture of the current kernel (profiles/k_decode_gu_decode-layer.md); set to
+# None whenever the kernel changes until it is captured again
+GU_TRAFFIC = 163_920_128
+GU_TRAFFIC_SOURCE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum, full decode layer, "
+                     "profiles/k_decode_gu_decode-layer.md")
 
 
 def _peaks():
@@ -368,7 +374,8 @@ def bench_decode(args, torch, moe, gen, gd, dev, rank, world, local_rank, peaks)
                      "kernel": "k_decode_gu (routed NVFP4 gate/up of the 8 experts + shared "
                                "bf16 gate/up, SiLU*mul)",
                      "achieved": round(gu_gbs, 1), "peak": hbm, "unit": "GB/s",
-                     "frac": round(gu_gbs / hbm, 4), "traffic": None,
+                     "frac": round(gu_gbs / hbm, 4), "traffic": GU_TRAFFIC,
+                     "traffic_source": GU_TRAFFIC_SOURCE,
                      "bytes_per_launch": gu_bytes, "avg_launch_ms": round(gu_ms, 5)},
         "kernels": {
             "k_decode_gu": {"ms": round(gu_ms, 5), "GB/s": round(gu_gbs, 1),
