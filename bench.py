@@ -4,13 +4,16 @@ Headline (the JSON line's `value`): the decode MoE layer - hidden 6144, expert
 intermediate 2048, 288 experts top-8 (fp32 softmax router), one bf16 shared
 expert, NVFP4 routed experts all resident in HBM, 1 token per forward.  A step
 is one pass of the whole hot path (route -> permute -> cache lookup -> expert
-FFN gate/up -> down -> combine) over one fresh token; L2 is flushed between
+FFN gate/up -> down -> combine; three kernels for one token: router with the
+permutation and lookup, gate/up, down with the combine) over one fresh token;
+L2 is flushed between
 steps outside the timed events (a buffer larger than L2 written, then another
 read, so that no dirty line of the flush is written back inside a timed step).
 
 The same run also measures (the `also` object), each in its own bounded pass:
-  prefill  one layer on a 4096-token chunk, experts walked in groups of 64
+  prefill  one layer on a 4096-token chunk, one launch per GEMM over all experts
            (tcgen05 NVFP4 grouped GEMMs): tokens/s, HBM and FP4 tensor fractions;
+           and the same walked in launch groups of 64 experts;
   stack    16 decode layers, per-layer Zipf-skewed routing, 66 hot experts per
            layer in HBM, misses gathered from pinned host memory: tokens/s,
            hit rate, gather GB/s against the measured host->device link;
@@ -249,13 +252,14 @@ class ExplicitLayer:
         moe.moe_combine(self.ca, sp)
 
     def layer_launches(self):
-        """Kernels one moe_layer_forward launches for this layer and T: the
-        router (one kernel for T <= 8), permutation + slot lookup (one
-        kernel), per expert group the gather (if staging) and the two FFN
-        kernels, and the combine."""
+        """Kernels one decode moe_layer_forward launches for this layer and T:
+        router + permutation + slot lookup (one kernel for T <= 8, else the
+        router GEMM, top-k and the permutation), per expert group the gather
+        (if staging) and the two FFN kernels, and the combine unless a single
+        group's down kernel writes y."""
         S = self.dw.cache.n_stage
-        route = 1 if self.T <= 8 else 2
-        return route + 1 + self.groups * (2 + (1 if S > 0 else 0)) + 1
+        route = 1 if self.T <= 8 else 3
+        return route + self.groups * (2 + (1 if S > 0 else 0)) + (0 if self.groups == 1 else 1)
 
 
 # --------------------------------------------------------------- decode

@@ -4,7 +4,7 @@
 #include <stdlib.h>
 #include <string.h>
 
-#include "common.cuh"
+#include "permute_body.cuh"
 
 namespace moe {
 const uint8_t* cache_arena(const expcache* c);
@@ -15,7 +15,7 @@ int cache_L(const expcache* c);
 int cache_H(const expcache* c);
 int cache_I(const expcache* c);
 size_t decode_workspace_bytes(int T, int I, int k, int Is);
-moe_status decode_ffn(const moe_ffn_args* a, cudaStream_t s, bool shared_early);
+moe_status decode_ffn(const moe_ffn_args* a, cudaStream_t s, const DecodeFuse& fz);
 moe_status decode_setup();
 size_t prefill_workspace_bytes(int T, int H, int I, int E, int k, int Is);
 moe_status prefill_ffn(const moe_ffn_args* a, cudaStream_t s);
@@ -28,6 +28,7 @@ moe_status launch_permute(const int32_t* ids, int T, int k, int E, int32_t* coun
                           int pad_align, int32_t* status, const LookupArgs& lk, cudaStream_t s);
 void cache_lookup_args(const expcache* c, int layer, int32_t* src_slot, int32_t* act_list,
                        int32_t* n_act, int32_t* miss_ids, int32_t* n_miss, LookupArgs* out);
+moe_status route_permute_small(const moe_route_args* a, const PermArgs& pa, cudaStream_t s);
 }  // namespace moe
 
 namespace moe {
@@ -41,6 +42,10 @@ bool pdl_enabled() {
 }  // namespace moe
 
 using namespace moe;
+
+// the layer's control area: the few-token router's counter, then one counter
+// per 128-row tile for the combine in the decode down kernel (H <= 16384)
+constexpr size_t kRouteCtlBytes = 256, kTileCtlBytes = 128 * 4;
 
 MOE_API const char* moe_status_string(moe_status s) {
   switch (s) {
@@ -76,9 +81,8 @@ MOE_API size_t moe_ffn_workspace_bytes(int mode, int T, int H, int I, int E, int
   return decode_workspace_bytes(T, I, k, Is);
 }
 
-// shared_early: the caller's previous kernel on the stream neither reads nor
-// writes the workspace's shared-expert buffer (see DecodeParams)
-static moe_status expert_ffn(const moe_ffn_args* a, void* stream, bool shared_early) {
+// fz: what the layer's own sequence allows beyond the public call (DecodeFuse)
+static moe_status expert_ffn(const moe_ffn_args* a, void* stream, const DecodeFuse& fz) {
   if (!a || !a->cache || !a->gscale || !a->src_slot || !a->act_list || !a->n_act || !a->offsets ||
       !a->perm || !a->w || !a->x)
     return MOE_ERR_INVALID_ARG;
@@ -98,7 +102,7 @@ static moe_status expert_ffn(const moe_ffn_args* a, void* stream, bool shared_ea
   if (st != MOE_OK) return st;
   if (a->mode == MOE_MODE_DECODE) {
     if (!a->o_route || a->stages < 1 || a->stages > 3) return MOE_ERR_INVALID_ARG;
-    return decode_ffn(a, (cudaStream_t)stream, shared_early);
+    return decode_ffn(a, (cudaStream_t)stream, fz);
   }
   if (a->mode == MOE_MODE_PREFILL) {
     if (!a->y_acc || !a->pad_offsets) return MOE_ERR_INVALID_ARG;
@@ -108,7 +112,8 @@ static moe_status expert_ffn(const moe_ffn_args* a, void* stream, bool shared_ea
 }
 
 MOE_API moe_status moe_expert_ffn(const moe_ffn_args* a, void* stream) {
-  return expert_ffn(a, stream, false);
+  const DecodeFuse none = {false, nullptr, nullptr, nullptr};
+  return expert_ffn(a, stream, none);
 }
 
 // ------------------------------------------------------------------- layer
@@ -169,7 +174,7 @@ MOE_API moe_status moe_layer_create(const moe_layer_desc* d, moe_layer** out) {
       (size_t)T * H * 4,  /* o_shared */
       prefill ? (size_t)T * H * 4 : 0, /* y_acc */
       l->ffn_ws_bytes,
-      256 /* route_ctl */};
+      kRouteCtlBytes + kTileCtlBytes /* route_ctl, then the combine's tile counters */};
   const int n = (int)(sizeof(sizes) / sizeof(sizes[0]));
   size_t total = 0;
   for (int i = 0; i < n; ++i) total += align256(sizes[i]);
@@ -237,15 +242,22 @@ MOE_API moe_status moe_layer_forward(moe_layer* l, const void* x, int T, void* y
   ra.ids = l->ids; ra.w = l->w; ra.p_sel = l->p_sel; ra.logits = l->logits;
   ra.workspace = l->route_ctl; ra.workspace_bytes = 256;
   ra.status = l->status;
-  if ((st = moe_route(&ra, stream)) != MOE_OK) return st;
-
-  // permutation and slot lookup in one launch
   LookupArgs lk;
   cache_lookup_args(d.cache, d.layer, l->src_slot, l->act_list, l->n_act, l->miss_ids, l->n_miss,
                     &lk);
-  if ((st = launch_permute(l->ids, T, d.k, d.E, l->counts, l->offsets, l->perm, l->inv,
-                           prefill ? l->pad_offsets : nullptr, 128, l->status, lk, s)) != MOE_OK)
-    return st;
+  // up to 8 tokens: router, permutation and slot lookup in one launch;
+  // otherwise the router, then the permutation with the lookup as its tail
+  PermArgs pa;
+  pa.counts = l->counts; pa.offsets = l->offsets; pa.perm = l->perm; pa.inv = l->inv;
+  pa.pad_offsets = prefill ? l->pad_offsets : nullptr; pa.pad_align = 128;
+  pa.status = l->status; pa.lk = lk;
+  st = route_permute_small(&ra, pa, s);
+  if (st == MOE_ERR_UNSUPPORTED) {
+    if ((st = moe_route(&ra, stream)) != MOE_OK) return st;
+    st = launch_permute(l->ids, T, d.k, d.E, l->counts, l->offsets, l->perm, l->inv,
+                        pa.pad_offsets, 128, l->status, lk, s);
+  }
+  if (st != MOE_OK) return st;
 
   const int n_stage = cache_n_stage(d.cache);
   const int max_miss = T * d.k < d.E ? T * d.k : d.E;
@@ -278,8 +290,19 @@ MOE_API moe_status moe_layer_forward(moe_layer* l, const void* x, int T, void* y
         return st;
     }
     fa.group = g;
-    // the kernel before this call is the permutation or the gather
-    if ((st = expert_ffn(&fa, stream, true)) != MOE_OK) return st;
+    // the kernel before this call is the permutation or the gather; a single
+    // decode group's down kernel also writes y (no separate combine)
+    DecodeFuse fz = {true, nullptr, nullptr, nullptr};
+    if (!prefill && groups == 1) {
+      fz.comb_ctl = (unsigned int*)((char*)l->route_ctl + kRouteCtlBytes);
+      fz.inv = l->inv;
+      fz.y = (uint16_t*)y;
+    }
+    if ((st = expert_ffn(&fa, stream, fz)) != MOE_OK) return st;
+  }
+  if (!prefill && groups == 1) {
+    l->last_T = T;
+    return MOE_OK;
   }
 
   moe_combine_args ca;

@@ -121,6 +121,18 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 
 bool pdl_enabled();  // on unless the environment sets MOE_PDL=0
 
+// What the layer's own sequence lets the decode FFN do beyond moe_expert_ffn:
+// start the shared-expert gate/up units before the routing is complete (the
+// kernel before it neither reads nor writes their buffer), and write y in
+// the down kernel (comb_ctl: H/128 zeroed tile counters; only when that
+// launch is the last FFN launch of the forward).
+struct DecodeFuse {
+  bool shared_early;
+  unsigned int* comb_ctl;
+  const int32_t* inv;
+  uint16_t* y;
+};
+
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
                        cudaStream_t s, Args... args) {

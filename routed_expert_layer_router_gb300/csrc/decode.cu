@@ -58,6 +58,13 @@ struct DecodeParams {
   // nor writes h_shared (the layer's own sequence, where it is the
   // permutation or the gather)
   int shared_early;
+  // combine in K-decode-down: per 128-row tile a counter (zero before the
+  // launch, reset by the tile's last CTA) and the CTAs that count into it;
+  // the last one writes y's columns of that tile.  comb_ctl == nullptr: off.
+  unsigned int* comb_ctl;
+  int comb_target;
+  const int32_t* inv;
+  uint16_t* y;
 };
 
 // act_list index range of this group
@@ -478,13 +485,34 @@ __device__ void down_shared_pass(const DecodeParams& p, int r0, int t0, int mm, 
     }
 }
 
+// y[t] for the columns of tile rt, summed in K-combine's order (routes j <
+// k, then the shared expert) from the other CTAs' outputs, read through L2
+__device__ void combine_tile(const DecodeParams& p, int rt) {
+  const int c0 = rt * 128;
+  for (int i = threadIdx.x; i < p.T * 32; i += blockDim.x) {
+    const int t = i >> 5, c = c0 + (i & 31) * 4;
+    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < p.k; ++j) {
+      const int pp = p.inv[t * p.k + j];
+      if (pp < 0) continue;
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(p.o_route + (size_t)pp * p.H + c));
+      s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+    }
+    if (p.o_shared) {
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(p.o_shared + (size_t)t * p.H + c));
+      s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+    }
+    uint2 out;
+    out.x = (uint32_t)f32_to_bf16_rne(s.x) | ((uint32_t)f32_to_bf16_rne(s.y) << 16);
+    out.y = (uint32_t)f32_to_bf16_rne(s.z) | ((uint32_t)f32_to_bf16_rne(s.w) << 16);
+    *reinterpret_cast<uint2*>(p.y + (size_t)t * p.H + c) = out;
+  }
+}
+
 template <int MAXM>
-__global__ void __launch_bounds__(kDecThreads) k_decode_down(DecodeParams p) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
+__device__ __forceinline__ void down_unit(const DecodeParams& p, unsigned char* smem_raw) {
   const int wid = threadIdx.x >> 5;
   const int u = blockIdx.x;
-  pdl_wait();
-  pdl_launch_dependents();
   if (u < p.n_shared_units) {
     float* hs = reinterpret_cast<float*>(smem_raw);
     const int r0 = u * (kDecWarps * 4) + wid * 4;
@@ -528,6 +556,27 @@ __global__ void __launch_bounds__(kDecThreads) k_decode_down(DecodeParams p) {
   }
 }
 
+template <int MAXM>
+__global__ void __launch_bounds__(kDecThreads) k_decode_down(DecodeParams p) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  __shared__ int s_last;
+  pdl_wait();
+  pdl_launch_dependents();
+  down_unit<MAXM>(p, smem_raw);
+  if (!p.comb_ctl) return;
+  // shared units cover 32 rows each (4 per tile); routed units one tile
+  const int u = blockIdx.x;
+  const int rt = u < p.n_shared_units ? u / 4 : (u - p.n_shared_units) % (p.H / 128);
+  __threadfence();  // this CTA's outputs are visible before it is counted
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = atomicAdd(&p.comb_ctl[rt], 1u) == (unsigned)p.comb_target - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  combine_tile(p, rt);
+  if (threadIdx.x == 0) p.comb_ctl[rt] = 0u;  // ready for the next launch
+}
+
 // ---- K-combine ---------------------------------------------------------------
 __global__ void k_combine(int T, int H, int k, const float* __restrict__ y_acc,
                           const float* __restrict__ o_route, const int32_t* __restrict__ inv,
@@ -566,9 +615,13 @@ size_t decode_workspace_bytes(int T, int I, int k, int Is) {
 static size_t smem_f16(int maxm, int K) { return (size_t)maxm * (K / 32) * kHPad * sizeof(__half); }
 static size_t smem_f32(int maxm, int K) { return (size_t)maxm * (K / 32) * kXPad * sizeof(float); }
 
-moe_status decode_ffn(const moe_ffn_args* a, cudaStream_t s, bool shared_early) {
+moe_status decode_ffn(const moe_ffn_args* a, cudaStream_t s, const DecodeFuse& fz) {
   DecodeParams p;
-  p.shared_early = shared_early ? 1 : 0;
+  p.shared_early = fz.shared_early ? 1 : 0;
+  p.comb_ctl = nullptr;
+  p.comb_target = 0;
+  p.inv = fz.inv;
+  p.y = fz.y;
   p.T = a->T; p.H = a->H; p.I = a->I; p.E = a->E; p.k = a->k; p.Is = a->Is;
   p.x = (const uint16_t*)a->x;
   p.arena = cache_arena(a->cache);
@@ -610,6 +663,10 @@ moe_status decode_ffn(const moe_ffn_args* a, cudaStream_t s, bool shared_early) 
     size_t smem = smem_f16(p.maxm, a->I);
     if (shared && smem_f32(p.maxm, a->Is) > smem) smem = smem_f32(p.maxm, a->Is);
     const int grid = p.n_shared_units + routed;
+    if (fz.comb_ctl && fz.inv && fz.y && (!a->Is || a->o_shared)) {
+      p.comb_ctl = fz.comb_ctl;
+      p.comb_target = max_act + (shared ? 4 : 0);  // CTAs per 128-row tile
+    }
     if (grid > 0) {
       if (launch_pdl(p.maxm == 2 ? k_decode_down<2> : k_decode_down<1>, grid, kDecThreads, smem,
                      s, p) != cudaSuccess)

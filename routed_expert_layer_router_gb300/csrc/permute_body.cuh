@@ -1,0 +1,179 @@
+// permute_body.cuh - the body of K-perm (histogram, exclusive scans, stable
+// permutation of the routes by expert, optional cache lookup), shared by the
+// permutation kernel and the few-token router kernel that ends with it.
+#pragma once
+#include "common.cuh"
+
+namespace moe {
+
+constexpr int kPermThreads = 1024;
+constexpr int kPermWarps = kPermThreads / 32;
+
+// outputs of the permutation (see moe_permute) and the optional lookup
+struct PermArgs {
+  int32_t *counts, *offsets, *perm, *inv, *pad_offsets;
+  int pad_align;
+  int32_t* status;
+  LookupArgs lk;
+};
+
+// shared-memory bytes of permute_body for E experts
+__host__ __device__ constexpr size_t permute_smem_bytes(int E) {
+  return sizeof(int) * ((size_t)E * (3 + kPermWarps) + 33);
+}
+
+// block-wide exclusive scan of one int per thread (returns the total)
+__device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int& total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int n = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  if (lane == 31) s_warp[wid] = incl;
+  __syncthreads();
+  if (wid == 0) {
+    int w = (lane < (int)(blockDim.x >> 5)) ? s_warp[lane] : 0;
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int n = __shfl_up_sync(0xFFFFFFFFu, wi, o);
+      if (lane >= o) wi += n;
+    }
+    s_warp[lane] = wi - w;  // exclusive prefix of warp totals
+    if (lane == 31) s_warp[32] = wi;
+  }
+  __syncthreads();
+  int r = s_warp[wid] + incl - v;
+  total = s_warp[32];
+  __syncthreads();
+  return r;
+}
+
+// one expert per thread (E <= 1024 = blockDim); c = routes to expert e
+__device__ __forceinline__ void lookup_body(const LookupArgs& a, int E, int c, int* s_scan, int32_t* status) {
+  const int e = threadIdx.x;
+  bool active = (e < E) && c > 0;
+  int slot = active ? a.table[e] : -1;
+  if (active && slot >= 0 && (slot < a.slot_lo || slot >= a.slot_hi)) {
+    set_status(status, MOE_ERR_DEVICE);  // stale or foreign slot: treat as a miss
+    slot = -1;
+  }
+  bool hit = active && slot >= 0;
+  bool miss = active && slot < 0;
+  int nh, nm;
+  int ph = block_exclusive_scan(hit ? 1 : 0, s_scan, nh);
+  int pm = block_exclusive_scan(miss ? 1 : 0, s_scan, nm);
+  if (e < E) {
+    int s = -1;
+    if (hit) {
+      s = slot;
+      a.act_list[ph] = e;
+    } else if (miss) {
+      a.act_list[nh + pm] = e;
+      a.miss_ids[pm] = e;
+      if (a.n_stage > 0) s = a.n_cache + (pm % a.n_stage);
+      else set_status(status, MOE_ERR_DEVICE);
+    }
+    a.src_slot[e] = s;
+  }
+  if (e == 0) {
+    a.n_act[0] = nh + nm;
+    a.n_act[1] = nh;
+    *a.n_miss = nm;
+  }
+}
+
+// One CTA per 1024-route chunk.  Every CTA histograms all n routes (split into
+// those before its chunk and the rest), so each knows both the global offsets
+// and its chunk's starting rank per expert without any exchange between CTAs;
+// CTA 0 alone writes counts/offsets/pad_offsets and runs the lookup.
+// smem: counts[E] | before[E] | base[E] | wcnt[32][E] | scan scratch[33]
+// `chunk` is the CTA's 1024-route chunk; `sm` holds (3 + 32) * E + 33 ints.
+// ids are read through L2 (ld.global.cg): the caller may have written them
+// in the same kernel.
+__device__ __forceinline__ void permute_body(const int32_t* ids, int n, int E,
+                                             int32_t* __restrict__ counts,
+                                             int32_t* __restrict__ offsets,
+                                             int32_t* __restrict__ perm,
+                                             int32_t* __restrict__ inv,
+                                             int32_t* __restrict__ pad_offsets, int pad_align,
+                                             int32_t* status, const LookupArgs& lk, int* sm,
+                                             int chunk) {
+  int* s_cnt = sm;
+  int* s_pre = s_cnt + E;
+  int* s_base = s_pre + E;
+  int* s_w = s_base + E;  // [32][E]
+  int* s_scan = s_w + kPermWarps * E;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const bool lead = chunk == 0;
+  const int r0 = chunk * kPermThreads;
+
+  for (int e = tid; e < E; e += kPermThreads) {
+    s_cnt[e] = 0;
+    s_pre[e] = 0;
+  }
+  __syncthreads();
+  // routes before this chunk count into s_pre, the rest into s_cnt
+#pragma unroll 4
+  for (int r = tid; r < n; r += kPermThreads) {
+    const int e = __ldcg(ids + r);
+    if (e >= 0 && e < E) atomicAdd(r < r0 ? &s_pre[e] : &s_cnt[e], 1);
+    else if (lead) set_status(status, MOE_ERR_DEVICE);
+  }
+  __syncthreads();
+  // exclusive scans of counts (and of padded counts); E <= 1024 = one per thread
+  const int pre = (tid < E) ? s_pre[tid] : 0;
+  const int c = (tid < E) ? s_cnt[tid] + pre : 0;
+  int tot;
+  const int off = block_exclusive_scan(c, s_scan, tot);
+  if (tid < E) s_base[tid] = off + pre;
+  if (lead) {
+    if (tid < E) {
+      counts[tid] = c;
+      offsets[tid] = off;
+    }
+    if (tid == 0) offsets[E] = tot;
+    if (pad_offsets) {
+      int cp = (tid < E) ? ((c + pad_align - 1) / pad_align) * pad_align : 0;
+      int ptot;
+      int poff = block_exclusive_scan(cp, s_scan, ptot);
+      if (tid < E) pad_offsets[tid] = poff;
+      if (tid == 0) pad_offsets[E] = ptot;
+    }
+    if (lk.table) lookup_body(lk, E, c, s_scan, status);
+  }
+  for (int i = tid; i < kPermWarps * E; i += kPermThreads) s_w[i] = 0;
+  __syncthreads();
+
+  // stable positions of this chunk's routes: rank within the warp from the
+  // match mask, then the per-expert prefix over the warps
+  const int r = r0 + tid;
+  const int e = (r < n) ? __ldcg(ids + r) : -1;
+  const bool ok = (e >= 0 && e < E);
+  const unsigned peers = __match_any_sync(0xFFFFFFFFu, ok ? e : -1);
+  const int rank = __popc(peers & ((1u << lane) - 1u));
+  if (ok && rank == 0) s_w[wid * E + e] = __popc(peers);
+  __syncthreads();
+  for (int x = tid; x < E; x += kPermThreads) {
+    int run = s_base[x];
+#pragma unroll 8
+    for (int w = 0; w < kPermWarps; ++w) {
+      const int cw = s_w[w * E + x];
+      s_w[w * E + x] = run;
+      run += cw;
+    }
+  }
+  __syncthreads();
+  if (ok) {
+    const int p = s_w[wid * E + e] + rank;
+    perm[p] = r;
+    inv[r] = p;
+  } else if (r < n) {
+    inv[r] = -1;
+  }
+}
+
+
+}  // namespace moe

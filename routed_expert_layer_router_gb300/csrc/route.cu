@@ -2,7 +2,7 @@
 // weights.  The router is the device-side router of the "Project Maya" page
 // ("Three tiers and the rules between them"): fp32 router weights, top-8 of
 // 288 experts per token, selection kept on the device.
-#include "common.cuh"
+#include "permute_body.cuh"
 
 namespace moe {
 
@@ -34,7 +34,7 @@ __device__ __forceinline__ void logits_of_expert(const uint16_t* __restrict__ x,
       }
     }
   }
-  __shared__ float red[kGemvMaxT][8];
+  __shared__ float red[kGemvMaxT][32];
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
 #pragma unroll
   for (int t = 0; t < kGemvMaxT; ++t) {
@@ -342,6 +342,33 @@ __global__ void __launch_bounds__(256) k_route_small(const uint16_t* __restrict_
   if (threadIdx.x == 0) *done = 0u;  // ready for the next call
 }
 
+// The same, with the permutation of the routes by expert and the cache
+// lookup (permute_body) run by that last CTA as well: one launch from the
+// token to the FFN's expert list.  1024 threads per CTA.
+__global__ void __launch_bounds__(kPermThreads) k_route_permute_small(
+    const uint16_t* __restrict__ x, const float* __restrict__ wr, const float* __restrict__ bias,
+    int T, int H, int E, int k, float* __restrict__ logits, int32_t* __restrict__ ids,
+    float* __restrict__ w, float* __restrict__ p_sel, unsigned int* __restrict__ done,
+    PermArgs pa) {
+  extern __shared__ float sl[];  // top-k: [8 warps][E] floats; then the permutation's ints
+  __shared__ int s_last;
+  pdl_wait();
+  pdl_launch_dependents();
+  logits_of_expert(x, wr, bias, T, H, E, blockIdx.x, logits);
+  __threadfence();  // this CTA's logits are visible before it is counted
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = atomicAdd(done, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const int wid = threadIdx.x >> 5;
+  if (wid < T) topk_token(logits + (size_t)wid * E, sl + (size_t)wid * E, wid, E, k, ids, w, p_sel);
+  __syncthreads();  // ids written by this CTA: read back through L2 below
+  permute_body(ids, T * k, E, pa.counts, pa.offsets, pa.perm, pa.inv, pa.pad_offsets,
+               pa.pad_align, pa.status, pa.lk, reinterpret_cast<int*>(sl), 0);
+  if (threadIdx.x == 0) *done = 0u;  // ready for the next call
+}
+
 }  // namespace moe
 
 using namespace moe;
@@ -354,11 +381,47 @@ MOE_API size_t moe_route_workspace_bytes(int T, int E) {
   return (T > 0 && E > 0) ? kRouteCtl + (size_t)T * E * sizeof(float) : 0;
 }
 
-MOE_API moe_status moe_route(const moe_route_args* a, void* stream) {
+static moe_status route_check(const moe_route_args* a) {
   if (!a || !a->x || !a->w_router || !a->ids || !a->w) return MOE_ERR_INVALID_ARG;
   if (a->T < 0 || a->H <= 0 || a->E <= 0 || a->k <= 0 || a->k > a->E || a->k > 32)
     return MOE_ERR_INVALID_ARG;
   if (a->H % 256 || a->E > 1024) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+namespace moe {
+// Router, permutation and lookup in one launch for T <= 8 tokens (the layer's
+// decode sequence).  Needs a->workspace (the control area) and a->logits.
+// Returns MOE_ERR_UNSUPPORTED when the shape does not qualify (the caller then
+// runs moe_route and the permutation separately).
+moe_status route_permute_small(const moe_route_args* a, const PermArgs& pa, cudaStream_t s) {
+  moe_status st = route_check(a);
+  if (st != MOE_OK) return st;
+  if (a->T < 1 || a->T > kGemvMaxT || !a->logits || !a->workspace ||
+      a->workspace_bytes < kRouteCtl)
+    return MOE_ERR_UNSUPPORTED;
+  if (!pa.counts || !pa.offsets || !pa.perm || !pa.inv || (pa.pad_offsets && pa.pad_align <= 0))
+    return MOE_ERR_INVALID_ARG;
+  size_t smem = (size_t)8 * a->E * sizeof(float);
+  if (permute_smem_bytes(a->E) > smem) smem = permute_smem_bytes(a->E);
+  static bool attr = false;
+  if (smem > 48 * 1024 && !attr) {
+    if (cudaFuncSetAttribute(k_route_permute_small, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)permute_smem_bytes(1024)) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    attr = true;
+  }
+  if (launch_pdl(k_route_permute_small, a->E, kPermThreads, smem, s, (const uint16_t*)a->x,
+                 a->w_router, a->bias, a->T, a->H, a->E, a->k, a->logits, a->ids, a->w, a->p_sel,
+                 (unsigned int*)a->workspace, pa) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+}  // namespace moe
+
+MOE_API moe_status moe_route(const moe_route_args* a, void* stream) {
+  moe_status st0 = route_check(a);
+  if (st0 != MOE_OK) return st0;
   if (a->T == 0) return MOE_OK;
   float* logits = a->logits;
   if (!logits) {
