@@ -28,7 +28,8 @@ moe_status launch_permute(const int32_t* ids, int T, int k, int E, int32_t* coun
                           int pad_align, int32_t* status, const LookupArgs& lk, cudaStream_t s);
 void cache_lookup_args(const expcache* c, int layer, int32_t* src_slot, int32_t* act_list,
                        int32_t* n_act, int32_t* miss_ids, int32_t* n_miss, LookupArgs* out);
-moe_status route_permute_small(const moe_route_args* a, const PermArgs& pa, cudaStream_t s);
+moe_status route_permute_small(const moe_route_args* a, const PermArgs& pa,
+                               const SharedGuArgs& sg, cudaStream_t s);
 }  // namespace moe
 
 namespace moe {
@@ -112,7 +113,7 @@ static moe_status expert_ffn(const moe_ffn_args* a, void* stream, const DecodeFu
 }
 
 MOE_API moe_status moe_expert_ffn(const moe_ffn_args* a, void* stream) {
-  const DecodeFuse none = {false, nullptr, nullptr, nullptr};
+  const DecodeFuse none = {false, false, nullptr, nullptr, nullptr};
   return expert_ffn(a, stream, none);
 }
 
@@ -251,7 +252,17 @@ MOE_API moe_status moe_layer_forward(moe_layer* l, const void* x, int T, void* y
   pa.counts = l->counts; pa.offsets = l->offsets; pa.perm = l->perm; pa.inv = l->inv;
   pa.pad_offsets = prefill ? l->pad_offsets : nullptr; pa.pad_align = 128;
   pa.status = l->status; pa.lk = lk;
-  st = route_permute_small(&ra, pa, s);
+  // one decode token: the shared expert's gate/up runs beside the router,
+  // into the FFN workspace's h_shared (after the routes' h)
+  SharedGuArgs sg = {nullptr, nullptr, 0, nullptr};
+  if (!prefill && T == 1 && d.Is > 0) {
+    sg.s_gate = (const uint16_t*)d.s_gate;
+    sg.s_up = (const uint16_t*)d.s_up;
+    sg.Is = d.Is;
+    sg.h_shared = (float*)l->ffn_ws + (size_t)T * d.k * d.I;
+  }
+  st = route_permute_small(&ra, pa, sg, s);
+  const bool shared_gu_done = st == MOE_OK && sg.Is > 0;
   if (st == MOE_ERR_UNSUPPORTED) {
     if ((st = moe_route(&ra, stream)) != MOE_OK) return st;
     st = launch_permute(l->ids, T, d.k, d.E, l->counts, l->offsets, l->perm, l->inv,
@@ -292,7 +303,7 @@ MOE_API moe_status moe_layer_forward(moe_layer* l, const void* x, int T, void* y
     fa.group = g;
     // the kernel before this call is the permutation or the gather; a single
     // decode group's down kernel also writes y (no separate combine)
-    DecodeFuse fz = {true, nullptr, nullptr, nullptr};
+    DecodeFuse fz = {true, shared_gu_done && g == 0, nullptr, nullptr, nullptr};
     if (!prefill && groups == 1) {
       fz.comb_ctl = (unsigned int*)((char*)l->route_ctl + kRouteCtlBytes);
       fz.inv = l->inv;

@@ -128,6 +128,7 @@ bool pdl_enabled();  // on unless the environment sets MOE_PDL=0
 // launch is the last FFN launch of the forward).
 struct DecodeFuse {
   bool shared_early;
+  bool shared_gu_done;  // the shared expert's h is already in the workspace (one token)
   unsigned int* comb_ctl;
   const int32_t* inv;
   uint16_t* y;

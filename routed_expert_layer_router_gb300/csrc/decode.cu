@@ -645,7 +645,7 @@ moe_status decode_ffn(const moe_ffn_args* a, cudaStream_t s, const DecodeFuse& f
   if (a->group > 0) max_act = a->n_stage < max_act ? a->n_stage : max_act;
   const bool shared = a->group == 0 && a->Is > 0;
   if (a->stages & MOE_STAGE_GATE_UP) {
-    p.n_shared_units = shared ? a->Is / 4 : 0;
+    p.n_shared_units = (shared && !fz.shared_gu_done) ? a->Is / 4 : 0;
     const int routed = max_act * (a->I / 128) * 4;
     p.n_routed_units = routed;
     size_t smem = smem_f16(p.maxm, a->H);

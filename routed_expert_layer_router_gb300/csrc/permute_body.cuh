@@ -17,6 +17,14 @@ struct PermArgs {
   LookupArgs lk;
 };
 
+// the bf16 shared expert's gate/up for one token, run beside the router
+// (Is == 0: none): h_shared[i] = silu(gate_i . x) * (up_i . x)
+struct SharedGuArgs {
+  const uint16_t *s_gate, *s_up;  // [Is][H]
+  int Is;
+  float* h_shared;  // [Is]
+};
+
 // shared-memory bytes of permute_body for E experts
 __host__ __device__ constexpr size_t permute_smem_bytes(int E) {
   return sizeof(int) * ((size_t)E * (3 + kPermWarps) + 33);

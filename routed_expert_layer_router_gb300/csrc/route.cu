@@ -342,22 +342,99 @@ __global__ void __launch_bounds__(256) k_route_small(const uint16_t* __restrict_
   if (threadIdx.x == 0) *done = 0u;  // ready for the next call
 }
 
+// One token's shared-expert gate/up by one CTA of 1024 threads: 8 row pairs
+// (gate row i, up row i), each split over 4 warps by quarters of H, 8 bf16 per
+// lane and load, two loads of each row in flight (two CTAs of 1024 threads fit
+// an SM at 32 registers); x is staged once in fp32.  The quarters' sums are
+// added in a fixed order.
+constexpr int kShSplit = 4, kShRows = (kPermThreads / 32) / kShSplit;
+__device__ void shared_gu_cta(const uint16_t* __restrict__ x, int H, const SharedGuArgs& sg,
+                              int cta, float* xs) {
+  __shared__ float red[kPermThreads / 32][2];
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  for (int i = threadIdx.x; i < H / 2; i += blockDim.x) {
+    const uint32_t v = __ldg(reinterpret_cast<const uint32_t*>(x) + i);
+    xs[2 * i] = bf16_lo(v);
+    xs[2 * i + 1] = bf16_hi(v);
+  }
+  __syncthreads();
+  const int i = cta * kShRows + wid / kShSplit, qt = wid % kShSplit;
+  float ag = 0.f, au = 0.f;
+  if (i < sg.Is) {
+    const int np = H / 8, nq = np / kShSplit;  // 16-byte pieces per row, per quarter
+    const uint4* g = reinterpret_cast<const uint4*>(sg.s_gate + (size_t)i * H) + qt * nq;
+    const uint4* u = reinterpret_cast<const uint4*>(sg.s_up + (size_t)i * H) + qt * nq;
+    const float* xq = xs + qt * nq * 8;
+    for (int p0 = lane; p0 < nq; p0 += 2 * 32) {
+      uint4 gv[2], uv[2];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int pp = p0 + 32 * j;
+        gv[j] = pp < nq ? ldg_stream(g + pp) : make_uint4(0u, 0u, 0u, 0u);
+        uv[j] = pp < nq ? ldg_stream(u + pp) : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int pp = p0 + 32 * j;
+        if (pp >= nq) break;
+        const float4 x0 = *reinterpret_cast<const float4*>(xq + pp * 8);
+        const float4 x1 = *reinterpret_cast<const float4*>(xq + pp * 8 + 4);
+        const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+        const uint32_t gw[4] = {gv[j].x, gv[j].y, gv[j].z, gv[j].w};
+        const uint32_t uw[4] = {uv[j].x, uv[j].y, uv[j].z, uv[j].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          ag = fmaf(bf16_lo(gw[q]), xv[2 * q], ag);
+          ag = fmaf(bf16_hi(gw[q]), xv[2 * q + 1], ag);
+          au = fmaf(bf16_lo(uw[q]), xv[2 * q], au);
+          au = fmaf(bf16_hi(uw[q]), xv[2 * q + 1], au);
+        }
+      }
+    }
+  }
+  ag = warp_sum(ag);
+  au = warp_sum(au);
+  if (lane == 0) {
+    red[wid][0] = ag;
+    red[wid][1] = au;
+  }
+  __syncthreads();
+  if (threadIdx.x < kShRows) {
+    const int r = cta * kShRows + threadIdx.x;
+    if (r < sg.Is) {
+      float g = 0.f, uu = 0.f;
+#pragma unroll
+      for (int q = 0; q < kShSplit; ++q) {
+        g += red[threadIdx.x * kShSplit + q][0];
+        uu += red[threadIdx.x * kShSplit + q][1];
+      }
+      sg.h_shared[r] = g / (1.f + expf(-g)) * uu;
+    }
+  }
+}
+
 // The same, with the permutation of the routes by expert and the cache
 // lookup (permute_body) run by that last CTA as well: one launch from the
-// token to the FFN's expert list.  1024 threads per CTA.
-__global__ void __launch_bounds__(kPermThreads) k_route_permute_small(
+// token to the FFN's expert list.  1024 threads per CTA.  CTAs E.. run the
+// shared expert's gate/up for one token (sg.Is > 0): HBM work that needs no
+// routing, streaming while the last router CTA selects and permutes.
+__global__ void __launch_bounds__(kPermThreads, 2) k_route_permute_small(
     const uint16_t* __restrict__ x, const float* __restrict__ wr, const float* __restrict__ bias,
     int T, int H, int E, int k, float* __restrict__ logits, int32_t* __restrict__ ids,
     float* __restrict__ w, float* __restrict__ p_sel, unsigned int* __restrict__ done,
-    PermArgs pa) {
+    PermArgs pa, SharedGuArgs sg) {
   extern __shared__ float sl[];  // top-k: [8 warps][E] floats; then the permutation's ints
   __shared__ int s_last;
   pdl_wait();
   pdl_launch_dependents();
+  if ((int)blockIdx.x >= E) {
+    shared_gu_cta(x, H, sg, blockIdx.x - E, sl);
+    return;
+  }
   logits_of_expert(x, wr, bias, T, H, E, blockIdx.x, logits);
   __threadfence();  // this CTA's logits are visible before it is counted
   __syncthreads();
-  if (threadIdx.x == 0) s_last = atomicAdd(done, 1u) == gridDim.x - 1;
+  if (threadIdx.x == 0) s_last = atomicAdd(done, 1u) == (unsigned)E - 1;
   __syncthreads();
   if (!s_last) return;
   __threadfence();
@@ -394,7 +471,8 @@ namespace moe {
 // decode sequence).  Needs a->workspace (the control area) and a->logits.
 // Returns MOE_ERR_UNSUPPORTED when the shape does not qualify (the caller then
 // runs moe_route and the permutation separately).
-moe_status route_permute_small(const moe_route_args* a, const PermArgs& pa, cudaStream_t s) {
+moe_status route_permute_small(const moe_route_args* a, const PermArgs& pa,
+                               const SharedGuArgs& sg, cudaStream_t s) {
   moe_status st = route_check(a);
   if (st != MOE_OK) return st;
   if (a->T < 1 || a->T > kGemvMaxT || !a->logits || !a->workspace ||
@@ -402,18 +480,25 @@ moe_status route_permute_small(const moe_route_args* a, const PermArgs& pa, cuda
     return MOE_ERR_UNSUPPORTED;
   if (!pa.counts || !pa.offsets || !pa.perm || !pa.inv || (pa.pad_offsets && pa.pad_align <= 0))
     return MOE_ERR_INVALID_ARG;
+  if (sg.Is > 0 && (a->T != 1 || !sg.s_gate || !sg.s_up || !sg.h_shared))
+    return MOE_ERR_INVALID_ARG;
   size_t smem = (size_t)8 * a->E * sizeof(float);
   if (permute_smem_bytes(a->E) > smem) smem = permute_smem_bytes(a->E);
+  if (sg.Is > 0 && (size_t)a->H * sizeof(float) > smem) smem = (size_t)a->H * sizeof(float);
   static bool attr = false;
   if (smem > 48 * 1024 && !attr) {
     if (cudaFuncSetAttribute(k_route_permute_small, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)permute_smem_bytes(1024)) != cudaSuccess)
+                             (int)(64 * 1024 > permute_smem_bytes(1024)
+                                       ? 64 * 1024 : permute_smem_bytes(1024))) != cudaSuccess)
       return MOE_ERR_CUDA;
     attr = true;
   }
-  if (launch_pdl(k_route_permute_small, a->E, kPermThreads, smem, s, (const uint16_t*)a->x,
-                 a->w_router, a->bias, a->T, a->H, a->E, a->k, a->logits, a->ids, a->w, a->p_sel,
-                 (unsigned int*)a->workspace, pa) != cudaSuccess)
+  if (smem > 64 * 1024 && smem > permute_smem_bytes(1024)) return MOE_ERR_UNSUPPORTED;
+  if (sg.Is > 0 && (a->H / 8) % kShSplit) return MOE_ERR_UNSUPPORTED;
+  const int sh_ctas = sg.Is > 0 ? (sg.Is + kShRows - 1) / kShRows : 0;
+  if (launch_pdl(k_route_permute_small, a->E + sh_ctas, kPermThreads, smem, s,
+                 (const uint16_t*)a->x, a->w_router, a->bias, a->T, a->H, a->E, a->k, a->logits,
+                 a->ids, a->w, a->p_sel, (unsigned int*)a->workspace, pa, sg) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
 }
