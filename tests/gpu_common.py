@@ -89,6 +89,19 @@ def check_outputs(y_gpu: np.ndarray, y_ref: np.ndarray, tol: float = TOL, bound=
     return err / rms
 
 
+def check_permutation(dbg: dict, ids_ref):
+    """The layer's permutation and lookup against their definitions: perm is
+    the stable sort of the routes by expert; every selected expert is active
+    (hits counted among them) and has a cache or staging slot."""
+    flat = np.asarray(ids_ref).ravel()
+    perm = dbg["perm"].cpu().numpy()
+    assert np.array_equal(perm, np.argsort(flat, kind="stable")), (perm, flat)
+    n_act = dbg["n_act"].cpu().numpy()
+    assert n_act[0] == len(np.unique(flat)) and 0 <= n_act[1] <= n_act[0], n_act
+    src = dbg["src_slot"].cpu().numpy()
+    assert np.all(src[np.unique(flat)] >= 0), src
+
+
 def check_router(dbg: dict, ids_ref, w_ref, p_ref):
     ids = dbg["ids"].cpu().numpy()
     assert np.array_equal(ids, ids_ref), f"ids differ:\n{ids}\nvs\n{ids_ref}"

@@ -8,8 +8,8 @@ import torch
 
 import gen
 import oracle
-from tests.gpu_common import (check_outputs, check_router, draw_tokens, host_inputs,
-                              oracle_layer, to_dev_bf16, y_to_f64)
+from tests.gpu_common import (check_outputs, check_permutation, check_router, draw_tokens,
+                              host_inputs, oracle_layer, to_dev_bf16, y_to_f64)
 from tests.helpers import TOL, identity_record, identity_x, bf16_to_f64
 
 pytestmark = pytest.mark.gpu
@@ -46,6 +46,7 @@ def test_tiny_layer_parity(tiny, T):
     y = _run(dw, 0, x)
     y_ref, ids_r, w_r, p_r = oracle_layer(dw, 0, x)
     check_router(dw.moe_layers[0].debug(T), ids_r, w_r, p_r)
+    check_permutation(dw.moe_layers[0].debug(T), ids_r)  # T <= 8: inside the router kernel
     check_outputs(y, y_ref)
     assert dw.moe_layers[0].read_status() == 0
 
@@ -67,11 +68,13 @@ def test_decode_layer_parity(decode):
         y = _run(dw, 0, x[t:t + 1])
         y_ref, ids_r, w_r, p_r = oracle_layer(dw, 0, x[t:t + 1], record_cache=recs)
         check_router(dw.moe_layers[0].debug(1), ids_r, w_r, p_r)
+        check_permutation(dw.moe_layers[0].debug(1), ids_r)
         check_outputs(y, y_ref)
     # a few tokens per forward as well (two-token staging path)
     y = _run(dw, 0, x)
     y_ref, ids_r, w_r, p_r = oracle_layer(dw, 0, x, record_cache=recs)
     check_router(dw.moe_layers[0].debug(3), ids_r, w_r, p_r)
+    check_permutation(dw.moe_layers[0].debug(3), ids_r)
     check_outputs(y, y_ref)
     assert dw.moe_layers[0].read_status() == 0
 
