@@ -44,6 +44,9 @@ struct DecodeParams {
   int group, n_stage;
   int n_shared_units;  // shared-expert grid units (down: leading; gate/up: trailing)
   int n_routed_units;  // gate/up: leading routed grid units
+  // gate/up: shared-expert down units after the routed ones (one token, when
+  // h_shared is already in the workspace: the down kernel then has none)
+  int n_sdown_units;
   const uint16_t* s_gate;
   const uint16_t* s_up;
   const uint16_t* s_down;
@@ -300,6 +303,24 @@ __device__ void warp_rows_bf16(const uint16_t* const* rows, int K, int k0, int k
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.f + expf(-g)); }
 
+// shared expert down: warp = 4 rows of s_down (r0..r0+3) over all of Is
+template <int M>
+__device__ void down_shared_pass(const DecodeParams& p, int r0, int t0, int mm, const float* hs) {
+  const uint16_t* rows[4];
+#pragma unroll
+  for (int r = 0; r < 4; ++r) rows[r] = p.s_down + (size_t)(r0 + r) * p.Is;
+  float acc[4][M];
+  warp_rows_bf16<M, 4>(rows, p.Is, 0, p.Is, hs, acc);
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int j = 0; j < M; ++j) {
+      const float v = warp_sum(acc[r][j]);
+      if (lane == r * M + j && j < mm) p.o_shared[(size_t)(t0 + j) * p.H + r0 + r] = v;
+    }
+}
+
 // ---- K-decode-gu -------------------------------------------------------------
 template <int M>
 __device__ void gu_routed_pass(const DecodeParams& p, const RecordLayout& L, const uint8_t* rec,
@@ -365,6 +386,19 @@ __global__ void __launch_bounds__(kDecThreads) k_decode_gu(DecodeParams p) {
   __shared__ float red[kDecWarps * 8 * 2];
   const int wid = threadIdx.x >> 5;
   const int u = blockIdx.x;
+  if (u >= p.n_routed_units && p.n_sdown_units > 0) {
+    // shared down: h_shared was written by the kernel before this one
+    pdl_wait();
+    pdl_launch_dependents();
+    float* hs = reinterpret_cast<float*>(smem_raw);
+    const int r0 = (u - p.n_routed_units) * (kDecWarps * 4) + wid * 4;
+    const float* row = p.h_shared;
+    __syncthreads();
+    stage_f32_to_f32(hs, &row, 1, p.Is);
+    __syncthreads();
+    if (r0 < p.H) down_shared_pass<1>(p, r0, 0, 1, hs);
+    return;
+  }
   if (u >= p.n_routed_units) {
     // the shared expert reads only x and its weights: in the layer's own
     // sequence it runs without waiting for the routing
@@ -466,23 +500,6 @@ __device__ void down_routed_pass(const DecodeParams& p, const RecordLayout& L, c
           p.o_route[(size_t)(q0 + j) * p.H + rt * 128 + wid + 8 * g + 32 * m1] = p.w[r] * gd * v;
         }
       }
-}
-
-template <int M>
-__device__ void down_shared_pass(const DecodeParams& p, int r0, int t0, int mm, const float* hs) {
-  const uint16_t* rows[4];
-#pragma unroll
-  for (int r = 0; r < 4; ++r) rows[r] = p.s_down + (size_t)(r0 + r) * p.Is;
-  float acc[4][M];
-  warp_rows_bf16<M, 4>(rows, p.Is, 0, p.Is, hs, acc);
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int r = 0; r < 4; ++r)
-#pragma unroll
-    for (int j = 0; j < M; ++j) {
-      const float v = warp_sum(acc[r][j]);
-      if (lane == r * M + j && j < mm) p.o_shared[(size_t)(t0 + j) * p.H + r0 + r] = v;
-    }
 }
 
 // y[t] for the columns of tile rt, summed in K-combine's order (routes j <
@@ -629,6 +646,7 @@ moe_status decode_ffn(const moe_ffn_args* a, cudaStream_t s, const DecodeFuse& f
   p.n_slots = cache_n_cache(a->cache) + cache_n_stage(a->cache);
   p.gscale = a->gscale; p.src_slot = a->src_slot; p.act_list = a->act_list; p.n_act = a->n_act;
   p.offsets = a->offsets; p.perm = a->perm; p.w = a->w;
+  p.n_sdown_units = 0;
   p.group = a->group;
   p.n_stage = a->n_stage;
   p.s_gate = (const uint16_t*)a->s_gate; p.s_up = (const uint16_t*)a->s_up;
@@ -643,14 +661,17 @@ moe_status decode_ffn(const moe_ffn_args* a, cudaStream_t s, const DecodeFuse& f
   // experts this group can hold at most
   int max_act = a->T * a->k < a->E ? a->T * a->k : a->E;
   if (a->group > 0) max_act = a->n_stage < max_act ? a->n_stage : max_act;
-  const bool shared = a->group == 0 && a->Is > 0;
+  bool shared = a->group == 0 && a->Is > 0;
   if (a->stages & MOE_STAGE_GATE_UP) {
     p.n_shared_units = (shared && !fz.shared_gu_done) ? a->Is / 4 : 0;
+    p.n_sdown_units = (shared && fz.shared_gu_done && a->T == 1 && (a->stages & MOE_STAGE_DOWN))
+                          ? (a->H + kDecWarps * 4 - 1) / (kDecWarps * 4) : 0;
     const int routed = max_act * (a->I / 128) * 4;
     p.n_routed_units = routed;
     size_t smem = smem_f16(p.maxm, a->H);
-    if (shared && smem_f32(p.maxm, a->H) > smem) smem = smem_f32(p.maxm, a->H);
-    const int grid = p.n_shared_units + routed;
+    if (p.n_shared_units && smem_f32(p.maxm, a->H) > smem) smem = smem_f32(p.maxm, a->H);
+    if (p.n_sdown_units && smem_f32(1, a->Is) > smem) smem = smem_f32(1, a->Is);
+    const int grid = p.n_shared_units + p.n_sdown_units + routed;
     if (grid > 0) {
       if (launch_pdl(p.maxm == 2 ? k_decode_gu<2> : k_decode_gu<1>, grid, kDecThreads, smem, s,
                      p) != cudaSuccess)
@@ -658,6 +679,8 @@ moe_status decode_ffn(const moe_ffn_args* a, cudaStream_t s, const DecodeFuse& f
     }
   }
   if (a->stages & MOE_STAGE_DOWN) {
+    const bool sdown_done = p.n_sdown_units > 0;  // in the gate/up kernel above
+    if (sdown_done) shared = false;
     p.n_shared_units = shared ? (a->H + kDecWarps * 4 - 1) / (kDecWarps * 4) : 0;
     const int routed = max_act * (a->H / 128);
     size_t smem = smem_f16(p.maxm, a->I);
