@@ -45,7 +45,7 @@ FP4_OVER_BF16 = 6.0  # nominal dense FP4 / dense bf16 tensor throughput (13.5 / 
 # DRAM bytes (read + write) of one k_decode_gu launch on the full decode layer, from
 # one ncu capture of the current kernel (profiles/k_decode_gu_decode-layer.md); set to
 # None whenever the kernel changes until it is captured again
-GU_TRAFFIC = 163_920_128
+GU_TRAFFIC = None
 GU_TRAFFIC_SOURCE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum, full decode layer, "
                      "profiles/k_decode_gu_decode-layer.md")
 
@@ -319,18 +319,26 @@ def bench_decode(args, torch, moe, gen, gd, dev, rank, world, local_rank, peaks)
     del graphs
     assert layer.read_status() == 0, "device status set during the bench"
 
-    # ---- pass 2: events around the two expert-FFN launches (individual ABI calls)
-    ex.step(xs[0].data_ptr(), ys[0].data_ptr(), sp)
-    kev = [(_events(torch, 1)[0], torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
+    # ---- pass 2: events at the layer's own launch boundaries (its timing hook),
+    # eager launches, one step at a time: router kernel (with the permutation,
+    # lookup and the shared expert's gate/up), gate/up kernel (routed, with the
+    # shared expert's down), down kernel (routed, with the combine)
+    hev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    for e in hev:  # torch creates the CUDA event on its first record
+        e.record(stream)
+    torch.cuda.synchronize()
+    moe.moe_layer_set_timing(layer.handle, [e.cuda_event for e in hev])
+    k_ms = [[], [], []]
     for j in range(args.steps):
         flush()
-        ex.step(xs[args.warmup + j].data_ptr(), ys[args.warmup + j].data_ptr(), sp,
-                ev_gu=kev[j][0], ev_dn=kev[j][1])
-    torch.cuda.synchronize()
-    gu_ms = statistics.mean(e[0][0].elapsed_time(e[0][1]) for e in kev)
-    dn_ms = statistics.mean(e[0][1].elapsed_time(e[1]) for e in kev)
-    assert int(ex.b["status"].item()) == 0, "device status set during the bench"
+        layer.forward(xs[args.warmup + j:args.warmup + j + 1],
+                      ys[args.warmup + j:args.warmup + j + 1], stream=stream)
+        hev[3].synchronize()
+        for i in range(3):
+            k_ms[i].append(hev[i].elapsed_time(hev[i + 1]))
+    moe.moe_layer_set_timing(layer.handle, [])
+    rt_ms, gu_ms, dn_ms = (statistics.mean(v) for v in k_ms)
+    assert layer.read_status() == 0, "device status set during the bench"
 
     # ---- e2e: the public call with host buffers
     xh = torch.empty((n_steps, H), dtype=torch.bfloat16, pin_memory=True)
@@ -363,11 +371,14 @@ def bench_decode(args, torch, moe, gen, gd, dev, rank, world, local_rank, peaks)
         torch.distributed.all_reduce(tot, op=torch.distributed.ReduceOp.MAX)
     total_ms = float(tot.item())
     rb = gen.record_bytes(H, I)
-    gu_bytes = (k * (2 * I * H // 2 + 2 * I * H // 16) + 2 * Is * H * 2 + T * H * 2
-                + (T * k * I + T * Is) * 4)
-    dn_bytes = (k * (H * I // 2 + H * I // 16) + H * Is * 2 + (T * k * I + T * Is) * 4
-                + (T * k + T) * H * 4)
+    # algorithmic bytes of the three kernels of the one-token sequence
+    rt_bytes = E * H * 4 + 2 * Is * H * 2 + T * H * 2 + T * Is * 4 + T * E * 4
+    gu_bytes = (k * (2 * I * H // 2 + 2 * I * H // 16) + H * Is * 2 + T * H * 2
+                + T * k * I * 4 + T * Is * 4 + T * H * 4)
+    dn_bytes = (k * (H * I // 2 + H * I // 16) + T * k * I * 4 + (T * k + T) * H * 4 * 2
+                + T * H * 2)
     step_bytes = k * rb + 3 * Is * H * 2 + E * H * 4 + 2 * T * H * 2
+    rt_gbs = rt_bytes / (rt_ms * 1e-3) / 1e9
     gu_gbs = gu_bytes / (gu_ms * 1e-3) / 1e9
     dn_gbs = dn_bytes / (dn_ms * 1e-3) / 1e9
     hbm = peaks["hbm_gbs"]
@@ -375,17 +386,23 @@ def bench_decode(args, torch, moe, gen, gd, dev, rank, world, local_rank, peaks)
         "value": round(world * args.steps * T / (total_ms * 1e-3), 2),
         "ms_per_step": round(total_ms / args.steps, 5),
         "roofline": {"bound": "hbm",
-                     "kernel": "k_decode_gu (routed NVFP4 gate/up of the 8 experts + shared "
-                               "bf16 gate/up, SiLU*mul)",
+                     "kernel": "k_decode_gu as the layer launches it for one token (routed "
+                               "NVFP4 gate/up of the 8 experts, SiLU*mul, + the bf16 shared "
+                               "expert's down)",
                      "achieved": round(gu_gbs, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(gu_gbs / hbm, 4), "traffic": GU_TRAFFIC,
                      "traffic_source": GU_TRAFFIC_SOURCE,
                      "bytes_per_launch": gu_bytes, "avg_launch_ms": round(gu_ms, 5)},
         "kernels": {
+            "k_route_permute_small": {"ms": round(rt_ms, 5), "GB/s": round(rt_gbs, 1),
+                                      "frac_hbm": round(rt_gbs / hbm, 4),
+                                      "bytes": rt_bytes},
             "k_decode_gu": {"ms": round(gu_ms, 5), "GB/s": round(gu_gbs, 1),
-                            "frac_hbm": round(gu_gbs / hbm, 4)},
+                            "frac_hbm": round(gu_gbs / hbm, 4), "bytes": gu_bytes},
             "k_decode_down": {"ms": round(dn_ms, 5), "GB/s": round(dn_gbs, 1),
-                              "frac_hbm": round(dn_gbs / hbm, 4)},
+                              "frac_hbm": round(dn_gbs / hbm, 4), "bytes": dn_bytes},
+            "timing": "the layer's timing hook: events at its launch boundaries, eager "
+                      "launches, L2 flushed before each step",
             "step_bytes": step_bytes,
             "step_frac_hbm": round(step_bytes / (total_ms / args.steps * 1e-3) / 1e9 / hbm, 4)},
         "e2e": {"value": round(e2e_steps / (sum(e2e_ms) * 1e-3), 2), "unit": UNIT,

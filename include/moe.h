@@ -352,6 +352,16 @@ moe_status moe_layer_forward(moe_layer* l, const void* x, int T, void* y, void* 
 moe_status moe_layer_debug_ptrs(const moe_layer* l, const int32_t** ids, const float** w,
                                 const float** p_sel, const int32_t** perm,
                                 const int32_t** src_slot, const int32_t** n_act);
+/* Timing hook (the pages have no counterpart; it serves measurement):
+ * events[0..n) are cudaEvent_t handles owned by the caller.  While set, every
+ * moe_layer_forward records events[0] before its first kernel and events[i]
+ * (i < n) after its i-th launch step: the router (with the permutation and
+ * lookup when they share its kernel: up to 8 tokens), the permutation, each
+ * gather, then the gate/up and the down kernel (decode) or the whole FFN
+ * (prefill), then the combine (when it is a kernel of its own).  So the caller
+ * can time each kernel of the layer's own sequence.
+ * n = 0 clears the hook.  n > 16 is MOE_ERR_INVALID_ARG. */
+moe_status moe_layer_set_timing(moe_layer* l, void* const* events, int n);
 /* Synchronises `stream`, returns the layer's sticky device status in
  * *status_out and clears it. */
 moe_status moe_read_device_status(moe_layer* l, void* stream, int32_t* status_out);

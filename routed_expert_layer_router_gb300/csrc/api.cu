@@ -113,7 +113,7 @@ static moe_status expert_ffn(const moe_ffn_args* a, void* stream, const DecodeFu
 }
 
 MOE_API moe_status moe_expert_ffn(const moe_ffn_args* a, void* stream) {
-  const DecodeFuse none = {false, false, nullptr, nullptr, nullptr};
+  const DecodeFuse none = {nullptr, nullptr, false, false, nullptr, nullptr, nullptr};
   return expert_ffn(a, stream, none);
 }
 
@@ -131,6 +131,10 @@ struct moe_layer {
   void* ffn_ws;
   size_t ffn_ws_bytes;
   int last_T;
+  // timing hook: events recorded at the forward's launch boundaries
+  cudaEvent_t ev[16];
+  int n_ev, ev_i;
+  cudaStream_t ev_stream;
 };
 
 static size_t align256(size_t b) { return (b + 255) & ~(size_t)255; }
@@ -228,6 +232,12 @@ MOE_API moe_status moe_layer_destroy(moe_layer* l) {
   return MOE_OK;
 }
 
+// the timing hook: record the next event, if any, on the forward's stream
+static void layer_mark(moe_layer* l) {
+  if (l->ev_i < l->n_ev) cudaEventRecord(l->ev[l->ev_i++], l->ev_stream);
+}
+static void layer_mark_cb(void* ctx) { layer_mark((moe_layer*)ctx); }
+
 MOE_API moe_status moe_layer_forward(moe_layer* l, const void* x, int T, void* y, void* stream) {
   if (!l || !x || !y || T < 0 || T > l->d.T_max) return MOE_ERR_INVALID_ARG;
   if (T == 0) return MOE_OK;
@@ -235,6 +245,9 @@ MOE_API moe_status moe_layer_forward(moe_layer* l, const void* x, int T, void* y
   cudaStream_t s = (cudaStream_t)stream;
   const bool prefill = d.prefill_min_tokens > 0 && T >= d.prefill_min_tokens;
   moe_status st;
+  l->ev_i = 0;
+  l->ev_stream = s;
+  layer_mark(l);
 
   moe_route_args ra;
   memset(&ra, 0, sizeof(ra));
@@ -265,10 +278,12 @@ MOE_API moe_status moe_layer_forward(moe_layer* l, const void* x, int T, void* y
   const bool shared_gu_done = st == MOE_OK && sg.Is > 0;
   if (st == MOE_ERR_UNSUPPORTED) {
     if ((st = moe_route(&ra, stream)) != MOE_OK) return st;
+    layer_mark(l);
     st = launch_permute(l->ids, T, d.k, d.E, l->counts, l->offsets, l->perm, l->inv,
                         pa.pad_offsets, 128, l->status, lk, s);
   }
   if (st != MOE_OK) return st;
+  layer_mark(l);
 
   const int n_stage = cache_n_stage(d.cache);
   const int max_miss = T * d.k < d.E ? T * d.k : d.E;
@@ -299,17 +314,19 @@ MOE_API moe_status moe_layer_forward(moe_layer* l, const void* x, int T, void* y
       if ((st = expcache_fill(d.cache, d.layer, l->miss_ids, l->n_miss, g * S, cnt, nullptr,
                               l->status, stream)) != MOE_OK)
         return st;
+      layer_mark(l);
     }
     fa.group = g;
     // the kernel before this call is the permutation or the gather; a single
     // decode group's down kernel also writes y (no separate combine)
-    DecodeFuse fz = {true, shared_gu_done && g == 0, nullptr, nullptr, nullptr};
+    DecodeFuse fz = {layer_mark_cb, l, true, shared_gu_done && g == 0, nullptr, nullptr, nullptr};
     if (!prefill && groups == 1) {
       fz.comb_ctl = (unsigned int*)((char*)l->route_ctl + kRouteCtlBytes);
       fz.inv = l->inv;
       fz.y = (uint16_t*)y;
     }
     if ((st = expert_ffn(&fa, stream, fz)) != MOE_OK) return st;
+    if (prefill) layer_mark(l);  // the prefill FFN: one step
   }
   if (!prefill && groups == 1) {
     l->last_T = T;
@@ -325,6 +342,7 @@ MOE_API moe_status moe_layer_forward(moe_layer* l, const void* x, int T, void* y
   ca.o_shared = (d.Is > 0 && !prefill) ? l->o_shared : nullptr;  // prefill adds it into y_acc
   ca.y = y;
   if ((st = moe_combine(&ca, stream)) != MOE_OK) return st;
+  layer_mark(l);
   l->last_T = T;
   return MOE_OK;
 }
@@ -339,6 +357,13 @@ MOE_API moe_status moe_layer_debug_ptrs(const moe_layer* l, const int32_t** ids,
   if (perm) *perm = l->perm;
   if (src_slot) *src_slot = l->src_slot;
   if (n_act) *n_act = l->n_act;
+  return MOE_OK;
+}
+
+MOE_API moe_status moe_layer_set_timing(moe_layer* l, void* const* events, int n) {
+  if (!l || n < 0 || n > 16 || (n > 0 && !events)) return MOE_ERR_INVALID_ARG;
+  for (int i = 0; i < n; ++i) l->ev[i] = (cudaEvent_t)events[i];
+  l->n_ev = n;
   return MOE_OK;
 }
 

@@ -127,6 +127,8 @@ bool pdl_enabled();  // on unless the environment sets MOE_PDL=0
 // the down kernel (comb_ctl: H/128 zeroed tile counters; only when that
 // launch is the last FFN launch of the forward).
 struct DecodeFuse {
+  void (*mark)(void*);  // called after each kernel launch (timing hook), or nullptr
+  void* mark_ctx;
   bool shared_early;
   bool shared_gu_done;  // the shared expert's h is already in the workspace (one token)
   unsigned int* comb_ctl;

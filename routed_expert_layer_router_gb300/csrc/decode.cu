@@ -573,8 +573,10 @@ __device__ __forceinline__ void down_unit(const DecodeParams& p, unsigned char* 
   }
 }
 
+// one token: three CTAs per SM (at most 85 registers), so that the routed
+// units (8 experts x 48 tiles) run in one wave
 template <int MAXM>
-__global__ void __launch_bounds__(kDecThreads) k_decode_down(DecodeParams p) {
+__global__ void __launch_bounds__(kDecThreads, MAXM == 1 ? 3 : 2) k_decode_down(DecodeParams p) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   __shared__ int s_last;
   pdl_wait();
@@ -676,6 +678,7 @@ moe_status decode_ffn(const moe_ffn_args* a, cudaStream_t s, const DecodeFuse& f
       if (launch_pdl(p.maxm == 2 ? k_decode_gu<2> : k_decode_gu<1>, grid, kDecThreads, smem, s,
                      p) != cudaSuccess)
         return MOE_ERR_CUDA;
+      if (fz.mark) fz.mark(fz.mark_ctx);
     }
   }
   if (a->stages & MOE_STAGE_DOWN) {
@@ -694,6 +697,7 @@ moe_status decode_ffn(const moe_ffn_args* a, cudaStream_t s, const DecodeFuse& f
       if (launch_pdl(p.maxm == 2 ? k_decode_down<2> : k_decode_down<1>, grid, kDecThreads, smem,
                      s, p) != cudaSuccess)
         return MOE_ERR_CUDA;
+      if (fz.mark) fz.mark(fz.mark_ctx);
     }
   }
   return MOE_OK;

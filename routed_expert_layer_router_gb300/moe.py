@@ -86,6 +86,7 @@ SIGNATURES = {
     "moe_layer_destroy": (i32, [vp]),
     "moe_layer_forward": (i32, [vp, vp, i32, vp, vp]),
     "moe_layer_debug_ptrs": (i32, [vp, vp, vp, vp, vp, vp, vp]),
+    "moe_layer_set_timing": (i32, [vp, vp, i32]),
     "moe_read_device_status": (i32, [vp, vp, ctypes.POINTER(ctypes.c_int32)]),
 }
 
@@ -223,6 +224,12 @@ def moe_layer_debug_ptrs(layer: int) -> dict:
     _ck("moe_layer_debug_ptrs",
         lib().moe_layer_debug_ptrs(layer, *[ctypes.byref(o) for o in outs]))
     return dict(zip(["ids", "w", "p_sel", "perm", "src_slot", "n_act"], [o.value for o in outs]))
+
+
+def moe_layer_set_timing(layer: int, events: list) -> None:
+    """events: cudaEvent_t handles (ints); [] clears the hook."""
+    arr = (vp * max(1, len(events)))(*events)
+    _ck("moe_layer_set_timing", lib().moe_layer_set_timing(layer, arr, len(events)))
 
 
 def moe_read_device_status(layer: int, stream: int = 0) -> int:
