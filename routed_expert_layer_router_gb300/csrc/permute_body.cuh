@@ -184,4 +184,92 @@ __device__ __forceinline__ void permute_body(const int32_t* ids, int n, int E,
 }
 
 
+// The same results as permute_body (and lookup_body) for n <= 32 routes and
+// no padded offsets, without block-wide scans: warp 0 ranks the routes by
+// (expert, route) with shuffles and runs the lookup over the distinct
+// experts (at most 32); every thread writes the counts/offsets of its
+// experts by counting the staged ids.  `s_ids` holds 32 ints of shared
+// memory.  Called by all threads of the CTA.
+__device__ __forceinline__ void permute_small(const int32_t* ids, int n, int E,
+                                              int32_t* __restrict__ counts,
+                                              int32_t* __restrict__ offsets,
+                                              int32_t* __restrict__ perm,
+                                              int32_t* __restrict__ inv, int32_t* status,
+                                              const LookupArgs& lk, int* s_ids) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  if (tid < 32) {
+    const int r = lane;
+    int e = r < n ? __ldcg(ids + r) : -1;
+    const bool valid = r < n && e >= 0 && e < E;
+    if (r < n && !valid) set_status(status, MOE_ERR_DEVICE);
+    if (!valid) e = -1;
+    s_ids[r] = e;
+    // rank among the valid routes by (expert, route), and whether this route
+    // is the first of its expert
+    int rank = 0;
+    bool first = valid;
+    for (int j = 0; j < 32; ++j) {
+      const int ej = __shfl_sync(0xFFFFFFFFu, e, j);
+      if (ej >= 0 && valid && (ej < e || (ej == e && j < r))) ++rank;
+      if (ej == e && j < r) first = false;
+    }
+    if (valid) {
+      perm[rank] = r;
+      inv[r] = rank;
+    } else if (r < n) {
+      inv[r] = -1;
+    }
+    if (lk.table) {
+      // lookup over the distinct experts, in expert order: hits, then misses
+      int slot = first ? lk.table[e] : -1;
+      if (first && slot >= 0 && (slot < lk.slot_lo || slot >= lk.slot_hi)) {
+        set_status(status, MOE_ERR_DEVICE);  // stale or foreign slot: treat as a miss
+        slot = -1;
+      }
+      const bool hit = first && slot >= 0, miss = first && slot < 0;
+      const unsigned hb = __ballot_sync(0xFFFFFFFFu, hit), mb = __ballot_sync(0xFFFFFFFFu, miss);
+      int ph = 0, pm = 0;  // hits / misses among the distinct experts below e
+      for (int j = 0; j < 32; ++j) {
+        const int ej = __shfl_sync(0xFFFFFFFFu, e, j);
+        if (ej < e) {
+          ph += (hb >> j) & 1u;
+          pm += (mb >> j) & 1u;
+        }
+      }
+      const int nh = __popc(hb), nm = __popc(mb);
+      if (hit) {
+        lk.act_list[ph] = e;
+        lk.src_slot[e] = slot;
+      } else if (miss) {
+        lk.act_list[nh + pm] = e;
+        lk.miss_ids[pm] = e;
+        int sm = -1;
+        if (lk.n_stage > 0) sm = lk.n_cache + (pm % lk.n_stage);
+        else set_status(status, MOE_ERR_DEVICE);
+        lk.src_slot[e] = sm;
+      }
+      if (lane == 0) {
+        lk.n_act[0] = nh + nm;
+        lk.n_act[1] = nh;
+        *lk.n_miss = nm;
+      }
+    }
+  }
+  __syncthreads();
+  int nv = 0;  // valid routes
+  for (int j = 0; j < n; ++j) nv += s_ids[j] >= 0;
+  for (int x = tid; x < E; x += blockDim.x) {
+    int c = 0, below = 0;
+    for (int j = 0; j < n; ++j) {
+      const int ej = s_ids[j];
+      c += ej == x;
+      below += ej >= 0 && ej < x;
+    }
+    counts[x] = c;
+    offsets[x] = below;
+    if (lk.table && c == 0) lk.src_slot[x] = -1;  // the active experts' slots: warp 0
+  }
+  if (tid == 0) offsets[E] = nv;
+}
+
 }  // namespace moe

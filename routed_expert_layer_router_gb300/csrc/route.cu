@@ -248,50 +248,64 @@ __global__ void __launch_bounds__(kGemmThreads) k_logits_gemm(const uint16_t* __
 // ---- softmax + top-k + renormalisation: one warp per token ------------------
 // `src` holds the token's E logits (read once, through L2), `l` is the warp's
 // shared-memory copy of them.  Ties go to the lower expert id.
-__device__ __forceinline__ void topk_token(const float* src, float* l, int t, int E, int k,
-                                           int32_t* __restrict__ ids, float* __restrict__ w,
-                                           float* __restrict__ p_sel) {
+// Softmax over the E logits of token t (staged in shared memory `l`), then the
+// top-k by (logit desc, id asc), renormalised; one warp.  Lane j holds the
+// logits of experts j, j + 32, ... in registers (PER of them, PER >= E/32),
+// so that each of the k selection rounds is a register scan plus one warp
+// argmax, with no memory access.
+template <int PER>
+__device__ __forceinline__ void topk_token_r(const float* l, int t, int E, int k,
+                                             int32_t* __restrict__ ids, float* __restrict__ w,
+                                             float* __restrict__ p_sel) {
   const int lane = threadIdx.x & 31;
-  const int per = (E + 31) / 32;
+  float v[PER];
   float lmax = -INFINITY;
-  for (int j = 0; j < per; ++j) {
-    int e = lane + 32 * j;
-    float v = (e < E) ? __ldcg(src + e) : -INFINITY;
-    if (e < E) l[e] = v;
-    lmax = fmaxf(lmax, v);
+#pragma unroll
+  for (int j = 0; j < PER; ++j) {
+    const int e = lane + 32 * j;
+    v[j] = e < E ? l[e] : -INFINITY;
+    lmax = fmaxf(lmax, v[j]);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) lmax = fmaxf(lmax, __shfl_xor_sync(0xFFFFFFFFu, lmax, o));
   float z = 0.f;
-  for (int j = 0; j < per; ++j) {
-    int e = lane + 32 * j;
-    if (e < E) z += expf(l[e] - lmax);
-  }
+#pragma unroll
+  for (int j = 0; j < PER; ++j)
+    if (lane + 32 * j < E) z += expf(v[j] - lmax);
   z = warp_sum(z);
-  uint32_t taken = 0;  // bit j: element lane + 32 j selected
-  float sel_sum = 0.f;
-  float my_v = 0.f;
+  float sel_sum = 0.f, my_v = 0.f;
   int my_id = -1;
   for (int s = 0; s < k; ++s) {
     float bv = -INFINITY;
     int bid = 0x7FFFFFFF;
-    for (int j = 0; j < per; ++j) {
-      int e = lane + 32 * j;
-      if (e < E && !((taken >> j) & 1u)) {
-        float v = l[e];
-        if (v > bv || (v == bv && e < bid)) { bv = v; bid = e; }
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {  // ids ascend with j: strict > keeps the lower id
+      const int e = lane + 32 * j;
+      if (e < E && v[j] > bv) {
+        bv = v[j];
+        bid = e;
       }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
-      float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
-      int oid = __shfl_xor_sync(0xFFFFFFFFu, bid, o);
-      if (ov > bv || (ov == bv && oid < bid)) { bv = ov; bid = oid; }
+      const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
+      const int oid = __shfl_xor_sync(0xFFFFFFFFu, bid, o);
+      if (ov > bv || (ov == bv && oid < bid)) {
+        bv = ov;
+        bid = oid;
+      }
     }
-    if ((bid & 31) == lane) taken |= 1u << (bid >> 5);
-    float pe = expf(bv - lmax);
+    if ((bid & 31) == lane) {  // taken: out of the later rounds
+#pragma unroll
+      for (int j = 0; j < PER; ++j)
+        if (j == (bid >> 5)) v[j] = -INFINITY;
+    }
+    const float pe = expf(bv - lmax);
     sel_sum += pe;  // same value and order in every lane
-    if (lane == s) { my_v = pe; my_id = bid; }
+    if (lane == s) {
+      my_v = pe;
+      my_id = bid;
+    }
   }
   if (lane < k) {
     ids[(size_t)t * k + lane] = my_id;
@@ -300,16 +314,34 @@ __device__ __forceinline__ void topk_token(const float* src, float* l, int t, in
   }
 }
 
+__device__ __forceinline__ void topk_token(const float* l, int t, int E, int k,
+                                           int32_t* __restrict__ ids, float* __restrict__ w,
+                                           float* __restrict__ p_sel) {
+  if (E <= 4 * 32) topk_token_r<4>(l, t, E, k, ids, w, p_sel);
+  else if (E <= 9 * 32) topk_token_r<9>(l, t, E, k, ids, w, p_sel);
+  else if (E <= 16 * 32) topk_token_r<16>(l, t, E, k, ids, w, p_sel);
+  else topk_token_r<32>(l, t, E, k, ids, w, p_sel);
+}
+
+// the logits of tokens [t0, t0 + nt) into shared memory, read through L2 by
+// every thread of the CTA (coalesced)
+__device__ __forceinline__ void stage_logits(const float* logits, int t0, int nt, int E,
+                                             float* sl) {
+  for (int i = threadIdx.x; i < nt * E; i += blockDim.x) sl[i] = __ldcg(logits + (size_t)t0 * E + i);
+  __syncthreads();
+}
+
 __global__ void __launch_bounds__(256) k_topk(const float* __restrict__ logits, int T, int E,
                                               int k, int32_t* __restrict__ ids,
                                               float* __restrict__ w, float* __restrict__ p_sel) {
-  extern __shared__ float sl[];  // [8 warps][E]
+  extern __shared__ float sl[];  // [8 tokens][E]
   pdl_wait();
   pdl_launch_dependents();
   const int wid = threadIdx.x >> 5;
-  const int t = blockIdx.x * 8 + wid;
+  const int t0 = blockIdx.x * 8, t = t0 + wid;
+  stage_logits(logits, t0, min(8, T - t0), E, sl);
   if (t >= T) return;
-  topk_token(logits + (size_t)t * E, sl + (size_t)wid * E, t, E, k, ids, w, p_sel);
+  topk_token(sl + (size_t)wid * E, t, E, k, ids, w, p_sel);
 }
 
 // ---- few tokens: logits and top-k in one kernel -----------------------------
@@ -338,7 +370,8 @@ __global__ void __launch_bounds__(256) k_route_small(const uint16_t* __restrict_
   if (!s_last) return;
   __threadfence();
   const int wid = threadIdx.x >> 5;
-  if (wid < T) topk_token(logits + (size_t)wid * E, sl + (size_t)wid * E, wid, E, k, ids, w, p_sel);
+  stage_logits(logits, 0, T, E, sl);
+  if (wid < T) topk_token(sl + (size_t)wid * E, wid, E, k, ids, w, p_sel);
   if (threadIdx.x == 0) *done = 0u;  // ready for the next call
 }
 
@@ -439,10 +472,15 @@ __global__ void __launch_bounds__(kPermThreads, 2) k_route_permute_small(
   if (!s_last) return;
   __threadfence();
   const int wid = threadIdx.x >> 5;
-  if (wid < T) topk_token(logits + (size_t)wid * E, sl + (size_t)wid * E, wid, E, k, ids, w, p_sel);
+  stage_logits(logits, 0, T, E, sl);
+  if (wid < T) topk_token(sl + (size_t)wid * E, wid, E, k, ids, w, p_sel);
   __syncthreads();  // ids written by this CTA: read back through L2 below
-  permute_body(ids, T * k, E, pa.counts, pa.offsets, pa.perm, pa.inv, pa.pad_offsets,
-               pa.pad_align, pa.status, pa.lk, reinterpret_cast<int*>(sl), 0);
+  if (T * k <= 32 && !pa.pad_offsets)
+    permute_small(ids, T * k, E, pa.counts, pa.offsets, pa.perm, pa.inv, pa.status, pa.lk,
+                  reinterpret_cast<int*>(sl));
+  else
+    permute_body(ids, T * k, E, pa.counts, pa.offsets, pa.perm, pa.inv, pa.pad_offsets,
+                 pa.pad_align, pa.status, pa.lk, reinterpret_cast<int*>(sl), 0);
   if (threadIdx.x == 0) *done = 0u;  // ready for the next call
 }
 
