@@ -84,32 +84,55 @@ __device__ __forceinline__ void group_range(const DecodeParams& p, int& a0, int&
 }
 
 // ---- staging ---------------------------------------------------------------
+// Each thread issues the loads of up to kStageBatch of its elements before
+// storing any of them, so that a CTA's staging costs about one round trip.
+constexpr int kStageBatch = 8;
+
 // f16 layout: row j, half-k-group hk (32 values) at (j*nhk + hk)*kHPad halves
 __device__ __forceinline__ void stage_bf16_to_f16(__half* xs, const uint16_t* const* rows, int m,
                                                   int K) {
-  const int nhk = K / 32;
+  const int nhk = K / 32, n = K / 2;
   for (int j = 0; j < m; ++j) {
     const uint32_t* src = reinterpret_cast<const uint32_t*>(rows[j]);
     __half* dst = xs + (size_t)j * nhk * kHPad;
-    for (int i = threadIdx.x; i < K / 2; i += blockDim.x) {
-      uint32_t v = __ldg(src + i);
-      const int e = 2 * i;
-      *reinterpret_cast<__half2*>(dst + (e >> 5) * kHPad + (e & 31)) =
-          __floats2half2_rn(bf16_lo(v), bf16_hi(v));
+    for (int i0 = threadIdx.x; i0 < n; i0 += kStageBatch * blockDim.x) {
+      uint32_t v[kStageBatch];
+#pragma unroll
+      for (int u = 0; u < kStageBatch; ++u) {
+        const int i = i0 + u * blockDim.x;
+        v[u] = i < n ? __ldg(src + i) : 0u;
+      }
+#pragma unroll
+      for (int u = 0; u < kStageBatch; ++u) {
+        const int e = 2 * (i0 + u * blockDim.x);
+        if (e < K)
+          *reinterpret_cast<__half2*>(dst + (e >> 5) * kHPad + (e & 31)) =
+              __floats2half2_rn(bf16_lo(v[u]), bf16_hi(v[u]));
+      }
     }
   }
 }
 
 __device__ __forceinline__ void stage_f32_to_f16(__half* xs, const float* const* rows, int m,
                                                  int K) {
-  const int nhk = K / 32;
+  const int nhk = K / 32, n = K / 2;
   for (int j = 0; j < m; ++j) {
     const float2* src = reinterpret_cast<const float2*>(rows[j]);
     __half* dst = xs + (size_t)j * nhk * kHPad;
-    for (int i = threadIdx.x; i < K / 2; i += blockDim.x) {
-      float2 v = src[i];
-      const int e = 2 * i;
-      *reinterpret_cast<__half2*>(dst + (e >> 5) * kHPad + (e & 31)) = __floats2half2_rn(v.x, v.y);
+    for (int i0 = threadIdx.x; i0 < n; i0 += kStageBatch * blockDim.x) {
+      float2 v[kStageBatch];
+#pragma unroll
+      for (int u = 0; u < kStageBatch; ++u) {
+        const int i = i0 + u * blockDim.x;
+        v[u] = i < n ? src[i] : make_float2(0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < kStageBatch; ++u) {
+        const int e = 2 * (i0 + u * blockDim.x);
+        if (e < K)
+          *reinterpret_cast<__half2*>(dst + (e >> 5) * kHPad + (e & 31)) =
+              __floats2half2_rn(v[u].x, v[u].y);
+      }
     }
   }
 }
@@ -117,29 +140,47 @@ __device__ __forceinline__ void stage_f32_to_f16(__half* xs, const float* const*
 // fp32 layout: row j, half-k-group hk at (j*nhk + hk)*kXPad floats
 __device__ __forceinline__ void stage_bf16_to_f32(float* xs, const uint16_t* const* rows, int m,
                                                   int K) {
-  const int nhk = K / 32;
+  const int nhk = K / 32, n = K / 2;
   for (int j = 0; j < m; ++j) {
     const uint32_t* src = reinterpret_cast<const uint32_t*>(rows[j]);
     float* dst = xs + (size_t)j * nhk * kXPad;
-    for (int i = threadIdx.x; i < K / 2; i += blockDim.x) {
-      uint32_t v = __ldg(src + i);
-      const int e = 2 * i;
-      dst[(e >> 5) * kXPad + (e & 31)] = bf16_lo(v);
-      dst[(e >> 5) * kXPad + (e & 31) + 1] = bf16_hi(v);
+    for (int i0 = threadIdx.x; i0 < n; i0 += kStageBatch * blockDim.x) {
+      uint32_t v[kStageBatch];
+#pragma unroll
+      for (int u = 0; u < kStageBatch; ++u) {
+        const int i = i0 + u * blockDim.x;
+        v[u] = i < n ? __ldg(src + i) : 0u;
+      }
+#pragma unroll
+      for (int u = 0; u < kStageBatch; ++u) {
+        const int e = 2 * (i0 + u * blockDim.x);
+        if (e < K) {
+          dst[(e >> 5) * kXPad + (e & 31)] = bf16_lo(v[u]);
+          dst[(e >> 5) * kXPad + (e & 31) + 1] = bf16_hi(v[u]);
+        }
+      }
     }
   }
 }
 
 __device__ __forceinline__ void stage_f32_to_f32(float* xs, const float* const* rows, int m,
                                                  int K) {
-  const int nhk = K / 32;
+  const int nhk = K / 32, n = K / 4;
   for (int j = 0; j < m; ++j) {
     const float4* src = reinterpret_cast<const float4*>(rows[j]);
     float* dst = xs + (size_t)j * nhk * kXPad;
-    for (int i = threadIdx.x; i < K / 4; i += blockDim.x) {
-      float4 v = src[i];
-      const int e = 4 * i;
-      *reinterpret_cast<float4*>(dst + (e >> 5) * kXPad + (e & 31)) = v;
+    for (int i0 = threadIdx.x; i0 < n; i0 += kStageBatch * blockDim.x) {
+      float4 v[kStageBatch];
+#pragma unroll
+      for (int u = 0; u < kStageBatch; ++u) {
+        const int i = i0 + u * blockDim.x;
+        v[u] = i < n ? src[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < kStageBatch; ++u) {
+        const int e = 4 * (i0 + u * blockDim.x);
+        if (e < K) *reinterpret_cast<float4*>(dst + (e >> 5) * kXPad + (e & 31)) = v[u];
+      }
     }
   }
 }
