@@ -33,13 +33,15 @@ moe_status route_permute_small(const moe_route_args* a, const PermArgs& pa,
 }  // namespace moe
 
 namespace moe {
-bool pdl_enabled() {
-  static const int on = [] {
+static int pdl_mode() {
+  static const int m = [] {
     const char* v = getenv("MOE_PDL");
-    return (v && v[0] == '0') ? 0 : 1;
+    return !v ? 2 : v[0] == '0' ? 0 : v[0] == '1' ? 1 : 2;
   }();
-  return on != 0;
+  return m;
 }
+bool pdl_enabled() { return pdl_mode() != 0; }
+bool pdl_in_graphs() { return pdl_mode() == 2; }
 }  // namespace moe
 
 using namespace moe;

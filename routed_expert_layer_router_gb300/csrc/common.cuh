@@ -106,9 +106,8 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 // ---- programmatic dependent launch ------------------------------------------
-// A kernel launched with launch_pdl() on a stream that is not being captured
-// may start while the previous kernel on its stream is still running (inside
-// a CUDA graph the launches stay plain: measured slower there).  pdl_wait() blocks until that kernel has
+// A kernel launched with launch_pdl() may start while the previous kernel on
+// its stream is still running (in streams and in captured CUDA graphs).  pdl_wait() blocks until that kernel has
 // completed and its writes are visible; pdl_launch_dependents() lets the next
 // kernel start launching.  Every kernel launched with launch_pdl() calls
 // pdl_wait() before it touches memory that an earlier kernel writes or reads,
@@ -119,7 +118,8 @@ __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-bool pdl_enabled();  // on unless the environment sets MOE_PDL=0
+bool pdl_enabled();    // on unless the environment sets MOE_PDL=0
+bool pdl_in_graphs();  // also inside stream capture, unless MOE_PDL=1
 
 // What the layer's own sequence lets the decode FFN do beyond moe_expert_ffn:
 // start the shared-expert gate/up units before the routing is complete (the
@@ -154,7 +154,7 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
     cudaGetLastError();  // not a launch error: launch without the attribute
     plain = true;
   }
-  cfg.numAttrs = (plain || cs != cudaStreamCaptureStatusNone) ? 0 : 1;
+  cfg.numAttrs = (plain || (cs != cudaStreamCaptureStatusNone && !pdl_in_graphs())) ? 0 : 1;
   return cudaLaunchKernelEx(&cfg, kern, ((KArgs)args)...);
 }
 
