@@ -115,7 +115,7 @@ static moe_status expert_ffn(const moe_ffn_args* a, void* stream, const DecodeFu
 }
 
 MOE_API moe_status moe_expert_ffn(const moe_ffn_args* a, void* stream) {
-  const DecodeFuse none = {nullptr, nullptr, false, false, nullptr, nullptr, nullptr};
+  const DecodeFuse none = {nullptr, nullptr, nullptr, false, false, nullptr, nullptr, nullptr};
   return expert_ffn(a, stream, none);
 }
 
@@ -130,6 +130,7 @@ struct moe_layer {
   int32_t *src_slot, *act_list, *n_act, *miss_ids, *n_miss, *status;
   float *o_route, *o_shared, *y_acc;
   void* route_ctl;
+  int4* act_meta;  // compact per-expert records of the small-route path
   void* ffn_ws;
   size_t ffn_ws_bytes;
   int last_T;
@@ -179,6 +180,7 @@ MOE_API moe_status moe_layer_create(const moe_layer_desc* d, moe_layer** out) {
       4,                  /* status */
       (size_t)T * k * H * 4, /* o_route */
       (size_t)T * H * 4,  /* o_shared */
+      (size_t)E * 32,     /* act_meta */
       prefill ? (size_t)T * H * 4 : 0, /* y_acc */
       l->ffn_ws_bytes,
       kRouteCtlBytes + kTileCtlBytes /* route_ctl, then the combine's tile counters */};
@@ -192,7 +194,7 @@ MOE_API moe_status moe_layer_create(const moe_layer_desc* d, moe_layer** out) {
   }
   l->ws_bytes = total;
   uint8_t* p = (uint8_t*)l->ws;
-  void* ptrs[20];
+  void* ptrs[21];
   for (int i = 0; i < n; ++i) {
     ptrs[i] = sizes[i] ? p : nullptr;
     p += align256(sizes[i]);
@@ -214,9 +216,10 @@ MOE_API moe_status moe_layer_create(const moe_layer_desc* d, moe_layer** out) {
   l->status = (int32_t*)ptrs[14];
   l->o_route = (float*)ptrs[15];
   l->o_shared = (float*)ptrs[16];
-  l->y_acc = (float*)ptrs[17];
-  l->ffn_ws = ptrs[18];
-  l->route_ctl = ptrs[19];
+  l->act_meta = (int4*)ptrs[17];
+  l->y_acc = (float*)ptrs[18];
+  l->ffn_ws = ptrs[19];
+  l->route_ctl = ptrs[20];
   if (cudaMemset(l->ws, 0, total) != cudaSuccess) {
     cudaFree(l->ws);
     free(l);
@@ -267,6 +270,13 @@ MOE_API moe_status moe_layer_forward(moe_layer* l, const void* x, int T, void* y
   pa.counts = l->counts; pa.offsets = l->offsets; pa.perm = l->perm; pa.inv = l->inv;
   pa.pad_offsets = prefill ? l->pad_offsets : nullptr; pa.pad_align = 128;
   pa.status = l->status; pa.lk = lk;
+  // few routes and no padding: the fused kernel's permutation also writes the
+  // compact per-expert records that the decode FFN reads
+  const bool small_routes = T * d.k <= 32 && !prefill;
+  if (small_routes) {
+    pa.lk.meta = l->act_meta;
+    pa.lk.gscale = d.gscale;
+  }
   // one decode token: the shared expert's gate/up runs beside the router,
   // into the FFN workspace's h_shared (after the routes' h)
   SharedGuArgs sg = {nullptr, nullptr, 0, nullptr};
@@ -278,6 +288,7 @@ MOE_API moe_status moe_layer_forward(moe_layer* l, const void* x, int T, void* y
   }
   st = route_permute_small(&ra, pa, sg, s);
   const bool shared_gu_done = st == MOE_OK && sg.Is > 0;
+  const int4* act_meta = (st == MOE_OK && small_routes) ? l->act_meta : nullptr;
   if (st == MOE_ERR_UNSUPPORTED) {
     if ((st = moe_route(&ra, stream)) != MOE_OK) return st;
     layer_mark(l);
@@ -321,7 +332,8 @@ MOE_API moe_status moe_layer_forward(moe_layer* l, const void* x, int T, void* y
     fa.group = g;
     // the kernel before this call is the permutation or the gather; a single
     // decode group's down kernel also writes y (no separate combine)
-    DecodeFuse fz = {layer_mark_cb, l, true, shared_gu_done && g == 0, nullptr, nullptr, nullptr};
+    DecodeFuse fz = {layer_mark_cb, l, act_meta, true, shared_gu_done && g == 0,
+                     nullptr, nullptr, nullptr};
     if (!prefill && groups == 1) {
       fz.comb_ctl = (unsigned int*)((char*)l->route_ctl + kRouteCtlBytes);
       fz.inv = l->inv;

@@ -219,6 +219,8 @@ void cache_lookup_args(const expcache* c, int layer, int32_t* src_slot, int32_t*
   out->n_act = n_act;
   out->miss_ids = miss_ids;
   out->n_miss = n_miss;
+  out->meta = nullptr;
+  out->gscale = nullptr;
 }
 }  // namespace moe
 

@@ -23,6 +23,11 @@ struct LookupArgs {
   const int32_t* table;  // the layer's row of the slot table, nullptr: no lookup
   int slot_lo, slot_hi, n_cache, n_stage;
   int32_t *src_slot, *act_list, *n_act, *miss_ids, *n_miss;
+  // optional (small-route path): per act_list position a, meta[2a] = {expert,
+  // slot, first route position, routes}, meta[2a+1] = its gscale row (fp32
+  // bits), so that the FFN's CTAs read one record instead of a chain of loads
+  int4* meta;
+  const float* gscale;
 };
 
 // ---- record layout (see moe.h) ---------------------------------------------
@@ -129,6 +134,7 @@ bool pdl_in_graphs();  // also inside stream capture, unless MOE_PDL=1
 struct DecodeFuse {
   void (*mark)(void*);  // called after each kernel launch (timing hook), or nullptr
   void* mark_ctx;
+  const int4* act_meta;  // LookupArgs::meta of this forward, or nullptr
   bool shared_early;
   bool shared_gu_done;  // the shared expert's h is already in the workspace (one token)
   unsigned int* comb_ctl;

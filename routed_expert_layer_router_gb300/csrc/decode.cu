@@ -66,9 +66,52 @@ struct DecodeParams {
   // the last one writes y's columns of that tile.  comb_ctl == nullptr: off.
   unsigned int* comb_ctl;
   int comb_target;
+  const int4* act_meta;  // per act_list position: {expert, slot, route, routes}, gscale row
   const int32_t* inv;
   uint16_t* y;
 };
+
+// An active expert of this group: its id, slot, first route position,
+// number of routes and global scales.  From the compact record when the
+// routing wrote one (a single round trip), else from act_list, src_slot,
+// offsets and gscale.  False: position a is past the group's end.
+struct ActExpert {
+  int e, slot, pb, cnt;
+  float g[3];
+};
+__device__ __forceinline__ void group_range(const DecodeParams& p, int& a0, int& a1);
+__device__ __forceinline__ bool act_expert(const DecodeParams& p, int a, ActExpert& x) {
+  int4 m0 = make_int4(0, 0, 0, 0), m1 = m0;
+  if (p.act_meta && p.group == 0) {  // issued before the group's bounds are known
+    m0 = p.act_meta[2 * a];
+    m1 = p.act_meta[2 * a + 1];
+  }
+  int a0, a1;
+  group_range(p, a0, a1);
+  if (a0 + a >= a1) return false;
+  if (p.act_meta) {
+    if (p.group != 0) {
+      m0 = p.act_meta[2 * (a0 + a)];
+      m1 = p.act_meta[2 * (a0 + a) + 1];
+    }
+    x.e = m0.x; x.slot = m0.y; x.pb = m0.z; x.cnt = m0.w;
+    x.g[0] = __int_as_float(m1.x); x.g[1] = __int_as_float(m1.y); x.g[2] = __int_as_float(m1.z);
+    return true;
+  }
+  x.e = p.act_list[a0 + a];
+  x.slot = (x.e >= 0 && x.e < p.E) ? p.src_slot[x.e] : -1;
+  if (x.e >= 0 && x.e < p.E) {
+    x.pb = p.offsets[x.e];
+    x.cnt = p.offsets[x.e + 1] - x.pb;
+    x.g[0] = p.gscale[x.e * 3 + 0];
+    x.g[1] = p.gscale[x.e * 3 + 1];
+    x.g[2] = p.gscale[x.e * 3 + 2];
+  } else {
+    x.pb = x.cnt = 0;
+    x.g[0] = x.g[1] = x.g[2] = 0.f;
+  }
+  return true;
+}
 
 // act_list index range of this group
 __device__ __forceinline__ void group_range(const DecodeParams& p, int& a0, int& a1) {
@@ -466,19 +509,17 @@ __global__ void __launch_bounds__(kDecThreads) k_decode_gu(DecodeParams p) {
   const int tiles = p.I / 128;
   const int a = ur / (tiles * 4), rem = ur % (tiles * 4);
   const int rt = rem >> 2, m0 = (rem & 3) * kDecWarps + wid;
-  int a0, a1;
-  group_range(p, a0, a1);
-  if (a0 + a >= a1) return;
-  const int e = p.act_list[a0 + a];
-  const int slot = (e >= 0 && e < p.E) ? p.src_slot[e] : -1;
+  ActExpert ax;
+  if (!act_expert(p, a, ax)) return;
+  const int slot = ax.slot;
   if (slot < 0 || slot >= p.n_slots) {
     if (threadIdx.x == 0) set_status(p.status, MOE_ERR_DEVICE);
     return;
   }
   const uint8_t* rec = p.arena + (uint64_t)slot * p.rec_bytes;
   const RecordLayout L(p.H, p.I);
-  const float gg = p.gscale[e * 3 + 0], gu = p.gscale[e * 3 + 1];
-  const int pb = p.offsets[e], pe = p.offsets[e + 1];
+  const float gg = ax.g[0], gu = ax.g[1];
+  const int pb = ax.pb, pe = ax.pb + ax.cnt;
   for (int q0 = pb; q0 < pe; q0 += p.maxm) {
     const int mm = min(p.maxm, pe - q0);
     const uint16_t* rows[2];
@@ -592,16 +633,14 @@ __device__ __forceinline__ void down_unit(const DecodeParams& p, unsigned char* 
   const int ur = u - p.n_shared_units;
   const int tiles = p.H / 128;
   const int a = ur / tiles, rt = ur % tiles;
-  int a0, a1;
-  group_range(p, a0, a1);
-  if (a0 + a >= a1) return;
-  const int e = p.act_list[a0 + a];
-  const int slot = (e >= 0 && e < p.E) ? p.src_slot[e] : -1;
+  ActExpert ax;
+  if (!act_expert(p, a, ax)) return;
+  const int slot = ax.slot;
   if (slot < 0 || slot >= p.n_slots) return;  // reported by K-decode-gu
   const uint8_t* rec = p.arena + (uint64_t)slot * p.rec_bytes;
   const RecordLayout L(p.H, p.I);
-  const float gd = p.gscale[e * 3 + 2];
-  const int pb = p.offsets[e], pe = p.offsets[e + 1];
+  const float gd = ax.g[2];
+  const int pb = ax.pb, pe = ax.pb + ax.cnt;
   for (int q0 = pb; q0 < pe; q0 += p.maxm) {
     const int mm = min(p.maxm, pe - q0);
     const float* rows[2];
@@ -680,6 +719,7 @@ moe_status decode_ffn(const moe_ffn_args* a, cudaStream_t s, const DecodeFuse& f
   p.shared_early = fz.shared_early ? 1 : 0;
   p.comb_ctl = nullptr;
   p.comb_target = 0;
+  p.act_meta = fz.act_meta;
   p.inv = fz.inv;
   p.y = fz.y;
   p.T = a->T; p.H = a->H; p.I = a->I; p.E = a->E; p.k = a->k; p.Is = a->Is;

@@ -206,12 +206,13 @@ __device__ __forceinline__ void permute_small(const int32_t* ids, int n, int E,
     s_ids[r] = e;
     // rank among the valid routes by (expert, route), and whether this route
     // is the first of its expert
-    int rank = 0;
+    int rank = 0, cnt = 0;
     bool first = valid;
     for (int j = 0; j < 32; ++j) {
       const int ej = __shfl_sync(0xFFFFFFFFu, e, j);
       if (ej >= 0 && valid && (ej < e || (ej == e && j < r))) ++rank;
       if (ej == e && j < r) first = false;
+      cnt += valid && ej == e;
     }
     if (valid) {
       perm[rank] = r;
@@ -237,16 +238,25 @@ __device__ __forceinline__ void permute_small(const int32_t* ids, int n, int E,
         }
       }
       const int nh = __popc(hb), nm = __popc(mb);
+      int pos = -1, fslot = -1;
       if (hit) {
+        pos = ph;
+        fslot = slot;
         lk.act_list[ph] = e;
         lk.src_slot[e] = slot;
       } else if (miss) {
+        pos = nh + pm;
         lk.act_list[nh + pm] = e;
         lk.miss_ids[pm] = e;
-        int sm = -1;
-        if (lk.n_stage > 0) sm = lk.n_cache + (pm % lk.n_stage);
+        if (lk.n_stage > 0) fslot = lk.n_cache + (pm % lk.n_stage);
         else set_status(status, MOE_ERR_DEVICE);
-        lk.src_slot[e] = sm;
+        lk.src_slot[e] = fslot;
+      }
+      if (lk.meta && pos >= 0) {  // the first route of expert e is at rank
+        lk.meta[2 * pos] = make_int4(e, fslot, rank, cnt);
+        lk.meta[2 * pos + 1] = make_int4(__float_as_int(lk.gscale[e * 3 + 0]),
+                                         __float_as_int(lk.gscale[e * 3 + 1]),
+                                         __float_as_int(lk.gscale[e * 3 + 2]), 0);
       }
       if (lane == 0) {
         lk.n_act[0] = nh + nm;
