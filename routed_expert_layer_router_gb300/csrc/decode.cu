@@ -288,30 +288,55 @@ __device__ __forceinline__ void load_xh(const __half* xs, int nhk, int hk, uint3
 
 // gate+up of the 4 rows {rt*128 + m0 + 32*m1} of one expert, M staged tokens.
 // Returns warp-reduced sums (all lanes).
-template <int M>
-__device__ void warp_gu_fp4(const uint8_t* rec, const RecordLayout& L, int H, int rt, int m0,
-                            const __half* xs, float accg[4][M], float accu[4][M]) {
-  const int lane = threadIdx.x & 31;
-  const int KB = H / 16, nhk = H / 32;
+// One lane's 32-value step of a warp's 4 gate + 4 up rows: codes and the two
+// scale atom rows.
+struct GuRegs {
+  uint4 g[4], u[4], sg, su;
+};
+__device__ __forceinline__ void gu_fetch(const uint8_t* rec, const RecordLayout& L, int H, int rt,
+                                         int m0, int hk, GuRegs& r) {
   const uint8_t* gc = rec + L.gate_codes + (uint64_t)(rt * 128 + m0) * (H / 2);
   const uint8_t* uc = rec + L.up_codes + (uint64_t)(rt * 128 + m0) * (H / 2);
   const uint64_t rstride = (uint64_t)32 * (H / 2);
+  const uint64_t aoff = atom_offset(rt, hk >> 1, H / 16) + (uint64_t)m0 * 16;
+  r.sg = ldg_stream(rec + L.gate_scales + aoff);
+  r.su = ldg_stream(rec + L.up_scales + aoff);
+#pragma unroll
+  for (int m1 = 0; m1 < 4; ++m1) {
+    r.g[m1] = ldg_stream(gc + m1 * rstride + (uint64_t)hk * 16);
+    r.u[m1] = ldg_stream(uc + m1 * rstride + (uint64_t)hk * 16);
+  }
+}
+
+// `first` holds the step hk = lane, fetched by the caller (before it staged
+// the tokens, so that those loads were already in flight)
+template <int M>
+__device__ void warp_gu_fp4(const uint8_t* rec, const RecordLayout& L, int H, int rt, int m0,
+                            const __half* xs, float accg[4][M], float accu[4][M],
+                            const GuRegs& first) {
+  const int lane = threadIdx.x & 31;
+  const int nhk = H / 32;
 #pragma unroll
   for (int m1 = 0; m1 < 4; ++m1)
 #pragma unroll
     for (int j = 0; j < M; ++j) accg[m1][j] = accu[m1][j] = 0.f;
-  uint4 cg[4], cu[4], sg, su;
+  uint4 cg[4], cu[4], sg = first.sg, su = first.su;
+#pragma unroll
+  for (int m1 = 0; m1 < 4; ++m1) {
+    cg[m1] = first.g[m1];
+    cu[m1] = first.u[m1];
+  }
   auto fetch = [&](int hk, uint4* g4, uint4* u4, uint4& sgv, uint4& suv) {
-    const uint64_t aoff = atom_offset(rt, hk >> 1, KB) + (uint64_t)m0 * 16;
-    sgv = ldg_stream(rec + L.gate_scales + aoff);
-    suv = ldg_stream(rec + L.up_scales + aoff);
+    GuRegs r;
+    gu_fetch(rec, L, H, rt, m0, hk, r);
+    sgv = r.sg;
+    suv = r.su;
 #pragma unroll
     for (int m1 = 0; m1 < 4; ++m1) {
-      g4[m1] = ldg_stream(gc + m1 * rstride + (uint64_t)hk * 16);
-      u4[m1] = ldg_stream(uc + m1 * rstride + (uint64_t)hk * 16);
+      g4[m1] = r.g[m1];
+      u4[m1] = r.u[m1];
     }
   };
-  if (lane < nhk) fetch(lane, cg, cu, sg, su);
   for (int hk = lane; hk < nhk; hk += 32) {
     uint4 ng[4], nu[4], nsg, nsu;
     const bool more = hk + 32 < nhk;
@@ -409,9 +434,9 @@ __device__ void down_shared_pass(const DecodeParams& p, int r0, int t0, int mm, 
 template <int M>
 __device__ void gu_routed_pass(const DecodeParams& p, const RecordLayout& L, const uint8_t* rec,
                                int rt, int m0, int q0, int mm, const __half* xs, float gg,
-                               float gu) {
+                               float gu, const GuRegs& first) {
   float accg[4][M], accu[4][M];
-  warp_gu_fp4<M>(rec, L, p.H, rt, m0, xs, accg, accu);
+  warp_gu_fp4<M>(rec, L, p.H, rt, m0, xs, accg, accu, first);
   const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int m1 = 0; m1 < 4; ++m1)
@@ -465,7 +490,7 @@ __device__ void gu_shared_pass(const DecodeParams& p, int i0, int t0, int mm, co
 // 32 atom rows) first, then the shared-expert units (4 row pairs each), which
 // are half as large and so fill the last wave.
 template <int MAXM>
-__global__ void __launch_bounds__(kDecThreads) k_decode_gu(DecodeParams p) {
+__global__ void __launch_bounds__(kDecThreads, MAXM == 1 ? 2 : 1) k_decode_gu(DecodeParams p) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   __shared__ float red[kDecWarps * 8 * 2];
   const int wid = threadIdx.x >> 5;
@@ -520,15 +545,18 @@ __global__ void __launch_bounds__(kDecThreads) k_decode_gu(DecodeParams p) {
   const RecordLayout L(p.H, p.I);
   const float gg = ax.g[0], gu = ax.g[1];
   const int pb = ax.pb, pe = ax.pb + ax.cnt;
+  const int lane = threadIdx.x & 31;
   for (int q0 = pb; q0 < pe; q0 += p.maxm) {
     const int mm = min(p.maxm, pe - q0);
+    GuRegs first;  // the weights' first step, in flight while the tokens are staged
+    if (lane < p.H / 32) gu_fetch(rec, L, p.H, rt, m0, lane, first);
     const uint16_t* rows[2];
     for (int j = 0; j < mm; ++j) rows[j] = p.x + (size_t)(p.perm[q0 + j] / p.k) * p.H;
     __syncthreads();
     stage_bf16_to_f16(xs, rows, mm, p.H);
     __syncthreads();
-    if (MAXM == 2 && mm == 2) gu_routed_pass<MAXM>(p, L, rec, rt, m0, q0, mm, xs, gg, gu);
-    else gu_routed_pass<1>(p, L, rec, rt, m0, q0, mm, xs, gg, gu);
+    if (MAXM == 2 && mm == 2) gu_routed_pass<MAXM>(p, L, rec, rt, m0, q0, mm, xs, gg, gu, first);
+    else gu_routed_pass<1>(p, L, rec, rt, m0, q0, mm, xs, gg, gu, first);
   }
 }
 
