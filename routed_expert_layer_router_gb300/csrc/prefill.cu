@@ -9,14 +9,16 @@
 //            tcgen05.mma kind::mxf4nvf4 (block scale, 16-value E4M3 scales in
 //            tensor memory), fp32 accumulators in tensor memory; TMA tile loads
 //            of both operands (one 3-D tensor map spans the whole slot arena, so
-//            every expert record is addressed by its slot), 4-stage mbarrier
-//            pipeline, one warp loading, one warp issuing MMAs, four warps in the
-//            epilogue.  Gate and up share the activation tile and accumulate
-//            into two TMEM accumulators; the epilogue forms silu(g)*u.
-//   K-hq     h quantised to NVFP4 per route, same layout as K-actq;
-//   K-gemm   down projection; the epilogue scales by the routing weight and
-//            adds each route's 128-value row segment into y_acc[token] with
-//            TMA bulk reductions (the weighted combine).
+//            every expert record is addressed by its slot), an mbarrier ring
+//            (4 stages for gate/up, 6 for down), one warp loading, one warp
+//            issuing MMAs, eight warps in the epilogue.  Gate and up share the
+//            activation tile and accumulate into two TMEM accumulators; the
+//            epilogue forms silu(g)*u.
+//   K-hq     h quantised to NVFP4 per route, same layout as K-actq, with each
+//            route's down-epilogue data (weight x G x down scale, token);
+//   K-gemm   down projection, tiles in row-tile-major order; the epilogue
+//            scales by the routing weight and adds each route's 128-value row
+//            segment into y_acc[token] with L2 reductions (the weighted combine).
 // The bf16 shared expert runs through the same GEMM with kind::f16.
 // Experts are walked in act_list order in launch groups of prefill_group
 // experts (0: every expert in one launch per GEMM).
@@ -41,7 +43,6 @@ int cache_n_stage(const expcache* c);
 namespace pf {
 
 constexpr int kTileM = 128, kTileN = 128, kStageKB = 128;  // K bytes per stage and operand row
-constexpr int kStages = 4;
 constexpr int kThreads = 320;  // warp 0: TMA, warp 1: MMA, warps 2..9: epilogue
 constexpr int kEpiWarps = 8;   // two per tensor-memory lane quarter, each half of the columns
 constexpr uint64_t kWaitNs = 2000000000ull;  // no wait lasts longer than 2 s
@@ -54,7 +55,9 @@ struct GemmParams {
   int kstages;  // K / (128 bytes of each operand row)
   // routed experts of this launch: planned experts [g0, g1) (act_list order),
   // their tiles tiles[plan_begin[g0]*mtiles .. plan_begin[g1]*mtiles)
-  const uint32_t* tiles;     // packed (expert index j, m tile, n tile)
+  const uint32_t* tiles;     // gate/up: packed (expert index j, m tile, n tile)
+  const int4* ctab;          // down: column tiles {expert, slot, padded row of column 0, routes}
+  const float2* dcol;        // down: per padded row {weight x G x down scale, token bits}
   const int32_t* plan_e;     // expert id of index j
   const int32_t* plan_slot;  // its cache slot
   const int32_t* plan_begin; // prefix of its 128-route column tiles
@@ -89,7 +92,14 @@ __host__ __device__ __forceinline__ uint32_t tile_pack(int j, int mt, int nt) {
   return ((uint32_t)j << 21) | ((uint32_t)mt << 13) | (uint32_t)nt;
 }
 
-// tile t of a launch -> (m tile, n tile, expert id, slot)
+// Tile orders.  Gate/up: an expert-major table (the 16 row tiles of an expert
+// run side by side and share its activation tile in L2), decoded by tile_info.
+// Down: row-tile-major over the launch's ncols column tiles, t = m * ncols + c,
+// each column tile a record {expert, slot, padded row of column 0, routes}
+// (ctab); so at any time the CTAs add into a few 128-row bands of every
+// token's y_acc row, which stay in L2, instead of into all of y_acc.
+
+// gate/up or shared tile t of a launch -> (m tile, n tile, expert id, slot)
 template <bool ROUTED>
 __device__ __forceinline__ void tile_info(const GemmParams& p, int t, int& mt, int& nt, int& e,
                                           int& slot) {
@@ -111,23 +121,25 @@ __device__ __forceinline__ void tile_info(const GemmParams& p, int t, int& mt, i
 
 // K-plan: the routed experts in act_list order (all hits: the prefill path
 // reads every active expert from a cache slot), their 128-route column tiles,
-// and the tile tables of the gate/up (mt_gu row tiles) and down (mt_dn) GEMMs.
+// the gate/up tile table (mt_gu row tiles per column tile, expert-major) and
+// the column-tile table of the down GEMM.
 // One CTA of 1024 threads, one expert per thread.
 __global__ void __launch_bounds__(1024) k_tile_plan(
     const int32_t* __restrict__ act_list, const int32_t* __restrict__ n_act,
-    const int32_t* __restrict__ offsets, const int32_t* __restrict__ src_slot, int n_slots, int E,
-    int mt_gu, int mt_dn, uint32_t* __restrict__ tiles_gu, uint32_t* __restrict__ tiles_dn,
+    const int32_t* __restrict__ offsets, const int32_t* __restrict__ pad_offsets,
+    const int32_t* __restrict__ src_slot, int n_slots, int E, int mt_gu,
+    uint32_t* __restrict__ tiles_gu, int4* __restrict__ ctab,
     int32_t* __restrict__ plan_e, int32_t* __restrict__ plan_slot,
     int32_t* __restrict__ plan_begin, int32_t* __restrict__ plan_n, int32_t* status) {
   __shared__ int s_w[33];
   const int j = threadIdx.x, lane = j & 31, wid = j >> 5;
   const int hits = n_act[1];
   if (j == 0 && n_act[0] != hits) set_status(status, MOE_ERR_DEVICE);
-  int e = -1, slot = -1, nt = 0;
+  int e = -1, slot = -1, nt = 0, cnt = 0;
   if (j < hits && j < E) {
     e = act_list[j];
     slot = src_slot[e];
-    const int cnt = offsets[e + 1] - offsets[e];
+    cnt = offsets[e + 1] - offsets[e];
     if (slot < 0 || slot >= n_slots) set_status(status, MOE_ERR_DEVICE);
     else nt = (cnt + kTileN - 1) / kTileN;
   }
@@ -160,8 +172,8 @@ __global__ void __launch_bounds__(1024) k_tile_plan(
     plan_begin[j] = begin;
     for (int m = 0; m < mt_gu; ++m)
       for (int c = 0; c < nt; ++c) tiles_gu[(size_t)begin * mt_gu + m * nt + c] = tile_pack(j, m, c);
-    for (int m = 0; m < mt_dn; ++m)
-      for (int c = 0; c < nt; ++c) tiles_dn[(size_t)begin * mt_dn + m * nt + c] = tile_pack(j, m, c);
+    for (int c = 0; c < nt; ++c)
+      ctab[begin + c] = make_int4(e, slot, pad_offsets[e] + c * kTileN, min(kTileN, cnt - c * kTileN));
   }
   if (j == 0) {
     plan_begin[n] = s_w[32];
@@ -171,24 +183,49 @@ __global__ void __launch_bounds__(1024) k_tile_plan(
 
 template <int KIND, int EPI>
 struct Cfg {
+  // gate/up: two A operands (gate and up rows) against one B, two accumulators
   static constexpr bool kDual = (EPI == EPI_GU_ROUTED || EPI == EPI_GU_SHARED);
   static constexpr bool kRouted = (EPI == EPI_GU_ROUTED || EPI == EPI_DOWN_ROUTED);
+  // routed down: row-tile-major order over a table of column tiles (ctab)
+  static constexpr bool kMMajor = (EPI == EPI_DOWN_ROUTED);
   static constexpr bool kNvf4 = (KIND == 0);
   static constexpr int kTileBytes = kTileM * kStageKB;  // 16 KiB
   static constexpr int kSfBytes = kNvf4 ? 2048 : 0;     // 4 atoms of 512 B
   static constexpr int kStageBytes =
       kTileBytes * (kDual ? 3 : 2) + kSfBytes * (kDual ? 3 : 2);
-  static constexpr int kEpiStage = (EPI == EPI_DOWN_ROUTED || EPI == EPI_DOWN_SHARED)
-                                       ? kTileN * kTileM * 4 : 0;  // fp32 [routes][rows]
-  static constexpr int kSmem = 1024 + kStages * kStageBytes + kEpiStage;
+  // a single-A stage is two thirds of a dual one: six of them fit where four dual ones do
+  static constexpr int kStages = kDual ? 4 : 6;
+  static constexpr int kSmem = 1024 + kStages * kStageBytes;
   // tensor memory: accumulators, then per-stage scale-factor columns
   static constexpr uint32_t kAccCols = kDual ? 256 : 128;
   static constexpr uint32_t kSfColsPerStage = kNvf4 ? (kDual ? 48 : 32) : 0;
+  // two accumulators where they fit beside the scale factors, so that a tile's
+  // MMAs never wait for the previous tile's epilogue to read its accumulator
+  static constexpr int kAccBufs = (2 * kAccCols + kStages * kSfColsPerStage <= kTmemCols) ? 2 : 1;
+  static constexpr uint32_t kSfCol0 = kAccCols * kAccBufs;
+  static_assert(kSfCol0 + kStages * kSfColsPerStage <= kTmemCols, "tensor memory");
+  static_assert(kSmem <= 227 * 1024, "shared memory");
 };
 
 // SiLU with the fast exponential and division (a few ulp: far below the
 // tolerance and the rounding-boundary slack of the quantised h)
 __device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.f + __expf(-g)); }
+
+// Down epilogue of one thread: its accumulator row of 64 columns (routes or
+// tokens, ra then rb), each weighted by cs[j] and added into y_acc row cr[j]
+// at yb; a warp instruction adds 32 consecutive rows (one 128-byte reduction
+// in L2).  Columns from nv on are padding.
+__device__ __forceinline__ void add_columns(const uint32_t (&ra)[32], const uint32_t (&rb)[32],
+                                            float* yb, const float* cs, const int* cr, int H,
+                                            int nv) {
+#pragma unroll
+  for (int jj = 0; jj < 32; ++jj)
+    if (jj < nv) ptx::red_add_f32(yb + (size_t)cr[jj] * H, __uint_as_float(ra[jj]) * cs[jj]);
+#pragma unroll
+  for (int jj = 0; jj < 32; ++jj)
+    if (32 + jj < nv)
+      ptx::red_add_f32(yb + (size_t)cr[32 + jj] * H, __uint_as_float(rb[jj]) * cs[32 + jj]);
+}
 
 template <int KIND, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -198,10 +235,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-  __shared__ uint64_t full_bar[kStages], empty_bar[kStages], acc_full, acc_empty;
+  __shared__ uint64_t full_bar[C::kStages], empty_bar[C::kStages];
+  __shared__ uint64_t acc_full[C::kAccBufs], acc_empty[C::kAccBufs];
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
-  __shared__ int s_tlo, s_thi;
+  __shared__ int s_tlo, s_thi, s_cbase, s_ncols;
   __shared__ float col_scale[kTileN];
   __shared__ int col_row[kTileN];
 
@@ -213,18 +251,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (C::kRouted) {
       const int n = p.plan_n[0];
       const int g0 = min(p.g0, n), g1 = min(p.g1, n);
-      s_tlo = p.plan_begin[g0] * p.mtiles;
-      s_thi = p.plan_begin[g1] * p.mtiles;
+      s_cbase = p.plan_begin[g0];
+      s_ncols = p.plan_begin[g1] - s_cbase;
+      s_tlo = C::kMMajor ? 0 : s_cbase * p.mtiles;
+      s_thi = C::kMMajor ? s_ncols * p.mtiles : p.plan_begin[g1] * p.mtiles;
     } else {
+      s_cbase = 0;
+      s_ncols = 1;
       s_tlo = 0;
       s_thi = ((p.T + kTileN - 1) / kTileN) * p.mtiles;
     }
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < C::kStages; ++s) {
       ptx::mbar_init(&full_bar[s], 1);
       ptx::mbar_init(&empty_bar[s], 1);
     }
-    ptx::mbar_init(&acc_full, 1);
-    ptx::mbar_init(&acc_empty, kEpiWarps);
+    for (int b = 0; b < C::kAccBufs; ++b) {
+      ptx::mbar_init(&acc_full[b], 1);
+      ptx::mbar_init(&acc_empty[b], kEpiWarps);
+    }
     ptx::fence_barrier_init();
   }
   if (warp == 1) {
@@ -235,20 +279,51 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = tmem_base;
-  const int tlo = s_tlo, thi = s_thi;
+  const int tlo = s_tlo, thi = s_thi, cbase = s_cbase, ncols = s_ncols;
 
   if (warp == 0) {
     // ================= TMA producer =================
     if (lane == 0) {
       uint32_t g = 0;
-      for (int t = tlo + blockIdx.x; t < thi && !abort_flag; t += gridDim.x) {
-        int mt, nt, e, slot;
-        tile_info<C::kRouted>(p, t, mt, nt, e, slot);
-        int brow = nt * kTileN;  // activation row of the tile
-        if (C::kRouted) brow += p.pad_offsets[e];
+      // The next tile's info is loaded during this tile's stages: for the
+      // gate/up table a chain of three dependent loads (table entry, plan
+      // entry, padded row offset), one link per stage; for the down GEMM one
+      // column-tile record.  Either would otherwise stall the ring at every
+      // tile boundary.
+      int mt = 0, nt = 0, e = 0, slot = 0, brow = 0;
+      const int t0 = tlo + blockIdx.x;
+      if (t0 < thi) {
+        if (C::kMMajor) {
+          const int4 r = p.ctab[cbase + t0 % ncols];
+          mt = t0 / ncols;
+          slot = r.y;
+          brow = r.z;
+        } else {
+          tile_info<C::kRouted>(p, t0, mt, nt, e, slot);
+          brow = nt * kTileN + (C::kRouted ? p.pad_offsets[e] : 0);
+        }
+      }
+      for (int t = t0; t < thi && !abort_flag; t += gridDim.x) {
+        const int tn = t + gridDim.x;
+        uint32_t vn = 0;
+        int mtn = 0, ntn = 0, en = 0, sn = 0, pn = 0;
+        int4 rn = make_int4(0, 0, 0, 0);
+        const int kst = p.kstages;
+        const int arow = mt * kTileM;  // weight rows
         for (int kb = 0; kb < p.kstages; ++kb, ++g) {
-          const int s = g % kStages;
-          const uint32_t ph = (g / kStages) & 1;
+          if (C::kMMajor && tn < thi && kb == 0) rn = p.ctab[cbase + tn % ncols];
+          if (C::kRouted && !C::kMMajor && tn < thi) {  // one link per stage
+            if (kb == 0) vn = p.tiles[tn];
+            if (kb == min(1, kst - 1)) {
+              mtn = (int)((vn >> 13) & 0xFFu);
+              ntn = (int)(vn & 0x1FFFu);
+              en = p.plan_e[vn >> 21];
+              sn = p.plan_slot[vn >> 21];
+            }
+            if (kb == min(2, kst - 1)) pn = p.pad_offsets[en];
+          }
+          const int s = g % C::kStages;
+          const uint32_t ph = (g / C::kStages) & 1;
           if (!ptx::mbar_wait(&empty_bar[s], ph ^ 1, kWaitNs)) {
             set_status(p.status, MOE_ERR_TIMEOUT);
             abort_flag = 1;
@@ -257,27 +332,52 @@ __global__ void __launch_bounds__(kThreads, 1)
           unsigned char* st = smem + (size_t)s * C::kStageBytes;
           ptx::mbar_arrive_expect_tx(&full_bar[s], C::kStageBytes);
           const int kc = C::kNvf4 ? kb * kStageKB : kb * (kStageKB / 2);  // bytes or bf16s
-          if (C::kRouted) {
-            ptx::tma_load_3d(st, &tmA0, kc, mt * kTileM, slot, &full_bar[s]);
-            if (C::kDual)
-              ptx::tma_load_3d(st + C::kTileBytes, &tmA1, kc, mt * kTileM, slot,
-                               &full_bar[s]);
+          // Down: the weights are read once, the activation tiles by every row
+          // tile of their column, and y_acc is added into meanwhile; the cache
+          // policies keep the activations and y_acc in L2 ahead of the weights.
+          const uint64_t pol_w = ptx::l2_evict_first(), pol_a = ptx::l2_evict_last();
+          if (C::kMMajor) {
+            ptx::tma_load_3d_hint(st, &tmA0, kc, arow, slot, &full_bar[s], pol_w);
+          } else if (C::kRouted) {
+            ptx::tma_load_3d(st, &tmA0, kc, arow, slot, &full_bar[s]);
+            if (C::kDual) ptx::tma_load_3d(st + C::kTileBytes, &tmA1, kc, arow, slot, &full_bar[s]);
           } else {
-            ptx::tma_load_2d(st, &tmA0, kc, mt * kTileM, &full_bar[s]);
-            if (C::kDual) ptx::tma_load_2d(st + C::kTileBytes, &tmA1, kc, mt * kTileM, &full_bar[s]);
+            ptx::tma_load_2d(st, &tmA0, kc, arow, &full_bar[s]);
+            if (C::kDual) ptx::tma_load_2d(st + C::kTileBytes, &tmA1, kc, arow, &full_bar[s]);
           }
           unsigned char* bdst = st + C::kTileBytes * (C::kDual ? 2 : 1);
-          ptx::tma_load_2d(bdst, &tmB, kc, brow, &full_bar[s]);
+          if (C::kMMajor) ptx::tma_load_2d_hint(bdst, &tmB, kc, brow, &full_bar[s], pol_a);
+          else ptx::tma_load_2d(bdst, &tmB, kc, brow, &full_bar[s]);
           if (C::kNvf4) {
             // 4 scale atoms (512 B each) per operand: k groups kb*4 .. kb*4+3
             unsigned char* sf = bdst + C::kTileBytes;
             const uint8_t* rec = p.arena + (uint64_t)slot * p.rec_bytes;
             const uint64_t aoff = ((uint64_t)mt * p.kgroups + (uint64_t)kb * 4) * 512;
-            ptx::bulk_load(sf, rec + p.sfa_off0 + aoff, 2048, &full_bar[s]);
-            if (C::kDual) ptx::bulk_load(sf + 2048, rec + p.sfa_off1 + aoff, 2048, &full_bar[s]);
             const uint64_t boff = ((uint64_t)(brow / kTileN) * p.kgroups + (uint64_t)kb * 4) * 512;
-            ptx::bulk_load(sf + (C::kDual ? 4096 : 2048), p.b_scales + boff, 2048, &full_bar[s]);
+            unsigned char* sfb = sf + (C::kDual ? 4096 : 2048);
+            if (C::kMMajor) {
+              ptx::bulk_load_hint(sf, rec + p.sfa_off0 + aoff, 2048, &full_bar[s], pol_w);
+              ptx::bulk_load_hint(sfb, p.b_scales + boff, 2048, &full_bar[s], pol_a);
+            } else {
+              ptx::bulk_load(sf, rec + p.sfa_off0 + aoff, 2048, &full_bar[s]);
+              if (C::kDual) ptx::bulk_load(sf + 2048, rec + p.sfa_off1 + aoff, 2048, &full_bar[s]);
+              ptx::bulk_load(sfb, p.b_scales + boff, 2048, &full_bar[s]);
+            }
           }
+        }
+        if (C::kMMajor) {
+          mt = tn / ncols;
+          slot = rn.y;
+          brow = rn.z;
+        } else if (C::kRouted) {
+          mt = mtn;
+          nt = ntn;
+          e = en;
+          slot = sn;
+          brow = ntn * kTileN + pn;
+        } else if (tn < thi) {
+          tile_info<false>(p, tn, mt, nt, e, slot);
+          brow = nt * kTileN;
         }
       }
     }
@@ -290,7 +390,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       else idesc |= (1u << 4) | (1u << 7) | (1u << 10);            // fp32 D, bf16 A and B
       uint32_t g = 0, it = 0;
       for (int t = tlo + blockIdx.x; t < thi && !abort_flag; t += gridDim.x, ++it) {
-        if (!ptx::mbar_wait(&acc_empty, (it & 1) ^ 1, kWaitNs)) {
+        const int ab = (int)(it % C::kAccBufs);           // accumulator of this tile
+        const uint32_t au = it / C::kAccBufs;              // its earlier uses
+        const uint32_t acc = tmem + (uint32_t)ab * C::kAccCols;
+        if (!ptx::mbar_wait(&acc_empty[ab], (au & 1) ^ 1, kWaitNs)) {
           set_status(p.status, MOE_ERR_TIMEOUT);
           abort_flag = 1;
           break;
@@ -298,8 +401,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_fence_after();
         bool ok = true;
         for (int kb = 0; kb < p.kstages; ++kb, ++g) {
-          const int s = g % kStages;
-          const uint32_t ph = (g / kStages) & 1;
+          const int s = g % C::kStages;
+          const uint32_t ph = (g / C::kStages) & 1;
           if (!ptx::mbar_wait(&full_bar[s], ph, kWaitNs)) {
             set_status(p.status, MOE_ERR_TIMEOUT);
             abort_flag = 1;
@@ -312,7 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t a1 = a0 + C::kTileBytes;
           const uint32_t b = a0 + C::kTileBytes * (C::kDual ? 2 : 1);
           const uint32_t sf = b + C::kTileBytes;
-          const uint32_t sfcol = C::kAccCols + (uint32_t)s * C::kSfColsPerStage;
+          const uint32_t sfcol = C::kSfCol0 + (uint32_t)s * C::kSfColsPerStage;
           if (C::kNvf4) {
             // scale atoms -> tensor memory (4 columns each)
             for (int kk = 0; kk < 4; ++kk) {
@@ -329,23 +432,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool accum = (kb > 0) || (kk > 0);
             if (C::kNvf4) {
               const uint32_t sfb = tmem + sfcol + (C::kDual ? 32 : 16) + kk * 4;
-              ptx::mma_nvf4(tmem, da0, db, idesc, tmem + sfcol + kk * 4, sfb, accum);
+              ptx::mma_nvf4(acc, da0, db, idesc, tmem + sfcol + kk * 4, sfb, accum);
               if (C::kDual) {
                 const uint64_t da1 = ptx::smem_desc(a1 + kk * 32, 16, 1024, 2);
-                ptx::mma_nvf4(tmem + 128, da1, db, idesc, tmem + sfcol + 16 + kk * 4, sfb, accum);
+                ptx::mma_nvf4(acc + 128, da1, db, idesc, tmem + sfcol + 16 + kk * 4, sfb, accum);
               }
             } else {
-              ptx::mma_bf16(tmem, da0, db, idesc, accum);
+              ptx::mma_bf16(acc, da0, db, idesc, accum);
               if (C::kDual) {
                 const uint64_t da1 = ptx::smem_desc(a1 + kk * 32, 16, 1024, 2);
-                ptx::mma_bf16(tmem + 128, da1, db, idesc, accum);
+                ptx::mma_bf16(acc + 128, da1, db, idesc, accum);
               }
             }
           }
           ptx::tc_commit(&empty_bar[s]);  // stage reusable once these MMAs finish
         }
         if (!ok) break;
-        ptx::tc_commit(&acc_full);
+        ptx::tc_commit(&acc_full[ab]);
       }
     }
   } else {
@@ -359,112 +462,140 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = q * 32 + lane;      // weight row within the tile
     const int et = threadIdx.x - 64;    // 0..255
     constexpr int kHalf = kTileN / 2;
-    float* stage_out = reinterpret_cast<float*>(smem + (size_t)kStages * C::kStageBytes);
-    uint32_t it = 0;
-    for (int t = tlo + blockIdx.x; t < thi; t += gridDim.x, ++it) {
-      int mt, nt, e, slot;
-      tile_info<C::kRouted>(p, t, mt, nt, e, slot);
-      int n_valid, col0;
-      if (C::kRouted) {
-        const int cnt = p.offsets[e + 1] - p.offsets[e];
-        n_valid = min(kTileN, cnt - nt * kTileN);
-        col0 = p.pad_offsets[e] + nt * kTileN;  // padded activation row of column 0
-      } else {
-        n_valid = min(kTileN, p.T - nt * kTileN);
-        col0 = nt * kTileN;
+
+    if (C::kMMajor) {
+      // Routed down.  The column data of a tile (combine weight x activation
+      // scale x expert scale, and token, per route) comes precomputed per
+      // padded row (dcol); the next tile's record and column data are loaded
+      // while this tile waits and is reduced, so no chain of loads sits
+      // between two tiles.
+      const int t0 = tlo + blockIdx.x;
+      int4 r = make_int4(0, 0, 0, 0);
+      float2 dc = make_float2(0.f, 0.f);
+      if (t0 < thi) {
+        r = p.ctab[cbase + t0 % ncols];
+        if (et < kTileN) dc = p.dcol[r.z + et];
       }
-      // per-column data (column = route or token)
-      if (et < kTileN) {
-        float sc = 1.f;
-        int rr = col0 + et;
-        if (et < n_valid) {
-          if (EPI == EPI_GU_ROUTED) {
-            sc = p.b_gscale[col0 + et];
-          } else if (EPI == EPI_DOWN_ROUTED) {
-            const int route = p.perm[p.offsets[e] + nt * kTileN + et];
-            sc = p.b_gscale[col0 + et] * p.w[route] * p.gscale[e * 3 + 2];
-            rr = route / p.k;  // token
-          }
+      uint32_t it = 0;
+      for (int t = t0; t < thi; t += gridDim.x, ++it) {
+        const int mt = t / ncols, n_valid = r.w;
+        if (et < kTileN) {
+          col_scale[et] = et < n_valid ? dc.x : 0.f;
+          col_row[et] = __float_as_int(dc.y);
         }
-        col_scale[et] = sc;
-        col_row[et] = rr;
-      }
-      float gg = 1.f, gu = 1.f;
-      if (EPI == EPI_GU_ROUTED) {
-        gg = p.gscale[e * 3 + 0];
-        gu = p.gscale[e * 3 + 1];
-      }
-      asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
-      if (!ptx::mbar_wait(&acc_full, it & 1, kWaitNs)) {
-        set_status(p.status, MOE_ERR_TIMEOUT);
-        abort_flag = 1;
-        break;
-      }
-      ptx::tc_fence_after();
-      const uint32_t lane_addr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(ch * kHalf);
-      if (C::kDual) {
-        // gate/up: h = silu(g) * u formed chunk by chunk (64 values kept), then
-        // the accumulator is released and h is written
-        float hv[kHalf];
-#pragma unroll
-        for (int c = 0; c < kHalf; c += 16) {
-          uint32_t ga[16], ua[16];
-          ptx::tmem_ld_32x32b_x16(lane_addr + c, ga);
-          ptx::tmem_ld_32x32b_x16(lane_addr + 128 + c, ua);
-          ptx::tmem_ld_wait();
-#pragma unroll
-          for (int jj = 0; jj < 16; ++jj) {
-            const float g = __uint_as_float(ga[jj]), u = __uint_as_float(ua[jj]);
-            if (EPI == EPI_GU_ROUTED) {
-              const float G = col_scale[ch * kHalf + c + jj];
-              hv[c + jj] = silu_f(g * gg * G) * (u * gu * G);
-            } else {
-              hv[c + jj] = silu_f(g) * u;
-            }
-          }
+        asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
+        const int tn = t + gridDim.x;
+        int4 rn = r;
+        if (tn < thi) rn = p.ctab[cbase + tn % ncols];
+        const int ab = (int)(it % C::kAccBufs);
+        if (!ptx::mbar_wait(&acc_full[ab], (it / C::kAccBufs) & 1, kWaitNs)) {
+          set_status(p.status, MOE_ERR_TIMEOUT);
+          abort_flag = 1;
+          break;
         }
-        ptx::tc_fence_before();
-        if (lane == 0) ptx::mbar_arrive(&acc_empty);  // the accumulator is free
-#pragma unroll
-        for (int jj = 0; jj < kHalf; ++jj) {
-          const int n = ch * kHalf + jj;
-          if (n < n_valid) {
-            if (EPI == EPI_GU_ROUTED)
-              p.h32[(size_t)(col0 + n) * p.h_ld + mt * kTileM + row] = hv[jj];
-            else
-              p.hs[(size_t)(col0 + n) * p.hs_ld + mt * kTileM + row] = f32_to_bf16_rne(hv[jj]);
-          }
-        }
-      } else {
-        // down: the weighted columns to shared memory, then one bulk
-        // reduce-add per column (route) into y_acc
+        ptx::tc_fence_after();
+        const uint32_t lane_addr = tmem + ((uint32_t)(q * 32) << 16) +
+                                   (uint32_t)ab * C::kAccCols + (uint32_t)(ch * kHalf);
         uint32_t ra[32], rb[32];
         ptx::tmem_ld_32x32b_x32(lane_addr, ra);
         ptx::tmem_ld_32x32b_x32(lane_addr + 32, rb);
         ptx::tmem_ld_wait();
         ptx::tc_fence_before();
-        if (lane == 0) ptx::mbar_arrive(&acc_empty);  // the accumulator is free
-        float* so = stage_out + (size_t)ch * kHalf * kTileM + row;
-        const float* cs = col_scale + ch * kHalf;
-#pragma unroll
-        for (int jj = 0; jj < 32; ++jj) so[jj * kTileM] = __uint_as_float(ra[jj]) * cs[jj];
-#pragma unroll
-        for (int jj = 0; jj < 32; ++jj)
-          so[(32 + jj) * kTileM] = __uint_as_float(rb[jj]) * cs[32 + jj];
-      }
-      if (EPI == EPI_DOWN_ROUTED || EPI == EPI_DOWN_SHARED) {
-        ptx::fence_proxy_async_smem();
+        if (lane == 0) ptx::mbar_arrive(&acc_empty[ab]);  // the accumulator is free
+        float2 dn = dc;
+        if (tn < thi && et < kTileN) dn = p.dcol[rn.z + et];
+        add_columns(ra, rb, p.y_acc + mt * kTileM + row, col_scale + ch * kHalf,
+                    col_row + ch * kHalf, p.H, n_valid - ch * kHalf);
         asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
-        if (et < n_valid) {
-          ptx::bulk_reduce_add_f32(p.y_acc + (size_t)col_row[et] * p.H + mt * kTileM,
-                                   stage_out + et * kTileM, kTileM * 4);
-          ptx::bulk_commit();
-          ptx::bulk_wait_read0();
-        }
+        r = rn;
+        dc = dn;
       }
-      asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
+    } else {
+      uint32_t it = 0;
+      for (int t = tlo + blockIdx.x; t < thi; t += gridDim.x, ++it) {
+        int mt, nt, e, slot;
+        tile_info<C::kRouted>(p, t, mt, nt, e, slot);
+        int n_valid, col0;
+        if (C::kRouted) {
+          const int cnt = p.offsets[e + 1] - p.offsets[e];
+          n_valid = min(kTileN, cnt - nt * kTileN);
+          col0 = p.pad_offsets[e] + nt * kTileN;  // padded activation row of column 0
+        } else {
+          n_valid = min(kTileN, p.T - nt * kTileN);
+          col0 = nt * kTileN;
+        }
+        // per-column data (column = route or token)
+        if (et < kTileN) {
+          float sc = 1.f;
+          int rr = col0 + et;
+          if (et < n_valid) {
+            if (EPI == EPI_GU_ROUTED) sc = p.b_gscale[col0 + et];
+          }
+          col_scale[et] = sc;
+          col_row[et] = rr;
+        }
+        float gg = 1.f, gu = 1.f;
+        if (EPI == EPI_GU_ROUTED) {
+          gg = p.gscale[e * 3 + 0];
+          gu = p.gscale[e * 3 + 1];
+        }
+        asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
+        const int ab = (int)(it % C::kAccBufs);
+        if (!ptx::mbar_wait(&acc_full[ab], (it / C::kAccBufs) & 1, kWaitNs)) {
+          set_status(p.status, MOE_ERR_TIMEOUT);
+          abort_flag = 1;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t lane_addr =
+            tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)ab * C::kAccCols + (uint32_t)(ch * kHalf);
+        if (C::kDual) {
+          // gate/up: h = silu(g) * u formed chunk by chunk (64 values kept), then
+          // the accumulator is released and h is written
+          float hv[kHalf];
+#pragma unroll
+          for (int c = 0; c < kHalf; c += 16) {
+            uint32_t ga[16], ua[16];
+            ptx::tmem_ld_32x32b_x16(lane_addr + c, ga);
+            ptx::tmem_ld_32x32b_x16(lane_addr + 128 + c, ua);
+            ptx::tmem_ld_wait();
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) {
+              const float g = __uint_as_float(ga[jj]), u = __uint_as_float(ua[jj]);
+              if (EPI == EPI_GU_ROUTED) {
+                const float G = col_scale[ch * kHalf + c + jj];
+                hv[c + jj] = silu_f(g * gg * G) * (u * gu * G);
+              } else {
+                hv[c + jj] = silu_f(g) * u;
+              }
+            }
+          }
+          ptx::tc_fence_before();
+          if (lane == 0) ptx::mbar_arrive(&acc_empty[ab]);  // the accumulator is free
+#pragma unroll
+          for (int jj = 0; jj < kHalf; ++jj) {
+            const int n = ch * kHalf + jj;
+            if (n < n_valid) {
+              if (EPI == EPI_GU_ROUTED)
+                p.h32[(size_t)(col0 + n) * p.h_ld + mt * kTileM + row] = hv[jj];
+              else
+                p.hs[(size_t)(col0 + n) * p.hs_ld + mt * kTileM + row] = f32_to_bf16_rne(hv[jj]);
+            }
+          }
+        } else {
+          // shared down: the token columns added into y_acc
+          uint32_t ra[32], rb[32];
+          ptx::tmem_ld_32x32b_x32(lane_addr, ra);
+          ptx::tmem_ld_32x32b_x32(lane_addr + 32, rb);
+          ptx::tmem_ld_wait();
+          ptx::tc_fence_before();
+          if (lane == 0) ptx::mbar_arrive(&acc_empty[ab]);  // the accumulator is free
+          add_columns(ra, rb, p.y_acc + mt * kTileM + row, col_scale + ch * kHalf,
+                      col_row + ch * kHalf, p.H, n_valid - ch * kHalf);
+        }
+        asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
+      }
     }
-    if (EPI == EPI_DOWN_ROUTED || EPI == EPI_DOWN_SHARED) ptx::bulk_wait0();
   }
 
   ptx::tc_fence_before();
@@ -552,9 +683,10 @@ __device__ __forceinline__ size_t scale_word(int row, int kg, int KG) {
 // One fp32 row of K values (K % 256 == 0, K <= KMAX) by one warp into padded
 // row `row` of the tcgen05 layout.  Each load instruction covers 512
 // contiguous bytes (lane l holds float4 j*32 + l), so four lanes share a
-// 16-value block; the row is read once and held in registers.
+// 16-value block; the row is read once and held in registers.  Returns the
+// row's global scale G (on every lane).
 template <int KMAX>
-__device__ __forceinline__ void quant_row_f32(const float* __restrict__ hr, int K, int row,
+__device__ __forceinline__ float quant_row_f32(const float* __restrict__ hr, int K, int row,
                                               uint8_t* __restrict__ codes,
                                               uint8_t* __restrict__ scales,
                                               float* __restrict__ Gr) {
@@ -593,6 +725,7 @@ __device__ __forceinline__ void quant_row_f32(const float* __restrict__ hr, int 
           sc | (s1 << 8) | (s2 << 16) | (s3 << 24);
   }
   if (lane == 0) Gr[row] = G;
+  return G;
 }
 
 // zero padded rows [r0, r1) of a K-wide operand (codes, scale words, G) with
@@ -619,8 +752,10 @@ template <int KMAX>
 __global__ void __launch_bounds__(256) k_quant_h(
     const float* __restrict__ h32, int K, int g0, int g1, const int32_t* __restrict__ plan_e,
     const int32_t* __restrict__ plan_n, const int32_t* __restrict__ offsets,
-    const int32_t* __restrict__ pad_offsets, uint8_t* __restrict__ codes,
-    uint8_t* __restrict__ scales, float* __restrict__ G) {
+    const int32_t* __restrict__ pad_offsets, const int32_t* __restrict__ perm,
+    const float* __restrict__ w, const float* __restrict__ gscale, int k,
+    uint8_t* __restrict__ codes, uint8_t* __restrict__ scales, float* __restrict__ G,
+    float2* __restrict__ dcol) {
   const int n = plan_n[0];
   const int j = g0 + blockIdx.x;
   if (j >= g1 || j >= n) return;
@@ -630,9 +765,19 @@ __global__ void __launch_bounds__(256) k_quant_h(
   const int per = (nrow + gridDim.y - 1) / gridDim.y;
   const int lo = blockIdx.y * per, hi = min(nrow, lo + per);
   const int wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  for (int i = lo + wid; i < min(hi, cnt); i += nw)
-    quant_row_f32<KMAX>(h32 + (size_t)(r0 + i) * K, K, r0 + i, codes, scales, G);
+  const float gsd = gscale[e * 3 + 2];
+  for (int i = lo + wid; i < min(hi, cnt); i += nw) {
+    const float Gi = quant_row_f32<KMAX>(h32 + (size_t)(r0 + i) * K, K, r0 + i, codes, scales, G);
+    if ((threadIdx.x & 31) == 0) {
+      // the down GEMM's column data of this route: combine weight x G x the
+      // expert's down scale (in that order), and the token
+      const int route = perm[offsets[e] + i];
+      dcol[r0 + i] = make_float2(Gi * w[route] * gsd, __int_as_float(route / k));
+    }
+  }
   zero_rows(r0 + max(lo, cnt), r0 + hi, K, codes, scales, G);
+  for (int i = max(lo, cnt) + threadIdx.x; i < hi; i += blockDim.x)
+    dcol[r0 + i] = make_float2(0.f, 0.f);
 }
 
 // K-hq over plain rows: row t of x (fp32, T rows) -> row t, one warp per row
@@ -786,7 +931,7 @@ static moe_status make_map(CUtensorMap* m, const void* base, bool bf16, uint64_t
 // workspace layout for a prefill call on T tokens
 struct PrefillWs {
   size_t rows;  // padded rows
-  size_t xq_codes, xq_scales, xq_G, h32, hq_codes, hq_scales, hq_G, hs, tiles_gu, tiles_dn, plan,
+  size_t xq_codes, xq_scales, xq_G, h32, hq_codes, hq_scales, hq_G, dcol, hs, tiles_gu, ctab, plan,
       total;
   size_t max_ntiles;  // 128-route column tiles of all experts, at most
   PrefillWs(int T, int H, int I, int E, int k, int Is) {
@@ -803,7 +948,8 @@ struct PrefillWs {
     hs = take((size_t)T * Is * 2);
     max_ntiles = ((size_t)T * k + kTileN - 1) / kTileN + (size_t)E;
     tiles_gu = take(max_ntiles * (I / kTileM) * 4);
-    tiles_dn = take(max_ntiles * (H / kTileM) * 4);
+    ctab = take(max_ntiles * 16);  // down: column-tile records
+    dcol = take(rows * 8);
     plan = take(((size_t)3 * (E + 1) + 1) * 4);  // plan_e | plan_slot | plan_begin | plan_n
     total = o + 1024;
   }
@@ -893,7 +1039,7 @@ moe_status prefill_ffn(const moe_ffn_args* a, cudaStream_t s) {
   int32_t *plan_e = plan, *plan_slot = plan + (a->E + 1), *plan_begin = plan + 2 * (a->E + 1),
           *plan_n = plan + 3 * (a->E + 1);
   uint32_t* tiles_gu = (uint32_t*)(ws + W.tiles_gu);
-  uint32_t* tiles_dn = (uint32_t*)(ws + W.tiles_dn);
+  int4* ctab = (int4*)(ws + W.ctab);
   // the tokens, quantised once each into their routes' padded rows; the tile
   // tables of both GEMMs
   {
@@ -902,8 +1048,8 @@ moe_status prefill_ffn(const moe_ffn_args* a, cudaStream_t s) {
                                    a->pad_offsets, ws + W.xq_codes, ws + W.xq_scales,
                                    (float*)(ws + W.xq_G));
     MOE_CHECK_LAUNCH();
-    k_tile_plan<<<1, 1024, 0, s>>>(a->act_list, a->n_act, a->offsets, a->src_slot, n_slots, a->E,
-                                  I / kTileM, H / kTileM, tiles_gu, tiles_dn, plan_e, plan_slot,
+    k_tile_plan<<<1, 1024, 0, s>>>(a->act_list, a->n_act, a->offsets, a->pad_offsets, a->src_slot,
+                                  n_slots, a->E, I / kTileM, tiles_gu, ctab, plan_e, plan_slot,
                                   plan_begin, plan_n, a->status);
     MOE_CHECK_LAUNCH();
   }
@@ -929,11 +1075,13 @@ moe_status prefill_ffn(const moe_ffn_args* a, cudaStream_t s) {
     const int ng = (g1 < max_act ? g1 : max_act) - g0;
     auto* kq = I <= 2048 ? k_quant_h<2048> : k_quant_h<kQuantHMaxK>;
     kq<<<dim3(ng, 4), 256, 0, s>>>((const float*)(ws + W.h32), I, g0, g1, plan_e, plan_n,
-                                  a->offsets, a->pad_offsets, ws + W.hq_codes, ws + W.hq_scales,
-                                  (float*)(ws + W.hq_G));
+                                  a->offsets, a->pad_offsets, a->perm, a->w, a->gscale, a->k,
+                                  ws + W.hq_codes, ws + W.hq_scales, (float*)(ws + W.hq_G),
+                                  (float2*)(ws + W.dcol));
     MOE_CHECK_LAUNCH();
     // down, weighted, added into y_acc
-    gp.tiles = tiles_dn;
+    gp.ctab = ctab;
+    gp.dcol = (const float2*)(ws + W.dcol);
     gp.mtiles = H / kTileM;
     gp.kstages = (I / 2) / kStageKB;
     gp.kgroups = I / 64;
