@@ -609,23 +609,44 @@ def bench_multilayer(args, torch, moe, gen, gd, dev, name, link_gbs):
     ms = sum(a.elapsed_time(b) for a, b in ev) / steps
     for l in range(L):
         assert layers[l].read_status() == 0
-    # gather pass: explicit calls with events around each fill
-    exs = [ExplicitLayer(torch, moe, dw, l, T) for l in range(L)]
+    # gather pass: the same forwards, with the layer timing hook's events at
+    # every launch step of each layer; a gather's time is the interval that
+    # ends at its own mark (the mark before it closes the permutation or the
+    # previous group's down kernel)
+    S = dw.cache.n_stage
+    groups = (min(T * wl.k, wl.E) + S - 1) // S if S > 0 else 1
+    first = 2 if T <= 8 else 3  # marks before the first group: start, router (+ permutation)
+    marks = first + groups * (3 if S > 0 else 2) + (1 if groups > 1 else 0)
+    hev = [[torch.cuda.Event(enable_timing=True) for _ in range(marks)] for _ in range(L)]
+    for e in (e for row in hev for e in row):  # torch creates the CUDA event on its first record
+        e.record(stream)
+    torch.cuda.synchronize()
+    for l in range(L):
+        moe.moe_layer_set_timing(layers[l].handle, [e.cuda_event for e in hev[l]])
+    from routed_expert_layer_router_gb300.layer import device_view
+    nact = [moe.moe_layer_debug_ptrs(layers[l].handle)["n_act"] for l in range(L)]
     fill_ms, miss, act = 0.0, 0, 0
-    yy = torch.empty((T, wl.H), dtype=torch.bfloat16, device=dev)
-    for j in range(steps):
+    part_ms = [0.0] * (marks - 1)  # per interval between marks, summed over layers and steps
+    hook_ms = 0.0                  # whole steps of this pass
+    for j in range(steps if S > 0 else 0):
         flush()
+        fwd(args.warmup + j)
+        torch.cuda.synchronize()
+        hook_ms += hev[0][0].elapsed_time(hev[L - 1][marks - 1])
         for l in range(L):
-            evf = _events(torch, exs[l].groups)
-            exs[l].step(xs[args.warmup + j, l].data_ptr(), yy.data_ptr(), sp, ev_fill=evf)
-            torch.cuda.synchronize()
-            nm = int(exs[l].b["n_miss"].item())
-            na = int(exs[l].b["n_act"][0].item())
-            miss += nm
+            for i in range(1, marks):
+                part_ms[i - 1] += hev[l][i - 1].elapsed_time(hev[l][i])
+            for g in range(groups):
+                i = first + g * 3
+                fill_ms += hev[l][i - 1].elapsed_time(hev[l][i])
+        for l in range(L):
+            # n_act of the layer's last forward: [active, hits]
+            na, nh = (int(v) for v in device_view(nact[l], (2,), torch.int32).tolist())
             act += na
-            used = (nm + dw.cache.n_stage - 1) // max(dw.cache.n_stage, 1)
-            fill_ms += sum(evf[g][0].elapsed_time(evf[g][1]) for g in range(min(used, len(evf))))
-        assert all(int(e.b["status"].item()) == 0 for e in exs)
+            miss += na - nh
+    for l in range(L):
+        moe.moe_layer_set_timing(layers[l].handle, [])
+        assert layers[l].read_status() == 0
     rb = gen.record_bytes(wl.H, wl.I)
     gather_gbs = miss * rb / (fill_ms * 1e-3) / 1e9 if fill_ms > 0 else 0.0
     res = {
@@ -645,6 +666,11 @@ def bench_multilayer(args, torch, moe, gen, gd, dev, name, link_gbs):
                      "peak_source": "measured pinned host->device cudaMemcpyAsync (1 GiB)"},
         "host_records": "one host copy per expert id, shared by the layers",
     }
+    if S > 0 and steps > 0:
+        # the gather pass's own step time and its launch-step intervals, per
+        # layer (us): router (+ permutation), then per group gather, gate/up, down
+        res["gather_pass"] = {"ms_per_step": round(hook_ms / steps, 4),
+                              "us_per_layer": [round(v * 1e3 / (steps * L), 1) for v in part_ms]}
     dw.close()
     return res
 

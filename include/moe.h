@@ -360,7 +360,7 @@ moe_status moe_layer_debug_ptrs(const moe_layer* l, const int32_t** ids, const f
  * gather, then the gate/up and the down kernel (decode) or the whole FFN
  * (prefill), then the combine (when it is a kernel of its own).  So the caller
  * can time each kernel of the layer's own sequence.
- * n = 0 clears the hook.  n > 16 is MOE_ERR_INVALID_ARG. */
+ * n = 0 clears the hook.  n > 32 is MOE_ERR_INVALID_ARG. */
 moe_status moe_layer_set_timing(moe_layer* l, void* const* events, int n);
 /* Synchronises `stream`, returns the layer's sticky device status in
  * *status_out and clears it. */

@@ -135,7 +135,7 @@ struct moe_layer {
   size_t ffn_ws_bytes;
   int last_T;
   // timing hook: events recorded at the forward's launch boundaries
-  cudaEvent_t ev[16];
+  cudaEvent_t ev[32];
   int n_ev, ev_i;
   cudaStream_t ev_stream;
 };
@@ -375,7 +375,7 @@ MOE_API moe_status moe_layer_debug_ptrs(const moe_layer* l, const int32_t** ids,
 }
 
 MOE_API moe_status moe_layer_set_timing(moe_layer* l, void* const* events, int n) {
-  if (!l || n < 0 || n > 16 || (n > 0 && !events)) return MOE_ERR_INVALID_ARG;
+  if (!l || n < 0 || n > 32 || (n > 0 && !events)) return MOE_ERR_INVALID_ARG;
   for (int i = 0; i < n; ++i) l->ev[i] = (cudaEvent_t)events[i];
   l->n_ev = n;
   return MOE_OK;

@@ -79,6 +79,18 @@ __global__ void __launch_bounds__(kGatherThreads) k_gather(
 
 __global__ void k_set_table(int32_t* table_entry, int slot) { *table_entry = slot; }
 
+// One 16-byte read per 4 KiB page of the mapped host arena.  The device's
+// first read of a host page is slow: on the 16-layer stack a step whose misses
+// read records never read before took up to ten times as long as the same
+// step repeated.  The cache pays that once, at creation.
+constexpr uint64_t kTouchStride = 4096;
+__global__ void __launch_bounds__(256) k_touch_host(const uint8_t* __restrict__ host,
+                                                    uint64_t pages) {
+  for (uint64_t i = (uint64_t)blockIdx.x * 256 + threadIdx.x; i < pages;
+       i += (uint64_t)gridDim.x * 256)
+    (void)ldg_stream(host + i * kTouchStride);
+}
+
 moe_status launch_lookup(const LookupArgs& a, int E, const int32_t* counts, int32_t* status,
                          cudaStream_t s);
 
@@ -139,6 +151,13 @@ MOE_API moe_status expcache_create(const expcache_desc* d, expcache** out) {
                                    sizeof(int64_t) * (size_t)d->L * d->E,
                                    cudaMemcpyHostToDevice) != cudaSuccess)
       st = MOE_ERR_CUDA;
+    // the records are multiples of 16 bytes, so every read below ends inside the arena
+    const uint64_t bytes = c->host_records * c->rec_bytes;
+    if (st == MOE_OK && bytes > 0) {
+      k_touch_host<<<kSMs * 8, 256>>>(c->host_dev, (bytes + kTouchStride - 1) / kTouchStride);
+      if (cudaGetLastError() != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess)
+        st = MOE_ERR_CUDA;
+    }
   }
   if (st != MOE_OK) {
     cudaGetLastError();
