@@ -67,6 +67,9 @@ def lib():
         L.oracle_layer_forward.restype = i32
         L.oracle_set_defect.argtypes = [i32]
         L.oracle_quant_flip_delta.argtypes = [vp, i32, vp]
+        L.oracle_cache_policy_step.argtypes = [i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp,
+                                               vp, vp, vp]
+        L.oracle_cache_policy_step.restype = i32
         _lib = L
         try:
             openmp = "omp_get_num_threads" in open(_SO, "rb").read().decode("latin1")
@@ -225,3 +228,35 @@ def layer_forward(x, H, I, E, k, Wr, bias, records, g, shared_w=None, mode=0,
     if rc:
         raise ValueError("oracle_layer_forward: a selected expert has no record")
     return (y, ids, w, p, bound) if return_bound else (y, ids, w, p)
+
+
+class CachePolicy:
+    """The adaptive cache's state for all layers, stepped by the oracle's
+    policy (oracle_cache_policy_step): table [L,E] (slot or -1), cnt and last
+    [L,E], stamp [L], events, free [n_cache]."""
+
+    def __init__(self, L, E, n_cache, layer_slots, K, table):
+        self.L, self.E, self.K = L, E, K
+        self.layer_slots = [int(v) for v in layer_slots]
+        self.table = np.ascontiguousarray(table, dtype=np.int32).reshape(L, E).copy()
+        self.cnt = np.zeros((L, E), np.uint32)
+        self.last = np.zeros((L, E), np.uint32)
+        self.stamp = np.zeros(L, np.uint32)
+        self.events = np.zeros(1, np.uint32)
+        self.free = np.zeros(n_cache, np.uint8)
+        for l in range(L):
+            used = set(int(s) for s in self.table[l] if s >= 0)
+            for s in range(self.layer_slots[l], self.layer_slots[l + 1]):
+                if s not in used:
+                    self.free[s] = 1
+
+    def step(self, layer, counts):
+        """One forward of `layer` with routes counts[E]; returns the misses'
+        promoted slots (-1 = staged) in ascending expert id."""
+        counts = np.ascontiguousarray(counts, dtype=np.int32)
+        prom = np.zeros(self.E, np.int32)
+        n = lib().oracle_cache_policy_step(
+            self.L, self.E, layer, self.layer_slots[layer], self.layer_slots[layer + 1], self.K,
+            _p(self.table), _p(self.cnt), _p(self.last), _p(self.stamp), _p(self.events),
+            _p(self.free), _p(counts), _p(prom))
+        return prom[:n].copy()

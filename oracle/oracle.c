@@ -24,6 +24,10 @@
  *      q = e2m1_rne_sat(v / (s_b G)), all in IEEE fp32 with correctly
  *      rounded division; the shared expert's h is rounded to bf16.
  *   7. cache residency is not an input: the output depends on (x, weights).
+ *   8. the adaptive cache's bookkeeping ("Project Maya" page, sections "How
+ *      'most-used' is measured", "Promotion on every miss, eviction at the
+ *      boundary" and "VRAM: one partition per layer"), an integer state
+ *      machine simulated forward by forward (oracle_cache_policy_step).
  * Compiled with -ffp-contract=off so fp32 steps are single roundings.
  */
 #include <math.h>
@@ -536,4 +540,74 @@ ORC_API int oracle_layer_forward(const uint16_t* x, int T, int H, int I, int E, 
   if (p_out) memcpy(p_out, p, sizeof(double) * (size_t)T * k);
   free(ids); free(w); free(p); free(xd); free(xq); free(xf); free(o);
   return 0;
+}
+
+/* ------------------------------------------------------- adaptive cache policy */
+
+/* One layer forward of the adaptive expert cache ("Project Maya" page).
+ * State (caller-owned, all layers): table[L*E] slot or -1; cnt[L*E] decayed
+ * route counts; last[L*E] the layer-forward number of the expert's latest
+ * route (0 = never); stamp[L] forwards of each layer so far; *events route
+ * events since the last halving; freeslot[n_cache] 1 = a free (spare) slot.
+ * Layer `layer` owns cache slots [slot_lo, slot_hi).  counts[E] = this
+ * forward's routes per expert.  In this order:
+ *   1. lookup: the active experts (counts > 0) not in the table are the
+ *      misses, in ascending id;
+ *   2. promotion on the miss: miss i takes the i-th lowest free slot of the
+ *      layer, while there is one, and is resident from then on
+ *      (promoted[i] = that slot, else -1: it goes through a staging slot);
+ *   3. counts: each route adds 1, capped at 2^24; the expert's last = this
+ *      forward's number; every 32,768 route events (counted over all layers,
+ *      checked after a forward) every count of every layer is halved;
+ *   4. boundary: while the layer has fewer than K free slots, its resident
+ *      with the smallest (count, last, id) is evicted and its slot is free.
+ * Returns the number of misses. */
+ORC_API int oracle_cache_policy_step(int L, int E, int layer, int slot_lo, int slot_hi, int K,
+                                     int32_t* table, uint32_t* cnt, uint32_t* last,
+                                     uint32_t* stamp, uint32_t* events, uint8_t* freeslot,
+                                     const int32_t* counts, int32_t* promoted) {
+  int32_t* tab = table + (size_t)layer * E;
+  uint32_t* c = cnt + (size_t)layer * E;
+  uint32_t* ls = last + (size_t)layer * E;
+  int n_miss = 0;
+  for (int e = 0; e < E; ++e) {
+    if (counts[e] <= 0 || tab[e] >= 0) continue;
+    int slot = -1;
+    for (int s = slot_lo; s < slot_hi; ++s)
+      if (freeslot[s]) { slot = s; break; }
+    if (slot >= 0) {
+      freeslot[slot] = 0;
+      tab[e] = slot;
+    }
+    promoted[n_miss++] = slot;
+  }
+  const uint32_t now = ++stamp[layer];
+  uint64_t routes = 0;
+  for (int e = 0; e < E; ++e) {
+    if (counts[e] <= 0) continue;
+    routes += (uint64_t)counts[e];
+    uint64_t v = (uint64_t)c[e] + (uint64_t)counts[e];
+    c[e] = v > (1u << 24) ? (1u << 24) : (uint32_t)v;
+    ls[e] = now;
+  }
+  *events += (uint32_t)routes;
+  if (*events >= 32768u) {
+    for (size_t i = 0; i < (size_t)L * E; ++i) cnt[i] >>= 1;
+    *events = 0;
+  }
+  for (;;) {
+    int n_free = 0;
+    for (int s = slot_lo; s < slot_hi; ++s) n_free += freeslot[s] != 0;
+    if (n_free >= K) break;
+    int victim = -1;
+    for (int e = 0; e < E; ++e) {
+      if (tab[e] < 0) continue;
+      if (victim < 0 || c[e] < c[victim] || (c[e] == c[victim] && ls[e] < ls[victim]))
+        victim = e;  /* ascending e: the lowest id wins the remaining ties */
+    }
+    if (victim < 0) break;
+    freeslot[tab[victim]] = 1;
+    tab[victim] = -1;
+  }
+  return n_miss;
 }
