@@ -58,7 +58,7 @@ def _hot_set(wl: gen.Workload, layer: int, bias_rank, saliency_order):
 def build(wl: gen.Workload, layers: int | None = None, T_max: int | None = None,
           n_stage: int | None = None, saliency_order=None, prefill_min_tokens: int | None = None,
           alias_host_records: bool = False, resident=None, slot_alias: int = 0,
-          stream=None, prefill_group: int | None = None) -> DeviceWorkload:
+          stream=None, prefill_group: int | None = None, spares: int = 0) -> DeviceWorkload:
     """Device-resident layer(s) of workload `wl`.
 
     layers: how many of the workload's layers to build (default: all).
@@ -67,6 +67,10 @@ def build(wl: gen.Workload, layers: int | None = None, T_max: int | None = None,
     alias_host_records: store one host copy per expert id shared by all layers
       (the host-index table maps every layer to it) when host memory is short;
       the records then repeat across layers for both the GPU and the oracle.
+    spares: > 0 turns on the adaptive cache: each layer's slot run gets that
+      many free slots beyond its residents, every expert has a host record
+      (any of them can be evicted and gathered again), and the cache's
+      policy keeps that many spares per layer.
     """
     L = wl.layers if layers is None else layers
     E, H, I, k = wl.E, wl.H, wl.I, wl.k
@@ -90,9 +94,13 @@ def build(wl: gen.Workload, layers: int | None = None, T_max: int | None = None,
     else:
         resident = [sorted(int(e) for e in r) for r in resident]
     n_res = [len(r) for r in resident]
-    layer_slots = np.concatenate([[0], np.cumsum(n_res)]).astype(np.int32)
+    layer_slots = np.concatenate([[0], np.cumsum([n + spares for n in n_res])]).astype(np.int32)
     n_cache = int(layer_slots[-1])
-    miss_max = max(E - n for n in n_res)
+    miss_max = E if spares > 0 else max(E - n for n in n_res)
+    # experts with a host record in layer l: the non-resident ones, or all of
+    # them under the adaptive policy
+    hosted = [list(range(E)) if spares > 0 else [e for e in range(E) if e not in set(resident[l])]
+              for l in range(L)]
     if n_stage is None:
         n_stage = min(miss_max, T_max * k) if miss_max > 0 else 0
 
@@ -101,23 +109,19 @@ def build(wl: gen.Workload, layers: int | None = None, T_max: int | None = None,
     if miss_max > 0:
         host_index = np.full((L, E), -1, np.int64)
         if alias_host_records:
-            ids = sorted(set(e for l in range(L) for e in range(E) if e not in set(resident[l])))
+            ids = sorted(set(e for l in range(L) for e in hosted[l]))
             pos = {e: i for i, e in enumerate(ids)}
             for l in range(L):
-                rs = set(resident[l])
-                for e in range(E):
-                    if e not in rs:
-                        host_index[l, e] = pos[e]
+                for e in hosted[l]:
+                    host_index[l, e] = pos[e]
             host_arena = HostArena(len(ids), rb)
             fill_list = [(0, e, pos[e]) for e in ids]
         else:
             fill_list = []
             for l in range(L):
-                rs = set(resident[l])
-                for e in range(E):
-                    if e not in rs:
-                        host_index[l, e] = len(fill_list)
-                        fill_list.append((l, e, len(fill_list)))
+                for e in hosted[l]:
+                    host_index[l, e] = len(fill_list)
+                    fill_list.append((l, e, len(fill_list)))
             host_arena = HostArena(len(fill_list), rb)
         # generate on the device in batches and copy down into the arena
         batch = 16
@@ -146,6 +150,8 @@ def build(wl: gen.Workload, layers: int | None = None, T_max: int | None = None,
             if slot_alias == 0 or j < slot_alias:
                 gen.dev_expert_record(wl.seed, rec_layer[l], e, H, I, cache.slot_ptr(slot), sp)
             cache.set_resident(l, e, slot, s)
+    if spares > 0:
+        cache.set_policy(spares)
 
     w_router, gscale, gscale_host, bias, shared, mls = [], [], [], [], [], []
     pmin = prefill_min_tokens if prefill_min_tokens is not None else (

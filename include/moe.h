@@ -171,13 +171,17 @@ void* expcache_slot_ptr(const expcache* c, int s);
 const int32_t* expcache_slot_table(const expcache* c);
 /* Marks (layer, expert) resident in cache slot `slot` (the caller has written
  * the record there, e.g. with cudaMemcpyAsync on the same stream), or not
- * resident when slot == -1.  Stream-ordered table write. */
+ * resident when slot == -1.  Stream-ordered table write.  MOE_ERR_UNSUPPORTED
+ * once the adaptive policy is on (it owns the table). */
 moe_status expcache_set_resident(expcache* c, int layer, int expert, int slot, void* stream);
 
 /* Wide-read gather: for list entries i in [first, first + max_count) with
- * i < *d_n, copies the host record of (layer, d_expert_ids[i]) into cache
- * slot d_dst_slots[i] (and marks it resident), or, when d_dst_slots is NULL,
- * into staging slot n_cache_slots + (i mod n_stage).  The copy is done by
+ * i < *d_n, copies the host record of (layer, d_expert_ids[i]) into slot
+ * d_dst_slots[i] - a cache slot of the layer (which it marks resident, unless
+ * the adaptive policy is on: that owns the table) or a staging slot (no table
+ * change) - or, when d_dst_slots is NULL, into staging
+ * slot n_cache_slots + (i mod n_stage).  Any other destination sets
+ * MOE_ERR_DEVICE in *status.  The copy is done by
  * thread blocks reading the mapped host memory with 16-byte loads.  The list
  * and its length stay on the device (no host synchronisation), so the call
  * can be captured in a CUDA graph. */
@@ -196,6 +200,46 @@ moe_status expcache_fill(expcache* c, int layer, const int32_t* d_expert_ids, co
 moe_status expcache_lookup(const expcache* c, int layer, const int32_t* counts, int32_t* src_slot,
                            int32_t* act_list, int32_t* n_act, int32_t* miss_ids, int32_t* n_miss,
                            int32_t* status, void* stream);
+
+/* Adaptive cache ("Project Maya" page, sections "How 'most-used' is
+ * measured" and "Promotion on every miss, eviction at the boundary").
+ * expcache_set_policy turns it on for every layer: a decayed route count and
+ * the number of its latest forward per (layer, expert), all zero, and as free
+ * ("spare") slots those of each layer's run that its table row does not use.
+ * Needs per-layer slot runs (layer_slots) and spares_per_layer >= 0, else
+ * MOE_ERR_UNSUPPORTED / MOE_ERR_INVALID_ARG.  Synchronous; calling it again
+ * resets the state from the current table.
+ *
+ * expcache_policy_step, for one forward of `layer`, after expcache_lookup on
+ * the same stream (its counts, src_slot, n_act, miss_ids, n_miss are the
+ * lookup's arrays):
+ *   1. promotion: the misses, in ascending id, take the layer's free slots in
+ *      ascending slot order and are resident from then on (table, src_slot
+ *      and, when meta is given, the slot field of the compact expert records
+ *      meta[2 a] = {expert, slot, first route, routes}, a = n_act[1] + i);
+ *      miss_dst[i] (device, >= E entries) = the slot miss i is to be gathered
+ *      into: its cache slot, or the staging slot the lookup gave it;
+ *   2. counts: each route adds 1 to its expert's count, capped at 2^24, and
+ *      sets its latest forward; every 32,768 route events (over all layers,
+ *      checked once per step) every count of every layer is halved;
+ *   3. boundary: while the layer has fewer than spares_per_layer free slots,
+ *      its resident with the smallest (count, latest forward, id) is evicted
+ *      (its slot is free; the record stays until a promotion overwrites it,
+ *      which the stream orders after this forward's reads).
+ * Then expcache_fill(..., d_dst_slots = miss_dst, ...) gathers the misses.
+ * One CTA; MOE_ERR_UNSUPPORTED when the policy is off. */
+moe_status expcache_set_policy(expcache* c, int spares_per_layer);
+moe_status expcache_policy_step(expcache* c, int layer, const int32_t* counts, int32_t* src_slot,
+                                const int32_t* n_act, const int32_t* miss_ids,
+                                const int32_t* n_miss, int32_t* miss_dst, void* meta,
+                                void* stream);
+/* The policy's device state (read only; NULL before expcache_set_policy):
+ * cnt and last [L][E] uint32, stamp [L + 1] uint32 (forwards per layer, then
+ * the route events since the last halving), freeslot [n_cache_slots] int32
+ * (1 = free); *spares = spares_per_layer, or -1 when the policy is off. */
+moe_status expcache_policy_state(const expcache* c, int* spares, const uint32_t** cnt,
+                                 const uint32_t** last, const uint32_t** stamp,
+                                 const int32_t** freeslot);
 
 /* ------------------------------------------------------------- expert FFN
  * For each route p (p-th route of the expert-sorted order) of the active

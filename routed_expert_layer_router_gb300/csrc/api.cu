@@ -14,6 +14,7 @@ int cache_E(const expcache* c);
 int cache_L(const expcache* c);
 int cache_H(const expcache* c);
 int cache_I(const expcache* c);
+bool cache_has_policy(const expcache* c);
 size_t decode_workspace_bytes(int T, int I, int k, int Is);
 moe_status decode_ffn(const moe_ffn_args* a, cudaStream_t s, const DecodeFuse& fz);
 moe_status decode_setup();
@@ -63,7 +64,7 @@ MOE_API const char* moe_status_string(moe_status s) {
   }
 }
 
-MOE_API int moe_abi_version(void) { return 2; }
+MOE_API int moe_abi_version(void) { return 3; }
 
 static moe_status ensure_setup() {
   static int done = 0;
@@ -131,6 +132,7 @@ struct moe_layer {
   float *o_route, *o_shared, *y_acc;
   void* route_ctl;
   int4* act_meta;  // compact per-expert records of the small-route path
+  int32_t* miss_dst;  // adaptive cache: the slot each miss is gathered into
   void* ffn_ws;
   size_t ffn_ws_bytes;
   int last_T;
@@ -183,7 +185,8 @@ MOE_API moe_status moe_layer_create(const moe_layer_desc* d, moe_layer** out) {
       (size_t)E * 32,     /* act_meta */
       prefill ? (size_t)T * H * 4 : 0, /* y_acc */
       l->ffn_ws_bytes,
-      kRouteCtlBytes + kTileCtlBytes /* route_ctl, then the combine's tile counters */};
+      kRouteCtlBytes + kTileCtlBytes, /* route_ctl, then the combine's tile counters */
+      (size_t)E * 4       /* miss_dst */};
   const int n = (int)(sizeof(sizes) / sizeof(sizes[0]));
   size_t total = 0;
   for (int i = 0; i < n; ++i) total += align256(sizes[i]);
@@ -194,7 +197,7 @@ MOE_API moe_status moe_layer_create(const moe_layer_desc* d, moe_layer** out) {
   }
   l->ws_bytes = total;
   uint8_t* p = (uint8_t*)l->ws;
-  void* ptrs[21];
+  void* ptrs[22];
   for (int i = 0; i < n; ++i) {
     ptrs[i] = sizes[i] ? p : nullptr;
     p += align256(sizes[i]);
@@ -220,6 +223,7 @@ MOE_API moe_status moe_layer_create(const moe_layer_desc* d, moe_layer** out) {
   l->y_acc = (float*)ptrs[18];
   l->ffn_ws = ptrs[19];
   l->route_ctl = ptrs[20];
+  l->miss_dst = (int32_t*)ptrs[21];
   if (cudaMemset(l->ws, 0, total) != cudaSuccess) {
     cudaFree(l->ws);
     free(l);
@@ -297,6 +301,15 @@ MOE_API moe_status moe_layer_forward(moe_layer* l, const void* x, int T, void* y
   }
   if (st != MOE_OK) return st;
   layer_mark(l);
+  // adaptive cache: promotions, counts and the boundary's evictions, before
+  // the misses are gathered (into their promoted or staging slots)
+  const bool policy = cache_has_policy(d.cache);
+  if (policy) {
+    if ((st = expcache_policy_step(d.cache, d.layer, l->counts, l->src_slot, l->n_act, l->miss_ids,
+                                   l->n_miss, l->miss_dst, (void*)act_meta, stream)) != MOE_OK)
+      return st;
+    layer_mark(l);
+  }
 
   const int n_stage = cache_n_stage(d.cache);
   const int max_miss = T * d.k < d.E ? T * d.k : d.E;
@@ -324,8 +337,8 @@ MOE_API moe_status moe_layer_forward(moe_layer* l, const void* x, int T, void* y
   for (int g = 0; g < groups; ++g) {
     if (n_stage > 0) {
       int cnt = S < max_miss - g * S ? S : max_miss - g * S;
-      if ((st = expcache_fill(d.cache, d.layer, l->miss_ids, l->n_miss, g * S, cnt, nullptr,
-                              l->status, stream)) != MOE_OK)
+      if ((st = expcache_fill(d.cache, d.layer, l->miss_ids, l->n_miss, g * S, cnt,
+                              policy ? l->miss_dst : nullptr, l->status, stream)) != MOE_OK)
         return st;
       layer_mark(l);
     }

@@ -24,6 +24,13 @@ struct expcache {
   const uint8_t* host_dev;   // device-side address of the host arena (or NULL)
   uint64_t host_records;
   int64_t* host_index_dev;   // device [L][E] (or NULL)
+  bool partitioned;          // created with per-layer slot runs
+  // adaptive policy (expcache_set_policy), all device; spares < 0: off
+  int spares;
+  uint32_t* cnt;             // [L][E] decayed route counts
+  uint32_t* last;            // [L][E] layer-forward number of the latest route
+  uint32_t* stamp;           // [L] forwards of each layer, then [L] = route events
+  int32_t* freeslot;         // [n_cache] 1 = free (a spare)
 };
 
 namespace moe {
@@ -49,8 +56,11 @@ __global__ void __launch_bounds__(kGatherThreads) k_gather(
   const int64_t hr = host_index ? host_index[e] : -1;
   int slot;
   if (dst_slots) {
+    // a cache slot of this layer, or a staging slot (a miss the adaptive
+    // policy could not promote)
     slot = dst_slots[i];
-    if (slot < slot_lo || slot >= slot_hi) slot = -1;
+    const bool staging = n_stage > 0 && slot >= n_cache && slot < n_cache + n_stage;
+    if (!staging && (slot < slot_lo || slot >= slot_hi)) slot = -1;
   } else {
     slot = n_stage > 0 ? n_cache + (i % n_stage) : -1;
   }
@@ -74,10 +84,140 @@ __global__ void __launch_bounds__(kGatherThreads) k_gather(
     for (int u = 0; u < kGatherUnroll; ++u) d4[w + u * stride] = v[u];
   }
   for (; w < n16; w += stride) d4[w] = ldg_stream(s4 + w);
-  if (dst_slots && blockIdx.x == 0 && threadIdx.x == 0) table_row[e] = slot;
+  if (dst_slots && table_row && slot < n_cache && blockIdx.x == 0 && threadIdx.x == 0)
+    table_row[e] = slot;
 }
 
 __global__ void k_set_table(int32_t* table_entry, int slot) { *table_entry = slot; }
+
+// ---- K-policy: the adaptive cache ("Project Maya" page: "How 'most-used' is
+// measured", "Promotion on every miss, eviction at the boundary") --------------
+// One layer forward, after the lookup (one CTA, a thread per expert):
+//   1. promotion: the lookup's misses, in ascending id, take the layer's free
+//      slots in ascending order and are resident from then on; the others keep
+//      their staging slot (miss_dst[i] = where miss i is gathered);
+//   2. counts: +1 per route, capped at 2^24; last = this forward's number;
+//      every 32,768 route events (all layers) every count is halved;
+//   3. boundary: while fewer than `spares` slots are free, the resident with
+//      the smallest (count, last, id) is evicted.
+struct PolicyArgs {
+  int L, E, layer, slot_lo, slot_hi, spares;
+  int32_t* table_row;
+  uint32_t *cnt, *last, *stamp;  // stamp[L] = route events
+  int32_t* freeslot;
+  const int32_t* counts;
+  int32_t* src_slot;
+  const int32_t *n_act, *miss_ids, *n_miss;
+  int32_t* miss_dst;
+  int4* meta;  // the layer's compact expert records, or nullptr
+};
+
+constexpr int kPolicyThreads = 1024;
+constexpr uint32_t kCountCap = 1u << 24;
+constexpr uint32_t kHalveEvents = 32768;
+
+// (key, id) minimum over the CTA; every thread gets the winner's id (-1: none)
+__device__ int block_argmin(uint64_t key, int id, uint64_t* s_key, int* s_id) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  for (int o = 16; o > 0; o >>= 1) {
+    const uint64_t k2 = __shfl_down_sync(0xFFFFFFFFu, key, o);
+    const int i2 = __shfl_down_sync(0xFFFFFFFFu, id, o);
+    if (k2 < key || (k2 == key && (unsigned)i2 < (unsigned)id)) { key = k2; id = i2; }
+  }
+  if (lane == 0) { s_key[wid] = key; s_id[wid] = id; }
+  __syncthreads();
+  if (wid == 0) {
+    key = lane < (int)(blockDim.x >> 5) ? s_key[lane] : ~0ull;
+    id = lane < (int)(blockDim.x >> 5) ? s_id[lane] : -1;
+    for (int o = 16; o > 0; o >>= 1) {
+      const uint64_t k2 = __shfl_down_sync(0xFFFFFFFFu, key, o);
+      const int i2 = __shfl_down_sync(0xFFFFFFFFu, id, o);
+      if (k2 < key || (k2 == key && (unsigned)i2 < (unsigned)id)) { key = k2; id = i2; }
+    }
+    if (lane == 0) s_id[32] = key == ~0ull ? -1 : id;
+  }
+  __syncthreads();
+  const int w = s_id[32];
+  __syncthreads();
+  return w;
+}
+
+__global__ void __launch_bounds__(kPolicyThreads) k_cache_policy(PolicyArgs a) {
+  __shared__ uint64_t s_key[32];
+  __shared__ int s_id[33];
+  __shared__ unsigned long long s_routes;
+  __shared__ uint32_t s_now;
+  __shared__ int s_halve, s_free;
+  pdl_wait();
+  pdl_launch_dependents();
+  const int t = threadIdx.x;
+  // 1. promotion (one thread: misses and free slots in ascending order)
+  if (t == 0) {
+    const int nm = *a.n_miss, nh = a.n_act[1];
+    int s = a.slot_lo;
+    for (int i = 0; i < nm; ++i) {
+      const int e = a.miss_ids[i];
+      if (e < 0 || e >= a.E) {  // reported by the lookup's checks
+        a.miss_dst[i] = -1;
+        continue;
+      }
+      while (s < a.slot_hi && !a.freeslot[s]) ++s;
+      int dst = a.src_slot[e];  // its staging slot
+      if (s < a.slot_hi) {
+        dst = s++;
+        a.freeslot[dst] = 0;
+        a.table_row[e] = dst;
+        a.src_slot[e] = dst;
+        if (a.meta) a.meta[2 * (nh + i)].y = dst;
+      }
+      a.miss_dst[i] = dst;
+    }
+    s_now = a.stamp[a.layer] + 1;
+    a.stamp[a.layer] = s_now;
+    s_routes = 0;
+  }
+  __syncthreads();
+  // 2. counts
+  const size_t row = (size_t)a.layer * a.E;
+  if (t < a.E) {
+    const int c = a.counts[t];
+    if (c > 0) {
+      const uint64_t v = (uint64_t)a.cnt[row + t] + (uint64_t)c;
+      a.cnt[row + t] = v > kCountCap ? kCountCap : (uint32_t)v;
+      a.last[row + t] = s_now;
+      atomicAdd(&s_routes, (unsigned long long)c);
+    }
+  }
+  __syncthreads();
+  if (t == 0) {
+    uint64_t ev = (uint64_t)a.stamp[a.L] + s_routes;
+    s_halve = ev >= kHalveEvents;
+    a.stamp[a.L] = s_halve ? 0u : (uint32_t)ev;
+  }
+  __syncthreads();
+  if (s_halve)
+    for (size_t i = t; i < (size_t)a.L * a.E; i += blockDim.x) a.cnt[i] >>= 1;
+  __syncthreads();
+  // 3. boundary: evict down to the spares
+  for (;;) {
+    if (t == 0) s_free = 0;
+    __syncthreads();
+    int nf = 0;
+    for (int s = a.slot_lo + t; s < a.slot_hi; s += blockDim.x) nf += a.freeslot[s] != 0;
+    if (nf) atomicAdd(&s_free, nf);
+    __syncthreads();
+    if (s_free >= a.spares) break;
+    const bool res = t < a.E && a.table_row[t] >= 0;
+    const uint64_t key = res ? ((uint64_t)a.cnt[row + t] << 32) | a.last[row + t] : ~0ull;
+    const int victim = block_argmin(key, res ? t : -1, s_key, s_id);
+    if (victim < 0) break;
+    if (t == 0) {
+      a.freeslot[a.table_row[victim]] = 1;
+      a.table_row[victim] = -1;
+    }
+    __syncthreads();
+  }
+}
 
 // One 16-byte read per 4 KiB page of the mapped host arena.  The device's
 // first read of a host page is slow: on the 16-layer stack a step whose misses
@@ -120,6 +260,8 @@ MOE_API moe_status expcache_create(const expcache_desc* d, expcache** out) {
   if (!c) return MOE_ERR_OOM;
   c->L = d->L; c->E = d->E; c->H = d->H; c->I = d->I;
   c->n_cache = d->n_cache_slots; c->n_stage = d->n_stage;
+  c->partitioned = d->layer_slots != nullptr;
+  c->spares = -1;
   c->rec_bytes = RecordLayout(d->H, d->I).bytes;
   c->slot_lo = (int32_t*)malloc(sizeof(int32_t) * d->L);
   c->slot_hi = (int32_t*)malloc(sizeof(int32_t) * d->L);
@@ -174,6 +316,10 @@ MOE_API moe_status expcache_destroy(expcache* c) {
   if (c->arena) cudaFree(c->arena);
   if (c->table) cudaFree(c->table);
   if (c->host_index_dev) cudaFree(c->host_index_dev);
+  if (c->cnt) cudaFree(c->cnt);
+  if (c->last) cudaFree(c->last);
+  if (c->stamp) cudaFree(c->stamp);
+  if (c->freeslot) cudaFree(c->freeslot);
   free(c->slot_lo);
   free(c->slot_hi);
   free(c);
@@ -192,6 +338,7 @@ MOE_API moe_status expcache_set_resident(expcache* c, int layer, int expert, int
   if (!c || layer < 0 || layer >= c->L || expert < 0 || expert >= c->E) return MOE_ERR_INVALID_ARG;
   if (slot != -1 && (slot < c->slot_lo[layer] || slot >= c->slot_hi[layer]))
     return MOE_ERR_INVALID_ARG;
+  if (c->spares >= 0) return MOE_ERR_UNSUPPORTED;  // the adaptive policy owns the table
   k_set_table<<<1, 1, 0, (cudaStream_t)stream>>>(c->table + (size_t)layer * c->E + expert, slot);
   MOE_CHECK_LAUNCH();
   return MOE_OK;
@@ -218,7 +365,9 @@ MOE_API moe_status expcache_fill(expcache* c, int layer, const int32_t* d_expert
   dim3 grid(gather_blocks_per_record(c->rec_bytes, max_count), max_count);
   if (launch_pdl(k_gather, grid, kGatherThreads, 0, (cudaStream_t)stream, c->host_dev,
                  c->host_index_dev ? c->host_index_dev + (size_t)layer * c->E : nullptr,
-                 c->host_records, c->arena, c->table + (size_t)layer * c->E, c->E, c->rec_bytes,
+                 c->host_records, c->arena,
+                 c->spares >= 0 ? nullptr : c->table + (size_t)layer * c->E,  // the policy's table
+                 c->E, c->rec_bytes,
                  c->n_cache, c->n_stage, d_expert_ids, d_n, first, d_dst_slots,
                  c->slot_lo[layer], c->slot_hi[layer], status) != cudaSuccess)
     return MOE_ERR_CUDA;
@@ -265,4 +414,88 @@ int cache_E(const expcache* c) { return c->E; }
 int cache_L(const expcache* c) { return c->L; }
 int cache_H(const expcache* c) { return c->H; }
 int cache_I(const expcache* c) { return c->I; }
+}  // namespace moe
+
+// ---- adaptive policy: host entry points -------------------------------------
+MOE_API moe_status expcache_set_policy(expcache* c, int spares_per_layer) {
+  if (!c || spares_per_layer < 0) return MOE_ERR_INVALID_ARG;
+  if (!c->partitioned || c->E > kPolicyThreads) return MOE_ERR_UNSUPPORTED;
+  const size_t le = (size_t)c->L * c->E;
+  if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
+  if (!c->cnt) {
+    if (cudaMalloc((void**)&c->cnt, le * 4) != cudaSuccess ||
+        cudaMalloc((void**)&c->last, le * 4) != cudaSuccess ||
+        cudaMalloc((void**)&c->stamp, ((size_t)c->L + 1) * 4) != cudaSuccess ||
+        cudaMalloc((void**)&c->freeslot, ((size_t)c->n_cache + 1) * 4) != cudaSuccess) {
+      cudaGetLastError();
+      return MOE_ERR_OOM;
+    }
+  }
+  // free slots: those of each layer's run that its table row does not use
+  int32_t* tab = (int32_t*)malloc(le * 4);
+  int32_t* fr = (int32_t*)calloc((size_t)c->n_cache + 1, 4);
+  if (!tab || !fr) {
+    free(tab);
+    free(fr);
+    return MOE_ERR_OOM;
+  }
+  moe_status st = MOE_OK;
+  if (cudaMemcpy(tab, c->table, le * 4, cudaMemcpyDeviceToHost) != cudaSuccess) st = MOE_ERR_CUDA;
+  for (int l = 0; st == MOE_OK && l < c->L; ++l) {
+    for (int s = c->slot_lo[l]; s < c->slot_hi[l]; ++s) fr[s] = 1;
+    for (int e = 0; e < c->E; ++e) {
+      const int s = tab[(size_t)l * c->E + e];
+      if (s >= c->slot_lo[l] && s < c->slot_hi[l]) fr[s] = 0;
+    }
+  }
+  if (st == MOE_OK &&
+      (cudaMemset(c->cnt, 0, le * 4) != cudaSuccess || cudaMemset(c->last, 0, le * 4) != cudaSuccess ||
+       cudaMemset(c->stamp, 0, ((size_t)c->L + 1) * 4) != cudaSuccess ||
+       cudaMemcpy(c->freeslot, fr, ((size_t)c->n_cache + 1) * 4, cudaMemcpyHostToDevice) !=
+           cudaSuccess))
+    st = MOE_ERR_CUDA;
+  free(tab);
+  free(fr);
+  if (st != MOE_OK) {
+    cudaGetLastError();
+    return st;
+  }
+  c->spares = spares_per_layer;
+  return MOE_OK;
+}
+
+MOE_API moe_status expcache_policy_step(expcache* c, int layer, const int32_t* counts,
+                                        int32_t* src_slot, const int32_t* n_act,
+                                        const int32_t* miss_ids, const int32_t* n_miss,
+                                        int32_t* miss_dst, void* meta, void* stream) {
+  if (!c || !counts || !src_slot || !n_act || !miss_ids || !n_miss || !miss_dst || layer < 0 ||
+      layer >= c->L)
+    return MOE_ERR_INVALID_ARG;
+  if (c->spares < 0) return MOE_ERR_UNSUPPORTED;
+  PolicyArgs a;
+  a.L = c->L; a.E = c->E; a.layer = layer;
+  a.slot_lo = c->slot_lo[layer]; a.slot_hi = c->slot_hi[layer]; a.spares = c->spares;
+  a.table_row = c->table + (size_t)layer * c->E;
+  a.cnt = c->cnt; a.last = c->last; a.stamp = c->stamp; a.freeslot = c->freeslot;
+  a.counts = counts; a.src_slot = src_slot; a.n_act = n_act; a.miss_ids = miss_ids;
+  a.n_miss = n_miss; a.miss_dst = miss_dst; a.meta = (int4*)meta;
+  if (launch_pdl(k_cache_policy, 1, kPolicyThreads, 0, (cudaStream_t)stream, a) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+MOE_API moe_status expcache_policy_state(const expcache* c, int* spares, const uint32_t** cnt,
+                                         const uint32_t** last, const uint32_t** stamp,
+                                         const int32_t** freeslot) {
+  if (!c || !spares || !cnt || !last || !stamp || !freeslot) return MOE_ERR_INVALID_ARG;
+  *spares = c->spares;
+  *cnt = c->cnt;
+  *last = c->last;
+  *stamp = c->stamp;
+  *freeslot = c->freeslot;
+  return MOE_OK;
+}
+
+namespace moe {
+bool cache_has_policy(const expcache* c) { return c->spares >= 0; }
 }  // namespace moe

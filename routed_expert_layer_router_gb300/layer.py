@@ -103,6 +103,24 @@ class ExpertCache:
     def set_resident(self, layer: int, expert: int, slot: int, stream=None) -> None:
         moe.expcache_set_resident(self.handle, layer, expert, slot, _stream(stream))
 
+    def set_policy(self, spares_per_layer: int) -> None:
+        """Turns on the adaptive policy (expcache_set_policy); synchronous."""
+        torch.cuda.synchronize()
+        moe.expcache_set_policy(self.handle, spares_per_layer)
+
+    def policy_state(self) -> dict:
+        """Copies of the adaptive policy's device state (numpy): cnt, last
+        [L][E], stamp [L], events, free [n_cache_slots]."""
+        p = moe.expcache_policy_state(self.handle)
+        torch.cuda.synchronize()
+        L, E, n = self.L, self.E, self.n_cache_slots
+        st = device_view(p["stamp"], (L + 1,)).cpu().numpy().view(np.uint32)
+        return {"spares": p["spares"],
+                "cnt": device_view(p["cnt"], (L, E)).cpu().numpy().view(np.uint32),
+                "last": device_view(p["last"], (L, E)).cpu().numpy().view(np.uint32),
+                "stamp": st[:L].copy(), "events": int(st[L]),
+                "free": device_view(p["freeslot"], (n,)).cpu().numpy().astype(np.uint8)}
+
     def table(self) -> torch.Tensor:
         """Copy of the device slot table [L][E]."""
         torch.cuda.synchronize()

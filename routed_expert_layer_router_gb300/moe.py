@@ -77,6 +77,9 @@ SIGNATURES = {
     "expcache_set_resident": (i32, [vp, i32, i32, i32, vp]),
     "expcache_fill": (i32, [vp, i32, vp, vp, i32, i32, vp, vp, vp]),
     "expcache_lookup": (i32, [vp, i32, vp, vp, vp, vp, vp, vp, vp, vp]),
+    "expcache_set_policy": (i32, [vp, i32]),
+    "expcache_policy_step": (i32, [vp, i32, vp, vp, vp, vp, vp, vp, vp, vp]),
+    "expcache_policy_state": (i32, [vp, ctypes.POINTER(i32), vp, vp, vp, vp]),
     "moe_ffn_workspace_bytes": (sz, [i32, i32, i32, i32, i32, i32, i32]),
     "moe_expert_ffn": (i32, [ctypes.POINTER(moe_ffn_args), vp]),
     "moe_expert_ffn_noalloc": (i32, [ctypes.POINTER(moe_ffn_args), vp]),
@@ -174,6 +177,27 @@ def expcache_lookup(cache, layer, counts, src_slot, act_list, n_act, miss_ids, n
                     stream: int = 0) -> None:
     _ck("expcache_lookup", lib().expcache_lookup(cache, layer, counts, src_slot, act_list, n_act,
                                                  miss_ids, n_miss, status or None, stream))
+
+
+def expcache_set_policy(cache, spares_per_layer: int) -> None:
+    _ck("expcache_set_policy", lib().expcache_set_policy(cache, spares_per_layer))
+
+
+def expcache_policy_step(cache, layer, counts, src_slot, n_act, miss_ids, n_miss, miss_dst,
+                         meta=0, stream: int = 0) -> None:
+    _ck("expcache_policy_step", lib().expcache_policy_step(cache, layer, counts, src_slot, n_act,
+                                                           miss_ids, n_miss, miss_dst,
+                                                           meta or None, stream))
+
+
+def expcache_policy_state(cache) -> dict:
+    """Device pointers of the adaptive policy's state (see moe.h)."""
+    spares = i32()
+    outs = [vp() for _ in range(4)]
+    _ck("expcache_policy_state", lib().expcache_policy_state(
+        cache, ctypes.byref(spares), *[ctypes.byref(o) for o in outs]))
+    return dict(zip(["cnt", "last", "stamp", "freeslot"], [o.value for o in outs]),
+                spares=spares.value)
 
 
 def moe_ffn_workspace_bytes(mode, T, H, I, E, k, Is) -> int:
