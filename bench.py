@@ -18,7 +18,10 @@ The same run also measures (the `also` object), each in its own bounded pass:
            layer in HBM, misses gathered from pinned host memory: tokens/s,
            hit rate, gather GB/s against the measured host->device link;
   flat     8 layers, 64 tokens per step, unbiased routing, 72 experts per layer
-           cached by saliency, misses gathered from pinned host memory.
+           cached by saliency, misses gathered from pinned host memory;
+  stack_adaptive  the stack with the adaptive cache: per layer the 63 hottest
+           resident at start and 3 spare slots, misses promoted into them,
+           decayed-LFU eviction between forwards.
 
 Prints one JSON line (rank 0).  --impl reference times the CPU oracle on the
 decode workload instead (bounded sample, host cores).
@@ -41,6 +44,9 @@ import numpy as np  # noqa: E402
 
 METRIC = "MoE-layer tokens/s (decode, 4096-tok prefill); % of HBM / FP4-TC / PCIe roofline"
 UNIT = "tokens/s"
+# the adaptive cache keeps three spare slots per layer ("Project Maya" page)
+ADAPTIVE_SPARES = 3
+ADAPTIVE_WARM_TOKENS = 256  # about one halving period of its counts on the 16-layer stack
 FP4_OVER_BF16 = 6.0  # nominal dense FP4 / dense bf16 tensor throughput (13.5 / 2.25)
 # DRAM bytes (read + write) of one k_decode_gu launch on the full decode layer, from
 # one ncu capture of the current kernel (profiles/k_decode_gu_decode-layer.md); set to
@@ -571,7 +577,7 @@ def _saliency_order(torch, moe, gen, wl, layers, dev, n_tokens=512):
     return orders
 
 
-def bench_multilayer(args, torch, moe, gen, gd, dev, name, link_gbs):
+def bench_multilayer(args, torch, moe, gen, gd, dev, name, link_gbs, spares=0):
     wl = gen.WORKLOADS[name]
     L = wl.layers if args.layers <= 0 else min(args.layers, wl.layers)
     T = wl.T
@@ -579,12 +585,18 @@ def bench_multilayer(args, torch, moe, gen, gd, dev, name, link_gbs):
     n_stage = 64 if T > 1 else None
     # one host copy per expert id, shared by the layers (host memory bound;
     # the bytes each miss moves over the link are the same)
+    # spares > 0: the adaptive cache, its spare slots taken from the hot budget
     dw = gd.build(wl, layers=L, T_max=T, saliency_order=order, n_stage=n_stage,
-                  alias_host_records=True)
+                  alias_host_records=True, spares=spares)
     stream = torch.cuda.current_stream()
     sp = stream.cuda_stream
     steps = args.stack_steps
-    n = args.warmup + steps
+    # The adaptive cache learns from the routes it sees: it is warmed with a
+    # stream of distinct tokens (not a few tokens repeated), and its gather
+    # pass runs on fresh tokens too, so that its hit rate is that of new input.
+    n_warm = args.warmup if spares == 0 else max(args.warmup, ADAPTIVE_WARM_TOKENS)
+    g0 = n_warm + (steps if spares > 0 else 0)  # first token of the gather pass
+    n = g0 + steps
     xs = torch.empty((n, L, T, wl.H), dtype=torch.bfloat16, device=dev)
     for i in range(n):
         for l in range(L):
@@ -597,13 +609,18 @@ def bench_multilayer(args, torch, moe, gen, gd, dev, name, link_gbs):
         for l in range(L):
             layers[l].forward(xs[i, l], y[l])
 
-    prewarm(torch, lambda: [fwd(i) for i in range(args.warmup)], args.prewarm_s)
+    if spares > 0:
+        for i in range(n_warm):
+            fwd(i)
+        torch.cuda.synchronize()
+    else:
+        prewarm(torch, lambda: [fwd(i) for i in range(args.warmup)], args.prewarm_s)
     ev = _events(torch, steps)
     torch.cuda.synchronize()
     for j in range(steps):
         flush()
         ev[j][0].record(stream)
-        fwd(args.warmup + j)
+        fwd(n_warm + j)
         ev[j][1].record(stream)
     torch.cuda.synchronize()
     ms = sum(a.elapsed_time(b) for a, b in ev) / steps
@@ -615,7 +632,8 @@ def bench_multilayer(args, torch, moe, gen, gd, dev, name, link_gbs):
     # previous group's down kernel)
     S = dw.cache.n_stage
     groups = (min(T * wl.k, wl.E) + S - 1) // S if S > 0 else 1
-    first = 2 if T <= 8 else 3  # marks before the first group: start, router (+ permutation)
+    # marks before the first group: start, router (+ permutation), policy step
+    first = (2 if T <= 8 else 3) + (1 if spares > 0 else 0)
     marks = first + groups * (3 if S > 0 else 2) + (1 if groups > 1 else 0)
     hev = [[torch.cuda.Event(enable_timing=True) for _ in range(marks)] for _ in range(L)]
     for e in (e for row in hev for e in row):  # torch creates the CUDA event on its first record
@@ -630,7 +648,7 @@ def bench_multilayer(args, torch, moe, gen, gd, dev, name, link_gbs):
     hook_ms = 0.0                  # whole steps of this pass
     for j in range(steps if S > 0 else 0):
         flush()
-        fwd(args.warmup + j)
+        fwd(g0 + j)
         torch.cuda.synchronize()
         hook_ms += hev[0][0].elapsed_time(hev[L - 1][marks - 1])
         for l in range(L):
@@ -651,7 +669,11 @@ def bench_multilayer(args, torch, moe, gen, gd, dev, name, link_gbs):
     gather_gbs = miss * rb / (fill_ms * 1e-3) / 1e9 if fill_ms > 0 else 0.0
     res = {
         "workload": (f"{L} decode layers, {T} token(s) per step, "
-                     + ("per-layer Zipf bias (alpha 1.556), 66 hot experts per layer in HBM"
+                     + (("per-layer Zipf bias (alpha 1.556), 66 hot experts per layer in HBM"
+                         if spares == 0 else
+                         f"per-layer Zipf bias (alpha 1.556), 66 slots per layer in HBM: the "
+                         f"{66 - spares} hottest resident at start and {spares} spares, adaptive "
+                         f"cache (promotion on miss, decayed LFU eviction)")
                         if name == "stack" else
                         "unbiased routing, 72 experts per layer cached by saliency")
                      + ", misses gathered from pinned host memory"),
@@ -668,7 +690,8 @@ def bench_multilayer(args, torch, moe, gen, gd, dev, name, link_gbs):
     }
     if S > 0 and steps > 0:
         # the gather pass's own step time and its launch-step intervals, per
-        # layer (us): router (+ permutation), then per group gather, gate/up, down
+        # layer (us): router (+ permutation), the policy step (adaptive cache),
+        # then per group gather, gate/up, down
         res["gather_pass"] = {"ms_per_step": round(hook_ms / steps, 4),
                               "us_per_layer": [round(v * 1e3 / (steps * L), 1) for v in part_ms]}
     dw.close()
@@ -744,6 +767,10 @@ def run_ours(args, rank, world, local_rank):
     if args.only in ("stack", "flat"):
         link = link_h2d_gbs(torch, dev)
         return {args.only: bench_multilayer(args, torch, moe, gen, gd, dev, args.only, link)}
+    if args.only == "stack_adaptive":
+        link = link_h2d_gbs(torch, dev)
+        return {args.only: bench_multilayer(args, torch, moe, gen, gd, dev, "stack", link,
+                                            spares=ADAPTIVE_SPARES)}
     d = bench_decode(args, torch, moe, gen, gd, dev, rank, world, local_rank, peaks)
     d["roofline"]["peak_source"] = (f"{peak_kind}: MEASURED_PEAKS.json hbm_gbs (copy)"
                                     if peak_kind == "measured" else "fallback 6.8 TB/s")
@@ -770,9 +797,11 @@ def run_ours(args, rank, world, local_rank):
         try:
             link = link_h2d_gbs(torch, dev)
             also["link_h2d_gbs"] = round(link, 1)
-            for name in ("stack", "flat"):
+            for name, wname, sp in (("stack", "stack", 0), ("flat", "flat", 0),
+                                    ("stack_adaptive", "stack", ADAPTIVE_SPARES)):
                 try:
-                    also[name] = bench_multilayer(args, torch, moe, gen, gd, dev, name, link)
+                    also[name] = bench_multilayer(args, torch, moe, gen, gd, dev, wname, link,
+                                                  spares=sp)
                 except Exception as exc:
                     also[name] = {"error": repr(exc)}
                 torch.cuda.empty_cache()
@@ -814,7 +843,8 @@ def main():
     ap.add_argument("--decode-only", action="store_true")
     ap.add_argument("--small", action="store_true",
                     help="16 distinct expert records (profiler captures only)")
-    ap.add_argument("--only", default="", choices=["", "prefill", "route", "stack", "flat"],
+    ap.add_argument("--only", default="",
+                    choices=["", "prefill", "route", "stack", "flat", "stack_adaptive"],
                     help="run one secondary workload alone (profiler captures)")
     ap.add_argument("--prefill-experts", type=int, default=0,
                     help="prefill with fewer experts, same tokens per expert (profiling)")

@@ -45,13 +45,15 @@ class DeviceWorkload:
             self.host_arena.close()
 
 
-def _hot_set(wl: gen.Workload, layer: int, bias_rank, saliency_order):
+def _hot_set(wl: gen.Workload, layer: int, bias_rank, saliency_order, drop: int = 0):
+    """The layer's hot experts (the `hot` first by rule), less the `drop`
+    coldest of them."""
     if wl.hot <= 0 or wl.hot >= wl.E:
-        return list(range(wl.E))
+        return list(range(wl.E - drop))
     if wl.hot_rule == "zipf":
-        return sorted(int(e) for e in np.argsort(bias_rank)[:wl.hot])
+        return sorted(int(e) for e in np.argsort(bias_rank)[:wl.hot - drop])
     if wl.hot_rule == "saliency":
-        return sorted(int(e) for e in saliency_order[layer][:wl.hot])
+        return sorted(int(e) for e in saliency_order[layer][:wl.hot - drop])
     raise ValueError(wl.hot_rule)
 
 
@@ -68,7 +70,8 @@ def build(wl: gen.Workload, layers: int | None = None, T_max: int | None = None,
       (the host-index table maps every layer to it) when host memory is short;
       the records then repeat across layers for both the GPU and the oracle.
     spares: > 0 turns on the adaptive cache: each layer's slot run gets that
-      many free slots beyond its residents, every expert has a host record
+      many free slots beyond its residents (by default the hot set less its
+      `spares` coldest, so the run keeps the hot budget), every expert has a host record
       (any of them can be evicted and gathered again), and the cache's
       policy keeps that many spares per layer.
     """
@@ -90,7 +93,8 @@ def build(wl: gen.Workload, layers: int | None = None, T_max: int | None = None,
         ranks.append(r)
     rec_layer = [0 if alias_host_records else l for l in range(L)]
     if resident is None:
-        resident = [_hot_set(wl, l, ranks[l], saliency_order) for l in range(L)]
+        # under the adaptive policy the spares come out of the hot budget
+        resident = [_hot_set(wl, l, ranks[l], saliency_order, drop=spares) for l in range(L)]
     else:
         resident = [sorted(int(e) for e in r) for r in resident]
     n_res = [len(r) for r in resident]

@@ -113,6 +113,7 @@ struct PolicyArgs {
 };
 
 constexpr int kPolicyThreads = 1024;
+constexpr int kPolicyMaxRun = 8192;  // slots of one layer's run
 constexpr uint32_t kCountCap = 1u << 24;
 constexpr uint32_t kHalveEvents = 32768;
 
@@ -142,81 +143,110 @@ __device__ int block_argmin(uint64_t key, int id, uint64_t* s_key, int* s_id) {
   return w;
 }
 
+// The layer's row of the table and counts, and its slot run's free flags, are
+// staged in shared memory, so that the serial parts (promotions, evictions)
+// run on shared memory and the whole step costs a few global round trips.
 __global__ void __launch_bounds__(kPolicyThreads) k_cache_policy(PolicyArgs a) {
+  __shared__ int s_tab[kPolicyThreads], s_miss[kPolicyThreads], s_src[kPolicyThreads];
+  __shared__ uint32_t s_cnt[kPolicyThreads], s_last[kPolicyThreads];
+  __shared__ unsigned char s_free[kPolicyMaxRun];
   __shared__ uint64_t s_key[32];
   __shared__ int s_id[33];
   __shared__ unsigned long long s_routes;
   __shared__ uint32_t s_now;
-  __shared__ int s_halve, s_free;
+  __shared__ int s_halve, s_nfree;
   pdl_wait();
   pdl_launch_dependents();
-  const int t = threadIdx.x;
-  // 1. promotion (one thread: misses and free slots in ascending order)
+  const int t = threadIdx.x, E = a.E, P = a.slot_hi - a.slot_lo;
+  const size_t row = (size_t)a.layer * E;
+  // stage (one round trip)
+  int c = 0;
+  if (t < E) {
+    s_tab[t] = a.table_row[t];
+    s_cnt[t] = a.cnt[row + t];
+    s_last[t] = a.last[row + t];
+    s_miss[t] = a.miss_ids[t];
+    s_src[t] = a.src_slot[t];
+    c = a.counts[t];
+  }
+  for (int j = t; j < P; j += blockDim.x) s_free[j] = a.freeslot[a.slot_lo + j] != 0;
+  if (t == 0) {
+    s_routes = 0;
+    s_now = a.stamp[a.layer] + 1;
+  }
+  __syncthreads();
+  // 1. promotion: misses and free slots in ascending order (one thread)
   if (t == 0) {
     const int nm = *a.n_miss, nh = a.n_act[1];
-    int s = a.slot_lo;
+    int f = 0;
     for (int i = 0; i < nm; ++i) {
-      const int e = a.miss_ids[i];
-      if (e < 0 || e >= a.E) {  // reported by the lookup's checks
+      const int e = s_miss[i];
+      if (e < 0 || e >= E) {  // reported by the lookup's checks
         a.miss_dst[i] = -1;
         continue;
       }
-      while (s < a.slot_hi && !a.freeslot[s]) ++s;
-      int dst = a.src_slot[e];  // its staging slot
-      if (s < a.slot_hi) {
-        dst = s++;
-        a.freeslot[dst] = 0;
-        a.table_row[e] = dst;
+      while (f < P && !s_free[f]) ++f;
+      int dst = s_src[e];  // its staging slot
+      if (f < P) {
+        dst = a.slot_lo + f;
+        s_free[f++] = 0;
+        s_tab[e] = dst;
         a.src_slot[e] = dst;
         if (a.meta) a.meta[2 * (nh + i)].y = dst;
       }
       a.miss_dst[i] = dst;
     }
-    s_now = a.stamp[a.layer] + 1;
-    a.stamp[a.layer] = s_now;
-    s_routes = 0;
   }
-  __syncthreads();
   // 2. counts
-  const size_t row = (size_t)a.layer * a.E;
-  if (t < a.E) {
-    const int c = a.counts[t];
-    if (c > 0) {
-      const uint64_t v = (uint64_t)a.cnt[row + t] + (uint64_t)c;
-      a.cnt[row + t] = v > kCountCap ? kCountCap : (uint32_t)v;
-      a.last[row + t] = s_now;
-      atomicAdd(&s_routes, (unsigned long long)c);
-    }
+  if (c > 0) {
+    const uint64_t v = (uint64_t)s_cnt[t] + (uint64_t)c;
+    s_cnt[t] = v > kCountCap ? kCountCap : (uint32_t)v;
+    s_last[t] = s_now;
+    atomicAdd(&s_routes, (unsigned long long)c);
   }
   __syncthreads();
   if (t == 0) {
-    uint64_t ev = (uint64_t)a.stamp[a.L] + s_routes;
+    const uint64_t ev = (uint64_t)a.stamp[a.L] + s_routes;
     s_halve = ev >= kHalveEvents;
     a.stamp[a.L] = s_halve ? 0u : (uint32_t)ev;
+    a.stamp[a.layer] = s_now;
   }
   __syncthreads();
-  if (s_halve)
-    for (size_t i = t; i < (size_t)a.L * a.E; i += blockDim.x) a.cnt[i] >>= 1;
-  __syncthreads();
+  if (s_halve) {
+    if (t < E) s_cnt[t] >>= 1;
+    for (size_t i = t; i < (size_t)a.L * E; i += blockDim.x)
+      if (i < row || i >= row + E) a.cnt[i] >>= 1;  // the other layers
+  }
   // 3. boundary: evict down to the spares
-  for (;;) {
-    if (t == 0) s_free = 0;
-    __syncthreads();
+  if (t == 0) {
     int nf = 0;
-    for (int s = a.slot_lo + t; s < a.slot_hi; s += blockDim.x) nf += a.freeslot[s] != 0;
-    if (nf) atomicAdd(&s_free, nf);
-    __syncthreads();
-    if (s_free >= a.spares) break;
-    const bool res = t < a.E && a.table_row[t] >= 0;
-    const uint64_t key = res ? ((uint64_t)a.cnt[row + t] << 32) | a.last[row + t] : ~0ull;
+    for (int j = 0; j < P; ++j) nf += s_free[j];
+    s_nfree = nf;
+  }
+  __syncthreads();
+  while (s_nfree < a.spares) {
+    const bool res = t < E && s_tab[t] >= 0;
+    const uint64_t key = res ? ((uint64_t)s_cnt[t] << 32) | s_last[t] : ~0ull;
     const int victim = block_argmin(key, res ? t : -1, s_key, s_id);
     if (victim < 0) break;
     if (t == 0) {
-      a.freeslot[a.table_row[victim]] = 1;
-      a.table_row[victim] = -1;
+      const int f = s_tab[victim] - a.slot_lo;  // a slot outside the run: the lookup reports it
+      if (f >= 0 && f < P) {
+        s_free[f] = 1;
+        ++s_nfree;
+      }
+      s_tab[victim] = -1;
     }
     __syncthreads();
   }
+  __syncthreads();
+  // write back
+  if (t < E) {
+    a.table_row[t] = s_tab[t];
+    a.cnt[row + t] = s_cnt[t];
+    a.last[row + t] = s_last[t];
+  }
+  for (int j = t; j < P; j += blockDim.x) a.freeslot[a.slot_lo + j] = s_free[j];
 }
 
 // One 16-byte read per 4 KiB page of the mapped host arena.  The device's
@@ -420,6 +450,8 @@ int cache_I(const expcache* c) { return c->I; }
 MOE_API moe_status expcache_set_policy(expcache* c, int spares_per_layer) {
   if (!c || spares_per_layer < 0) return MOE_ERR_INVALID_ARG;
   if (!c->partitioned || c->E > kPolicyThreads) return MOE_ERR_UNSUPPORTED;
+  for (int l = 0; l < c->L; ++l)
+    if (c->slot_hi[l] - c->slot_lo[l] > kPolicyMaxRun) return MOE_ERR_UNSUPPORTED;
   const size_t le = (size_t)c->L * c->E;
   if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
   if (!c->cnt) {
