@@ -10,7 +10,8 @@
 //            tensor memory), fp32 accumulators in tensor memory; TMA tile loads
 //            of both operands (one 3-D tensor map spans the whole slot arena, so
 //            every expert record is addressed by its slot), an mbarrier ring
-//            (4 stages for gate/up, 6 for down), one warp loading, one warp
+//            (gate/up: 4 stages of one 128-byte K chunk; down: 3 stages of
+//            two), one warp loading, one warp
 //            issuing MMAs, eight warps in the epilogue.  Gate and up share the
 //            activation tile and accumulate into two TMEM accumulators; the
 //            epilogue forms silu(g)*u.
@@ -47,6 +48,8 @@ constexpr int kThreads = 320;  // warp 0: TMA, warp 1: MMA, warps 2..9: epilogue
 constexpr int kEpiWarps = 8;   // two per tensor-memory lane quarter, each half of the columns
 constexpr uint64_t kWaitNs = 2000000000ull;  // no wait lasts longer than 2 s
 constexpr uint32_t kTmemCols = 512;
+constexpr int kSingleChunks = 2;
+constexpr int kDualChunks = 1;
 
 enum Epi { EPI_GU_ROUTED = 0, EPI_GU_SHARED = 1, EPI_DOWN_ROUTED = 2, EPI_DOWN_SHARED = 3 };
 
@@ -191,14 +194,19 @@ struct Cfg {
   static constexpr bool kNvf4 = (KIND == 0);
   static constexpr int kTileBytes = kTileM * kStageKB;  // 16 KiB
   static constexpr int kSfBytes = kNvf4 ? 2048 : 0;     // 4 atoms of 512 B
-  static constexpr int kStageBytes =
-      kTileBytes * (kDual ? 3 : 2) + kSfBytes * (kDual ? 3 : 2);
-  // a single-A stage is two thirds of a dual one: six of them fit where four dual ones do
-  static constexpr int kStages = kDual ? 4 : 6;
+  // one 128-byte K chunk of every operand (A tiles, B tile, their scale atoms)
+  static constexpr int kChunkBytes = kTileBytes * (kDual ? 3 : 2) + kSfBytes * (kDual ? 3 : 2);
+  // several chunks per stage: fewer stages per tile, so fewer barrier round
+  // trips and commits for the same bytes in flight (4 dual or 6 single
+  // chunks fill the shared memory)
+  static constexpr int kChunks = kDual ? kDualChunks : kSingleChunks;
+  static constexpr int kStageBytes = kChunks * kChunkBytes;
+  static constexpr int kStages = (kDual ? 4 : 6) / kChunks;
   static constexpr int kSmem = 1024 + kStages * kStageBytes;
   // tensor memory: accumulators, then per-stage scale-factor columns
   static constexpr uint32_t kAccCols = kDual ? 256 : 128;
-  static constexpr uint32_t kSfColsPerStage = kNvf4 ? (kDual ? 48 : 32) : 0;
+  static constexpr uint32_t kSfColsPerChunk = kNvf4 ? (kDual ? 48 : 32) : 0;
+  static constexpr uint32_t kSfColsPerStage = kChunks * kSfColsPerChunk;
   // two accumulators where they fit beside the scale factors, so that a tile's
   // MMAs never wait for the previous tile's epilogue to read its accumulator
   static constexpr int kAccBufs = (2 * kAccCols + kStages * kSfColsPerStage <= kTmemCols) ? 2 : 1;
@@ -308,9 +316,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t vn = 0;
         int mtn = 0, ntn = 0, en = 0, sn = 0, pn = 0;
         int4 rn = make_int4(0, 0, 0, 0);
-        const int kst = p.kstages;
+        const int kst = (p.kstages + C::kChunks - 1) / C::kChunks;  // stages per tile
         const int arow = mt * kTileM;  // weight rows
-        for (int kb = 0; kb < p.kstages; ++kb, ++g) {
+        for (int kb = 0; kb < kst; ++kb, ++g) {
           if (C::kMMajor && tn < thi && kb == 0) rn = p.ctab[cbase + tn % ncols];
           if (C::kRouted && !C::kMMajor && tn < thi) {  // one link per stage
             if (kb == 0) vn = p.tiles[tn];
@@ -329,39 +337,44 @@ __global__ void __launch_bounds__(kThreads, 1)
             abort_flag = 1;
             break;
           }
-          unsigned char* st = smem + (size_t)s * C::kStageBytes;
-          ptx::mbar_arrive_expect_tx(&full_bar[s], C::kStageBytes);
-          const int kc = C::kNvf4 ? kb * kStageKB : kb * (kStageKB / 2);  // bytes or bf16s
-          // Down: the weights are read once, the activation tiles by every row
-          // tile of their column, and y_acc is added into meanwhile; the cache
-          // policies keep the activations and y_acc in L2 ahead of the weights.
-          const uint64_t pol_w = ptx::l2_evict_first(), pol_a = ptx::l2_evict_last();
-          if (C::kMMajor) {
-            ptx::tma_load_3d_hint(st, &tmA0, kc, arow, slot, &full_bar[s], pol_w);
-          } else if (C::kRouted) {
-            ptx::tma_load_3d(st, &tmA0, kc, arow, slot, &full_bar[s]);
-            if (C::kDual) ptx::tma_load_3d(st + C::kTileBytes, &tmA1, kc, arow, slot, &full_bar[s]);
-          } else {
-            ptx::tma_load_2d(st, &tmA0, kc, arow, &full_bar[s]);
-            if (C::kDual) ptx::tma_load_2d(st + C::kTileBytes, &tmA1, kc, arow, &full_bar[s]);
-          }
-          unsigned char* bdst = st + C::kTileBytes * (C::kDual ? 2 : 1);
-          if (C::kMMajor) ptx::tma_load_2d_hint(bdst, &tmB, kc, brow, &full_bar[s], pol_a);
-          else ptx::tma_load_2d(bdst, &tmB, kc, brow, &full_bar[s]);
-          if (C::kNvf4) {
-            // 4 scale atoms (512 B each) per operand: k groups kb*4 .. kb*4+3
-            unsigned char* sf = bdst + C::kTileBytes;
-            const uint8_t* rec = p.arena + (uint64_t)slot * p.rec_bytes;
-            const uint64_t aoff = ((uint64_t)mt * p.kgroups + (uint64_t)kb * 4) * 512;
-            const uint64_t boff = ((uint64_t)(brow / kTileN) * p.kgroups + (uint64_t)kb * 4) * 512;
-            unsigned char* sfb = sf + (C::kDual ? 4096 : 2048);
+          unsigned char* const st0 = smem + (size_t)s * C::kStageBytes;
+          const int ncs = min(C::kChunks, p.kstages - kb * C::kChunks);  // chunks in this stage
+          ptx::mbar_arrive_expect_tx(&full_bar[s], (uint32_t)(ncs * C::kChunkBytes));
+          for (int c = 0; c < ncs; ++c) {
+            unsigned char* st = st0 + (size_t)c * C::kChunkBytes;
+            const int kq = kb * C::kChunks + c;  // 128-byte K chunk
+            const int kc = C::kNvf4 ? kq * kStageKB : kq * (kStageKB / 2);  // bytes or bf16s
+            // Down: the weights are read once, the activation tiles by every row
+            // tile of their column, and y_acc is added into meanwhile; the cache
+            // policies keep the activations and y_acc in L2 ahead of the weights.
+            const uint64_t pol_w = ptx::l2_evict_first(), pol_a = ptx::l2_evict_last();
             if (C::kMMajor) {
-              ptx::bulk_load_hint(sf, rec + p.sfa_off0 + aoff, 2048, &full_bar[s], pol_w);
-              ptx::bulk_load_hint(sfb, p.b_scales + boff, 2048, &full_bar[s], pol_a);
+              ptx::tma_load_3d_hint(st, &tmA0, kc, arow, slot, &full_bar[s], pol_w);
+            } else if (C::kRouted) {
+              ptx::tma_load_3d(st, &tmA0, kc, arow, slot, &full_bar[s]);
+              if (C::kDual) ptx::tma_load_3d(st + C::kTileBytes, &tmA1, kc, arow, slot, &full_bar[s]);
             } else {
-              ptx::bulk_load(sf, rec + p.sfa_off0 + aoff, 2048, &full_bar[s]);
-              if (C::kDual) ptx::bulk_load(sf + 2048, rec + p.sfa_off1 + aoff, 2048, &full_bar[s]);
-              ptx::bulk_load(sfb, p.b_scales + boff, 2048, &full_bar[s]);
+              ptx::tma_load_2d(st, &tmA0, kc, arow, &full_bar[s]);
+              if (C::kDual) ptx::tma_load_2d(st + C::kTileBytes, &tmA1, kc, arow, &full_bar[s]);
+            }
+            unsigned char* bdst = st + C::kTileBytes * (C::kDual ? 2 : 1);
+            if (C::kMMajor) ptx::tma_load_2d_hint(bdst, &tmB, kc, brow, &full_bar[s], pol_a);
+            else ptx::tma_load_2d(bdst, &tmB, kc, brow, &full_bar[s]);
+            if (C::kNvf4) {
+              // 4 scale atoms (512 B each) per operand: k groups kb*4 .. kb*4+3
+              unsigned char* sf = bdst + C::kTileBytes;
+              const uint8_t* rec = p.arena + (uint64_t)slot * p.rec_bytes;
+              const uint64_t aoff = ((uint64_t)mt * p.kgroups + (uint64_t)kq * 4) * 512;
+              const uint64_t boff = ((uint64_t)(brow / kTileN) * p.kgroups + (uint64_t)kq * 4) * 512;
+              unsigned char* sfb = sf + (C::kDual ? 4096 : 2048);
+              if (C::kMMajor) {
+                ptx::bulk_load_hint(sf, rec + p.sfa_off0 + aoff, 2048, &full_bar[s], pol_w);
+                ptx::bulk_load_hint(sfb, p.b_scales + boff, 2048, &full_bar[s], pol_a);
+              } else {
+                ptx::bulk_load(sf, rec + p.sfa_off0 + aoff, 2048, &full_bar[s]);
+                if (C::kDual) ptx::bulk_load(sf + 2048, rec + p.sfa_off1 + aoff, 2048, &full_bar[s]);
+                ptx::bulk_load(sfb, p.b_scales + boff, 2048, &full_bar[s]);
+              }
             }
           }
         }
@@ -400,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ptx::tc_fence_after();
         bool ok = true;
-        for (int kb = 0; kb < p.kstages; ++kb, ++g) {
+        for (int kb = 0; kb * C::kChunks < p.kstages; ++kb, ++g) {
           const int s = g % C::kStages;
           const uint32_t ph = (g / C::kStages) & 1;
           if (!ptx::mbar_wait(&full_bar[s], ph, kWaitNs)) {
@@ -410,38 +423,42 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           ptx::tc_fence_after();
-          unsigned char* st = smem + (size_t)s * C::kStageBytes;
-          const uint32_t a0 = ptx::smem_u32(st);
-          const uint32_t a1 = a0 + C::kTileBytes;
-          const uint32_t b = a0 + C::kTileBytes * (C::kDual ? 2 : 1);
-          const uint32_t sf = b + C::kTileBytes;
-          const uint32_t sfcol = C::kSfCol0 + (uint32_t)s * C::kSfColsPerStage;
-          if (C::kNvf4) {
-            // scale atoms -> tensor memory (4 columns each)
-            for (int kk = 0; kk < 4; ++kk) {
-              const int nops = C::kDual ? 3 : 2;
-              for (int o = 0; o < nops; ++o) {
-                const uint64_t d = ptx::smem_desc(sf + o * 2048 + kk * 512, 128, 128, 0);
-                ptx::tmem_cp_32x128b_x4(tmem + sfcol + o * 16 + kk * 4, d);
+          const int ncs = min(C::kChunks, p.kstages - kb * C::kChunks);
+          for (int c = 0; c < ncs; ++c) {
+            unsigned char* st = smem + (size_t)s * C::kStageBytes + (size_t)c * C::kChunkBytes;
+            const uint32_t a0 = ptx::smem_u32(st);
+            const uint32_t a1 = a0 + C::kTileBytes;
+            const uint32_t b = a0 + C::kTileBytes * (C::kDual ? 2 : 1);
+            const uint32_t sf = b + C::kTileBytes;
+            const uint32_t sfcol =
+                C::kSfCol0 + (uint32_t)s * C::kSfColsPerStage + (uint32_t)c * C::kSfColsPerChunk;
+            if (C::kNvf4) {
+              // scale atoms -> tensor memory (4 columns each)
+              for (int kk = 0; kk < 4; ++kk) {
+                const int nops = C::kDual ? 3 : 2;
+                for (int o = 0; o < nops; ++o) {
+                  const uint64_t d = ptx::smem_desc(sf + o * 2048 + kk * 512, 128, 128, 0);
+                  ptx::tmem_cp_32x128b_x4(tmem + sfcol + o * 16 + kk * 4, d);
+                }
               }
             }
-          }
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t da0 = ptx::smem_desc(a0 + kk * 32, 16, 1024, 2);
-            const uint64_t db = ptx::smem_desc(b + kk * 32, 16, 1024, 2);
-            const bool accum = (kb > 0) || (kk > 0);
-            if (C::kNvf4) {
-              const uint32_t sfb = tmem + sfcol + (C::kDual ? 32 : 16) + kk * 4;
-              ptx::mma_nvf4(acc, da0, db, idesc, tmem + sfcol + kk * 4, sfb, accum);
-              if (C::kDual) {
-                const uint64_t da1 = ptx::smem_desc(a1 + kk * 32, 16, 1024, 2);
-                ptx::mma_nvf4(acc + 128, da1, db, idesc, tmem + sfcol + 16 + kk * 4, sfb, accum);
-              }
-            } else {
-              ptx::mma_bf16(acc, da0, db, idesc, accum);
-              if (C::kDual) {
-                const uint64_t da1 = ptx::smem_desc(a1 + kk * 32, 16, 1024, 2);
-                ptx::mma_bf16(acc + 128, da1, db, idesc, accum);
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t da0 = ptx::smem_desc(a0 + kk * 32, 16, 1024, 2);
+              const uint64_t db = ptx::smem_desc(b + kk * 32, 16, 1024, 2);
+              const bool accum = (kb > 0) || (c > 0) || (kk > 0);
+              if (C::kNvf4) {
+                const uint32_t sfb = tmem + sfcol + (C::kDual ? 32 : 16) + kk * 4;
+                ptx::mma_nvf4(acc, da0, db, idesc, tmem + sfcol + kk * 4, sfb, accum);
+                if (C::kDual) {
+                  const uint64_t da1 = ptx::smem_desc(a1 + kk * 32, 16, 1024, 2);
+                  ptx::mma_nvf4(acc + 128, da1, db, idesc, tmem + sfcol + 16 + kk * 4, sfb, accum);
+                }
+              } else {
+                ptx::mma_bf16(acc, da0, db, idesc, accum);
+                if (C::kDual) {
+                  const uint64_t da1 = ptx::smem_desc(a1 + kk * 32, 16, 1024, 2);
+                  ptx::mma_bf16(acc + 128, da1, db, idesc, accum);
+                }
               }
             }
           }
