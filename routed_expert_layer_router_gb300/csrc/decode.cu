@@ -55,7 +55,7 @@ struct DecodeParams {
   float* o_route;   // [T*k][H]
   float* o_shared;  // [T][H]
   int32_t* status;
-  int maxm;  // tokens staged per pass (1 or 2)
+  int maxm;  // tokens staged per pass (1; the kernels also take 2)
   // the shared-expert units of K-decode-gu may start before the previous
   // kernel on the stream completes: set only when that kernel neither reads
   // nor writes h_shared (the layer's own sequence, where it is the
@@ -768,7 +768,12 @@ moe_status decode_ffn(const moe_ffn_args* a, cudaStream_t s, const DecodeFuse& f
   p.o_route = a->o_route;
   p.o_shared = a->o_shared;
   p.status = a->status;
-  p.maxm = a->T >= 2 ? 2 : 1;
+  // One token per pass: a unit with several routes reads its weight rows again
+  // for each, from L2, at two CTAs per SM.  Two tokens per pass needed 255
+  // registers (one CTA per SM) and measured slower at every token count on an
+  // all-resident 6144 x 2048 layer: 2 tokens 157 against 134 us, 8 tokens 499
+  // against 382 us, 64 tokens 3.36 against 2.88 ms.
+  p.maxm = 1;
   // experts this group can hold at most
   int max_act = a->T * a->k < a->E ? a->T * a->k : a->E;
   if (a->group > 0) max_act = a->n_stage < max_act ? a->n_stage : max_act;
@@ -784,7 +789,7 @@ moe_status decode_ffn(const moe_ffn_args* a, cudaStream_t s, const DecodeFuse& f
     if (p.n_sdown_units && smem_f32(1, a->Is) > smem) smem = smem_f32(1, a->Is);
     const int grid = p.n_shared_units + p.n_sdown_units + routed;
     if (grid > 0) {
-      if (launch_pdl(p.maxm == 2 ? k_decode_gu<2> : k_decode_gu<1>, grid, kDecThreads, smem, s,
+      if (launch_pdl(k_decode_gu<1>, grid, kDecThreads, smem, s,
                      p) != cudaSuccess)
         return MOE_ERR_CUDA;
       if (fz.mark) fz.mark(fz.mark_ctx);
@@ -803,7 +808,7 @@ moe_status decode_ffn(const moe_ffn_args* a, cudaStream_t s, const DecodeFuse& f
       p.comb_target = max_act + (shared ? 4 : 0);  // CTAs per 128-row tile
     }
     if (grid > 0) {
-      if (launch_pdl(p.maxm == 2 ? k_decode_down<2> : k_decode_down<1>, grid, kDecThreads, smem,
+      if (launch_pdl(k_decode_down<1>, grid, kDecThreads, smem,
                      s, p) != cudaSuccess)
         return MOE_ERR_CUDA;
       if (fz.mark) fz.mark(fz.mark_ctx);
@@ -814,8 +819,7 @@ moe_status decode_ffn(const moe_ffn_args* a, cudaStream_t s, const DecodeFuse& f
 
 moe_status decode_setup() {
   // H up to 16384 with two staged tokens in fp32: 2 * 512 * 36 * 4 bytes
-  const void* fns[4] = {(const void*)k_decode_gu<1>, (const void*)k_decode_gu<2>,
-                        (const void*)k_decode_down<1>, (const void*)k_decode_down<2>};
+  const void* fns[2] = {(const void*)k_decode_gu<1>, (const void*)k_decode_down<1>};
   for (const void* f : fns)
     if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024) !=
         cudaSuccess)

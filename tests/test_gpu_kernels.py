@@ -78,7 +78,7 @@ def _route_gpu(x, Wr, bias, k, ctl=None):
 
 @pytest.mark.parametrize("name,T,one_kernel", [
     ("tiny", 4, False), ("tiny", 37, False), ("decode", 1, False), ("decode", 8, False),
-    ("decode", 64, False), ("decode", 300, False),
+    ("decode", 64, False), ("decode", 300, False), ("decode", 1100, False),
     ("tiny", 4, True), ("decode", 1, True), ("decode", 8, True), ("decode", 64, True)])
 def test_route_parity(name, T, one_kernel):
     wl = gen.WORKLOADS[name]
