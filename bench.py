@@ -632,8 +632,9 @@ def bench_multilayer(args, torch, moe, gen, gd, dev, name, link_gbs, spares=0):
     # previous group's down kernel)
     S = dw.cache.n_stage
     groups = (min(T * wl.k, wl.E) + S - 1) // S if S > 0 else 1
-    # marks before the first group: start, router (+ permutation), policy step
-    first = (2 if T <= 8 else 3) + (1 if spares > 0 else 0)
+    # marks before the first group: start, router (+ permutation), and the
+    # adaptive cache's step when it is a kernel of its own (more than 8 tokens)
+    first = (2 if T <= 8 else 3) + (1 if spares > 0 and T > 8 else 0)
     marks = first + groups * (3 if S > 0 else 2) + (1 if groups > 1 else 0)
     hev = [[torch.cuda.Event(enable_timing=True) for _ in range(marks)] for _ in range(L)]
     for e in (e for row in hev for e in row):  # torch creates the CUDA event on its first record
@@ -690,8 +691,9 @@ def bench_multilayer(args, torch, moe, gen, gd, dev, name, link_gbs, spares=0):
     }
     if S > 0 and steps > 0:
         # the gather pass's own step time and its launch-step intervals, per
-        # layer (us): router (+ permutation), the policy step (adaptive cache),
-        # then per group gather, gate/up, down
+        # layer (us): router (+ permutation, + the adaptive cache's step for up
+        # to 8 tokens), the policy step (more tokens), then per group gather,
+        # gate/up, down
         res["gather_pass"] = {"ms_per_step": round(hook_ms / steps, 4),
                               "us_per_layer": [round(v * 1e3 / (steps * L), 1) for v in part_ms]}
     dw.close()

@@ -5,6 +5,7 @@
 #include <string.h>
 
 #include "permute_body.cuh"
+#include "policy_body.cuh"
 
 namespace moe {
 const uint8_t* cache_arena(const expcache* c);
@@ -14,7 +15,6 @@ int cache_E(const expcache* c);
 int cache_L(const expcache* c);
 int cache_H(const expcache* c);
 int cache_I(const expcache* c);
-bool cache_has_policy(const expcache* c);
 size_t decode_workspace_bytes(int T, int I, int k, int Is);
 moe_status decode_ffn(const moe_ffn_args* a, cudaStream_t s, const DecodeFuse& fz);
 moe_status decode_setup();
@@ -30,7 +30,8 @@ moe_status launch_permute(const int32_t* ids, int T, int k, int E, int32_t* coun
 void cache_lookup_args(const expcache* c, int layer, int32_t* src_slot, int32_t* act_list,
                        int32_t* n_act, int32_t* miss_ids, int32_t* n_miss, LookupArgs* out);
 moe_status route_permute_small(const moe_route_args* a, const PermArgs& pa,
-                               const SharedGuArgs& sg, cudaStream_t s);
+                               const SharedGuArgs& sg, const PolicyArgs* pol, cudaStream_t s);
+bool cache_policy_args(const expcache* c, int layer, PolicyArgs* a);
 }  // namespace moe
 
 namespace moe {
@@ -290,7 +291,17 @@ MOE_API moe_status moe_layer_forward(moe_layer* l, const void* x, int T, void* y
     sg.Is = d.Is;
     sg.h_shared = (float*)l->ffn_ws + (size_t)T * d.k * d.I;
   }
-  st = route_permute_small(&ra, pa, sg, s);
+  // adaptive cache: its step (promotions, counts, the boundary's evictions)
+  // runs in the same kernel, on the lookup's results, when that kernel is used
+  PolicyArgs pol;
+  const bool policy = cache_policy_args(d.cache, d.layer, &pol);
+  if (policy) {
+    pol.counts = l->counts; pol.src_slot = l->src_slot; pol.n_act = l->n_act;
+    pol.miss_ids = l->miss_ids; pol.n_miss = l->n_miss; pol.miss_dst = l->miss_dst;
+    pol.meta = small_routes ? l->act_meta : nullptr;
+  }
+  st = route_permute_small(&ra, pa, sg, policy ? &pol : nullptr, s);
+  const bool policy_done = policy && st == MOE_OK;
   const bool shared_gu_done = st == MOE_OK && sg.Is > 0;
   const int4* act_meta = (st == MOE_OK && small_routes) ? l->act_meta : nullptr;
   if (st == MOE_ERR_UNSUPPORTED) {
@@ -301,10 +312,9 @@ MOE_API moe_status moe_layer_forward(moe_layer* l, const void* x, int T, void* y
   }
   if (st != MOE_OK) return st;
   layer_mark(l);
-  // adaptive cache: promotions, counts and the boundary's evictions, before
-  // the misses are gathered (into their promoted or staging slots)
-  const bool policy = cache_has_policy(d.cache);
-  if (policy) {
+  // otherwise the adaptive cache's step as a kernel of its own, before the
+  // misses are gathered (into their promoted or staging slots)
+  if (policy && !policy_done) {
     if ((st = expcache_policy_step(d.cache, d.layer, l->counts, l->src_slot, l->n_act, l->miss_ids,
                                    l->n_miss, l->miss_dst, (void*)act_meta, stream)) != MOE_OK)
       return st;

@@ -12,6 +12,7 @@
 #include <string.h>
 
 #include "common.cuh"
+#include "policy_body.cuh"
 
 struct expcache {
   int L, E, H, I;
@@ -90,163 +91,12 @@ __global__ void __launch_bounds__(kGatherThreads) k_gather(
 
 __global__ void k_set_table(int32_t* table_entry, int slot) { *table_entry = slot; }
 
-// ---- K-policy: the adaptive cache ("Project Maya" page: "How 'most-used' is
-// measured", "Promotion on every miss, eviction at the boundary") --------------
-// One layer forward, after the lookup (one CTA, a thread per expert):
-//   1. promotion: the lookup's misses, in ascending id, take the layer's free
-//      slots in ascending order and are resident from then on; the others keep
-//      their staging slot (miss_dst[i] = where miss i is gathered);
-//   2. counts: +1 per route, capped at 2^24; last = this forward's number;
-//      every 32,768 route events (all layers) every count is halved;
-//   3. boundary: while fewer than `spares` slots are free, the resident with
-//      the smallest (count, last, id) is evicted.
-struct PolicyArgs {
-  int L, E, layer, slot_lo, slot_hi, spares;
-  int32_t* table_row;
-  uint32_t *cnt, *last, *stamp;  // stamp[L] = route events
-  int32_t* freeslot;
-  const int32_t* counts;
-  int32_t* src_slot;
-  const int32_t *n_act, *miss_ids, *n_miss;
-  int32_t* miss_dst;
-  int4* meta;  // the layer's compact expert records, or nullptr
-};
-
-constexpr int kPolicyThreads = 1024;
-constexpr int kPolicyMaxRun = 8192;  // slots of one layer's run
-constexpr uint32_t kCountCap = 1u << 24;
-constexpr uint32_t kHalveEvents = 32768;
-
-// (key, id) minimum over the CTA; every thread gets the winner's id (-1: none)
-__device__ int block_argmin(uint64_t key, int id, uint64_t* s_key, int* s_id) {
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  for (int o = 16; o > 0; o >>= 1) {
-    const uint64_t k2 = __shfl_down_sync(0xFFFFFFFFu, key, o);
-    const int i2 = __shfl_down_sync(0xFFFFFFFFu, id, o);
-    if (k2 < key || (k2 == key && (unsigned)i2 < (unsigned)id)) { key = k2; id = i2; }
-  }
-  if (lane == 0) { s_key[wid] = key; s_id[wid] = id; }
-  __syncthreads();
-  if (wid == 0) {
-    key = lane < (int)(blockDim.x >> 5) ? s_key[lane] : ~0ull;
-    id = lane < (int)(blockDim.x >> 5) ? s_id[lane] : -1;
-    for (int o = 16; o > 0; o >>= 1) {
-      const uint64_t k2 = __shfl_down_sync(0xFFFFFFFFu, key, o);
-      const int i2 = __shfl_down_sync(0xFFFFFFFFu, id, o);
-      if (k2 < key || (k2 == key && (unsigned)i2 < (unsigned)id)) { key = k2; id = i2; }
-    }
-    if (lane == 0) s_id[32] = key == ~0ull ? -1 : id;
-  }
-  __syncthreads();
-  const int w = s_id[32];
-  __syncthreads();
-  return w;
-}
-
-// The layer's row of the table and counts, and its slot run's free flags, are
-// staged in shared memory, so that the serial parts (promotions, evictions)
-// run on shared memory and the whole step costs a few global round trips.
+// K-policy: one CTA running policy_body (policy_body.cuh)
 __global__ void __launch_bounds__(kPolicyThreads) k_cache_policy(PolicyArgs a) {
-  __shared__ int s_tab[kPolicyThreads], s_miss[kPolicyThreads], s_src[kPolicyThreads];
-  __shared__ uint32_t s_cnt[kPolicyThreads], s_last[kPolicyThreads];
-  __shared__ unsigned char s_free[kPolicyMaxRun];
-  __shared__ uint64_t s_key[32];
-  __shared__ int s_id[33];
-  __shared__ unsigned long long s_routes;
-  __shared__ uint32_t s_now;
-  __shared__ int s_halve, s_nfree;
+  extern __shared__ __align__(16) unsigned char smem_pol[];
   pdl_wait();
   pdl_launch_dependents();
-  const int t = threadIdx.x, E = a.E, P = a.slot_hi - a.slot_lo;
-  const size_t row = (size_t)a.layer * E;
-  // stage (one round trip)
-  int c = 0;
-  if (t < E) {
-    s_tab[t] = a.table_row[t];
-    s_cnt[t] = a.cnt[row + t];
-    s_last[t] = a.last[row + t];
-    s_miss[t] = a.miss_ids[t];
-    s_src[t] = a.src_slot[t];
-    c = a.counts[t];
-  }
-  for (int j = t; j < P; j += blockDim.x) s_free[j] = a.freeslot[a.slot_lo + j] != 0;
-  if (t == 0) {
-    s_routes = 0;
-    s_now = a.stamp[a.layer] + 1;
-  }
-  __syncthreads();
-  // 1. promotion: misses and free slots in ascending order (one thread)
-  if (t == 0) {
-    const int nm = *a.n_miss, nh = a.n_act[1];
-    int f = 0;
-    for (int i = 0; i < nm; ++i) {
-      const int e = s_miss[i];
-      if (e < 0 || e >= E) {  // reported by the lookup's checks
-        a.miss_dst[i] = -1;
-        continue;
-      }
-      while (f < P && !s_free[f]) ++f;
-      int dst = s_src[e];  // its staging slot
-      if (f < P) {
-        dst = a.slot_lo + f;
-        s_free[f++] = 0;
-        s_tab[e] = dst;
-        a.src_slot[e] = dst;
-        if (a.meta) a.meta[2 * (nh + i)].y = dst;
-      }
-      a.miss_dst[i] = dst;
-    }
-  }
-  // 2. counts
-  if (c > 0) {
-    const uint64_t v = (uint64_t)s_cnt[t] + (uint64_t)c;
-    s_cnt[t] = v > kCountCap ? kCountCap : (uint32_t)v;
-    s_last[t] = s_now;
-    atomicAdd(&s_routes, (unsigned long long)c);
-  }
-  __syncthreads();
-  if (t == 0) {
-    const uint64_t ev = (uint64_t)a.stamp[a.L] + s_routes;
-    s_halve = ev >= kHalveEvents;
-    a.stamp[a.L] = s_halve ? 0u : (uint32_t)ev;
-    a.stamp[a.layer] = s_now;
-  }
-  __syncthreads();
-  if (s_halve) {
-    if (t < E) s_cnt[t] >>= 1;
-    for (size_t i = t; i < (size_t)a.L * E; i += blockDim.x)
-      if (i < row || i >= row + E) a.cnt[i] >>= 1;  // the other layers
-  }
-  // 3. boundary: evict down to the spares
-  if (t == 0) {
-    int nf = 0;
-    for (int j = 0; j < P; ++j) nf += s_free[j];
-    s_nfree = nf;
-  }
-  __syncthreads();
-  while (s_nfree < a.spares) {
-    const bool res = t < E && s_tab[t] >= 0;
-    const uint64_t key = res ? ((uint64_t)s_cnt[t] << 32) | s_last[t] : ~0ull;
-    const int victim = block_argmin(key, res ? t : -1, s_key, s_id);
-    if (victim < 0) break;
-    if (t == 0) {
-      const int f = s_tab[victim] - a.slot_lo;  // a slot outside the run: the lookup reports it
-      if (f >= 0 && f < P) {
-        s_free[f] = 1;
-        ++s_nfree;
-      }
-      s_tab[victim] = -1;
-    }
-    __syncthreads();
-  }
-  __syncthreads();
-  // write back
-  if (t < E) {
-    a.table_row[t] = s_tab[t];
-    a.cnt[row + t] = s_cnt[t];
-    a.last[row + t] = s_last[t];
-  }
-  for (int j = t; j < P; j += blockDim.x) a.freeslot[a.slot_lo + j] = s_free[j];
+  policy_body(a, smem_pol);
 }
 
 // One 16-byte read per 4 KiB page of the mapped host arena.  The device's
@@ -447,6 +297,19 @@ int cache_I(const expcache* c) { return c->I; }
 }  // namespace moe
 
 // ---- adaptive policy: host entry points -------------------------------------
+namespace moe {
+// the cache-owned fields of one layer's policy step (false: the policy is off)
+bool cache_policy_args(const expcache* c, int layer, PolicyArgs* a) {
+  if (c->spares < 0) return false;
+  memset(a, 0, sizeof(*a));
+  a->L = c->L; a->E = c->E; a->layer = layer;
+  a->slot_lo = c->slot_lo[layer]; a->slot_hi = c->slot_hi[layer]; a->spares = c->spares;
+  a->table_row = c->table + (size_t)layer * c->E;
+  a->cnt = c->cnt; a->last = c->last; a->stamp = c->stamp; a->freeslot = c->freeslot;
+  return true;
+}
+}  // namespace moe
+
 MOE_API moe_status expcache_set_policy(expcache* c, int spares_per_layer) {
   if (!c || spares_per_layer < 0) return MOE_ERR_INVALID_ARG;
   if (!c->partitioned || c->E > kPolicyThreads) return MOE_ERR_UNSUPPORTED;
@@ -503,15 +366,12 @@ MOE_API moe_status expcache_policy_step(expcache* c, int layer, const int32_t* c
   if (!c || !counts || !src_slot || !n_act || !miss_ids || !n_miss || !miss_dst || layer < 0 ||
       layer >= c->L)
     return MOE_ERR_INVALID_ARG;
-  if (c->spares < 0) return MOE_ERR_UNSUPPORTED;
   PolicyArgs a;
-  a.L = c->L; a.E = c->E; a.layer = layer;
-  a.slot_lo = c->slot_lo[layer]; a.slot_hi = c->slot_hi[layer]; a.spares = c->spares;
-  a.table_row = c->table + (size_t)layer * c->E;
-  a.cnt = c->cnt; a.last = c->last; a.stamp = c->stamp; a.freeslot = c->freeslot;
+  if (!cache_policy_args(c, layer, &a)) return MOE_ERR_UNSUPPORTED;
   a.counts = counts; a.src_slot = src_slot; a.n_act = n_act; a.miss_ids = miss_ids;
   a.n_miss = n_miss; a.miss_dst = miss_dst; a.meta = (int4*)meta;
-  if (launch_pdl(k_cache_policy, 1, kPolicyThreads, 0, (cudaStream_t)stream, a) != cudaSuccess)
+  if (launch_pdl(k_cache_policy, 1, kPolicyThreads, policy_smem_bytes(a.E, a.slot_hi - a.slot_lo),
+                 (cudaStream_t)stream, a) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
 }
@@ -527,7 +387,3 @@ MOE_API moe_status expcache_policy_state(const expcache* c, int* spares, const u
   *freeslot = c->freeslot;
   return MOE_OK;
 }
-
-namespace moe {
-bool cache_has_policy(const expcache* c) { return c->spares >= 0; }
-}  // namespace moe

@@ -3,6 +3,7 @@
 // ("Three tiers and the rules between them"): fp32 router weights, top-8 of
 // 288 experts per token, selection kept on the device.
 #include "permute_body.cuh"
+#include "policy_body.cuh"
 
 namespace moe {
 
@@ -465,7 +466,7 @@ __global__ void __launch_bounds__(kPermThreads, 2) k_route_permute_small(
     const uint16_t* __restrict__ x, const float* __restrict__ wr, const float* __restrict__ bias,
     int T, int H, int E, int k, float* __restrict__ logits, int32_t* __restrict__ ids,
     float* __restrict__ w, float* __restrict__ p_sel, unsigned int* __restrict__ done,
-    PermArgs pa, SharedGuArgs sg) {
+    PermArgs pa, SharedGuArgs sg, PolicyArgs pol) {
   extern __shared__ float sl[];  // top-k: [8 warps][E] floats; then the permutation's ints
   __shared__ int s_last;
   pdl_wait();
@@ -491,6 +492,10 @@ __global__ void __launch_bounds__(kPermThreads, 2) k_route_permute_small(
   else
     permute_body(ids, T * k, E, pa.counts, pa.offsets, pa.perm, pa.inv, pa.pad_offsets,
                  pa.pad_align, pa.status, pa.lk, reinterpret_cast<int*>(sl), 0);
+  if (pol.table_row) {  // the adaptive cache's step, on this CTA's lookup results
+    __syncthreads();
+    policy_body(pol, reinterpret_cast<unsigned char*>(sl));
+  }
   if (threadIdx.x == 0) *done = 0u;  // ready for the next call
 }
 
@@ -520,7 +525,7 @@ namespace moe {
 // Returns MOE_ERR_UNSUPPORTED when the shape does not qualify (the caller then
 // runs moe_route and the permutation separately).
 moe_status route_permute_small(const moe_route_args* a, const PermArgs& pa,
-                               const SharedGuArgs& sg, cudaStream_t s) {
+                               const SharedGuArgs& sg, const PolicyArgs* pol, cudaStream_t s) {
   moe_status st = route_check(a);
   if (st != MOE_OK) return st;
   if (a->T < 1 || a->T > kGemvMaxT || !a->logits || !a->workspace ||
@@ -533,6 +538,8 @@ moe_status route_permute_small(const moe_route_args* a, const PermArgs& pa,
   size_t smem = (size_t)8 * a->E * sizeof(float);
   if (permute_smem_bytes(a->E) > smem) smem = permute_smem_bytes(a->E);
   if (sg.Is > 0 && (size_t)a->H * sizeof(float) > smem) smem = (size_t)a->H * sizeof(float);
+  if (pol && policy_smem_bytes(a->E, pol->slot_hi - pol->slot_lo) > smem)
+    smem = policy_smem_bytes(a->E, pol->slot_hi - pol->slot_lo);
   static bool attr = false;
   if (smem > 48 * 1024 && !attr) {
     if (cudaFuncSetAttribute(k_route_permute_small, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -546,7 +553,8 @@ moe_status route_permute_small(const moe_route_args* a, const PermArgs& pa,
   const int sh_ctas = sg.Is > 0 ? (sg.Is + kShRows - 1) / kShRows : 0;
   if (launch_pdl(k_route_permute_small, a->E + sh_ctas, kPermThreads, smem, s,
                  (const uint16_t*)a->x, a->w_router, a->bias, a->T, a->H, a->E, a->k, a->logits,
-                 a->ids, a->w, a->p_sel, (unsigned int*)a->workspace, pa, sg) != cudaSuccess)
+                 a->ids, a->w, a->p_sel, (unsigned int*)a->workspace, pa, sg,
+                 pol ? *pol : PolicyArgs{}) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
 }
