@@ -764,9 +764,11 @@ constexpr int kQuantXMaxK = 8192;  // H up to 8192
 
 // K-hq: h -> NVFP4 for the padded rows of planned experts [g0, g1): CTA
 // (j - g0, part) takes a quarter of expert plan_e[j]'s rows, one warp per
-// row; padding rows are zeroed.
+// row; padding rows are zeroed.  Three CTAs per SM for rows up to 2048 values
+// (80 registers, a few spilled): 101 -> 91 us for the 4096-token layer's h;
+// four CTAs spilled more and took 107.
 template <int KMAX>
-__global__ void __launch_bounds__(256) k_quant_h(
+__global__ void __launch_bounds__(256, KMAX <= 2048 ? 3 : 1) k_quant_h(
     const float* __restrict__ h32, int K, int g0, int g1, const int32_t* __restrict__ plan_e,
     const int32_t* __restrict__ plan_n, const int32_t* __restrict__ offsets,
     const int32_t* __restrict__ pad_offsets, const int32_t* __restrict__ perm,
