@@ -62,8 +62,9 @@ def lib():
         L.oracle_nvfp4_quant.argtypes = [vp, i32, vp, vp, vp]
         L.oracle_expert.argtypes = [vp, i32, i32, vp, vp, i32, vp]
         L.oracle_shared.argtypes = [vp, vp, vp, i32, i32, vp, i32, vp]
+        L.oracle_renorm_skip.argtypes = [vp, vp, i32, i32, vp, d, vp, vp]
         L.oracle_layer_forward.argtypes = [vp, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp,
-                                           vp, vp, vp, i32, vp, vp, vp, vp, vp]
+                                           vp, vp, vp, i32, vp, d, vp, vp, vp, vp, vp]
         L.oracle_layer_forward.restype = i32
         L.oracle_set_defect.argtypes = [i32]
         L.oracle_quant_flip_delta.argtypes = [vp, i32, vp]
@@ -198,11 +199,12 @@ def shared(wg, wu, wd, x, round_h_bf16=False):
 
 
 def layer_forward(x, H, I, E, k, Wr, bias, records, g, shared_w=None, mode=0,
-                  return_bound=False):
+                  return_bound=False, resident=None, tau=0.0):
     """y [T,H] fp64 plus ids, w, p_sel (and, with return_bound, the
     rounding-boundary slack [T,H] of the prefill numerics, zero in mode 0).
     ``records`` maps expert id -> uint8 record array (a dict or a sequence
-    with None for absent experts)."""
+    with None for absent experts).  resident [E] (bool) and tau: the
+    renorm-skip of low-weight misses (None: exact)."""
     x = np.ascontiguousarray(x, np.uint16)
     T = x.shape[0]
     keep = []
@@ -224,6 +226,7 @@ def layer_forward(x, H, I, E, k, Wr, bias, records, g, shared_w=None, mode=0,
         _p(x), T, H, I, E, k, Is, _p(np.ascontiguousarray(Wr, np.float32)),
         _p(None if bias is None else np.ascontiguousarray(bias, np.float32)), ptrs,
         _p(np.ascontiguousarray(g, np.float32)), _p(sg), _p(su), _p(sd), mode,
+        _p(None if resident is None else np.ascontiguousarray(resident, np.uint8)), float(tau),
         _p(y), _p(ids), _p(w), _p(p), _p(bound))
     if rc:
         raise ValueError("oracle_layer_forward: a selected expert has no record")
@@ -260,3 +263,17 @@ class CachePolicy:
             _p(self.table), _p(self.cnt), _p(self.last), _p(self.stamp), _p(self.events),
             _p(self.free), _p(counts), _p(prom))
         return prom[:n].copy()
+
+
+def renorm_skip(ids, w, resident, tau):
+    """The renorm-skip step alone: (w_eff, keep) for routes ids [T,k] with
+    weights w [T,k] (fp64), resident [E] bool."""
+    ids = np.ascontiguousarray(ids, np.int32)
+    w = np.ascontiguousarray(w, np.float64)
+    T, k = ids.shape
+    w_eff = np.empty((T, k), np.float64)
+    keep = np.empty((T, k), np.uint8)
+    lib().oracle_renorm_skip(_p(ids), _p(w), T, k,
+                             _p(np.ascontiguousarray(resident, np.uint8)), float(tau),
+                             _p(w_eff), _p(keep))
+    return w_eff, keep.astype(bool)

@@ -23,12 +23,17 @@
  *      G = amax/(6*448) (1 if amax == 0), s_b = e4m3_rne(amax_b / (6 G)),
  *      q = e2m1_rne_sat(v / (s_b G)), all in IEEE fp32 with correctly
  *      rounded division; the shared expert's h is rounded to bf16.
- *   7. cache residency is not an input: the output depends on (x, weights).
+ *   7. cache residency is not an input: the output depends on (x, weights)
+ *      (except under the optional renorm-skip of item 9).
  *   8. the adaptive cache's bookkeeping ("Project Maya" page, sections "How
  *      'most-used' is measured", "Promotion on every miss, eviction at the
  *      boundary" and "VRAM: one partition per layer"), an integer state
  *      machine simulated forward by forward (oracle_cache_policy_step).
  * Compiled with -ffp-contract=off so fp32 steps are single roundings.
+ *   9. optional renorm-skip (Strata-GLM blog, section "Uncensoring without
+ *      touching the weights"; oracle_renorm_skip): a token's cache-miss
+ *      routes with weight below tau are dropped and its remaining weights
+ *      renormalised.
  */
 #include <math.h>
 #include <stdint.h>
@@ -496,18 +501,49 @@ ORC_API void oracle_shared(const uint16_t* wg, const uint16_t* wu, const uint16_
  * that rounding-boundary flips of the intermediate quantisations (h to NVFP4,
  * shared h to bf16) can move each output, for comparisons with another
  * implementation of the same rounding steps. */
+/* --renorm-skip (Strata-GLM blog, "Uncensoring without touching the weights"):
+ * a route of token t whose expert is a cache miss (resident[e] == 0) and
+ * whose combine weight is below tau is dropped - never gathered or computed -
+ * and the token's remaining weights are renormalised to sum to 1.  keep[r] = 1 for kept routes; w_eff
+ * the renormalised weights (0 for dropped routes).  tau = 0 keeps every route
+ * and w_eff = w. */
+ORC_API void oracle_renorm_skip(const int32_t* ids, const double* w, int T, int k,
+                                const uint8_t* resident, double tau, double* w_eff,
+                                uint8_t* keep) {
+  for (int t = 0; t < T; ++t) {
+    double sum = 0.0;
+    for (int j = 0; j < k; ++j) {
+      const int r = t * k + j;
+      keep[r] = !(resident && !resident[ids[r]] && w[r] < tau);
+      if (keep[r]) sum += w[r];
+    }
+    for (int j = 0; j < k; ++j) {
+      const int r = t * k + j;
+      w_eff[r] = keep[r] ? w[r] / sum : 0.0;
+    }
+  }
+}
+
+/* The layer.  resident/tau: the renorm-skip above (resident == NULL: exact). */
 ORC_API int oracle_layer_forward(const uint16_t* x, int T, int H, int I, int E, int k, int Is,
                                  const float* Wr, const float* bias, const uint8_t* const* rec,
                                  const float* g, const uint16_t* sg, const uint16_t* su,
-                                 const uint16_t* sd, int mode, double* y, int32_t* ids_out,
-                                 double* w_out, double* p_out, double* ybound) {
+                                 const uint16_t* sd, int mode, const uint8_t* resident,
+                                 double tau, double* y, int32_t* ids_out, double* w_out,
+                                 double* p_out, double* ybound) {
   tables_init();
   int32_t* ids = (int32_t*)malloc(sizeof(int32_t) * (size_t)T * k);
   double* w = (double*)malloc(sizeof(double) * (size_t)T * k);
   double* p = (double*)malloc(sizeof(double) * (size_t)T * k);
+  double* weff = (double*)malloc(sizeof(double) * (size_t)T * k);
+  uint8_t* keep = (uint8_t*)malloc((size_t)T * k);
   oracle_route(x, Wr, bias, T, H, E, k, ids, w, p, NULL, NULL);
+  oracle_renorm_skip(ids, w, T, k, resident, resident ? tau : 0.0, weff, keep);
   for (int r = 0; r < T * k; ++r)
-    if (!rec[ids[r]]) { free(ids); free(w); free(p); return 2; }
+    if (keep[r] && !rec[ids[r]]) {
+      free(ids); free(w); free(p); free(weff); free(keep);
+      return 2;
+    }
   double* xd = (double*)malloc(sizeof(double) * (size_t)H);
   double* xq = (double*)malloc(sizeof(double) * (size_t)H);
   float* xf = (float*)malloc(sizeof(float) * (size_t)H);
@@ -524,8 +560,9 @@ ORC_API int oracle_layer_forward(const uint16_t* x, int T, int H, int I, int E, 
     if (ybound) for (int c = 0; c < H; ++c) ybound[(size_t)t * H + c] = 0.0;
     for (int c = 0; c < H; ++c) yt[c] = 0.0;
     for (int j = 0; j < k; ++j) {
+      if (!keep[(size_t)t * k + j]) continue;
       int e = ids[(size_t)t * k + j];
-      double wj = w[(size_t)t * k + j];
+      double wj = weff[(size_t)t * k + j];
       orc_expert_impl(rec[e], H, I, g + 3 * e, xq, mode == 1, o, fabs(wj), bt);
       if (g_defect == ORC_DEFECT_SCALING_2_5) wj *= 2.5;
       for (int c = 0; c < H; ++c) yt[c] += wj * o[c];
@@ -538,7 +575,7 @@ ORC_API int oracle_layer_forward(const uint16_t* x, int T, int H, int I, int E, 
   if (ids_out) memcpy(ids_out, ids, sizeof(int32_t) * (size_t)T * k);
   if (w_out) memcpy(w_out, w, sizeof(double) * (size_t)T * k);
   if (p_out) memcpy(p_out, p, sizeof(double) * (size_t)T * k);
-  free(ids); free(w); free(p); free(xd); free(xq); free(xf); free(o);
+  free(ids); free(w); free(p); free(weff); free(keep); free(xd); free(xq); free(xf); free(o);
   return 0;
 }
 

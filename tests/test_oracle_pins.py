@@ -175,3 +175,43 @@ def test_negative_control_tie_rule():
     with oracle.defect("tie_high_id"):
         ids_d, *_ = oracle.route(x, Wr, None, k)
     assert ids[0].tolist() == [2, 1] and ids_d[0].tolist() == [2, 4]
+
+
+def test_renorm_skip_drops_low_weight_misses_and_renormalises(tiny):
+    """The renorm-skip step: only misses below tau drop, the kept weights sum
+    to 1 and keep their ratios; tau = 0 (or every expert resident) changes
+    nothing; with one route dropped the layer equals the kept experts' own
+    outputs weighted by the renormalised weights (brute force)."""
+    wl, x, Wr = tiny
+    ids, w, p, logits, gap = oracle.route(x, Wr, None, wl.k)
+    T, k = ids.shape
+    resident = np.zeros(wl.E, bool)
+    resident[::2] = True
+    for tau in (0.0, 0.3, 0.45, 0.49):
+        w_eff, keep = oracle.renorm_skip(ids, w, resident, tau)
+        drop = (~resident[ids]) & (w < tau)
+        assert np.array_equal(~keep, drop)
+        assert np.allclose(w_eff.sum(1), 1.0, atol=1e-14)
+        assert np.all(w_eff[~keep] == 0.0)
+        for t in range(T):
+            kk = keep[t]
+            assert np.allclose(w_eff[t, kk], w[t, kk] / w[t, kk].sum(), rtol=1e-15)
+    w_eff, keep = oracle.renorm_skip(ids, w, np.ones(wl.E, bool), 0.49)
+    assert keep.all() and np.allclose(w_eff, w, rtol=1e-15)
+    # layer level: records for every expert, one token whose lower route misses
+    recs = gen.expert_records(wl.seed, 0, list(range(wl.E)), wl.H, wl.I)
+    g = gen.global_scales(wl.seed, 0, wl.E)
+    t = int(np.argmax(w[:, 1] < 0.45))
+    assert w[t, 1] < 0.45
+    xt = x[t:t + 1]
+    res = np.ones(wl.E, bool)
+    res[ids[t, 1]] = False
+    y_skip = oracle.layer_forward(xt, wl.H, wl.I, wl.E, wl.k, Wr, None, recs, g,
+                                  resident=res, tau=0.45)[0]
+    xd = _bf16_to_f64(xt[0])
+    o0 = oracle.expert(recs[ids[t, 0]], wl.H, wl.I, g[ids[t, 0]], xd)
+    assert np.allclose(y_skip[0], o0, rtol=1e-12, atol=1e-12)  # the kept route alone, weight 1
+    y_exact = oracle.layer_forward(xt, wl.H, wl.I, wl.E, wl.k, Wr, None, recs, g)[0]
+    y_res = oracle.layer_forward(xt, wl.H, wl.I, wl.E, wl.k, Wr, None, recs, g,
+                                 resident=np.ones(wl.E, bool), tau=0.45)[0]
+    assert np.array_equal(y_exact, y_res)
