@@ -60,7 +60,8 @@ def _hot_set(wl: gen.Workload, layer: int, bias_rank, saliency_order, drop: int 
 def build(wl: gen.Workload, layers: int | None = None, T_max: int | None = None,
           n_stage: int | None = None, saliency_order=None, prefill_min_tokens: int | None = None,
           alias_host_records: bool = False, resident=None, slot_alias: int = 0,
-          stream=None, prefill_group: int | None = None, spares: int = 0) -> DeviceWorkload:
+          stream=None, prefill_group: int | None = None, spares: int = 0,
+          skip_tau: float = 0.0) -> DeviceWorkload:
     """Device-resident layer(s) of workload `wl`.
 
     layers: how many of the workload's layers to build (default: all).
@@ -69,6 +70,7 @@ def build(wl: gen.Workload, layers: int | None = None, T_max: int | None = None,
     alias_host_records: store one host copy per expert id shared by all layers
       (the host-index table maps every layer to it) when host memory is short;
       the records then repeat across layers for both the GPU and the oracle.
+    skip_tau: > 0 turns on the layers' renorm-skip of low-weight misses.
     spares: > 0 turns on the adaptive cache: each layer's slot run gets that
       many free slots beyond its residents (by default the hot set less its
       `spares` coldest, so the run keeps the hot budget), every expert has a host record
@@ -180,7 +182,8 @@ def build(wl: gen.Workload, layers: int | None = None, T_max: int | None = None,
         shared.append(sh)
         mls.append(MoELayer(cache, l, wr, g, k, bias=b, shared=sh, T_max=T_max,
                             prefill_min_tokens=pmin,
-                            prefill_group=wl.group if prefill_group is None else prefill_group))
+                            prefill_group=wl.group if prefill_group is None else prefill_group,
+                            skip_tau=skip_tau))
     s.synchronize()
     return DeviceWorkload(wl, L, cache, mls, w_router, gscale, gscale_host, bias, bias_host,
                           shared, resident, host_arena, record_layer=rec_layer)

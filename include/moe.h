@@ -122,7 +122,9 @@ moe_status moe_route(const moe_route_args* a, void* stream);
  * p-th route in (expert asc, r asc) order - a stable sort, so the result is
  * unique; inv[r] = p.  pad_offsets (optional) is the exclusive scan of the
  * counts rounded up to multiples of pad_align (the prefill staging layout).
- * Out-of-range ids set MOE_ERR_DEVICE in *status and are dropped.
+ * Out-of-range ids set MOE_ERR_DEVICE in *status and are dropped; an id of
+ * -1 is a dropped route (the renorm-skip) and is left out without an error.
+ * A route left out is not counted and gets inv[r] = -1.
  * One thread block per 1024 routes (each block histograms all routes, so
  * the blocks never wait on one another); T*k <= 1<<20.
  */
@@ -368,6 +370,15 @@ moe_status moe_combine(const moe_combine_args* a, void* stream);
  * path (experts walked in groups of prefill_group through the staging
  * layout), otherwise DECODE.  The decode path never synchronises with the
  * host and can be captured in a CUDA graph.
+ *
+ * skip_tau > 0 turns on the renorm-skip (Strata-GLM blog, section
+ * "Uncensoring without touching the weights"): a route whose expert is not
+ * resident in the layer's cache when the forward looks it up and whose
+ * combine weight w is below skip_tau is dropped - never gathered or computed
+ * - and its token's remaining weights are renormalised to sum to 1.  An
+ * approximation of the layer; the routing outputs (ids, w, p_sel) stay the
+ * router's.  0 <= skip_tau < 1/k (the top route is always kept), else
+ * MOE_ERR_INVALID_ARG.
  */
 typedef struct moe_layer moe_layer;
 
@@ -384,6 +395,7 @@ typedef struct {
   int T_max;
   int prefill_min_tokens;  /* 0 = always DECODE                           */
   int prefill_group;       /* experts per prefill group (e.g. 64)         */
+  float skip_tau;          /* renorm-skip threshold, 0 = exact (below)    */
 } moe_layer_desc;
 
 moe_status moe_layer_create(const moe_layer_desc* d, moe_layer** out);

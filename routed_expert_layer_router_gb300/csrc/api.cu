@@ -30,7 +30,10 @@ moe_status launch_permute(const int32_t* ids, int T, int k, int E, int32_t* coun
 void cache_lookup_args(const expcache* c, int layer, int32_t* src_slot, int32_t* act_list,
                        int32_t* n_act, int32_t* miss_ids, int32_t* n_miss, LookupArgs* out);
 moe_status route_permute_small(const moe_route_args* a, const PermArgs& pa,
-                               const SharedGuArgs& sg, const PolicyArgs* pol, cudaStream_t s);
+                               const SharedGuArgs& sg, const PolicyArgs* pol,
+                               const SkipArgs* sk, cudaStream_t s);
+moe_status launch_route_skip(const SkipArgs& sk, const int32_t* ids, const float* w, int T, int k,
+                             int E, cudaStream_t s);
 bool cache_policy_args(const expcache* c, int layer, PolicyArgs* a);
 }  // namespace moe
 
@@ -65,7 +68,7 @@ MOE_API const char* moe_status_string(moe_status s) {
   }
 }
 
-MOE_API int moe_abi_version(void) { return 3; }
+MOE_API int moe_abi_version(void) { return 4; }
 
 static moe_status ensure_setup() {
   static int done = 0;
@@ -134,6 +137,8 @@ struct moe_layer {
   void* route_ctl;
   int4* act_meta;  // compact per-expert records of the small-route path
   int32_t* miss_dst;  // adaptive cache: the slot each miss is gathered into
+  int32_t* ids_eff;   // renorm-skip: the kept routes' experts (-1: dropped)
+  float* w_eff;       // renorm-skip: the kept routes' renormalised weights
   void* ffn_ws;
   size_t ffn_ws_bytes;
   int last_T;
@@ -154,6 +159,7 @@ MOE_API moe_status moe_layer_create(const moe_layer_desc* d, moe_layer** out) {
   if (d->H != cache_H(d->cache) || d->I != cache_I(d->cache) || d->E != cache_E(d->cache))
     return MOE_ERR_INVALID_ARG;
   if (d->Is > 0 && (!d->s_gate || !d->s_up || !d->s_down)) return MOE_ERR_INVALID_ARG;
+  if (!(d->skip_tau >= 0.f) || d->skip_tau * (float)d->k >= 1.f) return MOE_ERR_INVALID_ARG;
   if (d->H % 256 || d->I % 128 || d->Is % 128 || d->E > 1024) return MOE_ERR_UNSUPPORTED;
   moe_status st = ensure_setup();
   if (st != MOE_OK) return st;
@@ -187,7 +193,9 @@ MOE_API moe_status moe_layer_create(const moe_layer_desc* d, moe_layer** out) {
       prefill ? (size_t)T * H * 4 : 0, /* y_acc */
       l->ffn_ws_bytes,
       kRouteCtlBytes + kTileCtlBytes, /* route_ctl, then the combine's tile counters */
-      (size_t)E * 4       /* miss_dst */};
+      (size_t)E * 4,      /* miss_dst */
+      (size_t)T * k * 4,  /* ids_eff */
+      (size_t)T * k * 4   /* w_eff */};
   const int n = (int)(sizeof(sizes) / sizeof(sizes[0]));
   size_t total = 0;
   for (int i = 0; i < n; ++i) total += align256(sizes[i]);
@@ -198,7 +206,7 @@ MOE_API moe_status moe_layer_create(const moe_layer_desc* d, moe_layer** out) {
   }
   l->ws_bytes = total;
   uint8_t* p = (uint8_t*)l->ws;
-  void* ptrs[22];
+  void* ptrs[24];
   for (int i = 0; i < n; ++i) {
     ptrs[i] = sizes[i] ? p : nullptr;
     p += align256(sizes[i]);
@@ -225,6 +233,8 @@ MOE_API moe_status moe_layer_create(const moe_layer_desc* d, moe_layer** out) {
   l->ffn_ws = ptrs[19];
   l->route_ctl = ptrs[20];
   l->miss_dst = (int32_t*)ptrs[21];
+  l->ids_eff = (int32_t*)ptrs[22];
+  l->w_eff = (float*)ptrs[23];
   if (cudaMemset(l->ws, 0, total) != cudaSuccess) {
     cudaFree(l->ws);
     free(l);
@@ -300,15 +310,19 @@ MOE_API moe_status moe_layer_forward(moe_layer* l, const void* x, int T, void* y
     pol.miss_ids = l->miss_ids; pol.n_miss = l->n_miss; pol.miss_dst = l->miss_dst;
     pol.meta = small_routes ? l->act_meta : nullptr;
   }
-  st = route_permute_small(&ra, pa, sg, policy ? &pol : nullptr, s);
+  // renorm-skip: low-weight misses dropped before the permutation
+  const bool skip = d.skip_tau > 0.f;
+  SkipArgs sk = {lk.table, lk.slot_lo, lk.slot_hi, d.skip_tau, l->ids_eff, l->w_eff};
+  st = route_permute_small(&ra, pa, sg, policy ? &pol : nullptr, skip ? &sk : nullptr, s);
   const bool policy_done = policy && st == MOE_OK;
   const bool shared_gu_done = st == MOE_OK && sg.Is > 0;
   const int4* act_meta = (st == MOE_OK && small_routes) ? l->act_meta : nullptr;
   if (st == MOE_ERR_UNSUPPORTED) {
     if ((st = moe_route(&ra, stream)) != MOE_OK) return st;
     layer_mark(l);
-    st = launch_permute(l->ids, T, d.k, d.E, l->counts, l->offsets, l->perm, l->inv,
-                        pa.pad_offsets, 128, l->status, lk, s);
+    if (skip && (st = launch_route_skip(sk, l->ids, l->w, T, d.k, d.E, s)) != MOE_OK) return st;
+    st = launch_permute(skip ? l->ids_eff : l->ids, T, d.k, d.E, l->counts, l->offsets, l->perm,
+                        l->inv, pa.pad_offsets, 128, l->status, lk, s);
   }
   if (st != MOE_OK) return st;
   layer_mark(l);
@@ -334,7 +348,7 @@ MOE_API moe_status moe_layer_forward(moe_layer* l, const void* x, int T, void* y
   fa.x = x; fa.cache = d.cache; fa.gscale = d.gscale;
   fa.src_slot = l->src_slot; fa.act_list = l->act_list; fa.n_act = l->n_act;
   fa.offsets = l->offsets; fa.pad_offsets = l->pad_offsets; fa.perm = l->perm; fa.inv = l->inv;
-  fa.w = l->w;
+  fa.w = skip ? l->w_eff : l->w;
   fa.n_stage = n_stage;
   fa.prefill_group = d.prefill_group;
   fa.Is = d.Is; fa.s_gate = d.s_gate; fa.s_up = d.s_up; fa.s_down = d.s_down;

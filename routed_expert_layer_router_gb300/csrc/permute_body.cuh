@@ -10,6 +10,48 @@ constexpr int kPermThreads = 1024;
 constexpr int kPermWarps = kPermThreads / 32;
 
 // outputs of the permutation (see moe_permute) and the optional lookup
+// an id of -1 is a dropped route (the renorm-skip): not listed, inv = -1, no error
+constexpr int kDroppedRoute = -1;
+
+// The renorm-skip (Strata-GLM blog, "Uncensoring without touching the
+// weights"), token t by one thread: route r = t*k + j (expert ids[r], weight
+// w[r]) is dropped when its expert is not resident in the layer's slot run
+// and w[r] < tau: ids_eff[r] = kDroppedRoute, w_eff[r] = 0; the kept routes
+// keep their expert and get their weight divided by the token's kept sum.
+// ids and w are read through L2 (the caller may have written them in the same
+// kernel).
+struct SkipArgs {
+  const int32_t* table;  // the layer's row of the slot table
+  int slot_lo, slot_hi;
+  float tau;             // 0: off
+  int32_t* ids_eff;
+  float* w_eff;
+};
+
+__device__ __forceinline__ void skip_token(const SkipArgs& sk, const int32_t* ids, const float* w,
+                                           int t, int k, int E) {
+  float sum = 0.f;
+  unsigned keep = 0u;  // k <= 32
+  for (int j = 0; j < k; ++j) {
+    const int r = t * k + j;
+    const int e = __ldcg(ids + r);
+    const float wr = __ldcg(w + r);
+    int slot = -1;
+    if (e >= 0 && e < E) slot = sk.table[e];
+    const bool resident = slot >= sk.slot_lo && slot < sk.slot_hi;
+    if (resident || !(wr < sk.tau)) {
+      keep |= 1u << j;
+      sum += wr;
+    }
+  }
+  for (int j = 0; j < k; ++j) {
+    const int r = t * k + j;
+    const bool kept = (keep >> j) & 1u;
+    sk.ids_eff[r] = kept ? __ldcg(ids + r) : kDroppedRoute;
+    sk.w_eff[r] = kept ? __ldcg(w + r) / sum : 0.f;
+  }
+}
+
 struct PermArgs {
   int32_t *counts, *offsets, *perm, *inv, *pad_offsets;
   int pad_align;
@@ -128,7 +170,7 @@ __device__ __forceinline__ void permute_body(const int32_t* ids, int n, int E,
   for (int r = tid; r < n; r += kPermThreads) {
     const int e = __ldcg(ids + r);
     if (e >= 0 && e < E) atomicAdd(r < r0 ? &s_pre[e] : &s_cnt[e], 1);
-    else if (lead) set_status(status, MOE_ERR_DEVICE);
+    else if (lead && e != kDroppedRoute) set_status(status, MOE_ERR_DEVICE);
   }
   __syncthreads();
   // exclusive scans of counts (and of padded counts); E <= 1024 = one per thread
@@ -201,7 +243,7 @@ __device__ __forceinline__ void permute_small(const int32_t* ids, int n, int E,
     const int r = lane;
     int e = r < n ? __ldcg(ids + r) : -1;
     const bool valid = r < n && e >= 0 && e < E;
-    if (r < n && !valid) set_status(status, MOE_ERR_DEVICE);
+    if (r < n && !valid && e != kDroppedRoute) set_status(status, MOE_ERR_DEVICE);
     if (!valid) e = -1;
     s_ids[r] = e;
     // rank among the valid routes by (expert, route), and whether this route

@@ -466,7 +466,7 @@ __global__ void __launch_bounds__(kPermThreads, 2) k_route_permute_small(
     const uint16_t* __restrict__ x, const float* __restrict__ wr, const float* __restrict__ bias,
     int T, int H, int E, int k, float* __restrict__ logits, int32_t* __restrict__ ids,
     float* __restrict__ w, float* __restrict__ p_sel, unsigned int* __restrict__ done,
-    PermArgs pa, SharedGuArgs sg, PolicyArgs pol) {
+    PermArgs pa, SharedGuArgs sg, PolicyArgs pol, SkipArgs sk) {
   extern __shared__ float sl[];  // top-k: [8 warps][E] floats; then the permutation's ints
   __shared__ int s_last;
   pdl_wait();
@@ -486,11 +486,17 @@ __global__ void __launch_bounds__(kPermThreads, 2) k_route_permute_small(
   stage_logits(logits, 0, T, E, sl);
   if (wid < T) topk_token(sl + (size_t)wid * E, wid, E, k, ids, w, p_sel);
   __syncthreads();  // ids written by this CTA: read back through L2 below
+  const int32_t* pids = ids;
+  if (sk.tau > 0.f) {  // the renorm-skip: the permutation takes the kept routes
+    if ((int)threadIdx.x < T) skip_token(sk, ids, w, threadIdx.x, k, E);
+    __syncthreads();
+    pids = sk.ids_eff;
+  }
   if (T * k <= 32 && !pa.pad_offsets)
-    permute_small(ids, T * k, E, pa.counts, pa.offsets, pa.perm, pa.inv, pa.status, pa.lk,
+    permute_small(pids, T * k, E, pa.counts, pa.offsets, pa.perm, pa.inv, pa.status, pa.lk,
                   reinterpret_cast<int*>(sl));
   else
-    permute_body(ids, T * k, E, pa.counts, pa.offsets, pa.perm, pa.inv, pa.pad_offsets,
+    permute_body(pids, T * k, E, pa.counts, pa.offsets, pa.perm, pa.inv, pa.pad_offsets,
                  pa.pad_align, pa.status, pa.lk, reinterpret_cast<int*>(sl), 0);
   if (pol.table_row) {  // the adaptive cache's step, on this CTA's lookup results
     __syncthreads();
@@ -525,7 +531,8 @@ namespace moe {
 // Returns MOE_ERR_UNSUPPORTED when the shape does not qualify (the caller then
 // runs moe_route and the permutation separately).
 moe_status route_permute_small(const moe_route_args* a, const PermArgs& pa,
-                               const SharedGuArgs& sg, const PolicyArgs* pol, cudaStream_t s) {
+                               const SharedGuArgs& sg, const PolicyArgs* pol,
+                               const SkipArgs* sk, cudaStream_t s) {
   moe_status st = route_check(a);
   if (st != MOE_OK) return st;
   if (a->T < 1 || a->T > kGemvMaxT || !a->logits || !a->workspace ||
@@ -554,7 +561,24 @@ moe_status route_permute_small(const moe_route_args* a, const PermArgs& pa,
   if (launch_pdl(k_route_permute_small, a->E + sh_ctas, kPermThreads, smem, s,
                  (const uint16_t*)a->x, a->w_router, a->bias, a->T, a->H, a->E, a->k, a->logits,
                  a->ids, a->w, a->p_sel, (unsigned int*)a->workspace, pa, sg,
-                 pol ? *pol : PolicyArgs{}) != cudaSuccess)
+                 pol ? *pol : PolicyArgs{}, sk ? *sk : SkipArgs{}) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+// the renorm-skip alone (more than 8 tokens: after moe_route, before the permutation)
+__global__ void __launch_bounds__(256) k_route_skip(SkipArgs sk, const int32_t* ids,
+                                                    const float* w, int T, int k, int E) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t < T) skip_token(sk, ids, w, t, k, E);
+}
+
+moe_status launch_route_skip(const SkipArgs& sk, const int32_t* ids, const float* w, int T, int k,
+                             int E, cudaStream_t s) {
+  if (T <= 0) return MOE_OK;
+  if (launch_pdl(k_route_skip, (T + 255) / 256, 256, 0, s, sk, ids, w, T, k, E) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
 }

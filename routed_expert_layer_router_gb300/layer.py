@@ -138,7 +138,7 @@ class MoELayer:
     def __init__(self, cache: ExpertCache, layer: int, w_router: torch.Tensor,
                  gscale: torch.Tensor, k: int, bias: torch.Tensor | None = None,
                  shared=None, T_max: int = 1, prefill_min_tokens: int = 0,
-                 prefill_group: int = 64):
+                 prefill_group: int = 64, skip_tau: float = 0.0):
         self.cache, self.layer = cache, layer
         self.H, self.I, self.E, self.k = cache.H, cache.I, cache.E, k
         self._keep = [w_router, gscale, bias, shared]
@@ -154,6 +154,7 @@ class MoELayer:
         d.T_max = T_max
         d.prefill_min_tokens = prefill_min_tokens
         d.prefill_group = prefill_group
+        d.skip_tau = skip_tau
         self.T_max = T_max
         self.handle = moe.moe_layer_create(d)
 

@@ -59,7 +59,8 @@ class moe_layer_desc(ctypes.Structure):
     _fields_ = [("H", i32), ("I", i32), ("E", i32), ("k", i32), ("Is", i32),
                 ("w_router", vp), ("bias", vp), ("gscale", vp), ("s_gate", vp), ("s_up", vp),
                 ("s_down", vp), ("cache", vp), ("layer", i32), ("T_max", i32),
-                ("prefill_min_tokens", i32), ("prefill_group", i32)]
+                ("prefill_min_tokens", i32), ("prefill_group", i32),
+                ("skip_tau", ctypes.c_float)]
 
 
 # every function declared in include/moe.h: name -> (restype, argtypes)
