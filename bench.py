@@ -19,6 +19,9 @@ The same run also measures (the `also` object), each in its own bounded pass:
            hit rate, gather GB/s against the measured host->device link;
   flat     8 layers, 64 tokens per step, unbiased routing, 72 experts per layer
            cached by saliency, misses gathered from pinned host memory;
+  stack_skip  the stack with the renorm-skip (tau 0.05): misses with a
+           combine weight below tau dropped, the token's weights renormalised;
+           with its error against the exact layer on the same inputs;
   stack_adaptive  the stack with the adaptive cache: per layer the 63 hottest
            resident at start and 3 spare slots, misses promoted into them,
            decayed-LFU eviction between forwards.
@@ -46,7 +49,9 @@ METRIC = "MoE-layer tokens/s (decode, 4096-tok prefill); % of HBM / FP4-TC / PCI
 UNIT = "tokens/s"
 # the adaptive cache keeps three spare slots per layer ("Project Maya" page)
 ADAPTIVE_SPARES = 3
-ADAPTIVE_WARM_TOKENS = 256  # about one halving period of its counts on the 16-layer stack
+ADAPTIVE_WARM_TOKENS = 256
+# renorm-skip threshold of the stack_skip pass (an approximation of the layer)
+SKIP_TAU = 0.05  # about one halving period of its counts on the 16-layer stack
 FP4_OVER_BF16 = 6.0  # nominal dense FP4 / dense bf16 tensor throughput (13.5 / 2.25)
 # DRAM bytes (read + write) of one k_decode_gu launch on the full decode layer, from
 # one ncu capture of the current kernel (profiles/k_decode_gu_decode-layer.md); set to
@@ -577,7 +582,38 @@ def _saliency_order(torch, moe, gen, wl, layers, dev, n_tokens=512):
     return orders
 
 
-def bench_multilayer(args, torch, moe, gen, gd, dev, name, link_gbs, spares=0):
+def _skip_error(torch, dw, xs, i0, n, L, T):
+    """The renorm-skip against the exact layer on the same cache and inputs:
+    per layer and token max |y_skip - y_exact| / rms(y_exact), and the routes
+    dropped per layer forward (one token per forward: k - active experts)."""
+    from routed_expert_layer_router_gb300 import moe
+    from routed_expert_layer_router_gb300.layer import MoELayer, device_view
+    wl = dw.wl
+    errs, dropped = [], []
+    exact = [MoELayer(dw.cache, l, dw.w_router[l], dw.gscale[l], wl.k, bias=dw.bias[l],
+                      shared=dw.shared[l], T_max=T) for l in range(L)]
+    try:
+        ys = torch.empty((T, wl.H), dtype=torch.bfloat16, device=xs.device)
+        ye = torch.empty_like(ys)
+        for i in range(i0, i0 + n):
+            for l in range(L):
+                dw.moe_layers[l].forward(xs[i, l], ys)
+                na = int(device_view(moe.moe_layer_debug_ptrs(dw.moe_layers[l].handle)["n_act"],
+                                     (2,), torch.int32)[0].item())
+                exact[l].forward(xs[i, l], ye)
+                a, b = ys.float(), ye.float()
+                errs.append(((a - b).abs().max() / b.pow(2).mean().sqrt()).item())
+                dropped.append(wl.k * T - na)
+    finally:
+        for m in exact:
+            m.close()
+    return {"dropped_routes_per_layer_step": round(sum(dropped) / len(dropped), 2),
+            "error_vs_exact": {"max_abs_over_rms_mean": round(sum(errs) / len(errs), 4),
+                               "max_abs_over_rms_max": round(max(errs), 4),
+                               "forwards": len(errs)}}
+
+
+def bench_multilayer(args, torch, moe, gen, gd, dev, name, link_gbs, spares=0, skip_tau=0.0):
     wl = gen.WORKLOADS[name]
     L = wl.layers if args.layers <= 0 else min(args.layers, wl.layers)
     T = wl.T
@@ -587,7 +623,7 @@ def bench_multilayer(args, torch, moe, gen, gd, dev, name, link_gbs, spares=0):
     # the bytes each miss moves over the link are the same)
     # spares > 0: the adaptive cache, its spare slots taken from the hot budget
     dw = gd.build(wl, layers=L, T_max=T, saliency_order=order, n_stage=n_stage,
-                  alias_host_records=True, spares=spares)
+                  alias_host_records=True, spares=spares, skip_tau=skip_tau)
     stream = torch.cuda.current_stream()
     sp = stream.cuda_stream
     steps = args.stack_steps
@@ -666,11 +702,16 @@ def bench_multilayer(args, torch, moe, gen, gd, dev, name, link_gbs, spares=0):
     for l in range(L):
         moe.moe_layer_set_timing(layers[l].handle, [])
         assert layers[l].read_status() == 0
+    skip_res = None
+    if skip_tau > 0:
+        skip_res = _skip_error(torch, dw, xs, g0, min(steps, 16), L, T)
     rb = gen.record_bytes(wl.H, wl.I)
     gather_gbs = miss * rb / (fill_ms * 1e-3) / 1e9 if fill_ms > 0 else 0.0
     res = {
         "workload": (f"{L} decode layers, {T} token(s) per step, "
                      + (("per-layer Zipf bias (alpha 1.556), 66 hot experts per layer in HBM"
+                         + (f", renorm-skip of misses with weight < {skip_tau} (approximate)"
+                            if skip_tau > 0 else "")
                          if spares == 0 else
                          f"per-layer Zipf bias (alpha 1.556), 66 slots per layer in HBM: the "
                          f"{66 - spares} hottest resident at start and {spares} spares, adaptive "
@@ -689,6 +730,8 @@ def bench_multilayer(args, torch, moe, gen, gd, dev, name, link_gbs, spares=0):
                      "peak_source": "measured pinned host->device cudaMemcpyAsync (1 GiB)"},
         "host_records": "one host copy per expert id, shared by the layers",
     }
+    if skip_res is not None:
+        res["renorm_skip"] = {"tau": skip_tau, **skip_res}
     if S > 0 and steps > 0:
         # the gather pass's own step time and its launch-step intervals, per
         # layer (us): router (+ permutation, + the adaptive cache's step for up
@@ -769,6 +812,10 @@ def run_ours(args, rank, world, local_rank):
     if args.only in ("stack", "flat"):
         link = link_h2d_gbs(torch, dev)
         return {args.only: bench_multilayer(args, torch, moe, gen, gd, dev, args.only, link)}
+    if args.only == "stack_skip":
+        link = link_h2d_gbs(torch, dev)
+        return {args.only: bench_multilayer(args, torch, moe, gen, gd, dev, "stack", link,
+                                            skip_tau=SKIP_TAU)}
     if args.only == "stack_adaptive":
         link = link_h2d_gbs(torch, dev)
         return {args.only: bench_multilayer(args, torch, moe, gen, gd, dev, "stack", link,
@@ -799,11 +846,12 @@ def run_ours(args, rank, world, local_rank):
         try:
             link = link_h2d_gbs(torch, dev)
             also["link_h2d_gbs"] = round(link, 1)
-            for name, wname, sp in (("stack", "stack", 0), ("flat", "flat", 0),
-                                    ("stack_adaptive", "stack", ADAPTIVE_SPARES)):
+            for name, wname, sp, tau in (("stack", "stack", 0, 0.0), ("flat", "flat", 0, 0.0),
+                                         ("stack_adaptive", "stack", ADAPTIVE_SPARES, 0.0),
+                                         ("stack_skip", "stack", 0, SKIP_TAU)):
                 try:
                     also[name] = bench_multilayer(args, torch, moe, gen, gd, dev, wname, link,
-                                                  spares=sp)
+                                                  spares=sp, skip_tau=tau)
                 except Exception as exc:
                     also[name] = {"error": repr(exc)}
                 torch.cuda.empty_cache()
@@ -846,7 +894,8 @@ def main():
     ap.add_argument("--small", action="store_true",
                     help="16 distinct expert records (profiler captures only)")
     ap.add_argument("--only", default="",
-                    choices=["", "prefill", "route", "stack", "flat", "stack_adaptive"],
+                    choices=["", "prefill", "route", "stack", "flat", "stack_adaptive",
+                             "stack_skip"],
                     help="run one secondary workload alone (profiler captures)")
     ap.add_argument("--prefill-experts", type=int, default=0,
                     help="prefill with fewer experts, same tokens per expert (profiling)")
