@@ -645,7 +645,7 @@ def bench_multilayer(args, torch, moe, gen, gd, dev, name, link_gbs, spares=0, s
         for l in range(L):
             layers[l].forward(xs[i, l], y[l])
 
-    if spares > 0:
+    if n_warm > args.warmup:
         for i in range(n_warm):
             fwd(i)
         torch.cuda.synchronize()

@@ -45,8 +45,10 @@ __global__ void __launch_bounds__(kGatherThreads) k_gather(
     uint8_t* __restrict__ arena, int32_t* __restrict__ table_row, int E, uint64_t rec_bytes,
     int n_cache, int n_stage, const int32_t* __restrict__ ids, const int32_t* __restrict__ d_n,
     int first, const int32_t* __restrict__ dst_slots, int slot_lo, int slot_hi, int32_t* status) {
+  // The next kernel (the FFN, which waits for this one anyway) is let launch
+  // only when a CTA has done its copying: launched early, its CTAs would sit
+  // on the SMs that this grid's later CTAs need to keep the link busy.
   pdl_wait();
-  pdl_launch_dependents();
   const int i = first + blockIdx.y;
   if (i >= *d_n) return;
   const int e = ids[i];
@@ -87,6 +89,7 @@ __global__ void __launch_bounds__(kGatherThreads) k_gather(
   for (; w < n16; w += stride) d4[w] = ldg_stream(s4 + w);
   if (dst_slots && table_row && slot < n_cache && blockIdx.x == 0 && threadIdx.x == 0)
     table_row[e] = slot;
+  pdl_launch_dependents();
 }
 
 __global__ void k_set_table(int32_t* table_entry, int slot) { *table_entry = slot; }
