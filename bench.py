@@ -659,7 +659,11 @@ def bench_multilayer(args, torch, moe, gen, gd, dev, name, link_gbs, spares=0, s
         fwd(n_warm + j)
         ev[j][1].record(stream)
     torch.cuda.synchronize()
-    ms = sum(a.elapsed_time(b) for a, b in ev) / steps
+    # median over the steps (and p10 / p90 beside it): a few steps of a fresh
+    # stream can take several times the rest
+    step_ms = sorted(a.elapsed_time(b) for a, b in ev)
+    ms = statistics.median(step_ms)
+    p10, p90 = step_ms[int(0.1 * (steps - 1))], step_ms[int(0.9 * (steps - 1))]
     for l in range(L):
         assert layers[l].read_status() == 0
     # gather pass: the same forwards, with the layer timing hook's events at
@@ -721,6 +725,7 @@ def bench_multilayer(args, torch, moe, gen, gd, dev, name, link_gbs, spares=0, s
                      + ", misses gathered from pinned host memory"),
         "value": round(T / (ms * 1e-3), 2), "unit": UNIT + " (whole stack)",
         "ms_per_step": round(ms, 4),
+        "ms_per_step_p10_p90": [round(p10, 4), round(p90, 4)],
         "per_layer_tokens_s": round(T * L / (ms * 1e-3), 1),
         "hit_rate": round(1 - miss / max(act, 1), 4),
         "misses_per_layer_step": round(miss / (steps * L), 2),
