@@ -658,6 +658,8 @@ def bench_multilayer(args, torch, moe, gen, gd, dev, name, link_gbs, spares=0, s
         ev[j][0].record(stream)
         fwd(n_warm + j)
         ev[j][1].record(stream)
+        # a decode step ends on the host (the next token depends on this one)
+        ev[j][1].synchronize()
     torch.cuda.synchronize()
     # median over the steps (and p10 / p90 beside it): a few steps of a fresh
     # stream can take several times the rest
