@@ -97,13 +97,15 @@ def test_policy_step_matches_oracle(K):
         cache.close()
 
 
-def test_layer_forward_with_adaptive_cache():
+@pytest.mark.parametrize("T", [4, 12])
+def test_layer_forward_with_adaptive_cache(T):
     """Two tiny layers with 3 residents + 2 spares each; every forward's
     outputs match the oracle and the slot table follows the oracle's policy
-    fed the oracle's routing."""
+    fed the oracle's routing.  4 tokens: the step runs in the router kernel;
+    12: as a kernel of its own after the permutation."""
     import gen.device as gd
     wl = gen.WORKLOADS["tiny"]
-    L, T, K = 2, 4, 2
+    L, K = 2, 2
     resident = [[0, 5, 9], [1, 2, 3]]
     dw = gd.build(wl, layers=L, T_max=T, resident=resident, spares=K)
     try:
