@@ -53,12 +53,11 @@ ADAPTIVE_WARM_TOKENS = 256
 # renorm-skip threshold of the stack_skip pass (an approximation of the layer)
 SKIP_TAU = 0.05  # about one halving period of its counts on the 16-layer stack
 FP4_OVER_BF16 = 6.0  # nominal dense FP4 / dense bf16 tensor throughput (13.5 / 2.25)
-# DRAM bytes (read + write) of one k_decode_gu launch on the full decode layer, from
-# one ncu capture of the current kernel (profiles/k_decode_gu_decode-layer.md); set to
-# None whenever the kernel changes until it is captured again
-GU_TRAFFIC = 138_484_480 + 3_983_488
-GU_TRAFFIC_SOURCE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum, full decode layer, "
-                     "profiles/k_decode_gu_decode-layer.md")
+# DRAM bytes (read + write) of one launch of the roofline kernel on the full decode
+# layer, from one ncu capture of the current kernel; None whenever the kernel has
+# changed since it was captured
+GU_TRAFFIC = None
+GU_TRAFFIC_SOURCE = "ncu dram__bytes_read.sum + dram__bytes_write.sum, one launch, full decode layer"
 
 
 def _peaks():

@@ -53,13 +53,13 @@ def _lib_host():
         L.gen_router_f32.argtypes = [u64, i32, i32, i32, vp]
         L.gen_shared_bf16.argtypes = [u64, i32, i32, i32, vp, vp, vp]
         L.gen_global_scales.argtypes = [u64, i32, i32, vp]
-        L.gen_expert_record.argtypes = [u64, i32, i32, i32, i32, vp]
-        L.gen_expert_records_mt.argtypes = [u64, i32, vp, i32, i32, i32, vp, i32]
+        L.gen_expert_record.argtypes = [u64, i32, i32, i32, i32, i32, vp]
+        L.gen_expert_records_mt.argtypes = [u64, i32, vp, i32, i32, i32, i32, vp, i32]
         L.gen_zipf_bias.argtypes = [u64, i32, i32, ctypes.c_double, vp, vp]
         L.gen_expert_prequant_row.argtypes = [u64, i32, i32, i32, i32, i32, i32, vp]
         L.gen_mix64_export.argtypes = [u64]
         L.gen_mix64_export.restype = u64
-        L.gen_record_size.argtypes = [i32, i32]
+        L.gen_record_size.argtypes = [i32, i32, i32]
         L.gen_record_size.restype = u64
         _host = L
     return _host
@@ -72,7 +72,7 @@ def _lib_cuda():
             raise RuntimeError("device generator not built (gen.build(cuda=True))")
         L = ctypes.CDLL(_CUDA_SO)
         u64, i32, i64, vp = ctypes.c_uint64, ctypes.c_int, ctypes.c_int64, ctypes.c_void_p
-        L.gen_dev_expert_record.argtypes = [u64, i32, i32, i32, i32, vp, vp]
+        L.gen_dev_expert_record.argtypes = [u64, i32, i32, i32, i32, i32, vp, vp]
         L.gen_dev_x_bf16.argtypes = [u64, i32, i64, i32, i32, vp, vp]
         L.gen_dev_router_f32.argtypes = [u64, i32, i32, i32, vp, vp]
         L.gen_dev_shared_bf16.argtypes = [u64, i32, i32, i32, vp, vp, vp, vp]
@@ -90,8 +90,12 @@ def _p(a: np.ndarray) -> int:
 
 # ------------------------------------------------------------------ host side
 
-def record_bytes(H: int, I: int) -> int:
-    return 3 * I * H // 2 + 3 * I * H // 16
+# record formats: 0 = NVFP4 (E4M3 scale per 16 values), 1 = MXFP4 (E8M0 per 32)
+NVFP4, MXFP4 = 0, 1
+
+
+def record_bytes(H: int, I: int, fmt: int = NVFP4) -> int:
+    return 3 * I * H // 2 + 3 * I * H // (32 if fmt == MXFP4 else 16)
 
 
 def x_bf16(seed: int, layer: int, draw0: int, T: int, H: int) -> np.ndarray:
@@ -120,17 +124,18 @@ def global_scales(seed: int, layer: int, E: int) -> np.ndarray:
     return out
 
 
-def expert_records(seed: int, layer: int, experts, H: int, I: int, nthreads: int = 0) -> np.ndarray:
+def expert_records(seed: int, layer: int, experts, H: int, I: int, nthreads: int = 0,
+                   fmt: int = NVFP4) -> np.ndarray:
     """Records of the listed experts, [n, record_bytes] uint8 (threaded)."""
     experts = np.ascontiguousarray(np.asarray(experts, np.int32))
     n = len(experts)
-    rb = record_bytes(H, I)
+    rb = record_bytes(H, I, fmt)
     out = np.empty((n, rb), np.uint8)
     if n == 0:
         return out
     ptrs = (ctypes.c_void_p * n)(*[out.ctypes.data + i * rb for i in range(n)])
     nt = nthreads or min(os.cpu_count() or 1, 64)
-    _lib_host().gen_expert_records_mt(seed, layer, _p(experts), n, H, I, ptrs, nt)
+    _lib_host().gen_expert_records_mt(seed, layer, _p(experts), n, H, I, fmt, ptrs, nt)
     return out
 
 
@@ -156,8 +161,9 @@ def zipf_bias(seed: int, layer: int, E: int, alpha: float):
 
 # ---------------------------------------------------------------- device side
 
-def dev_expert_record(seed, layer, expert, H, I, dst_ptr: int, stream: int = 0) -> None:
-    if _lib_cuda().gen_dev_expert_record(seed, layer, expert, H, I, dst_ptr, stream):
+def dev_expert_record(seed, layer, expert, H, I, dst_ptr: int, stream: int = 0,
+                      fmt: int = NVFP4) -> None:
+    if _lib_cuda().gen_dev_expert_record(seed, layer, expert, H, I, fmt, dst_ptr, stream):
         raise RuntimeError("gen_dev_expert_record failed")
 
 
@@ -195,6 +201,7 @@ class Workload:
     hot_rule: str = "all"     # "all" | "zipf" (smallest ranks) | "saliency"
     prefill: bool = False
     group: int = 64           # prefill: experts per staging group
+    fmt: int = NVFP4          # routed expert record format
     extra: dict = field(default_factory=dict)
 
 

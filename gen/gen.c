@@ -63,35 +63,36 @@ GEN_API void gen_global_scales(uint64_t seed, int layer, int E, float* g /* [E][
     }
 }
 
-/* one matrix (rows [r0, r1)) of one expert record */
+/* one matrix (rows [r0, r1)) of one expert record in format fmt */
 static void gen_matrix_rows(uint64_t seed, int layer, int expert, int H, int I, int m, int r0,
-                            int r1, uint8_t* rec) {
+                            int r1, int fmt, uint8_t* rec) {
   int K = (m == 2) ? I : H;
-  int KB = K / 16;
+  int bl = gen_block_len(fmt), KB = K / bl;
   uint64_t key = gen_key(seed, GEN_KIND_EXPERT, (uint64_t)layer, (uint64_t)(expert * 4 + m));
   uint8_t* codes = rec + gen_codes_off(H, I, m);
-  uint8_t* scales = rec + gen_scales_off(H, I, m);
+  uint8_t* scales = rec + gen_scales_off(H, I, m, fmt);
   for (int r = r0; r < r1; ++r)
     for (int kb = 0; kb < KB; ++kb) {
-      uint8_t c8[8];
-      int sb = gen_expert_block(key, r, kb, K, c8);
-      memcpy(codes + (size_t)r * (K / 2) + (size_t)kb * 8, c8, 8);
+      uint8_t c[16];
+      int sb = fmt ? gen_expert_block_mx(key, r, kb, K, c) : gen_expert_block(key, r, kb, K, c);
+      memcpy(codes + (size_t)r * (K / 2) + (size_t)kb * (bl / 2), c, (size_t)bl / 2);
       scales[gen_scale_index(r, kb, KB)] = (uint8_t)sb;
     }
 }
 
-GEN_API uint64_t gen_record_size(int H, int I) { return gen_record_bytes(H, I); }
+GEN_API uint64_t gen_record_size(int H, int I, int fmt) { return gen_record_bytes(H, I, fmt); }
 
-GEN_API void gen_expert_record(uint64_t seed, int layer, int expert, int H, int I, uint8_t* rec) {
-  gen_matrix_rows(seed, layer, expert, H, I, 0, 0, I, rec);
-  gen_matrix_rows(seed, layer, expert, H, I, 1, 0, I, rec);
-  gen_matrix_rows(seed, layer, expert, H, I, 2, 0, H, rec);
+GEN_API void gen_expert_record(uint64_t seed, int layer, int expert, int H, int I, int fmt,
+                               uint8_t* rec) {
+  gen_matrix_rows(seed, layer, expert, H, I, 0, 0, I, fmt, rec);
+  gen_matrix_rows(seed, layer, expert, H, I, 1, 0, I, fmt, rec);
+  gen_matrix_rows(seed, layer, expert, H, I, 2, 0, H, fmt, rec);
 }
 
 /* ---- threaded fill of several records ---- */
 typedef struct {
   uint64_t seed;
-  int layer, H, I, n;
+  int layer, H, I, n, fmt;
   const int32_t* experts;
   uint8_t* const* dst;
   int64_t n_units; /* units = (record, matrix, 64-row chunk) */
@@ -127,16 +128,17 @@ static void* gen_worker(void* arg) {
     for (; u < ue; ++u) {
       int rec, m, r0, r1;
       unit_decode(j, u, &rec, &m, &r0, &r1);
-      gen_matrix_rows(j->seed, j->layer, j->experts[rec], j->H, j->I, m, r0, r1, j->dst[rec]);
+      gen_matrix_rows(j->seed, j->layer, j->experts[rec], j->H, j->I, m, r0, r1, j->fmt,
+                      j->dst[rec]);
     }
   }
   return NULL;
 }
 
 GEN_API void gen_expert_records_mt(uint64_t seed, int layer, const int32_t* experts, int n, int H,
-                                   int I, uint8_t* const* dst, int nthreads) {
+                                   int I, int fmt, uint8_t* const* dst, int nthreads) {
   gen_job j;
-  j.seed = seed; j.layer = layer; j.H = H; j.I = I; j.n = n;
+  j.seed = seed; j.layer = layer; j.H = H; j.I = I; j.n = n; j.fmt = fmt;
   j.experts = experts; j.dst = dst; j.next = 0;
   j.n_units = (int64_t)n * (2 * ((I + 63) / 64) + (H + 63) / 64);
   pthread_mutex_init(&j.mu, NULL);

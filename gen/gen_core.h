@@ -27,6 +27,11 @@
  *   With the per-matrix global scale g, the represented weight is
  *   e2m1(code) * e4m3(s) * g and the weight "before quantisation" was
  *   d * g / 64.  Everything here is integer arithmetic.
+ *   MXFP4 records (OCP Microscaling Formats v1.0, element E2M1, block 32,
+ *   scale E8M0): a block of 32 weights w = d/64 shares the scale X =
+ *   2^(floor(log2 max|w|) - 2) (byte 127 + floor(log2 max|d|) - 8; byte 0
+ *   and codes 0 for an all-zero block) and each code is the nearest E2M1
+ *   magnitude of |w| / X, ties to the even code, saturating at 6.
  */
 #ifndef GEN_CORE_H
 #define GEN_CORE_H
@@ -123,6 +128,23 @@ GEN_HD uint32_t gen_e2m1_code(int32_t d, int sb) {
   return c;
 }
 
+/* MXFP4 code of d in a block whose largest |d| has floor(log2) = E:
+ * nearest E2M1 magnitude of q = |d| / 2^(E - 2), i.e. compare 16 |d| with
+ * (4 x midpoint) x 2^E; ties to the even code; saturating at 6. */
+GEN_HD uint32_t gen_e2m1_code_mx(int32_t d, int E) {
+  int64_t n = (int64_t)(d < 0 ? -d : d) * 16;
+  const int mid4[7] = {1, 3, 5, 7, 10, 14, 20};
+  uint32_t c = 0;
+  for (int j = 0; j < 7; ++j) {
+    int64_t t = (int64_t)mid4[j] << E;
+    if (n > t) c = (uint32_t)(j + 1);
+    else if (n == t) { c = (uint32_t)(((j & 1) == 0) ? j : j + 1); break; }
+    else break;
+  }
+  if (c != 0 && d < 0) c |= 8u;
+  return c;
+}
+
 /* ---- expert record layout (the storage format) ----
  * Matrices: 0 = gate [I x H], 1 = up [I x H], 2 = down [H x I].
  * Codes: row-major, two E2M1 codes per byte, element 2j in the low nibble.
@@ -130,17 +152,21 @@ GEN_HD uint32_t gen_e2m1_code(int32_t d, int sb) {
  *   atom (row_tile = r / 128, k_group = kb / 4) at ((row_tile * KB/4) + k_group) * 512,
  *   byte (r % 32) * 16 + ((r % 128) / 32) * 4 + (kb % 4) inside the atom.
  */
+/* fmt 0 = NVFP4 (E4M3 scale per 16 values), 1 = MXFP4 (E8M0 scale per 32,
+ * in the same 512-byte atoms with kb counting blocks of 32) */
+GEN_HD int gen_block_len(int fmt) { return fmt ? 32 : 16; }
 GEN_HD uint64_t gen_codes_off(int H, int I, int m) {
   uint64_t gu = (uint64_t)I * (uint64_t)H / 2;
   return m == 0 ? 0 : (m == 1 ? gu : 2 * gu);
 }
-GEN_HD uint64_t gen_scales_off(int H, int I, int m) {
+GEN_HD uint64_t gen_scales_off(int H, int I, int m, int fmt) {
   uint64_t codes = 3ull * (uint64_t)I * (uint64_t)H / 2;
-  uint64_t gu = (uint64_t)I * (uint64_t)H / 16;
+  uint64_t gu = (uint64_t)I * (uint64_t)H / (uint64_t)gen_block_len(fmt);
   return codes + (m == 0 ? 0 : (m == 1 ? gu : 2 * gu));
 }
-GEN_HD uint64_t gen_record_bytes(int H, int I) {
-  return 3ull * (uint64_t)I * (uint64_t)H / 2 + 3ull * (uint64_t)I * (uint64_t)H / 16;
+GEN_HD uint64_t gen_record_bytes(int H, int I, int fmt) {
+  return 3ull * (uint64_t)I * (uint64_t)H / 2 +
+         3ull * (uint64_t)I * (uint64_t)H / (uint64_t)gen_block_len(fmt);
 }
 GEN_HD uint64_t gen_scale_index(int r, int kb, int KB) {
   return ((uint64_t)(r / 128) * (uint64_t)(KB / 4) + (uint64_t)(kb / 4)) * 512u +
@@ -165,6 +191,31 @@ GEN_HD int gen_expert_block(uint64_t key, int r, int kb, int K, uint8_t codes[8]
     codes[j] = (uint8_t)(lo | (hi << 4));
   }
   return sb;
+}
+
+/* One 32-element MXFP4 block (row r, block kb of 32) of matrix m: writes 16
+ * code bytes and returns the E8M0 scale byte. */
+GEN_HD int gen_expert_block_mx(uint64_t key, int r, int kb, int K, uint8_t codes[16]) {
+  int32_t d[32];
+  int64_t amax = 0;
+  uint64_t base = (uint64_t)r * (uint64_t)K + (uint64_t)kb * 32u;
+  for (int j = 0; j < 32; ++j) {
+    d[j] = gen_ih(gen_draw(key, base + (uint64_t)j));
+    int64_t a = d[j] < 0 ? -(int64_t)d[j] : (int64_t)d[j];
+    if (a > amax) amax = a;
+  }
+  if (amax == 0) {
+    for (int j = 0; j < 16; ++j) codes[j] = 0;
+    return 0;
+  }
+  int E = 0;
+  while ((amax >> (E + 1)) != 0) ++E; /* floor(log2 amax) */
+  for (int j = 0; j < 16; ++j) {
+    uint32_t lo = gen_e2m1_code_mx(d[2 * j], E);
+    uint32_t hi = gen_e2m1_code_mx(d[2 * j + 1], E);
+    codes[j] = (uint8_t)(lo | (hi << 4));
+  }
+  return 127 + E - 8;
 }
 
 #endif

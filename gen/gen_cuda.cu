@@ -12,8 +12,10 @@
 
 static const double kSd = GEN_IH_SD;
 
-__global__ void k_gen_expert(uint64_t seed, int layer, int expert, int H, int I, uint8_t* rec) {
-  const uint64_t nb_gu = (uint64_t)I * (uint64_t)(H / 16);
+__global__ void k_gen_expert(uint64_t seed, int layer, int expert, int H, int I, int fmt,
+                             uint8_t* rec) {
+  const int bl = gen_block_len(fmt);
+  const uint64_t nb_gu = (uint64_t)I * (uint64_t)(H / bl);
   const uint64_t nb_total = 3 * nb_gu;
   for (uint64_t b = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; b < nb_total;
        b += (uint64_t)gridDim.x * blockDim.x) {
@@ -22,23 +24,25 @@ __global__ void k_gen_expert(uint64_t seed, int layer, int expert, int H, int I,
       m = (int)(b / nb_gu);
       uint64_t w = b % nb_gu;
       K = H;
-      r = (int)(w / (H / 16));
-      kb = (int)(w % (H / 16));
+      r = (int)(w / (H / bl));
+      kb = (int)(w % (H / bl));
     } else {
       m = 2;
       uint64_t w = b - 2 * nb_gu;
       K = I;
-      r = (int)(w / (I / 16));
-      kb = (int)(w % (I / 16));
+      r = (int)(w / (I / bl));
+      kb = (int)(w % (I / bl));
     }
     uint64_t key = gen_key(seed, GEN_KIND_EXPERT, (uint64_t)layer, (uint64_t)(expert * 4 + m));
-    uint8_t c8[8];
-    int sb = gen_expert_block(key, r, kb, K, c8);
-    uint64_t packed = 0;
-    for (int j = 0; j < 8; ++j) packed |= (uint64_t)c8[j] << (8 * j);
-    *reinterpret_cast<uint64_t*>(rec + gen_codes_off(H, I, m) + (uint64_t)r * (K / 2) +
-                                 (uint64_t)kb * 8) = packed;
-    rec[gen_scales_off(H, I, m) + gen_scale_index(r, kb, K / 16)] = (uint8_t)sb;
+    uint8_t c[16];
+    int sb = fmt ? gen_expert_block_mx(key, r, kb, K, c) : gen_expert_block(key, r, kb, K, c);
+    uint8_t* dst = rec + gen_codes_off(H, I, m) + (uint64_t)r * (K / 2) + (uint64_t)kb * (bl / 2);
+    for (int h = 0; h < bl / 16; ++h) {
+      uint64_t packed = 0;
+      for (int j = 0; j < 8; ++j) packed |= (uint64_t)c[8 * h + j] << (8 * j);
+      *reinterpret_cast<uint64_t*>(dst + 8 * h) = packed;
+    }
+    rec[gen_scales_off(H, I, m, fmt) + gen_scale_index(r, kb, K / bl)] = (uint8_t)sb;
   }
 }
 
@@ -78,11 +82,12 @@ static int grid_for(uint64_t n) {
   return (int)g;
 }
 
-GEN_API int gen_dev_expert_record(uint64_t seed, int layer, int expert, int H, int I, uint8_t* dst,
-                                  void* stream) {
-  if (H % 128 || I % 128 || !dst) return 1;
-  uint64_t nb = 3ull * I * (H / 16);
-  k_gen_expert<<<grid_for(nb), 256, 0, (cudaStream_t)stream>>>(seed, layer, expert, H, I, dst);
+GEN_API int gen_dev_expert_record(uint64_t seed, int layer, int expert, int H, int I, int fmt,
+                                  uint8_t* dst, void* stream) {
+  if (H % 128 || I % 128 || !dst || fmt < 0 || fmt > 1) return 1;
+  uint64_t nb = 3ull * I * (H / gen_block_len(fmt));
+  k_gen_expert<<<grid_for(nb), 256, 0, (cudaStream_t)stream>>>(seed, layer, expert, H, I, fmt,
+                                                                dst);
   return cudaGetLastError() == cudaSuccess ? 0 : 2;
 }
 

@@ -243,14 +243,39 @@ moe_status expcache_policy_state(const expcache* c, int* spares, const uint32_t*
                                  const uint32_t** last, const uint32_t** stamp,
                                  const int32_t** freeslot);
 
+/* Per-layer slot budgets ("Project Maya" page, section "VRAM: one partition
+ * per layer, sized by what the layer routes"): splits total_slots cache slots
+ * over L layers from route counts per (layer, expert) - for instance the
+ * moe_permute counts of a calibration batch summed per layer, or the
+ * adaptive policy's decayed counts.  Each layer's experts are ordered by
+ * count, descending, ties to the lower id (d_order [L][E]); every layer gets
+ * `floor` slots; each further slot goes to the layer whose next expert in
+ * that order serves the largest share of that layer's lookups (count / the
+ * layer's total; 0 for a layer without routes), ties to the lower layer; a
+ * full layer (E slots) takes no more, and slots beyond L*E stay unassigned.
+ * d_layer_slots [L+1] receives the partition's prefix sums, ready for
+ * expcache_desc.layer_slots (copied to the host); layer l's residents are
+ * d_order[l][0 .. layer_slots[l+1] - layer_slots[l]).
+ *   d_counts device [L][E] uint32; outputs device.  floor > E or total_slots <
+ *   L*floor: MOE_ERR_INVALID_ARG; L > 4096 or E > 1024: MOE_ERR_UNSUPPORTED.
+ *   One thread block; stream-ordered. */
+moe_status expcache_plan_slots(const uint32_t* d_counts, int L, int E, int total_slots, int floor,
+                               int32_t* d_layer_slots, int32_t* d_order, void* stream);
+
 /* ------------------------------------------------------------- expert FFN
  * For each route p (p-th route of the expert-sorted order) of the active
  * experts of group `group` (group 0 = all hits and misses [0, n_stage);
  * group g > 0 = misses [g*n_stage, (g+1)*n_stage)), with e its expert and t
  * its token: g = Wg x_t, u = Wu x_t, h = silu(g) * u, o = Wd h, all weights
  * read from the record in slot src_slot[e] (SiLU-gated FFN without biases).
- * DECODE mode: weights dequantised in registers, fp32 FMA on the bf16
- *   activations; writes o_route[p] = w[t][j] * o (fp32).  For routes whose
+ * DECODE mode: weights dequantised in registers; the activations (x, then h)
+ *   are held in f16 and every product is an exact f16 x f16 product summed
+ *   in fp32 (x is bf16: exact in f16 for magnitudes in [2^-14, 65504];
+ *   smaller ones are rounded to f16's subnormal grid, an absolute error of at
+ *   most 2^-25; h is fp32 rounded to f16, relative error 2^-11).  A value
+ *   of x or h beyond 65504 (or inf or NaN) is outside the decode path: the
+ *   kernel sets MOE_ERR_UNSUPPORTED in *status (its outputs are then not
+ *   defined).  Writes o_route[p] = w[t][j] * o (fp32).  For routes whose
  *   expert is not in the group nothing is written.
  * PREFILL mode: activations quantised to NVFP4 (per token, and h per route:
  *   G = amax/(6*448), block scale e4m3_rne(amax_b/(6 G)), codes
@@ -316,9 +341,14 @@ moe_status moe_expert_ffn(const moe_ffn_args* a, void* stream);
  *   - Returns MOE_ERR_UNSUPPORTED when mode is not MOE_MODE_DECODE or when
  *     moe_ffn_workspace_bytes(MOE_MODE_DECODE, T, H, I, E, k, Is) exceeds
  *     MOE_NOALLOC_SCRATCH_BYTES (use moe_expert_ffn for such sizes).
- *   - The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress, with that device current); make that first call
- *     before any stream capture.
+ *   - Every call looks up the array's device address on the current device
+ *     (cudaGetSymbolAddress).  CUDA loads the library's array lazily, and
+ *     loading it reserves its MOE_NOALLOC_SCRATCH_BYTES of device memory:
+ *     the library's first expcache_create, moe_layer_create or FFN call in
+ *     the process does that on its current device.  On any other device the
+ *     first moe_expert_ffn_noalloc loads it, so a caller that reserves all
+ *     device memory up front makes one call on each device first, before
+ *     any stream capture.
  *   - All calls share the one array and it keeps the last call's contents;
  *     no part of it needs to start at zero.  Calls that overlap on the GPU
  *     (different streams, no ordering between them) race on it and give
@@ -408,6 +438,15 @@ moe_status moe_layer_forward(moe_layer* l, const void* x, int T, void* y, void* 
 moe_status moe_layer_debug_ptrs(const moe_layer* l, const int32_t** ids, const float** w,
                                 const float** p_sel, const int32_t** perm,
                                 const int32_t** src_slot, const int32_t** n_act);
+/* After a forward that took the PREFILL path: device pointers to its fp32
+ * h = silu(g) * u rows before their NVFP4 quantisation (I values per padded
+ * route row: the route at expert-sorted position p of expert e is row
+ * pad_offsets[e] + p - offsets[e]), and to offsets [E+1] and pad_offsets
+ * [E+1].  Valid until the next forward.  MOE_ERR_INVALID_ARG when the last
+ * forward took the DECODE path.  (For tests; the pages have no
+ * counterpart.) */
+moe_status moe_layer_debug_prefill(const moe_layer* l, const float** h_rows,
+                                   const int32_t** offsets, const int32_t** pad_offsets);
 /* Timing hook (the pages have no counterpart; it serves measurement):
  * events[0..n) are cudaEvent_t handles owned by the caller.  While set, every
  * moe_layer_forward records events[0] before its first kernel and events[i]

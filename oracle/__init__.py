@@ -49,9 +49,12 @@ def lib():
         L.oracle_e4m3.restype = d
         L.oracle_bf16.argtypes = [ctypes.c_uint16]
         L.oracle_bf16.restype = d
-        L.oracle_weight.argtypes = [vp, i32, i32, i32, i32, i32, vp]
+        L.oracle_weight.argtypes = [vp, i32, i32, i32, i32, i32, i32, vp]
         L.oracle_weight.restype = d
-        L.oracle_dequant_matrix.argtypes = [vp, i32, i32, i32, vp, vp]
+        L.oracle_dequant_matrix.argtypes = [vp, i32, i32, i32, i32, vp, vp]
+        L.oracle_e8m0.argtypes = [ctypes.c_uint]
+        L.oracle_e8m0.restype = d
+        L.oracle_mxfp4_quant.argtypes = [vp, i32, vp, vp]
         L.oracle_route.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp]
         L.oracle_permute.argtypes = [vp, i32, i32, i32, vp, vp, vp, vp]
         L.oracle_permute.restype = i32
@@ -60,14 +63,20 @@ def lib():
         L.oracle_e2m1_rne_sat.argtypes = [ctypes.c_float]
         L.oracle_e2m1_rne_sat.restype = ctypes.c_uint
         L.oracle_nvfp4_quant.argtypes = [vp, i32, vp, vp, vp]
-        L.oracle_expert.argtypes = [vp, i32, i32, vp, vp, i32, vp]
+        L.oracle_expert.argtypes = [vp, i32, i32, i32, vp, vp, i32, vp]
         L.oracle_shared.argtypes = [vp, vp, vp, i32, i32, vp, i32, vp]
         L.oracle_renorm_skip.argtypes = [vp, vp, i32, i32, vp, d, vp, vp]
-        L.oracle_layer_forward.argtypes = [vp, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp,
+        L.oracle_layer_forward.argtypes = [vp, i32, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp,
                                            vp, vp, vp, i32, vp, d, vp, vp, vp, vp, vp]
         L.oracle_layer_forward.restype = i32
         L.oracle_set_defect.argtypes = [i32]
-        L.oracle_quant_flip_delta.argtypes = [vp, i32, vp]
+        L.oracle_quant_flip_delta.argtypes = [vp, i32, i32, vp]
+        L.oracle_bf16_flip_delta.argtypes = [vp, i32, vp]
+        L.oracle_set_flip_margins.argtypes = [d, d, d]
+        L.oracle_slot_budget.argtypes = [i32, i32, vp, i32, i32, vp, vp]
+        L.oracle_slot_budget.restype = i32
+        L.oracle_expert_h.argtypes = [vp, i32, i32, i32, vp, vp, vp]
+        L.oracle_prefill_near_boundary.argtypes = [vp, i32, i32, i32, i32, i32, vp, vp, vp, vp]
         L.oracle_cache_policy_step.argtypes = [i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp,
                                                vp, vp, vp]
         L.oracle_cache_policy_step.restype = i32
@@ -117,14 +126,20 @@ def bf16(h: int) -> float:
     return lib().oracle_bf16(h)
 
 
-def weight(rec, H, I, m, r, c, g3) -> float:
-    return lib().oracle_weight(_p(rec), H, I, m, r, c, _p(np.ascontiguousarray(g3, np.float32)))
+# record formats (gen.NVFP4, gen.MXFP4)
+NVFP4, MXFP4 = 0, 1
 
 
-def dequant_matrix(rec, H, I, m, g3) -> np.ndarray:
+def weight(rec, H, I, m, r, c, g3, fmt=NVFP4) -> float:
+    return lib().oracle_weight(_p(rec), H, I, fmt, m, r, c,
+                               _p(np.ascontiguousarray(g3, np.float32)))
+
+
+def dequant_matrix(rec, H, I, m, g3, fmt=NVFP4) -> np.ndarray:
     R, K = (H, I) if m == 2 else (I, H)
     out = np.empty((R, K), np.float64)
-    lib().oracle_dequant_matrix(_p(rec), H, I, m, _p(np.ascontiguousarray(g3, np.float32)), _p(out))
+    lib().oracle_dequant_matrix(_p(rec), H, I, fmt, m, _p(np.ascontiguousarray(g3, np.float32)),
+                                _p(out))
     return out
 
 
@@ -174,18 +189,81 @@ def nvfp4_quant(v):
     return codes, scales, float(G[0])
 
 
-def quant_flip_delta(v):
-    """Per-element rounding-boundary slack of the NVFP4 quantisation of v."""
+def e8m0(b: int) -> float:
+    return lib().oracle_e8m0(b)
+
+
+def mxfp4_quant(v):
+    """MXFP4 codes [n/2] and E8M0 scales [n/32] of an fp32 row (OCP MX rule)."""
+    v = np.ascontiguousarray(v, np.float32)
+    n = v.shape[0]
+    codes = np.empty(n // 2, np.uint8)
+    scales = np.empty(n // 32, np.uint8)
+    lib().oracle_mxfp4_quant(_p(v), n, _p(codes), _p(scales))
+    return codes, scales
+
+
+def quant_flip_delta(v, fmt=NVFP4):
+    """Per-element rounding-boundary slack of the NVFP4 (or MXFP4)
+    quantisation of v."""
     v = np.ascontiguousarray(v, np.float32)
     out = np.empty(v.shape[0], np.float64)
-    lib().oracle_quant_flip_delta(_p(v), v.shape[0], _p(out))
+    lib().oracle_quant_flip_delta(_p(v), v.shape[0], fmt, _p(out))
     return out
 
 
-def expert(rec, H, I, g3, x, act_quant=False):
+# margins of the rounding-boundary slack (oracle.c, orc_quant_flip_delta):
+# E2M1 code units, relative E4M3 scale argument, relative bf16 value
+FLIP_Q, FLIP_T, FLIP_BF16 = 2e-5, 1e-5, 2e-6
+
+
+def set_flip_margins(q=FLIP_Q, t=FLIP_T, bf16=FLIP_BF16):
+    lib().oracle_set_flip_margins(float(q), float(t), float(bf16))
+
+
+def expert_h(rec, H, I, g3, x, fmt=NVFP4):
+    """h = silu(Wg x) * (Wu x) [I] in fp64 for one routed expert (x fp64 [H])."""
+    x = np.ascontiguousarray(x, np.float64)
+    h = np.empty(I, np.float64)
+    lib().oracle_expert_h(_p(rec), H, I, fmt, _p(np.ascontiguousarray(g3, np.float32)), _p(x),
+                          _p(h))
+    return h
+
+
+def prefill_near_boundary(x, H, I, k, ids, records, g, fmt=NVFP4):
+    """Per token of x [T,H] (bf16) with routes ids [T,k]: the number of
+    elements of its routes' h that lie within the margins of an NVFP4
+    rounding boundary (where another implementation may take the
+    neighbouring code).  records: expert id -> record (dict or sequence)."""
+    x = np.ascontiguousarray(x, np.uint16)
+    ids = np.ascontiguousarray(ids, np.int32)
+    T = x.shape[0]
+    E = int(ids.max()) + 1 if ids.size else 1
+    keep = []
+    ptrs = (ctypes.c_void_p * E)()
+    for e in set(ids.ravel().tolist()):
+        r = np.ascontiguousarray(records[e])
+        keep.append(r)
+        ptrs[e] = r.ctypes.data
+    count = np.empty(T, np.int32)
+    lib().oracle_prefill_near_boundary(_p(x), T, H, I, fmt, k, _p(ids), ptrs,
+                                       _p(np.ascontiguousarray(g, np.float32)), _p(count))
+    return count
+
+
+def bf16_flip_delta(v):
+    """Per-element bf16 rounding-boundary slack of fp64 values v: one bf16
+    step where v lies within relative FLIP_BF16 of a bf16 rounding midpoint."""
+    v = np.ascontiguousarray(v, np.float64)
+    out = np.empty(v.shape[0], np.float64)
+    lib().oracle_bf16_flip_delta(_p(v), v.shape[0], _p(out))
+    return out
+
+
+def expert(rec, H, I, g3, x, act_quant=False, fmt=NVFP4):
     x = np.ascontiguousarray(x, np.float64)
     o = np.empty(H, np.float64)
-    lib().oracle_expert(_p(rec), H, I, _p(np.ascontiguousarray(g3, np.float32)), _p(x),
+    lib().oracle_expert(_p(rec), H, I, fmt, _p(np.ascontiguousarray(g3, np.float32)), _p(x),
                         int(act_quant), _p(o))
     return o
 
@@ -199,7 +277,7 @@ def shared(wg, wu, wd, x, round_h_bf16=False):
 
 
 def layer_forward(x, H, I, E, k, Wr, bias, records, g, shared_w=None, mode=0,
-                  return_bound=False, resident=None, tau=0.0):
+                  return_bound=False, resident=None, tau=0.0, fmt=NVFP4):
     """y [T,H] fp64 plus ids, w, p_sel (and, with return_bound, the
     rounding-boundary slack [T,H] of the prefill numerics, zero in mode 0).
     ``records`` maps expert id -> uint8 record array (a dict or a sequence
@@ -223,7 +301,7 @@ def layer_forward(x, H, I, E, k, Wr, bias, records, g, shared_w=None, mode=0,
     Is = 0 if shared_w is None else shared_w[0].shape[0]
     sg, su, sd = (None, None, None) if shared_w is None else shared_w
     rc = lib().oracle_layer_forward(
-        _p(x), T, H, I, E, k, Is, _p(np.ascontiguousarray(Wr, np.float32)),
+        _p(x), T, H, I, fmt, E, k, Is, _p(np.ascontiguousarray(Wr, np.float32)),
         _p(None if bias is None else np.ascontiguousarray(bias, np.float32)), ptrs,
         _p(np.ascontiguousarray(g, np.float32)), _p(sg), _p(su), _p(sd), mode,
         _p(None if resident is None else np.ascontiguousarray(resident, np.uint8)), float(tau),
@@ -277,3 +355,17 @@ def renorm_skip(ids, w, resident, tau):
                              _p(np.ascontiguousarray(resident, np.uint8)), float(tau),
                              _p(w_eff), _p(keep))
     return w_eff, keep.astype(bool)
+
+
+def slot_budget(counts, total, floor):
+    """Greedy per-layer slot budget from per-layer route counts [L,E]:
+    (layer_slots [L+1], order [L,E]) - layer l owns slots [layer_slots[l],
+    layer_slots[l+1]) and caches order[l][:n_l].  None when the floor does
+    not fit."""
+    counts = np.ascontiguousarray(counts, np.uint32)
+    L, E = counts.shape
+    ls = np.empty(L + 1, np.int32)
+    order = np.empty((L, E), np.int32)
+    if lib().oracle_slot_budget(L, E, _p(counts), int(total), int(floor), _p(ls), _p(order)):
+        return None
+    return ls, order

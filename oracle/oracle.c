@@ -63,6 +63,13 @@ ORC_API double oracle_e4m3(unsigned b) {
   return s ? -mag : mag;
 }
 
+/* E8M0 (the MX scale, OCP Microscaling Formats v1.0): 8 exponent bits,
+ * bias 127, no sign and no mantissa; 0xFF is NaN.  value = 2^(b - 127). */
+ORC_API double oracle_e8m0(unsigned b) {
+  b &= 0xFFu;
+  return b == 0xFFu ? NAN : ldexp(1.0, (int)b - 127);
+}
+
 /* bf16 is the top half of an IEEE binary32 */
 ORC_API double oracle_bf16(uint16_t h) {
   uint32_t u = (uint32_t)h << 16;
@@ -81,35 +88,44 @@ ORC_API void oracle_set_defect(int d) { g_defect = d; }
 
 static double g_e2m1[16];
 static double g_e4m3[256];
+static double g_e8m0[256];
 static int g_tables_ready = 0;
 
 static void tables_init(void) {
   if (g_tables_ready) return;
   for (unsigned c = 0; c < 16; ++c) g_e2m1[c] = oracle_e2m1(c);
   for (unsigned b = 0; b < 256; ++b) g_e4m3[b] = oracle_e4m3(b);
+  for (unsigned b = 0; b < 256; ++b) g_e8m0[b] = oracle_e8m0(b);
   g_tables_ready = 1;
 }
+
+/* record formats: NVFP4 = E4M3 scale per 16 values; MXFP4 = E8M0 scale per
+ * 32 values (windlass README: GLM-5.2 in MXFP4) */
+enum { ORC_NVFP4 = 0, ORC_MXFP4 = 1 };
+static int orc_block(int fmt) { return fmt == ORC_MXFP4 ? 32 : 16; }
 
 /* ----------------------------------------------------------- record access */
 
 /* Expert record: codes of gate [I][H], up [I][H], down [H][I] (row-major,
- * element 2j in the low nibble), then their E4M3 scales, one per 16 elements,
- * in 512-byte atoms: atom (r/128, kb/4) at ((r/128)*(KB/4) + kb/4)*512, byte
- * (r%32)*16 + ((r%128)/32)*4 + kb%4 inside it. */
+ * element 2j in the low nibble), then their scales, one per block of 16
+ * (NVFP4, E4M3) or 32 (MXFP4, E8M0) elements, in 512-byte atoms: block kb of
+ * row r in atom (r/128, kb/4) at ((r/128)*(KB/4) + kb/4)*512, byte
+ * (r%32)*16 + ((r%128)/32)*4 + kb%4 inside it, KB = blocks per row. */
 typedef struct {
   const uint8_t* codes;
   const uint8_t* scales;
-  int R, K;
+  int R, K, fmt;
   double g;
 } orc_mat;
 
-static orc_mat orc_matrix(const uint8_t* rec, int H, int I, int m, const float* g3) {
+static orc_mat orc_matrix(const uint8_t* rec, int H, int I, int fmt, int m, const float* g3) {
   orc_mat M;
   size_t gu_codes = (size_t)I * (size_t)H / 2;
   size_t all_codes = 3 * gu_codes;
-  size_t gu_scales = (size_t)I * (size_t)H / 16;
+  size_t gu_scales = (size_t)I * (size_t)H / (size_t)orc_block(fmt);
   M.R = (m == 2) ? H : I;
   M.K = (m == 2) ? I : H;
+  M.fmt = fmt;
   M.codes = rec + (size_t)m * gu_codes;
   M.scales = rec + all_codes + (size_t)m * gu_scales;
   M.g = (double)g3[m];
@@ -127,18 +143,22 @@ static double orc_w(const orc_mat* M, int r, int c) {
   int hi = (c & 1);
   if (g_defect == ORC_DEFECT_NIBBLE_SWAP) hi = !hi;
   unsigned code = hi ? (byte >> 4) : (byte & 15u);
-  int kb = c / 16;
-  if (g_defect == ORC_DEFECT_BLOCK_OFF_BY_ONE) kb = (kb + 1) % (M->K / 16);
-  uint8_t sb = M->scales[orc_scale_pos(r, kb, M->K / 16)];
-  double s = (g_defect == ORC_DEFECT_SCALE_UE8M0) ? ldexp(1.0, (int)sb - 127) : g_e4m3[sb];
+  const int bl = orc_block(M->fmt), KB = M->K / bl;
+  int kb = c / bl;
+  if (g_defect == ORC_DEFECT_BLOCK_OFF_BY_ONE) kb = (kb + 1) % KB;
+  uint8_t sb = M->scales[orc_scale_pos(r, kb, KB)];
+  /* the scale-decoding defect reads each format's byte as the other's */
+  int mx = M->fmt == ORC_MXFP4;
+  if (g_defect == ORC_DEFECT_SCALE_UE8M0) mx = !mx;
+  double s = mx ? g_e8m0[sb] : g_e4m3[sb];
   return g_e2m1[code] * s * M->g;
 }
 
 /* one dequantised weight, exported for the format pins */
-ORC_API double oracle_weight(const uint8_t* rec, int H, int I, int m, int r, int c,
+ORC_API double oracle_weight(const uint8_t* rec, int H, int I, int fmt, int m, int r, int c,
                              const float* g3) {
   tables_init();
-  orc_mat M = orc_matrix(rec, H, I, m, g3);
+  orc_mat M = orc_matrix(rec, H, I, fmt, m, g3);
   return orc_w(&M, r, c);
 }
 
@@ -153,10 +173,10 @@ static void orc_matvec(const orc_mat* M, const double* x, double* y) {
 }
 
 /* whole matrix dequantised, row-major [R][K], for brute-force pins */
-ORC_API void oracle_dequant_matrix(const uint8_t* rec, int H, int I, int m, const float* g3,
-                                   double* out) {
+ORC_API void oracle_dequant_matrix(const uint8_t* rec, int H, int I, int fmt, int m,
+                                   const float* g3, double* out) {
   tables_init();
-  orc_mat M = orc_matrix(rec, H, I, m, g3);
+  orc_mat M = orc_matrix(rec, H, I, fmt, m, g3);
   for (int r = 0; r < M.R; ++r)
     for (int c = 0; c < M.K; ++c) out[(size_t)r * M.K + c] = orc_w(&M, r, c);
 }
@@ -321,13 +341,73 @@ static void orc_nvfp4_dequant(const uint8_t* codes, const uint8_t* scales, float
   }
 }
 
-/* quantise-then-dequantise of a row given in fp32 */
-static void orc_act_quant(const float* v, int n, double* out) {
+/* nearest E2M1 magnitude to |q| for an exact double q (ties to the even
+ * code, saturating at 6), sign bit from q */
+static unsigned orc_e2m1_rne_sat_d(double q) {
+  double a = fabs(q);
+  unsigned best = 0;
+  double bd = INFINITY;
+  for (unsigned c = 0; c < 8; ++c) {
+    double d = fabs(g_e2m1[c] - a);
+    if (d < bd || (d == bd && (c & 1u) == 0)) { bd = d; best = c; }
+  }
+  if (a > 6.0) best = 7;
+  return signbit(q) ? (best | 8u) : best;
+}
+
+/* MXFP4 quantisation of one row of n fp32 values (n % 32 == 0), after OCP
+ * Microscaling Formats v1.0 (the conversion of a block of 32 values to an
+ * MX block): the block's shared exponent is X = floor(log2(max |v|)) - 2 (2
+ * = the exponent of E2M1's largest normal, 6 = 1.5 x 2^2), limited to the
+ * E8M0 range [-127, 127]; scale byte X + 127; each element's code is the
+ * E2M1 value nearest v / 2^X (exact), ties to even, saturating at 6.  An
+ * all-zero block gets scale byte 0 and codes 0.  codes [n/2] (element 2j in
+ * the low nibble), scales [n/32] in row order. */
+ORC_API void oracle_mxfp4_quant(const float* v, int n, uint8_t* codes, uint8_t* scales) {
+  tables_init();
+  for (int b = 0; b < n / 32; ++b) {
+    double amax = 0.0;
+    for (int i = 0; i < 32; ++i) {
+      double a = fabs((double)v[b * 32 + i]);
+      if (a > amax) amax = a;
+    }
+    int X = -127;
+    if (amax > 0.0) {
+      int e;
+      frexp(amax, &e);  /* amax = f 2^e, f in [0.5, 1): floor(log2 amax) = e - 1 */
+      X = e - 1 - 2;
+      if (X < -127) X = -127;
+      if (X > 127) X = 127;
+    }
+    scales[b] = (uint8_t)(amax > 0.0 ? X + 127 : 0);
+    for (int i = 0; i < 32; i += 2) {
+      unsigned lo = 0, hi = 0;
+      if (amax > 0.0) {
+        lo = orc_e2m1_rne_sat_d(ldexp((double)v[b * 32 + i], -X));
+        hi = orc_e2m1_rne_sat_d(ldexp((double)v[b * 32 + i + 1], -X));
+      }
+      codes[(b * 32 + i) / 2] = (uint8_t)(lo | (hi << 4));
+    }
+  }
+}
+
+/* quantise-then-dequantise of a row given in fp32, in the prefill numerics
+ * of the record format: NVFP4 (E4M3 per 16, fp32 global) or MXFP4 (E8M0 per
+ * 32) - the tensor cores take both operands' block scales in one format */
+static void orc_act_quant(const float* v, int n, int fmt, double* out) {
   uint8_t* codes = (uint8_t*)malloc((size_t)n / 2);
   uint8_t* scales = (uint8_t*)malloc((size_t)n / 16);
-  float G;
-  oracle_nvfp4_quant(v, n, codes, scales, &G);
-  orc_nvfp4_dequant(codes, scales, G, n, out);
+  if (fmt == ORC_MXFP4) {
+    oracle_mxfp4_quant(v, n, codes, scales);
+    for (int i = 0; i < n; ++i) {
+      unsigned c = (i & 1) ? (codes[i / 2] >> 4) : (codes[i / 2] & 15u);
+      out[i] = g_e2m1[c] * g_e8m0[scales[i / 32]];
+    }
+  } else {
+    float G;
+    oracle_nvfp4_quant(v, n, codes, scales, &G);
+    orc_nvfp4_dequant(codes, scales, G, n, out);
+  }
   free(codes);
   free(scales);
 }
@@ -335,15 +415,40 @@ static void orc_act_quant(const float* v, int n, double* out) {
 /* Rounding-boundary slack of an NVFP4 quantisation.  Two implementations
  * whose fp32 inputs differ in the last bits may round an element that sits
  * next to a rounding boundary to either neighbour; both results are correct.
+ * The margins say how close counts as "next to":
+ *   - an element whose scaled magnitude q = |v| / (s G) lies within
+ *     g_flip_q code units of an E2M1 midpoint (0.25, 0.75, ..., 5) may take
+ *     either neighbouring code: delta = the distance between the two codes'
+ *     values, (hi - lo) s G;
+ *   - a block whose scale argument t = amax_b / (6 G) lies within relative
+ *     g_flip_t of an E4M3 midpoint may take either neighbouring scale s1 <
+ *     s2.  Under s2 a value is within half a code step (at most 1, between
+ *     codes 4 and 6) of v / (s2 G); under s1 the values above 6 s1 G
+ *     saturate, by at most 6 G (t - s1) <= 3 s2 G (s1 = 0 included), the
+ *     others are within s1 G.  So every element gets delta = 4 s2 G.
  * delta[i] receives the largest change of element i's quantised value that
- * such a flip can cause (0 when the element is not within relative FLIP_EPS
- * of an E2M1 boundary and its block scale is not within FLIP_EPS of an E4M3
- * boundary).  Same fp32 steps as oracle_nvfp4_quant. */
-#define FLIP_EPS 1e-4
-static void orc_quant_flip_delta(const float* v, int n, double* delta) {
-  static const double mids[7] = {0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0};
-  static const double lo_mag[7] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0};
-  static const double hi_mag[7] = {0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+ * such a flip can cause, 0 elsewhere.  Same fp32 steps as
+ * oracle_nvfp4_quant.  The margins are set well above the difference
+ * between an fp64 value rounded to fp32 and the same value summed in fp32
+ * by another implementation (oracle_set_flip_margins). */
+static double g_flip_q = 2e-5;
+static double g_flip_t = 1e-5;
+static double g_flip_bf16 = 2e-6;
+
+ORC_API void oracle_set_flip_margins(double q_codes, double t_rel, double bf16_rel) {
+  g_flip_q = q_codes;
+  g_flip_t = t_rel;
+  g_flip_bf16 = bf16_rel;
+}
+
+static const double g_mids[7] = {0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0};
+static const double g_lo_mag[7] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0};
+static const double g_hi_mag[7] = {0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+
+static void orc_nv_flip_delta(const float* v, int n, double* delta) {
+  const double* mids = g_mids;
+  const double* lo_mag = g_lo_mag;
+  const double* hi_mag = g_hi_mag;
   float amax = 0.0f;
   for (int i = 0; i < n; ++i) {
     float a = fabsf(v[i]);
@@ -360,34 +465,76 @@ static void orc_quant_flip_delta(const float* v, int n, double* delta) {
     volatile float sixG = 6.0f * G;
     float t = ab / sixG;
     unsigned s = oracle_e4m3_rne(t);
-    /* block scale near an E4M3 rounding boundary: the block may take the
-     * neighbouring scale, every value may move by up to its own size */
-    int scale_flip = 0;
-    for (unsigned c = 1; c <= 0x7E && !scale_flip; ++c) {
+    /* block scale next to an E4M3 rounding boundary (between codes c-1, c) */
+    double s_hi = -1.0;
+    for (unsigned c = 1; c <= 0x7E && s_hi < 0.0; ++c) {
       double mid = 0.5 * (g_e4m3[c - 1] + g_e4m3[c]);
-      if (fabs((double)t - mid) <= FLIP_EPS * mid) scale_flip = 1;
+      if (fabs((double)t - mid) <= g_flip_t * mid) s_hi = g_e4m3[c];
     }
     double sg = g_e4m3[s] * (double)G;
     for (int i = 0; i < 16; ++i) {
       double d = 0.0;
-      if (scale_flip) d = fabs((double)v[b * 16 + i]) + 6.0 * sg / 8.0;
+      if (s_hi >= 0.0) d = 4.0 * s_hi * (double)G;
       else if (s != 0) {
         double q = fabs((double)v[b * 16 + i]) / sg;
         for (int j = 0; j < 7; ++j)
-          if (fabs(q - mids[j]) <= FLIP_EPS * mids[j]) d = (hi_mag[j] - lo_mag[j]) * sg;
+          if (fabs(q - mids[j]) <= g_flip_q) d = (hi_mag[j] - lo_mag[j]) * sg;
       }
       delta[b * 16 + i] = d;
     }
   }
 }
 
-ORC_API void oracle_quant_flip_delta(const float* v, int n, double* delta) {
+/* The same for MXFP4 blocks of 32: an element within g_flip_q code units of
+ * an E2M1 midpoint of v / 2^X gets one code step x 2^X; a block whose max
+ * |v| lies within relative g_flip_t of a power of two may take the shared
+ * exponent X or X + 1: under 2^(X+1) a value is within one code unit
+ * (2^(X+1)) of v, under 2^X within 2^X or, saturated at 6 x 2^X, within
+ * 8 x 2^X - 6 x 2^X = 2^(X+1); every element gets delta = 2 x 2^(X+1). */
+static void orc_mx_flip_delta(const float* v, int n, double* delta) {
+  for (int b = 0; b < n / 32; ++b) {
+    double amax = 0.0;
+    for (int i = 0; i < 32; ++i) {
+      double a = fabs((double)v[b * 32 + i]);
+      if (a > amax) amax = a;
+    }
+    int X = -127, near_pow2 = 0;
+    if (amax > 0.0) {
+      int e;
+      double f = frexp(amax, &e);  /* amax = f 2^e, f in [0.5, 1) */
+      X = e - 3;
+      if (X < -127) X = -127;
+      if (X > 127) X = 127;
+      /* distance to 2^(e-1) (just above it) or 2^e (just below it) */
+      near_pow2 = (f - 0.5) <= g_flip_t * 0.5 || (1.0 - f) <= g_flip_t;
+      if (near_pow2 && (1.0 - f) <= g_flip_t) X = X + 1 > 127 ? 127 : X + 1;
+    }
+    const double sx = ldexp(1.0, X);
+    for (int i = 0; i < 32; ++i) {
+      double d = 0.0;
+      if (near_pow2) d = 2.0 * sx;
+      else if (amax > 0.0) {
+        double q = fabs((double)v[b * 32 + i]) / sx;
+        for (int j = 0; j < 7; ++j)
+          if (fabs(q - g_mids[j]) <= g_flip_q) d = (g_hi_mag[j] - g_lo_mag[j]) * sx;
+      }
+      delta[b * 32 + i] = d;
+    }
+  }
+}
+
+static void orc_quant_flip_delta(const float* v, int n, int fmt, double* delta) {
+  if (fmt == ORC_MXFP4) orc_mx_flip_delta(v, n, delta);
+  else orc_nv_flip_delta(v, n, delta);
+}
+
+ORC_API void oracle_quant_flip_delta(const float* v, int n, int fmt, double* delta) {
   tables_init();
-  orc_quant_flip_delta(v, n, delta);
+  orc_quant_flip_delta(v, n, fmt, delta);
 }
 
 /* bf16 rounding slack: one bf16 step when the value lies within relative
- * FLIP_EPS of a bf16 rounding midpoint */
+ * g_flip_bf16 of a bf16 rounding midpoint */
 static double orc_bf16_flip_delta(double hv) {
   float f = (float)hv;
   uint32_t b;
@@ -397,54 +544,110 @@ static double orc_bf16_flip_delta(double hv) {
   memcpy(&flo, &lo, 4);
   memcpy(&fhi, &hi, 4);
   double mid = 0.5 * ((double)flo + (double)fhi);
-  return (fabs(hv - mid) <= FLIP_EPS * fabs(mid)) ? fabs((double)fhi - (double)flo) : 0.0;
+  return (fabs(hv - mid) <= g_flip_bf16 * fabs(mid)) ? fabs((double)fhi - (double)flo) : 0.0;
+}
+
+ORC_API void oracle_bf16_flip_delta(const double* v, int n, double* delta) {
+  for (int i = 0; i < n; ++i) delta[i] = orc_bf16_flip_delta(v[i]);
 }
 
 /* ------------------------------------------------------------------ experts */
 
 static double orc_silu(double g) { return g / (1.0 + exp(-g)); }
 
+/* h = silu(Wg x) * (Wu x), fp64, for one activation vector x [H] -> h [I] */
+static void orc_expert_h(const orc_mat* Mg, const orc_mat* Mu, int I, const double* x,
+                         double* h) {
+  double* g = (double*)malloc(sizeof(double) * (size_t)I);
+  double* u = (double*)malloc(sizeof(double) * (size_t)I);
+  orc_matvec(Mg, x, g);
+  orc_matvec(Mu, x, u);
+  for (int i = 0; i < I; ++i) h[i] = orc_silu(g[i]) * u[i];
+  free(g);
+  free(u);
+}
+
 /* One routed expert on one activation vector x [H] -> o [H].
  * act_quant != 0: prefill numerics (h rounded to fp32 and NVFP4-quantised
  * before the down projection; x must already be the quantised value).
  * bound (nullable, act_quant only): bound[r] += wabs * sum_i |Wd[r][i]| *
  * delta_i, the most that rounding-boundary flips of h can move o[r] * wabs. */
-static void orc_expert_impl(const uint8_t* rec, int H, int I, const float* g3, const double* x,
+static void orc_expert_impl(const uint8_t* rec, int H, int I, int fmt, const float* g3,
+                            const double* x,
                             int act_quant, double* o, double wabs, double* bound) {
   tables_init();
-  orc_mat Mg = orc_matrix(rec, H, I, 0, g3);
-  orc_mat Mu = orc_matrix(rec, H, I, 1, g3);
-  orc_mat Md = orc_matrix(rec, H, I, 2, g3);
-  double* g = (double*)malloc(sizeof(double) * (size_t)I);
-  double* u = (double*)malloc(sizeof(double) * (size_t)I);
+  orc_mat Mg = orc_matrix(rec, H, I, fmt, 0, g3);
+  orc_mat Mu = orc_matrix(rec, H, I, fmt, 1, g3);
+  orc_mat Md = orc_matrix(rec, H, I, fmt, 2, g3);
   double* h = (double*)malloc(sizeof(double) * (size_t)I);
-  orc_matvec(&Mg, x, g);
-  orc_matvec(&Mu, x, u);
-  for (int i = 0; i < I; ++i) h[i] = orc_silu(g[i]) * u[i];
+  orc_expert_h(&Mg, &Mu, I, x, h);
   if (act_quant) {
     float* hf = (float*)malloc(sizeof(float) * (size_t)I);
     for (int i = 0; i < I; ++i) hf[i] = (float)h[i];
     if (bound) {
       double* delta = (double*)malloc(sizeof(double) * (size_t)I);
-      orc_quant_flip_delta(hf, I, delta);
+      orc_quant_flip_delta(hf, I, fmt, delta);
       for (int i = 0; i < I; ++i) {
         if (delta[i] == 0.0) continue;
         for (int r = 0; r < H; ++r) bound[r] += wabs * fabs(orc_w(&Md, r, i)) * delta[i];
       }
       free(delta);
     }
-    orc_act_quant(hf, I, h);
+    orc_act_quant(hf, I, fmt, h);
     free(hf);
   }
   orc_matvec(&Md, h, o);
-  free(g);
-  free(u);
   free(h);
 }
 
-ORC_API void oracle_expert(const uint8_t* rec, int H, int I, const float* g3, const double* x,
+ORC_API void oracle_expert(const uint8_t* rec, int H, int I, int fmt, const float* g3,
+                           const double* x,
                            int act_quant, double* o) {
-  orc_expert_impl(rec, H, I, g3, x, act_quant, o, 0.0, NULL);
+  orc_expert_impl(rec, H, I, fmt, g3, x, act_quant, o, 0.0, NULL);
+}
+
+/* h [I] (fp64, before any quantisation) of one routed expert on x [H]
+ * (already the quantised value in prefill numerics) */
+ORC_API void oracle_expert_h(const uint8_t* rec, int H, int I, int fmt, const float* g3,
+                             const double* x,
+                             double* h) {
+  tables_init();
+  orc_mat Mg = orc_matrix(rec, H, I, fmt, 0, g3);
+  orc_mat Mu = orc_matrix(rec, H, I, fmt, 1, g3);
+  orc_expert_h(&Mg, &Mu, I, x, h);
+}
+
+/* Prefill numerics: for each token t of x [T][H] (bf16) with routes ids
+ * [T][k], the number of elements of its routes' h (rounded to fp32) that
+ * lie within the margins of an NVFP4 rounding boundary (nonzero slack of
+ * orc_quant_flip_delta), where another implementation's fp32 sums may round
+ * them to the neighbouring code.  rec[e] as in oracle_layer_forward. */
+ORC_API void oracle_prefill_near_boundary(const uint16_t* x, int T, int H, int I, int fmt, int k,
+                                          const int32_t* ids, const uint8_t* const* rec,
+                                          const float* g, int32_t* count) {
+  tables_init();
+  #pragma omp parallel for schedule(dynamic, 1)
+  for (int t = 0; t < T; ++t) {
+    double* xq = (double*)malloc(sizeof(double) * (size_t)H);
+    float* xf = (float*)malloc(sizeof(float) * (size_t)H);
+    double* h = (double*)malloc(sizeof(double) * (size_t)I);
+    float* hf = (float*)malloc(sizeof(float) * (size_t)I);
+    double* delta = (double*)malloc(sizeof(double) * (size_t)I);
+    for (int c = 0; c < H; ++c) xf[c] = (float)oracle_bf16(x[(size_t)t * H + c]);
+    orc_act_quant(xf, H, fmt, xq);
+    int n = 0;
+    for (int j = 0; j < k; ++j) {
+      const int e = ids[(size_t)t * k + j];
+      orc_mat Mg = orc_matrix(rec[e], H, I, fmt, 0, g + 3 * e);
+      orc_mat Mu = orc_matrix(rec[e], H, I, fmt, 1, g + 3 * e);
+      orc_expert_h(&Mg, &Mu, I, xq, h);
+      for (int i = 0; i < I; ++i) hf[i] = (float)h[i];
+      orc_quant_flip_delta(hf, I, fmt, delta);
+      for (int i = 0; i < I; ++i) n += delta[i] != 0.0;
+    }
+    count[t] = n;
+    free(xq); free(xf); free(h); free(hf); free(delta);
+  }
 }
 
 /* Shared expert with bf16 weights gate/up [Is][H], down [H][Is].
@@ -525,7 +728,8 @@ ORC_API void oracle_renorm_skip(const int32_t* ids, const double* w, int T, int 
 }
 
 /* The layer.  resident/tau: the renorm-skip above (resident == NULL: exact). */
-ORC_API int oracle_layer_forward(const uint16_t* x, int T, int H, int I, int E, int k, int Is,
+ORC_API int oracle_layer_forward(const uint16_t* x, int T, int H, int I, int fmt, int E, int k,
+                                 int Is,
                                  const float* Wr, const float* bias, const uint8_t* const* rec,
                                  const float* g, const uint16_t* sg, const uint16_t* su,
                                  const uint16_t* sd, int mode, const uint8_t* resident,
@@ -544,16 +748,18 @@ ORC_API int oracle_layer_forward(const uint16_t* x, int T, int H, int I, int E, 
       free(ids); free(w); free(p); free(weff); free(keep);
       return 2;
     }
-  double* xd = (double*)malloc(sizeof(double) * (size_t)H);
-  double* xq = (double*)malloc(sizeof(double) * (size_t)H);
-  float* xf = (float*)malloc(sizeof(float) * (size_t)H);
-  double* o = (double*)malloc(sizeof(double) * (size_t)H);
+  /* tokens are independent: one per thread (each token's own steps in order) */
+  #pragma omp parallel for schedule(dynamic, 1)
   for (int t = 0; t < T; ++t) {
+    double* xd = (double*)malloc(sizeof(double) * (size_t)H);
+    double* xq = (double*)malloc(sizeof(double) * (size_t)H);
+    float* xf = (float*)malloc(sizeof(float) * (size_t)H);
+    double* o = (double*)malloc(sizeof(double) * (size_t)H);
     for (int c = 0; c < H; ++c) {
       xd[c] = oracle_bf16(x[(size_t)t * H + c]);
       xf[c] = (float)xd[c];
     }
-    if (mode == 1) orc_act_quant(xf, H, xq);
+    if (mode == 1) orc_act_quant(xf, H, fmt, xq);
     else memcpy(xq, xd, sizeof(double) * (size_t)H);
     double* yt = y + (size_t)t * H;
     double* bt = (ybound && mode == 1) ? ybound + (size_t)t * H : NULL;
@@ -563,7 +769,7 @@ ORC_API int oracle_layer_forward(const uint16_t* x, int T, int H, int I, int E, 
       if (!keep[(size_t)t * k + j]) continue;
       int e = ids[(size_t)t * k + j];
       double wj = weff[(size_t)t * k + j];
-      orc_expert_impl(rec[e], H, I, g + 3 * e, xq, mode == 1, o, fabs(wj), bt);
+      orc_expert_impl(rec[e], H, I, fmt, g + 3 * e, xq, mode == 1, o, fabs(wj), bt);
       if (g_defect == ORC_DEFECT_SCALING_2_5) wj *= 2.5;
       for (int c = 0; c < H; ++c) yt[c] += wj * o[c];
     }
@@ -571,11 +777,12 @@ ORC_API int oracle_layer_forward(const uint16_t* x, int T, int H, int I, int E, 
       orc_shared_impl(sg, su, sd, H, Is, xd, mode == 1, o, bt);
       for (int c = 0; c < H; ++c) yt[c] += o[c];
     }
+    free(xd); free(xq); free(xf); free(o);
   }
   if (ids_out) memcpy(ids_out, ids, sizeof(int32_t) * (size_t)T * k);
   if (w_out) memcpy(w_out, w, sizeof(double) * (size_t)T * k);
   if (p_out) memcpy(p_out, p, sizeof(double) * (size_t)T * k);
-  free(ids); free(w); free(p); free(weff); free(keep); free(xd); free(xq); free(xf); free(o);
+  free(ids); free(w); free(p); free(weff); free(keep);
   return 0;
 }
 
@@ -647,4 +854,68 @@ ORC_API int oracle_cache_policy_step(int L, int E, int layer, int slot_lo, int s
     tab[victim] = -1;
   }
   return n_miss;
+}
+
+/* ----------------------------------------------- per-layer slot budgets */
+
+/* Greedy per-layer slot budget ("Project Maya" page, section "VRAM: one
+ * partition per layer, sized by what the layer routes"): with counts[l][e]
+ * the routes of expert e in layer l (per-layer sums below 2^32):
+ *   1. order each layer's experts by count, descending, ties to the lower id
+ *      (order[l][0..E));
+ *   2. every layer gets `floor` slots (its `floor` most-routed experts);
+ *   3. each further slot, one at a time, goes to the layer whose next
+ *      expert in that order serves the largest share of the layer's lookups,
+ *      counts[l][next] / sum_e counts[l][e] (0 for a layer without routes),
+ *      ties to the lower layer; a layer whose E experts all have slots takes
+ *      no more.
+ * Slots left once every layer is full stay unassigned.  layer_slots[L+1] =
+ * the partition's prefix sums (layer l owns [layer_slots[l],
+ * layer_slots[l+1])); layer l's residents are order[l][0 .. n_l).  Returns
+ * 0, or 1 when floor > E or total < L * floor. */
+ORC_API int oracle_slot_budget(int L, int E, const uint32_t* counts, int total, int floor,
+                               int32_t* layer_slots, int32_t* order) {
+  if (floor < 0 || floor > E || total < L * floor) return 1;
+  uint64_t* sum = (uint64_t*)calloc((size_t)L, sizeof(uint64_t));
+  int* n = (int*)malloc(sizeof(int) * (size_t)L);
+  for (int l = 0; l < L; ++l) {
+    const uint32_t* c = counts + (size_t)l * E;
+    int32_t* o = order + (size_t)l * E;
+    for (int e = 0; e < E; ++e) {
+      o[e] = e;
+      sum[l] += c[e];
+    }
+    /* insertion sort: count descending, then id ascending */
+    for (int i = 1; i < E; ++i) {
+      int32_t v = o[i];
+      int j = i - 1;
+      while (j >= 0 && (c[o[j]] < c[v] || (c[o[j]] == c[v] && o[j] > v))) {
+        o[j + 1] = o[j];
+        --j;
+      }
+      o[j + 1] = v;
+    }
+    n[l] = floor;
+  }
+  for (int given = L * floor; given < total; ++given) {
+    int best = -1;
+    for (int l = 0; l < L; ++l) {
+      if (n[l] >= E) continue;
+      if (best < 0) { best = l; continue; }
+      /* share of l's next expert > share of best's next expert, exactly:
+       * c_l / S_l > c_b / S_b  <=>  c_l * S_b > c_b * S_l (a layer without
+       * routes has share 0) */
+      uint64_t cl = sum[l] ? counts[(size_t)l * E + order[(size_t)l * E + n[l]]] : 0;
+      uint64_t cb = sum[best] ? counts[(size_t)best * E + order[(size_t)best * E + n[best]]] : 0;
+      uint64_t Sl = sum[l] ? sum[l] : 1, Sb = sum[best] ? sum[best] : 1;
+      if (cl * Sb > cb * Sl) best = l;
+    }
+    if (best < 0) break;
+    ++n[best];
+  }
+  layer_slots[0] = 0;
+  for (int l = 0; l < L; ++l) layer_slots[l + 1] = layer_slots[l] + n[l];
+  free(sum);
+  free(n);
+  return 0;
 }

@@ -19,11 +19,13 @@ size_t decode_workspace_bytes(int T, int I, int k, int Is);
 moe_status decode_ffn(const moe_ffn_args* a, cudaStream_t s, const DecodeFuse& fz);
 moe_status decode_setup();
 size_t prefill_workspace_bytes(int T, int H, int I, int E, int k, int Is);
+const float* prefill_h_rows(const void* workspace, int T, int H, int I, int E, int k, int Is);
 moe_status prefill_ffn(const moe_ffn_args* a, cudaStream_t s);
 moe_status prefill_setup();
 moe_status nvfp4_quantize(const void* x, int dtype, int T, int K, uint8_t* codes,
                           uint8_t* scales, float* G, cudaStream_t s);
 moe_status permute_setup();
+moe_status noalloc_setup();
 moe_status launch_permute(const int32_t* ids, int T, int k, int E, int32_t* counts,
                           int32_t* offsets, int32_t* perm, int32_t* inv, int32_t* pad_offsets,
                           int pad_align, int32_t* status, const LookupArgs& lk, cudaStream_t s);
@@ -35,18 +37,6 @@ moe_status route_permute_small(const moe_route_args* a, const PermArgs& pa,
 moe_status launch_route_skip(const SkipArgs& sk, const int32_t* ids, const float* w, int T, int k,
                              int E, cudaStream_t s);
 bool cache_policy_args(const expcache* c, int layer, PolicyArgs* a);
-}  // namespace moe
-
-namespace moe {
-static int pdl_mode() {
-  static const int m = [] {
-    const char* v = getenv("MOE_PDL");
-    return !v ? 2 : v[0] == '0' ? 0 : v[0] == '1' ? 1 : 2;
-  }();
-  return m;
-}
-bool pdl_enabled() { return pdl_mode() != 0; }
-bool pdl_in_graphs() { return pdl_mode() == 2; }
 }  // namespace moe
 
 using namespace moe;
@@ -70,7 +60,8 @@ MOE_API const char* moe_status_string(moe_status s) {
 
 MOE_API int moe_abi_version(void) { return 4; }
 
-static moe_status ensure_setup() {
+namespace moe {
+moe_status ensure_setup() {
   static int done = 0;
   if (done) return MOE_OK;
   moe_status s = decode_setup();
@@ -79,9 +70,12 @@ static moe_status ensure_setup() {
   if (s != MOE_OK) return s;
   s = prefill_setup();
   if (s != MOE_OK) return s;
+  s = noalloc_setup();
+  if (s != MOE_OK) return s;
   done = 1;
   return MOE_OK;
 }
+}  // namespace moe
 
 MOE_API size_t moe_ffn_workspace_bytes(int mode, int T, int H, int I, int E, int k, int Is) {
   if (T < 0 || H <= 0 || I <= 0 || E <= 0 || k <= 0 || Is < 0) return 0;
@@ -408,6 +402,18 @@ MOE_API moe_status moe_layer_debug_ptrs(const moe_layer* l, const int32_t** ids,
   if (perm) *perm = l->perm;
   if (src_slot) *src_slot = l->src_slot;
   if (n_act) *n_act = l->n_act;
+  return MOE_OK;
+}
+
+MOE_API moe_status moe_layer_debug_prefill(const moe_layer* l, const float** h_rows,
+                                           const int32_t** offsets,
+                                           const int32_t** pad_offsets) {
+  if (!l || !h_rows || !offsets || !pad_offsets) return MOE_ERR_INVALID_ARG;
+  const moe_layer_desc& d = l->d;
+  if (!(d.prefill_min_tokens > 0 && l->last_T >= d.prefill_min_tokens)) return MOE_ERR_INVALID_ARG;
+  *h_rows = prefill_h_rows(l->ffn_ws, l->last_T, d.H, d.I, d.E, d.k, d.Is);
+  *offsets = l->offsets;
+  *pad_offsets = l->pad_offsets;
   return MOE_OK;
 }
 

@@ -126,6 +126,10 @@ MOE_API uint64_t moe_record_bytes(int H, int I) {
   return RecordLayout(H, I).bytes;
 }
 
+namespace moe {
+moe_status ensure_setup();
+}
+
 MOE_API moe_status expcache_create(const expcache_desc* d, expcache** out) {
   if (!d || !out) return MOE_ERR_INVALID_ARG;
   *out = nullptr;
@@ -139,6 +143,7 @@ MOE_API moe_status expcache_create(const expcache_desc* d, expcache** out) {
       if (d->layer_slots[l + 1] < d->layer_slots[l]) return MOE_ERR_INVALID_ARG;
     if (d->layer_slots[d->L] > d->n_cache_slots) return MOE_ERR_INVALID_ARG;
   }
+  if (moe_status st = moe::ensure_setup()) return st;
   expcache* c = (expcache*)calloc(1, sizeof(expcache));
   if (!c) return MOE_ERR_OOM;
   c->L = d->L; c->E = d->E; c->H = d->H; c->I = d->I;
@@ -388,5 +393,108 @@ MOE_API moe_status expcache_policy_state(const expcache* c, int* spares, const u
   *last = c->last;
   *stamp = c->stamp;
   *freeslot = c->freeslot;
+  return MOE_OK;
+}
+
+// ---- per-layer slot budgets ------------------------------------------------
+// "Project Maya" page, section "VRAM: one partition per layer, sized by what
+// the layer routes": a floor per layer, then each further slot to the layer
+// whose next-most-routed expert serves the largest share of its lookups.
+// Within a layer the shares of successive experts (by count, descending) never
+// grow, so handing out slots one at a time in that way takes the candidates
+// (layer l, rank r >= floor) in one global order - share descending, then
+// layer ascending, then rank ascending - and keeps the first N of them.  Here
+// each candidate finds its place in that order directly: in its own layer r -
+// floor candidates precede it, and in every other layer a prefix of the ranks
+// (found by binary search, since the shares there never grow).
+namespace moe {
+
+constexpr int kPlanThreads = 1024;
+
+// c1 / s1 > c2 / s2 for counts c < 2^32 and sums s < 2^64, exactly (128-bit
+// products); a layer without routes (s == 0) has share 0
+__device__ __forceinline__ int share_cmp(uint32_t c1, uint64_t s1, uint32_t c2, uint64_t s2) {
+  const uint64_t a = s1 ? c1 : 0, b = s2 ? c2 : 0;
+  const uint64_t t1 = s1 ? s1 : 1, t2 = s2 ? s2 : 1;
+  // compare a * t2 with b * t1
+  const uint64_t hi1 = __umul64hi(a, t2), lo1 = a * t2;
+  const uint64_t hi2 = __umul64hi(b, t1), lo2 = b * t1;
+  if (hi1 != hi2) return hi1 > hi2 ? 1 : -1;
+  if (lo1 != lo2) return lo1 > lo2 ? 1 : -1;
+  return 0;
+}
+
+__global__ void __launch_bounds__(kPlanThreads) k_plan_slots(
+    const uint32_t* __restrict__ counts, int L, int E, int floor, int n_extra,
+    int32_t* __restrict__ layer_slots, int32_t* __restrict__ order) {
+  extern __shared__ unsigned long long s_sum[];  // [L] route sums, then [L] slot counts
+  int* s_n = reinterpret_cast<int*>(s_sum + L);
+  for (int l = threadIdx.x; l < L; l += blockDim.x) {
+    s_sum[l] = 0ull;
+    s_n[l] = floor;
+  }
+  __syncthreads();
+  // 1. per layer: rank of every expert (count descending, id ascending) and the sums
+  for (int i = threadIdx.x; i < L * E; i += blockDim.x) {
+    const int l = i / E, e = i % E;
+    const uint32_t* c = counts + (size_t)l * E;
+    const uint32_t v = c[e];
+    int rank = 0;
+    for (int f = 0; f < E; ++f) {
+      const uint32_t u = c[f];
+      rank += (u > v) || (u == v && f < e);
+    }
+    order[(size_t)l * E + rank] = e;
+    atomicAdd(&s_sum[l], (unsigned long long)v);
+  }
+  __syncthreads();
+  // 2. every candidate (l, r >= floor): its position in the global order
+  const int per = E - floor;
+  for (int i = threadIdx.x; i < L * per; i += blockDim.x) {
+    const int l = i / per, r = floor + i % per;
+    const uint32_t cv = counts[(size_t)l * E + order[(size_t)l * E + r]];
+    const uint64_t sv = s_sum[l];
+    long long pos = r - floor;
+    for (int m = 0; m < L; ++m) {
+      if (m == l) continue;
+      // ranks of layer m that come first: share greater, or equal and m < l
+      const uint64_t sm = s_sum[m];
+      int lo = floor, hi = E;  // first rank of m that does not come first
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        const int c = share_cmp(counts[(size_t)m * E + order[(size_t)m * E + mid]], sm, cv, sv);
+        if (c > 0 || (c == 0 && m < l)) lo = mid + 1;
+        else hi = mid;
+      }
+      pos += lo - floor;
+    }
+    if (pos < n_extra) atomicAdd(&s_n[l], 1);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int acc = 0;
+    layer_slots[0] = 0;
+    for (int l = 0; l < L; ++l) {
+      acc += s_n[l];
+      layer_slots[l + 1] = acc;
+    }
+  }
+}
+
+}  // namespace moe
+
+MOE_API moe_status expcache_plan_slots(const uint32_t* d_counts, int L, int E, int total_slots,
+                                       int floor, int32_t* d_layer_slots, int32_t* d_order,
+                                       void* stream) {
+  if (!d_counts || !d_layer_slots || !d_order || L <= 0 || E <= 0 || floor < 0 || total_slots < 0)
+    return MOE_ERR_INVALID_ARG;
+  if (floor > E || (long long)total_slots < (long long)L * floor) return MOE_ERR_INVALID_ARG;
+  if (L > 4096 || E > 1024) return MOE_ERR_UNSUPPORTED;
+  long long all = (long long)L * E;
+  const int n_extra = (int)((total_slots < all ? total_slots : all) - (long long)L * floor);
+  const size_t smem = (size_t)L * (sizeof(unsigned long long) + sizeof(int));
+  moe::k_plan_slots<<<1, moe::kPlanThreads, smem, (cudaStream_t)stream>>>(
+      d_counts, L, E, floor, n_extra, d_layer_slots, d_order);
+  MOE_CHECK_LAUNCH();
   return MOE_OK;
 }

@@ -112,7 +112,8 @@ __device__ __forceinline__ float warp_sum(float v) {
 
 // ---- programmatic dependent launch ------------------------------------------
 // A kernel launched with launch_pdl() may start while the previous kernel on
-// its stream is still running (in streams and in captured CUDA graphs).  pdl_wait() blocks until that kernel has
+// its stream is still running (in streams and in captured CUDA graphs, where
+// it measured faster too).  pdl_wait() blocks until that kernel has
 // completed and its writes are visible; pdl_launch_dependents() lets the next
 // kernel start launching.  Every kernel launched with launch_pdl() calls
 // pdl_wait() before it touches memory that an earlier kernel writes or reads,
@@ -122,9 +123,6 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
-
-bool pdl_enabled();    // on unless the environment sets MOE_PDL=0
-bool pdl_in_graphs();  // also inside stream capture, unless MOE_PDL=1
 
 // What the layer's own sequence lets the decode FFN do beyond moe_expert_ffn:
 // start the shared-expert gate/up units before the routing is complete (the
@@ -154,13 +152,7 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
-  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-  bool plain = !pdl_enabled();
-  if (!plain && cudaStreamIsCapturing(s, &cs) != cudaSuccess) {
-    cudaGetLastError();  // not a launch error: launch without the attribute
-    plain = true;
-  }
-  cfg.numAttrs = (plain || (cs != cudaStreamCaptureStatusNone && !pdl_in_graphs())) ? 0 : 1;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, ((KArgs)args)...);
 }
 

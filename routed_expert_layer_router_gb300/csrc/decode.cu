@@ -131,10 +131,21 @@ __device__ __forceinline__ void group_range(const DecodeParams& p, int& a0, int&
 // storing any of them, so that a CTA's staging costs about one round trip.
 constexpr int kStageBatch = 8;
 
+// Largest magnitude the f16 staging holds (f16's largest finite value): the
+// decode FFN's products are f16 x f16, so an activation beyond it (or inf or
+// NaN) is outside what the decode path computes.  The staging functions
+// return true when a thread saw such a value; the kernel then sets
+// MOE_ERR_UNSUPPORTED in the status word.
+constexpr float kF16Max = 65504.f;
+__device__ __forceinline__ bool f16_out_of_range(float a, float b) {
+  return !(fabsf(a) <= kF16Max) || !(fabsf(b) <= kF16Max);
+}
+
 // f16 layout: row j, half-k-group hk (32 values) at (j*nhk + hk)*kHPad halves
-__device__ __forceinline__ void stage_bf16_to_f16(__half* xs, const uint16_t* const* rows, int m,
+__device__ __forceinline__ bool stage_bf16_to_f16(__half* xs, const uint16_t* const* rows, int m,
                                                   int K) {
   const int nhk = K / 32, n = K / 2;
+  bool bad = false;
   for (int j = 0; j < m; ++j) {
     const uint32_t* src = reinterpret_cast<const uint32_t*>(rows[j]);
     __half* dst = xs + (size_t)j * nhk * kHPad;
@@ -148,17 +159,21 @@ __device__ __forceinline__ void stage_bf16_to_f16(__half* xs, const uint16_t* co
 #pragma unroll
       for (int u = 0; u < kStageBatch; ++u) {
         const int e = 2 * (i0 + u * blockDim.x);
-        if (e < K)
+        if (e < K) {
+          bad |= f16_out_of_range(bf16_lo(v[u]), bf16_hi(v[u]));
           *reinterpret_cast<__half2*>(dst + (e >> 5) * kHPad + (e & 31)) =
               __floats2half2_rn(bf16_lo(v[u]), bf16_hi(v[u]));
+        }
       }
     }
   }
+  return bad;
 }
 
-__device__ __forceinline__ void stage_f32_to_f16(__half* xs, const float* const* rows, int m,
+__device__ __forceinline__ bool stage_f32_to_f16(__half* xs, const float* const* rows, int m,
                                                  int K) {
   const int nhk = K / 32, n = K / 2;
+  bool bad = false;
   for (int j = 0; j < m; ++j) {
     const float2* src = reinterpret_cast<const float2*>(rows[j]);
     __half* dst = xs + (size_t)j * nhk * kHPad;
@@ -172,12 +187,15 @@ __device__ __forceinline__ void stage_f32_to_f16(__half* xs, const float* const*
 #pragma unroll
       for (int u = 0; u < kStageBatch; ++u) {
         const int e = 2 * (i0 + u * blockDim.x);
-        if (e < K)
+        if (e < K) {
+          bad |= f16_out_of_range(v[u].x, v[u].y);
           *reinterpret_cast<__half2*>(dst + (e >> 5) * kHPad + (e & 31)) =
               __floats2half2_rn(v[u].x, v[u].y);
+        }
       }
     }
   }
+  return bad;
 }
 
 // fp32 layout: row j, half-k-group hk at (j*nhk + hk)*kXPad floats
@@ -553,8 +571,8 @@ __global__ void __launch_bounds__(kDecThreads, MAXM == 1 ? 2 : 1) k_decode_gu(De
     const uint16_t* rows[2];
     for (int j = 0; j < mm; ++j) rows[j] = p.x + (size_t)(p.perm[q0 + j] / p.k) * p.H;
     __syncthreads();
-    stage_bf16_to_f16(xs, rows, mm, p.H);
-    __syncthreads();
+    const bool bad = stage_bf16_to_f16(xs, rows, mm, p.H);
+    if (__syncthreads_or(bad) && threadIdx.x == 0) set_status(p.status, MOE_ERR_UNSUPPORTED);
     if (MAXM == 2 && mm == 2) gu_routed_pass<MAXM>(p, L, rec, rt, m0, q0, mm, xs, gg, gu, first);
     else gu_routed_pass<1>(p, L, rec, rt, m0, q0, mm, xs, gg, gu, first);
   }
@@ -674,8 +692,8 @@ __device__ __forceinline__ void down_unit(const DecodeParams& p, unsigned char* 
     const float* rows[2];
     for (int j = 0; j < mm; ++j) rows[j] = p.h_route + (size_t)(q0 + j) * p.I;
     __syncthreads();
-    stage_f32_to_f16(hs, rows, mm, p.I);
-    __syncthreads();
+    const bool bad = stage_f32_to_f16(hs, rows, mm, p.I);
+    if (__syncthreads_or(bad) && threadIdx.x == 0) set_status(p.status, MOE_ERR_UNSUPPORTED);
     if (MAXM == 2 && mm == 2) down_routed_pass<MAXM>(p, L, rec, rt, q0, mm, hs, gd);
     else down_routed_pass<1>(p, L, rec, rt, q0, mm, hs, gd);
   }

@@ -8,8 +8,6 @@
 // memory, so the call itself allocates nothing (no cudaMalloc, no cudaFree, no
 // allocating library routine).  Every GPU that loads the library holds the
 // array (kNoAllocScratchBytes) until the process exits.
-#include <mutex>
-
 #include "common.cuh"
 
 // 8 MiB of fp32 scratch (MOE_NOALLOC_SCRATCH_BYTES in moe.h): enough for
@@ -19,30 +17,33 @@ constexpr size_t kNoAllocScratchBytes = MOE_NOALLOC_SCRATCH_BYTES;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 namespace {
-// Device address of g_noalloc_scratch per device ordinal.  In host code the
-// array's name is only a host-side stand-in, so the real address is taken
-// with cudaGetSymbolAddress, once per device, with that device current.
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void* g_scratch_addr[kMaxDevices];
-
+// Device address of g_noalloc_scratch on the current device.  In host code
+// the array's name is only a host-side stand-in, so the real address is
+// asked for with cudaGetSymbolAddress, with the device current.  It is asked
+// on every call (after the first it costs a driver lookup, no allocation),
+// so a device reset or another context never leaves a stale address behind.
 moe_status scratch_address(void** out) {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
-  if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch_addr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
-      cudaGetLastError();
-      return MOE_ERR_CUDA;
-    }
-    g_scratch_addr[dev] = p;
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
+    cudaGetLastError();
+    return MOE_ERR_CUDA;
   }
-  *out = g_scratch_addr[dev];
+  *out = p;
   return MOE_OK;
 }
 }  // namespace
+
+namespace moe {
+// Loads the array's module on the current device.  CUDA loads a module
+// lazily, on the first use of something in it, and loading it reserves the
+// array's device memory; the library's set-up (the first expcache_create,
+// moe_layer_create or FFN call of the process) calls this, so that on that
+// device the first moe_expert_ffn_noalloc allocates nothing either.
+moe_status noalloc_setup() {
+  void* p = nullptr;
+  return scratch_address(&p);
+}
+}  // namespace moe
 
 namespace moe {
 size_t decode_workspace_bytes(int T, int I, int k, int Is);

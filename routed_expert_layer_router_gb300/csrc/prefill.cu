@@ -1015,6 +1015,13 @@ size_t prefill_workspace_bytes(int T, int H, int I, int E, int k, int Is) {
   return pf::PrefillWs(T, H, I, E, k, Is).total;
 }
 
+// the fp32 h rows (one per padded route row, I values) inside a prefill
+// call's workspace
+const float* prefill_h_rows(const void* workspace, int T, int H, int I, int E, int k, int Is) {
+  const uint8_t* ws = (const uint8_t*)(((uintptr_t)workspace + 1023) & ~(uintptr_t)1023);
+  return (const float*)(ws + pf::PrefillWs(T, H, I, E, k, Is).h32);
+}
+
 moe_status prefill_setup() { return pf::load_encoder(); }
 
 moe_status prefill_ffn(const moe_ffn_args* a, cudaStream_t s) {

@@ -181,6 +181,23 @@ class MoELayer:
                 "src_slot": grab(p["src_slot"], self.E, torch.int32),
                 "n_act": grab(p["n_act"], 2, torch.int32)}
 
+    def debug_prefill(self, T: int) -> dict:
+        """After a forward on the PREFILL path: h of every route before its
+        NVFP4 quantisation, [T*k, I] fp32 in the permutation's order (row p is
+        the route at expert-sorted position p), plus offsets [E+1]."""
+        p = moe.moe_layer_debug_prefill(self.handle)
+        torch.cuda.synchronize()
+        E = self.E
+        off = device_view(p["offsets"], (E + 1,), torch.int32).clone()
+        pad = device_view(p["pad_offsets"], (E + 1,), torch.int32).clone()
+        rows = int(pad[-1].item())
+        h = device_view(p["h_rows"], (rows, self.I), torch.float32)
+        # padded row of sorted position q of expert e: pad[e] + q - off[e]
+        e_of = torch.repeat_interleave(torch.arange(E, device=off.device), (off[1:] - off[:-1]).long())
+        q = torch.arange(int(off[-1].item()), device=off.device)
+        idx = (pad[:-1].long()[e_of] + q - off[:-1].long()[e_of])
+        return {"h": h[idx].clone(), "offsets": off}
+
     def read_status(self, stream=None) -> int:
         return moe.moe_read_device_status(self.handle, _stream(stream))
 

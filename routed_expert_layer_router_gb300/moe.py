@@ -78,6 +78,7 @@ SIGNATURES = {
     "expcache_set_resident": (i32, [vp, i32, i32, i32, vp]),
     "expcache_fill": (i32, [vp, i32, vp, vp, i32, i32, vp, vp, vp]),
     "expcache_lookup": (i32, [vp, i32, vp, vp, vp, vp, vp, vp, vp, vp]),
+    "expcache_plan_slots": (i32, [vp, i32, i32, i32, i32, vp, vp, vp]),
     "expcache_set_policy": (i32, [vp, i32]),
     "expcache_policy_step": (i32, [vp, i32, vp, vp, vp, vp, vp, vp, vp, vp]),
     "expcache_policy_state": (i32, [vp, ctypes.POINTER(i32), vp, vp, vp, vp]),
@@ -90,6 +91,7 @@ SIGNATURES = {
     "moe_layer_destroy": (i32, [vp]),
     "moe_layer_forward": (i32, [vp, vp, i32, vp, vp]),
     "moe_layer_debug_ptrs": (i32, [vp, vp, vp, vp, vp, vp, vp]),
+    "moe_layer_debug_prefill": (i32, [vp, vp, vp, vp]),
     "moe_layer_set_timing": (i32, [vp, vp, i32]),
     "moe_read_device_status": (i32, [vp, vp, ctypes.POINTER(ctypes.c_int32)]),
 }
@@ -180,6 +182,12 @@ def expcache_lookup(cache, layer, counts, src_slot, act_list, n_act, miss_ids, n
                                                  miss_ids, n_miss, status or None, stream))
 
 
+def expcache_plan_slots(d_counts, L, E, total_slots, floor, d_layer_slots, d_order,
+                        stream: int = 0) -> None:
+    _ck("expcache_plan_slots", lib().expcache_plan_slots(d_counts, L, E, total_slots, floor,
+                                                         d_layer_slots, d_order, stream))
+
+
 def expcache_set_policy(cache, spares_per_layer: int) -> None:
     _ck("expcache_set_policy", lib().expcache_set_policy(cache, spares_per_layer))
 
@@ -249,6 +257,13 @@ def moe_layer_debug_ptrs(layer: int) -> dict:
     _ck("moe_layer_debug_ptrs",
         lib().moe_layer_debug_ptrs(layer, *[ctypes.byref(o) for o in outs]))
     return dict(zip(["ids", "w", "p_sel", "perm", "src_slot", "n_act"], [o.value for o in outs]))
+
+
+def moe_layer_debug_prefill(layer: int) -> dict:
+    outs = [vp() for _ in range(3)]
+    _ck("moe_layer_debug_prefill",
+        lib().moe_layer_debug_prefill(layer, *[ctypes.byref(o) for o in outs]))
+    return dict(zip(["h_rows", "offsets", "pad_offsets"], [o.value for o in outs]))
 
 
 def moe_layer_set_timing(layer: int, events: list) -> None:

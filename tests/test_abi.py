@@ -69,3 +69,8 @@ def test_argument_errors_return_before_touching_the_device(libmoe):
     assert L.expcache_create(ctypes.byref(d), ctypes.byref(h)) == moe.MOE_ERR_UNSUPPORTED
     assert L.moe_combine(None, None) == moe.MOE_ERR_INVALID_ARG
     assert L.moe_layer_forward(None, None, 1, None, None) == moe.MOE_ERR_INVALID_ARG
+    # slot planner: floors that do not fit, a floor above E, oversized shapes
+    assert L.expcache_plan_slots(16, 2, 4, 3, 2, 16, 16, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.expcache_plan_slots(16, 2, 4, 10, 5, 16, 16, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.expcache_plan_slots(None, 2, 4, 10, 1, 16, 16, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.expcache_plan_slots(16, 2, 2000, 10, 1, 16, 16, None) == moe.MOE_ERR_UNSUPPORTED

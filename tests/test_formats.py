@@ -121,32 +121,128 @@ def test_nvfp4_quant_zero_row():
     assert G == 1.0 and not codes.any() and not scales.any()
 
 
+def _blocks_sg(v):
+    """Per element: the dequantised block scale s*G of v's NVFP4 quantisation."""
+    codes, scales, G = oracle.nvfp4_quant(v)
+    return np.repeat([oracle.e4m3(int(b)) * G for b in scales], 16)
+
+
 def test_quant_flip_slack_covers_nearby_inputs():
-    """The rounding-boundary slack is zero away from boundaries and covers
-    every change of the quantised value that a relative perturbation of
-    5e-5 of one element can cause (the row amax element is left alone, so G
-    does not move)."""
+    """The NVFP4 rounding-boundary slack covers every change of the quantised
+    value that moving each element by up to half the code margin (in units of
+    its block scale) can cause; the row amax element is left alone, so G does
+    not move, and the block scales move by far less than their margin."""
     rng = np.random.default_rng(9)
-    for trial in range(40):
+    hits = 0
+    for trial in range(200):
         v = (rng.standard_normal(256) * rng.uniform(0.1, 10)).astype(np.float32)
         amax_i = int(np.argmax(np.abs(v)))
         codes, scales, G = oracle.nvfp4_quant(v)
         base = _dequant_row(codes, scales, G)
         delta = oracle.quant_flip_delta(v)
-        for rel in (5e-5, -5e-5):
-            vp = v.copy()
-            mask = np.ones(256, bool)
-            mask[amax_i] = False
-            vp[mask] = (vp[mask].astype(np.float64) * (1 + rel)).astype(np.float32)
+        sg = _blocks_sg(v)
+        # plant elements right next to E2M1 midpoints so that flips do happen
+        mids = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0])
+        for i in rng.choice(256, 24, replace=False):
+            if i != amax_i and abs(v[i]) < np.abs(v[(i // 16) * 16:(i // 16 + 1) * 16]).max():
+                q = rng.choice(mids) + rng.uniform(-0.3, 0.3) * oracle.FLIP_Q
+                v[i] = np.float32(np.sign(v[i]) * q * sg[i])
+        codes, scales, G = oracle.nvfp4_quant(v)
+        base = _dequant_row(codes, scales, G)
+        delta = oracle.quant_flip_delta(v)
+        sg = _blocks_sg(v)
+        for sign in (1.0, -1.0):
+            vp = v.astype(np.float64) + sign * 0.5 * oracle.FLIP_Q * sg * np.sign(v)
+            vp[amax_i] = v[amax_i]
+            vp = vp.astype(np.float32)
             c2, s2, G2 = oracle.nvfp4_quant(vp)
             assert G2 == G
             moved = np.abs(_dequant_row(c2, s2, G2) - base)
             assert np.all(moved <= delta + 1e-12)
-    # an element exactly on an E2M1 midpoint (1.25 of its block scale) is flagged
+            hits += int((moved > 0).sum())
+    assert hits > 100  # the planted elements did flip
+    # an element exactly on an E2M1 midpoint (1.25 of its block scale) is
+    # flagged with one code step; one at twice the margin from it is not
     v = np.zeros(16, np.float32)
     v[0] = 6.0
     v[1] = 1.25
+    v[2] = 1.25 + 2 * oracle.FLIP_Q
     d = oracle.quant_flip_delta(v)
     codes, scales, G = oracle.nvfp4_quant(v)
     s = oracle.e4m3(int(scales[0])) * G
-    assert d[1] == pytest.approx(0.5 * s) and d[2] == 0.0
+    assert d[1] == pytest.approx(0.5 * s) and d[2] == 0.0 and d[3] == 0.0
+
+
+def test_quant_flip_slack_of_block_scales():
+    """A block whose scale argument amax_b/(6G) sits on an E4M3 midpoint is
+    flagged on every element with 4 x the upper scale x G, and that covers the
+    requantisation under either neighbouring scale; a block whose argument is
+    clear of every midpoint carries no scale slack."""
+    rng = np.random.default_rng(21)
+    checked = 0
+    for c in range(9, 0x7E):  # normal E4M3 scales
+        s1, s2 = oracle.e4m3(c - 1), oracle.e4m3(c)
+        v = np.zeros(32, np.float32)
+        v[16] = 2688.0  # row amax: G = 1 exactly
+        v[17:32] = rng.uniform(-2688, 2688, 15)
+        blk = rng.uniform(-1, 1, 16) * 3 * (s1 + s2)
+        blk[0] = 3.0 * (s1 + s2)  # block amax on the midpoint: t = (s1 + s2) / 2
+        v[:16] = blk
+        if np.float32(v[0]) / np.float32(6.0) != np.float32(0.5 * (s1 + s2)):
+            continue  # midpoint not representable at this magnitude
+        d = oracle.quant_flip_delta(v)
+        assert np.all(d[:16] == 4 * s2), (c, d[:16])
+        # requantise the block under each neighbouring scale (nudging its max)
+        base = _dequant_row(*oracle.nvfp4_quant(v))
+        for nudge in (1 - 1e-6, 1 + 1e-6):
+            vp = v.copy()
+            vp[0] = np.float32(v[0] * nudge)
+            moved = np.abs(_dequant_row(*oracle.nvfp4_quant(vp)) - base)
+            assert np.all(moved[:16] <= d[:16])
+        checked += 1
+        # clear of the midpoint by 10x the margin: no scale slack in the block
+        vq = v.copy()
+        vq[0] = np.float32(v[0] * (1 + 10 * oracle.FLIP_T))
+        assert np.all(oracle.quant_flip_delta(vq)[:16] != 4 * s2)
+    assert checked > 60
+
+
+def test_bf16_flip_slack_pins():
+    """The bf16 rounding-boundary slack (the shared expert's h before its
+    bf16 down GEMM): one bf16 step exactly where a value sits within relative
+    FLIP_BF16 of a round-to-nearest-even midpoint, zero elsewhere.  Checked against
+    numpy's RNE rounding of perturbed values and against midpoints built bit
+    by bit."""
+    from tests.helpers import bf16_to_f64, f32_to_bf16
+    rng = np.random.default_rng(11)
+    v = rng.standard_normal(50000) * 10.0 ** rng.uniform(-4, 4, 50000)
+    d = oracle.bf16_flip_delta(v)
+
+    def rne(a):
+        return bf16_to_f64(f32_to_bf16(np.asarray(a, np.float64).astype(np.float32)))
+
+    base = rne(v)
+    # every change of the bf16 value that a relative perturbation of 5e-5 can
+    # cause is covered, and is exactly one bf16 step
+    for rel in (0.5 * oracle.FLIP_BF16, -0.5 * oracle.FLIP_BF16):
+        moved = np.abs(rne(v * (1 + rel)) - base)
+        assert np.all(moved <= d)
+        flipped = moved > 0
+        assert np.all(d[flipped] == moved[flipped])
+    # values further than twice the margin from every midpoint carry no slack
+    m = 2 * oracle.FLIP_BF16
+    far = np.abs(rne(v * (1 + m)) - rne(v * (1 - m))) == 0
+    assert far.sum() > 45000 and not d[far].any()
+    # exact midpoints between two adjacent bf16 values (both signs, across
+    # binades): flagged with the distance between the two
+    bits = rng.integers(0x0080, 0x7F7F, 2000).astype(np.uint16)
+    bits[:4] = [0x3F7F, 0x3F80, 0x0080, 0x7F7E]  # mantissa carry, 1.0, smallest normal, near max
+    lo = bf16_to_f64(bits)
+    hi = bf16_to_f64(bits + 1)
+    mid = 0.5 * (lo + hi)
+    for sgn in (1.0, -1.0):
+        assert np.array_equal(oracle.bf16_flip_delta(sgn * mid), hi - lo)
+        # a quarter step either side of the midpoint, and the grid values themselves
+        assert not oracle.bf16_flip_delta(sgn * (0.75 * lo + 0.25 * hi)).any()
+        assert not oracle.bf16_flip_delta(sgn * (0.25 * lo + 0.75 * hi)).any()
+        assert not oracle.bf16_flip_delta(sgn * lo).any()

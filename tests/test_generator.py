@@ -25,7 +25,11 @@ def test_splitmix64_published_vector():
 def test_record_sizes_golden():
     for H, I, n in _golden("record_sizes.txt"):
         assert gen.record_bytes(int(H), int(I)) == int(n)
-        assert gen._lib_host().gen_record_size(int(H), int(I)) == int(n)
+        assert gen._lib_host().gen_record_size(int(H), int(I), gen.NVFP4) == int(n)
+        # MXFP4: the same codes, one E8M0 byte per 32 values instead of an E4M3 per 16
+        mx = int(n) - 3 * int(H) * int(I) // 32
+        assert gen.record_bytes(int(H), int(I), gen.MXFP4) == mx
+        assert gen._lib_host().gen_record_size(int(H), int(I), gen.MXFP4) == mx
 
 
 def test_activation_and_router_moments():

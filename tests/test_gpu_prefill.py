@@ -1,13 +1,21 @@
 """GPU parity of the prefill path (NVFP4 activation quantisation + tcgen05
-grouped GEMMs) against the oracle's prefill numerics: identity expert exact,
-a small layer on every token, the 4096-token layer on sampled tokens."""
+grouped GEMMs) against the oracle's prefill numerics: the identity expert
+exact; a small layer on every token; the 4096-token layer's router outputs
+on every token and its outputs on 64 tokens spread over every expert group;
+the masked prefill (experts the chunk does not route to are skipped) at 8,
+20 and 47 tokens.  The gate/up GEMM's h is compared with the oracle's h
+before its re-quantisation.  Output comparisons keep the tokens whose routes'
+h is clear of every NVFP4 rounding boundary by the oracle's margin
+(prefill_clean), as the router comparisons keep tokens clear of near-ties."""
 import numpy as np
 import pytest
 import torch
 
 import gen
-from tests.gpu_common import (check_outputs, check_router, draw_tokens, host_inputs,
-                              oracle_layer, to_dev_bf16, y_to_f64)
+import oracle
+from tests.gpu_common import (check_outputs, check_permutation, check_prefill_h, check_router,
+                              draw_prefill_tokens, draw_tokens, host_inputs, oracle_layer,
+                              prefill_clean, to_dev_bf16, y_to_f64)
 from tests.helpers import identity_record, nvfp4_exact_x
 
 pytestmark = pytest.mark.gpu
@@ -59,38 +67,96 @@ def test_prefill_small_layer_parity():
     import gen.device as gd
     dw = gd.build(SMALL, T_max=SMALL.T)
     try:
-        Wr, bias, sh = host_inputs(dw, 0)
-        x, _ = draw_tokens(SMALL, 0, SMALL.T, Wr, bias)
-        y = dw.moe_layers[0].forward(to_dev_bf16(x))
+        x = draw_prefill_tokens(dw, 0, SMALL.T)
+        layer = dw.moe_layers[0]
+        y = layer.forward(to_dev_bf16(x))
         torch.cuda.synchronize()
-        assert dw.moe_layers[0].read_status() == 0
+        assert layer.read_status() == 0
         y_ref, ids, w, p, bound = oracle_layer(dw, 0, x, mode=1, return_bound=True)
-        check_router(dw.moe_layers[0].debug(SMALL.T), ids, w, p)
+        dbg = layer.debug(SMALL.T)
+        check_router(dbg, ids, w, p)
+        check_permutation(dbg, ids)
+        check_prefill_h(dw, 0, x, layer.debug_prefill(SMALL.T)["h"].cpu().numpy(),
+                        dbg["perm"].cpu().numpy(), list(range(0, SMALL.T, 7)))
         check_outputs(y_to_f64(y), y_ref, bound=bound)
     finally:
         dw.close()
 
 
-def test_prefill_4096_tokens_sampled_parity():
-    """The 4096-token prefill layer (288 experts top-8, all resident, groups of
-    64) in the launch configuration the bench times; the oracle recomputes
-    eight sampled tokens."""
+def test_prefill_4096_tokens_parity():
+    """The 4096-token prefill layer (288 experts top-8, all resident) in the
+    launch configuration the bench times: ids, weights and probabilities of
+    all 4096 tokens and the permutation against the oracle's router; outputs
+    of 64 tokens spread over the chunk whose routes reach every group of 64
+    experts (the order the GEMMs walk them), and the h of 8 of them."""
     import gen.device as gd
     wl = gen.WORKLOADS["prefill"]
     dw = gd.build(wl, T_max=wl.T)
     try:
         Wr, bias, sh = host_inputs(dw, 0)
         x, _ = draw_tokens(wl, 0, wl.T, Wr, bias, batch=512)
-        y = dw.moe_layers[0].forward(to_dev_bf16(x))
+        layer = dw.moe_layers[0]
+        y = layer.forward(to_dev_bf16(x))
         torch.cuda.synchronize()
-        assert dw.moe_layers[0].read_status() == 0
-        dbg = dw.moe_layers[0].debug(wl.T)
-        ids = dbg["ids"].cpu().numpy()
-        assert len(np.unique(ids)) == wl.E  # every expert is hit
-        sample = [0, 1, 511, 1024, 2047, 2500, 4000, 4095]
-        y_ref, ids_r, w_r, p_r, bound = oracle_layer(dw, 0, x[sample], mode=1, return_bound=True)
-        check_router({kk: (v[sample] if kk in ("ids", "w", "p_sel") else v) for kk, v in dbg.items()},
-                     ids_r, w_r, p_r)
+        assert layer.read_status() == 0
+        dbg = layer.debug(wl.T)
+        ids_r, w_r, p_r, _, _ = oracle.route(x, Wr, bias, wl.k)
+        check_router(dbg, ids_r, w_r, p_r)
+        check_permutation(dbg, ids_r)
+        assert len(np.unique(ids_r)) == wl.E  # every expert is hit
+        # 64 clean tokens, taken in a stride over the chunk
+        order = (np.arange(wl.T) * 1031) % wl.T
+        sample = []
+        for i0 in range(0, wl.T, 48):
+            cand = order[i0:i0 + 48]
+            ok = prefill_clean(dw, 0, x[cand], ids_r[cand])
+            sample += [int(t) for t in cand[ok]]
+            if len(sample) >= 64:
+                break
+        sample = sorted(sample[:64])
+        assert len(sample) == 64
+        assert set(ids_r[sample].ravel() // 64) == set(range((wl.E + 63) // 64))
+        y_ref, ids_s, w_s, p_s, bound = oracle_layer(dw, 0, x[sample], mode=1, return_bound=True)
+        assert np.array_equal(ids_s, ids_r[sample])
         check_outputs(y_to_f64(y)[sample], y_ref, bound=bound)
+        check_prefill_h(dw, 0, x, layer.debug_prefill(wl.T)["h"].cpu().numpy(),
+                        dbg["perm"].cpu().numpy(), sample[::8])
+    finally:
+        dw.close()
+
+
+_POOL = {}
+
+
+@pytest.mark.parametrize("group", [0, 64])
+def test_masked_prefill_parity(group):
+    """The masked grouped prefill (the tile plan walks only the experts the
+    chunk routes to) on the 6144 x 2048, 288-expert layer switched to the
+    prefill path from 8 tokens: at 8, 20 and 47 tokens most experts are
+    unused.  Router, permutation, h and every output against the oracle."""
+    import gen.device as gd
+    wl = gen.WORKLOADS["decode"]
+    dw = gd.build(wl, T_max=47, prefill_min_tokens=8, prefill_group=group)
+    try:
+        layer = dw.moe_layers[0]
+        if "decode" not in _POOL:  # the same tokens for both groupings
+            _POOL["decode"] = draw_prefill_tokens(dw, 0, 8 + 20 + 47, draw0=5000)
+        pool = _POOL["decode"]
+        i0 = 0
+        for T in (8, 20, 47):
+            x = pool[i0:i0 + T]
+            i0 += T
+            y = layer.forward(to_dev_bf16(x))
+            torch.cuda.synchronize()
+            assert layer.read_status() == 0
+            dbg = layer.debug(T)
+            y_ref, ids, w, p, bound = oracle_layer(dw, 0, x, mode=1, return_bound=True)
+            check_router(dbg, ids, w, p)
+            check_permutation(dbg, ids)
+            n_act = int(dbg["n_act"][0])
+            assert n_act == len(np.unique(ids)) < wl.E  # experts left out
+            check_prefill_h(dw, 0, x, layer.debug_prefill(T)["h"].cpu().numpy(),
+                            dbg["perm"].cpu().numpy(), [0, T - 1])
+            check_outputs(y_to_f64(y), y_ref, bound=bound)
     finally:
         dw.close()
