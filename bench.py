@@ -265,16 +265,16 @@ class ExplicitLayer:
         """Kernels one decode moe_layer_forward launches for this layer and T:
         router + permutation + slot lookup (one kernel for T <= 8, else the
         router GEMM, top-k and the permutation), per expert group the gather
-        (if staging) and the two FFN kernels, and the combine unless a single
-        group's down kernel writes y."""
+        (if staging) and the one-launch FFN, and the combine unless a single
+        group's FFN writes y."""
         S = self.dw.cache.n_stage
         route = 1 if self.T <= 8 else 3
-        return route + self.groups * (2 + (1 if S > 0 else 0)) + (0 if self.groups == 1 else 1)
+        return route + self.groups * (1 + (1 if S > 0 else 0)) + (0 if self.groups == 1 else 1)
 
 
 # --------------------------------------------------------------- decode
-def bench_decode(args, torch, moe, gen, gd, dev, rank, world, local_rank, peaks):
-    wl = gen.WORKLOADS["decode"]
+def bench_decode(args, torch, moe, gen, gd, dev, rank, world, local_rank, peaks, wl=None):
+    wl = wl or gen.WORKLOADS["decode"]
     H, I, E, k, Is = wl.H, wl.I, wl.E, wl.k, wl.Is
     T = 1
     # --small: the same layer with only 16 distinct expert records (expert e
@@ -331,23 +331,23 @@ def bench_decode(args, torch, moe, gen, gd, dev, rank, world, local_rank, peaks)
 
     # ---- pass 2: events at the layer's own launch boundaries (its timing hook),
     # eager launches, one step at a time: router kernel (with the permutation,
-    # lookup and the shared expert's gate/up), gate/up kernel (routed, with the
-    # shared expert's down), down kernel (routed, with the combine)
-    hev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    # lookup and the shared expert's gate/up), then the one-launch FFN (routed
+    # gate/up and down, the shared expert's down, the combine)
+    hev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
     for e in hev:  # torch creates the CUDA event on its first record
         e.record(stream)
     torch.cuda.synchronize()
     moe.moe_layer_set_timing(layer.handle, [e.cuda_event for e in hev])
-    k_ms = [[], [], []]
+    k_ms = [[], []]
     for j in range(args.steps):
         flush()
         layer.forward(xs[args.warmup + j:args.warmup + j + 1],
                       ys[args.warmup + j:args.warmup + j + 1], stream=stream)
-        hev[3].synchronize()
-        for i in range(3):
+        hev[2].synchronize()
+        for i in range(2):
             k_ms[i].append(hev[i].elapsed_time(hev[i + 1]))
     moe.moe_layer_set_timing(layer.handle, [])
-    rt_ms, gu_ms, dn_ms = (statistics.mean(v) for v in k_ms)
+    rt_ms, ffn_ms = (statistics.mean(v) for v in k_ms)
     assert layer.read_status() == 0, "device status set during the bench"
 
     # ---- e2e: the public call with host buffers
@@ -380,37 +380,35 @@ def bench_decode(args, torch, moe, gen, gd, dev, rank, world, local_rank, peaks)
     if world > 1:
         torch.distributed.all_reduce(tot, op=torch.distributed.ReduceOp.MAX)
     total_ms = float(tot.item())
-    rb = gen.record_bytes(H, I)
-    # algorithmic bytes of the three kernels of the one-token sequence
+    rb = gen.record_bytes(H, I, wl.fmt)
+    # algorithmic bytes of the two kernels of the one-token sequence: the router
+    # kernel (router weights, the shared expert's gate/up, x, h_shared, logits)
+    # and the FFN (k whole records, the shared down, x, h written and read,
+    # the routes' and shared outputs written and read by the combine, y)
     rt_bytes = E * H * 4 + 2 * Is * H * 2 + T * H * 2 + T * Is * 4 + T * E * 4
-    gu_bytes = (k * (2 * I * H // 2 + 2 * I * H // 16) + H * Is * 2 + T * H * 2
-                + T * k * I * 4 + T * Is * 4 + T * H * 4)
-    dn_bytes = (k * (H * I // 2 + H * I // 16) + T * k * I * 4 + (T * k + T) * H * 4 * 2
-                + T * H * 2)
+    ffn_bytes = (k * rb + H * Is * 2 + T * H * 2 + 2 * T * k * I * 4 + T * Is * 4
+                 + 2 * (T * k + T) * H * 4 + T * H * 2)
     step_bytes = k * rb + 3 * Is * H * 2 + E * H * 4 + 2 * T * H * 2
     rt_gbs = rt_bytes / (rt_ms * 1e-3) / 1e9
-    gu_gbs = gu_bytes / (gu_ms * 1e-3) / 1e9
-    dn_gbs = dn_bytes / (dn_ms * 1e-3) / 1e9
+    ffn_gbs = ffn_bytes / (ffn_ms * 1e-3) / 1e9
     hbm = peaks["hbm_gbs"]
     res = {
         "value": round(world * args.steps * T / (total_ms * 1e-3), 2),
         "ms_per_step": round(total_ms / args.steps, 5),
         "roofline": {"bound": "hbm",
-                     "kernel": "k_decode_gu as the layer launches it for one token (routed "
-                               "NVFP4 gate/up of the 8 experts, SiLU*mul, + the bf16 shared "
-                               "expert's down)",
-                     "achieved": round(gu_gbs, 1), "peak": hbm, "unit": "GB/s",
-                     "frac": round(gu_gbs / hbm, 4), "traffic": GU_TRAFFIC,
+                     "kernel": "k_decode_ffn as the layer launches it for one token (routed "
+                               "NVFP4 gate/up, SiLU*mul and down of the 8 experts, the bf16 "
+                               "shared expert's down, the weighted combine)",
+                     "achieved": round(ffn_gbs, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(ffn_gbs / hbm, 4), "traffic": GU_TRAFFIC,
                      "traffic_source": GU_TRAFFIC_SOURCE,
-                     "bytes_per_launch": gu_bytes, "avg_launch_ms": round(gu_ms, 5)},
+                     "bytes_per_launch": ffn_bytes, "avg_launch_ms": round(ffn_ms, 5)},
         "kernels": {
             "k_route_permute_small": {"ms": round(rt_ms, 5), "GB/s": round(rt_gbs, 1),
                                       "frac_hbm": round(rt_gbs / hbm, 4),
                                       "bytes": rt_bytes},
-            "k_decode_gu": {"ms": round(gu_ms, 5), "GB/s": round(gu_gbs, 1),
-                            "frac_hbm": round(gu_gbs / hbm, 4), "bytes": gu_bytes},
-            "k_decode_down": {"ms": round(dn_ms, 5), "GB/s": round(dn_gbs, 1),
-                              "frac_hbm": round(dn_gbs / hbm, 4), "bytes": dn_bytes},
+            "k_decode_ffn": {"ms": round(ffn_ms, 5), "GB/s": round(ffn_gbs, 1),
+                             "frac_hbm": round(ffn_gbs / hbm, 4), "bytes": ffn_bytes},
             "timing": "the layer's timing hook: events at its launch boundaries, eager "
                       "launches, L2 flushed before each step",
             "step_bytes": step_bytes,
@@ -428,9 +426,34 @@ def bench_decode(args, torch, moe, gen, gd, dev, rank, world, local_rank, peaks)
 
 
 # --------------------------------------------------------------- prefill
-def bench_prefill(args, torch, moe, gen, gd, dev, peaks, group=None):
-    wl = gen.WORKLOADS["prefill"]
-    if args.prefill_experts > 0:
+def _mx(gen, name):
+    """The workload with MXFP4 records (own seed)."""
+    import dataclasses
+    wl = gen.WORKLOADS[name]
+    return dataclasses.replace(wl, name=name + "-mx", fmt=gen.MXFP4, seed=wl.seed + 100)
+
+
+PREFILL_GEMM_LABEL = ("supplementary, the routed FP4 GEMMs above the HBM ridge: 64 experts "
+                      "(H=6144, I=2048, NVFP4, all resident), 8192 tokens top-8, 1024 routes per "
+                      "expert, no shared expert")
+PREFILL_MX_LABEL = ("prefill MoE layer with MXFP4 records (E8M0 scale per 32; MXFP4 "
+                    "activations): 4096 tokens, H=6144, I=2048, 288 experts top-8, bf16 shared "
+                    "expert, all resident, one launch per GEMM")
+
+
+def _prefill_gemm_wl():
+    import gen
+    return gen.Workload("prefill-gemm", H=6144, I=2048, E=64, k=8, T=8192, layers=1, Is=0,
+                        seed=6, prefill=True, group=0)
+
+
+PREFILL_GEMM_WL = None
+
+
+def bench_prefill(args, torch, moe, gen, gd, dev, peaks, group=None, wl=None, label=None):
+    custom = wl is not None
+    wl = wl if custom else gen.WORKLOADS["prefill"]
+    if args.prefill_experts > 0 and not custom:
         # profiler captures only: fewer experts and proportionally fewer tokens,
         # the same tokens per expert (tile shapes) and kernels
         E2 = args.prefill_experts
@@ -484,16 +507,59 @@ def bench_prefill(args, torch, moe, gen, gd, dev, peaks, group=None):
         b.record(stream)
         b.synchronize()
         e2e.append(a.elapsed_time(b))
-    rb = gen.record_bytes(H, I)
+    # per-kernel pass: the layer's timing hook marks every kernel of the step
+    # (router, permutation, token quantisation, tile tables, per launch group
+    # the gate/up GEMM, h quantisation and down GEMM, the shared expert's two
+    # GEMMs, the combine); L2 flushed before each step
+    n_lg = (-(-min(T * k, E) // dw_group)) if dw_group else 1
+    names = (["router", "permute", "quant_tokens", "tile_plan"]
+             + [n for _ in range(n_lg) for n in ("gemm_gate_up", "quant_h", "gemm_down")]
+             + (["gemm_shared_gate_up", "gemm_shared_down"] if Is else []) + ["combine"])
+    hev = [torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
+    for e in hev:
+        e.record(stream)
+    torch.cuda.synchronize()
+    moe.moe_layer_set_timing(layer.handle, [e.cuda_event for e in hev])
+    kt = {}
+    n_hook = min(steps, 5)
+    for j in range(n_hook):
+        flush()
+        layer.forward(xs[args.warmup + j], y)
+        hev[-1].synchronize()
+        for i, nm in enumerate(names):
+            kt[nm] = kt.get(nm, 0.0) + hev[i].elapsed_time(hev[i + 1]) / n_hook
+    moe.moe_layer_set_timing(layer.handle, [])
+    assert layer.read_status() == 0
+    rb = gen.record_bytes(H, I, wl.fmt)
     weight_bytes = E * rb + 3 * Is * H * 2 + E * H * 4
     flops_fp4 = 2.0 * T * k * (2 * I * H + H * I)
     flops_bf16 = 2.0 * T * 3 * Is * H
     gbs = (weight_bytes + 2 * T * H * 2) / (ms * 1e-3) / 1e9
     fp4_peak = peaks["bf16_tflops"] * FP4_OVER_BF16
+    # the routed GEMMs alone: FP4 tensor rate, and the weights (+ activation
+    # codes and scales) they read against the HBM peak
+    blk = 32 if wl.fmt == gen.MXFP4 else 16
+    gu_ms, dn_ms = kt["gemm_gate_up"], kt["gemm_down"]
+    R = T * k
+    gu_bytes = E * (2 * I * H // 2 + 2 * I * H // blk) + R * (H // 2 + H // 16)
+    dn_bytes = E * (H * I // 2 + H * I // blk) + R * (I // 2 + I // 16)
+    gemm = {
+        "gate_up": {"ms": round(gu_ms, 4),
+                    "fp4_tflops": round(2.0 * R * 2 * I * H / (gu_ms * 1e-3) / 1e12, 1),
+                    "frac_fp4": round(2.0 * R * 2 * I * H / (gu_ms * 1e-3) / 1e12 / fp4_peak, 4),
+                    "frac_hbm": round(gu_bytes / (gu_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)},
+        "down": {"ms": round(dn_ms, 4),
+                 "fp4_tflops": round(2.0 * R * H * I / (dn_ms * 1e-3) / 1e12, 1),
+                 "frac_fp4": round(2.0 * R * H * I / (dn_ms * 1e-3) / 1e12 / fp4_peak, 4),
+                 "frac_hbm": round(dn_bytes / (dn_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)},
+        "routes_per_expert": round(R / E, 1),
+        "timing": "the layer's timing hook: events around each kernel, L2 flushed before each "
+                  f"step, mean of {n_hook} steps"}
     res = {
-        "workload": "prefill MoE layer: 4096 tokens, H=6144, I=2048, 288 experts top-8, bf16 "
-                    "shared expert, all experts resident, experts walked in act_list order in "
-                    + (f"launch groups of {dw_group}" if dw_group else "one launch per GEMM"),
+        "workload": label or (
+            "prefill MoE layer: 4096 tokens, H=6144, I=2048, 288 experts top-8, bf16 "
+            "shared expert, all experts resident, experts walked in act_list order in "
+            + (f"launch groups of {dw_group}" if dw_group else "one launch per GEMM")),
         "value": round(T / (ms * 1e-3), 1), "unit": UNIT, "ms_per_step": round(ms, 4),
         "roofline": {
             "bound": "hbm", "unit": "GB/s",
@@ -510,8 +576,117 @@ def bench_prefill(args, torch, moe, gen, gd, dev, peaks, group=None):
                        "shared_bf16_tflop_per_step": round(flops_bf16 / 1e12, 3)},
         "e2e": {"value": round(T / (statistics.mean(e2e) * 1e-3), 1), "unit": UNIT,
                 "h2d_bytes_per_step": T * H * 2, "d2h_bytes_per_step": T * H * 2},
+        "kernels_ms": {nm: round(v, 4) for nm, v in kt.items()},
+        "routed_gemms": gemm,
         "clocks": clk,
     }
+    dw.close()
+    return res
+
+
+# ------------------------------------------------- slot budgets (Maya page)
+def bench_stack_budget(args, torch, moe, gen, gd, dev, link_gbs, calib_tokens=512, floor=33):
+    """The 16-layer stack with per-layer slot budgets from the library's planner
+    (expcache_plan_slots): every layer's route counts over a separate seeded
+    calibration batch (the library's router on the device), the same total
+    HBM slots as 66 per layer, a floor of 33; then the stack pass on fresh
+    tokens (hit rate and tok/s beside the fixed 66 per layer)."""
+    wl = gen.WORKLOADS["stack"]
+    L = wl.layers if args.layers <= 0 else min(args.layers, wl.layers)
+    E, H, k = wl.E, wl.H, wl.k
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+    counts = torch.zeros((L, E), dtype=torch.int32, device=dev)
+    x = torch.empty((calib_tokens, H), dtype=torch.bfloat16, device=dev)
+    wr = torch.empty((E, H), dtype=torch.float32, device=dev)
+    ids = torch.empty((calib_tokens, k), dtype=torch.int32, device=dev)
+    w = torch.empty((calib_tokens, k), dtype=torch.float32, device=dev)
+    lg = torch.empty((calib_tokens, E), dtype=torch.float32, device=dev)
+    for l in range(L):
+        gen.dev_router_f32(wl.seed, l, E, H, wr.data_ptr(), sp)
+        gen.dev_x_bf16(wl.seed, l, 9_000_000, calib_tokens, H, x.data_ptr(), sp)
+        b, _ = gen.zipf_bias(wl.seed, l, E, wl.zipf_alpha)
+        bd = torch.from_numpy(b).to(dev)
+        ra = moe.moe_route_args()
+        ra.x, ra.w_router, ra.bias = x.data_ptr(), wr.data_ptr(), bd.data_ptr()
+        ra.T, ra.H, ra.E, ra.k = calib_tokens, H, E, k
+        ra.ids, ra.w, ra.p_sel, ra.logits = ids.data_ptr(), w.data_ptr(), None, lg.data_ptr()
+        moe.moe_route(ra, sp)
+        counts[l] = torch.bincount(ids.flatten().long(), minlength=E).int()
+    ls = torch.zeros(L + 1, dtype=torch.int32, device=dev)
+    order = torch.zeros((L, E), dtype=torch.int32, device=dev)
+    total = L * wl.hot
+    moe.expcache_plan_slots(counts.data_ptr(), L, E, total, floor, ls.data_ptr(),
+                            order.data_ptr(), sp)
+    torch.cuda.synchronize()
+    n = (ls[1:] - ls[:-1]).tolist()
+    resident = [order[l, :n[l]].tolist() for l in range(L)]
+    res = bench_multilayer(args, torch, moe, gen, gd, dev, "stack", link_gbs, resident=resident)
+    res["workload"] = (f"{L} decode layers, 1 token per step, per-layer Zipf bias, "
+                       f"{total} HBM slots split by the greedy per-layer budget (floor {floor}) "
+                       f"from {calib_tokens} calibration tokens per layer, misses gathered from "
+                       "pinned host memory")
+    res["slots_per_layer"] = n
+    return res
+
+
+# ------------------------------------------- prefill over a partly cached layer
+def bench_prefill_streamed(args, torch, moe, gen, gd, dev, peaks, link_gbs, resident_ms=None):
+    """4096-token prefill of the stack's layer (66 hot experts in HBM, the
+    other 222 in pinned host memory), the misses gathered on the layer's
+    second stream into the two halves of a 64-slot staging ring while the
+    GEMMs run: tok/s, the gathered bytes against the measured host link, and
+    the time saved against running the gather and the all-resident step one
+    after the other."""
+    wl = gen.WORKLOADS["stack"]
+    T, H, I, k = 4096, wl.H, wl.I, wl.k
+    dw = gd.build(wl, layers=1, T_max=T, n_stage=64, prefill_min_tokens=8, prefill_group=0)
+    layer = dw.moe_layers[0]
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+    steps = max(3, args.prefill_steps // 2)
+    n = args.warmup + steps
+    xs = torch.empty((n, T, H), dtype=torch.bfloat16, device=dev)
+    for i in range(n):
+        gen.dev_x_bf16(wl.seed, 0, 7_000_000 + i * T, T, H, xs[i].data_ptr(), sp)
+    y = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    flush = L2Flush(torch, args.flush_mb, dev)
+    for i in range(args.warmup):
+        layer.forward(xs[i], y)
+    ev = _events(torch, steps)
+    from routed_expert_layer_router_gb300.layer import device_view
+    nact = moe.moe_layer_debug_ptrs(layer.handle)["n_act"]
+    miss = 0
+    torch.cuda.synchronize()
+    for j in range(steps):
+        flush()
+        ev[j][0].record(stream)
+        layer.forward(xs[args.warmup + j], y)
+        ev[j][1].record(stream)
+        ev[j][1].synchronize()
+        na, nh = device_view(nact, (2,), torch.int32).tolist()
+        miss += na - nh
+    assert layer.read_status() == 0
+    ms = sum(a.elapsed_time(b) for a, b in ev) / steps
+    rb = gen.record_bytes(H, I)
+    gbytes = miss / steps * rb
+    res = {
+        "workload": "prefill of the stack's layer: 4096 tokens, 66 hot experts of 288 in HBM, "
+                    "the misses gathered from pinned host memory through a 64-slot staging "
+                    "ring (2 x 32) on a second stream while the tensor-core GEMMs run",
+        "value": round(T / (ms * 1e-3), 1), "unit": UNIT, "ms_per_step": round(ms, 3),
+        "misses_per_step": round(miss / steps, 1),
+        "roofline": {"bound": "link", "achieved": round(gbytes / (ms * 1e-3) / 1e9, 1),
+                     "peak": round(link_gbs, 1), "unit": "GB/s",
+                     "frac": round(gbytes / (ms * 1e-3) / 1e9 / link_gbs, 4),
+                     "bytes_per_step": int(gbytes),
+                     "peak_source": "measured pinned host->device cudaMemcpyAsync (1 GiB)"},
+    }
+    if resident_ms:
+        serial = gbytes / (link_gbs * 1e9) * 1e3 + resident_ms
+        res["overlap"] = {"gather_at_link_ms": round(gbytes / (link_gbs * 1e9) * 1e3, 3),
+                          "all_resident_step_ms": round(resident_ms, 3),
+                          "saved_ms_vs_one_after_the_other": round(serial - ms, 3)}
     dw.close()
     return res
 
@@ -612,7 +787,10 @@ def _skip_error(torch, dw, xs, i0, n, L, T):
                                "forwards": len(errs)}}
 
 
-def bench_multilayer(args, torch, moe, gen, gd, dev, name, link_gbs, spares=0, skip_tau=0.0):
+def bench_multilayer(args, torch, moe, gen, gd, dev, name, link_gbs, spares=0, skip_tau=0.0,
+                     resident=None):
+    """resident (per layer): the experts each layer caches, instead of the
+    workload's rule (its slot run is sized to them)."""
     wl = gen.WORKLOADS[name]
     L = wl.layers if args.layers <= 0 else min(args.layers, wl.layers)
     T = wl.T
@@ -622,7 +800,8 @@ def bench_multilayer(args, torch, moe, gen, gd, dev, name, link_gbs, spares=0, s
     # the bytes each miss moves over the link are the same)
     # spares > 0: the adaptive cache, its spare slots taken from the hot budget
     dw = gd.build(wl, layers=L, T_max=T, saliency_order=order, n_stage=n_stage,
-                  alias_host_records=True, spares=spares, skip_tau=skip_tau)
+                  alias_host_records=True, spares=spares, skip_tau=skip_tau,
+                  resident=None if resident is None else resident[:L])
     stream = torch.cuda.current_stream()
     sp = stream.cuda_stream
     steps = args.stack_steps
@@ -652,13 +831,16 @@ def bench_multilayer(args, torch, moe, gen, gd, dev, name, link_gbs, spares=0, s
         prewarm(torch, lambda: [fwd(i) for i in range(args.warmup)], args.prewarm_s)
     ev = _events(torch, steps)
     torch.cuda.synchronize()
+    host_ms = []
     for j in range(steps):
         flush()
+        t_h = time.perf_counter()
         ev[j][0].record(stream)
         fwd(n_warm + j)
         ev[j][1].record(stream)
         # a decode step ends on the host (the next token depends on this one)
         ev[j][1].synchronize()
+        host_ms.append((time.perf_counter() - t_h) * 1e3)
     torch.cuda.synchronize()
     # median over the steps (and p10 / p90 beside it): a few steps of a fresh
     # stream can take several times the rest
@@ -676,7 +858,10 @@ def bench_multilayer(args, torch, moe, gen, gd, dev, name, link_gbs, spares=0, s
     # marks before the first group: start, router (+ permutation), and the
     # adaptive cache's step when it is a kernel of its own (more than 8 tokens)
     first = (2 if T <= 8 else 3) + (1 if spares > 0 and T > 8 else 0)
-    marks = first + groups * (3 if S > 0 else 2) + (1 if groups > 1 else 0)
+    # one staging group: the FFN kernel gathers the misses itself (one mark);
+    # else per group a gather and the FFN, then the combine
+    ffn_gathers = S > 0 and groups == 1
+    marks = first + (1 if ffn_gathers else groups * (2 if S > 0 else 1)) + (1 if groups > 1 else 0)
     hev = [[torch.cuda.Event(enable_timing=True) for _ in range(marks)] for _ in range(L)]
     for e in (e for row in hev for e in row):  # torch creates the CUDA event on its first record
         e.record(stream)
@@ -688,17 +873,25 @@ def bench_multilayer(args, torch, moe, gen, gd, dev, name, link_gbs, spares=0, s
     fill_ms, miss, act = 0.0, 0, 0
     part_ms = [0.0] * (marks - 1)  # per interval between marks, summed over layers and steps
     hook_ms = 0.0                  # whole steps of this pass
+    pev = _events(torch, steps)
+    pass_ms = []
     for j in range(steps if S > 0 else 0):
         flush()
+        pev[j][0].record(stream)
         fwd(g0 + j)
+        pev[j][1].record(stream)
         torch.cuda.synchronize()
-        hook_ms += hev[0][0].elapsed_time(hev[L - 1][marks - 1])
+        pass_ms.append(pev[j][0].elapsed_time(pev[j][1]))
+        hook_ms += pass_ms[-1]
         for l in range(L):
             for i in range(1, marks):
                 part_ms[i - 1] += hev[l][i - 1].elapsed_time(hev[l][i])
-            for g in range(groups):
-                i = first + g * 3
-                fill_ms += hev[l][i - 1].elapsed_time(hev[l][i])
+            if ffn_gathers:  # the FFN launch that moves the misses
+                fill_ms += hev[l][first - 1].elapsed_time(hev[l][first])
+            else:
+                for g in range(groups):
+                    i = first + g * 2
+                    fill_ms += hev[l][i - 1].elapsed_time(hev[l][i])
         for l in range(L):
             # n_act of the layer's last forward: [active, hits]
             na, nh = (int(v) for v in device_view(nact[l], (2,), torch.int32).tolist())
@@ -727,10 +920,14 @@ def bench_multilayer(args, torch, moe, gen, gd, dev, name, link_gbs, spares=0, s
         "value": round(T / (ms * 1e-3), 2), "unit": UNIT + " (whole stack)",
         "ms_per_step": round(ms, 4),
         "ms_per_step_p10_p90": [round(p10, 4), round(p90, 4)],
+        "host_ms_per_step_median": round(statistics.median(host_ms), 4),
         "per_layer_tokens_s": round(T * L / (ms * 1e-3), 1),
         "hit_rate": round(1 - miss / max(act, 1), 4),
         "misses_per_layer_step": round(miss / (steps * L), 2),
-        "roofline": {"bound": "link", "kernel": "k_gather (expcache_fill)",
+        "roofline": {"bound": "link",
+                     "kernel": ("k_decode_ffn with the misses' gather inside (bytes gathered / "
+                                "the whole launch: a lower bound of the link rate)"
+                                if ffn_gathers else "k_gather (expcache_fill)"),
                      "achieved": round(gather_gbs, 1), "peak": round(link_gbs, 1),
                      "unit": "GB/s", "frac": round(gather_gbs / link_gbs, 4) if link_gbs else None,
                      "peak_source": "measured pinned host->device cudaMemcpyAsync (1 GiB)"},
@@ -741,18 +938,20 @@ def bench_multilayer(args, torch, moe, gen, gd, dev, name, link_gbs, spares=0, s
     if S > 0 and steps > 0:
         # the gather pass's own step time and its launch-step intervals, per
         # layer (us): router (+ permutation, + the adaptive cache's step for up
-        # to 8 tokens), the policy step (more tokens), then per group gather,
-        # gate/up, down
+        # to 8 tokens), the policy step (more tokens), then the FFN with its
+        # gather (one staging group) or per group the gather and the FFN
         res["gather_pass"] = {"ms_per_step": round(hook_ms / steps, 4),
+                              "ms_per_step_median": round(statistics.median(pass_ms), 4),
                               "us_per_layer": [round(v * 1e3 / (steps * L), 1) for v in part_ms]}
     dw.close()
     return res
 
 
 # ------------------------------------------------------- CPU oracle timing
-def oracle_sample(seconds: float, wl_name: str = "decode"):
-    """Times the oracle (as it stands) on decode tokens of the same workload
-    until `seconds` of CPU work are spent; returns (tokens/s, tokens, threads, s)."""
+def oracle_sample(seconds: float, wl_name: str = "decode", mode: int = 0, batch: int = 1):
+    """Times the oracle (as it stands) on tokens of the workload's layer, `batch`
+    tokens per call, until `seconds` of CPU work are spent (record generation
+    excluded); mode 1 = prefill numerics.  Returns (tokens/s, tokens, threads, s)."""
     import gen
     import oracle
     wl = gen.WORKLOADS[wl_name]
@@ -763,18 +962,82 @@ def oracle_sample(seconds: float, wl_name: str = "decode"):
     ids, *_ = oracle.route(x, Wr, None, wl.k)
     n_done, t_spent = 0, 0.0
     recs = {}
-    while t_spent < seconds and n_done < 64:
-        need = [e for e in ids[n_done] if e not in recs]
+    while t_spent < seconds and n_done + batch <= 64:
+        sl = slice(n_done, n_done + batch)
+        need = [int(e) for e in set(ids[sl].ravel().tolist()) if int(e) not in recs]
         if need:
             for e, r in zip(need, gen.expert_records(wl.seed, 0, need, wl.H, wl.I)):
-                recs[int(e)] = r
+                recs[e] = r
         t0 = time.perf_counter()
-        oracle.layer_forward(x[n_done:n_done + 1], wl.H, wl.I, wl.E, wl.k, Wr, None,
-                             {int(e): recs[int(e)] for e in ids[n_done]}, g, shared_w=sh)
+        oracle.layer_forward(x[sl], wl.H, wl.I, wl.E, wl.k, Wr, None,
+                             {int(e): recs[int(e)] for e in ids[sl].ravel()}, g, shared_w=sh,
+                             mode=mode)
         t_spent += time.perf_counter() - t0
-        n_done += 1
+        n_done += batch
     threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
     return n_done / t_spent, n_done, threads, t_spent
+
+
+def _oracle_single_thread(seconds: float, wl_name: str, mode: int):
+    """oracle_sample in a child process with OMP_NUM_THREADS=1."""
+    import subprocess
+    code = ("import json, bench; print(json.dumps(bench.oracle_sample(%r, %r, %d, 1)))"
+            % (seconds, wl_name, mode))
+    env = {**os.environ, "OMP_NUM_THREADS": "1"}
+    out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
+                         cwd=os.path.dirname(os.path.abspath(__file__)), timeout=600)
+    tps, n, threads, spent = json.loads(out.stdout.strip().splitlines()[-1])
+    return tps, n, spent
+
+
+def _cpu_model() -> str:
+    try:
+        out = subprocess_run(["lscpu"])
+        for ln in out.splitlines():
+            if ln.strip().startswith("Model name"):
+                return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        for ln in open("/proc/cpuinfo"):
+            if ln.lower().startswith(("model name", "cpu part")):
+                return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def subprocess_run(cmd):
+    import subprocess
+    return subprocess.run(cmd, capture_output=True, text=True, timeout=30).stdout
+
+
+def cpu_baseline(seconds: float) -> dict:
+    """The oracle timed on this host: decode tokens and prefill tokens (the
+    4096-token layer's numerics, a sample of its tokens), on all cores
+    (OpenMP over the tokens of a call and the rows of each product) and on
+    one thread, with the CPU model."""
+    tps, n, threads, spent = oracle_sample(seconds)
+    res = {"value": round(tps, 4), "unit": UNIT, "cores": threads, "kind": "oracle",
+           "sample": f"{n} decode tokens of the same layer ({spent:.1f} s)",
+           "cpu_model": _cpu_model()}
+    try:
+        t1, n1, s1 = _oracle_single_thread(seconds / 3, "decode", 0)
+        res["single_thread"] = {"value": round(t1, 4), "unit": UNIT, "cores": 1,
+                                "sample": f"{n1} decode tokens ({s1:.1f} s)"}
+    except Exception as exc:
+        res["single_thread"] = {"error": repr(exc)}
+    try:
+        tp, n_p, _, sp_ = oracle_sample(seconds / 2, "prefill", 1, batch=threads)
+        res["prefill"] = {"value": round(tp, 4), "unit": UNIT, "cores": threads,
+                          "sample": f"{n_p} tokens of the 4096-token prefill layer in its "
+                                    f"prefill numerics, {threads} per call ({sp_:.1f} s)"}
+        t1, n1, s1 = _oracle_single_thread(seconds / 3, "prefill", 1)
+        res["prefill_single_thread"] = {"value": round(t1, 4), "unit": UNIT, "cores": 1,
+                                        "sample": f"{n1} prefill tokens ({s1:.1f} s)"}
+    except Exception as exc:
+        res["prefill"] = {"error": repr(exc)}
+    return res
 
 
 def run_reference(args, rank, world):
@@ -810,6 +1073,8 @@ def run_ours(args, rank, world, local_rank):
     # a non-default stream: graph capture and all timing happen on it
     torch.cuda.set_stream(torch.cuda.Stream(device=dev))
     moe.lib()
+    global PREFILL_GEMM_WL
+    PREFILL_GEMM_WL = _prefill_gemm_wl()
     peaks, peak_kind = _peaks()
     if args.only == "prefill":
         return {"prefill": bench_prefill(args, torch, moe, gen, gd, dev, peaks)}
@@ -826,6 +1091,21 @@ def run_ours(args, rank, world, local_rank):
         link = link_h2d_gbs(torch, dev)
         return {args.only: bench_multilayer(args, torch, moe, gen, gd, dev, "stack", link,
                                             spares=ADAPTIVE_SPARES)}
+    if args.only == "stack_budget":
+        link = link_h2d_gbs(torch, dev)
+        return {args.only: bench_stack_budget(args, torch, moe, gen, gd, dev, link)}
+    if args.only == "prefill_streamed":
+        link = link_h2d_gbs(torch, dev)
+        return {args.only: bench_prefill_streamed(args, torch, moe, gen, gd, dev, peaks, link)}
+    if args.only == "prefill_gemm":
+        return {args.only: bench_prefill(args, torch, moe, gen, gd, dev, peaks, group=0,
+                                         wl=PREFILL_GEMM_WL, label=PREFILL_GEMM_LABEL)}
+    if args.only == "prefill_mx":
+        return {args.only: bench_prefill(args, torch, moe, gen, gd, dev, peaks, group=0,
+                                         wl=_mx(gen, "prefill"), label=PREFILL_MX_LABEL)}
+    if args.only == "decode_mx":
+        return {args.only: bench_decode(args, torch, moe, gen, gd, dev, rank, world, local_rank,
+                                        peaks, wl=_mx(gen, "decode"))}
     d = bench_decode(args, torch, moe, gen, gd, dev, rank, world, local_rank, peaks)
     d["roofline"]["peak_source"] = (f"{peak_kind}: MEASURED_PEAKS.json hbm_gbs (copy)"
                                     if peak_kind == "measured" else "fallback 6.8 TB/s")
@@ -845,7 +1125,7 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": d["gpu_launches"], "clocks": d["clocks"], "wall_s": d["wall_s"],
     }
     torch.cuda.empty_cache()
-    if rank == 0 and not args.decode_only and not args.small:
+    if rank == 0 and not args.decode_only and not args.small and args.only != "decode":
         also = {}
         # the link-bound stacks first: after the prefill passes (two 6 GB
         # layers built and freed) the gathers over the host link measured slower
@@ -864,9 +1144,40 @@ def run_ours(args, rank, world, local_rank):
         except Exception as exc:
             also["link_h2d_gbs"] = {"error": repr(exc)}
         try:
+            link = link if isinstance(also.get("link_h2d_gbs"), float) else link_h2d_gbs(torch, dev)
+            also["stack_budget"] = bench_stack_budget(args, torch, moe, gen, gd, dev, link)
+        except Exception as exc:
+            also["stack_budget"] = {"error": repr(exc)}
+        torch.cuda.empty_cache()
+        try:
             also["prefill"] = bench_prefill(args, torch, moe, gen, gd, dev, peaks)
         except Exception as exc:  # reported, not hidden
             also["prefill"] = {"error": repr(exc)}
+        torch.cuda.empty_cache()
+        try:
+            also["prefill_streamed"] = bench_prefill_streamed(
+                args, torch, moe, gen, gd, dev, peaks, link_h2d_gbs(torch, dev),
+                resident_ms=also["prefill"].get("ms_per_step"))
+        except Exception as exc:
+            also["prefill_streamed"] = {"error": repr(exc)}
+        torch.cuda.empty_cache()
+        for name, kw in (("prefill_gemm", dict(wl=PREFILL_GEMM_WL, label=PREFILL_GEMM_LABEL)),
+                         ("prefill_mx", dict(wl=_mx(gen, "prefill"), label=PREFILL_MX_LABEL))):
+            try:
+                also[name] = bench_prefill(args, torch, moe, gen, gd, dev, peaks, group=0, **kw)
+            except Exception as exc:
+                also[name] = {"error": repr(exc)}
+            torch.cuda.empty_cache()
+        try:
+            a2 = argparse.Namespace(**{**vars(args), "steps": min(args.steps, 300)})
+            dm = bench_decode(a2, torch, moe, gen, gd, dev, rank, world, local_rank, peaks,
+                              wl=_mx(gen, "decode"))
+            also["decode_mx"] = {kk: dm[kk] for kk in ("value", "ms_per_step", "roofline",
+                                                         "kernels")}
+            also["decode_mx"]["workload"] = ("the decode layer with MXFP4 records (E8M0 scale "
+                                             "per 32 values), 1 token per forward")
+        except Exception as exc:
+            also["decode_mx"] = {"error": repr(exc)}
         torch.cuda.empty_cache()
         try:  # the same layer walked in launch groups of 64 experts
             g64 = bench_prefill(args, torch, moe, gen, gd, dev, peaks,
@@ -900,8 +1211,9 @@ def main():
     ap.add_argument("--small", action="store_true",
                     help="16 distinct expert records (profiler captures only)")
     ap.add_argument("--only", default="",
-                    choices=["", "prefill", "route", "stack", "flat", "stack_adaptive",
-                             "stack_skip"],
+                    choices=["", "decode", "prefill", "route", "stack", "flat",
+                             "stack_adaptive", "stack_skip", "stack_budget", "prefill_streamed",
+                             "prefill_gemm", "prefill_mx", "decode_mx"],
                     help="run one secondary workload alone (profiler captures)")
     ap.add_argument("--prefill-experts", type=int, default=0,
                     help="prefill with fewer experts, same tokens per expert (profiling)")
@@ -926,10 +1238,7 @@ def main():
         return
     if rank == 0:
         if not args.no_cpu_baseline and world == 1:
-            tps, n, threads, spent = oracle_sample(args.cpu_seconds)
-            out["cpu_baseline"] = {"value": round(tps, 4), "unit": UNIT, "cores": threads,
-                                   "kind": "oracle",
-                                   "sample": f"{n} decode tokens of the same layer ({spent:.1f} s)"}
+            out["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
         print(json.dumps(out), flush=True)
     if world > 1:
         import torch

@@ -81,7 +81,7 @@ def build(wl: gen.Workload, layers: int | None = None, T_max: int | None = None,
     E, H, I, k = wl.E, wl.H, wl.I, wl.k
     T_max = T_max or wl.T
     dev = torch.device("cuda")
-    rb = gen.record_bytes(H, I)
+    rb = gen.record_bytes(H, I, wl.fmt)
     s = torch.cuda.current_stream() if stream is None else stream
     sp = s.cuda_stream
 
@@ -135,7 +135,8 @@ def build(wl: gen.Workload, layers: int | None = None, T_max: int | None = None,
         for i0 in range(0, len(fill_list), batch):
             chunk = fill_list[i0:i0 + batch]
             for j, (l, e, _) in enumerate(chunk):
-                gen.dev_expert_record(wl.seed, rec_layer[l], e, H, I, buf[j].data_ptr(), sp)
+                gen.dev_expert_record(wl.seed, rec_layer[l], e, H, I, buf[j].data_ptr(), sp,
+                                      fmt=wl.fmt)
             s.synchronize()
             for j, (l, e, idx) in enumerate(chunk):
                 torch.from_numpy(host_arena.array[idx]).copy_(buf[j].cpu())
@@ -149,12 +150,13 @@ def build(wl: gen.Workload, layers: int | None = None, T_max: int | None = None,
         n_cache = slot_alias
         layer_slots = np.array([0, slot_alias], np.int32)
     cache = ExpertCache(L, E, H, I, n_cache, n_stage, layer_slots=layer_slots,
-                        host_arena=host_arena, host_index=host_index)
+                        host_arena=host_arena, host_index=host_index, fmt=wl.fmt)
     for l in range(L):
         for j, e in enumerate(resident[l]):
             slot = int(layer_slots[l]) + (j % slot_alias if slot_alias > 0 else j)
             if slot_alias == 0 or j < slot_alias:
-                gen.dev_expert_record(wl.seed, rec_layer[l], e, H, I, cache.slot_ptr(slot), sp)
+                gen.dev_expert_record(wl.seed, rec_layer[l], e, H, I, cache.slot_ptr(slot), sp,
+                                      fmt=wl.fmt)
             cache.set_resident(l, e, slot, s)
     if spares > 0:
         cache.set_policy(spares)

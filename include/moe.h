@@ -39,18 +39,24 @@
  *     kernel traps.  The kernel that sees such an error skips the bad item.
  *   - Shapes: H % 256 == 0, I % 128 == 0, 1 <= k <= min(E, 32), E <= 1024.
  *
- * Expert record (the storage and transfer unit; fixed stride per (H, I)):
+ * Expert record (the storage and transfer unit; fixed stride per (H, I) and
+ * format), in one of two 4-bit formats:
+ *   NVFP4 (MOE_FMT_NVFP4; dev.to page, "The wall"): E4M3 block scale per 16
+ *     values (B = 16);
+ *   MXFP4 (MOE_FMT_MXFP4; windlass README: GLM-5.2 in MXFP4): E8M0 block
+ *     scale (2^(b-127), OCP Microscaling Formats v1.0) per 32 values (B = 32).
  *   [gate codes I x H/2][up codes I x H/2][down codes H x I/2]
- *   [gate scales I x H/16][up scales I x H/16][down scales H x I/16]
+ *   [gate scales I x H/B][up scales I x H/B][down scales H x I/B]
  *   Codes: E2M1 (sign bit 3; magnitudes 0, .5, 1, 1.5, 2, 3, 4, 6), two per
  *   byte, element 2j in the low nibble, rows contiguous (K-major).
- *   Scales: E4M3 (FN; bias 7; max 448), one per 16 consecutive elements of a
- *   row, stored in 512-byte atoms: for row r and 16-block kb of a matrix
- *   with KB = K/16 blocks per row, byte
- *     ((r/128)*(KB/4) + kb/4)*512 + (r%32)*16 + ((r%128)/32)*4 + kb%4.
- *   weight(r, c) = e2m1(code) * e4m3(scale(r, c/16)) * g[expert][matrix],
- *   g an fp32 per-(expert, matrix) global scale held outside the record.
- *   Size: 3*I*H/2 + 3*I*H/16 bytes (21,233,664 for H = 6144, I = 2048).
+ *   Scales: one byte per B consecutive elements of a row, stored in 512-byte
+ *   atoms: for row r and block kb of a matrix with KB = K/B blocks per row,
+ *   byte ((r/128)*(KB/4) + kb/4)*512 + (r%32)*16 + ((r%128)/32)*4 + kb%4.
+ *   weight(r, c) = e2m1(code) * scale(r, c/B) * g[expert][matrix], g an
+ *   fp32 per-(expert, matrix) global scale held outside the record (for
+ *   MXFP4 g = 1 is the format as published).
+ *   Size: 3*I*H/2 + 3*I*H/B bytes (H = 6144, I = 2048: 21,233,664 NVFP4,
+ *   20,054,016 MXFP4).
  */
 #ifndef MOE_H
 #define MOE_H
@@ -79,8 +85,12 @@ const char* moe_status_string(moe_status s);
 /* ABI version of this header (bumped on any incompatible change). */
 int moe_abi_version(void);
 
-/* Bytes of one expert record for hidden size H and expert intermediate I. */
-uint64_t moe_record_bytes(int H, int I);
+/* Record formats. */
+enum { MOE_FMT_NVFP4 = 0, MOE_FMT_MXFP4 = 1 };
+
+/* Bytes of one expert record for hidden size H, expert intermediate I and
+ * format (0 for an unknown format). */
+uint64_t moe_record_bytes(int H, int I, int format);
 
 /* ------------------------------------------------------------------ route
  * Router of the "Project Maya" page (device-side router, fp32 router
@@ -159,6 +169,8 @@ typedef struct {
   uint64_t host_arena_records;  /* records in the host arena                        */
   const int64_t* host_index;    /* host [L][E]: record index in the host arena of
                                    (layer, expert), -1 = not there; NULL = none     */
+  int format;                   /* MOE_FMT_NVFP4 or MOE_FMT_MXFP4: every record of
+                                   the cache (the layers' FFN kernels follow it)    */
 } expcache_desc;
 
 /* Allocates the slot arenas and the device slot table (all entries -1 = not
@@ -277,13 +289,19 @@ moe_status expcache_plan_slots(const uint32_t* d_counts, int L, int E, int total
  *   kernel sets MOE_ERR_UNSUPPORTED in *status (its outputs are then not
  *   defined).  Writes o_route[p] = w[t][j] * o (fp32).  For routes whose
  *   expert is not in the group nothing is written.
- * PREFILL mode: activations quantised to NVFP4 (per token, and h per route:
- *   G = amax/(6*448), block scale e4m3_rne(amax_b/(6 G)), codes
- *   e2m1_rne(v/(s G))) and multiplied on the tcgen05 tensor cores (FP4 x FP4,
- *   fp32 accumulation in tensor memory); adds w[t][j] * o into y_acc[t]
- *   (fp32, caller-zeroed).  Experts are taken prefill_group at a time; every
- *   active expert must be resident (a hit), group must be 0, and H and I must
- *   be multiples of 256 (else MOE_ERR_UNSUPPORTED).
+ * PREFILL mode: activations quantised to the records' format (NVFP4 records:
+ *   per token, and h per route, G = amax/(6*448), block scale
+ *   e4m3_rne(amax_b/(6 G)), codes e2m1_rne(v/(s G)); MXFP4 records: per block
+ *   of 32 the OCP MX rule, scale 2^(floor(log2 amax_b) - 2), codes
+ *   e2m1_rne(v / scale)) and multiplied on the tcgen05 tensor cores (FP4 x
+ *   FP4, fp32 accumulation in tensor memory); adds w[t][j] * o into y_acc[t]
+ *   (fp32, caller-zeroed).  Each expert is read from the slot src_slot gives
+ *   it: a hit's cache slot, or the staging slot a miss's record was gathered
+ *   into (expcache_fill) before this call.  The group-0 call also quantises
+ *   the tokens and plans the tiles of every active expert; the calls of the
+ *   later groups reuse that plan (same arguments and workspace, in group
+ *   order on one stream).  Experts are taken prefill_group at a time; H and
+ *   I must be multiples of 256 (else MOE_ERR_UNSUPPORTED).
  * Shared expert (Is > 0, group 0 only): bf16 gate/up [Is][H], down [H][Is];
  *   DECODE writes o_shared[t] = shared(x_t) (fp32); PREFILL adds it into
  *   y_acc[t] (bf16 tensor-core GEMMs, h rounded to bf16).
@@ -398,8 +416,17 @@ moe_status moe_combine(const moe_combine_args* a, void* stream);
  * permute -> lookup -> (fill group g -> ffn group g, for every group) ->
  * combine on one stream.  T >= prefill_min_tokens (> 0) takes the PREFILL
  * path (experts walked in groups of prefill_group through the staging
- * layout), otherwise DECODE.  The decode path never synchronises with the
- * host and can be captured in a CUDA graph.
+ * layout), otherwise DECODE.  Neither path synchronises with the host, and
+ * the decode path can be captured in a CUDA graph.
+ * Misses: decode gathers them into the staging slots group by group, or,
+ * when every miss fits in them, inside the FFN kernel itself (copy units run
+ * beside the hits' units; a miss's units wait for its record, bounded).  A
+ * prefill with at least 2 staging slots gathers its misses on a second
+ * stream of the layer, in groups of n_stage/2 into alternating halves of the
+ * staging slots, while the first stream runs the GEMMs of the hits and of
+ * the groups already landed (the "groups of 64 experts through a staging
+ * buffer" of the dev.to page); the streams are joined before the forward's
+ * last kernel.
  *
  * skip_tau > 0 turns on the renorm-skip (Strata-GLM blog, section
  * "Uncensoring without touching the weights"): a route whose expert is not
@@ -451,10 +478,14 @@ moe_status moe_layer_debug_prefill(const moe_layer* l, const float** h_rows,
  * events[0..n) are cudaEvent_t handles owned by the caller.  While set, every
  * moe_layer_forward records events[0] before its first kernel and events[i]
  * (i < n) after its i-th launch step: the router (with the permutation and
- * lookup when they share its kernel: up to 8 tokens), the permutation, each
- * gather, then the gate/up and the down kernel (decode) or the whole FFN
- * (prefill), then the combine (when it is a kernel of its own).  So the caller
- * can time each kernel of the layer's own sequence.
+ * lookup when they share its kernel: up to 8 tokens), the permutation, the
+ * adaptive cache's step (when a kernel of its own), then per expert group the
+ * gather (unless the FFN gathers itself or a second stream does) and the FFN:
+ * decode one kernel, prefill each of its kernels (token quantisation, tile
+ * tables, per launch group the gate/up GEMM, h quantisation and down GEMM,
+ * then the shared expert's two GEMMs), then the combine (when it is a kernel
+ * of its own).  So the caller can time each kernel of the layer's own
+ * sequence.
  * n = 0 clears the hook.  n > 32 is MOE_ERR_INVALID_ARG. */
 moe_status moe_layer_set_timing(moe_layer* l, void* const* events, int n);
 /* Synchronises `stream`, returns the layer's sticky device status in

@@ -15,7 +15,7 @@
 #include "policy_body.cuh"
 
 struct expcache {
-  int L, E, H, I;
+  int L, E, H, I, fmt;
   int n_cache, n_stage;
   uint64_t rec_bytes;
   uint8_t* arena;            // device, (n_cache + n_stage) * rec_bytes
@@ -121,9 +121,10 @@ moe_status launch_lookup(const LookupArgs& a, int E, const int32_t* counts, int3
 
 using namespace moe;
 
-MOE_API uint64_t moe_record_bytes(int H, int I) {
+MOE_API uint64_t moe_record_bytes(int H, int I, int format) {
   if (H <= 0 || I <= 0) return 0;
-  return RecordLayout(H, I).bytes;
+  if (format != MOE_FMT_NVFP4 && format != MOE_FMT_MXFP4) return 0;
+  return RecordLayout(H, I, format).bytes;
 }
 
 namespace moe {
@@ -136,6 +137,7 @@ MOE_API moe_status expcache_create(const expcache_desc* d, expcache** out) {
   if (d->L <= 0 || d->E <= 0 || d->H <= 0 || d->I <= 0 || d->n_cache_slots < 0 || d->n_stage < 0)
     return MOE_ERR_INVALID_ARG;
   if (d->H % 256 || d->I % 128 || d->E > 1024) return MOE_ERR_UNSUPPORTED;
+  if (d->format != MOE_FMT_NVFP4 && d->format != MOE_FMT_MXFP4) return MOE_ERR_UNSUPPORTED;
   if (d->host_arena && !d->host_index) return MOE_ERR_INVALID_ARG;
   if (d->layer_slots) {
     if (d->layer_slots[0] < 0) return MOE_ERR_INVALID_ARG;
@@ -150,7 +152,8 @@ MOE_API moe_status expcache_create(const expcache_desc* d, expcache** out) {
   c->n_cache = d->n_cache_slots; c->n_stage = d->n_stage;
   c->partitioned = d->layer_slots != nullptr;
   c->spares = -1;
-  c->rec_bytes = RecordLayout(d->H, d->I).bytes;
+  c->fmt = d->format;
+  c->rec_bytes = RecordLayout(d->H, d->I, d->format).bytes;
   c->slot_lo = (int32_t*)malloc(sizeof(int32_t) * d->L);
   c->slot_hi = (int32_t*)malloc(sizeof(int32_t) * d->L);
   if (!c->slot_lo || !c->slot_hi) {
@@ -263,6 +266,16 @@ MOE_API moe_status expcache_fill(expcache* c, int layer, const int32_t* d_expert
 }
 
 namespace moe {
+void cache_gather_args(const expcache* c, int layer, GatherArgs* out) {
+  out->host = c->host_dev;
+  out->host_index = c->host_index_dev ? c->host_index_dev + (size_t)layer * c->E : nullptr;
+  out->host_records = c->host_records;
+  out->n_cache = c->n_cache;
+  out->n_stage = c->n_stage;
+  out->slot_lo = c->slot_lo[layer];
+  out->slot_hi = c->slot_hi[layer];
+}
+
 void cache_lookup_args(const expcache* c, int layer, int32_t* src_slot, int32_t* act_list,
                        int32_t* n_act, int32_t* miss_ids, int32_t* n_miss, LookupArgs* out) {
   out->table = c->table + (size_t)layer * c->E;
@@ -296,6 +309,7 @@ MOE_API moe_status expcache_lookup(const expcache* c, int layer, const int32_t* 
 namespace moe {
 const uint8_t* cache_arena(const expcache* c) { return c->arena; }
 uint64_t cache_rec_bytes(const expcache* c) { return c->rec_bytes; }
+int cache_format(const expcache* c) { return c->fmt; }
 int cache_n_cache(const expcache* c) { return c->n_cache; }
 int cache_n_stage(const expcache* c) { return c->n_stage; }
 int cache_E(const expcache* c) { return c->E; }

@@ -31,16 +31,19 @@ struct LookupArgs {
 };
 
 // ---- record layout (see moe.h) ---------------------------------------------
+// values per block scale: NVFP4 16 (E4M3), MXFP4 32 (E8M0)
+__host__ __device__ __forceinline__ int fmt_block(int fmt) { return fmt == MOE_FMT_MXFP4 ? 32 : 16; }
+
 struct RecordLayout {
   uint64_t gate_codes, up_codes, down_codes;
   uint64_t gate_scales, up_scales, down_scales;
   uint64_t bytes;
-  __host__ __device__ RecordLayout(int H, int I) {
+  __host__ __device__ RecordLayout(int H, int I, int fmt) {
     uint64_t gu = (uint64_t)I * H / 2;
     gate_codes = 0;
     up_codes = gu;
     down_codes = 2 * gu;
-    uint64_t sgu = (uint64_t)I * H / 16;
+    uint64_t sgu = (uint64_t)I * H / (uint64_t)fmt_block(fmt);
     gate_scales = 3 * gu;
     up_scales = gate_scales + sgu;
     down_scales = up_scales + sgu;
@@ -83,6 +86,14 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t w16) {
   uint32_t r;
   asm("{\n .reg .b16 a;\n cvt.u16.u32 a, %1;\n cvt.rn.f16x2.e4m3x2 %0, a;\n}" : "=r"(r) : "r"(w16));
   return r;
+}
+
+// E8M0 byte (MX scale) -> its value 2^(b - 127); 0xFF is NaN
+__device__ __forceinline__ float e8m0_value(uint32_t b) {
+  uint32_t u = b << 23;                      // 2^(b - 127) for b in [1, 254]
+  u = b == 0u ? 0x00400000u : u;             // 2^-127 (an fp32 subnormal)
+  u = b == 0xFFu ? 0x7FC00000u : u;          // NaN
+  return __uint_as_float(u);
 }
 
 __device__ __forceinline__ float f16_lo(uint32_t h2) {
@@ -138,7 +149,28 @@ struct DecodeFuse {
   unsigned int* comb_ctl;
   const int32_t* inv;
   uint16_t* y;
+  // the layer's control words for the one-launch decode FFN (zero before a
+  // launch, left zero by it): ticket, done, shared h ready, pad, then one
+  // h-ready count per act position (up to 1024); nullptr: two launches
+  unsigned int* ffn_ctl;
+  // the misses' records are gathered by the FFN itself (one staging group):
+  // the cache and layer, the lookup's miss list, and the adaptive policy's
+  // destination slots (nullptr: staging slot i mod n_stage)
+  const expcache* g_cache;
+  int g_layer;
+  const int32_t* g_miss_ids;
+  const int32_t* g_n_miss;
+  const int32_t* g_dst_slots;
 };
+
+// the gather fields of one layer's records (cache.cu)
+struct GatherArgs {
+  const uint8_t* host;
+  const int64_t* host_index;
+  uint64_t host_records;
+  int n_cache, n_stage, slot_lo, slot_hi;
+};
+void cache_gather_args(const expcache* c, int layer, GatherArgs* out);
 
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,

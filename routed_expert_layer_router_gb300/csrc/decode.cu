@@ -19,6 +19,7 @@ namespace moe {
 
 const uint8_t* cache_arena(const expcache* c);
 uint64_t cache_rec_bytes(const expcache* c);
+int cache_format(const expcache* c);
 int cache_n_cache(const expcache* c);
 int cache_n_stage(const expcache* c);
 
@@ -69,7 +70,29 @@ struct DecodeParams {
   const int4* act_meta;  // per act_list position: {expert, slot, route, routes}, gscale row
   const int32_t* inv;
   uint16_t* y;
+  // K-decode-ffn (one launch): routed down units after the gate/up and
+  // shared-down units, and its control words (ticket, done, shared h ready,
+  // then one h-ready count per act position), zero before and after a launch
+  int n_rdown_units;
+  unsigned int* ffn_ctl;
+  // the misses' records gathered inside K-decode-ffn (n_gather_workers > 0):
+  // the leading tickets copy them from the mapped host arena, chunk by chunk
+  // in miss order, and count the chunks of each miss as they land
+  int n_gather_workers;
+  const uint8_t* g_host;          // device address of the mapped host arena
+  const int64_t* g_host_index;    // this layer's row: expert -> host record
+  uint64_t g_host_records;
+  const int32_t* g_miss_ids;      // the lookup's misses (ascending id)
+  const int32_t* g_n_miss;
+  const int32_t* g_dst_slots;     // adaptive cache: each miss's slot; nullptr: staging i mod S
+  int g_n_cache, g_n_stage, g_slot_lo, g_slot_hi;
+  int g_chunks;                   // chunks per record
 };
+
+constexpr int kFfnMaxPos = 1024;             // act positions (E <= 1024)
+constexpr uint64_t kGatherChunkBytes = 256 * 1024;
+constexpr int kGatherWorkers = 96;           // CTAs copying at once: the link, not the SMs, bounds them
+constexpr int kGatherUnroll = 8;             // 16-byte loads in flight per worker thread
 
 // An active expert of this group: its id, slot, first route position,
 // number of routes and global scales.  From the compact record when the
@@ -280,12 +303,59 @@ __device__ __forceinline__ void fp4_dot32h(const uint4& c, float s0, float s1, c
   }
 }
 
-// the two E4M3 scales (bytes 2*half, 2*half+1 of 4-byte word m1 of an atom row)
-__device__ __forceinline__ void scales_of(const uint4& a, int m1, int half, float& s0, float& s1) {
+// The two E4M3 scales of a lane's 32-value NVFP4 step hk of row m0 + 32 m1,
+// from the 16-byte atom row a (the 4-byte word m1 holds that row's four block
+// scales; the step's blocks of 16 are bytes 2 (hk & 1) and 2 (hk & 1) + 1).
+// An MXFP4 step is one block of 32 whose E8M0 scale is byte hk & 3 (row_step).
+__device__ __forceinline__ void scales_of(const uint4& a, int m1, int hk, float& s0, float& s1) {
   uint32_t wd = (m1 == 0) ? a.x : (m1 == 1) ? a.y : (m1 == 2) ? a.z : a.w;
-  uint32_t h2 = e4m3x2_to_f16x2((wd >> (16 * half)) & 0xFFFFu);
+  uint32_t h2 = e4m3x2_to_f16x2((wd >> (16 * (hk & 1))) & 0xFFFFu);
   s0 = f16_lo(h2);
   s1 = f16_hi(h2);
+}
+
+// byte offset, within a matrix's scales, of the atom row holding step hk of
+// row tile rt, row m0 (K values per row)
+template <int FMT>
+__device__ __forceinline__ uint64_t step_atom_row(int rt, int hk, int m0, int K) {
+  return FMT == MOE_FMT_MXFP4 ? atom_offset(rt, hk >> 2, K / 32) + (uint64_t)m0 * 16
+                              : atom_offset(rt, hk >> 1, K / 16) + (uint64_t)m0 * 16;
+}
+
+// The same for an MXFP4 step: the 32 codes share one scale, applied once.
+template <int M>
+__device__ __forceinline__ void fp4_dot32h_mx(const uint4& c, float sc, const uint32_t* xh,
+                                              float* acc) {
+  const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
+  float pa[M], pb[M];
+#pragma unroll
+  for (int j = 0; j < M; ++j) pa[j] = pb[j] = 0.f;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint32_t h[4];
+    e2m1x8_to_f16x2x4(cw[q], h);
+#pragma unroll
+    for (int b = 0; b < 4; ++b)
+#pragma unroll
+      for (int j = 0; j < M; ++j) fma_h2(pa[j], pb[j], h[b], xh[j * 16 + q * 4 + b]);
+  }
+#pragma unroll
+  for (int j = 0; j < M; ++j) acc[j] = fmaf(sc, pa[j] + pb[j], acc[j]);
+}
+
+// one row's step: dot products against the staged vectors, scaled per block
+template <int M, int FMT>
+__device__ __forceinline__ void row_step(const uint4& c, const uint4& atom_row, int m1, int hk,
+                                         const uint32_t* xh, float* acc) {
+  if (FMT == MOE_FMT_MXFP4) {
+    const uint32_t wd = (m1 == 0) ? atom_row.x : (m1 == 1) ? atom_row.y
+                      : (m1 == 2) ? atom_row.z : atom_row.w;
+    fp4_dot32h_mx<M>(c, e8m0_value((wd >> (8 * (hk & 3))) & 0xFFu), xh, acc);
+  } else {
+    float s0, s1;
+    scales_of(atom_row, m1, hk, s0, s1);
+    fp4_dot32h<M>(c, s0, s1, xh, acc);
+  }
 }
 
 template <int M>
@@ -311,12 +381,13 @@ __device__ __forceinline__ void load_xh(const __half* xs, int nhk, int hk, uint3
 struct GuRegs {
   uint4 g[4], u[4], sg, su;
 };
+template <int FMT>
 __device__ __forceinline__ void gu_fetch(const uint8_t* rec, const RecordLayout& L, int H, int rt,
                                          int m0, int hk, GuRegs& r) {
   const uint8_t* gc = rec + L.gate_codes + (uint64_t)(rt * 128 + m0) * (H / 2);
   const uint8_t* uc = rec + L.up_codes + (uint64_t)(rt * 128 + m0) * (H / 2);
   const uint64_t rstride = (uint64_t)32 * (H / 2);
-  const uint64_t aoff = atom_offset(rt, hk >> 1, H / 16) + (uint64_t)m0 * 16;
+  const uint64_t aoff = step_atom_row<FMT>(rt, hk, m0, H);
   r.sg = ldg_stream(rec + L.gate_scales + aoff);
   r.su = ldg_stream(rec + L.up_scales + aoff);
 #pragma unroll
@@ -328,7 +399,7 @@ __device__ __forceinline__ void gu_fetch(const uint8_t* rec, const RecordLayout&
 
 // `first` holds the step hk = lane, fetched by the caller (before it staged
 // the tokens, so that those loads were already in flight)
-template <int M>
+template <int M, int FMT>
 __device__ void warp_gu_fp4(const uint8_t* rec, const RecordLayout& L, int H, int rt, int m0,
                             const __half* xs, float accg[4][M], float accu[4][M],
                             const GuRegs& first) {
@@ -346,7 +417,7 @@ __device__ void warp_gu_fp4(const uint8_t* rec, const RecordLayout& L, int H, in
   }
   auto fetch = [&](int hk, uint4* g4, uint4* u4, uint4& sgv, uint4& suv) {
     GuRegs r;
-    gu_fetch(rec, L, H, rt, m0, hk, r);
+    gu_fetch<FMT>(rec, L, H, rt, m0, hk, r);
     sgv = r.sg;
     suv = r.su;
 #pragma unroll
@@ -361,14 +432,10 @@ __device__ void warp_gu_fp4(const uint8_t* rec, const RecordLayout& L, int H, in
     if (more) fetch(hk + 32, ng, nu, nsg, nsu);
     uint32_t xh[M * 16];
     load_xh<M>(xs, nhk, hk, xh);
-    const int half = hk & 1;
 #pragma unroll
     for (int m1 = 0; m1 < 4; ++m1) {
-      float s0, s1;
-      scales_of(sg, m1, half, s0, s1);
-      fp4_dot32h<M>(cg[m1], s0, s1, xh, accg[m1]);
-      scales_of(su, m1, half, s0, s1);
-      fp4_dot32h<M>(cu[m1], s0, s1, xh, accu[m1]);
+      row_step<M, FMT>(cg[m1], sg, m1, hk, xh, accg[m1]);
+      row_step<M, FMT>(cu[m1], su, m1, hk, xh, accu[m1]);
     }
     if (more) {
 #pragma unroll
@@ -449,12 +516,12 @@ __device__ void down_shared_pass(const DecodeParams& p, int r0, int t0, int mm, 
 }
 
 // ---- K-decode-gu -------------------------------------------------------------
-template <int M>
+template <int M, int FMT>
 __device__ void gu_routed_pass(const DecodeParams& p, const RecordLayout& L, const uint8_t* rec,
                                int rt, int m0, int q0, int mm, const __half* xs, float gg,
                                float gu, const GuRegs& first) {
   float accg[4][M], accu[4][M];
-  warp_gu_fp4<M>(rec, L, p.H, rt, m0, xs, accg, accu, first);
+  warp_gu_fp4<M, FMT>(rec, L, p.H, rt, m0, xs, accg, accu, first);
   const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int m1 = 0; m1 < 4; ++m1)
@@ -507,7 +574,7 @@ __device__ void gu_shared_pass(const DecodeParams& p, int i0, int t0, int mm, co
 // Grid: the routed units (one expert x one 128-row tile x a quarter of its
 // 32 atom rows) first, then the shared-expert units (4 row pairs each), which
 // are half as large and so fill the last wave.
-template <int MAXM>
+template <int MAXM, int FMT>
 __global__ void __launch_bounds__(kDecThreads, MAXM == 1 ? 2 : 1) k_decode_gu(DecodeParams p) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   __shared__ float red[kDecWarps * 8 * 2];
@@ -560,31 +627,33 @@ __global__ void __launch_bounds__(kDecThreads, MAXM == 1 ? 2 : 1) k_decode_gu(De
     return;
   }
   const uint8_t* rec = p.arena + (uint64_t)slot * p.rec_bytes;
-  const RecordLayout L(p.H, p.I);
+  const RecordLayout L(p.H, p.I, FMT);
   const float gg = ax.g[0], gu = ax.g[1];
   const int pb = ax.pb, pe = ax.pb + ax.cnt;
   const int lane = threadIdx.x & 31;
   for (int q0 = pb; q0 < pe; q0 += p.maxm) {
     const int mm = min(p.maxm, pe - q0);
     GuRegs first;  // the weights' first step, in flight while the tokens are staged
-    if (lane < p.H / 32) gu_fetch(rec, L, p.H, rt, m0, lane, first);
+    if (lane < p.H / 32) gu_fetch<FMT>(rec, L, p.H, rt, m0, lane, first);
     const uint16_t* rows[2];
     for (int j = 0; j < mm; ++j) rows[j] = p.x + (size_t)(p.perm[q0 + j] / p.k) * p.H;
     __syncthreads();
     const bool bad = stage_bf16_to_f16(xs, rows, mm, p.H);
     if (__syncthreads_or(bad) && threadIdx.x == 0) set_status(p.status, MOE_ERR_UNSUPPORTED);
-    if (MAXM == 2 && mm == 2) gu_routed_pass<MAXM>(p, L, rec, rt, m0, q0, mm, xs, gg, gu, first);
-    else gu_routed_pass<1>(p, L, rec, rt, m0, q0, mm, xs, gg, gu, first);
+    if (MAXM == 2 && mm == 2)
+      gu_routed_pass<MAXM, FMT>(p, L, rec, rt, m0, q0, mm, xs, gg, gu, first);
+    else
+      gu_routed_pass<1, FMT>(p, L, rec, rt, m0, q0, mm, xs, gg, gu, first);
   }
 }
 
 // ---- K-decode-down -----------------------------------------------------------
 // routed: CTA = one 128-row tile of one expert; warp w owns m0 in {w, w+8, w+16, w+24}
-template <int M>
+template <int M, int FMT>
 __device__ void down_routed_pass(const DecodeParams& p, const RecordLayout& L, const uint8_t* rec,
                                  int rt, int q0, int mm, const __half* hs, float gd) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  const int KB = p.I / 16, nhk = p.I / 32;
+  const int nhk = p.I / 32;
   const uint8_t* dc = rec + L.down_codes;
   float acc[4][4][M];
 #pragma unroll
@@ -594,12 +663,11 @@ __device__ void down_routed_pass(const DecodeParams& p, const RecordLayout& L, c
 #pragma unroll
       for (int j = 0; j < M; ++j) acc[g][m1][j] = 0.f;
   for (int hk = lane; hk < nhk; hk += 32) {
-    const int half = hk & 1;
     uint4 cd[4][4], sd[4];
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
       const int m0 = wid + 8 * g;
-      sd[g] = ldg_stream(rec + L.down_scales + atom_offset(rt, hk >> 1, KB) + (uint64_t)m0 * 16);
+      sd[g] = ldg_stream(rec + L.down_scales + step_atom_row<FMT>(rt, hk, m0, p.I));
 #pragma unroll
       for (int m1 = 0; m1 < 4; ++m1)
         cd[g][m1] = ldg_stream(dc + (uint64_t)(rt * 128 + m0 + 32 * m1) * (p.I / 2) +
@@ -611,9 +679,7 @@ __device__ void down_routed_pass(const DecodeParams& p, const RecordLayout& L, c
     for (int g = 0; g < 4; ++g)
 #pragma unroll
       for (int m1 = 0; m1 < 4; ++m1) {
-        float s0, s1;
-        scales_of(sd[g], m1, half, s0, s1);
-        fp4_dot32h<M>(cd[g][m1], s0, s1, xh, acc[g][m1]);
+        row_step<M, FMT>(cd[g][m1], sd[g], m1, hk, xh, acc[g][m1]);
       }
   }
 #pragma unroll
@@ -654,7 +720,7 @@ __device__ void combine_tile(const DecodeParams& p, int rt) {
   }
 }
 
-template <int MAXM>
+template <int MAXM, int FMT>
 __device__ __forceinline__ void down_unit(const DecodeParams& p, unsigned char* smem_raw) {
   const int wid = threadIdx.x >> 5;
   const int u = blockIdx.x;
@@ -684,7 +750,7 @@ __device__ __forceinline__ void down_unit(const DecodeParams& p, unsigned char* 
   const int slot = ax.slot;
   if (slot < 0 || slot >= p.n_slots) return;  // reported by K-decode-gu
   const uint8_t* rec = p.arena + (uint64_t)slot * p.rec_bytes;
-  const RecordLayout L(p.H, p.I);
+  const RecordLayout L(p.H, p.I, FMT);
   const float gd = ax.g[2];
   const int pb = ax.pb, pe = ax.pb + ax.cnt;
   for (int q0 = pb; q0 < pe; q0 += p.maxm) {
@@ -694,20 +760,20 @@ __device__ __forceinline__ void down_unit(const DecodeParams& p, unsigned char* 
     __syncthreads();
     const bool bad = stage_f32_to_f16(hs, rows, mm, p.I);
     if (__syncthreads_or(bad) && threadIdx.x == 0) set_status(p.status, MOE_ERR_UNSUPPORTED);
-    if (MAXM == 2 && mm == 2) down_routed_pass<MAXM>(p, L, rec, rt, q0, mm, hs, gd);
-    else down_routed_pass<1>(p, L, rec, rt, q0, mm, hs, gd);
+    if (MAXM == 2 && mm == 2) down_routed_pass<MAXM, FMT>(p, L, rec, rt, q0, mm, hs, gd);
+    else down_routed_pass<1, FMT>(p, L, rec, rt, q0, mm, hs, gd);
   }
 }
 
 // one token: three CTAs per SM (at most 85 registers), so that the routed
 // units (8 experts x 48 tiles) run in one wave
-template <int MAXM>
+template <int MAXM, int FMT>
 __global__ void __launch_bounds__(kDecThreads, MAXM == 1 ? 3 : 2) k_decode_down(DecodeParams p) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   __shared__ int s_last;
   pdl_wait();
   pdl_launch_dependents();
-  down_unit<MAXM>(p, smem_raw);
+  down_unit<MAXM, FMT>(p, smem_raw);
   if (!p.comb_ctl) return;
   // shared units cover 32 rows each (4 per tile); routed units one tile
   const int u = blockIdx.x;
@@ -752,6 +818,280 @@ __global__ void k_combine(int T, int H, int k, const float* __restrict__ y_acc,
   }
 }
 
+// ---- K-decode-ffn: gate/up, down and the combine in one launch ----------------
+// The units of both steps run as one grid.  A CTA takes its unit from a ticket
+// counter, not from blockIdx: tickets are handed out in order, so a unit that
+// waits only ever waits for units with earlier tickets, which CTAs already
+// running hold - every wait ends.  Ticket order: the shared expert's gate/up
+// units (when its h is not ready yet), the routed gate/up units expert by
+// expert, the shared expert's down units, the routed down units expert by
+// expert.  A routed down unit of act position a starts when all gate/up units
+// of a have written their h (a count per position); a shared down unit when
+// the shared gate/up units have.  So the down units of the first experts
+// stream their weights while the gate/up units of the last ones still run,
+// and the grid has one tail instead of two.  The combine is done by the last
+// CTA of each 128-row tile, as in K-decode-down.  The last CTA to finish
+// resets the control words for the next launch.  Every wait is bounded
+// (MOE_ERR_TIMEOUT in the status word).
+constexpr uint64_t kFfnWaitNs = 2000000000ull;
+
+__device__ __forceinline__ uint64_t gtimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ unsigned int ld_acquire(const unsigned int* p) {
+  unsigned int v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+// thread 0 waits for *c >= target, bounded; the CTA then reads what the
+// counted units wrote (through L2)
+__device__ __forceinline__ void cta_wait_count(const unsigned int* c, unsigned int target,
+                                               int32_t* status) {
+  if (threadIdx.x == 0) {
+    const uint64_t t0 = gtimer_ns();
+    while (ld_acquire(c) < target) {
+      if (gtimer_ns() - t0 > kFfnWaitNs) {
+        set_status(status, MOE_ERR_TIMEOUT);
+        break;
+      }
+      __nanosleep(100);
+    }
+    __threadfence();
+  }
+  __syncthreads();
+}
+// the CTA's writes are visible before the count (called by every thread:
+// each fences its own writes, then one thread counts)
+__device__ __forceinline__ void cta_signal(unsigned int* c) {
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) atomicAdd(c, 1u);
+}
+
+// one routed down unit (expert at act position a, 128-row tile rt), after
+// its h is complete
+template <int FMT>
+__device__ __forceinline__ void ffn_down_routed(const DecodeParams& p, int a, int rt,
+                                                unsigned char* smem_raw, int gu_units) {
+  ActExpert ax;
+  if (!act_expert(p, a, ax)) return;
+  const int slot = ax.slot;
+  if (slot < 0 || slot >= p.n_slots) return;  // reported by its gate/up units
+  cta_wait_count(p.ffn_ctl + 4 + a, (unsigned int)gu_units, p.status);
+  __half* hs = reinterpret_cast<__half*>(smem_raw);
+  const uint8_t* rec = p.arena + (uint64_t)slot * p.rec_bytes;
+  const RecordLayout L(p.H, p.I, FMT);
+  for (int q0 = ax.pb; q0 < ax.pb + ax.cnt; ++q0) {
+    const float* row = p.h_route + (size_t)q0 * p.I;
+    __syncthreads();
+    const bool bad = stage_f32_to_f16(hs, &row, 1, p.I);
+    if (__syncthreads_or(bad) && threadIdx.x == 0) set_status(p.status, MOE_ERR_UNSUPPORTED);
+    down_routed_pass<1, FMT>(p, L, rec, rt, q0, 1, hs, ax.g[2]);
+  }
+}
+
+// One gather worker: takes chunks (miss i, part c) from a counter in miss
+// order and copies each with 16-byte loads of the mapped host record, then
+// counts it in landed[i].  A miss whose record or slot is missing sets
+// MOE_ERR_DEVICE and is counted as landed (its experts' outputs are then
+// undefined), so that no unit waits for it.
+__device__ void ffn_gather_worker(const DecodeParams& p, unsigned int* ctl, unsigned int* landed) {
+  __shared__ unsigned int s_c;
+  const int n_miss = *p.g_n_miss;
+  const uint64_t total = (uint64_t)n_miss * (uint64_t)p.g_chunks;
+  const uint64_t rb = p.rec_bytes;
+  for (;;) {
+    __syncthreads();
+    if (threadIdx.x == 0) s_c = atomicAdd(&ctl[3], 1u);
+    __syncthreads();
+    const uint64_t c = s_c;
+    if (c >= total) break;
+    const int i = (int)(c / (uint64_t)p.g_chunks);
+    const uint64_t part = c % (uint64_t)p.g_chunks;
+    const int e = p.g_miss_ids[i];
+    const int64_t hr = (e >= 0 && e < p.E && p.g_host_index) ? p.g_host_index[e] : -1;
+    int slot;
+    if (p.g_dst_slots) {
+      slot = p.g_dst_slots[i];
+      const bool staging = p.g_n_stage > 0 && slot >= p.g_n_cache && slot < p.g_n_cache + p.g_n_stage;
+      if (!staging && (slot < p.g_slot_lo || slot >= p.g_slot_hi)) slot = -1;
+    } else {
+      slot = p.g_n_stage > 0 ? p.g_n_cache + (i % p.g_n_stage) : -1;
+    }
+    if (hr < 0 || (uint64_t)hr >= p.g_host_records || !p.g_host || slot < 0) {
+      if (threadIdx.x == 0 && part == 0) set_status(p.status, MOE_ERR_DEVICE);
+    } else {
+      const uint64_t b0 = part * kGatherChunkBytes;
+      const uint64_t b1 = min(rb, b0 + kGatherChunkBytes);
+      const uint4* s4 = reinterpret_cast<const uint4*>(p.g_host + (uint64_t)hr * rb + b0);
+      uint4* d4 = reinterpret_cast<uint4*>(const_cast<uint8_t*>(p.arena) + (uint64_t)slot * rb + b0);
+      const uint64_t n16 = (b1 - b0) / 16;
+      constexpr int kU = kGatherUnroll;  // 16-byte loads in flight per thread
+      uint64_t w = threadIdx.x;
+      for (; w + (kU - 1) * kDecThreads < n16; w += kU * kDecThreads) {
+        uint4 v[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) v[u] = ldg_stream(s4 + w + u * kDecThreads);
+#pragma unroll
+        for (int u = 0; u < kU; ++u) d4[w + u * kDecThreads] = v[u];
+      }
+      for (; w < n16; w += kDecThreads) d4[w] = ldg_stream(s4 + w);
+    }
+    cta_signal(&landed[i]);
+  }
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(kDecThreads, 2) k_decode_ffn(DecodeParams p) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  __shared__ float red[kDecWarps * 8 * 2];
+  __shared__ unsigned int s_ticket;
+  __shared__ int s_last;
+  unsigned int* ctl = p.ffn_ctl;
+  pdl_wait();
+  pdl_launch_dependents();
+  if (threadIdx.x == 0) s_ticket = atomicAdd(&ctl[0], 1u);
+  __syncthreads();
+  const int wid = threadIdx.x >> 5;
+  const int n_gw = p.n_gather_workers;
+  const int n_sgu = p.n_shared_units, n_rgu = p.n_routed_units;
+  const int n_sd = p.n_sdown_units, n_rd = p.n_rdown_units;
+  const int gu_units = (p.I / 128) * 4;  // gate/up units of one expert
+  const int tiles = p.H / 128;           // down units of one expert
+  unsigned int* h_ready = ctl + 4;
+  unsigned int* landed = ctl + 4 + kFfnMaxPos;
+  int tile = -1;                         // the 128-row tile a down unit adds to
+  // With the gather inside, the hits' whole FFN comes before the misses':
+  // gate/up (hits) | shared down | down (hits) | gate/up (misses) | down
+  // (misses), so that no unit waiting for a record holds an SM the hits need.
+  // Unit (phase, position) of this ticket:
+  int t = (int)s_ticket - n_gw;
+  int gu_a = -1, gu_r = 0, dn_a = -1, dn_rt = 0, sd_u = -1;
+  if ((int)s_ticket < n_gw) {
+    ffn_gather_worker(p, ctl, landed);
+  } else if (t < n_sgu) {
+    // handled below
+  } else if (n_gw > 0) {
+    const int n_hit = p.n_act[1];
+    const int max_act = n_rgu / gu_units;
+    t -= n_sgu;
+    if (t < n_hit * gu_units) {
+      gu_a = t / gu_units;
+      gu_r = t % gu_units;
+    } else if ((t -= n_hit * gu_units) < n_sd) {
+      sd_u = t;
+    } else if ((t -= n_sd) < n_hit * tiles) {
+      dn_a = t / tiles;
+      dn_rt = t % tiles;
+    } else if ((t -= n_hit * tiles) < (max_act - n_hit) * gu_units) {
+      gu_a = n_hit + t / gu_units;
+      gu_r = t % gu_units;
+    } else {
+      t -= (max_act - n_hit) * gu_units;
+      dn_a = n_hit + t / tiles;
+      dn_rt = t % tiles;
+    }
+    t = -1;
+  } else {
+    t -= n_sgu;
+    if (t < n_rgu) {
+      gu_a = t / gu_units;
+      gu_r = t % gu_units;
+    } else if ((t -= n_rgu) < n_sd) sd_u = t;
+    else if ((t -= n_sd) < n_rd) {
+      dn_a = t / tiles;
+      dn_rt = t % tiles;
+    }
+    t = -1;
+  }
+  if (t >= 0 && t < n_sgu) {
+    // shared gate/up: 4 row pairs
+    float* xs = reinterpret_cast<float*>(smem_raw);
+    for (int t0 = 0; t0 < p.T; ++t0) {
+      const uint16_t* row = p.x + (size_t)t0 * p.H;
+      __syncthreads();
+      stage_bf16_to_f32(xs, &row, 1, p.H);
+      __syncthreads();
+      gu_shared_pass<1>(p, t * 4, t0, 1, xs, red);
+    }
+    cta_signal(&ctl[2]);
+  } else if (gu_a >= 0) {
+    // routed gate/up: expert at act position a, tile rt, quarter of its rows
+    const int a = gu_a;
+    const int rt = gu_r >> 2, m0 = (gu_r & 3) * kDecWarps + wid;
+    ActExpert ax;
+    if (act_expert(p, a, ax)) {
+      // a miss gathered by this launch: wait until its record has landed
+      if (n_gw > 0 && a >= p.n_act[1])
+        cta_wait_count(&landed[a - p.n_act[1]], (unsigned int)p.g_chunks, p.status);
+      const int slot = ax.slot;
+      if (slot < 0 || slot >= p.n_slots) {
+        if (threadIdx.x == 0) set_status(p.status, MOE_ERR_DEVICE);
+      } else {
+        __half* xs = reinterpret_cast<__half*>(smem_raw);
+        const uint8_t* rec = p.arena + (uint64_t)slot * p.rec_bytes;
+        const RecordLayout L(p.H, p.I, FMT);
+        const int lane = threadIdx.x & 31;
+        for (int q0 = ax.pb; q0 < ax.pb + ax.cnt; ++q0) {
+          GuRegs first;  // the weights' first step, in flight while the token is staged
+          if (lane < p.H / 32) gu_fetch<FMT>(rec, L, p.H, rt, m0, lane, first);
+          const uint16_t* row = p.x + (size_t)(p.perm[q0] / p.k) * p.H;
+          __syncthreads();
+          const bool bad = stage_bf16_to_f16(xs, &row, 1, p.H);
+          if (__syncthreads_or(bad) && threadIdx.x == 0) set_status(p.status, MOE_ERR_UNSUPPORTED);
+          gu_routed_pass<1, FMT>(p, L, rec, rt, m0, q0, 1, xs, ax.g[0], ax.g[1], first);
+        }
+      }
+    }
+    cta_signal(&h_ready[a]);
+  } else if (sd_u >= 0) {
+    // shared down: 32 rows of H over all of Is
+    const int u = sd_u;
+    if (n_sgu > 0) cta_wait_count(&ctl[2], (unsigned int)n_sgu, p.status);
+    float* hs = reinterpret_cast<float*>(smem_raw);
+    const int r0 = u * (kDecWarps * 4) + wid * 4;
+    for (int t0 = 0; t0 < p.T; ++t0) {
+      const float* row = p.h_shared + (size_t)t0 * p.Is;
+      __syncthreads();
+      stage_f32_to_f32(hs, &row, 1, p.Is);
+      __syncthreads();
+      if (r0 < p.H) down_shared_pass<1>(p, r0, t0, 1, hs);
+    }
+    tile = u / 4;
+  } else if (dn_a >= 0) {
+    tile = dn_rt;
+    ffn_down_routed<FMT>(p, dn_a, tile, smem_raw, gu_units);
+  }
+  // combine: the last CTA of a 128-row tile sums its columns into y
+  if (p.comb_ctl && tile >= 0) {
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0)
+      s_last = atomicAdd(&p.comb_ctl[tile], 1u) == (unsigned)p.comb_target - 1;
+    __syncthreads();
+    if (s_last) {
+      __threadfence();
+      combine_tile(p, tile);
+      if (threadIdx.x == 0) p.comb_ctl[tile] = 0u;
+    }
+  }
+  // the last CTA resets the control words (every other CTA is done with them)
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    s_last = atomicAdd(&ctl[1], 1u) == gridDim.x - 1;
+  }
+  __syncthreads();
+  if (s_last) {
+    const int n_pos = n_rgu / gu_units;
+    for (int i = threadIdx.x; i < 4 + n_pos; i += blockDim.x) ctl[i] = 0u;
+    if (n_gw > 0)
+      for (int i = threadIdx.x; i < n_pos; i += blockDim.x) landed[i] = 0u;
+  }
+}
+
 // ---- host launchers -----------------------------------------------------------
 size_t decode_workspace_bytes(int T, int I, int k, int Is) {
   return ((size_t)T * k * I + (size_t)T * Is) * sizeof(float) + 256;
@@ -762,6 +1102,14 @@ static size_t smem_f32(int maxm, int K) { return (size_t)maxm * (K / 32) * kXPad
 
 moe_status decode_ffn(const moe_ffn_args* a, cudaStream_t s, const DecodeFuse& fz) {
   DecodeParams p;
+  p.n_rdown_units = 0;
+  p.ffn_ctl = nullptr;
+  p.n_gather_workers = 0;
+  p.g_host = nullptr;
+  p.g_host_index = nullptr;
+  p.g_host_records = 0;
+  p.g_miss_ids = p.g_n_miss = p.g_dst_slots = nullptr;
+  p.g_n_cache = p.g_n_stage = p.g_slot_lo = p.g_slot_hi = p.g_chunks = 0;
   p.shared_early = fz.shared_early ? 1 : 0;
   p.comb_ctl = nullptr;
   p.comb_target = 0;
@@ -772,6 +1120,7 @@ moe_status decode_ffn(const moe_ffn_args* a, cudaStream_t s, const DecodeFuse& f
   p.x = (const uint16_t*)a->x;
   p.arena = cache_arena(a->cache);
   p.rec_bytes = cache_rec_bytes(a->cache);
+  const bool mx = cache_format(a->cache) == MOE_FMT_MXFP4;
   p.n_slots = cache_n_cache(a->cache) + cache_n_stage(a->cache);
   p.gscale = a->gscale; p.src_slot = a->src_slot; p.act_list = a->act_list; p.n_act = a->n_act;
   p.offsets = a->offsets; p.perm = a->perm; p.w = a->w;
@@ -796,6 +1145,45 @@ moe_status decode_ffn(const moe_ffn_args* a, cudaStream_t s, const DecodeFuse& f
   int max_act = a->T * a->k < a->E ? a->T * a->k : a->E;
   if (a->group > 0) max_act = a->n_stage < max_act ? a->n_stage : max_act;
   bool shared = a->group == 0 && a->Is > 0;
+  if (fz.ffn_ctl && a->stages == MOE_STAGE_ALL) {
+    // one launch: gate/up, down and (one group) the combine
+    p.ffn_ctl = fz.ffn_ctl;
+    p.n_shared_units = (shared && !fz.shared_gu_done) ? a->Is / 4 : 0;
+    p.n_routed_units = max_act * (a->I / 128) * 4;
+    p.n_sdown_units = shared ? (a->H + kDecWarps * 4 - 1) / (kDecWarps * 4) : 0;
+    p.n_rdown_units = max_act * (a->H / 128);
+    if (fz.g_cache && a->group == 0) {
+      GatherArgs ga;
+      cache_gather_args(fz.g_cache, fz.g_layer, &ga);
+      p.n_gather_workers = kGatherWorkers;
+      p.g_host = ga.host;
+      p.g_host_index = ga.host_index;
+      p.g_host_records = ga.host_records;
+      p.g_miss_ids = fz.g_miss_ids;
+      p.g_n_miss = fz.g_n_miss;
+      p.g_dst_slots = fz.g_dst_slots;
+      p.g_n_cache = ga.n_cache;
+      p.g_n_stage = ga.n_stage;
+      p.g_slot_lo = ga.slot_lo;
+      p.g_slot_hi = ga.slot_hi;
+      p.g_chunks = (int)((p.rec_bytes + kGatherChunkBytes - 1) / kGatherChunkBytes);
+    }
+    size_t smem = smem_f16(1, a->H);
+    if (p.n_shared_units && smem_f32(1, a->H) > smem) smem = smem_f32(1, a->H);
+    if (shared && smem_f32(1, a->Is) > smem) smem = smem_f32(1, a->Is);
+    if (fz.comb_ctl && fz.inv && fz.y && (!a->Is || a->o_shared)) {
+      p.comb_ctl = fz.comb_ctl;
+      p.comb_target = max_act + (shared ? 4 : 0);  // CTAs per 128-row tile
+    }
+    const int grid = p.n_gather_workers + p.n_shared_units + p.n_routed_units + p.n_sdown_units +
+                     p.n_rdown_units;
+    if (grid > 0) {
+      auto* kern = mx ? k_decode_ffn<MOE_FMT_MXFP4> : k_decode_ffn<MOE_FMT_NVFP4>;
+      if (launch_pdl(kern, grid, kDecThreads, smem, s, p) != cudaSuccess) return MOE_ERR_CUDA;
+      if (fz.mark) fz.mark(fz.mark_ctx);
+    }
+    return MOE_OK;
+  }
   if (a->stages & MOE_STAGE_GATE_UP) {
     p.n_shared_units = (shared && !fz.shared_gu_done) ? a->Is / 4 : 0;
     p.n_sdown_units = (shared && fz.shared_gu_done && a->T == 1 && (a->stages & MOE_STAGE_DOWN))
@@ -807,8 +1195,8 @@ moe_status decode_ffn(const moe_ffn_args* a, cudaStream_t s, const DecodeFuse& f
     if (p.n_sdown_units && smem_f32(1, a->Is) > smem) smem = smem_f32(1, a->Is);
     const int grid = p.n_shared_units + p.n_sdown_units + routed;
     if (grid > 0) {
-      if (launch_pdl(k_decode_gu<1>, grid, kDecThreads, smem, s,
-                     p) != cudaSuccess)
+      auto* kern = mx ? k_decode_gu<1, MOE_FMT_MXFP4> : k_decode_gu<1, MOE_FMT_NVFP4>;
+      if (launch_pdl(kern, grid, kDecThreads, smem, s, p) != cudaSuccess)
         return MOE_ERR_CUDA;
       if (fz.mark) fz.mark(fz.mark_ctx);
     }
@@ -826,8 +1214,8 @@ moe_status decode_ffn(const moe_ffn_args* a, cudaStream_t s, const DecodeFuse& f
       p.comb_target = max_act + (shared ? 4 : 0);  // CTAs per 128-row tile
     }
     if (grid > 0) {
-      if (launch_pdl(k_decode_down<1>, grid, kDecThreads, smem,
-                     s, p) != cudaSuccess)
+      auto* kern = mx ? k_decode_down<1, MOE_FMT_MXFP4> : k_decode_down<1, MOE_FMT_NVFP4>;
+      if (launch_pdl(kern, grid, kDecThreads, smem, s, p) != cudaSuccess)
         return MOE_ERR_CUDA;
       if (fz.mark) fz.mark(fz.mark_ctx);
     }
@@ -837,7 +1225,12 @@ moe_status decode_ffn(const moe_ffn_args* a, cudaStream_t s, const DecodeFuse& f
 
 moe_status decode_setup() {
   // H up to 16384 with two staged tokens in fp32: 2 * 512 * 36 * 4 bytes
-  const void* fns[2] = {(const void*)k_decode_gu<1>, (const void*)k_decode_down<1>};
+  const void* fns[6] = {(const void*)k_decode_gu<1, MOE_FMT_NVFP4>,
+                        (const void*)k_decode_down<1, MOE_FMT_NVFP4>,
+                        (const void*)k_decode_gu<1, MOE_FMT_MXFP4>,
+                        (const void*)k_decode_down<1, MOE_FMT_MXFP4>,
+                        (const void*)k_decode_ffn<MOE_FMT_NVFP4>,
+                        (const void*)k_decode_ffn<MOE_FMT_MXFP4>};
   for (const void* f : fns)
     if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024) !=
         cudaSuccess)

@@ -38,6 +38,7 @@ namespace moe {
 
 const uint8_t* cache_arena(const expcache* c);
 uint64_t cache_rec_bytes(const expcache* c);
+int cache_format(const expcache* c);
 int cache_n_cache(const expcache* c);
 int cache_n_stage(const expcache* c);
 
@@ -56,16 +57,20 @@ enum Epi { EPI_GU_ROUTED = 0, EPI_GU_SHARED = 1, EPI_DOWN_ROUTED = 2, EPI_DOWN_S
 struct GemmParams {
   int mtiles;   // 128-row weight tiles per expert
   int kstages;  // K / (128 bytes of each operand row)
-  // routed experts of this launch: planned experts [g0, g1) (act_list order),
-  // their tiles tiles[plan_begin[g0]*mtiles .. plan_begin[g1]*mtiles)
+  // routed experts of this launch: planned experts (act_list order) [lo + g0,
+  // min(lo + g1, hi)) where [lo, hi) is the FFN call's expert group
+  // (pf_group_range), their tiles tiles[plan_begin[g0]*mtiles ..
+  // plan_begin[g1]*mtiles)
   const uint32_t* tiles;     // gate/up: packed (expert index j, m tile, n tile)
   const int4* ctab;          // down: column tiles {expert, slot, padded row of column 0, routes}
   const float2* dcol;        // down: per padded row {weight x G x down scale, token bits}
   const int32_t* plan_e;     // expert id of index j
   const int32_t* plan_slot;  // its cache slot
   const int32_t* plan_begin; // prefix of its 128-route column tiles
-  const int32_t* plan_n;     // [0]: planned experts
+  const int32_t* plan_n;     // [0]: planned experts, [1]: of them hits (act_list first)
   int g0, g1;
+  int group, gsize;          // the FFN call's expert group and misses per group
+  int part;                  // group 0 only: 0 all of it, 1 its hits, 2 its misses
   const int32_t* offsets;
   const int32_t* pad_offsets;
   const int32_t* perm;
@@ -102,6 +107,23 @@ __host__ __device__ __forceinline__ uint32_t tile_pack(int j, int mt, int nt) {
 // (ctab); so at any time the CTAs add into a few 128-row bands of every
 // token's y_acc row, which stay in L2, instead of into all of y_acc.
 
+// act_list range [lo, hi) of FFN group `group` among the planned experts:
+// group 0 = the hits and misses [0, S), group g > 0 = misses [g S, (g+1) S)
+// (S misses per group, all of them when S == 0)
+__device__ __forceinline__ void pf_group_range(const int32_t* plan_n, int group, int S, int part,
+                                               int& lo, int& hi) {
+  const int n = plan_n[0], n_hit = plan_n[1], n_miss = n - n_hit;
+  const int sz = S > 0 ? S : (n_miss > 0 ? n_miss : 1);
+  if (group == 0) {
+    lo = part == 2 ? n_hit : 0;
+    hi = part == 1 ? n_hit : n_hit + min(sz, n_miss);
+  } else {
+    lo = n_hit + group * sz;
+    hi = n_hit + min((group + 1) * sz, n_miss);
+  }
+  if (hi < lo) hi = lo;
+}
+
 // gate/up or shared tile t of a launch -> (m tile, n tile, expert id, slot)
 template <bool ROUTED>
 __device__ __forceinline__ void tile_info(const GemmParams& p, int t, int& mt, int& nt, int& e,
@@ -122,10 +144,10 @@ __device__ __forceinline__ void tile_info(const GemmParams& p, int t, int& mt, i
   }
 }
 
-// K-plan: the routed experts in act_list order (all hits: the prefill path
-// reads every active expert from a cache slot), their 128-route column tiles,
-// the gate/up tile table (mt_gu row tiles per column tile, expert-major) and
-// the column-tile table of the down GEMM.
+// K-plan: the active experts in act_list order (hits, then the misses, which
+// the FFN reads from the staging slots the lookup gave them), their 128-route
+// column tiles, the gate/up tile table (mt_gu row tiles per column tile,
+// expert-major) and the column-tile table of the down GEMM.
 // One CTA of 1024 threads, one expert per thread.
 __global__ void __launch_bounds__(1024) k_tile_plan(
     const int32_t* __restrict__ act_list, const int32_t* __restrict__ n_act,
@@ -136,10 +158,9 @@ __global__ void __launch_bounds__(1024) k_tile_plan(
     int32_t* __restrict__ plan_begin, int32_t* __restrict__ plan_n, int32_t* status) {
   __shared__ int s_w[33];
   const int j = threadIdx.x, lane = j & 31, wid = j >> 5;
-  const int hits = n_act[1];
-  if (j == 0 && n_act[0] != hits) set_status(status, MOE_ERR_DEVICE);
+  const int act = n_act[0];
   int e = -1, slot = -1, nt = 0, cnt = 0;
-  if (j < hits && j < E) {
+  if (j < act && j < E) {
     e = act_list[j];
     slot = src_slot[e];
     cnt = offsets[e + 1] - offsets[e];
@@ -168,7 +189,7 @@ __global__ void __launch_bounds__(1024) k_tile_plan(
   }
   __syncthreads();
   const int begin = s_w[wid] + incl - nt;
-  const int n = hits < E ? hits : E;
+  const int n = act < E ? act : E;
   if (j < n) {
     plan_e[j] = e;
     plan_slot[j] = slot;
@@ -181,6 +202,7 @@ __global__ void __launch_bounds__(1024) k_tile_plan(
   if (j == 0) {
     plan_begin[n] = s_w[32];
     plan_n[0] = n;
+    plan_n[1] = min(n_act[1], n);
   }
 }
 
@@ -192,8 +214,13 @@ struct Cfg {
   // routed down: row-tile-major order over a table of column tiles (ctab)
   static constexpr bool kMMajor = (EPI == EPI_DOWN_ROUTED);
   static constexpr bool kNvf4 = (KIND == 0);
+  static constexpr bool kMxf4 = (KIND == 2);
+  static constexpr bool kFp4 = kNvf4 || kMxf4;
   static constexpr int kTileBytes = kTileM * kStageKB;  // 16 KiB
-  static constexpr int kSfBytes = kNvf4 ? 2048 : 0;     // 4 atoms of 512 B
+  // scale atoms (512 B: 128 rows x 4 blocks) per operand and 128-byte K chunk
+  // (256 values): blocks of 16 (NVFP4) take 4 atoms, blocks of 32 (MXFP4) 2
+  static constexpr int kAtoms = kNvf4 ? 4 : (kMxf4 ? 2 : 0);
+  static constexpr int kSfBytes = kAtoms * 512;
   // one 128-byte K chunk of every operand (A tiles, B tile, their scale atoms)
   static constexpr int kChunkBytes = kTileBytes * (kDual ? 3 : 2) + kSfBytes * (kDual ? 3 : 2);
   // several chunks per stage: fewer stages per tile, so fewer barrier round
@@ -205,7 +232,8 @@ struct Cfg {
   static constexpr int kSmem = 1024 + kStages * kStageBytes;
   // tensor memory: accumulators, then per-stage scale-factor columns
   static constexpr uint32_t kAccCols = kDual ? 256 : 128;
-  static constexpr uint32_t kSfColsPerChunk = kNvf4 ? (kDual ? 48 : 32) : 0;
+  static constexpr uint32_t kOpSfCols = kAtoms * 4;  // tensor-memory columns per operand
+  static constexpr uint32_t kSfColsPerChunk = kOpSfCols * (kDual ? 3 : 2);
   static constexpr uint32_t kSfColsPerStage = kChunks * kSfColsPerChunk;
   // two accumulators where they fit beside the scale factors, so that a tile's
   // MMAs never wait for the previous tile's epilogue to read its accumulator
@@ -257,8 +285,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     abort_flag = 0;
     if (C::kRouted) {
-      const int n = p.plan_n[0];
-      const int g0 = min(p.g0, n), g1 = min(p.g1, n);
+      int lo, hi;
+      pf_group_range(p.plan_n, p.group, p.gsize, p.part, lo, hi);
+      const int g0 = min(lo + p.g0, hi), g1 = min(lo + p.g1, hi);
       s_cbase = p.plan_begin[g0];
       s_ncols = p.plan_begin[g1] - s_cbase;
       s_tlo = C::kMMajor ? 0 : s_cbase * p.mtiles;
@@ -343,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < ncs; ++c) {
             unsigned char* st = st0 + (size_t)c * C::kChunkBytes;
             const int kq = kb * C::kChunks + c;  // 128-byte K chunk
-            const int kc = C::kNvf4 ? kq * kStageKB : kq * (kStageKB / 2);  // bytes or bf16s
+            const int kc = C::kFp4 ? kq * kStageKB : kq * (kStageKB / 2);  // bytes or bf16s
             // Down: the weights are read once, the activation tiles by every row
             // tile of their column, and y_acc is added into meanwhile; the cache
             // policies keep the activations and y_acc in L2 ahead of the weights.
@@ -360,20 +389,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             unsigned char* bdst = st + C::kTileBytes * (C::kDual ? 2 : 1);
             if (C::kMMajor) ptx::tma_load_2d_hint(bdst, &tmB, kc, brow, &full_bar[s], pol_a);
             else ptx::tma_load_2d(bdst, &tmB, kc, brow, &full_bar[s]);
-            if (C::kNvf4) {
-              // 4 scale atoms (512 B each) per operand: k groups kb*4 .. kb*4+3
+            if (C::kFp4) {
+              // kAtoms scale atoms (512 B each) per operand: atom columns
+              // kq*kAtoms .. (kq+1)*kAtoms-1 of the row tile
               unsigned char* sf = bdst + C::kTileBytes;
               const uint8_t* rec = p.arena + (uint64_t)slot * p.rec_bytes;
-              const uint64_t aoff = ((uint64_t)mt * p.kgroups + (uint64_t)kq * 4) * 512;
-              const uint64_t boff = ((uint64_t)(brow / kTileN) * p.kgroups + (uint64_t)kq * 4) * 512;
-              unsigned char* sfb = sf + (C::kDual ? 4096 : 2048);
+              const uint64_t aoff = ((uint64_t)mt * p.kgroups + (uint64_t)kq * C::kAtoms) * 512;
+              const uint64_t boff =
+                  ((uint64_t)(brow / kTileN) * p.kgroups + (uint64_t)kq * C::kAtoms) * 512;
+              unsigned char* sfb = sf + C::kSfBytes * (C::kDual ? 2 : 1);
               if (C::kMMajor) {
-                ptx::bulk_load_hint(sf, rec + p.sfa_off0 + aoff, 2048, &full_bar[s], pol_w);
-                ptx::bulk_load_hint(sfb, p.b_scales + boff, 2048, &full_bar[s], pol_a);
+                ptx::bulk_load_hint(sf, rec + p.sfa_off0 + aoff, C::kSfBytes, &full_bar[s], pol_w);
+                ptx::bulk_load_hint(sfb, p.b_scales + boff, C::kSfBytes, &full_bar[s], pol_a);
               } else {
-                ptx::bulk_load(sf, rec + p.sfa_off0 + aoff, 2048, &full_bar[s]);
-                if (C::kDual) ptx::bulk_load(sf + 2048, rec + p.sfa_off1 + aoff, 2048, &full_bar[s]);
-                ptx::bulk_load(sfb, p.b_scales + boff, 2048, &full_bar[s]);
+                ptx::bulk_load(sf, rec + p.sfa_off0 + aoff, C::kSfBytes, &full_bar[s]);
+                if (C::kDual)
+                  ptx::bulk_load(sf + C::kSfBytes, rec + p.sfa_off1 + aoff, C::kSfBytes, &full_bar[s]);
+                ptx::bulk_load(sfb, p.b_scales + boff, C::kSfBytes, &full_bar[s]);
               }
             }
           }
@@ -400,6 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // instruction descriptor: M = 128, N = 128, K-major A and B
       uint32_t idesc = ((uint32_t)(kTileN >> 3) << 17) | ((uint32_t)(kTileM >> 4) << 24);
       if (C::kNvf4) idesc |= (1u << 7) | (1u << 10);               // E2M1 x E2M1, UE4M3 scales
+      else if (C::kMxf4) idesc |= (1u << 7) | (1u << 10) | (1u << 23);  // E2M1 x E2M1, UE8M0
       else idesc |= (1u << 4) | (1u << 7) | (1u << 10);            // fp32 D, bf16 A and B
       uint32_t g = 0, it = 0;
       for (int t = tlo + blockIdx.x; t < thi && !abort_flag; t += gridDim.x, ++it) {
@@ -432,13 +465,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t sf = b + C::kTileBytes;
             const uint32_t sfcol =
                 C::kSfCol0 + (uint32_t)s * C::kSfColsPerStage + (uint32_t)c * C::kSfColsPerChunk;
-            if (C::kNvf4) {
+            if (C::kFp4) {
               // scale atoms -> tensor memory (4 columns each)
-              for (int kk = 0; kk < 4; ++kk) {
+              for (int kk = 0; kk < C::kAtoms; ++kk) {
                 const int nops = C::kDual ? 3 : 2;
                 for (int o = 0; o < nops; ++o) {
-                  const uint64_t d = ptx::smem_desc(sf + o * 2048 + kk * 512, 128, 128, 0);
-                  ptx::tmem_cp_32x128b_x4(tmem + sfcol + o * 16 + kk * 4, d);
+                  const uint64_t d = ptx::smem_desc(sf + o * C::kSfBytes + kk * 512, 128, 128, 0);
+                  ptx::tmem_cp_32x128b_x4(tmem + sfcol + o * C::kOpSfCols + kk * 4, d);
                 }
               }
             }
@@ -452,6 +485,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (C::kDual) {
                   const uint64_t da1 = ptx::smem_desc(a1 + kk * 32, 16, 1024, 2);
                   ptx::mma_nvf4(acc + 128, da1, db, idesc, tmem + sfcol + 16 + kk * 4, sfb, accum);
+                }
+              } else if (C::kMxf4) {
+                // this K = 64 step's scales: atom kk / 2, bytes 0-1 (kk even)
+                // or 2-3 (kk odd) of each row's word
+                const uint32_t at = (uint32_t)(kk >> 1) * 4;
+                const uint32_t id = (kk & 1) ? ((2u << 29) | (2u << 4)) : 0u;
+                const uint32_t sfb = tmem + sfcol + C::kOpSfCols * (C::kDual ? 2 : 1) + at;
+                ptx::mma_mxf4(acc, da0, db, idesc | id, tmem + sfcol + at, sfb, accum);
+                if (C::kDual) {
+                  const uint64_t da1 = ptx::smem_desc(a1 + kk * 32, 16, 1024, 2);
+                  ptx::mma_mxf4(acc + 128, da1, db, idesc | id, tmem + sfcol + C::kOpSfCols + at,
+                                sfb, accum);
                 }
               } else {
                 ptx::mma_bf16(acc, da0, db, idesc, accum);
@@ -691,6 +736,30 @@ __device__ __forceinline__ float absmax4(float a, float b, float c, float d) {
   return fmaxf(fmaxf(fabsf(a), fabsf(b)), fmaxf(fabsf(c), fabsf(d)));
 }
 
+// ---- MXFP4 activation quantisation (records in MXFP4: the tensor cores take
+// both operands' scales in one format).  OCP Microscaling Formats v1.0: a
+// block of 32 values shares X = floor(log2 max|v|) - 2, kept in E8M0's range
+// [-127, 127] (scale byte X + 127); each code is E2M1(v / 2^X), round to
+// nearest even, saturating at 6; an all-zero block gets byte 0 and codes 0.
+// v / 2^X is a multiplication by an exact power of two.
+__device__ __forceinline__ uint32_t mx_scale(float ab, float& inv) {
+  if (!(ab > 0.f)) {
+    inv = 0.f;
+    return 0u;
+  }
+  const int X = max(ilogbf(ab) - 2, -127);
+  inv = __uint_as_float((uint32_t)(127 - X) << 23);  // 2^-X (X <= 125)
+  return (uint32_t)(X + 127);
+}
+template <int N>
+__device__ __forceinline__ uint32_t mx_codes(const float* v, float ab, float inv) {
+  if (!(ab > 0.f)) return 0u;
+  uint32_t c = 0;
+#pragma unroll
+  for (int i = 0; i < N; i += 2) c |= e2m1x2_rn(v[i] * inv, v[i + 1] * inv) << (4 * i);
+  return c;
+}
+
 // byte offset of the scale word (4 blocks, kg = block / 4) of padded row `row`
 // in the 512-byte scale atoms of a K-wide operand
 __device__ __forceinline__ size_t scale_word(int row, int kg, int KG) {
@@ -700,16 +769,16 @@ __device__ __forceinline__ size_t scale_word(int row, int kg, int KG) {
 // One fp32 row of K values (K % 256 == 0, K <= KMAX) by one warp into padded
 // row `row` of the tcgen05 layout.  Each load instruction covers 512
 // contiguous bytes (lane l holds float4 j*32 + l), so four lanes share a
-// 16-value block; the row is read once and held in registers.  Returns the
-// row's global scale G (on every lane).
-template <int KMAX>
+// 16-value block (eight a 32-value MX block); the row is read once and held
+// in registers.  Returns the row's global scale G (on every lane; 1 for MX).
+template <int KMAX, int FMT>
 __device__ __forceinline__ float quant_row_f32(const float* __restrict__ hr, int K, int row,
                                               uint8_t* __restrict__ codes,
                                               uint8_t* __restrict__ scales,
                                               float* __restrict__ Gr) {
   constexpr int kNJ = KMAX / 128;
   const int lane = threadIdx.x & 31;
-  const int NJ = K / 128, KG = K / 64;
+  const int NJ = K / 128, KG = K / (4 * fmt_block(FMT));
   float4 v[kNJ];
   float amax = 0.f;
 #pragma unroll
@@ -723,6 +792,29 @@ __device__ __forceinline__ float quant_row_f32(const float* __restrict__ hr, int
   const float G = amax > 0.f ? __fdiv_rn(amax, 2688.0f) : 1.0f;
   const float sixG = __fmul_rn(6.0f, G);
   uint16_t* crow = reinterpret_cast<uint16_t*>(codes + (size_t)row * (K / 2));
+  if (FMT == MOE_FMT_MXFP4) {
+#pragma unroll
+    for (int j = 0; j < kNJ; ++j) {
+      if (j >= NJ) break;
+      float ab = absmax4(v[j].x, v[j].y, v[j].z, v[j].w);
+      ab = fmaxf(ab, __shfl_xor_sync(0xFFFFFFFFu, ab, 1));
+      ab = fmaxf(ab, __shfl_xor_sync(0xFFFFFFFFu, ab, 2));
+      ab = fmaxf(ab, __shfl_xor_sync(0xFFFFFFFFu, ab, 4));
+      float inv;
+      const uint32_t sc = mx_scale(ab, inv);
+      const float f[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+      crow[j * 32 + lane] = (uint16_t)mx_codes<4>(f, ab, inv);
+      // blocks j*4 + lane/8: lane 0 gathers the scale word of the 128 values
+      const uint32_t s1 = __shfl_down_sync(0xFFFFFFFFu, sc, 8);
+      const uint32_t s2 = __shfl_down_sync(0xFFFFFFFFu, sc, 16);
+      const uint32_t s3 = __shfl_down_sync(0xFFFFFFFFu, sc, 24);
+      if (lane == 0)
+        *reinterpret_cast<uint32_t*>(scales + scale_word(row, j, KG)) =
+            sc | (s1 << 8) | (s2 << 16) | (s3 << 24);
+    }
+    if (lane == 0) Gr[row] = 1.0f;
+    return 1.0f;
+  }
 #pragma unroll
   for (int j = 0; j < kNJ; ++j) {
     if (j >= NJ) break;
@@ -746,12 +838,13 @@ __device__ __forceinline__ float quant_row_f32(const float* __restrict__ hr, int
 }
 
 // zero padded rows [r0, r1) of a K-wide operand (codes, scale words, G) with
-// the threads of one CTA
-__device__ __forceinline__ void zero_rows(int r0, int r1, int K, uint8_t* __restrict__ codes,
+// the threads of one CTA; blk = values per block scale
+__device__ __forceinline__ void zero_rows(int r0, int r1, int K, int blk,
+                                          uint8_t* __restrict__ codes,
                                           uint8_t* __restrict__ scales, float* __restrict__ G) {
   const int n = r1 - r0;
   if (n <= 0) return;
-  const int n16 = K / 32, KG = K / 64;  // 16-byte chunks of a codes row; scale words
+  const int n16 = K / 32, KG = K / (4 * blk);  // 16-byte chunks of a codes row; scale words
   uint4* c = reinterpret_cast<uint4*>(codes + (size_t)r0 * (K / 2));
   for (int i = threadIdx.x; i < n * n16; i += blockDim.x) c[i] = make_uint4(0u, 0u, 0u, 0u);
   for (int i = threadIdx.x; i < n * KG; i += blockDim.x)
@@ -767,17 +860,19 @@ constexpr int kQuantXMaxK = 8192;  // H up to 8192
 // row; padding rows are zeroed.  Three CTAs per SM for rows up to 2048 values
 // (80 registers, a few spilled): 101 -> 91 us for the 4096-token layer's h;
 // four CTAs spilled more and took 107.
-template <int KMAX>
+template <int KMAX, int FMT>
 __global__ void __launch_bounds__(256, KMAX <= 2048 ? 3 : 1) k_quant_h(
-    const float* __restrict__ h32, int K, int g0, int g1, const int32_t* __restrict__ plan_e,
+    const float* __restrict__ h32, int K, int g0, int g1, int group, int gsize, int part,
+    const int32_t* __restrict__ plan_e,
     const int32_t* __restrict__ plan_n, const int32_t* __restrict__ offsets,
     const int32_t* __restrict__ pad_offsets, const int32_t* __restrict__ perm,
     const float* __restrict__ w, const float* __restrict__ gscale, int k,
     uint8_t* __restrict__ codes, uint8_t* __restrict__ scales, float* __restrict__ G,
     float2* __restrict__ dcol) {
-  const int n = plan_n[0];
-  const int j = g0 + blockIdx.x;
-  if (j >= g1 || j >= n) return;
+  int glo, ghi;
+  pf_group_range(plan_n, group, gsize, part, glo, ghi);
+  const int j = glo + g0 + (int)blockIdx.x;
+  if (j >= min(glo + g1, ghi)) return;
   const int e = plan_e[j];
   const int cnt = offsets[e + 1] - offsets[e];
   const int r0 = pad_offsets[e], nrow = pad_offsets[e + 1] - r0;
@@ -786,7 +881,8 @@ __global__ void __launch_bounds__(256, KMAX <= 2048 ? 3 : 1) k_quant_h(
   const int wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
   const float gsd = gscale[e * 3 + 2];
   for (int i = lo + wid; i < min(hi, cnt); i += nw) {
-    const float Gi = quant_row_f32<KMAX>(h32 + (size_t)(r0 + i) * K, K, r0 + i, codes, scales, G);
+    const float Gi =
+        quant_row_f32<KMAX, FMT>(h32 + (size_t)(r0 + i) * K, K, r0 + i, codes, scales, G);
     if ((threadIdx.x & 31) == 0) {
       // the down GEMM's column data of this route: combine weight x G x the
       // expert's down scale (in that order), and the token
@@ -794,7 +890,7 @@ __global__ void __launch_bounds__(256, KMAX <= 2048 ? 3 : 1) k_quant_h(
       dcol[r0 + i] = make_float2(Gi * w[route] * gsd, __int_as_float(route / k));
     }
   }
-  zero_rows(r0 + max(lo, cnt), r0 + hi, K, codes, scales, G);
+  zero_rows(r0 + max(lo, cnt), r0 + hi, K, fmt_block(FMT), codes, scales, G);
   for (int i = max(lo, cnt) + threadIdx.x; i < hi; i += blockDim.x)
     dcol[r0 + i] = make_float2(0.f, 0.f);
 }
@@ -806,7 +902,7 @@ __global__ void __launch_bounds__(256) k_quant_rows_f32(const float* __restrict_
                                                         uint8_t* __restrict__ scales,
                                                         float* __restrict__ G) {
   const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  if (t < T) quant_row_f32<KMAX>(x + (size_t)t * K, K, t, codes, scales, G);
+  if (t < T) quant_row_f32<KMAX, MOE_FMT_NVFP4>(x + (size_t)t * K, K, t, codes, scales, G);
 }
 
 // K-actq: the tokens quantised once each and written straight into the
@@ -815,7 +911,7 @@ __global__ void __launch_bounds__(256) k_quant_rows_f32(const float* __restrict_
 // token t: 256 threads, thread i holding 16-byte chunks i + 256 m (8 values;
 // two threads per block).  CTA T + e zeroes expert e's padding rows.  With
 // inv == NULL (k = 1) token t goes to row t and no rows are padded.
-template <int KMAX>
+template <int KMAX, int FMT>
 __global__ void __launch_bounds__(256) k_quant_routes(
     const uint16_t* __restrict__ x, int T, int K, int E, int k, const int32_t* __restrict__ inv,
     const int32_t* __restrict__ offsets, const int32_t* __restrict__ pad_offsets,
@@ -827,12 +923,12 @@ __global__ void __launch_bounds__(256) k_quant_routes(
   if ((int)blockIdx.x >= T) {
     const int e = blockIdx.x - T;
     if (inv && e < E)
-      zero_rows(pad_offsets[e] + offsets[e + 1] - offsets[e], pad_offsets[e + 1], K, codes,
-                scales, G);
+      zero_rows(pad_offsets[e] + offsets[e + 1] - offsets[e], pad_offsets[e + 1], K,
+                fmt_block(FMT), codes, scales, G);
     return;
   }
   const int t = blockIdx.x;
-  const int NC = K / 8, KG = K / 64;
+  const int NC = K / 8, KG = K / (4 * fmt_block(FMT));
   const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)t * K);
   uint4 v[kNJ];
 #pragma unroll
@@ -890,6 +986,18 @@ __global__ void __launch_bounds__(256) k_quant_routes(
 #pragma unroll
     for (int q = 0; q < 8; ++q) ab = fmaxf(ab, fabsf(f[q]));
     ab = fmaxf(ab, __shfl_xor_sync(0xFFFFFFFFu, ab, 1));  // the other half of the block
+    if (FMT == MOE_FMT_MXFP4) {
+      ab = fmaxf(ab, __shfl_xor_sync(0xFFFFFFFFu, ab, 2));  // four threads per block of 32
+      float inv;
+      const uint32_t sc = mx_scale(ab, inv);
+      cw[m] = mx_codes<8>(f, ab, inv);
+      // block (tid + 256 m) / 4; lanes 16i gather the scale word of blocks 4i..4i+3
+      const uint32_t s1 = __shfl_down_sync(0xFFFFFFFFu, sc, 4);
+      const uint32_t s2 = __shfl_down_sync(0xFFFFFFFFu, sc, 8);
+      const uint32_t s3 = __shfl_down_sync(0xFFFFFFFFu, sc, 12);
+      sw[m] = sc | (s1 << 8) | (s2 << 16) | (s3 << 24);
+      continue;
+    }
     float sdq;
     const uint32_t sc = block_scale(ab, sixG, Gt, sdq);
     cw[m] = block_codes<8>(f, sc, sdq);
@@ -908,10 +1016,14 @@ __global__ void __launch_bounds__(256) k_quant_routes(
       const int c = tid + 256 * m;
       if (c >= NC) break;
       crow[c] = cw[m];
-      if ((lane & 7) == 0)
+      if (FMT == MOE_FMT_MXFP4) {
+        if ((lane & 15) == 0)
+          *reinterpret_cast<uint32_t*>(scales + scale_word(row, c >> 4, KG)) = sw[m];
+      } else if ((lane & 7) == 0) {
         *reinterpret_cast<uint32_t*>(scales + scale_word(row, c >> 3, KG)) = sw[m];
+      }
     }
-    if (tid == 0) G[row] = Gt;
+    if (tid == 0) G[row] = FMT == MOE_FMT_MXFP4 ? 1.0f : Gt;
   }
 }
 
@@ -969,7 +1081,7 @@ struct PrefillWs {
     tiles_gu = take(max_ntiles * (I / kTileM) * 4);
     ctab = take(max_ntiles * 16);  // down: column-tile records
     dcol = take(rows * 8);
-    plan = take(((size_t)3 * (E + 1) + 1) * 4);  // plan_e | plan_slot | plan_begin | plan_n
+    plan = take(((size_t)3 * (E + 1) + 2) * 4);  // plan_e | plan_slot | plan_begin | plan_n
     total = o + 1024;
   }
 };
@@ -1000,7 +1112,8 @@ moe_status nvfp4_quantize(const void* x, int dtype, int T, int K, uint8_t* codes
   if (T == 0) return MOE_OK;
   if (!x || !codes || !scales || !G) return MOE_ERR_INVALID_ARG;
   if (dtype == 0) {
-    auto* kx = K <= 4096 ? k_quant_routes<4096> : k_quant_routes<kQuantXMaxK>;
+    auto* kx = K <= 4096 ? k_quant_routes<4096, MOE_FMT_NVFP4>
+                         : k_quant_routes<kQuantXMaxK, MOE_FMT_NVFP4>;
     kx<<<T, 256, 0, s>>>((const uint16_t*)x, T, K, 1, 1, nullptr, nullptr, nullptr, codes, scales,
                          G);
   } else {
@@ -1024,17 +1137,28 @@ const float* prefill_h_rows(const void* workspace, int T, int H, int I, int E, i
 
 moe_status prefill_setup() { return pf::load_encoder(); }
 
-moe_status prefill_ffn(const moe_ffn_args* a, cudaStream_t s) {
+// part (the layer's own sequence): 0 = the call's whole group; for group 0, 1 =
+// the token quantisation, tile tables, hits and shared expert, 2 = the first
+// misses (whose records the layer gathers meanwhile)
+moe_status prefill_ffn(const moe_ffn_args* a, cudaStream_t s, int part, void (*mark)(void*),
+                       void* mark_ctx) {
+  // the timing hook: a mark after every kernel of the FFN
+  auto marked = [&]() {
+    if (mark) mark(mark_ctx);
+  };
   using namespace pf;
   if (!a->inv || !a->pad_offsets) return MOE_ERR_INVALID_ARG;
-  if (a->H % 256 || a->I % 256 || a->Is % 128 || a->group != 0 || a->I > kQuantHMaxK ||
-      a->H > kQuantXMaxK || a->k > 32)
+  if (a->H % 256 || a->I % 256 || a->Is % 128 || a->I > kQuantHMaxK || a->H > kQuantXMaxK ||
+      a->k > 32)
     return MOE_ERR_UNSUPPORTED;
   moe_status st = load_encoder();
   if (st != MOE_OK) return st;
   const PrefillWs W(a->T, a->H, a->I, a->E, a->k, a->Is);
   uint8_t* ws = (uint8_t*)(((uintptr_t)a->workspace + 1023) & ~(uintptr_t)1023);
-  const RecordLayout L(a->H, a->I);
+  const int fmt = cache_format(a->cache);
+  const bool is_mx = fmt == MOE_FMT_MXFP4;
+  const int blk = fmt_block(fmt);
+  const RecordLayout L(a->H, a->I, fmt);
   const uint8_t* arena = cache_arena(a->cache);
   const uint64_t rb = cache_rec_bytes(a->cache);
   const int n_slots = cache_n_cache(a->cache) + cache_n_stage(a->cache);
@@ -1048,7 +1172,7 @@ moe_status prefill_ffn(const moe_ffn_args* a, cudaStream_t s) {
       (st = make_map(&mxq, ws + W.xq_codes, false, H / 2, W.rows, H / 2, 0, 0)) ||
       (st = make_map(&mhq, ws + W.hq_codes, false, I / 2, W.rows, I / 2, 0, 0)))
     return st;
-  const bool shared = a->Is > 0;
+  const bool shared = a->Is > 0 && a->group == 0 && part != 2;
   if (shared) {
     if ((st = make_map(&msg, a->s_gate, true, H, a->Is, (uint64_t)H * 2, 0, 0)) ||
         (st = make_map(&msu, a->s_up, true, H, a->Is, (uint64_t)H * 2, 0, 0)) ||
@@ -1058,33 +1182,44 @@ moe_status prefill_ffn(const moe_ffn_args* a, cudaStream_t s) {
       return st;
   }
 
-  // routed experts, walked in groups of `grp` (act_list order); 0 = all at once
+  // the call's expert group (group 0: hits and the first misses; group g: the
+  // next n_stage misses), walked in launch groups of `grp` (act_list order);
+  // 0 = all at once
   const int grp = a->prefill_group > 0 ? a->prefill_group : a->E;
   const int max_act = a->T * a->k < a->E ? a->T * a->k : a->E;
+  const int gmax = (a->group == 0 || a->n_stage == 0) ? max_act
+                   : (a->n_stage < max_act ? a->n_stage : max_act);  // experts in the group, at most
   int32_t* plan = (int32_t*)(ws + W.plan);
   int32_t *plan_e = plan, *plan_slot = plan + (a->E + 1), *plan_begin = plan + 2 * (a->E + 1),
           *plan_n = plan + 3 * (a->E + 1);
   uint32_t* tiles_gu = (uint32_t*)(ws + W.tiles_gu);
   int4* ctab = (int4*)(ws + W.ctab);
-  // the tokens, quantised once each into their routes' padded rows; the tile
-  // tables of both GEMMs
-  {
-    auto* kx = H <= 4096 ? k_quant_routes<4096> : k_quant_routes<kQuantXMaxK>;
+  // group 0: the tokens, quantised once each into their routes' padded rows;
+  // the tile tables of both GEMMs for every active expert (the later groups'
+  // calls reuse them: same workspace, same stream)
+  if (a->group == 0 && part != 2) {
+    auto* kx = is_mx ? (H <= 4096 ? k_quant_routes<4096, MOE_FMT_MXFP4>
+                               : k_quant_routes<kQuantXMaxK, MOE_FMT_MXFP4>)
+                  : (H <= 4096 ? k_quant_routes<4096, MOE_FMT_NVFP4>
+                               : k_quant_routes<kQuantXMaxK, MOE_FMT_NVFP4>);
     kx<<<a->T + a->E, 256, 0, s>>>((const uint16_t*)a->x, a->T, H, a->E, a->k, a->inv, a->offsets,
                                    a->pad_offsets, ws + W.xq_codes, ws + W.xq_scales,
                                    (float*)(ws + W.xq_G));
     MOE_CHECK_LAUNCH();
+    marked();
     k_tile_plan<<<1, 1024, 0, s>>>(a->act_list, a->n_act, a->offsets, a->pad_offsets, a->src_slot,
                                   n_slots, a->E, I / kTileM, tiles_gu, ctab, plan_e, plan_slot,
                                   plan_begin, plan_n, a->status);
     MOE_CHECK_LAUNCH();
+    marked();
   }
-  for (int g0 = 0; g0 < max_act; g0 += grp) {
+  for (int g0 = 0; g0 < gmax; g0 += grp) {
     const int g1 = g0 + grp;
     GemmParams gp;
     memset(&gp, 0, sizeof(gp));
     gp.plan_e = plan_e; gp.plan_slot = plan_slot; gp.plan_begin = plan_begin;
     gp.plan_n = plan_n; gp.g0 = g0; gp.g1 = g1;
+    gp.group = a->group; gp.gsize = a->n_stage; gp.part = part;
     gp.offsets = a->offsets; gp.pad_offsets = a->pad_offsets;
     gp.perm = a->perm; gp.gscale = a->gscale; gp.w = a->w; gp.k = a->k; gp.n_slots = n_slots;
     gp.arena = arena; gp.rec_bytes = rb; gp.H = H; gp.status = a->status;
@@ -1092,29 +1227,40 @@ moe_status prefill_ffn(const moe_ffn_args* a, cudaStream_t s) {
     gp.tiles = tiles_gu;
     gp.mtiles = I / kTileM;
     gp.kstages = (H / 2) / kStageKB;
-    gp.kgroups = H / 64;
+    gp.kgroups = H / (4 * blk);  // scale atoms per 128-row tile
     gp.sfa_off0 = L.gate_scales; gp.sfa_off1 = L.up_scales;
     gp.b_scales = ws + W.xq_scales; gp.b_gscale = (const float*)(ws + W.xq_G);
     gp.h32 = (float*)(ws + W.h32); gp.h_ld = I;
-    if ((st = launch_gemm<0, EPI_GU_ROUTED>(mg, mu, mxq, gp, s)) != MOE_OK) return st;
+    st = is_mx ? launch_gemm<2, EPI_GU_ROUTED>(mg, mu, mxq, gp, s)
+               : launch_gemm<0, EPI_GU_ROUTED>(mg, mu, mxq, gp, s);
+    if (st != MOE_OK) return st;
+    marked();
     // h -> NVFP4
-    const int ng = (g1 < max_act ? g1 : max_act) - g0;
-    auto* kq = I <= 2048 ? k_quant_h<2048> : k_quant_h<kQuantHMaxK>;
-    kq<<<dim3(ng, 4), 256, 0, s>>>((const float*)(ws + W.h32), I, g0, g1, plan_e, plan_n,
+    const int ng = (g1 < gmax ? g1 : gmax) - g0;
+    auto* kq = is_mx ? (I <= 2048 ? k_quant_h<2048, MOE_FMT_MXFP4>
+                               : k_quant_h<kQuantHMaxK, MOE_FMT_MXFP4>)
+                  : (I <= 2048 ? k_quant_h<2048, MOE_FMT_NVFP4>
+                               : k_quant_h<kQuantHMaxK, MOE_FMT_NVFP4>);
+    kq<<<dim3(ng, 4), 256, 0, s>>>((const float*)(ws + W.h32), I, g0, g1, a->group, a->n_stage,
+                                  part, plan_e, plan_n,
                                   a->offsets, a->pad_offsets, a->perm, a->w, a->gscale, a->k,
                                   ws + W.hq_codes, ws + W.hq_scales, (float*)(ws + W.hq_G),
                                   (float2*)(ws + W.dcol));
     MOE_CHECK_LAUNCH();
+    marked();
     // down, weighted, added into y_acc
     gp.ctab = ctab;
     gp.dcol = (const float2*)(ws + W.dcol);
     gp.mtiles = H / kTileM;
     gp.kstages = (I / 2) / kStageKB;
-    gp.kgroups = I / 64;
+    gp.kgroups = I / (4 * blk);
     gp.sfa_off0 = L.down_scales; gp.sfa_off1 = 0;
     gp.b_scales = ws + W.hq_scales; gp.b_gscale = (const float*)(ws + W.hq_G);
     gp.y_acc = a->y_acc;
-    if ((st = launch_gemm<0, EPI_DOWN_ROUTED>(md, md, mhq, gp, s)) != MOE_OK) return st;
+    st = is_mx ? launch_gemm<2, EPI_DOWN_ROUTED>(md, md, mhq, gp, s)
+               : launch_gemm<0, EPI_DOWN_ROUTED>(md, md, mhq, gp, s);
+    if (st != MOE_OK) return st;
+    marked();
   }
 
   // shared expert (bf16): y_acc += Wd (silu(Wg x) * Wu x)
@@ -1126,10 +1272,12 @@ moe_status prefill_ffn(const moe_ffn_args* a, cudaStream_t s) {
     gp.kstages = (H * 2) / kStageKB;
     gp.hs = (uint16_t*)(ws + W.hs); gp.hs_ld = a->Is;
     if ((st = launch_gemm<1, EPI_GU_SHARED>(msg, msu, mx, gp, s)) != MOE_OK) return st;
+    marked();
     gp.mtiles = H / kTileM;
     gp.kstages = (a->Is * 2) / kStageKB;
     gp.y_acc = a->y_acc;
     if ((st = launch_gemm<1, EPI_DOWN_SHARED>(msd, msd, mhs, gp, s)) != MOE_OK) return st;
+    marked();
   }
   return MOE_OK;
 }

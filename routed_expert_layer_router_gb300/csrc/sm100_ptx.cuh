@@ -163,6 +163,18 @@ __device__ __forceinline__ void mma_nvf4(uint32_t d, uint64_t adesc, uint64_t bd
       " [%0], %1, %2, %3, [%4], [%5], p;\n}" ::"r"(d),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"((uint32_t)accumulate));
 }
+// D[tmem] (+)= (A x SFA) * (B x SFB)^T, E2M1 inputs, UE8M0 scales per 32
+// values: each 32-bit scale column word holds four blocks' scales (128
+// values); the instruction descriptor's scale-factor IDs (bits 29-30 for A,
+// 4-5 for B: 0 or 2) pick the two bytes this K = 64 step uses
+__device__ __forceinline__ void mma_mxf4(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t sfa, uint32_t sfb, bool accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::2X"
+      " [%0], %1, %2, %3, [%4], [%5], p;\n}" ::"r"(d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"((uint32_t)accumulate));
+}
 // 32 rows x 128 bits of shared memory to tensor memory, copied to all four
 // 32-lane quarters
 __device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {

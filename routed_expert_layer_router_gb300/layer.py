@@ -81,9 +81,10 @@ class ExpertCache:
     """expcache handle: n_cache_slots HBM cache slots + n_stage staging slots."""
 
     def __init__(self, L, E, H, I, n_cache_slots, n_stage=0, layer_slots=None,
-                 host_arena: HostArena | None = None, host_index=None):
-        self.L, self.E, self.H, self.I = L, E, H, I
-        self.record_bytes = moe.moe_record_bytes(H, I)
+                 host_arena: HostArena | None = None, host_index=None,
+                 fmt: int = moe.MOE_FMT_NVFP4):
+        self.L, self.E, self.H, self.I, self.fmt = L, E, H, I, fmt
+        self.record_bytes = moe.moe_record_bytes(H, I, fmt)
         self.n_cache_slots, self.n_stage = n_cache_slots, n_stage
         self._layer_slots = None if layer_slots is None else np.ascontiguousarray(layer_slots, np.int32)
         self._host_index = None if host_index is None else np.ascontiguousarray(host_index, np.int64)
@@ -95,6 +96,7 @@ class ExpertCache:
         d.host_arena = host_arena.ptr if host_arena is not None else None
         d.host_arena_records = host_arena.n_records if host_arena is not None else 0
         d.host_index = _ptr(self._host_index) or None
+        d.format = fmt
         self.handle = moe.expcache_create(d)
 
     def slot_ptr(self, slot: int) -> int:

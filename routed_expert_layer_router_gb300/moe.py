@@ -37,7 +37,7 @@ class moe_route_args(ctypes.Structure):
 class expcache_desc(ctypes.Structure):
     _fields_ = [("L", i32), ("E", i32), ("H", i32), ("I", i32), ("n_cache_slots", i32),
                 ("layer_slots", vp), ("n_stage", i32), ("host_arena", vp),
-                ("host_arena_records", u64), ("host_index", vp)]
+                ("host_arena_records", u64), ("host_index", vp), ("format", i32)]
 
 
 class moe_ffn_args(ctypes.Structure):
@@ -67,7 +67,7 @@ class moe_layer_desc(ctypes.Structure):
 SIGNATURES = {
     "moe_status_string": (ctypes.c_char_p, [i32]),
     "moe_abi_version": (i32, []),
-    "moe_record_bytes": (u64, [i32, i32]),
+    "moe_record_bytes": (u64, [i32, i32, i32]),
     "moe_route_workspace_bytes": (sz, [i32, i32]),
     "moe_route": (i32, [ctypes.POINTER(moe_route_args), vp]),
     "moe_permute": (i32, [vp, i32, i32, i32, vp, vp, vp, vp, vp, i32, vp, vp]),
@@ -127,8 +127,11 @@ def moe_abi_version() -> int:
     return lib().moe_abi_version()
 
 
-def moe_record_bytes(H: int, I: int) -> int:
-    return int(lib().moe_record_bytes(H, I))
+MOE_FMT_NVFP4, MOE_FMT_MXFP4 = 0, 1
+
+
+def moe_record_bytes(H: int, I: int, fmt: int = MOE_FMT_NVFP4) -> int:
+    return int(lib().moe_record_bytes(H, I, fmt))
 
 
 def moe_route_workspace_bytes(T: int, E: int) -> int:

@@ -56,13 +56,13 @@ def oracle_layer(dw, layer: int, x: np.ndarray, mode: int = 0, record_cache=None
     rl = dw.record_layer[layer] if dw.record_layer else layer
     missing = [e for e in need if (rl, e) not in cache]
     if missing:
-        recs = gen.expert_records(wl.seed, rl, missing, wl.H, wl.I)
+        recs = gen.expert_records(wl.seed, rl, missing, wl.H, wl.I, fmt=wl.fmt)
         for e, r in zip(missing, recs):
             cache[(rl, e)] = r
     records = {e: cache[(rl, e)] for e in need}
     y, ids2, w2, p2, bound = oracle.layer_forward(x, wl.H, wl.I, wl.E, wl.k, Wr, bias, records,
                                                   dw.gscale_host[layer], shared_w=sh, mode=mode,
-                                                  return_bound=True)
+                                                  return_bound=True, fmt=wl.fmt)
     if return_bound:
         return y, ids2, w2, p2, bound
     return y, ids2, w2, p2
@@ -109,9 +109,9 @@ def prefill_clean(dw, layer: int, x: np.ndarray, ids: np.ndarray) -> np.ndarray:
     wl = dw.wl
     rl = dw.record_layer[layer] if dw.record_layer else layer
     need = sorted(set(np.asarray(ids).ravel().tolist()))
-    recs = dict(zip(need, gen.expert_records(wl.seed, rl, need, wl.H, wl.I)))
+    recs = dict(zip(need, gen.expert_records(wl.seed, rl, need, wl.H, wl.I, fmt=wl.fmt)))
     return oracle.prefill_near_boundary(x, wl.H, wl.I, wl.k, ids, recs,
-                                        dw.gscale_host[layer]) == 0
+                                        dw.gscale_host[layer], fmt=wl.fmt) == 0
 
 
 _E2M1 = None
@@ -125,6 +125,15 @@ def nvfp4_dequant(codes, scales, G):
                  np.array([oracle.e4m3(b) for b in range(256)]))
     c = np.stack([codes & 15, codes >> 4], 1).ravel()
     return _E2M1[0][c] * np.repeat(_E2M1[1][scales], 16) * G
+
+
+def mxfp4_dequant(codes, scales):
+    """Values of an MXFP4-quantised row (oracle.mxfp4_quant layout), fp64."""
+    global _E2M1
+    if _E2M1 is None:
+        nvfp4_dequant(np.zeros(8, np.uint8), np.zeros(1, np.uint8), 1.0)
+    c = np.stack([codes & 15, codes >> 4], 1).ravel()
+    return _E2M1[0][c] * np.repeat([oracle.e8m0(int(b)) for b in scales], 32)
 
 
 def check_prefill_h(dw, layer: int, x: np.ndarray, h_gpu: np.ndarray, perm: np.ndarray,
@@ -142,19 +151,24 @@ def check_prefill_h(dw, layer: int, x: np.ndarray, h_gpu: np.ndarray, perm: np.n
     ids, *_ = oracle.route(x[tokens], Wr, bias, k)
     rl = dw.record_layer[layer] if dw.record_layer else layer
     need = sorted(set(ids.ravel().tolist()))
-    recs = dict(zip(need, gen.expert_records(wl.seed, rl, need, H, I)))
+    recs = dict(zip(need, gen.expert_records(wl.seed, rl, need, H, I, fmt=wl.fmt)))
     pos = np.empty(perm.size, np.int64)
     pos[perm] = np.arange(perm.size)  # route r -> its expert-sorted position
     worst = 0.0
+    mx = wl.fmt == oracle.MXFP4
     for i, t in enumerate(tokens):
         xf = bf16_to_f64(x[t]).astype(np.float32)
-        xq = nvfp4_dequant(*oracle.nvfp4_quant(xf))
+        xq = mxfp4_dequant(*oracle.mxfp4_quant(xf)) if mx else nvfp4_dequant(*oracle.nvfp4_quant(xf))
         for j in range(k):
             e = int(ids[i, j])
-            h_ref = oracle.expert_h(recs[e], H, I, dw.gscale_host[layer][e], xq)
+            h_ref = oracle.expert_h(recs[e], H, I, dw.gscale_host[layer][e], xq, fmt=wl.fmt)
             hf = h_ref.astype(np.float32)
-            _, sc, G = oracle.nvfp4_quant(hf)
-            sg = np.repeat(np.array([oracle.e4m3(int(b)) for b in sc]) * G, 16)
+            if mx:
+                _, sc = oracle.mxfp4_quant(hf)
+                sg = np.repeat(np.array([oracle.e8m0(int(b)) for b in sc]), 32)
+            else:
+                _, sc, G = oracle.nvfp4_quant(hf)
+                sg = np.repeat(np.array([oracle.e4m3(int(b)) for b in sc]) * G, 16)
             sg[sg == 0] = np.inf
             dq = np.abs(h_gpu[pos[t * k + j]].astype(np.float64) - h_ref) / sg
             worst = max(worst, float(dq.max()))
@@ -196,3 +210,52 @@ def check_router(dbg: dict, ids_ref, w_ref, p_ref):
     p = dbg["p_sel"].cpu().numpy().astype(np.float64)
     assert np.all(np.abs(w - w_ref) <= PROB_RTOL * np.abs(w_ref)), np.abs(w / w_ref - 1).max()
     assert np.all(np.abs(p - p_ref) <= PROB_RTOL * np.abs(p_ref)), np.abs(p / p_ref - 1).max()
+
+
+def ffn_fp32(dw, layer, x):
+    """The layer's output before the final bf16 rounding: the individual ABI
+    calls (route, permute, lookup, expert FFN) with test-owned buffers, then
+    sum_j o_route + o_shared in fp64 on the host (comparison only)."""
+    from routed_expert_layer_router_gb300 import moe
+    wl = dw.wl
+    T, H, I, E, k, Is = x.shape[0], wl.H, wl.I, wl.E, wl.k, wl.Is
+    s = torch.cuda.current_stream().cuda_stream
+    i32, f32 = torch.int32, torch.float32
+    z = {n: torch.zeros(sz, dtype=dt, device="cuda") for n, sz, dt in (
+        ("ids", T * k, i32), ("w", T * k, f32), ("p", T * k, f32), ("lg", T * E, f32),
+        ("counts", E, i32), ("off", E + 1, i32), ("perm", T * k, i32), ("inv", T * k, i32),
+        ("src", E, i32), ("act", E, i32), ("nact", 2, i32), ("miss", E, i32), ("nmiss", 1, i32),
+        ("st", 1, i32), ("o", T * k * H, f32), ("os", T * H, f32))}
+    xd = to_dev_bf16(x)
+    ra = moe.moe_route_args()
+    ra.x, ra.w_router = xd.data_ptr(), dw.w_router[layer].data_ptr()
+    ra.bias = dw.bias[layer].data_ptr() if dw.bias[layer] is not None else None
+    ra.T, ra.H, ra.E, ra.k = T, H, E, k
+    ra.ids, ra.w, ra.p_sel, ra.logits = (z[n].data_ptr() for n in ("ids", "w", "p", "lg"))
+    moe.moe_route(ra, s)
+    moe.moe_permute(z["ids"].data_ptr(), T, k, E, z["counts"].data_ptr(), z["off"].data_ptr(),
+                    z["perm"].data_ptr(), z["inv"].data_ptr(), 0, 128, z["st"].data_ptr(), s)
+    moe.expcache_lookup(dw.cache.handle, layer, z["counts"].data_ptr(), z["src"].data_ptr(),
+                        z["act"].data_ptr(), z["nact"].data_ptr(), z["miss"].data_ptr(),
+                        z["nmiss"].data_ptr(), z["st"].data_ptr(), s)
+    ws_b = moe.moe_ffn_workspace_bytes(0, T, H, I, E, k, Is)
+    ws = torch.empty(ws_b, dtype=torch.uint8, device="cuda")
+    fa = moe.moe_ffn_args()
+    fa.mode, fa.stages, fa.T, fa.H, fa.I, fa.E, fa.k = 0, 3, T, H, I, E, k
+    fa.x, fa.cache, fa.gscale = xd.data_ptr(), dw.cache.handle, dw.gscale[layer].data_ptr()
+    fa.src_slot, fa.act_list, fa.n_act = (z[n].data_ptr() for n in ("src", "act", "nact"))
+    fa.offsets, fa.perm, fa.w = z["off"].data_ptr(), z["perm"].data_ptr(), z["w"].data_ptr()
+    fa.group, fa.n_stage, fa.Is = 0, dw.cache.n_stage, Is
+    if Is:
+        fa.s_gate, fa.s_up, fa.s_down = (t.data_ptr() for t in dw.shared[layer])
+    fa.o_route, fa.o_shared = z["o"].data_ptr(), z["os"].data_ptr() if Is else None
+    fa.workspace, fa.workspace_bytes, fa.status = ws.data_ptr(), ws_b, z["st"].data_ptr()
+    moe.moe_expert_ffn(fa, s)
+    torch.cuda.synchronize()
+    assert z["st"].item() == 0
+    o = z["o"].double().view(T * k, H).cpu().numpy()
+    inv = z["inv"].cpu().numpy()
+    y = np.stack([o[inv[t * k:(t + 1) * k]].sum(0) for t in range(T)])
+    if Is:
+        y += z["os"].double().view(T, H).cpu().numpy()
+    return y

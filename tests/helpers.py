@@ -86,3 +86,56 @@ def nvfp4_exact_x(H, T, seed=0):
                 blk[1] = 1.5
             out[t, b * 16:(b + 1) * 16] = blk
     return f32_to_bf16(out)
+
+
+E8M0_ONE = 127        # 2^0
+E8M0_SIXTEEN = 131    # 2^4
+E8M0_2M6 = 121        # 2^-6
+
+
+def identity_record_mx(H, I):
+    """The identity expert in MXFP4 (blocks of 32, E8M0 scales): the same
+    construction as identity_record - gate row i = 64 e_0 (code 4.0, block
+    scale 16), up row i = e_{16+i} (code 1.0, scale 1), down row 16+i = e_i / 64
+    (code 1.0, scale 2^-6) - so that y[16+i] = x[16+i] when x[0] = 1 and
+    g = (1, 1, 1)."""
+    assert I <= H - 16
+    rb = 3 * I * H // 2 + 3 * I * H // 32
+    rec = np.zeros(rb, np.uint8)
+    codes = [0, I * H // 2, I * H]
+    scales = [3 * I * H // 2 + m * (I * H // 32) for m in range(3)]
+    KBh, KBi = H // 32, I // 32
+    for m, R, KB, sc in ((0, I, KBh, E8M0_ONE), (1, I, KBh, E8M0_ONE), (2, H, KBi, E8M0_2M6)):
+        for r in range(R):
+            for kb in range(KB):
+                rec[scales[m] + _scale_pos(r, kb, KB)] = sc
+
+    def put(m, r, c, code, K):
+        b = codes[m] + r * (K // 2) + c // 2
+        rec[b] |= (code << 4) if (c & 1) else code
+
+    for i in range(I):
+        put(0, i, 0, E2M1_FOUR, H)
+        rec[scales[0] + _scale_pos(i, 0, KBh)] = E8M0_SIXTEEN
+        put(1, i, 16 + i, E2M1_ONE, H)
+        put(2, 16 + i, i, E2M1_ONE, I)
+    return rec
+
+
+def mxfp4_exact_x(H, T, seed=0):
+    """bf16 activations that MXFP4 quantisation reproduces exactly, and whose
+    shift by 16 values (the identity expert's h = 64 x[16:]) does too: every
+    value is an E2M1 magnitude times 2^-1 and every run of 16 values holds a
+    +-3 (= 6 x 2^-1), so each block of 32 at any 16-value offset has the
+    shared exponent -1; x[0] = 1."""
+    rng = np.random.default_rng(seed)
+    out = np.empty((T, H), np.float32)
+    for t in range(T):
+        for h in range(H // 16):
+            mags = rng.choice(_E2M1[:7], 16) * rng.choice([-1, 1], 16)
+            mags[rng.integers(16)] = 6.0 * rng.choice([-1, 1])
+            out[t, h * 16:(h + 1) * 16] = mags * 0.5
+        out[t, 0] = 1.0
+        if not np.any(np.abs(out[t, :16]) == 3.0):
+            out[t, 1] = 3.0
+    return f32_to_bf16(out)

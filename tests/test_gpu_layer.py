@@ -8,7 +8,7 @@ import torch
 
 import gen
 import oracle
-from tests.gpu_common import (check_outputs, check_permutation, check_router, draw_tokens,
+from tests.gpu_common import (check_outputs, check_permutation, check_router, draw_tokens, ffn_fp32,
                               host_inputs, oracle_layer, to_dev_bf16, y_to_f64)
 from tests.helpers import TOL, identity_record, identity_x, bf16_to_f64
 
@@ -79,55 +79,6 @@ def test_decode_layer_parity(decode):
     assert dw.moe_layers[0].read_status() == 0
 
 
-def _ffn_fp32(dw, layer, x):
-    """The layer's output before the final bf16 rounding: the individual ABI
-    calls (route, permute, lookup, expert FFN) with test-owned buffers, then
-    sum_j o_route + o_shared in fp64 on the host (comparison only)."""
-    from routed_expert_layer_router_gb300 import moe
-    wl = dw.wl
-    T, H, I, E, k, Is = x.shape[0], wl.H, wl.I, wl.E, wl.k, wl.Is
-    s = torch.cuda.current_stream().cuda_stream
-    i32, f32 = torch.int32, torch.float32
-    z = {n: torch.zeros(sz, dtype=dt, device="cuda") for n, sz, dt in (
-        ("ids", T * k, i32), ("w", T * k, f32), ("p", T * k, f32), ("lg", T * E, f32),
-        ("counts", E, i32), ("off", E + 1, i32), ("perm", T * k, i32), ("inv", T * k, i32),
-        ("src", E, i32), ("act", E, i32), ("nact", 2, i32), ("miss", E, i32), ("nmiss", 1, i32),
-        ("st", 1, i32), ("o", T * k * H, f32), ("os", T * H, f32))}
-    xd = to_dev_bf16(x)
-    ra = moe.moe_route_args()
-    ra.x, ra.w_router = xd.data_ptr(), dw.w_router[layer].data_ptr()
-    ra.bias = dw.bias[layer].data_ptr() if dw.bias[layer] is not None else None
-    ra.T, ra.H, ra.E, ra.k = T, H, E, k
-    ra.ids, ra.w, ra.p_sel, ra.logits = (z[n].data_ptr() for n in ("ids", "w", "p", "lg"))
-    moe.moe_route(ra, s)
-    moe.moe_permute(z["ids"].data_ptr(), T, k, E, z["counts"].data_ptr(), z["off"].data_ptr(),
-                    z["perm"].data_ptr(), z["inv"].data_ptr(), 0, 128, z["st"].data_ptr(), s)
-    moe.expcache_lookup(dw.cache.handle, layer, z["counts"].data_ptr(), z["src"].data_ptr(),
-                        z["act"].data_ptr(), z["nact"].data_ptr(), z["miss"].data_ptr(),
-                        z["nmiss"].data_ptr(), z["st"].data_ptr(), s)
-    ws_b = moe.moe_ffn_workspace_bytes(0, T, H, I, E, k, Is)
-    ws = torch.empty(ws_b, dtype=torch.uint8, device="cuda")
-    fa = moe.moe_ffn_args()
-    fa.mode, fa.stages, fa.T, fa.H, fa.I, fa.E, fa.k = 0, 3, T, H, I, E, k
-    fa.x, fa.cache, fa.gscale = xd.data_ptr(), dw.cache.handle, dw.gscale[layer].data_ptr()
-    fa.src_slot, fa.act_list, fa.n_act = (z[n].data_ptr() for n in ("src", "act", "nact"))
-    fa.offsets, fa.perm, fa.w = z["off"].data_ptr(), z["perm"].data_ptr(), z["w"].data_ptr()
-    fa.group, fa.n_stage, fa.Is = 0, dw.cache.n_stage, Is
-    if Is:
-        fa.s_gate, fa.s_up, fa.s_down = (t.data_ptr() for t in dw.shared[layer])
-    fa.o_route, fa.o_shared = z["o"].data_ptr(), z["os"].data_ptr() if Is else None
-    fa.workspace, fa.workspace_bytes, fa.status = ws.data_ptr(), ws_b, z["st"].data_ptr()
-    moe.moe_expert_ffn(fa, s)
-    torch.cuda.synchronize()
-    assert z["st"].item() == 0
-    o = z["o"].double().view(T * k, H).cpu().numpy()
-    inv = z["inv"].cpu().numpy()
-    y = np.stack([o[inv[t * k:(t + 1) * k]].sum(0) for t in range(T)])
-    if Is:
-        y += z["os"].double().view(T, H).cpu().numpy()
-    return y
-
-
 def test_decode_negative_controls_are_far_from_gpu(decode):
     """Per-substep separation: the GPU's fp32 layer output (before the bf16
     rounding) is at least 100x closer to the oracle than to an oracle with a
@@ -135,7 +86,7 @@ def test_decode_negative_controls_are_far_from_gpu(decode):
     dw = decode
     Wr, bias, sh = host_inputs(dw, 0)
     x, _ = draw_tokens(dw.wl, 0, 1, Wr, bias, draw0=500)
-    y = _ffn_fp32(dw, 0, x)
+    y = ffn_fp32(dw, 0, x)
     recs = {}
     y_ref, *_ = oracle_layer(dw, 0, x, record_cache=recs)
     base = np.abs(y - y_ref).max()

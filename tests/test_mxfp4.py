@@ -174,3 +174,17 @@ def test_mx_nibble_order_negative_control():
         oracle.lib().oracle_set_defect(0)
     rms = np.sqrt(np.mean(o ** 2))
     assert np.abs(o_bad - o).max() > 100 * 2e-2 * rms
+
+
+@pytest.mark.parametrize("act_quant", [False, True])
+def test_mx_identity_expert_returns_its_input(act_quant):
+    """The bit-built MXFP4 identity expert maps x to y[16+i] = x[16+i] exactly,
+    in the decode numerics and in the prefill numerics (MXFP4 activations)."""
+    from tests.helpers import bf16_to_f64, identity_record_mx, mxfp4_exact_x
+    H, I = 512, 256
+    rec = identity_record_mx(H, I)
+    for xv in bf16_to_f64(mxfp4_exact_x(H, 4, seed=3)):
+        o = oracle.expert(rec, H, I, np.ones(3, np.float32), xv, act_quant=act_quant,
+                          fmt=oracle.MXFP4)
+        assert np.array_equal(o[16:16 + I], xv[16:16 + I])
+        assert not o[:16].any() and not o[16 + I:].any()
