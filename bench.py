@@ -56,7 +56,7 @@ FP4_OVER_BF16 = 6.0  # nominal dense FP4 / dense bf16 tensor throughput (13.5 / 
 # DRAM bytes (read + write) of one launch of the roofline kernel on the full decode
 # layer, from one ncu capture of the current kernel; None whenever the kernel has
 # changed since it was captured
-GU_TRAFFIC = None
+GU_TRAFFIC = 138_486_784 + 3_873_024
 GU_TRAFFIC_SOURCE = "ncu dram__bytes_read.sum + dram__bytes_write.sum, one launch, full decode layer"
 
 
@@ -264,12 +264,15 @@ class ExplicitLayer:
     def layer_launches(self):
         """Kernels one decode moe_layer_forward launches for this layer and T:
         router + permutation + slot lookup (one kernel for T <= 8, else the
-        router GEMM, top-k and the permutation), per expert group the gather
-        (if staging) and the one-launch FFN, and the combine unless a single
-        group's FFN writes y."""
+        router GEMM, top-k and the permutation), then with staging slots and
+        one group the FFN kernel that gathers the misses itself, otherwise per
+        group the gather (if staging) and the gate/up and down kernels, and the
+        combine unless a single group's down kernel writes y."""
         S = self.dw.cache.n_stage
         route = 1 if self.T <= 8 else 3
-        return route + self.groups * (1 + (1 if S > 0 else 0)) + (0 if self.groups == 1 else 1)
+        if S > 0 and self.groups == 1:
+            return route + 1
+        return route + self.groups * (2 + (1 if S > 0 else 0)) + (0 if self.groups == 1 else 1)
 
 
 # --------------------------------------------------------------- decode
@@ -331,23 +334,23 @@ def bench_decode(args, torch, moe, gen, gd, dev, rank, world, local_rank, peaks,
 
     # ---- pass 2: events at the layer's own launch boundaries (its timing hook),
     # eager launches, one step at a time: router kernel (with the permutation,
-    # lookup and the shared expert's gate/up), then the one-launch FFN (routed
-    # gate/up and down, the shared expert's down, the combine)
-    hev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    # lookup and the shared expert's gate/up), gate/up kernel (routed, with the
+    # shared expert's down), down kernel (routed, with the combine)
+    hev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
     for e in hev:  # torch creates the CUDA event on its first record
         e.record(stream)
     torch.cuda.synchronize()
     moe.moe_layer_set_timing(layer.handle, [e.cuda_event for e in hev])
-    k_ms = [[], []]
+    k_ms = [[], [], []]
     for j in range(args.steps):
         flush()
         layer.forward(xs[args.warmup + j:args.warmup + j + 1],
                       ys[args.warmup + j:args.warmup + j + 1], stream=stream)
-        hev[2].synchronize()
-        for i in range(2):
+        hev[3].synchronize()
+        for i in range(3):
             k_ms[i].append(hev[i].elapsed_time(hev[i + 1]))
     moe.moe_layer_set_timing(layer.handle, [])
-    rt_ms, ffn_ms = (statistics.mean(v) for v in k_ms)
+    rt_ms, gu_ms, dn_ms = (statistics.mean(v) for v in k_ms)
     assert layer.read_status() == 0, "device status set during the bench"
 
     # ---- e2e: the public call with host buffers
@@ -381,34 +384,42 @@ def bench_decode(args, torch, moe, gen, gd, dev, rank, world, local_rank, peaks,
         torch.distributed.all_reduce(tot, op=torch.distributed.ReduceOp.MAX)
     total_ms = float(tot.item())
     rb = gen.record_bytes(H, I, wl.fmt)
-    # algorithmic bytes of the two kernels of the one-token sequence: the router
-    # kernel (router weights, the shared expert's gate/up, x, h_shared, logits)
-    # and the FFN (k whole records, the shared down, x, h written and read,
-    # the routes' and shared outputs written and read by the combine, y)
+    # algorithmic bytes of the three kernels of the one-token sequence: the
+    # router kernel (router weights, the shared expert's gate/up, x, h_shared,
+    # logits), gate/up (the k records' gate and up rows with their scales, the
+    # shared down, x, h written, h_shared read, o_shared written), down (the k
+    # records' down rows and scales, h read, o_route written, the combine's
+    # reads of o_route and o_shared, y)
+    blk = 32 if wl.fmt == gen.MXFP4 else 16
     rt_bytes = E * H * 4 + 2 * Is * H * 2 + T * H * 2 + T * Is * 4 + T * E * 4
-    ffn_bytes = (k * rb + H * Is * 2 + T * H * 2 + 2 * T * k * I * 4 + T * Is * 4
-                 + 2 * (T * k + T) * H * 4 + T * H * 2)
+    gu_bytes = (k * (2 * I * H // 2 + 2 * I * H // blk) + H * Is * 2 + T * H * 2
+                + T * k * I * 4 + T * Is * 4 + T * H * 4)
+    dn_bytes = (k * (H * I // 2 + H * I // blk) + T * k * I * 4 + (T * k + T) * H * 4 * 2
+                + T * H * 2)
     step_bytes = k * rb + 3 * Is * H * 2 + E * H * 4 + 2 * T * H * 2
     rt_gbs = rt_bytes / (rt_ms * 1e-3) / 1e9
-    ffn_gbs = ffn_bytes / (ffn_ms * 1e-3) / 1e9
+    gu_gbs = gu_bytes / (gu_ms * 1e-3) / 1e9
+    dn_gbs = dn_bytes / (dn_ms * 1e-3) / 1e9
     hbm = peaks["hbm_gbs"]
     res = {
         "value": round(world * args.steps * T / (total_ms * 1e-3), 2),
         "ms_per_step": round(total_ms / args.steps, 5),
         "roofline": {"bound": "hbm",
-                     "kernel": "k_decode_ffn as the layer launches it for one token (routed "
-                               "NVFP4 gate/up, SiLU*mul and down of the 8 experts, the bf16 "
-                               "shared expert's down, the weighted combine)",
-                     "achieved": round(ffn_gbs, 1), "peak": hbm, "unit": "GB/s",
-                     "frac": round(ffn_gbs / hbm, 4), "traffic": GU_TRAFFIC,
+                     "kernel": "k_decode_gu as the layer launches it for one token (routed "
+                               "gate/up of the 8 experts, SiLU*mul, + the bf16 shared "
+                               "expert's down)",
+                     "achieved": round(gu_gbs, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(gu_gbs / hbm, 4), "traffic": GU_TRAFFIC,
                      "traffic_source": GU_TRAFFIC_SOURCE,
-                     "bytes_per_launch": ffn_bytes, "avg_launch_ms": round(ffn_ms, 5)},
+                     "bytes_per_launch": gu_bytes, "avg_launch_ms": round(gu_ms, 5)},
         "kernels": {
             "k_route_permute_small": {"ms": round(rt_ms, 5), "GB/s": round(rt_gbs, 1),
                                       "frac_hbm": round(rt_gbs / hbm, 4),
                                       "bytes": rt_bytes},
-            "k_decode_ffn": {"ms": round(ffn_ms, 5), "GB/s": round(ffn_gbs, 1),
-                             "frac_hbm": round(ffn_gbs / hbm, 4), "bytes": ffn_bytes},
+            "k_decode_gu": {"ms": round(gu_ms, 5), "GB/s": round(gu_gbs, 1),
+                            "frac_hbm": round(gu_gbs / hbm, 4), "bytes": gu_bytes},
+            "k_decode_down": {"ms": round(dn_ms, 5), "GB/s": round(dn_gbs, 1),
+                              "frac_hbm": round(dn_gbs / hbm, 4), "bytes": dn_bytes},
             "timing": "the layer's timing hook: events at its launch boundaries, eager "
                       "launches, L2 flushed before each step",
             "step_bytes": step_bytes,
@@ -453,7 +464,7 @@ PREFILL_GEMM_WL = None
 def bench_prefill(args, torch, moe, gen, gd, dev, peaks, group=None, wl=None, label=None):
     custom = wl is not None
     wl = wl if custom else gen.WORKLOADS["prefill"]
-    if args.prefill_experts > 0 and not custom:
+    if args.prefill_experts > 0:
         # profiler captures only: fewer experts and proportionally fewer tokens,
         # the same tokens per expert (tile shapes) and kernels
         E2 = args.prefill_experts
@@ -861,7 +872,7 @@ def bench_multilayer(args, torch, moe, gen, gd, dev, name, link_gbs, spares=0, s
     # one staging group: the FFN kernel gathers the misses itself (one mark);
     # else per group a gather and the FFN, then the combine
     ffn_gathers = S > 0 and groups == 1
-    marks = first + (1 if ffn_gathers else groups * (2 if S > 0 else 1)) + (1 if groups > 1 else 0)
+    marks = first + (1 if ffn_gathers else groups * (3 if S > 0 else 2)) + (1 if groups > 1 else 0)
     hev = [[torch.cuda.Event(enable_timing=True) for _ in range(marks)] for _ in range(L)]
     for e in (e for row in hev for e in row):  # torch creates the CUDA event on its first record
         e.record(stream)
@@ -890,7 +901,7 @@ def bench_multilayer(args, torch, moe, gen, gd, dev, name, link_gbs, spares=0, s
                 fill_ms += hev[l][first - 1].elapsed_time(hev[l][first])
             else:
                 for g in range(groups):
-                    i = first + g * 2
+                    i = first + g * 3
                     fill_ms += hev[l][i - 1].elapsed_time(hev[l][i])
         for l in range(L):
             # n_act of the layer's last forward: [active, hits]
@@ -939,7 +950,7 @@ def bench_multilayer(args, torch, moe, gen, gd, dev, name, link_gbs, spares=0, s
         # the gather pass's own step time and its launch-step intervals, per
         # layer (us): router (+ permutation, + the adaptive cache's step for up
         # to 8 tokens), the policy step (more tokens), then the FFN with its
-        # gather (one staging group) or per group the gather and the FFN
+        # gather (one staging group) or per group the gather, gate/up and down
         res["gather_pass"] = {"ms_per_step": round(hook_ms / steps, 4),
                               "ms_per_step_median": round(statistics.median(pass_ms), 4),
                               "us_per_layer": [round(v * 1e3 / (steps * L), 1) for v in part_ms]}

@@ -748,8 +748,9 @@ ORC_API int oracle_layer_forward(const uint16_t* x, int T, int H, int I, int fmt
       free(ids); free(w); free(p); free(weff); free(keep);
       return 2;
     }
-  /* tokens are independent: one per thread (each token's own steps in order) */
-  #pragma omp parallel for schedule(dynamic, 1)
+  /* tokens are independent: one per thread (each token's own steps in order);
+   * a single token keeps the threads for its row loops instead */
+  #pragma omp parallel for schedule(dynamic, 1) if (T > 1)
   for (int t = 0; t < T; ++t) {
     double* xd = (double*)malloc(sizeof(double) * (size_t)H);
     double* xq = (double*)malloc(sizeof(double) * (size_t)H);
