@@ -398,7 +398,10 @@ __device__ __forceinline__ void gu_fetch(const uint8_t* rec, const RecordLayout&
 }
 
 // `first` holds the step hk = lane, fetched by the caller (before it staged
-// the tokens, so that those loads were already in flight)
+// the tokens, so that those loads were already in flight).  The next step's
+// loads are issued after this step's arithmetic, into the same registers: a
+// second register set (loads issued before the arithmetic) needed more than
+// the 128 registers a thread has at two CTAs per SM and spilled.
 template <int M, int FMT>
 __device__ void warp_gu_fp4(const uint8_t* rec, const RecordLayout& L, int H, int rt, int m0,
                             const __half* xs, float accg[4][M], float accu[4][M],
@@ -427,9 +430,7 @@ __device__ void warp_gu_fp4(const uint8_t* rec, const RecordLayout& L, int H, in
     }
   };
   for (int hk = lane; hk < nhk; hk += 32) {
-    uint4 ng[4], nu[4], nsg, nsu;
     const bool more = hk + 32 < nhk;
-    if (more) fetch(hk + 32, ng, nu, nsg, nsu);
     uint32_t xh[M * 16];
     load_xh<M>(xs, nhk, hk, xh);
 #pragma unroll
@@ -437,15 +438,7 @@ __device__ void warp_gu_fp4(const uint8_t* rec, const RecordLayout& L, int H, in
       row_step<M, FMT>(cg[m1], sg, m1, hk, xh, accg[m1]);
       row_step<M, FMT>(cu[m1], su, m1, hk, xh, accu[m1]);
     }
-    if (more) {
-#pragma unroll
-      for (int m1 = 0; m1 < 4; ++m1) {
-        cg[m1] = ng[m1];
-        cu[m1] = nu[m1];
-      }
-      sg = nsg;
-      su = nsu;
-    }
+    if (more) fetch(hk + 32, cg, cu, sg, su);
   }
 #pragma unroll
   for (int m1 = 0; m1 < 4; ++m1)
