@@ -719,27 +719,39 @@ def bench_route(args, torch, moe, gen, dev, T=4096):
     ids = torch.empty((T, k), dtype=torch.int32, device=dev)
     w = torch.empty((T, k), dtype=torch.float32, device=dev)
     lg = torch.empty((T, E), dtype=torch.float32, device=dev)
-    a = moe.moe_route_args()
-    a.w_router, a.T, a.H, a.E, a.k = wr.data_ptr(), T, H, E, k
-    a.ids, a.w, a.logits = ids.data_ptr(), w.data_ptr(), lg.data_ptr()
+    split = torch.empty(moe.moe_route_split_bytes(E, H), dtype=torch.uint8, device=dev)
     flush = L2Flush(torch, args.flush_mb, dev)
-    for i in range(args.warmup):
-        a.x = xs[i].data_ptr()
-        moe.moe_route(a, sp)
-    ev = _events(torch, args.prefill_steps)
-    torch.cuda.synchronize()
-    for j in range(args.prefill_steps):
-        flush()
-        a.x = xs[args.warmup + j].data_ptr()
-        ev[j][0].record(stream)
-        moe.moe_route(a, sp)
-        ev[j][1].record(stream)
-    torch.cuda.synchronize()
-    us = sum(x.elapsed_time(y) for x, y in ev) / args.prefill_steps * 1e3
+
+    def timed(use_split):
+        a = moe.moe_route_args()
+        a.w_router, a.T, a.H, a.E, a.k = wr.data_ptr(), T, H, E, k
+        a.ids, a.w, a.logits = ids.data_ptr(), w.data_ptr(), lg.data_ptr()
+        if use_split:
+            a.w_split, a.w_split_bytes = split.data_ptr(), split.numel()
+        for i in range(args.warmup):
+            a.x = xs[i].data_ptr()
+            moe.moe_route(a, sp)
+        ev = _events(torch, args.prefill_steps)
+        torch.cuda.synchronize()
+        for j in range(args.prefill_steps):
+            flush()
+            a.x = xs[args.warmup + j].data_ptr()
+            ev[j][0].record(stream)
+            moe.moe_route(a, sp)
+            ev[j][1].record(stream)
+        torch.cuda.synchronize()
+        return sum(x.elapsed_time(y) for x, y in ev) / args.prefill_steps * 1e3
+
+    us_tc, us_simt = timed(True), timed(False)
     flops = 2.0 * T * E * H
     return {"workload": f"router: {T} tokens, H={H}, {E} experts top-{k}, fp32 weights and "
-                        "logits (SIMT FMA, Kahan per 32-value chunk), softmax/top-k",
-            "us_per_call": round(us, 2), "fp32_tflops": round(flops / (us * 1e-6) / 1e12, 2)}
+                        "logits, softmax/top-k",
+            "us_per_call": round(us_tc, 2),
+            "path": "tensor cores: weights split into three bf16 pieces, 64-deep partial sums "
+                    "added with compensation",
+            "fp32_equiv_tflops": round(flops / (us_tc * 1e-6) / 1e12, 2),
+            "simt": {"us_per_call": round(us_simt, 2), "path": "SIMT fp32 FMA, Kahan per "
+                     "32-value chunk", "fp32_tflops": round(flops / (us_simt * 1e-6) / 1e12, 2)}}
 
 
 # --------------------------------------------------------------- stack / flat

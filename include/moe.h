@@ -120,9 +120,23 @@ typedef struct {
                            workspace must not overlap on the GPU.           */
   size_t workspace_bytes;
   int32_t* status;      /* device sticky status word, or NULL                    */
+  void* w_split;        /* device scratch of moe_route_split_bytes(E, H) bytes,
+                           16-byte aligned, or NULL.  With T > 1024, H a
+                           multiple of 64 and x and w_router 16-byte aligned,
+                           the call rewrites it with w_router as three bf16
+                           pieces (W = W1 + W2 + W3 exactly, rows padded to a
+                           multiple of 32 with zeros) and computes the logits
+                           on the tensor cores from them: every product exact,
+                           each 64-deep partial sum read out and added in fp32
+                           with compensation.  Otherwise (or NULL) the logits
+                           run on the CUDA cores in fp32.  Calls that share it
+                           must not overlap on the GPU.                      */
+  size_t w_split_bytes;
 } moe_route_args;
 
 size_t moe_route_workspace_bytes(int T, int E);
+/* 3 * ceil(E/32)*32 * H * 2: the bf16 pieces of the router weights (w_split). */
+size_t moe_route_split_bytes(int E, int H);
 moe_status moe_route(const moe_route_args* a, void* stream);
 
 /* ---------------------------------------------------------------- permute

@@ -38,6 +38,7 @@ moe_status route_permute_small(const moe_route_args* a, const PermArgs& pa,
 moe_status launch_route_skip(const SkipArgs& sk, const int32_t* ids, const float* w, int T, int k,
                              int E, cudaStream_t s);
 bool cache_policy_args(const expcache* c, int layer, PolicyArgs* a);
+size_t route_split_bytes(int E, int H);
 }  // namespace moe
 
 using namespace moe;
@@ -45,6 +46,8 @@ using namespace moe;
 // the layer's control area: the few-token router's counter, then one counter
 // per 128-row tile for the combine in the decode down kernel (H <= 16384),
 // then the one-launch decode FFN's control words (4 + one per act position)
+// moe_route's tensor-core logits serve more than this many tokens
+constexpr int kRouteTcMinT = 1024;
 constexpr size_t kRouteCtlBytes = 256, kTileCtlBytes = 128 * 4,
                  kFfnCtlBytes = (4 + 2 * 1024) * 4;  // + h-ready and landed counts
 
@@ -61,7 +64,7 @@ MOE_API const char* moe_status_string(moe_status s) {
   }
 }
 
-MOE_API int moe_abi_version(void) { return 5; }
+MOE_API int moe_abi_version(void) { return 6; }
 
 namespace moe {
 moe_status ensure_setup() {
@@ -139,6 +142,8 @@ struct moe_layer {
   int32_t* miss_dst;  // adaptive cache: the slot each miss is gathered into
   int32_t* ids_eff;   // renorm-skip: the kept routes' experts (-1: dropped)
   float* w_eff;       // renorm-skip: the kept routes' renormalised weights
+  void* w_split;      // the router weights' bf16 pieces (tensor-core router), or null
+  size_t w_split_bytes;
   void* ffn_ws;
   size_t ffn_ws_bytes;
   int last_T;
@@ -200,7 +205,8 @@ MOE_API moe_status moe_layer_create(const moe_layer_desc* d, moe_layer** out) {
       kRouteCtlBytes + kTileCtlBytes + kFfnCtlBytes, /* route_ctl, tile counters, FFN */
       (size_t)E * 4,      /* miss_dst */
       (size_t)T * k * 4,  /* ids_eff */
-      (size_t)T * k * 4   /* w_eff */};
+      (size_t)T * k * 4,  /* w_eff */
+      T > kRouteTcMinT ? route_split_bytes(E, H) : 0 /* router weight pieces */};
   const int n = (int)(sizeof(sizes) / sizeof(sizes[0]));
   size_t total = 0;
   for (int i = 0; i < n; ++i) total += align256(sizes[i]);
@@ -211,7 +217,7 @@ MOE_API moe_status moe_layer_create(const moe_layer_desc* d, moe_layer** out) {
   }
   l->ws_bytes = total;
   uint8_t* p = (uint8_t*)l->ws;
-  void* ptrs[24];
+  void* ptrs[25];
   for (int i = 0; i < n; ++i) {
     ptrs[i] = sizes[i] ? p : nullptr;
     p += align256(sizes[i]);
@@ -240,6 +246,8 @@ MOE_API moe_status moe_layer_create(const moe_layer_desc* d, moe_layer** out) {
   l->miss_dst = (int32_t*)ptrs[21];
   l->ids_eff = (int32_t*)ptrs[22];
   l->w_eff = (float*)ptrs[23];
+  l->w_split = ptrs[24];
+  l->w_split_bytes = sizes[24];
   bool ok = cudaMemset(l->ws, 0, total) == cudaSuccess &&
             cudaStreamCreateWithFlags(&l->side, cudaStreamNonBlocking) == cudaSuccess &&
             cudaEventCreateWithFlags(&l->ev_lookup, cudaEventDisableTiming) == cudaSuccess;
@@ -354,6 +362,7 @@ MOE_API moe_status moe_layer_forward(moe_layer* l, const void* x, int T, void* y
   ra.ids = l->ids; ra.w = l->w; ra.p_sel = l->p_sel; ra.logits = l->logits;
   ra.workspace = l->route_ctl; ra.workspace_bytes = 256;
   ra.status = l->status;
+  ra.w_split = l->w_split; ra.w_split_bytes = l->w_split_bytes;
   LookupArgs lk;
   cache_lookup_args(d.cache, d.layer, l->src_slot, l->act_list, l->n_act, l->miss_ids, l->n_miss,
                     &lk);

@@ -1137,6 +1137,23 @@ const float* prefill_h_rows(const void* workspace, int T, int H, int I, int E, i
 
 moe_status prefill_setup() { return pf::load_encoder(); }
 
+// 2-D bf16 tensor map (rows of `inner` values, `rows` rows), box 64 values x
+// box_rows rows, 128-byte swizzle, zero fill outside the rows
+moe_status tmap_bf16_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows,
+                        uint64_t row_stride_bytes, uint32_t box_rows) {
+  moe_status st = pf::load_encoder();
+  if (st != MOE_OK) return st;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {row_stride_bytes};
+  cuuint32_t box[2] = {64u, box_rows};
+  cuuint32_t estr[2] = {1u, 1u};
+  CUresult r = pf::g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                            strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
+}
+
 // part (the layer's own sequence): 0 = the call's whole group; for group 0, 1 =
 // the token quantisation, tile tables, hits and shared expert, 2 = the first
 // misses (whose records the layer gathers meanwhile)

@@ -526,6 +526,10 @@ static moe_status route_check(const moe_route_args* a) {
 }
 
 namespace moe {
+// the tensor-core logits for many tokens (route_tc.cu)
+bool route_tc_ok(const moe_route_args* a);
+moe_status route_logits_tc(const moe_route_args* a, float* logits, cudaStream_t s);
+
 // Router, permutation and lookup in one launch for T <= 8 tokens (the layer's
 // decode sequence).  Needs a->workspace (the control area) and a->logits.
 // Returns MOE_ERR_UNSUPPORTED when the shape does not qualify (the caller then
@@ -609,6 +613,9 @@ MOE_API moe_status moe_route(const moe_route_args* a, void* stream) {
     if (launch_pdl(k_logits_gemv, grid, 256, 0, s, x, a->w_router, a->bias, a->T, a->H, a->E,
                    logits) != cudaSuccess)
       return MOE_ERR_CUDA;
+  } else if (route_tc_ok(a)) {
+    moe_status st = route_logits_tc(a, logits, s);
+    if (st != MOE_OK) return st;
   } else {
     dim3 grid((a->E + kTN - 1) / kTN, (a->T + kTM - 1) / kTM);
     if (launch_pdl(k_logits_gemm, grid, kGemmThreads, 0, s, x, a->w_router, a->bias, a->T, a->H,

@@ -31,7 +31,8 @@ class MoeError(RuntimeError):
 class moe_route_args(ctypes.Structure):
     _fields_ = [("x", vp), ("w_router", vp), ("bias", vp), ("T", i32), ("H", i32), ("E", i32),
                 ("k", i32), ("ids", vp), ("w", vp), ("p_sel", vp), ("logits", vp),
-                ("workspace", vp), ("workspace_bytes", sz), ("status", vp)]
+                ("workspace", vp), ("workspace_bytes", sz), ("status", vp),
+                ("w_split", vp), ("w_split_bytes", sz)]
 
 
 class expcache_desc(ctypes.Structure):
@@ -69,6 +70,7 @@ SIGNATURES = {
     "moe_abi_version": (i32, []),
     "moe_record_bytes": (u64, [i32, i32, i32]),
     "moe_route_workspace_bytes": (sz, [i32, i32]),
+    "moe_route_split_bytes": (sz, [i32, i32]),
     "moe_route": (i32, [ctypes.POINTER(moe_route_args), vp]),
     "moe_permute": (i32, [vp, i32, i32, i32, vp, vp, vp, vp, vp, i32, vp, vp]),
     "expcache_create": (i32, [ctypes.POINTER(expcache_desc), ctypes.POINTER(vp)]),
@@ -136,6 +138,10 @@ def moe_record_bytes(H: int, I: int, fmt: int = MOE_FMT_NVFP4) -> int:
 
 def moe_route_workspace_bytes(T: int, E: int) -> int:
     return int(lib().moe_route_workspace_bytes(T, E))
+
+
+def moe_route_split_bytes(E: int, H: int) -> int:
+    return int(lib().moe_route_split_bytes(E, H))
 
 
 def moe_route(args: moe_route_args, stream: int = 0) -> None:

@@ -41,7 +41,7 @@ def test_binding_covers_the_header(libmoe):
     from routed_expert_layer_router_gb300 import moe
     assert sorted(moe.SIGNATURES) == _declared_functions()
     L = moe.lib()
-    assert L.moe_abi_version() == 5
+    assert L.moe_abi_version() == 6
     assert L.moe_record_bytes(6144, 2048, 0) == 21233664
     assert L.moe_record_bytes(6144, 2048, 1) == 20054016
     assert L.moe_record_bytes(6144, 2048, 7) == 0

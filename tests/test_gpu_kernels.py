@@ -8,7 +8,7 @@ import torch
 import gen
 import oracle
 from tests.gpu_common import draw_tokens, to_dev_bf16
-from tests.helpers import PROB_RTOL
+from tests.helpers import PROB_RTOL, bf16_to_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -52,9 +52,11 @@ def test_device_generator_matches_host(H, I):
     assert np.array_equal(sd.cpu().numpy().view(np.uint16), hd)
 
 
-def _route_gpu(x, Wr, bias, k, ctl=None):
+def _route_gpu(x, Wr, bias, k, ctl=None, split=None):
     """moe_route; with `ctl` (a zeroed device buffer) the call gets a workspace
-    control area, which lets up to 8 tokens run as one kernel."""
+    control area, which lets up to 8 tokens run as one kernel; with `split`
+    (a device buffer of moe_route_split_bytes) more than 1024 tokens take the
+    tensor-core logits."""
     from routed_expert_layer_router_gb300 import moe
     T, H = x.shape
     E = Wr.shape[0]
@@ -71,6 +73,8 @@ def _route_gpu(x, Wr, bias, k, ctl=None):
     a.ids, a.w, a.p_sel, a.logits = ids.data_ptr(), w.data_ptr(), p.data_ptr(), lg.data_ptr()
     if ctl is not None:
         a.workspace, a.workspace_bytes = ctl.data_ptr(), ctl.numel()
+    if split is not None:
+        a.w_split, a.w_split_bytes = split.data_ptr(), split.numel()
     moe.moe_route(a, _stream())
     torch.cuda.synchronize()
     return ids.cpu().numpy(), w.cpu().numpy(), p.cpu().numpy(), lg.cpu().numpy()
@@ -95,6 +99,39 @@ def test_route_parity(name, T, one_kernel):
         assert np.abs(lg - lg_r).max() <= 1e-5 * np.abs(lg_r).max()
     if one_kernel:
         assert int(ctl.view(torch.int32)[0].item()) == 0
+
+
+ODD = gen.Workload("tc-odd", H=512, I=128, E=100, k=6, T=1300, layers=1, Is=0, seed=11)
+
+
+@pytest.mark.parametrize("wl,T,with_bias", [(gen.WORKLOADS["tiny"], 1100, False),
+                                            (ODD, 1300, True),
+                                            (gen.WORKLOADS["decode"], 1100, False)])
+def test_route_tensor_core_parity(wl, T, with_bias):
+    """More than 1024 tokens with the weight-piece scratch: the logits run on
+    the tensor cores from the three bf16 pieces of the fp32 router weights.
+    The pieces must add up to the weights exactly (padding rows zero), and
+    ids, weights, probabilities and logits must meet the router's bar.  The
+    shapes cover a padded expert tile (16 and 100 experts) and a ragged last
+    token tile (1100 and 1300 tokens)."""
+    from routed_expert_layer_router_gb300 import moe
+    Wr = gen.router_f32(wl.seed, 0, wl.E, wl.H)
+    bias = gen.zipf_bias(wl.seed, 0, wl.E, 1.556)[0] if with_bias else None
+    x, _ = draw_tokens(wl, 0, T, Wr, bias, batch=512)
+    ids_r, w_r, p_r, lg_r, _ = oracle.route(x, Wr, bias, wl.k)
+    split = torch.zeros(moe.moe_route_split_bytes(wl.E, wl.H), dtype=torch.uint8, device="cuda")
+    ids, w, p, lg = _route_gpu(x, Wr, bias, wl.k, split=split)
+    E_pad = (wl.E + 31) // 32 * 32
+    pieces = split.cpu().numpy().view(np.uint16).reshape(3, E_pad, wl.H)
+    total = sum(bf16_to_f64(pieces[i]) for i in range(3))
+    assert np.array_equal(total[:wl.E], Wr.astype(np.float64))
+    assert not total[wl.E:].any()
+    assert np.array_equal(ids, ids_r)
+    assert np.all(np.abs(w - w_r) <= PROB_RTOL * w_r)
+    assert np.all(np.abs(p - p_r) <= PROB_RTOL * p_r)
+    err = np.abs(lg - lg_r).max()
+    print(f"max logit error {err:.3g} (max |logit| {np.abs(lg_r).max():.3g})")
+    assert err <= 1e-5 * np.abs(lg_r).max()
 
 
 @pytest.mark.parametrize("T,k,E", [(1, 8, 288), (4, 2, 16), (64, 8, 288), (4096, 8, 288),
