@@ -102,10 +102,15 @@ __host__ __device__ __forceinline__ uint32_t tile_pack(int j, int mt, int nt) {
 
 // Tile orders.  Gate/up: an expert-major table (the 16 row tiles of an expert
 // run side by side and share its activation tile in L2), decoded by tile_info.
-// Down: row-tile-major over the launch's ncols column tiles, t = m * ncols + c,
-// each column tile a record {expert, slot, padded row of column 0, routes}
-// (ctab); so at any time the CTAs add into a few 128-row bands of every
-// token's y_acc row, which stay in L2, instead of into all of y_acc.
+// Down: a tile is a pair of adjacent 128-row tiles (m = 0 .. mtiles/2 - 1,
+// rows 256 m .. 256 m + 255) and one column tile, row-pair-major over the
+// launch's ncols column tiles, t = m * ncols + c, each column tile a record
+// {expert, slot, padded row of column 0, routes} (ctab); so at any time the
+// CTAs add into a few 256-row bands of every token's y_acc row, which stay in
+// L2, instead of into all of y_acc.  A CTA's shared-memory fill rate, not
+// HBM, limited the down GEMM with one row tile per activation tile (its
+// activations were half of every stage); two row tiles per activation tile
+// measured 441 -> 412 us for the 4096-token layer.
 
 // act_list range [lo, hi) of FFN group `group` among the planned experts:
 // group 0 = the hits and misses [0, S), group g > 0 = misses [g S, (g+1) S)
@@ -208,8 +213,10 @@ __global__ void __launch_bounds__(1024) k_tile_plan(
 
 template <int KIND, int EPI>
 struct Cfg {
-  // gate/up: two A operands (gate and up rows) against one B, two accumulators
-  static constexpr bool kDual = (EPI == EPI_GU_ROUTED || EPI == EPI_GU_SHARED);
+  // two A operands against one B, two accumulators: gate/up takes the gate
+  // and up rows of one row tile, the routed down two adjacent row tiles (so
+  // each activation tile loaded serves 256 weight rows)
+  static constexpr bool kDual = (EPI == EPI_GU_ROUTED || EPI == EPI_GU_SHARED || EPI == EPI_DOWN_ROUTED);
   static constexpr bool kRouted = (EPI == EPI_GU_ROUTED || EPI == EPI_DOWN_ROUTED);
   // routed down: row-tile-major order over a table of column tiles (ctab)
   static constexpr bool kMMajor = (EPI == EPI_DOWN_ROUTED);
@@ -291,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       s_cbase = p.plan_begin[g0];
       s_ncols = p.plan_begin[g1] - s_cbase;
       s_tlo = C::kMMajor ? 0 : s_cbase * p.mtiles;
-      s_thi = C::kMMajor ? s_ncols * p.mtiles : p.plan_begin[g1] * p.mtiles;
+      s_thi = C::kMMajor ? s_ncols * (C::kDual ? p.mtiles / 2 : p.mtiles) : p.plan_begin[g1] * p.mtiles;
     } else {
       s_cbase = 0;
       s_ncols = 1;
@@ -346,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int mtn = 0, ntn = 0, en = 0, sn = 0, pn = 0;
         int4 rn = make_int4(0, 0, 0, 0);
         const int kst = (p.kstages + C::kChunks - 1) / C::kChunks;  // stages per tile
-        const int arow = mt * kTileM;  // weight rows
+        const int arow = mt * kTileM * (C::kMMajor && C::kDual ? 2 : 1);  // weight rows
         for (int kb = 0; kb < kst; ++kb, ++g) {
           if (C::kMMajor && tn < thi && kb == 0) rn = p.ctab[cbase + tn % ncols];
           if (C::kRouted && !C::kMMajor && tn < thi) {  // one link per stage
@@ -379,6 +386,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t pol_w = ptx::l2_evict_first(), pol_a = ptx::l2_evict_last();
             if (C::kMMajor) {
               ptx::tma_load_3d_hint(st, &tmA0, kc, arow, slot, &full_bar[s], pol_w);
+              if (C::kDual)
+                ptx::tma_load_3d_hint(st + C::kTileBytes, &tmA0, kc, arow + kTileM, slot,
+                                      &full_bar[s], pol_w);
             } else if (C::kRouted) {
               ptx::tma_load_3d(st, &tmA0, kc, arow, slot, &full_bar[s]);
               if (C::kDual) ptx::tma_load_3d(st + C::kTileBytes, &tmA1, kc, arow, slot, &full_bar[s]);
@@ -394,12 +404,17 @@ __global__ void __launch_bounds__(kThreads, 1)
               // kq*kAtoms .. (kq+1)*kAtoms-1 of the row tile
               unsigned char* sf = bdst + C::kTileBytes;
               const uint8_t* rec = p.arena + (uint64_t)slot * p.rec_bytes;
-              const uint64_t aoff = ((uint64_t)mt * p.kgroups + (uint64_t)kq * C::kAtoms) * 512;
+              const uint64_t aoff =
+                  ((uint64_t)(arow / kTileM) * p.kgroups + (uint64_t)kq * C::kAtoms) * 512;
               const uint64_t boff =
                   ((uint64_t)(brow / kTileN) * p.kgroups + (uint64_t)kq * C::kAtoms) * 512;
               unsigned char* sfb = sf + C::kSfBytes * (C::kDual ? 2 : 1);
               if (C::kMMajor) {
                 ptx::bulk_load_hint(sf, rec + p.sfa_off0 + aoff, C::kSfBytes, &full_bar[s], pol_w);
+                if (C::kDual)
+                  ptx::bulk_load_hint(sf + C::kSfBytes,
+                                      rec + p.sfa_off0 + aoff + (uint64_t)p.kgroups * 512,
+                                      C::kSfBytes, &full_bar[s], pol_w);
                 ptx::bulk_load_hint(sfb, p.b_scales + boff, C::kSfBytes, &full_bar[s], pol_a);
               } else {
                 ptx::bulk_load(sf, rec + p.sfa_off0 + aoff, C::kSfBytes, &full_bar[s]);
@@ -558,15 +573,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_fence_after();
         const uint32_t lane_addr = tmem + ((uint32_t)(q * 32) << 16) +
                                    (uint32_t)ab * C::kAccCols + (uint32_t)(ch * kHalf);
-        uint32_t ra[32], rb[32];
+        uint32_t ra[32], rb[32], ra2[32], rb2[32];
         ptx::tmem_ld_32x32b_x32(lane_addr, ra);
         ptx::tmem_ld_32x32b_x32(lane_addr + 32, rb);
+        ptx::tmem_ld_32x32b_x32(lane_addr + 128, ra2);
+        ptx::tmem_ld_32x32b_x32(lane_addr + 160, rb2);
         ptx::tmem_ld_wait();
         ptx::tc_fence_before();
         if (lane == 0) ptx::mbar_arrive(&acc_empty[ab]);  // the accumulator is free
         float2 dn = dc;
         if (tn < thi && et < kTileN) dn = p.dcol[rn.z + et];
-        add_columns(ra, rb, p.y_acc + mt * kTileM + row, col_scale + ch * kHalf,
+        add_columns(ra, rb, p.y_acc + 2 * mt * kTileM + row, col_scale + ch * kHalf,
+                    col_row + ch * kHalf, p.H, n_valid - ch * kHalf);
+        add_columns(ra2, rb2, p.y_acc + (2 * mt + 1) * kTileM + row, col_scale + ch * kHalf,
                     col_row + ch * kHalf, p.H, n_valid - ch * kHalf);
         asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
         r = rn;
