@@ -785,75 +785,126 @@ __device__ __forceinline__ size_t scale_word(int row, int kg, int KG) {
   return ((size_t)(row >> 7) * KG + kg) * 512 + (row & 31) * 16 + ((row & 127) >> 5) * 4;
 }
 
+// codes of N consecutive values (N % 8 == 0) of one NVFP4 block with scale
+// byte sc and dequantised scale sdq, 8 codes per word (one reciprocal)
+template <int N>
+__device__ __forceinline__ void block_codes_w(const float* v, uint32_t sc, float sdq,
+                                              uint32_t* out) {
+  if (sc == 0) {  // the whole block quantises to +-0; written as +0
+#pragma unroll
+    for (int w = 0; w < N / 8; ++w) out[w] = 0u;
+    return;
+  }
+  float q[N];
+  if (sdq >= 0x1p-56f && sdq <= 0x1p48f) {
+    const float y = __frcp_rn(sdq);
+#pragma unroll
+    for (int i = 0; i < N; ++i) q[i] = quot_rn(v[i], sdq, y);
+  } else {
+#pragma unroll
+    for (int i = 0; i < N; ++i) q[i] = __fdiv_rn(v[i], sdq);
+  }
+#pragma unroll
+  for (int w = 0; w < N / 8; ++w) {
+    uint32_t c = 0;
+#pragma unroll
+    for (int i = 0; i < 8; i += 2) c |= e2m1x2_rn(q[8 * w + i], q[8 * w + i + 1]) << (4 * i);
+    out[w] = c;
+  }
+}
+
 // One fp32 row of K values (K % 256 == 0, K <= KMAX) by one warp into padded
-// row `row` of the tcgen05 layout.  Each load instruction covers 512
-// contiguous bytes (lane l holds float4 j*32 + l), so four lanes share a
-// 16-value block (eight a 32-value MX block); the row is read once and held
-// in registers.  Returns the row's global scale G (on every lane; 1 for MX).
+// row `row` of the tcgen05 layout.  Lane l owns the 64 consecutive values
+// 64 (l + 32 p) .. + 63 of each pass p over 2048 values: four NVFP4 blocks
+// (one scale word) or two MXFP4 blocks, so no block spans lanes and a lane
+// writes its 32 code bytes and its scale word (half word for MX) itself.  The
+// row is read once (through L1: consecutive loads of a lane share sectors)
+// and held in registers.  The block scales' quotients amax_b / (6 G) use one
+// correctly rounded reciprocal of 6 G per row and two residual steps (as the
+// codes do), dividing when 6 G is outside [2^-56, 2^48].  Returns the row's
+// global scale G (on every lane; 1 for MX).
 template <int KMAX, int FMT>
 __device__ __forceinline__ float quant_row_f32(const float* __restrict__ hr, int K, int row,
                                               uint8_t* __restrict__ codes,
                                               uint8_t* __restrict__ scales,
                                               float* __restrict__ Gr) {
-  constexpr int kNJ = KMAX / 128;
+  constexpr int kNP = (KMAX + 2047) / 2048;
   const int lane = threadIdx.x & 31;
-  const int NJ = K / 128, KG = K / (4 * fmt_block(FMT));
-  float4 v[kNJ];
+  const int KG = K / (4 * fmt_block(FMT));
+  float4 v[kNP][16];
   float amax = 0.f;
 #pragma unroll
-  for (int j = 0; j < kNJ; ++j) {
-    v[j] = j < NJ ? __ldcg(reinterpret_cast<const float4*>(hr) + j * 32 + lane)
-                  : make_float4(0.f, 0.f, 0.f, 0.f);
-    amax = fmaxf(amax, absmax4(v[j].x, v[j].y, v[j].z, v[j].w));
+  for (int p = 0; p < kNP; ++p) {
+    const int c0 = 64 * (lane + 32 * p);
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      v[p][q] = c0 < K ? __ldg(reinterpret_cast<const float4*>(hr + c0) + q)
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+      amax = fmaxf(amax, absmax4(v[p][q].x, v[p][q].y, v[p][q].z, v[p][q].w));
+    }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
   const float G = amax > 0.f ? __fdiv_rn(amax, 2688.0f) : 1.0f;
   const float sixG = __fmul_rn(6.0f, G);
-  uint16_t* crow = reinterpret_cast<uint16_t*>(codes + (size_t)row * (K / 2));
-  if (FMT == MOE_FMT_MXFP4) {
+  const bool fast = sixG >= 0x1p-56f && sixG <= 0x1p48f;
+  const float y6 = fast ? __frcp_rn(sixG) : 0.f;
 #pragma unroll
-    for (int j = 0; j < kNJ; ++j) {
-      if (j >= NJ) break;
-      float ab = absmax4(v[j].x, v[j].y, v[j].z, v[j].w);
-      ab = fmaxf(ab, __shfl_xor_sync(0xFFFFFFFFu, ab, 1));
-      ab = fmaxf(ab, __shfl_xor_sync(0xFFFFFFFFu, ab, 2));
-      ab = fmaxf(ab, __shfl_xor_sync(0xFFFFFFFFu, ab, 4));
-      float inv;
-      const uint32_t sc = mx_scale(ab, inv);
-      const float f[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-      crow[j * 32 + lane] = (uint16_t)mx_codes<4>(f, ab, inv);
-      // blocks j*4 + lane/8: lane 0 gathers the scale word of the 128 values
-      const uint32_t s1 = __shfl_down_sync(0xFFFFFFFFu, sc, 8);
-      const uint32_t s2 = __shfl_down_sync(0xFFFFFFFFu, sc, 16);
-      const uint32_t s3 = __shfl_down_sync(0xFFFFFFFFu, sc, 24);
-      if (lane == 0)
-        *reinterpret_cast<uint32_t*>(scales + scale_word(row, j, KG)) =
-            sc | (s1 << 8) | (s2 << 16) | (s3 << 24);
+  for (int p = 0; p < kNP; ++p) {
+    const int u = lane + 32 * p;  // 64-value unit of the row
+    if (64 * u >= K) break;
+    uint32_t cw[8];
+    uint32_t sw = 0;
+    if (FMT == MOE_FMT_MXFP4) {
+#pragma unroll
+      for (int b = 0; b < 2; ++b) {
+        float f[32];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          f[4 * q] = v[p][8 * b + q].x;
+          f[4 * q + 1] = v[p][8 * b + q].y;
+          f[4 * q + 2] = v[p][8 * b + q].z;
+          f[4 * q + 3] = v[p][8 * b + q].w;
+        }
+        float ab = 0.f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) ab = fmaxf(ab, fabsf(f[i]));
+        float inv;
+        const uint32_t sc = mx_scale(ab, inv);
+#pragma unroll
+        for (int w = 0; w < 4; ++w) cw[4 * b + w] = mx_codes<8>(f + 8 * w, ab, inv);
+        sw |= sc << (8 * b);
+      }
+      *reinterpret_cast<uint16_t*>(scales + scale_word(row, u >> 1, KG) + 2 * (u & 1)) =
+          (uint16_t)sw;
+    } else {
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        float f[16];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          f[4 * q] = v[p][4 * b + q].x;
+          f[4 * q + 1] = v[p][4 * b + q].y;
+          f[4 * q + 2] = v[p][4 * b + q].z;
+          f[4 * q + 3] = v[p][4 * b + q].w;
+        }
+        float ab = 0.f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) ab = fmaxf(ab, fabsf(f[i]));
+        const uint32_t sc = e4m3_rne(fast ? quot_rn(ab, sixG, y6) : __fdiv_rn(ab, sixG));
+        const float sdq = __fmul_rn(e4m3_value(sc), G);
+        block_codes_w<16>(f, sc, sdq, cw + 2 * b);
+        sw |= sc << (8 * b);
+      }
+      *reinterpret_cast<uint32_t*>(scales + scale_word(row, u, KG)) = sw;
     }
-    if (lane == 0) Gr[row] = 1.0f;
-    return 1.0f;
+    uint4* crow = reinterpret_cast<uint4*>(codes + (size_t)row * (K / 2) + 32 * (size_t)u);
+    crow[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+    crow[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
   }
-#pragma unroll
-  for (int j = 0; j < kNJ; ++j) {
-    if (j >= NJ) break;
-    float ab = absmax4(v[j].x, v[j].y, v[j].z, v[j].w);
-    ab = fmaxf(ab, __shfl_xor_sync(0xFFFFFFFFu, ab, 1));
-    ab = fmaxf(ab, __shfl_xor_sync(0xFFFFFFFFu, ab, 2));
-    float sdq;
-    const uint32_t sc = block_scale(ab, sixG, G, sdq);
-    const float f[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-    crow[j * 32 + lane] = (uint16_t)block_codes<4>(f, sc, sdq);
-    // blocks j*8 + lane/4; lanes 0 and 16 gather the two scale words
-    const uint32_t s1 = __shfl_down_sync(0xFFFFFFFFu, sc, 4);
-    const uint32_t s2 = __shfl_down_sync(0xFFFFFFFFu, sc, 8);
-    const uint32_t s3 = __shfl_down_sync(0xFFFFFFFFu, sc, 12);
-    if ((lane & 15) == 0)
-      *reinterpret_cast<uint32_t*>(scales + scale_word(row, j * 2 + (lane >> 4), KG)) =
-          sc | (s1 << 8) | (s2 << 16) | (s3 << 24);
-  }
-  if (lane == 0) Gr[row] = G;
-  return G;
+  const float Gout = FMT == MOE_FMT_MXFP4 ? 1.0f : G;
+  if (lane == 0) Gr[row] = Gout;
+  return Gout;
 }
 
 // zero padded rows [r0, r1) of a K-wide operand (codes, scale words, G) with
@@ -875,10 +926,11 @@ constexpr int kQuantHMaxK = 4096;  // I up to 4096 (the prefill path checks)
 constexpr int kQuantXMaxK = 8192;  // H up to 8192
 
 // K-hq: h -> NVFP4 for the padded rows of planned experts [g0, g1): CTA
-// (j - g0, part) takes a quarter of expert plan_e[j]'s rows, one warp per
+// (j - g0, part) takes an eighth of expert plan_e[j]'s rows, one warp per
 // row; padding rows are zeroed.  Three CTAs per SM for rows up to 2048 values
-// (80 registers, a few spilled): 101 -> 91 us for the 4096-token layer's h;
-// four CTAs spilled more and took 107.
+// (80 registers, a few bytes spilled).  The kernel is bound by latency, not
+// by HBM: for the 4096-token layer's h, lane-owned blocks (no shuffles) took
+// 95 -> 90 us, eighths instead of quarters and the next-row prefetch 85 us.
 template <int KMAX, int FMT>
 __global__ void __launch_bounds__(256, KMAX <= 2048 ? 3 : 1) k_quant_h(
     const float* __restrict__ h32, int K, int g0, int g1, int group, int gsize, int part,
@@ -900,6 +952,10 @@ __global__ void __launch_bounds__(256, KMAX <= 2048 ? 3 : 1) k_quant_h(
   const int wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
   const float gsd = gscale[e * 3 + 2];
   for (int i = lo + wid; i < min(hi, cnt); i += nw) {
+    // the warp's next row is fetched into L2 while this one is quantised
+    if ((threadIdx.x & 31) == 0 && i + nw < min(hi, cnt))
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
+                   ::"l"(h32 + (size_t)(r0 + i + nw) * K), "r"((uint32_t)K * 4u) : "memory");
     const float Gi =
         quant_row_f32<KMAX, FMT>(h32 + (size_t)(r0 + i) * K, K, r0 + i, codes, scales, G);
     if ((threadIdx.x & 31) == 0) {
@@ -1277,7 +1333,7 @@ moe_status prefill_ffn(const moe_ffn_args* a, cudaStream_t s, int part, void (*m
                                : k_quant_h<kQuantHMaxK, MOE_FMT_MXFP4>)
                   : (I <= 2048 ? k_quant_h<2048, MOE_FMT_NVFP4>
                                : k_quant_h<kQuantHMaxK, MOE_FMT_NVFP4>);
-    kq<<<dim3(ng, 4), 256, 0, s>>>((const float*)(ws + W.h32), I, g0, g1, a->group, a->n_stage,
+    kq<<<dim3(ng, 8), 256, 0, s>>>((const float*)(ws + W.h32), I, g0, g1, a->group, a->n_stage,
                                   part, plan_e, plan_n,
                                   a->offsets, a->pad_offsets, a->perm, a->w, a->gscale, a->k,
                                   ws + W.hq_codes, ws + W.hq_scales, (float*)(ws + W.hq_G),
