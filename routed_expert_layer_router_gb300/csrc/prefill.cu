@@ -45,6 +45,11 @@ int cache_n_stage(const expcache* c);
 namespace pf {
 
 constexpr int kTileM = 128, kTileN = 128, kStageKB = 128;  // K bytes per stage and operand row
+// tokens per tile of the bf16 shared-expert GEMMs: 256 halves the weight
+// tiles loaded per token against 128 (bf16 needs no scale-factor columns, so
+// two 256-column accumulators fit in tensor memory)
+constexpr int kSharedN = 256;
+constexpr int kMaxN = 256;
 constexpr int kThreads = 320;  // warp 0: TMA, warp 1: MMA, warps 2..9: epilogue
 constexpr int kEpiWarps = 8;   // two per tensor-memory lane quarter, each half of the columns
 constexpr uint64_t kWaitNs = 2000000000ull;  // no wait lasts longer than 2 s
@@ -129,8 +134,9 @@ __device__ __forceinline__ void pf_group_range(const int32_t* plan_n, int group,
   if (hi < lo) hi = lo;
 }
 
-// gate/up or shared tile t of a launch -> (m tile, n tile, expert id, slot)
-template <bool ROUTED>
+// gate/up or shared tile t of a launch -> (m tile, n tile, expert id, slot);
+// N columns per shared tile
+template <bool ROUTED, int N>
 __device__ __forceinline__ void tile_info(const GemmParams& p, int t, int& mt, int& nt, int& e,
                                           int& slot) {
   if (ROUTED) {
@@ -141,7 +147,7 @@ __device__ __forceinline__ void tile_info(const GemmParams& p, int t, int& mt, i
     e = p.plan_e[j];
     slot = p.plan_slot[j];
   } else {
-    const int ntn = (p.T + kTileN - 1) / kTileN;
+    const int ntn = (p.T + N - 1) / N;
     mt = t / ntn;
     nt = t % ntn;
     e = 0;
@@ -223,22 +229,28 @@ struct Cfg {
   static constexpr bool kNvf4 = (KIND == 0);
   static constexpr bool kMxf4 = (KIND == 2);
   static constexpr bool kFp4 = kNvf4 || kMxf4;
-  static constexpr int kTileBytes = kTileM * kStageKB;  // 16 KiB
+  static constexpr int kTileBytes = kTileM * kStageKB;  // 16 KiB (an A tile)
+  // B rows (routes or tokens) per tile and their bytes per 128-byte K chunk
+  static constexpr int kN = (KIND == 1) ? kSharedN : kTileN;
+  static constexpr int kBBytes = kN * kStageKB;
   // scale atoms (512 B: 128 rows x 4 blocks) per operand and 128-byte K chunk
   // (256 values): blocks of 16 (NVFP4) take 4 atoms, blocks of 32 (MXFP4) 2
   static constexpr int kAtoms = kNvf4 ? 4 : (kMxf4 ? 2 : 0);
   static constexpr int kSfBytes = kAtoms * 512;
   // one 128-byte K chunk of every operand (A tiles, B tile, their scale atoms)
-  static constexpr int kChunkBytes = kTileBytes * (kDual ? 3 : 2) + kSfBytes * (kDual ? 3 : 2);
+  static constexpr int kChunkBytes =
+      kTileBytes * (kDual ? 2 : 1) + kBBytes + kSfBytes * (kDual ? 3 : 2);
   // several chunks per stage: fewer stages per tile, so fewer barrier round
   // trips and commits for the same bytes in flight (4 dual or 6 single
   // chunks fill the shared memory)
-  static constexpr int kChunks = kDual ? kDualChunks : kSingleChunks;
+  static constexpr int kChunks = kDual ? kDualChunks : (kN > kTileN ? 1 : kSingleChunks);
   static constexpr int kStageBytes = kChunks * kChunkBytes;
-  static constexpr int kStages = (kDual ? 4 : 6) / kChunks;
+  static constexpr int kStagesFit = (226 * 1024) / kStageBytes;
+  static constexpr int kStages =
+      (kDual ? 4 : 6) / kChunks < kStagesFit ? (kDual ? 4 : 6) / kChunks : kStagesFit;
   static constexpr int kSmem = 1024 + kStages * kStageBytes;
   // tensor memory: accumulators, then per-stage scale-factor columns
-  static constexpr uint32_t kAccCols = kDual ? 256 : 128;
+  static constexpr uint32_t kAccCols = (uint32_t)kN * (kDual ? 2 : 1);
   static constexpr uint32_t kOpSfCols = kAtoms * 4;  // tensor-memory columns per operand
   static constexpr uint32_t kSfColsPerChunk = kOpSfCols * (kDual ? 3 : 2);
   static constexpr uint32_t kSfColsPerStage = kChunks * kSfColsPerChunk;
@@ -283,8 +295,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
   __shared__ int s_tlo, s_thi, s_cbase, s_ncols;
-  __shared__ float col_scale[kTileN];
-  __shared__ int col_row[kTileN];
+  __shared__ float col_scale[kMaxN];
+  __shared__ int col_row[kMaxN];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -303,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       s_cbase = 0;
       s_ncols = 1;
       s_tlo = 0;
-      s_thi = ((p.T + kTileN - 1) / kTileN) * p.mtiles;
+      s_thi = ((p.T + C::kN - 1) / C::kN) * p.mtiles;
     }
     for (int s = 0; s < C::kStages; ++s) {
       ptx::mbar_init(&full_bar[s], 1);
@@ -343,8 +355,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           slot = r.y;
           brow = r.z;
         } else {
-          tile_info<C::kRouted>(p, t0, mt, nt, e, slot);
-          brow = nt * kTileN + (C::kRouted ? p.pad_offsets[e] : 0);
+          tile_info<C::kRouted, C::kN>(p, t0, mt, nt, e, slot);
+          brow = nt * C::kN + (C::kRouted ? p.pad_offsets[e] : 0);
         }
       }
       for (int t = t0; t < thi && !abort_flag; t += gridDim.x) {
@@ -402,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (C::kFp4) {
               // kAtoms scale atoms (512 B each) per operand: atom columns
               // kq*kAtoms .. (kq+1)*kAtoms-1 of the row tile
-              unsigned char* sf = bdst + C::kTileBytes;
+              unsigned char* sf = bdst + C::kBBytes;
               const uint8_t* rec = p.arena + (uint64_t)slot * p.rec_bytes;
               const uint64_t aoff =
                   ((uint64_t)(arow / kTileM) * p.kgroups + (uint64_t)kq * C::kAtoms) * 512;
@@ -436,8 +448,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           slot = sn;
           brow = ntn * kTileN + pn;
         } else if (tn < thi) {
-          tile_info<false>(p, tn, mt, nt, e, slot);
-          brow = nt * kTileN;
+          tile_info<false, C::kN>(p, tn, mt, nt, e, slot);
+          brow = nt * C::kN;
         }
       }
     }
@@ -445,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ================= MMA issuer =================
     if (lane == 0) {
       // instruction descriptor: M = 128, N = 128, K-major A and B
-      uint32_t idesc = ((uint32_t)(kTileN >> 3) << 17) | ((uint32_t)(kTileM >> 4) << 24);
+      uint32_t idesc = ((uint32_t)(C::kN >> 3) << 17) | ((uint32_t)(kTileM >> 4) << 24);
       if (C::kNvf4) idesc |= (1u << 7) | (1u << 10);               // E2M1 x E2M1, UE4M3 scales
       else if (C::kMxf4) idesc |= (1u << 7) | (1u << 10) | (1u << 23);  // E2M1 x E2M1, UE8M0
       else idesc |= (1u << 4) | (1u << 7) | (1u << 10);            // fp32 D, bf16 A and B
@@ -477,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t a0 = ptx::smem_u32(st);
             const uint32_t a1 = a0 + C::kTileBytes;
             const uint32_t b = a0 + C::kTileBytes * (C::kDual ? 2 : 1);
-            const uint32_t sf = b + C::kTileBytes;
+            const uint32_t sf = b + C::kBBytes;
             const uint32_t sfcol =
                 C::kSfCol0 + (uint32_t)s * C::kSfColsPerStage + (uint32_t)c * C::kSfColsPerChunk;
             if (C::kFp4) {
@@ -499,7 +511,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::mma_nvf4(acc, da0, db, idesc, tmem + sfcol + kk * 4, sfb, accum);
                 if (C::kDual) {
                   const uint64_t da1 = ptx::smem_desc(a1 + kk * 32, 16, 1024, 2);
-                  ptx::mma_nvf4(acc + 128, da1, db, idesc, tmem + sfcol + 16 + kk * 4, sfb, accum);
+                  ptx::mma_nvf4(acc + C::kN, da1, db, idesc, tmem + sfcol + 16 + kk * 4, sfb, accum);
                 }
               } else if (C::kMxf4) {
                 // this K = 64 step's scales: atom kk / 2, bytes 0-1 (kk even)
@@ -510,14 +522,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::mma_mxf4(acc, da0, db, idesc | id, tmem + sfcol + at, sfb, accum);
                 if (C::kDual) {
                   const uint64_t da1 = ptx::smem_desc(a1 + kk * 32, 16, 1024, 2);
-                  ptx::mma_mxf4(acc + 128, da1, db, idesc | id, tmem + sfcol + C::kOpSfCols + at,
+                  ptx::mma_mxf4(acc + C::kN, da1, db, idesc | id, tmem + sfcol + C::kOpSfCols + at,
                                 sfb, accum);
                 }
               } else {
                 ptx::mma_bf16(acc, da0, db, idesc, accum);
                 if (C::kDual) {
                   const uint64_t da1 = ptx::smem_desc(a1 + kk * 32, 16, 1024, 2);
-                  ptx::mma_bf16(acc + 128, da1, db, idesc, accum);
+                  ptx::mma_bf16(acc + C::kN, da1, db, idesc, accum);
                 }
               }
             }
@@ -592,21 +604,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         dc = dn;
       }
     } else {
+      constexpr int kHalfN = C::kN / 2;  // columns per thread (the warp's column half)
       uint32_t it = 0;
       for (int t = tlo + blockIdx.x; t < thi; t += gridDim.x, ++it) {
         int mt, nt, e, slot;
-        tile_info<C::kRouted>(p, t, mt, nt, e, slot);
+        tile_info<C::kRouted, C::kN>(p, t, mt, nt, e, slot);
         int n_valid, col0;
         if (C::kRouted) {
           const int cnt = p.offsets[e + 1] - p.offsets[e];
-          n_valid = min(kTileN, cnt - nt * kTileN);
-          col0 = p.pad_offsets[e] + nt * kTileN;  // padded activation row of column 0
+          n_valid = min(C::kN, cnt - nt * C::kN);
+          col0 = p.pad_offsets[e] + nt * C::kN;  // padded activation row of column 0
         } else {
-          n_valid = min(kTileN, p.T - nt * kTileN);
-          col0 = nt * kTileN;
+          n_valid = min(C::kN, p.T - nt * C::kN);
+          col0 = nt * C::kN;
         }
         // per-column data (column = route or token)
-        if (et < kTileN) {
+        if (et < C::kN) {
           float sc = 1.f;
           int rr = col0 + et;
           if (et < n_valid) {
@@ -628,51 +641,68 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         ptx::tc_fence_after();
-        const uint32_t lane_addr =
-            tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)ab * C::kAccCols + (uint32_t)(ch * kHalf);
-        if (C::kDual) {
-          // gate/up: h = silu(g) * u formed chunk by chunk (64 values kept), then
-          // the accumulator is released and h is written
-          float hv[kHalf];
+        const uint32_t lane_addr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)ab * C::kAccCols +
+                                   (uint32_t)(ch * kHalfN);
+        if (EPI == EPI_GU_ROUTED) {
+          // routed gate/up: h = silu(g) * u formed chunk by chunk (64 values
+          // kept), then the accumulator is released and h is written
+          float hv[kHalfN];
 #pragma unroll
-          for (int c = 0; c < kHalf; c += 16) {
+          for (int c = 0; c < kHalfN; c += 16) {
             uint32_t ga[16], ua[16];
             ptx::tmem_ld_32x32b_x16(lane_addr + c, ga);
-            ptx::tmem_ld_32x32b_x16(lane_addr + 128 + c, ua);
+            ptx::tmem_ld_32x32b_x16(lane_addr + C::kN + c, ua);
             ptx::tmem_ld_wait();
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) {
               const float g = __uint_as_float(ga[jj]), u = __uint_as_float(ua[jj]);
-              if (EPI == EPI_GU_ROUTED) {
-                const float G = col_scale[ch * kHalf + c + jj];
-                hv[c + jj] = silu_f(g * gg * G) * (u * gu * G);
-              } else {
-                hv[c + jj] = silu_f(g) * u;
-              }
+              const float G = col_scale[ch * kHalfN + c + jj];
+              hv[c + jj] = silu_f(g * gg * G) * (u * gu * G);
             }
           }
           ptx::tc_fence_before();
           if (lane == 0) ptx::mbar_arrive(&acc_empty[ab]);  // the accumulator is free
 #pragma unroll
-          for (int jj = 0; jj < kHalf; ++jj) {
-            const int n = ch * kHalf + jj;
-            if (n < n_valid) {
-              if (EPI == EPI_GU_ROUTED)
-                p.h32[(size_t)(col0 + n) * p.h_ld + mt * kTileM + row] = hv[jj];
-              else
-                p.hs[(size_t)(col0 + n) * p.hs_ld + mt * kTileM + row] = f32_to_bf16_rne(hv[jj]);
+          for (int jj = 0; jj < kHalfN; ++jj) {
+            const int n = ch * kHalfN + jj;
+            if (n < n_valid) p.h32[(size_t)(col0 + n) * p.h_ld + mt * kTileM + row] = hv[jj];
+          }
+        } else if (C::kDual) {
+          // shared gate/up: h = silu(g) * u written as bf16 16 columns at a
+          // time; the (single) accumulator is released after the last read
+#pragma unroll 2
+          for (int c = 0; c < kHalfN; c += 16) {
+            uint32_t ga[16], ua[16];
+            ptx::tmem_ld_32x32b_x16(lane_addr + c, ga);
+            ptx::tmem_ld_32x32b_x16(lane_addr + C::kN + c, ua);
+            ptx::tmem_ld_wait();
+            if (c + 16 >= kHalfN) {
+              ptx::tc_fence_before();
+              if (lane == 0) ptx::mbar_arrive(&acc_empty[ab]);  // the accumulator is free
+            }
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) {
+              const int n = ch * kHalfN + c + jj;
+              const float h = silu_f(__uint_as_float(ga[jj])) * __uint_as_float(ua[jj]);
+              if (n < n_valid)
+                p.hs[(size_t)(col0 + n) * p.hs_ld + mt * kTileM + row] = f32_to_bf16_rne(h);
             }
           }
         } else {
-          // shared down: the token columns added into y_acc
-          uint32_t ra[32], rb[32];
-          ptx::tmem_ld_32x32b_x32(lane_addr, ra);
-          ptx::tmem_ld_32x32b_x32(lane_addr + 32, rb);
-          ptx::tmem_ld_wait();
-          ptx::tc_fence_before();
-          if (lane == 0) ptx::mbar_arrive(&acc_empty[ab]);  // the accumulator is free
-          add_columns(ra, rb, p.y_acc + mt * kTileM + row, col_scale + ch * kHalf,
-                      col_row + ch * kHalf, p.H, n_valid - ch * kHalf);
+          // shared down: the token columns added into y_acc, 64 at a time
+#pragma unroll 1
+          for (int c0 = 0; c0 < kHalfN; c0 += 64) {
+            uint32_t ra[32], rb[32];
+            ptx::tmem_ld_32x32b_x32(lane_addr + c0, ra);
+            ptx::tmem_ld_32x32b_x32(lane_addr + c0 + 32, rb);
+            ptx::tmem_ld_wait();
+            if (c0 + 64 >= kHalfN) {
+              ptx::tc_fence_before();
+              if (lane == 0) ptx::mbar_arrive(&acc_empty[ab]);  // the accumulator is free
+            }
+            add_columns(ra, rb, p.y_acc + mt * kTileM + row, col_scale + ch * kHalfN + c0,
+                        col_row + ch * kHalfN + c0, p.H, n_valid - ch * kHalfN - c0);
+          }
         }
         asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
       }
@@ -1117,14 +1147,14 @@ static moe_status load_encoder() {
   return MOE_OK;
 }
 
-// rows of `inner` elements (uint8 codes or bf16), box = 128 bytes x 128 rows,
+// rows of `inner` elements (uint8 codes or bf16), box = 128 bytes x box_rows rows,
 // 128-byte swizzle; optional third dimension (slots)
 static moe_status make_map(CUtensorMap* m, const void* base, bool bf16, uint64_t inner,
                            uint64_t rows, uint64_t row_stride_bytes, uint64_t slots,
-                           uint64_t slot_stride_bytes) {
+                           uint64_t slot_stride_bytes, uint32_t box_rows = 128) {
   cuuint64_t dims[3] = {inner, rows, slots};
   cuuint64_t strides[2] = {row_stride_bytes, slot_stride_bytes};
-  cuuint32_t box[3] = {bf16 ? 64u : 128u, 128u, 1u};
+  cuuint32_t box[3] = {bf16 ? 64u : 128u, box_rows, 1u};
   cuuint32_t estr[3] = {1u, 1u, 1u};
   const cuuint32_t rank = slots > 0 ? 3 : 2;
   CUresult r = g_encode(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8,
@@ -1269,8 +1299,8 @@ moe_status prefill_ffn(const moe_ffn_args* a, cudaStream_t s, int part, void (*m
     if ((st = make_map(&msg, a->s_gate, true, H, a->Is, (uint64_t)H * 2, 0, 0)) ||
         (st = make_map(&msu, a->s_up, true, H, a->Is, (uint64_t)H * 2, 0, 0)) ||
         (st = make_map(&msd, a->s_down, true, a->Is, H, (uint64_t)a->Is * 2, 0, 0)) ||
-        (st = make_map(&mx, a->x, true, H, a->T, (uint64_t)H * 2, 0, 0)) ||
-        (st = make_map(&mhs, ws + W.hs, true, a->Is, a->T, (uint64_t)a->Is * 2, 0, 0)))
+        (st = make_map(&mx, a->x, true, H, a->T, (uint64_t)H * 2, 0, 0, kSharedN)) ||
+        (st = make_map(&mhs, ws + W.hs, true, a->Is, a->T, (uint64_t)a->Is * 2, 0, 0, kSharedN)))
       return st;
   }
 
