@@ -521,11 +521,12 @@ def bench_prefill(args, torch, moe, gen, gd, dev, peaks, group=None, wl=None, la
     # per-kernel pass: the layer's timing hook marks every kernel of the step
     # (router, permutation, token quantisation, tile tables, per launch group
     # the gate/up GEMM, h quantisation and down GEMM, the shared expert's two
-    # GEMMs, the combine); L2 flushed before each step
+    # GEMMs - the down one writes y - or else the combine); L2 flushed before
+    # each step
     n_lg = (-(-min(T * k, E) // dw_group)) if dw_group else 1
     names = (["router", "permute", "quant_tokens", "tile_plan"]
              + [n for _ in range(n_lg) for n in ("gemm_gate_up", "quant_h", "gemm_down")]
-             + (["gemm_shared_gate_up", "gemm_shared_down"] if Is else []) + ["combine"])
+             + (["gemm_shared_gate_up", "gemm_shared_down"] if Is else ["combine"]))
     hev = [torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
     for e in hev:
         e.record(stream)

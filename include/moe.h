@@ -440,7 +440,11 @@ moe_status moe_combine(const moe_combine_args* a, void* stream);
  * staging slots, while the first stream runs the GEMMs of the hits and of
  * the groups already landed (the "groups of 64 experts through a staging
  * buffer" of the dev.to page); the streams are joined before the forward's
- * last kernel.
+ * last kernel.  The prefill path clears its fp32 sum of the experts'
+ * outputs inside the token quantisation; with a shared expert and one FFN
+ * call (every active expert resident, or no staging slots) the shared
+ * expert's down GEMM, the last to add into that sum, writes y = bf16(sum +
+ * shared) itself and no separate combine runs.
  *
  * skip_tau > 0 turns on the renorm-skip (Strata-GLM blog, section
  * "Uncensoring without touching the weights"): a route whose expert is not
@@ -498,7 +502,8 @@ moe_status moe_layer_debug_prefill(const moe_layer* l, const float** h_rows,
  * decode one kernel, prefill each of its kernels (token quantisation, tile
  * tables, per launch group the gate/up GEMM, h quantisation and down GEMM,
  * then the shared expert's two GEMMs), then the combine (when it is a kernel
- * of its own).  So the caller can time each kernel of the layer's own
+ * of its own: not in a prefill whose shared-expert down GEMM writes y).  So
+ * the caller can time each kernel of the layer's own
  * sequence.
  * n = 0 clears the hook.  n > 32 is MOE_ERR_INVALID_ARG. */
 moe_status moe_layer_set_timing(moe_layer* l, void* const* events, int n);

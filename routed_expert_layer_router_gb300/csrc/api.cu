@@ -21,7 +21,7 @@ moe_status decode_setup();
 size_t prefill_workspace_bytes(int T, int H, int I, int E, int k, int Is);
 const float* prefill_h_rows(const void* workspace, int T, int H, int I, int E, int k, int Is);
 moe_status prefill_ffn(const moe_ffn_args* a, cudaStream_t s, int part, void (*mark)(void*),
-                       void* mark_ctx);
+                       void* mark_ctx, bool zero_y, uint16_t* y);
 moe_status prefill_setup();
 moe_status nvfp4_quantize(const void* x, int dtype, int T, int K, uint8_t* codes,
                           uint8_t* scales, float* G, cudaStream_t s);
@@ -116,7 +116,7 @@ static moe_status expert_ffn(const moe_ffn_args* a, void* stream, const DecodeFu
   }
   if (a->mode == MOE_MODE_PREFILL) {
     if (!a->y_acc || !a->pad_offsets) return MOE_ERR_INVALID_ARG;
-    return prefill_ffn(a, (cudaStream_t)stream, part, fz.mark, fz.mark_ctx);
+    return prefill_ffn(a, (cudaStream_t)stream, part, fz.mark, fz.mark_ctx, fz.pf_zero_y, fz.pf_y);
   }
   return MOE_ERR_INVALID_ARG;
 }
@@ -297,8 +297,11 @@ static moe_status prefill_streamed(moe_layer* l, moe_ffn_args* fa, cudaStream_t 
   const int max_miss = fa->T * d.k < d.E ? fa->T * d.k : d.E;
   const int groups = (max_miss + S2 - 1) / S2;
   const int32_t* dst = policy ? l->miss_dst : nullptr;
+  // the token quantisation (first call) clears y_acc; the shared expert runs
+  // with the hits, before the misses' GEMMs, so a separate combine writes y
   const DecodeFuse marks = {layer_mark_cb, l, nullptr, false, false, nullptr, nullptr,
-                            nullptr, nullptr, nullptr, 0,       nullptr, nullptr, nullptr};
+                            nullptr, nullptr, nullptr, 0,       nullptr, nullptr, nullptr,
+                            true,          nullptr};
   moe_status st;
   auto gather = [&](int g) -> moe_status {
     const int h = g & 1, cnt = S2 < max_miss - g * S2 ? S2 : max_miss - g * S2;
@@ -329,8 +332,12 @@ static moe_status prefill_streamed(moe_layer* l, moe_ffn_args* fa, cudaStream_t 
   return MOE_OK;
 }
 
-// y = bf16(y_acc): the prefill path's combine (its down GEMMs added into y_acc)
-static moe_status finish_prefill(moe_layer* l, int T, void* y, void* stream) {
+// y = bf16(y_acc): the prefill path's combine (its down GEMMs added into y_acc),
+// unless the shared expert's down GEMM already wrote y (y_written)
+static moe_status finish_prefill(moe_layer* l, int T, void* y, void* stream,
+                                 bool y_written = false) {
+  l->last_T = T;
+  if (y_written) return MOE_OK;
   moe_combine_args ca;
   memset(&ca, 0, sizeof(ca));
   ca.T = T; ca.H = l->d.H; ca.k = l->d.k;
@@ -340,7 +347,6 @@ static moe_status finish_prefill(moe_layer* l, int T, void* y, void* stream) {
   moe_status st = moe_combine(&ca, stream);
   if (st != MOE_OK) return st;
   layer_mark(l);
-  l->last_T = T;
   return MOE_OK;
 }
 
@@ -443,8 +449,6 @@ MOE_API moe_status moe_layer_forward(moe_layer* l, const void* x, int T, void* y
   fa.y_acc = l->y_acc;
   fa.workspace = l->ffn_ws; fa.workspace_bytes = l->ffn_ws_bytes;
   fa.status = l->status;
-  if (prefill && cudaMemsetAsync(l->y_acc, 0, (size_t)T * d.H * 4, s) != cudaSuccess)
-    return MOE_ERR_CUDA;
   if (prefill && n_stage >= 2) {
     if ((st = prefill_streamed(l, &fa, s, policy)) != MOE_OK) return st;
     return finish_prefill(l, T, y, stream);
@@ -478,6 +482,10 @@ MOE_API moe_status moe_layer_forward(moe_layer* l, const void* x, int T, void* y
       fz.inv = l->inv;
       fz.y = (uint16_t*)y;
     }
+    // prefill: the token quantisation clears y_acc; with one FFN call its
+    // shared-expert down GEMM is the last writer of y_acc and writes y
+    fz.pf_zero_y = prefill;
+    fz.pf_y = (prefill && groups == 1 && d.Is > 0) ? (uint16_t*)y : nullptr;
     if ((st = expert_ffn(&fa, stream, fz)) != MOE_OK) return st;
   }
   if (!prefill && groups == 1) {
@@ -485,7 +493,7 @@ MOE_API moe_status moe_layer_forward(moe_layer* l, const void* x, int T, void* y
     return MOE_OK;
   }
 
-  if (prefill) return finish_prefill(l, T, y, stream);
+  if (prefill) return finish_prefill(l, T, y, stream, groups == 1 && d.Is > 0);
   moe_combine_args ca;
   memset(&ca, 0, sizeof(ca));
   ca.T = T; ca.H = d.H; ca.k = d.k;

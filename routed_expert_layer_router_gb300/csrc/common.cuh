@@ -161,6 +161,10 @@ struct DecodeFuse {
   const int32_t* g_miss_ids;
   const int32_t* g_n_miss;
   const int32_t* g_dst_slots;
+  // prefill: clear y_acc in the token quantisation; write y from the shared
+  // expert's down GEMM (the call's last writer of y_acc), or nullptr
+  bool pf_zero_y;
+  uint16_t* pf_y;
 };
 
 // the gather fields of one layer's records (cache.cu)

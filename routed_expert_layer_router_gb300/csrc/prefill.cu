@@ -96,6 +96,8 @@ struct GemmParams {
   float* h32;       int h_ld;   // routed gate/up: h [rows][I]
   uint16_t* hs;     int hs_ld;  // shared gate/up: h [T][Is] bf16
   float* y_acc;     int H;      // down: y_acc [T][H]
+  uint16_t* y;                  // shared down only: write y = bf16(y_acc + shared) instead of
+                                // adding into y_acc (it is then the last writer of y_acc)
   int32_t* status;
 };
 
@@ -280,6 +282,26 @@ __device__ __forceinline__ void add_columns(const uint32_t (&ra)[32], const uint
   for (int jj = 0; jj < 32; ++jj)
     if (32 + jj < nv)
       ptx::red_add_f32(yb + (size_t)cr[32 + jj] * H, __uint_as_float(rb[jj]) * cs[32 + jj]);
+}
+
+// The same columns as add_columns, as the layer's last contribution: each
+// y_acc element plus the column's value, rounded to bf16 into y (one 128-byte
+// read and one 64-byte write per warp instruction); no other CTA writes them.
+// All 32 reads of a register set are issued before the first write.
+__device__ __forceinline__ void write_col32(const uint32_t (&r)[32], const float* ya,
+                                            uint16_t* yb, const int* cr, int H, int nv) {
+  float v[32];
+#pragma unroll
+  for (int jj = 0; jj < 32; ++jj) v[jj] = jj < nv ? __ldcg(ya + (size_t)cr[jj] * H) : 0.f;
+#pragma unroll
+  for (int jj = 0; jj < 32; ++jj)
+    if (jj < nv) yb[(size_t)cr[jj] * H] = f32_to_bf16_rne(v[jj] + __uint_as_float(r[jj]));
+}
+__device__ __forceinline__ void write_columns(const uint32_t (&ra)[32], const uint32_t (&rb)[32],
+                                              const float* ya, uint16_t* yb, const int* cr,
+                                              int H, int nv) {
+  write_col32(ra, ya, yb, cr, H, nv);
+  write_col32(rb, ya, yb, cr + 32, H, nv - 32);
 }
 
 template <int KIND, int EPI>
@@ -700,8 +722,12 @@ __global__ void __launch_bounds__(kThreads, 1)
               ptx::tc_fence_before();
               if (lane == 0) ptx::mbar_arrive(&acc_empty[ab]);  // the accumulator is free
             }
-            add_columns(ra, rb, p.y_acc + mt * kTileM + row, col_scale + ch * kHalfN + c0,
-                        col_row + ch * kHalfN + c0, p.H, n_valid - ch * kHalfN - c0);
+            if (p.y)
+              write_columns(ra, rb, p.y_acc + mt * kTileM + row, p.y + mt * kTileM + row,
+                            col_row + ch * kHalfN + c0, p.H, n_valid - ch * kHalfN - c0);
+            else
+              add_columns(ra, rb, p.y_acc + mt * kTileM + row, col_scale + ch * kHalfN + c0,
+                          col_row + ch * kHalfN + c0, p.H, n_valid - ch * kHalfN - c0);
           }
         }
         asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
@@ -1015,12 +1041,15 @@ __global__ void __launch_bounds__(256) k_quant_rows_f32(const float* __restrict_
 // of expert e goes to row pad_offsets[e] + p - offsets[e]).  CTA t < T takes
 // token t: 256 threads, thread i holding 16-byte chunks i + 256 m (8 values;
 // two threads per block).  CTA T + e zeroes expert e's padding rows.  With
-// inv == NULL (k = 1) token t goes to row t and no rows are padded.
+// inv == NULL (k = 1) token t goes to row t and no rows are padded.  With
+// y_zero, CTA t also zeroes row t of y_zero (K floats): the down GEMMs' sum,
+// cleared inside this latency-bound kernel instead of by a separate pass.
 template <int KMAX, int FMT>
 __global__ void __launch_bounds__(256) k_quant_routes(
     const uint16_t* __restrict__ x, int T, int K, int E, int k, const int32_t* __restrict__ inv,
     const int32_t* __restrict__ offsets, const int32_t* __restrict__ pad_offsets,
-    uint8_t* __restrict__ codes, uint8_t* __restrict__ scales, float* __restrict__ G) {
+    uint8_t* __restrict__ codes, uint8_t* __restrict__ scales, float* __restrict__ G,
+    float* __restrict__ y_zero) {
   constexpr int kNJ = KMAX / 2048;
   __shared__ int s_row[32];
   __shared__ float s_max[8];
@@ -1040,6 +1069,10 @@ __global__ void __launch_bounds__(256) k_quant_routes(
   for (int m = 0; m < kNJ; ++m) {
     const int c = tid + 256 * m;
     v[m] = c < NC ? __ldg(xr + c) : make_uint4(0u, 0u, 0u, 0u);
+  }
+  if (y_zero) {
+    float4* yz = reinterpret_cast<float4*>(y_zero + (size_t)t * K);
+    for (int c = tid; c < K / 4; c += 256) yz[c] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
   if (tid < k) {
     int row = -1;
@@ -1220,7 +1253,7 @@ moe_status nvfp4_quantize(const void* x, int dtype, int T, int K, uint8_t* codes
     auto* kx = K <= 4096 ? k_quant_routes<4096, MOE_FMT_NVFP4>
                          : k_quant_routes<kQuantXMaxK, MOE_FMT_NVFP4>;
     kx<<<T, 256, 0, s>>>((const uint16_t*)x, T, K, 1, 1, nullptr, nullptr, nullptr, codes, scales,
-                         G);
+                         G, nullptr);
   } else {
     auto* kq = K <= 2048 ? k_quant_rows_f32<2048> : k_quant_rows_f32<kQuantHMaxK>;
     kq<<<(T + 7) / 8, 256, 0, s>>>((const float*)x, T, K, codes, scales, G);
@@ -1261,9 +1294,12 @@ moe_status tmap_bf16_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64
 
 // part (the layer's own sequence): 0 = the call's whole group; for group 0, 1 =
 // the token quantisation, tile tables, hits and shared expert, 2 = the first
-// misses (whose records the layer gathers meanwhile)
+// misses (whose records the layer gathers meanwhile).  Also the layer's own:
+// zero_y clears y_acc in the token quantisation (instead of the caller); y,
+// when this call's shared-expert down is the last writer of y_acc, makes it
+// write y = bf16(y_acc + shared) itself (no separate combine).
 moe_status prefill_ffn(const moe_ffn_args* a, cudaStream_t s, int part, void (*mark)(void*),
-                       void* mark_ctx) {
+                       void* mark_ctx, bool zero_y, uint16_t* y) {
   // the timing hook: a mark after every kernel of the FFN
   auto marked = [&]() {
     if (mark) mark(mark_ctx);
@@ -1326,7 +1362,7 @@ moe_status prefill_ffn(const moe_ffn_args* a, cudaStream_t s, int part, void (*m
                                : k_quant_routes<kQuantXMaxK, MOE_FMT_NVFP4>);
     kx<<<a->T + a->E, 256, 0, s>>>((const uint16_t*)a->x, a->T, H, a->E, a->k, a->inv, a->offsets,
                                    a->pad_offsets, ws + W.xq_codes, ws + W.xq_scales,
-                                   (float*)(ws + W.xq_G));
+                                   (float*)(ws + W.xq_G), zero_y ? a->y_acc : nullptr);
     MOE_CHECK_LAUNCH();
     marked();
     k_tile_plan<<<1, 1024, 0, s>>>(a->act_list, a->n_act, a->offsets, a->pad_offsets, a->src_slot,
@@ -1398,6 +1434,7 @@ moe_status prefill_ffn(const moe_ffn_args* a, cudaStream_t s, int part, void (*m
     gp.mtiles = H / kTileM;
     gp.kstages = (a->Is * 2) / kStageKB;
     gp.y_acc = a->y_acc;
+    gp.y = y;
     if ((st = launch_gemm<1, EPI_DOWN_SHARED>(msd, msd, mhs, gp, s)) != MOE_OK) return st;
     marked();
   }

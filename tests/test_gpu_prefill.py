@@ -160,3 +160,67 @@ def test_masked_prefill_parity(group):
             check_outputs(y_to_f64(y), y_ref, bound=bound)
     finally:
         dw.close()
+
+
+def test_prefill_public_calls_match_the_layer():
+    """The PREFILL expert FFN through the individual ABI calls (route, padded
+    permutation, lookup, moe_expert_ffn adding into a caller-zeroed y_acc,
+    moe_combine) against the oracle, beside the layer's own sequence (which
+    clears its sum in the token quantisation and lets the shared expert's
+    down GEMM write y): both within the tolerance on the same tokens."""
+    from routed_expert_layer_router_gb300 import moe
+    import gen.device as gd
+    dw = gd.build(SMALL, T_max=SMALL.T)
+    try:
+        wl = SMALL
+        T, H, I, E, k, Is = wl.T, wl.H, wl.I, wl.E, wl.k, wl.Is
+        x = draw_prefill_tokens(dw, 0, T)
+        y_layer = dw.moe_layers[0].forward(to_dev_bf16(x))
+        s = torch.cuda.current_stream().cuda_stream
+        i32, f32 = torch.int32, torch.float32
+        z = {n: torch.zeros(sz, dtype=dt, device="cuda") for n, sz, dt in (
+            ("ids", T * k, i32), ("w", T * k, f32), ("p", T * k, f32), ("lg", T * E, f32),
+            ("counts", E, i32), ("off", E + 1, i32), ("pad", E + 1, i32), ("perm", T * k, i32),
+            ("inv", T * k, i32), ("src", E, i32), ("act", E, i32), ("nact", 2, i32),
+            ("miss", E, i32), ("nmiss", 1, i32), ("st", 1, i32), ("os", T * H, f32),
+            ("yacc", T * H, f32))}
+        xd = to_dev_bf16(x)
+        ra = moe.moe_route_args()
+        ra.x, ra.w_router = xd.data_ptr(), dw.w_router[0].data_ptr()
+        ra.T, ra.H, ra.E, ra.k = T, H, E, k
+        ra.ids, ra.w, ra.p_sel, ra.logits = (z[n].data_ptr() for n in ("ids", "w", "p", "lg"))
+        moe.moe_route(ra, s)
+        moe.moe_permute(z["ids"].data_ptr(), T, k, E, z["counts"].data_ptr(), z["off"].data_ptr(),
+                        z["perm"].data_ptr(), z["inv"].data_ptr(), z["pad"].data_ptr(), 128,
+                        z["st"].data_ptr(), s)
+        moe.expcache_lookup(dw.cache.handle, 0, z["counts"].data_ptr(), z["src"].data_ptr(),
+                            z["act"].data_ptr(), z["nact"].data_ptr(), z["miss"].data_ptr(),
+                            z["nmiss"].data_ptr(), z["st"].data_ptr(), s)
+        ws_b = moe.moe_ffn_workspace_bytes(1, T, H, I, E, k, Is)
+        ws = torch.empty(ws_b, dtype=torch.uint8, device="cuda")
+        fa = moe.moe_ffn_args()
+        fa.mode, fa.stages, fa.T, fa.H, fa.I, fa.E, fa.k = 1, 3, T, H, I, E, k
+        fa.x, fa.cache, fa.gscale = xd.data_ptr(), dw.cache.handle, dw.gscale[0].data_ptr()
+        fa.src_slot, fa.act_list, fa.n_act = (z[n].data_ptr() for n in ("src", "act", "nact"))
+        fa.offsets, fa.pad_offsets = z["off"].data_ptr(), z["pad"].data_ptr()
+        fa.perm, fa.inv, fa.w = z["perm"].data_ptr(), z["inv"].data_ptr(), z["w"].data_ptr()
+        fa.group, fa.n_stage, fa.prefill_group, fa.Is = 0, 0, wl.group, Is
+        fa.s_gate, fa.s_up, fa.s_down = (t.data_ptr() for t in dw.shared[0])
+        fa.o_shared, fa.y_acc = z["os"].data_ptr(), z["yacc"].data_ptr()
+        fa.workspace, fa.workspace_bytes, fa.status = ws.data_ptr(), ws_b, z["st"].data_ptr()
+        moe.moe_expert_ffn(fa, s)
+        y_pub = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+        ca = moe.moe_combine_args()
+        ca.T, ca.H, ca.k = T, H, k
+        ca.y_acc, ca.inv, ca.y = z["yacc"].data_ptr(), z["inv"].data_ptr(), y_pub.data_ptr()
+        moe.moe_combine(ca, s)
+        torch.cuda.synchronize()
+        assert z["st"].item() == 0 and dw.moe_layers[0].read_status() == 0
+        y_ref, _, _, _, bound = oracle_layer(dw, 0, x, mode=1, return_bound=True)
+        check_outputs(y_to_f64(y_pub), y_ref, bound=bound)
+        check_outputs(y_to_f64(y_layer), y_ref, bound=bound)
+        # the two orders of adding the shared expert differ by bf16 rounding at most
+        d = np.abs(y_to_f64(y_pub) - y_to_f64(y_layer))
+        assert d.max() <= 2.0 ** -7 * np.abs(y_to_f64(y_layer)).max()
+    finally:
+        dw.close()
