@@ -4,7 +4,8 @@ against the oracle: the bit-built identity expert exact through the decode
 and the prefill (tcgen05 kind::mxf4nvf4, scale_vec::2X) paths; the tiny layer
 and the 6144 x 2048, 288-expert decode layer; negative controls (flipped
 nibble order, scales decoded as the other format) far from the GPU; the
-prefill path on a small layer and, masked, on the 288-expert layer."""
+prefill path on a small layer, masked on the 288-expert layer, and on the
+4096-token layer (every token's routing; 32 clean tokens' outputs)."""
 import dataclasses
 
 import numpy as np
@@ -157,5 +158,48 @@ def test_mx_masked_prefill_parity():
             check_prefill_h(dw, 0, x, layer.debug_prefill(T)["h"].cpu().numpy(),
                             dbg["perm"].cpu().numpy(), [0, T - 1])
             check_outputs(y_to_f64(y), y_ref, bound=bound)
+    finally:
+        dw.close()
+
+
+PREFILL_MX = dataclasses.replace(gen.WORKLOADS["prefill"], name="prefill-mx", fmt=gen.MXFP4,
+                                 seed=13)
+
+
+def test_mx_prefill_4096_tokens_parity():
+    """The 4096-token MXFP4 prefill layer (288 experts top-8, all resident,
+    router logits on the tensor cores) in the bench's launch configuration:
+    ids, weights and probabilities of every token and the permutation against
+    the oracle's router; outputs of 32 clean tokens whose routes reach every
+    group of 64 experts."""
+    import gen.device as gd
+    from tests.gpu_common import prefill_clean
+    wl = PREFILL_MX
+    dw = gd.build(wl, T_max=wl.T)
+    try:
+        Wr, bias, sh = host_inputs(dw, 0)
+        x, _ = draw_tokens(wl, 0, wl.T, Wr, bias, batch=512)
+        layer = dw.moe_layers[0]
+        y = layer.forward(to_dev_bf16(x))
+        torch.cuda.synchronize()
+        assert layer.read_status() == 0
+        dbg = layer.debug(wl.T)
+        ids_r, w_r, p_r, _, _ = oracle.route(x, Wr, bias, wl.k)
+        check_router(dbg, ids_r, w_r, p_r)
+        check_permutation(dbg, ids_r)
+        order = (np.arange(wl.T) * 1031) % wl.T
+        sample = []
+        for i0 in range(0, wl.T, 48):
+            cand = order[i0:i0 + 48]
+            ok = prefill_clean(dw, 0, x[cand], ids_r[cand])
+            sample += [int(t) for t in cand[ok]]
+            if len(sample) >= 32:
+                break
+        sample = sorted(sample[:32])
+        assert len(sample) == 32
+        assert set(ids_r[sample].ravel() // 64) == set(range((wl.E + 63) // 64))
+        y_ref, ids_s, _, _, bound = oracle_layer(dw, 0, x[sample], mode=1, return_bound=True)
+        assert np.array_equal(ids_s, ids_r[sample])
+        check_outputs(y_to_f64(y)[sample], y_ref, bound=bound)
     finally:
         dw.close()
