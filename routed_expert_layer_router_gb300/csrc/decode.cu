@@ -28,6 +28,12 @@ constexpr int kDecThreads = kDecWarps * 32;
 constexpr int kXPad = 36;  // fp32 staging: floats per 32 values (bank spread)
 constexpr int kHPad = 40;  // f16 staging: halves per 32 values (80-byte stride, conflict-free)
 constexpr int kSharedKSplit = kDecWarps;  // shared gate/up: warps splitting the row length
+// routed gate/up units: a warp takes kGuRows rows of the gate and of the up
+// matrix, rows m0 + 32 (mo + m1) (m1 < kGuRows) of a 128-row tile; a tile is
+// kGuParts units (4 quarters of m0 times the row groups mo)
+constexpr int kGuRows = 4;
+constexpr int kGuParts = 4 * (4 / kGuRows);
+constexpr int kGuMinBlocks = 2;  // CTAs per SM the gate/up kernel is compiled for
 
 struct DecodeParams {
   int T, H, I, E, k, Is;
@@ -374,24 +380,24 @@ __device__ __forceinline__ void load_xh(const __half* xs, int nhk, int hk, uint3
   }
 }
 
-// gate+up of the 4 rows {rt*128 + m0 + 32*m1} of one expert, M staged tokens.
-// Returns warp-reduced sums (all lanes).
-// One lane's 32-value step of a warp's 4 gate + 4 up rows: codes and the two
-// scale atom rows.
+// gate+up of the kGuRows rows {rt*128 + m0 + 32*(mo + m1)} of one expert, M
+// staged tokens.  Returns warp-reduced sums (all lanes).
+// One lane's 32-value step of a warp's gate and up rows: codes and the two
+// scale atom rows (an atom row holds the scales of rows m0 + 32 i, i < 4).
 struct GuRegs {
-  uint4 g[4], u[4], sg, su;
+  uint4 g[kGuRows], u[kGuRows], sg, su;
 };
 template <int FMT>
 __device__ __forceinline__ void gu_fetch(const uint8_t* rec, const RecordLayout& L, int H, int rt,
-                                         int m0, int hk, GuRegs& r) {
-  const uint8_t* gc = rec + L.gate_codes + (uint64_t)(rt * 128 + m0) * (H / 2);
-  const uint8_t* uc = rec + L.up_codes + (uint64_t)(rt * 128 + m0) * (H / 2);
+                                         int m0, int mo, int hk, GuRegs& r) {
+  const uint8_t* gc = rec + L.gate_codes + (uint64_t)(rt * 128 + m0 + 32 * mo) * (H / 2);
+  const uint8_t* uc = rec + L.up_codes + (uint64_t)(rt * 128 + m0 + 32 * mo) * (H / 2);
   const uint64_t rstride = (uint64_t)32 * (H / 2);
   const uint64_t aoff = step_atom_row<FMT>(rt, hk, m0, H);
   r.sg = ldg_stream(rec + L.gate_scales + aoff);
   r.su = ldg_stream(rec + L.up_scales + aoff);
 #pragma unroll
-  for (int m1 = 0; m1 < 4; ++m1) {
+  for (int m1 = 0; m1 < kGuRows; ++m1) {
     r.g[m1] = ldg_stream(gc + m1 * rstride + (uint64_t)hk * 16);
     r.u[m1] = ldg_stream(uc + m1 * rstride + (uint64_t)hk * 16);
   }
@@ -404,27 +410,27 @@ __device__ __forceinline__ void gu_fetch(const uint8_t* rec, const RecordLayout&
 // the 128 registers a thread has at two CTAs per SM and spilled.
 template <int M, int FMT>
 __device__ void warp_gu_fp4(const uint8_t* rec, const RecordLayout& L, int H, int rt, int m0,
-                            const __half* xs, float accg[4][M], float accu[4][M],
-                            const GuRegs& first) {
+                            int mo, const __half* xs, float accg[kGuRows][M],
+                            float accu[kGuRows][M], const GuRegs& first) {
   const int lane = threadIdx.x & 31;
   const int nhk = H / 32;
 #pragma unroll
-  for (int m1 = 0; m1 < 4; ++m1)
+  for (int m1 = 0; m1 < kGuRows; ++m1)
 #pragma unroll
     for (int j = 0; j < M; ++j) accg[m1][j] = accu[m1][j] = 0.f;
-  uint4 cg[4], cu[4], sg = first.sg, su = first.su;
+  uint4 cg[kGuRows], cu[kGuRows], sg = first.sg, su = first.su;
 #pragma unroll
-  for (int m1 = 0; m1 < 4; ++m1) {
+  for (int m1 = 0; m1 < kGuRows; ++m1) {
     cg[m1] = first.g[m1];
     cu[m1] = first.u[m1];
   }
   auto fetch = [&](int hk, uint4* g4, uint4* u4, uint4& sgv, uint4& suv) {
     GuRegs r;
-    gu_fetch<FMT>(rec, L, H, rt, m0, hk, r);
+    gu_fetch<FMT>(rec, L, H, rt, m0, mo, hk, r);
     sgv = r.sg;
     suv = r.su;
 #pragma unroll
-    for (int m1 = 0; m1 < 4; ++m1) {
+    for (int m1 = 0; m1 < kGuRows; ++m1) {
       g4[m1] = r.g[m1];
       u4[m1] = r.u[m1];
     }
@@ -434,14 +440,14 @@ __device__ void warp_gu_fp4(const uint8_t* rec, const RecordLayout& L, int H, in
     uint32_t xh[M * 16];
     load_xh<M>(xs, nhk, hk, xh);
 #pragma unroll
-    for (int m1 = 0; m1 < 4; ++m1) {
-      row_step<M, FMT>(cg[m1], sg, m1, hk, xh, accg[m1]);
-      row_step<M, FMT>(cu[m1], su, m1, hk, xh, accu[m1]);
+    for (int m1 = 0; m1 < kGuRows; ++m1) {
+      row_step<M, FMT>(cg[m1], sg, mo + m1, hk, xh, accg[m1]);
+      row_step<M, FMT>(cu[m1], su, mo + m1, hk, xh, accu[m1]);
     }
     if (more) fetch(hk + 32, cg, cu, sg, su);
   }
 #pragma unroll
-  for (int m1 = 0; m1 < 4; ++m1)
+  for (int m1 = 0; m1 < kGuRows; ++m1)
 #pragma unroll
     for (int j = 0; j < M; ++j) {
       accg[m1][j] = warp_sum(accg[m1][j]);
@@ -511,18 +517,18 @@ __device__ void down_shared_pass(const DecodeParams& p, int r0, int t0, int mm, 
 // ---- K-decode-gu -------------------------------------------------------------
 template <int M, int FMT>
 __device__ void gu_routed_pass(const DecodeParams& p, const RecordLayout& L, const uint8_t* rec,
-                               int rt, int m0, int q0, int mm, const __half* xs, float gg,
-                               float gu, const GuRegs& first) {
-  float accg[4][M], accu[4][M];
-  warp_gu_fp4<M, FMT>(rec, L, p.H, rt, m0, xs, accg, accu, first);
+                               int rt, int m0, int mo, int q0, int mm, const __half* xs,
+                               float gg, float gu, const GuRegs& first) {
+  float accg[kGuRows][M], accu[kGuRows][M];
+  warp_gu_fp4<M, FMT>(rec, L, p.H, rt, m0, mo, xs, accg, accu, first);
   const int lane = threadIdx.x & 31;
 #pragma unroll
-  for (int m1 = 0; m1 < 4; ++m1)
+  for (int m1 = 0; m1 < kGuRows; ++m1)
 #pragma unroll
     for (int j = 0; j < M; ++j)
       if (lane == m1 * M + j && j < mm) {
         const float g = accg[m1][j] * gg, u = accu[m1][j] * gu;
-        p.h_route[(size_t)(q0 + j) * p.I + rt * 128 + m0 + 32 * m1] = silu_f(g) * u;
+        p.h_route[(size_t)(q0 + j) * p.I + rt * 128 + m0 + 32 * (mo + m1)] = silu_f(g) * u;
       }
 }
 
@@ -568,7 +574,7 @@ __device__ void gu_shared_pass(const DecodeParams& p, int i0, int t0, int mm, co
 // 32 atom rows) first, then the shared-expert units (4 row pairs each), which
 // are half as large and so fill the last wave.
 template <int MAXM, int FMT>
-__global__ void __launch_bounds__(kDecThreads, MAXM == 1 ? 2 : 1) k_decode_gu(DecodeParams p) {
+__global__ void __launch_bounds__(kDecThreads, MAXM == 1 ? kGuMinBlocks : 1) k_decode_gu(DecodeParams p) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   __shared__ float red[kDecWarps * 8 * 2];
   const int wid = threadIdx.x >> 5;
@@ -610,8 +616,9 @@ __global__ void __launch_bounds__(kDecThreads, MAXM == 1 ? 2 : 1) k_decode_gu(De
   __half* xs = reinterpret_cast<__half*>(smem_raw);
   const int ur = u;
   const int tiles = p.I / 128;
-  const int a = ur / (tiles * 4), rem = ur % (tiles * 4);
-  const int rt = rem >> 2, m0 = (rem & 3) * kDecWarps + wid;
+  const int a = ur / (tiles * kGuParts), rem = ur % (tiles * kGuParts);
+  const int rt = rem / kGuParts, part = rem % kGuParts;
+  const int m0 = (part & 3) * kDecWarps + wid, mo = (part >> 2) * kGuRows;
   ActExpert ax;
   if (!act_expert(p, a, ax)) return;
   const int slot = ax.slot;
@@ -627,16 +634,16 @@ __global__ void __launch_bounds__(kDecThreads, MAXM == 1 ? 2 : 1) k_decode_gu(De
   for (int q0 = pb; q0 < pe; q0 += p.maxm) {
     const int mm = min(p.maxm, pe - q0);
     GuRegs first;  // the weights' first step, in flight while the tokens are staged
-    if (lane < p.H / 32) gu_fetch<FMT>(rec, L, p.H, rt, m0, lane, first);
+    if (lane < p.H / 32) gu_fetch<FMT>(rec, L, p.H, rt, m0, mo, lane, first);
     const uint16_t* rows[2];
     for (int j = 0; j < mm; ++j) rows[j] = p.x + (size_t)(p.perm[q0 + j] / p.k) * p.H;
     __syncthreads();
     const bool bad = stage_bf16_to_f16(xs, rows, mm, p.H);
     if (__syncthreads_or(bad) && threadIdx.x == 0) set_status(p.status, MOE_ERR_UNSUPPORTED);
     if (MAXM == 2 && mm == 2)
-      gu_routed_pass<MAXM, FMT>(p, L, rec, rt, m0, q0, mm, xs, gg, gu, first);
+      gu_routed_pass<MAXM, FMT>(p, L, rec, rt, m0, mo, q0, mm, xs, gg, gu, first);
     else
-      gu_routed_pass<1, FMT>(p, L, rec, rt, m0, q0, mm, xs, gg, gu, first);
+      gu_routed_pass<1, FMT>(p, L, rec, rt, m0, mo, q0, mm, xs, gg, gu, first);
   }
 }
 
@@ -951,7 +958,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) k_decode_ffn(DecodeParams p) {
   const int n_gw = p.n_gather_workers;
   const int n_sgu = p.n_shared_units, n_rgu = p.n_routed_units;
   const int n_sd = p.n_sdown_units, n_rd = p.n_rdown_units;
-  const int gu_units = (p.I / 128) * 4;  // gate/up units of one expert
+  const int gu_units = (p.I / 128) * kGuParts;  // gate/up units of one expert
   const int tiles = p.H / 128;           // down units of one expert
   unsigned int* h_ready = ctl + 4;
   unsigned int* landed = ctl + 4 + kFfnMaxPos;
@@ -1011,9 +1018,10 @@ __global__ void __launch_bounds__(kDecThreads, 2) k_decode_ffn(DecodeParams p) {
     }
     cta_signal(&ctl[2]);
   } else if (gu_a >= 0) {
-    // routed gate/up: expert at act position a, tile rt, quarter of its rows
+    // routed gate/up: expert at act position a, tile rt, part of its rows
     const int a = gu_a;
-    const int rt = gu_r >> 2, m0 = (gu_r & 3) * kDecWarps + wid;
+    const int rt = gu_r / kGuParts, part = gu_r % kGuParts;
+    const int m0 = (part & 3) * kDecWarps + wid, mo = (part >> 2) * kGuRows;
     ActExpert ax;
     if (act_expert(p, a, ax)) {
       // a miss gathered by this launch: wait until its record has landed
@@ -1029,12 +1037,12 @@ __global__ void __launch_bounds__(kDecThreads, 2) k_decode_ffn(DecodeParams p) {
         const int lane = threadIdx.x & 31;
         for (int q0 = ax.pb; q0 < ax.pb + ax.cnt; ++q0) {
           GuRegs first;  // the weights' first step, in flight while the token is staged
-          if (lane < p.H / 32) gu_fetch<FMT>(rec, L, p.H, rt, m0, lane, first);
+          if (lane < p.H / 32) gu_fetch<FMT>(rec, L, p.H, rt, m0, mo, lane, first);
           const uint16_t* row = p.x + (size_t)(p.perm[q0] / p.k) * p.H;
           __syncthreads();
           const bool bad = stage_bf16_to_f16(xs, &row, 1, p.H);
           if (__syncthreads_or(bad) && threadIdx.x == 0) set_status(p.status, MOE_ERR_UNSUPPORTED);
-          gu_routed_pass<1, FMT>(p, L, rec, rt, m0, q0, 1, xs, ax.g[0], ax.g[1], first);
+          gu_routed_pass<1, FMT>(p, L, rec, rt, m0, mo, q0, 1, xs, ax.g[0], ax.g[1], first);
         }
       }
     }
@@ -1142,7 +1150,7 @@ moe_status decode_ffn(const moe_ffn_args* a, cudaStream_t s, const DecodeFuse& f
     // one launch: gate/up, down and (one group) the combine
     p.ffn_ctl = fz.ffn_ctl;
     p.n_shared_units = (shared && !fz.shared_gu_done) ? a->Is / 4 : 0;
-    p.n_routed_units = max_act * (a->I / 128) * 4;
+    p.n_routed_units = max_act * (a->I / 128) * kGuParts;
     p.n_sdown_units = shared ? (a->H + kDecWarps * 4 - 1) / (kDecWarps * 4) : 0;
     p.n_rdown_units = max_act * (a->H / 128);
     if (fz.g_cache && a->group == 0) {
@@ -1181,7 +1189,7 @@ moe_status decode_ffn(const moe_ffn_args* a, cudaStream_t s, const DecodeFuse& f
     p.n_shared_units = (shared && !fz.shared_gu_done) ? a->Is / 4 : 0;
     p.n_sdown_units = (shared && fz.shared_gu_done && a->T == 1 && (a->stages & MOE_STAGE_DOWN))
                           ? (a->H + kDecWarps * 4 - 1) / (kDecWarps * 4) : 0;
-    const int routed = max_act * (a->I / 128) * 4;
+    const int routed = max_act * (a->I / 128) * kGuParts;
     p.n_routed_units = routed;
     size_t smem = smem_f16(p.maxm, a->H);
     if (p.n_shared_units && smem_f32(p.maxm, a->H) > smem) smem = smem_f32(p.maxm, a->H);
