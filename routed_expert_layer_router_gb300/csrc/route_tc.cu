@@ -53,23 +53,26 @@ constexpr int kKC = 64;                 // bf16 values per K chunk (128 bytes a 
 constexpr int kABytes = kM * 128;       // 16 KiB
 constexpr int kPieceBytes = kNE * 128;  // 4 KiB
 constexpr int kBBytes = 3 * kPieceBytes;
-constexpr int kStageBytes = kABytes + kBBytes;  // 28 KiB
-constexpr int kStages = 6;
-constexpr int kSmem = 1024 + kStages * kStageBytes;
+// TP token tiles of 128 per CTA share each stage's weight-piece tile: a
+// stage holds TP x tiles and the pieces
+template <int TP> struct TC {
+  static constexpr int kStageBytes = TP * kABytes + kBBytes;  // 28 or 44 KiB
+  static constexpr int kStages = TP == 1 ? 6 : 5;
+  static constexpr int kSmem = 1024 + kStages * kStageBytes;
+  static_assert(kSmem <= 227 * 1024, "shared memory");
+};
 constexpr int kThreads = 320;           // warp 0: TMA, warp 1: MMA, warps 2..9: epilogue
 constexpr int kEpiWarps = 8;
 constexpr uint32_t kAccStride = 128;    // tensor-memory columns per accumulator
-constexpr uint32_t kAccBufs = 2;        // accumulators in rotation
-constexpr uint32_t kTmemCols = kAccStride * kAccBufs;
+constexpr uint32_t kAccBufs = 2;        // accumulators (per token tile) in rotation
+constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitNs = 2000000000ull;  // no wait lasts longer than 2 s
-static_assert(kSmem <= 227 * 1024, "shared memory");
 static_assert(kN <= (int)kAccStride, "accumulator columns");
-static_assert(kTmemCols == 256 || kTmemCols == 512, "tensor-memory allocation");
 
 struct Params {
   int T, E, E_pad, H;
   int n_nt;      // expert tiles (E_pad / kNE)
-  int n_tiles;   // token tiles x expert tiles
+  int n_tiles;   // tiles (TP token tiles of 128 each) x expert tiles
   const float* bias;
   float* logits;
   int32_t* status;
@@ -105,9 +108,11 @@ __global__ void __launch_bounds__(256) k_router_split(const float* __restrict__ 
   pdl_launch_dependents();
 }
 
+template <int TP>
 __global__ void __launch_bounds__(kThreads, 1)
     k_logits_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                 Params p) {
+  constexpr int kStages = TC<TP>::kStages, kStageBytes = TC<TP>::kStageBytes;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -156,10 +161,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           unsigned char* st = smem + (size_t)s * kStageBytes;
           ptx::mbar_arrive_expect_tx(&full_bar[s], (uint32_t)kStageBytes);
-          ptx::tma_load_2d(st, &tmX, kc * kKC, mt * kM, &full_bar[s]);
+#pragma unroll
+          for (int tp = 0; tp < TP; ++tp)
+            ptx::tma_load_2d(st + tp * kABytes, &tmX, kc * kKC, (mt * TP + tp) * kM, &full_bar[s]);
 #pragma unroll
           for (int pc = 0; pc < 3; ++pc)
-            ptx::tma_load_2d(st + kABytes + pc * kPieceBytes, &tmW, kc * kKC,
+            ptx::tma_load_2d(st + TP * kABytes + pc * kPieceBytes, &tmW, kc * kKC,
                              pc * p.E_pad + nt * kNE, &full_bar[s]);
         }
       }
@@ -188,11 +195,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           ptx::tc_fence_after();
           const uint32_t a0 = ptx::smem_u32(smem + (size_t)s * kStageBytes);
-          const uint32_t b0 = a0 + kABytes;
+          const uint32_t b0 = a0 + TP * kABytes;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            ptx::mma_bf16(tmem + b * kAccStride, ptx::smem_desc(a0 + kk * 32, 16, 1024, 2),
-                          ptx::smem_desc(b0 + kk * 32, 16, 1024, 2), idesc, kk > 0);
+          for (int tp = 0; tp < TP; ++tp)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              ptx::mma_bf16(tmem + (b * TP + tp) * kAccStride,
+                            ptx::smem_desc(a0 + tp * kABytes + kk * 32, 16, 1024, 2),
+                            ptx::smem_desc(b0 + kk * 32, 16, 1024, 2), idesc, kk > 0);
           ptx::tc_commit(&empty_bar[s]);  // the stage is free once these MMAs finish
           ptx::tc_commit(&acc_full[b]);   // and the chunk's sums are ready
         }
@@ -206,9 +216,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int t = blockIdx.x; t < p.n_tiles && ok; t += gridDim.x) {
       const int mt = t / p.n_nt, nt = t % p.n_nt;
-      float sum[16], comp[16], lo[16];
+      float sum[TP][16], comp[TP][16], lo[TP][16];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) sum[j] = comp[j] = lo[j] = 0.f;
+      for (int tp = 0; tp < TP; ++tp)
+#pragma unroll
+        for (int j = 0; j < 16; ++j) sum[tp][j] = comp[tp][j] = lo[tp][j] = 0.f;
       for (int kc = 0; kc < nk; ++kc, ++d) {
         const uint32_t b = d % kAccBufs, u = d / kAccBufs;
         if (!ptx::mbar_wait(&acc_full[b], u & 1, kWaitNs)) {
@@ -218,35 +230,44 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         ptx::tc_fence_after();
-        const uint32_t base =
-            tmem + ((uint32_t)(q * 32) << 16) + b * kAccStride + (uint32_t)(half * 16);
-        uint32_t r1[16], r2[16], r3[16];
-        ptx::tmem_ld_32x32b_x16(base, r1);
-        ptx::tmem_ld_32x32b_x16(base + kNE, r2);
-        ptx::tmem_ld_32x32b_x16(base + 2 * kNE, r3);
-        ptx::tmem_ld_wait();
-        ptx::tc_fence_before();
-        if (lane == 0) ptx::mbar_arrive(&acc_empty[b]);  // the accumulator is free
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const float y = __fsub_rn(__uint_as_float(r1[j]), comp[j]);
-          const float s = __fadd_rn(sum[j], y);
-          comp[j] = __fsub_rn(__fsub_rn(s, sum[j]), y);
-          sum[j] = s;
-          lo[j] = __fadd_rn(lo[j], __fadd_rn(__uint_as_float(r2[j]), __uint_as_float(r3[j])));
+        for (int tp = 0; tp < TP; ++tp) {
+          const uint32_t base = tmem + ((uint32_t)(q * 32) << 16) + (b * TP + tp) * kAccStride +
+                                (uint32_t)(half * 16);
+          uint32_t r1[16], r2[16], r3[16];
+          ptx::tmem_ld_32x32b_x16(base, r1);
+          ptx::tmem_ld_32x32b_x16(base + kNE, r2);
+          ptx::tmem_ld_32x32b_x16(base + 2 * kNE, r3);
+          ptx::tmem_ld_wait();
+          if (tp == TP - 1) {
+            ptx::tc_fence_before();
+            if (lane == 0) ptx::mbar_arrive(&acc_empty[b]);  // the accumulators are free
+          }
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float y = __fsub_rn(__uint_as_float(r1[j]), comp[tp][j]);
+            const float s = __fadd_rn(sum[tp][j], y);
+            comp[tp][j] = __fsub_rn(__fsub_rn(s, sum[tp][j]), y);
+            sum[tp][j] = s;
+            lo[tp][j] =
+                __fadd_rn(lo[tp][j], __fadd_rn(__uint_as_float(r2[j]), __uint_as_float(r3[j])));
+          }
         }
       }
       if (!ok) break;
-      const int tok = mt * kM + q * 32 + lane;
       const int e0 = nt * kNE + half * 16;
-      if (tok < p.T) {
-        float* out = p.logits + (size_t)tok * p.E;
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int e = e0 + j;
-          if (e < p.E) {
-            const float v = __fadd_rn(sum[j], __fsub_rn(lo[j], comp[j]));
-            out[e] = p.bias ? __fadd_rn(v, p.bias[e]) : v;
+      for (int tp = 0; tp < TP; ++tp) {
+        const int tok = (mt * TP + tp) * kM + q * 32 + lane;
+        if (tok < p.T) {
+          float* out = p.logits + (size_t)tok * p.E;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int e = e0 + j;
+            if (e < p.E) {
+              const float v = __fadd_rn(sum[tp][j], __fsub_rn(lo[tp][j], comp[tp][j]));
+              out[e] = p.bias ? __fadd_rn(v, p.bias[e]) : v;
+            }
           }
         }
       }
@@ -294,8 +315,10 @@ moe_status route_logits_tc(const moe_route_args* a, float* logits, cudaStream_t 
     return st;
   static bool attr = false;
   if (!attr) {
-    if (cudaFuncSetAttribute(k_logits_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) !=
-        cudaSuccess)
+    if (cudaFuncSetAttribute(k_logits_tc<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             TC<1>::kSmem) != cudaSuccess ||
+        cudaFuncSetAttribute(k_logits_tc<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             TC<2>::kSmem) != cudaSuccess)
       return MOE_ERR_CUDA;
     attr = true;
   }
@@ -305,12 +328,18 @@ moe_status route_logits_tc(const moe_route_args* a, float* logits, cudaStream_t 
   p.E_pad = E_pad;
   p.H = a->H;
   p.n_nt = E_pad / kNE;
-  p.n_tiles = (a->T + kM - 1) / kM * p.n_nt;
+  // two token tiles per CTA (each weight-piece tile loaded once for both)
+  // once the 128-token tiles would need more than one wave
+  const int tiles1 = (a->T + kM - 1) / kM * p.n_nt;
+  const bool two = tiles1 > kSMs;
+  p.n_tiles = two ? (a->T + 2 * kM - 1) / (2 * kM) * p.n_nt : tiles1;
   p.bias = a->bias;
   p.logits = logits;
   p.status = a->status;
   const int grid = p.n_tiles < kSMs ? p.n_tiles : kSMs;
-  if (launch_pdl(k_logits_tc, grid, kThreads, (size_t)kSmem, s, tx, tw, p) != cudaSuccess)
+  if ((two ? launch_pdl(k_logits_tc<2>, grid, kThreads, (size_t)TC<2>::kSmem, s, tx, tw, p)
+           : launch_pdl(k_logits_tc<1>, grid, kThreads, (size_t)TC<1>::kSmem, s, tx, tw, p)) !=
+      cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
 }
