@@ -46,6 +46,11 @@ def test_binding_covers_the_header(libmoe):
     assert L.moe_record_bytes(6144, 2048, 1) == 20054016
     assert L.moe_record_bytes(6144, 2048, 7) == 0
     assert L.moe_status_string(6) == b"MOE_ERR_DEVICE"
+    # the router weights' three bf16 pieces, expert rows padded to multiples of 32
+    assert L.moe_route_split_bytes(288, 6144) == 3 * 288 * 6144 * 2
+    assert L.moe_route_split_bytes(100, 512) == 3 * 128 * 512 * 2
+    assert L.moe_route_split_bytes(16, 256) == 3 * 32 * 256 * 2
+    assert L.moe_route_split_bytes(0, 256) == 0 and L.moe_route_split_bytes(16, 0) == 0
 
 
 def test_argument_errors_return_before_touching_the_device(libmoe):
