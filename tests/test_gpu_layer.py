@@ -229,3 +229,26 @@ def test_decode_flags_activation_beyond_f16():
         assert layer.read_status() == 0
     finally:
         dw.close()
+
+
+def test_decode_output_in_pinned_host_memory():
+    """moe_layer_forward writing y straight into pinned host memory (the
+    decode path's last kernel stores it there): bit for bit the output written
+    into device memory."""
+    import gen.device as gd
+    wl = gen.WORKLOADS["decode"]
+    dw = gd.build(wl, T_max=1)
+    try:
+        layer = dw.moe_layers[0]
+        x = torch.empty((3, wl.H), dtype=torch.bfloat16, device="cuda")
+        gen.dev_x_bf16(wl.seed, 0, 9000, 3, wl.H, x.data_ptr(), torch.cuda.current_stream().cuda_stream)
+        yd = torch.empty((3, wl.H), dtype=torch.bfloat16, device="cuda")
+        yh = torch.empty((3, wl.H), dtype=torch.bfloat16, pin_memory=True)
+        for t in range(3):
+            layer.forward(x[t:t + 1], yd[t:t + 1])
+            layer.forward(x[t:t + 1], yh[t:t + 1])
+        torch.cuda.synchronize()
+        assert layer.read_status() == 0
+        assert torch.equal(yd.cpu().view(torch.int16), yh.view(torch.int16))
+    finally:
+        dw.close()
