@@ -475,12 +475,14 @@ typedef struct {
 
 moe_status moe_layer_create(const moe_layer_desc* d, moe_layer** out);
 moe_status moe_layer_destroy(moe_layer* l);
-/* x: device [T][H] bf16.  y: [T][H] bf16, device memory or pinned host memory
- * (cudaHostAlloc / cudaHostRegister; the kernels address it directly under
- * unified addressing): the forward's last kernel writes it with plain
- * stores, so a host y is the device->host transfer of the result, without a
- * copy after the forward.  x is read by many CTAs (and by TMA on the
- * many-token paths), so it belongs in device memory. */
+/* x: [T][H] bf16, device memory or pinned host memory (cudaHostAlloc /
+ * cudaHostRegister); a host x is copied into the layer's own buffer by the
+ * forward's first kernel (16-byte loads; the copy engine when x is not
+ * 16-byte aligned), since the later kernels read it many times.  y: [T][H]
+ * bf16, device memory or pinned host memory, which the kernels address
+ * directly under unified addressing: the forward's last kernel writes it with
+ * plain stores, so a host y is the device->host transfer of the result.
+ * Pageable (unregistered) host memory is MOE_ERR_INVALID_ARG. */
 moe_status moe_layer_forward(moe_layer* l, const void* x, int T, void* y, void* stream);
 /* Device pointers (inside the layer's workspace) to the last forward's router
  * outputs: ids [T][k] int32, w [T][k] fp32, p_sel [T][k] fp32; and the

@@ -144,6 +144,7 @@ struct moe_layer {
   float* w_eff;       // renorm-skip: the kept routes' renormalised weights
   void* w_split;      // the router weights' bf16 pieces (tensor-core router), or null
   size_t w_split_bytes;
+  uint16_t* x_dev;    // the tokens, when the caller passes them in pinned host memory
   void* ffn_ws;
   size_t ffn_ws_bytes;
   int last_T;
@@ -206,7 +207,8 @@ MOE_API moe_status moe_layer_create(const moe_layer_desc* d, moe_layer** out) {
       (size_t)E * 4,      /* miss_dst */
       (size_t)T * k * 4,  /* ids_eff */
       (size_t)T * k * 4,  /* w_eff */
-      T > kRouteTcMinT ? route_split_bytes(E, H) : 0 /* router weight pieces */};
+      T > kRouteTcMinT ? route_split_bytes(E, H) : 0, /* router weight pieces */
+      (size_t)T * H * 2   /* x copied in from pinned host memory */};
   const int n = (int)(sizeof(sizes) / sizeof(sizes[0]));
   size_t total = 0;
   for (int i = 0; i < n; ++i) total += align256(sizes[i]);
@@ -217,7 +219,7 @@ MOE_API moe_status moe_layer_create(const moe_layer_desc* d, moe_layer** out) {
   }
   l->ws_bytes = total;
   uint8_t* p = (uint8_t*)l->ws;
-  void* ptrs[25];
+  void* ptrs[26];
   for (int i = 0; i < n; ++i) {
     ptrs[i] = sizes[i] ? p : nullptr;
     p += align256(sizes[i]);
@@ -248,6 +250,7 @@ MOE_API moe_status moe_layer_create(const moe_layer_desc* d, moe_layer** out) {
   l->w_eff = (float*)ptrs[23];
   l->w_split = ptrs[24];
   l->w_split_bytes = sizes[24];
+  l->x_dev = (uint16_t*)ptrs[25];
   bool ok = cudaMemset(l->ws, 0, total) == cudaSuccess &&
             cudaStreamCreateWithFlags(&l->side, cudaStreamNonBlocking) == cudaSuccess &&
             cudaEventCreateWithFlags(&l->ev_lookup, cudaEventDisableTiming) == cudaSuccess;
@@ -332,6 +335,27 @@ static moe_status prefill_streamed(moe_layer* l, moe_ffn_args* fa, cudaStream_t 
   return MOE_OK;
 }
 
+// `bytes` of tokens from pinned host memory into device memory: one kernel of
+// 16-byte loads (the copy engine's setup costs more than this for a token or
+// a few), or the copy engine when an address is not 16-byte aligned
+__global__ void __launch_bounds__(256) k_copy_rows(const uint4* __restrict__ src,
+                                                   uint4* __restrict__ dst, size_t n) {
+  pdl_wait();  // the previous forward's kernels may still read dst
+  for (size_t i = blockIdx.x * (size_t)256 + threadIdx.x; i < n; i += (size_t)gridDim.x * 256)
+    dst[i] = src[i];
+  pdl_launch_dependents();
+}
+static moe_status copy_rows_in(const void* src, void* dst, size_t bytes, cudaStream_t s) {
+  if (((uintptr_t)src & 15) || ((uintptr_t)dst & 15) || (bytes & 15))
+    return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, s) == cudaSuccess
+               ? MOE_OK : MOE_ERR_CUDA;
+  const size_t n = bytes / 16;
+  const size_t blocks = (n + 255) / 256;
+  const int grid = (int)(blocks < (size_t)kSMs * 4 ? blocks : (size_t)kSMs * 4);
+  return launch_pdl(k_copy_rows, grid, 256, 0, s, (const uint4*)src, (uint4*)dst, n) ==
+                 cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
 // y = bf16(y_acc): the prefill path's combine (its down GEMMs added into y_acc),
 // unless the shared expert's down GEMM already wrote y (y_written)
 static moe_status finish_prefill(moe_layer* l, int T, void* y, void* stream,
@@ -350,8 +374,9 @@ static moe_status finish_prefill(moe_layer* l, int T, void* y, void* stream,
   return MOE_OK;
 }
 
-MOE_API moe_status moe_layer_forward(moe_layer* l, const void* x, int T, void* y, void* stream) {
-  if (!l || !x || !y || T < 0 || T > l->d.T_max) return MOE_ERR_INVALID_ARG;
+MOE_API moe_status moe_layer_forward(moe_layer* l, const void* x_in, int T, void* y,
+                                     void* stream) {
+  if (!l || !x_in || !y || T < 0 || T > l->d.T_max) return MOE_ERR_INVALID_ARG;
   if (T == 0) return MOE_OK;
   const moe_layer_desc& d = l->d;
   cudaStream_t s = (cudaStream_t)stream;
@@ -360,6 +385,19 @@ MOE_API moe_status moe_layer_forward(moe_layer* l, const void* x, int T, void* y
   l->ev_i = 0;
   l->ev_stream = s;
   layer_mark(l);
+  // tokens in pinned host memory: copied once into the layer's buffer by the
+  // forward's first kernel (the later kernels read them many times)
+  const void* x = x_in;
+  cudaPointerAttributes pat;
+  if (cudaPointerGetAttributes(&pat, x_in) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (pat.type == cudaMemoryTypeUnregistered) return MOE_ERR_INVALID_ARG;
+  if (pat.type == cudaMemoryTypeHost) {
+    if ((st = copy_rows_in(x_in, l->x_dev, (size_t)T * d.H * 2, s)) != MOE_OK) return st;
+    x = l->x_dev;
+  }
 
   moe_route_args ra;
   memset(&ra, 0, sizeof(ra));

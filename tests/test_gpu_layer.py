@@ -231,10 +231,10 @@ def test_decode_flags_activation_beyond_f16():
         dw.close()
 
 
-def test_decode_output_in_pinned_host_memory():
-    """moe_layer_forward writing y straight into pinned host memory (the
-    decode path's last kernel stores it there): bit for bit the output written
-    into device memory."""
+def test_decode_tokens_and_output_in_pinned_host_memory():
+    """moe_layer_forward with y in pinned host memory (the decode path's last
+    kernel stores it there), and with x in pinned host memory too (the layer
+    copies it in with its first kernel): bit for bit the device-memory call."""
     import gen.device as gd
     wl = gen.WORKLOADS["decode"]
     dw = gd.build(wl, T_max=1)
@@ -244,11 +244,15 @@ def test_decode_output_in_pinned_host_memory():
         gen.dev_x_bf16(wl.seed, 0, 9000, 3, wl.H, x.data_ptr(), torch.cuda.current_stream().cuda_stream)
         yd = torch.empty((3, wl.H), dtype=torch.bfloat16, device="cuda")
         yh = torch.empty((3, wl.H), dtype=torch.bfloat16, pin_memory=True)
+        xh = x.cpu().pin_memory()
+        yhh = torch.empty((3, wl.H), dtype=torch.bfloat16, pin_memory=True)
         for t in range(3):
             layer.forward(x[t:t + 1], yd[t:t + 1])
             layer.forward(x[t:t + 1], yh[t:t + 1])
+            layer.forward(xh[t:t + 1], yhh[t:t + 1])
         torch.cuda.synchronize()
         assert layer.read_status() == 0
         assert torch.equal(yd.cpu().view(torch.int16), yh.view(torch.int16))
+        assert torch.equal(yd.cpu().view(torch.int16), yhh.view(torch.int16))
     finally:
         dw.close()
