@@ -224,3 +224,28 @@ def test_prefill_public_calls_match_the_layer():
         assert d.max() <= 2.0 ** -7 * np.abs(y_to_f64(y_layer)).max()
     finally:
         dw.close()
+
+
+def test_prefill_tokens_and_output_in_pinned_host_memory():
+    """The prefill layer called on pinned host buffers (the layer copies x in
+    with its first kernel; the shared expert's down GEMM stores y into host
+    memory) against the same call on device buffers.  The down GEMMs' L2
+    reductions add in any order, so the two may differ by a bf16 rounding."""
+    import gen.device as gd
+    dw = gd.build(SMALL, T_max=SMALL.T)
+    try:
+        layer = dw.moe_layers[0]
+        x = draw_prefill_tokens(dw, 0, SMALL.T)
+        xd = to_dev_bf16(x)
+        yd = layer.forward(xd)
+        xh = xd.cpu().pin_memory()
+        yh = torch.empty_like(xh).pin_memory()
+        layer.forward(xh, yh)
+        torch.cuda.synchronize()
+        assert layer.read_status() == 0
+        a, b = y_to_f64(yd), y_to_f64(yh)
+        assert np.abs(a - b).max() <= 2.0 ** -7 * np.abs(a).max()
+        y_ref, _, _, _, bound = oracle_layer(dw, 0, x, mode=1, return_bound=True)
+        check_outputs(b, y_ref, bound=bound)
+    finally:
+        dw.close()
