@@ -102,12 +102,14 @@ def test_route_parity(name, T, one_kernel):
 
 
 ODD = gen.Workload("tc-odd", H=512, I=128, E=100, k=6, T=1300, layers=1, Is=0, seed=11)
+WIDE = gen.Workload("tc-wide", H=512, I=128, E=1000, k=8, T=1100, layers=1, Is=0, seed=12)
 
 
 @pytest.mark.parametrize("wl,T,with_bias", [(gen.WORKLOADS["tiny"], 1100, False),
                                             (ODD, 1300, True),
                                             (gen.WORKLOADS["decode"], 1100, False),
-                                            (gen.WORKLOADS["decode"], 2200, True)])
+                                            (gen.WORKLOADS["decode"], 2200, True),
+                                            (WIDE, 1100, True)])
 def test_route_tensor_core_parity(wl, T, with_bias):
     """More than 1024 tokens with the weight-piece scratch: the logits run on
     the tensor cores from the three bf16 pieces of the fp32 router weights.
@@ -116,7 +118,8 @@ def test_route_tensor_core_parity(wl, T, with_bias):
     shapes cover a padded expert tile (16 and 100 experts) and a ragged last
     token tile (1100 and 1300 tokens), and two token tiles per CTA (2200
     tokens: more 128-token tiles than SMs), the second tile of the last pair
-    holding 24 tokens."""
+    holding 24 tokens; and 1000 experts (32 expert tiles, the last padded),
+    paired at 1100 tokens."""
     from routed_expert_layer_router_gb300 import moe
     Wr = gen.router_f32(wl.seed, 0, wl.E, wl.H)
     bias = gen.zipf_bias(wl.seed, 0, wl.E, 1.556)[0] if with_bias else None
