@@ -276,6 +276,26 @@ class ExplicitLayer:
 
 
 # --------------------------------------------------------------- decode
+def max_over_ranks(torch, value, world, device):
+    """The largest of `value` over the job's ranks: the job's timed region ends
+    when its slowest rank does."""
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world, steps, tokens_per_step, total_ms):
+    """Whole-job throughput: every rank processed `steps` steps of
+    `tokens_per_step` tokens within `total_ms` (the max over ranks)."""
+    return world * steps * tokens_per_step / (total_ms * 1e-3)
+
+
+def rank_draw0(rank, n_steps, base=1_000_000):
+    """First token draw of a rank: the ranks draw disjoint token ranges."""
+    return base + rank * n_steps
+
+
 def bench_decode(args, torch, moe, gen, gd, dev, rank, world, local_rank, peaks, wl=None):
     wl = wl or gen.WORKLOADS["decode"]
     H, I, E, k, Is = wl.H, wl.I, wl.E, wl.k, wl.Is
@@ -289,7 +309,7 @@ def bench_decode(args, torch, moe, gen, gd, dev, rank, world, local_rank, peaks,
     sp = stream.cuda_stream
     n_steps = args.warmup + args.steps
     xs = torch.empty((n_steps, H), dtype=torch.bfloat16, device=dev)
-    gen.dev_x_bf16(wl.seed, 0, 1_000_000 + rank * n_steps, n_steps, H, xs.data_ptr(), sp)
+    gen.dev_x_bf16(wl.seed, 0, rank_draw0(rank, n_steps), n_steps, H, xs.data_ptr(), sp)
     ys = torch.empty((n_steps, H), dtype=torch.bfloat16, device=dev)
     flush = L2Flush(torch, args.flush_mb, dev)
     ex = ExplicitLayer(torch, moe, dw, 0, T)
@@ -375,10 +395,7 @@ def bench_decode(args, torch, moe, gen, gd, dev, rank, world, local_rank, peaks,
         e2e_ms.append(a.elapsed_time(bb))
     assert layer.read_status() == 0
 
-    tot = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(tot, op=torch.distributed.ReduceOp.MAX)
-    total_ms = float(tot.item())
+    total_ms = max_over_ranks(torch, total_ms, world, dev)
     rb = gen.record_bytes(H, I, wl.fmt)
     # algorithmic bytes of the three kernels of the one-token sequence: the
     # router kernel (router weights, the shared expert's gate/up, x, h_shared,
@@ -398,7 +415,7 @@ def bench_decode(args, torch, moe, gen, gd, dev, rank, world, local_rank, peaks,
     dn_gbs = dn_bytes / (dn_ms * 1e-3) / 1e9
     hbm = peaks["hbm_gbs"]
     res = {
-        "value": round(world * args.steps * T / (total_ms * 1e-3), 2),
+        "value": round(job_tokens_per_s(world, args.steps, T, total_ms), 2),
         "ms_per_step": round(total_ms / args.steps, 5),
         "roofline": {"bound": "hbm",
                      "kernel": "k_decode_gu as the layer launches it for one token (routed "
