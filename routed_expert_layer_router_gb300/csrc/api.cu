@@ -519,6 +519,9 @@ MOE_API moe_status moe_layer_forward(moe_layer* l, const void* x_in, int T, void
       fz.comb_ctl = (unsigned int*)((char*)l->route_ctl + kRouteCtlBytes);
       fz.inv = l->inv;
       fz.y = (uint16_t*)y;
+      // the one-launch FFN's per-position counts, unused by the two launches
+      if (!ffn_gathers)
+        fz.h_counts = (unsigned int*)((char*)l->route_ctl + kRouteCtlBytes + kTileCtlBytes) + 4;
     }
     // prefill: the token quantisation clears y_acc; with one FFN call its
     // shared-expert down GEMM is the last writer of y_acc and writes y

@@ -165,6 +165,10 @@ struct DecodeFuse {
   // expert's down GEMM (the call's last writer of y_acc), or nullptr
   bool pf_zero_y;
   uint16_t* pf_y;
+  // two-launch decode FFN: 2 x 1024 counts (zero before a launch, left zero)
+  // with which the down kernel's routed units start as soon as their expert's
+  // h is written; nullptr: the down kernel waits for the gate/up kernel
+  unsigned int* h_counts;
 };
 
 // the gather fields of one layer's records (cache.cu)

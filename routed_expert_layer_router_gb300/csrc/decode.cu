@@ -76,6 +76,14 @@ struct DecodeParams {
   const int4* act_meta;  // per act_list position: {expert, slot, route, routes}, gscale row
   const int32_t* inv;
   uint16_t* y;
+  // two launches, the down kernel's routed units started early: per act
+  // position the gate/up units' count (h_ready, gu_units per expert) and the
+  // count of down units that waited on it (h_seen, H/128 per expert; the last
+  // one zeroes both).  nullptr: the down kernel waits for the whole gate/up
+  // kernel.
+  unsigned int* h_ready;
+  unsigned int* h_seen;
+  int gu_units;
   // K-decode-ffn (one launch): routed down units after the gate/up and
   // shared-down units, and its control words (ticket, done, shared h ready,
   // then one h-ready count per act position), zero before and after a launch
@@ -514,6 +522,46 @@ __device__ void down_shared_pass(const DecodeParams& p, int r0, int t0, int mm, 
     }
 }
 
+// ---- bounded waits on counts that other CTAs raise ------------------------------
+// Every wait is bounded (MOE_ERR_TIMEOUT in the status word).
+constexpr uint64_t kFfnWaitNs = 2000000000ull;
+
+__device__ __forceinline__ uint64_t gtimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ unsigned int ld_acquire(const unsigned int* p) {
+  unsigned int v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+// thread 0 waits for *c >= target, bounded; the CTA then reads what the
+// counted units wrote (through L2)
+__device__ __forceinline__ void cta_wait_count(const unsigned int* c, unsigned int target,
+                                               int32_t* status) {
+  if (threadIdx.x == 0) {
+    const uint64_t t0 = gtimer_ns();
+    while (ld_acquire(c) < target) {
+      if (gtimer_ns() - t0 > kFfnWaitNs) {
+        set_status(status, MOE_ERR_TIMEOUT);
+        break;
+      }
+      __nanosleep(100);
+    }
+    __threadfence();
+  }
+  __syncthreads();
+}
+// the CTA's writes are visible before the count (called by every thread:
+// each fences its own writes, then one thread counts)
+__device__ __forceinline__ void cta_signal(unsigned int* c) {
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) atomicAdd(c, 1u);
+}
+
+
 // ---- K-decode-gu -------------------------------------------------------------
 template <int M, int FMT>
 __device__ void gu_routed_pass(const DecodeParams& p, const RecordLayout& L, const uint8_t* rec,
@@ -645,6 +693,7 @@ __global__ void __launch_bounds__(kDecThreads, MAXM == 1 ? kGuMinBlocks : 1) k_d
     else
       gu_routed_pass<1, FMT>(p, L, rec, rt, m0, mo, q0, mm, xs, gg, gu, first);
   }
+  if (p.h_ready) cta_signal(&p.h_ready[a]);  // this unit's h rows are written
 }
 
 // ---- K-decode-down -----------------------------------------------------------
@@ -749,6 +798,14 @@ __device__ __forceinline__ void down_unit(const DecodeParams& p, unsigned char* 
   if (!act_expert(p, a, ax)) return;
   const int slot = ax.slot;
   if (slot < 0 || slot >= p.n_slots) return;  // reported by K-decode-gu
+  if (p.h_ready) {
+    // started before the gate/up kernel completed: wait for this expert's h
+    cta_wait_count(&p.h_ready[a], (unsigned int)p.gu_units, p.status);
+    if (threadIdx.x == 0 && atomicAdd(&p.h_seen[a], 1u) == (unsigned int)tiles - 1) {
+      p.h_ready[a] = 0u;  // every unit of this expert is past its wait
+      p.h_seen[a] = 0u;
+    }
+  }
   const uint8_t* rec = p.arena + (uint64_t)slot * p.rec_bytes;
   const RecordLayout L(p.H, p.I, FMT);
   const float gd = ax.g[2];
@@ -767,13 +824,27 @@ __device__ __forceinline__ void down_unit(const DecodeParams& p, unsigned char* 
 
 // one token: three CTAs per SM (at most 85 registers), so that the routed
 // units (8 experts x 48 tiles) run in one wave
+//
+// With p.h_ready set, the routed units do not wait for the gate/up kernel as a
+// whole: each waits for its own expert's h, and the grid waits for the kernel
+// before it only ahead of the combine (which reads the shared expert's output
+// from that kernel).  The routing they read first is complete: this kernel
+// launches only when every CTA of the gate/up kernel has passed its own wait
+// for the kernel before that (the host sets h_ready only when the gate/up
+// kernel has no unit that skips that wait and this kernel has no shared units).
 template <int MAXM, int FMT>
 __global__ void __launch_bounds__(kDecThreads, MAXM == 1 ? 3 : 2) k_decode_down(DecodeParams p) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   __shared__ int s_last;
-  pdl_wait();
-  pdl_launch_dependents();
+  if (!p.h_ready) {
+    pdl_wait();
+    pdl_launch_dependents();
+  }
   down_unit<MAXM, FMT>(p, smem_raw);
+  if (p.h_ready) {
+    pdl_wait();
+    pdl_launch_dependents();
+  }
   if (!p.comb_ctl) return;
   // shared units cover 32 rows each (4 per tile); routed units one tile
   const int u = blockIdx.x;
@@ -831,45 +902,7 @@ __global__ void k_combine(int T, int H, int k, const float* __restrict__ y_acc,
 // stream their weights while the gate/up units of the last ones still run,
 // and the grid has one tail instead of two.  The combine is done by the last
 // CTA of each 128-row tile, as in K-decode-down.  The last CTA to finish
-// resets the control words for the next launch.  Every wait is bounded
-// (MOE_ERR_TIMEOUT in the status word).
-constexpr uint64_t kFfnWaitNs = 2000000000ull;
-
-__device__ __forceinline__ uint64_t gtimer_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-__device__ __forceinline__ unsigned int ld_acquire(const unsigned int* p) {
-  unsigned int v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-// thread 0 waits for *c >= target, bounded; the CTA then reads what the
-// counted units wrote (through L2)
-__device__ __forceinline__ void cta_wait_count(const unsigned int* c, unsigned int target,
-                                               int32_t* status) {
-  if (threadIdx.x == 0) {
-    const uint64_t t0 = gtimer_ns();
-    while (ld_acquire(c) < target) {
-      if (gtimer_ns() - t0 > kFfnWaitNs) {
-        set_status(status, MOE_ERR_TIMEOUT);
-        break;
-      }
-      __nanosleep(100);
-    }
-    __threadfence();
-  }
-  __syncthreads();
-}
-// the CTA's writes are visible before the count (called by every thread:
-// each fences its own writes, then one thread counts)
-__device__ __forceinline__ void cta_signal(unsigned int* c) {
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) atomicAdd(c, 1u);
-}
-
+// resets the control words for the next launch.
 // one routed down unit (expert at act position a, 128-row tile rt), after
 // its h is complete
 template <int FMT>
@@ -1105,6 +1138,8 @@ moe_status decode_ffn(const moe_ffn_args* a, cudaStream_t s, const DecodeFuse& f
   DecodeParams p;
   p.n_rdown_units = 0;
   p.ffn_ctl = nullptr;
+  p.h_ready = p.h_seen = nullptr;
+  p.gu_units = (a->I / 128) * kGuParts;
   p.n_gather_workers = 0;
   p.g_host = nullptr;
   p.g_host_index = nullptr;
@@ -1184,6 +1219,15 @@ moe_status decode_ffn(const moe_ffn_args* a, cudaStream_t s, const DecodeFuse& f
       if (fz.mark) fz.mark(fz.mark_ctx);
     }
     return MOE_OK;
+  }
+  // down units started per expert: both steps in this call, no shared-expert
+  // gate/up units in the gate/up kernel (they may skip its wait), and the
+  // shared down (if any) in the gate/up kernel, not in the down kernel
+  if (fz.h_counts && (a->stages & MOE_STAGE_GATE_UP) && (a->stages & MOE_STAGE_DOWN) &&
+      max_act <= kFfnMaxPos &&
+      (!shared || (fz.shared_gu_done && a->T == 1))) {
+    p.h_ready = fz.h_counts;
+    p.h_seen = fz.h_counts + kFfnMaxPos;
   }
   if (a->stages & MOE_STAGE_GATE_UP) {
     p.n_shared_units = (shared && !fz.shared_gu_done) ? a->Is / 4 : 0;
