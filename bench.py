@@ -56,7 +56,7 @@ FP4_OVER_BF16 = 6.0  # nominal dense FP4 / dense bf16 tensor throughput (13.5 / 
 # DRAM bytes (read + write) of one launch of the roofline kernel on the full decode
 # layer, from one ncu capture of the current kernel; None whenever the kernel has
 # changed since it was captured
-GU_TRAFFIC = 138_482_816 + 357_888
+GU_TRAFFIC = 138_482_944 + 365_056
 GU_TRAFFIC_SOURCE = "ncu dram__bytes_read.sum + dram__bytes_write.sum, one launch, full decode layer"
 
 
