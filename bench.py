@@ -297,6 +297,8 @@ def rank_draw0(rank, n_steps, base=1_000_000):
 
 
 def bench_decode(args, torch, moe, gen, gd, dev, rank, world, local_rank, peaks, wl=None):
+    # the captured DRAM traffic is that of the NVFP4 decode layer's gate/up kernel
+    traffic_captured = wl is None and not args.small
     wl = wl or gen.WORKLOADS["decode"]
     H, I, E, k, Is = wl.H, wl.I, wl.E, wl.k, wl.Is
     T = 1
@@ -422,8 +424,9 @@ def bench_decode(args, torch, moe, gen, gd, dev, rank, world, local_rank, peaks,
                                "gate/up of the 8 experts, SiLU*mul, + the bf16 shared "
                                "expert's down)",
                      "achieved": round(gu_gbs, 1), "peak": hbm, "unit": "GB/s",
-                     "frac": round(gu_gbs / hbm, 4), "traffic": GU_TRAFFIC,
-                     "traffic_source": GU_TRAFFIC_SOURCE,
+                     "frac": round(gu_gbs / hbm, 4),
+                     "traffic": GU_TRAFFIC if traffic_captured else None,
+                     "traffic_source": GU_TRAFFIC_SOURCE if traffic_captured else "not captured",
                      "bytes_per_launch": gu_bytes, "avg_launch_ms": round(gu_ms, 5)},
         "kernels": {
             "k_route_permute_small": {"ms": round(rt_ms, 5), "GB/s": round(rt_gbs, 1),
