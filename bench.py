@@ -49,7 +49,9 @@ METRIC = "MoE-layer tokens/s (decode, 4096-tok prefill); % of HBM / FP4-TC / PCI
 UNIT = "tokens/s"
 # the adaptive cache keeps three spare slots per layer ("Project Maya" page)
 ADAPTIVE_SPARES = 3
-ADAPTIVE_WARM_TOKENS = 256
+# the stack passes warm up on this many distinct tokens (their misses touch
+# most experts' host records once before the timed steps)
+STACK_WARM_TOKENS = 256
 # renorm-skip threshold of the stack_skip pass (an approximation of the layer)
 SKIP_TAU = 0.05  # about one halving period of its counts on the 16-layer stack
 FP4_OVER_BF16 = 6.0  # nominal dense FP4 / dense bf16 tensor throughput (13.5 / 2.25)
@@ -846,10 +848,13 @@ def bench_multilayer(args, torch, moe, gen, gd, dev, name, link_gbs, spares=0, s
     stream = torch.cuda.current_stream()
     sp = stream.cuda_stream
     steps = args.stack_steps
-    # The adaptive cache learns from the routes it sees: it is warmed with a
-    # stream of distinct tokens (not a few tokens repeated), and its gather
-    # pass runs on fresh tokens too, so that its hit rate is that of new input.
-    n_warm = args.warmup if spares == 0 else max(args.warmup, ADAPTIVE_WARM_TOKENS)
+    # Warm-up on a stream of distinct tokens, not a few tokens repeated: the
+    # first device read of a host record is several times slower than later
+    # ones, and a few repeated tokens leave most experts' records unread until
+    # the timed steps.  The adaptive cache also learns from the routes it sees;
+    # its gather pass runs on fresh tokens too, so that its hit rate is that of
+    # new input.
+    n_warm = max(args.warmup, -(-STACK_WARM_TOKENS // T))  # steps of T tokens
     g0 = n_warm + (steps if spares > 0 else 0)  # first token of the gather pass
     n = g0 + steps
     xs = torch.empty((n, L, T, wl.H), dtype=torch.bfloat16, device=dev)
