@@ -434,7 +434,12 @@ moe_status moe_combine(const moe_combine_args* a, void* stream);
  * the decode path can be captured in a CUDA graph.
  * Misses: decode gathers them into the staging slots group by group, or,
  * when every miss fits in them, inside the FFN kernel itself (copy units run
- * beside the hits' units; a miss's units wait for its record, bounded).  A
+ * beside the hits' units; a miss's units wait for its record, bounded).  With
+ * every active expert resident and one group, the decode down kernel's units
+ * of an expert start as soon as that expert's gate/up units have written h
+ * (counts in the layer's workspace, a bounded wait each).  A wait that runs
+ * out sets MOE_ERR_TIMEOUT in the status word; the layer's counts are then
+ * undefined and the layer should be destroyed.  A
  * prefill with at least 2 staging slots gathers its misses on a second
  * stream of the layer, in groups of n_stage/2 into alternating halves of the
  * staging slots, while the first stream runs the GEMMs of the hits and of
