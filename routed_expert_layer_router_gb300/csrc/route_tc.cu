@@ -7,8 +7,9 @@
 // weight is the exact sum of three bf16 values,
 //   W1 = bf16(W), W2 = bf16(W - W1), W3 = W - W1 - W2
 // (W - W1 keeps at most 16 significant bits and W - W1 - W2 at most 8, each
-// exact in fp32; bf16 has fp32's exponent range).  So x.W = x.W1 + x.W2 + x.W3
-// with every product exact, and only the sums round.
+// exact in fp32; bf16 has fp32's exponent range, so the split is exact for
+// |W| >= 2^-110, below which the third piece can lose low bits).  So x.W =
+// x.W1 + x.W2 + x.W3 with every product exact, and only the sums round.
 //
 //   k_router_split  W [E][H] fp32 -> pieces [3][E_pad][H] bf16 (rows E..E_pad-1
 //                   zero), rewritten by every call (the weights may change
