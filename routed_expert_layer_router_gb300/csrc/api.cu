@@ -123,7 +123,8 @@ static moe_status expert_ffn(const moe_ffn_args* a, void* stream, const DecodeFu
 
 MOE_API moe_status moe_expert_ffn(const moe_ffn_args* a, void* stream) {
   const DecodeFuse none = {nullptr, nullptr, nullptr, false, false, nullptr, nullptr,
-                           nullptr, nullptr, nullptr, 0,       nullptr, nullptr, nullptr};
+                           nullptr, nullptr, nullptr, 0,       nullptr, nullptr, nullptr,
+                           false,   nullptr, nullptr};
   return expert_ffn(a, stream, none);
 }
 
@@ -304,7 +305,7 @@ static moe_status prefill_streamed(moe_layer* l, moe_ffn_args* fa, cudaStream_t 
   // with the hits, before the misses' GEMMs, so a separate combine writes y
   const DecodeFuse marks = {layer_mark_cb, l, nullptr, false, false, nullptr, nullptr,
                             nullptr, nullptr, nullptr, 0,       nullptr, nullptr, nullptr,
-                            true,          nullptr};
+                            true,          nullptr, nullptr};
   moe_status st;
   auto gather = [&](int g) -> moe_status {
     const int h = g & 1, cnt = S2 < max_miss - g * S2 ? S2 : max_miss - g * S2;
@@ -514,7 +515,7 @@ MOE_API moe_status moe_layer_forward(moe_layer* l, const void* x_in, int T, void
                                                    kTileCtlBytes)
                                  : nullptr,
                      ffn_gathers ? d.cache : nullptr, d.layer, l->miss_ids, l->n_miss,
-                     policy ? l->miss_dst : nullptr};
+                     policy ? l->miss_dst : nullptr, false, nullptr, nullptr};
     if (!prefill && groups == 1) {
       fz.comb_ctl = (unsigned int*)((char*)l->route_ctl + kRouteCtlBytes);
       fz.inv = l->inv;
