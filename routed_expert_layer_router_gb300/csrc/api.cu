@@ -395,6 +395,14 @@ MOE_API moe_status moe_layer_forward(moe_layer* l, const void* x_in, int T, void
     return MOE_ERR_INVALID_ARG;
   }
   if (pat.type == cudaMemoryTypeUnregistered) return MOE_ERR_INVALID_ARG;
+  // y is written by a kernel: device memory, managed memory or pinned host
+  // memory (pageable host memory would fault the kernel that stores it)
+  cudaPointerAttributes yat;
+  if (cudaPointerGetAttributes(&yat, y) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (yat.type == cudaMemoryTypeUnregistered) return MOE_ERR_INVALID_ARG;
   if (pat.type == cudaMemoryTypeHost) {
     if ((st = copy_rows_in(x_in, l->x_dev, (size_t)T * d.H * 2, s)) != MOE_OK) return st;
     x = l->x_dev;
